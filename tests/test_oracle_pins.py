@@ -1,0 +1,442 @@
+"""Pins for the oracle: each test checks it against something other than itself.
+
+Closed forms, invariants of the gated delta rule, brute force in exact
+rational arithmetic, and independent library routines (scipy, numpy) on tiny
+inputs.  Each is chosen so that a plausible slip in the oracle (a dropped
+term, a wrong sign, a transposed operand, a wrong index) fails at least one.
+"""
+import ctypes
+import os
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special as sp
+
+import oracle
+import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def bf(x):
+    """float -> bf16 bits via the oracle (used only to build exactly-representable inputs)."""
+    return oracle.round_bf16(np.asarray(x, dtype=np.float64))
+
+
+# ----------------------------------------------------------------- bf16
+
+@pytest.fixture(scope="module")
+def bracket():
+    src = os.path.join(HERE, "pins", "bf16_bracket.c")
+    so = os.path.join(HERE, "pins", "libbf16_bracket.so")
+    if not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+        tmp = so + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, src, "-lm"])
+        os.replace(tmp, so)
+    lib = ctypes.CDLL(so)
+    lib.bracket_range.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
+    return lib
+
+
+def test_bf16_rne_exhaustive_all_float_patterns(bracket):
+    """Every one of the 2^32 float bit patterns rounds like the bracket-and-compare reference."""
+    chunk = 1 << 26
+    ref = np.empty(chunk, dtype=np.uint16)
+    for lo in range(0, 1 << 32, chunk):
+        got = oracle.bf16_rne_f32_range(lo, lo + chunk)
+        bracket.bracket_range(lo, lo + chunk, ref.ctypes.data)
+        nan = ref == 0xFFFF
+        if not np.array_equal(got[~nan], ref[~nan]):
+            bad = np.nonzero(got[~nan] != ref[~nan])[0][0]
+            raise AssertionError("mismatch near float pattern 0x%08x" % (lo + int(np.nonzero(~nan)[0][bad])))
+        g = got[nan]  # NaNs stay NaN with the sign kept
+        assert np.all((g & 0x7F80) == 0x7F80) and np.all((g & 0x7F) != 0)
+        signs = (np.arange(lo, lo + chunk, dtype=np.uint64)[nan] >> 31).astype(np.uint16)
+        assert np.array_equal(g >> 15, signs)
+
+
+def test_bf16_rne_known_values():
+    assert oracle.bf16_rne(1.0) == 0x3F80
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8) == 0x3F80          # tie -> even (down)
+    assert oracle.bf16_rne(1.0 + 3 * 2.0 ** -8) == 0x3F82      # tie -> even (up)
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81  # just above the tie
+    assert oracle.bf16_rne(-2.0) == 0xC000
+    assert oracle.bf16_rne(2.0 ** 128) == 0x7F80
+    assert oracle.bf16_rne((2 - 2 ** -8) * 2.0 ** 127) == 0x7F80  # overflow tie rounds to inf
+    assert oracle.bf16_rne((2 - 2 ** -7) * 2.0 ** 127) == 0x7F7F
+    assert oracle.bf16_rne(2.0 ** -133) == 0x0001                # smallest subnormal
+    assert oracle.bf16_rne(2.0 ** -134) == 0x0000                # tie -> even (zero)
+    assert oracle.bf16_rne(1.5 * 2.0 ** -134) == 0x0001
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81  # no double rounding via float
+
+
+# ----------------------------------------------------------------- GEMM
+
+def test_gemm_one_hot_rows_pick_columns():
+    rng = np.random.default_rng(1)
+    M, N, K = 5, 7, 24
+    W = bf(rng.normal(size=(N, K)))
+    X = np.zeros((M, K), dtype=np.uint16)
+    cols = [0, 3, 11, 23, 5]
+    for m, c in enumerate(cols):
+        X[m, c] = 0x3F80  # 1.0
+    Y = oracle.gemm(X, W)
+    Wf = oracle.bf16_to_f64(W)
+    for m, c in enumerate(cols):
+        assert np.array_equal(Y[m], Wf[:, c])  # row m of Y is column c of W: X @ W^T, not W @ X^T
+
+
+def test_gemm_one_hot_weights_pick_inputs():
+    rng = np.random.default_rng(2)
+    M, N, K = 4, 6, 16
+    X = bf(rng.normal(size=(M, K)))
+    W = np.zeros((N, K), dtype=np.uint16)
+    for n in range(N):
+        W[n, (5 * n) % K] = 0x4000  # 2.0
+    Y = oracle.gemm(X, W)
+    Xf = oracle.bf16_to_f64(X)
+    for n in range(N):
+        assert np.array_equal(Y[:, n], 2.0 * Xf[:, (5 * n) % K])
+
+
+def test_gemm_small_integers_exact():
+    rng = np.random.default_rng(3)
+    M, N, K = 9, 13, 300
+    Xi = rng.integers(-8, 9, size=(M, K))
+    Wi = rng.integers(-8, 9, size=(N, K))
+    Y = oracle.gemm(bf(Xi), bf(Wi))
+    assert np.array_equal(Y, (Xi @ Wi.T).astype(np.float64))
+
+
+def test_gemm_against_numpy_on_random_bf16():
+    X = synth.normal_bf16(0, 11, (3, 200))
+    W = synth.normal_bf16(0, 12, (17, 200), sigma=0.02)
+    Y = oracle.gemm(X, W)
+    ref = oracle.bf16_to_f64(X) @ oracle.bf16_to_f64(W).T
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-15)
+
+
+# ------------------------------------------------------------ norms / MLP
+
+def test_rmsnorm_constant_vector():
+    H = 64
+    for c in (0.75, -3.0, 40.0):
+        x = bf(np.full(H, c))
+        y = oracle.rmsnorm(x, bf(np.zeros(H)), eps=0.0)
+        assert np.all(oracle.bf16_to_f64(y) == np.sign(c))
+        y = oracle.rmsnorm(x, bf(np.full(H, 0.25)), eps=0.0)
+        assert np.all(oracle.bf16_to_f64(y) == np.sign(c) * 1.25)
+
+
+def test_rmsnorm_3_4_pattern_and_eps():
+    H = 8
+    x = bf(np.array([3.0, 4.0] * 4))  # mean square 12.5
+    y = oracle.bf16_to_f64(oracle.rmsnorm(x, bf(np.zeros(H)), eps=0.5))  # sqrt(13) below
+    exp = oracle.bf16_to_f64(bf(np.array([3.0, 4.0] * 4) / np.sqrt(13.0)))
+    assert np.array_equal(y, exp)
+
+
+def test_swiglu_closed_forms():
+    u = bf(np.array([1.0, -2.0, 0.5, 3.0]))
+    assert np.all(oracle.bf16_to_f64(oracle.swiglu(bf(np.zeros(4)), u)) == 0.0)
+    g = bf(np.array([1.0, 1.0, -1.0, 2.0]))
+    gf, uf = oracle.bf16_to_f64(g), oracle.bf16_to_f64(u)
+    ref = gf * sp.expit(gf) * uf
+    assert np.array_equal(oracle.bf16_to_f64(oracle.swiglu(g, u)), oracle.bf16_to_f64(bf(ref)))
+    assert oracle.bf16_to_f64(oracle.swiglu(bf(np.array([60.0])), bf(np.array([1.5]))))[0] == 90.0
+
+
+def test_gdn_gates_closed_forms():
+    b = bf(np.array([0.0, 2.0, -3.0, 30.0]))
+    a = bf(np.array([0.0, 25.0, -30.0, 1.0]))
+    beta, gate = oracle.gdn_gates(b, a)
+    bf_, af = oracle.bf16_to_f64(b), oracle.bf16_to_f64(a)
+    assert oracle.bf16_to_f64(beta)[0] == 0.5
+    assert oracle.bf16_to_f64(gate)[0] == 0.5                 # exp(-ln 2)
+    np.testing.assert_array_equal(beta, bf(sp.expit(bf_)))
+    np.testing.assert_array_equal(gate, bf(np.exp(-np.logaddexp(0.0, af))))
+    assert oracle.bf16_to_f64(gate)[2] == 1.0                 # softplus(-30) ~ 1e-13
+
+
+def test_l2norm():
+    y = oracle.l2norm(np.array([3.0, 4.0]), eps=0.0)
+    assert y[0] == 0.6 and y[1] == 0.8
+    y = oracle.l2norm(np.array([3.0, 4.0]), eps=11.0)         # sqrt(36)
+    assert y[0] == 0.5 and abs(y[1] - 4.0 / 6.0) < 1e-16
+
+
+# ------------------------------------------------------------------ GDN
+
+def _rand_unit(rng, n):
+    x = rng.normal(size=n)
+    return x / np.linalg.norm(x)
+
+
+def test_gdn_1x1_closed_form():
+    s0, q, k, v, b, a = 0.75, 0.5, -1.25, 2.0, 0.375, 0.875
+    S = np.array([[s0]])
+    o = oracle.gdn_step(S, [q], [k], [v], b, a)
+    s1 = Fraction(a) * Fraction(s0) * (1 - Fraction(b) * Fraction(k) ** 2) + Fraction(b) * Fraction(v) * Fraction(k)
+    assert S[0, 0] == float(s1)
+    assert o[0] == float(s1 * Fraction(q))
+
+
+def test_gdn_2x2_brute_force_rationals():
+    """S (I - b k k^T) multiplied out entry by entry in exact rationals."""
+    S0 = [[Fraction(1, 2), Fraction(-3, 4)], [Fraction(5, 8), Fraction(1, 4)]]
+    k = [Fraction(3, 4), Fraction(-1, 2)]
+    v = [Fraction(1, 8), Fraction(-5, 4)]
+    q = [Fraction(1, 4), Fraction(7, 8)]
+    a, b = Fraction(7, 8), Fraction(1, 2)
+    P = [[(1 if i == j else 0) - b * k[i] * k[j] for j in range(2)] for i in range(2)]
+    S1 = [[a * sum(S0[r][i] * P[i][c] for i in range(2)) + b * v[r] * k[c] for c in range(2)] for r in range(2)]
+    o = [sum(S1[r][c] * q[c] for c in range(2)) for r in range(2)]
+    S = np.array([[float(x) for x in row] for row in S0])
+    got_o = oracle.gdn_step(S, [float(x) for x in q], [float(x) for x in k], [float(x) for x in v], float(b), float(a))
+    assert np.array_equal(S, np.array([[float(x) for x in row] for row in S1]))
+    assert np.array_equal(got_o, np.array([float(x) for x in o]))
+
+
+def test_gdn_beta_zero_is_pure_decay():
+    rng = np.random.default_rng(5)
+    dv, dk = 6, 5
+    S = rng.normal(size=(dv, dk))
+    S_ref = 0.625 * S
+    q = rng.normal(size=dk)
+    o = oracle.gdn_step(S, q, rng.normal(size=dk), rng.normal(size=dv), 0.0, 0.625)
+    np.testing.assert_allclose(S, S_ref, rtol=1e-15)
+    np.testing.assert_allclose(o, S_ref @ q, rtol=1e-13)
+
+
+def test_gdn_delta_rule_overwrite():
+    """a = b = 1 and |k| = 1: afterwards S k = v (the value at key k is replaced)."""
+    rng = np.random.default_rng(6)
+    dv, dk = 7, 9
+    S = rng.normal(size=(dv, dk))
+    k, v = _rand_unit(rng, dk), rng.normal(size=dv)
+    oracle.gdn_step(S, rng.normal(size=dk), k, v, 1.0, 1.0)
+    np.testing.assert_allclose(S @ k, v, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_partial_write_and_orthogonal_complement():
+    """|k| = 1: S'k = (1-b) a S k + b v, and S'w = a S w for every w orthogonal to k.
+    The second identity fails if the update is applied on the wrong side of S."""
+    rng = np.random.default_rng(7)
+    dv, dk = 5, 8
+    S = rng.normal(size=(dv, dk))
+    S0 = S.copy()
+    k, v = _rand_unit(rng, dk), rng.normal(size=dv)
+    a, b = 0.8, 0.3
+    w = rng.normal(size=dk)
+    w -= (w @ k) * k
+    o = oracle.gdn_step(S, k, k, v, b, a)
+    np.testing.assert_allclose(S @ k, (1 - b) * a * (S0 @ k) + b * v, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S @ w, a * (S0 @ w), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(o, S @ k, rtol=1e-13)          # o = S' q with q = k
+
+
+def test_gdn_orthonormal_keys_store_and_recall():
+    rng = np.random.default_rng(8)
+    d = 6
+    Q, _ = np.linalg.qr(rng.normal(size=(d, d)))
+    V = rng.normal(size=(d, 4))
+    S = np.zeros((4, d))
+    for i in range(d):
+        oracle.gdn_step(S, Q[:, i], Q[:, i], V[i], 1.0, 1.0)
+    for i in range(d):
+        np.testing.assert_allclose(S @ Q[:, i], V[i], rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_no_growth_without_writes():
+    rng = np.random.default_rng(9)
+    S = rng.normal(size=(6, 6))
+    for _ in range(20):
+        before = np.linalg.norm(S)
+        oracle.gdn_step(S, rng.normal(size=6), _rand_unit(rng, 6), np.zeros(6), rng.uniform(0, 1), rng.uniform(0, 1))
+        assert np.linalg.norm(S) <= before * (1 + 1e-14)
+
+
+def test_gdn_matches_error_correcting_form():
+    """Widrow-Hoff form of the same rule: decay, read r = S k, write b (v - r) k^T."""
+    rng = np.random.default_rng(10)
+    dv, dk = 8, 8
+    S = rng.normal(size=(dv, dk))
+    ref = S.copy()
+    for _ in range(5):
+        q, k, v = rng.normal(size=dk), _rand_unit(rng, dk), rng.normal(size=dv)
+        a, b = rng.uniform(0.2, 1), rng.uniform(0, 1)
+        o = oracle.gdn_step(S, q, k, v, b, a)
+        ref = a * ref
+        r = ref @ k
+        ref = ref + np.outer(b * (v - r), k)
+        np.testing.assert_allclose(S, ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(o, ref @ q, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_heads_bf16_path_normalises_and_rounds():
+    rng = np.random.default_rng(11)
+    H, dk, dv = 3, 4, 5
+    S = rng.normal(size=(H, dv, dk))
+    S_ref = S.copy()
+    q, k, v = bf(rng.normal(size=(H, dk))), bf(rng.normal(size=(H, dk))), bf(rng.normal(size=(H, dv)))
+    beta, gate = bf(np.array([0.5, 0.25, 0.75])), bf(np.array([0.875, 1.0, 0.5]))
+    o = oracle.gdn_step_heads(S, q, k, v, beta, gate, l2=True)
+    for h in range(H):
+        qd, kd = oracle.bf16_to_f64(q[h]), oracle.bf16_to_f64(k[h])
+        qd, kd = qd / np.sqrt(qd @ qd + 1e-6), kd / np.sqrt(kd @ kd + 1e-6)
+        oo = oracle.gdn_step(S_ref[h], qd, kd, oracle.bf16_to_f64(v[h]),
+                             oracle.bf16_to_f64(beta)[h], oracle.bf16_to_f64(gate)[h])
+        np.testing.assert_allclose(S[h], S_ref[h], rtol=1e-14, atol=1e-15)
+        assert np.array_equal(o[h], bf(oo))
+
+
+# ------------------------------------------------------------ attention
+
+def test_attn_single_position_returns_v0():
+    rng = np.random.default_rng(12)
+    hd = 16
+    q, K, V = bf(rng.normal(size=hd)), bf(rng.normal(size=(4, hd))), bf(rng.normal(size=(4, hd)))
+    out = oracle.attn_row(q, K, V, 1, 0.25)
+    assert np.array_equal(out, oracle.bf16_to_f64(V[0]))
+
+
+def test_attn_identical_keys_mean_of_values():
+    rng = np.random.default_rng(13)
+    hd, L = 8, 10
+    K = np.tile(bf(rng.normal(size=hd)), (L, 1))
+    V = bf(rng.normal(size=(L, hd)))
+    out = oracle.attn_row(bf(rng.normal(size=hd)), K, V, L, 0.5)
+    np.testing.assert_allclose(out, oracle.bf16_to_f64(V).mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def test_attn_dominant_key():
+    hd, L = 8, 6
+    rng = np.random.default_rng(14)
+    K = bf(rng.normal(size=(L, hd)) * 0.01)
+    K[3] = bf(np.full(hd, 4.0))
+    q = bf(np.full(hd, 4.0))  # score gap about 128 * scale
+    V = bf(rng.normal(size=(L, hd)))
+    out = oracle.attn_row(q, K, V, L, 0.5)
+    np.testing.assert_allclose(out, oracle.bf16_to_f64(V[3]), rtol=0, atol=1e-20)
+
+
+def test_attn_matches_scipy_softmax_and_respects_length():
+    rng = np.random.default_rng(15)
+    hd, Lmax, n = 16, 12, 9
+    q, K, V = bf(rng.normal(size=hd)), bf(rng.normal(size=(Lmax, hd))), bf(rng.normal(size=(Lmax, hd)))
+    s = oracle.bf16_to_f64(K[:n]) @ oracle.bf16_to_f64(q) * 0.25
+    ref = sp.softmax(s) @ oracle.bf16_to_f64(V[:n])
+    np.testing.assert_allclose(oracle.attn_row(q, K, V, n, 0.25), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_attn_rows_gqa_mapping_and_causal_rows():
+    rng = np.random.default_rng(16)
+    R, Hq, Hkv, hd, Lmax, len0 = 3, 4, 2, 8, 10, 5
+    q = bf(rng.normal(size=(R, Hq, hd)))
+    kc, vc = bf(rng.normal(size=(Hkv, Lmax, hd))), bf(rng.normal(size=(Hkv, Lmax, hd)))
+    out = oracle.bf16_to_f64(oracle.attn_rows(q, kc, vc, len0, 0.35))
+    for r in range(R):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)  # consecutive q heads share a kv head
+            s = oracle.bf16_to_f64(kc[g, :len0 + r]) @ oracle.bf16_to_f64(q[r, h]) * 0.35
+            ref = sp.softmax(s) @ oracle.bf16_to_f64(vc[g, :len0 + r])
+            assert np.max(np.abs(out[r, h] - ref)) <= 2.0 ** -8 * np.max(np.abs(ref))
+
+
+# ------------------------------------------------------- argmax / accept
+
+def test_argmax_lowest_index_on_ties():
+    assert oracle.argmax(np.array([1.0, 3.0, 2.0, 3.0])) == 1
+    assert oracle.argmax(np.array([-5.0, -5.0])) == 0
+    x = np.zeros(1000)
+    x[[17, 400, 999]] = 2.5
+    assert oracle.argmax(x) == 17
+
+
+def test_accept_rule():
+    assert oracle.accept([9, 1, 2, 3], [1, 2, 3, 7]) == 3   # every draft accepted
+    assert oracle.accept([9, 1, 2, 3], [1, 5, 3, 7]) == 1   # stops at the first mismatch
+    assert oracle.accept([9, 1, 2, 3], [4, 2, 3, 7]) == 0   # forced reject
+    assert oracle.accept([9], [4]) == 0                     # k = 1 is plain decode
+
+
+# --------------------------------------------------------------- stack
+
+def _tiny_cfg():
+    return dict(H=32, V=50, F=48, kinds=[0, 1], gdn_h=2, gdn_dk=8, gdn_dv=8,
+                at_hq=2, at_hkv=1, at_hd=8, eps=1e-6)
+
+
+def _tiny_weights(cfg, seed=0, zero_mixers=False, zero_mlp=False):
+    H, F, V = cfg["H"], cfg["F"], cfg["V"]
+    gin = cfg["gdn_h"] * (2 * cfg["gdn_dk"] + cfg["gdn_dv"]) + 2 * cfg["gdn_h"]
+    ain = 2 * cfg["at_hq"] * cfg["at_hd"] + 2 * cfg["at_hkv"] * cfg["at_hd"]
+    w = {"embed": synth.normal_bf16(seed, 1, (V, H)), "final_norm": synth.normal_bf16(seed, 2, H, sigma=0.02),
+         "lm_head": synth.normal_bf16(seed, 3, (V, H), sigma=0.02)}
+    for l, kd in enumerate(cfg["kinds"]):
+        inn = gin if kd == 0 else ain
+        inner = cfg["gdn_h"] * cfg["gdn_dv"] if kd == 0 else cfg["at_hq"] * cfg["at_hd"]
+        w[f"{l}.norm1"] = synth.normal_bf16(seed, 10 + l, H, sigma=0.02)
+        w[f"{l}.w_in"] = synth.normal_bf16(seed, 20 + l, (inn, H), sigma=0.2)
+        w[f"{l}.w_out"] = synth.normal_bf16(seed, 30 + l, (H, inner), sigma=0.2)
+        w[f"{l}.norm2"] = synth.normal_bf16(seed, 40 + l, H, sigma=0.02)
+        w[f"{l}.w_gu"] = synth.normal_bf16(seed, 50 + l, (2 * F, H), sigma=0.2)
+        w[f"{l}.w_down"] = synth.normal_bf16(seed, 60 + l, (H, F), sigma=0.2)
+        if zero_mixers:
+            w[f"{l}.w_out"][...] = 0
+        if zero_mlp:
+            w[f"{l}.w_down"][...] = 0
+    return w
+
+
+def test_stack_identity_path_is_embed_norm_head():
+    """With every mixer and MLP output zeroed the residual stream is the embedding row,
+    so the logits are lm_head @ rmsnorm(embed[token]) (checked with numpy)."""
+    cfg = _tiny_cfg()
+    w = _tiny_weights(cfg, zero_mixers=True, zero_mlp=True)
+    st = oracle.Stack(cfg, w, Lmax=16)
+    tok = 7
+    logits = st.decode(tok)
+    x = oracle.bf16_to_f64(w["embed"][tok])
+    xn = x / np.sqrt(np.mean(x * x) + 1e-6) * (1 + oracle.bf16_to_f64(w["final_norm"]))
+    ref = oracle.bf16_to_f64(w["lm_head"]) @ oracle.bf16_to_f64(bf(xn))
+    np.testing.assert_allclose(logits, ref, rtol=1e-12, atol=1e-14)
+    assert st.len == 1
+
+
+def test_stack_kv_append_position_and_projection():
+    """The token at position p puts bf16(rmsnorm(x) @ W_k^T) into K row p (numpy matmul check)."""
+    cfg = _tiny_cfg()
+    cfg["kinds"] = [1]
+    w = _tiny_weights(cfg)
+    st = oracle.Stack(cfg, w, Lmax=16)
+    for tok in (3, 11, 5):
+        st.decode(tok)
+    assert st.len == 3
+    hd, hq, hkv = cfg["at_hd"], cfg["at_hq"], cfg["at_hkv"]
+    assert np.any(st.kc[0][:, 2] != 0) and np.all(st.kc[0][:, 3:] == 0)
+    x = oracle.bf16_to_f64(w["embed"][3])   # first layer input of the first token is its embedding
+    xn = bf(x / np.sqrt(np.mean(x * x) + 1e-6) * (1 + oracle.bf16_to_f64(w["0.norm1"])))
+    Wk = oracle.bf16_to_f64(w["0.w_in"][2 * hq * hd: 2 * hq * hd + hkv * hd])
+    Wv = oracle.bf16_to_f64(w["0.w_in"][2 * hq * hd + hkv * hd:])
+    assert np.array_equal(st.kc[0][:, 0].reshape(-1), bf(Wk @ oracle.bf16_to_f64(xn)))
+    assert np.array_equal(st.vc[0][:, 0].reshape(-1), bf(Wv @ oracle.bf16_to_f64(xn)))
+
+
+def test_stack_verify_is_sequential_decode_and_state_advances():
+    cfg = _tiny_cfg()
+    w = _tiny_weights(cfg)
+    a = oracle.Stack(cfg, w, Lmax=16)
+    b = oracle.Stack(cfg, w, Lmax=16)
+    toks = [4, 9, 1]
+    la = a.verify(toks)
+    lb = np.stack([b.decode(t) for t in toks])
+    assert np.array_equal(la, lb)
+    snap = a.snapshot()
+    a.decode(2)
+    assert not np.array_equal(a.S[0], snap[0][0])
+    a.restore(snap)
+    assert np.array_equal(a.S[0], snap[0][0]) and a.len == 3
