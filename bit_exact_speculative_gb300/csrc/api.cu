@@ -1,0 +1,264 @@
+// C-ABI entry points of libxv.so (except the block, in block.cu): argument
+// validation, error reporting, the device error word and tensor-map encoding.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "xv_internal.h"
+
+namespace xv {
+
+namespace {
+thread_local char g_msg[512] = "";
+std::atomic<unsigned long long> g_launches{0};
+
+// One error word per device; kernels OR error bits into it.
+__device__ unsigned g_dev_err;
+constexpr int MAX_DEVICES = 64;
+unsigned* g_err_ptr[MAX_DEVICES] = {};
+std::mutex g_err_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+xv_status fail(xv_status code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+xv_status cuda_check(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return XV_OK;
+    return fail(XV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+xv_status launched(const char* what) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_check(cudaGetLastError(), what);
+}
+
+unsigned* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+xv_status encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    if (!g_encode) return fail(XV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, b, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(XV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return XV_OK;
+}
+
+}  // namespace xv
+
+using namespace xv;
+
+extern "C" {
+
+int xv_abi_version(void) { return XV_ABI_VERSION; }
+
+const char* xv_last_error(void) { return g_msg; }
+
+unsigned long long xv_launch_count(void) { return g_launches.load(); }
+
+xv_status xv_device_check(xv_stream s, unsigned* code) {
+    unsigned* w = device_error_word();
+    if (!w) return fail(XV_ERR_CUDA, "cannot resolve the device error word");
+    xv_status st = cuda_check(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    if (st) return st;
+    unsigned v = 0;
+    if ((st = cuda_check(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost), "read device error word"))) return st;
+    if (v) {
+        unsigned zero = 0;
+        if ((st = cuda_check(cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice), "clear device error word")))
+            return st;
+    }
+    if (code) *code = v;
+    if (v) return fail(XV_ERR_DEVICE_CHECK, "device-side error bits 0x%x", v);
+    return XV_OK;
+}
+
+// ------------------------------------------------------------------ GEMM
+
+int xv_gemm_splits(int N, int K) { return (N > 0 && K > 0) ? gemm_splits(N, K) : 0; }
+
+size_t xv_gemm_workspace_size(int M, int N, int K) {
+    if (M < 1 || N < 1 || K < 1) return 0;
+    return gemm_workspace_size(M, N, K);
+}
+
+static xv_status gemm_checks(const uint16_t* X, int ldx, const uint16_t* W, const void* Y, int ldy, int M, int N, int K,
+                             const void* ws, size_t ws_bytes) {
+    if (!X || !W || !Y) return fail(XV_ERR_ARG, "gemm: null X, W or Y");
+    if (M < 1 || N < 1 || K < 8) return fail(XV_ERR_ARG, "gemm: need M >= 1, N >= 1, K >= 8 (got %d, %d, %d)", M, N, K);
+    if (M > XV_GEMM_M_MAX) return fail(XV_ERR_UNSUPPORTED, "gemm: M = %d exceeds %d", M, XV_GEMM_M_MAX);
+    if (ldx < K || ldy < N) return fail(XV_ERR_ARG, "gemm: ldx < K or ldy < N");
+    if (K % 8 || ldx % 8) return fail(XV_ERR_UNSUPPORTED, "gemm: K and ldx must be multiples of 8");
+    if (!aligned16(X) || !aligned16(W)) return fail(XV_ERR_UNSUPPORTED, "gemm: X and W must be 16-byte aligned");
+    size_t need = gemm_workspace_size(M, N, K);
+    if (need && (!ws || ws_bytes < need))
+        return fail(XV_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed, %zu given", need, ws ? ws_bytes : 0);
+    return XV_OK;
+}
+
+xv_status xv_gemm_small_m(const uint16_t* X, int ldx, const uint16_t* W, uint16_t* Y, int ldy, int M, int N, int K,
+                          void* ws, size_t ws_bytes, xv_stream s) {
+    if (xv_status st = gemm_checks(X, ldx, W, Y, ldy, M, N, K, ws, ws_bytes)) return st;
+    return gemm_launch(X, ldx, W, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, float* Y, int ldy, int M, int N, int K,
+                                 void* ws, size_t ws_bytes, xv_stream s) {
+    if (xv_status st = gemm_checks(X, ldx, W, Y, ldy, M, N, K, ws, ws_bytes)) return st;
+    return gemm_launch(X, ldx, W, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+// ------------------------------------------------------------------- GDN
+
+static xv_status gdn_dims(int B, int H, int dk, int dv) {
+    if (B < 1 || H < 1) return fail(XV_ERR_ARG, "gdn: need B >= 1 and H >= 1");
+    if (dk != 64 && dk != 128) return fail(XV_ERR_UNSUPPORTED, "gdn: dk must be 64 or 128 (got %d)", dk);
+    if (dv < 16 || dv % 16) return fail(XV_ERR_UNSUPPORTED, "gdn: dv must be a positive multiple of 16 (got %d)", dv);
+    if (B > 65535 || H > 65535) return fail(XV_ERR_UNSUPPORTED, "gdn: B and H must be below 65536");
+    return XV_OK;
+}
+
+static xv_status gdn_steps_ok(const xv_gdn_steps* st, const char* which, int dk, int H) {
+    if (!st) return fail(XV_ERR_ARG, "gdn: %s steps missing", which);
+    if (!st->q || !st->k || !st->v || !st->beta || !st->gate) return fail(XV_ERR_ARG, "gdn: null pointer in %s", which);
+    if (st->rows_per_seq < 1) return fail(XV_ERR_ARG, "gdn: %s.rows_per_seq must be >= 1", which);
+    if (st->qkv_stride < 0 || st->gate_stride < H) return fail(XV_ERR_ARG, "gdn: bad strides in %s", which);
+    if (!aligned16(st->q) || !aligned16(st->k) || (st->qkv_stride % 8))
+        return fail(XV_ERR_UNSUPPORTED, "gdn: q/k of %s must be 16-byte aligned with qkv_stride %% 8 == 0", which);
+    (void)dk;
+    return XV_OK;
+}
+
+static GdnStepsDev to_dev(const xv_gdn_steps& s) {
+    return GdnStepsDev{s.q, s.k, s.v, s.beta, s.gate, s.qkv_stride, s.gate_stride, s.rows_per_seq};
+}
+
+xv_status xv_gdn_decode_step(float* state, const xv_gdn_steps* step, uint16_t* o, long long o_stride, int B, int H,
+                             int dk, int dv, int qk_l2norm, xv_stream s) {
+    if (xv_status st = gdn_dims(B, H, dk, dv)) return st;
+    if (!state || !o) return fail(XV_ERR_ARG, "gdn: null state or o");
+    if (xv_status st = gdn_steps_ok(step, "step", dk, H)) return st;
+    if (o_stride < (long long)H * dv) return fail(XV_ERR_ARG, "gdn: o_stride below H*dv");
+    GdnStepsDev p = to_dev(*step), none{};
+    return gdn_launch(state, p, nullptr, 1, 1, true, none, 0, o, o_stride, B, H, dk, dv, qk_l2norm,
+                      reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gdn_verify(float* state, const xv_gdn_steps* pending, const int32_t* n_commit, int max_commit,
+                        const xv_gdn_steps* draft, int k, uint16_t* o, long long o_stride, int B, int H, int dk, int dv,
+                        int qk_l2norm, xv_stream s) {
+    if (xv_status st = gdn_dims(B, H, dk, dv)) return st;
+    if (!state) return fail(XV_ERR_ARG, "gdn: null state");
+    if (k < 0 || k > XV_KMAX) return fail(XV_ERR_UNSUPPORTED, "gdn: k = %d outside [0, %d]", k, XV_KMAX);
+    if (max_commit < 0 || max_commit > XV_KMAX)
+        return fail(XV_ERR_UNSUPPORTED, "gdn: max_commit = %d outside [0, %d]", max_commit, XV_KMAX);
+    if (max_commit > 0) {
+        if (!n_commit) return fail(XV_ERR_ARG, "gdn: n_commit missing");
+        if (xv_status st = gdn_steps_ok(pending, "pending", dk, H)) return st;
+        if (pending->rows_per_seq < max_commit) return fail(XV_ERR_ARG, "gdn: pending.rows_per_seq < max_commit");
+    }
+    if (k > 0) {
+        if (xv_status st = gdn_steps_ok(draft, "draft", dk, H)) return st;
+        if (draft->rows_per_seq < k) return fail(XV_ERR_ARG, "gdn: draft.rows_per_seq < k");
+        if (!o) return fail(XV_ERR_ARG, "gdn: null o");
+        if (o_stride < (long long)H * dv) return fail(XV_ERR_ARG, "gdn: o_stride below H*dv");
+    }
+    if (k == 0 && max_commit == 0) return XV_OK;
+    GdnStepsDev p = max_commit > 0 ? to_dev(*pending) : GdnStepsDev{};
+    GdnStepsDev d = k > 0 ? to_dev(*draft) : GdnStepsDev{};
+    return gdn_launch(state, p, max_commit > 0 ? n_commit : nullptr, 0, max_commit, false, d, k, o, o_stride, B, H, dk,
+                      dv, qk_l2norm, reinterpret_cast<cudaStream_t>(s));
+}
+
+// ------------------------------------------------------------- attention
+
+int xv_attn_split_size(void) { return ATTN_SPLIT; }
+
+size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx) {
+    if (B < 1 || R < 1 || Hq < 1 || hd < 1 || max_ctx < 1) return 0;
+    return attn_workspace_size(B, R, Hq, hd, max_ctx);
+}
+
+static xv_status attn_checks(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
+                             const int32_t* ctx_len, int R, int B, int Hq, int Hkv, int hd, int Lmax, int max_len,
+                             const uint16_t* gate, long long gate_stride, const uint16_t* out, long long out_stride) {
+    if (!q || !kc || !vc || !ctx_len || !out) return fail(XV_ERR_ARG, "attn: null pointer");
+    if (B < 1 || R < 1 || Hq < 1 || Hkv < 1 || Lmax < 1) return fail(XV_ERR_ARG, "attn: sizes must be positive");
+    if (R > XV_KMAX) return fail(XV_ERR_UNSUPPORTED, "attn: R = %d exceeds %d", R, XV_KMAX);
+    if (Hq % Hkv) return fail(XV_ERR_ARG, "attn: Hq must be a multiple of Hkv");
+    if (hd != 64 && hd != 256) return fail(XV_ERR_UNSUPPORTED, "attn: hd must be 64 or 256 (got %d)", hd);
+    if (R * (Hq / Hkv) > 64) return fail(XV_ERR_UNSUPPORTED, "attn: R * Hq/Hkv = %d exceeds 64", R * (Hq / Hkv));
+    if (max_len < R || max_len > Lmax) return fail(XV_ERR_ARG, "attn: need R <= max_ctx <= Lmax");
+    if (B > 65535 || Hkv > 65535) return fail(XV_ERR_UNSUPPORTED, "attn: B and Hkv must be below 65536");
+    if ((long long)B * Hkv * Lmax > (1ll << 31)) return fail(XV_ERR_UNSUPPORTED, "attn: cache too large");
+    if (q_stride < (long long)Hq * hd || out_stride < (long long)Hq * hd) return fail(XV_ERR_ARG, "attn: row stride below Hq*hd");
+    if (gate && gate_stride < (long long)Hq * hd) return fail(XV_ERR_ARG, "attn: gate_stride below Hq*hd");
+    if (!aligned16(q) || (q_stride % 8) || !aligned16(kc) || !aligned16(vc))
+        return fail(XV_ERR_UNSUPPORTED, "attn: q rows and caches must be 16-byte aligned");
+    return XV_OK;
+}
+
+xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
+                              const int32_t* ctx_len, int R, int B, int Hq, int Hkv, int hd, int Lmax, int max_ctx,
+                              float scale, const uint16_t* gate, long long gate_stride, uint16_t* out,
+                              long long out_stride, void* ws, size_t ws_bytes, xv_stream s) {
+    if (xv_status st = attn_checks(q, q_stride, kc, vc, ctx_len, R, B, Hq, Hkv, hd, Lmax, max_ctx, gate, gate_stride,
+                                   out, out_stride))
+        return st;
+    size_t need = attn_workspace_size(B, R, Hq, hd, max_ctx);
+    if (!ws || ws_bytes < need) return fail(XV_ERR_WORKSPACE, "attn: workspace of %zu bytes needed", need);
+    return attn_launch(q, q_stride, kc, vc, ctx_len, 0, R, B, Hq, Hkv, hd, Lmax, max_ctx, scale, gate, gate_stride, out,
+                       out_stride, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_kv_append(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B, int Hkv,
+                       int hd, int Lmax, uint16_t* kc, uint16_t* vc, xv_stream s) {
+    if (!kv_src || !ctx_len || !kc || !vc) return fail(XV_ERR_ARG, "kv_append: null pointer");
+    if (R < 1 || B < 1 || Hkv < 1 || hd < 8 || Lmax < 1 || hd % 8) return fail(XV_ERR_ARG, "kv_append: bad sizes");
+    if (src_stride < 2ll * Hkv * hd) return fail(XV_ERR_ARG, "kv_append: src_stride below 2*Hkv*hd");
+    if (!aligned16(kv_src) || (src_stride % 8) || !aligned16(kc) || !aligned16(vc))
+        return fail(XV_ERR_UNSUPPORTED, "kv_append: 16-byte alignment required");
+    return kv_append_launch(kv_src, src_stride, ctx_len, -1, R, B, Hkv, hd, Lmax, kc, vc,
+                            reinterpret_cast<cudaStream_t>(s));
+}
+
+}  // extern "C"

@@ -1,0 +1,262 @@
+// The verify block: a stack of hybrid decoder layers under an embedding and
+// an LM head, run for B sequences x k tokens in one stream-ordered pass.
+//
+// Decode is the same pass with k = 1; nothing in it depends on k except the
+// row count, and every kernel it calls gives a row the same bits whatever the
+// row count ("Follow-up to my earlier post on Qwen3.8-27B decode speed",
+// r/LocalLLaMA post: with the verify fixes, every token id and every logprob
+// matched decoding without speculation, also with every draft forced to
+// reject and with 8 requests in flight).
+//
+// GDN layers use deferred commit: a verify call first replays the pending
+// steps (the inputs of the previous verify's kept positions) into the
+// committed state, then speculates over this call's k tokens without
+// writing the state; its own inputs become the next pending steps.  State
+// traffic is one read and one write per call instead of k writes.
+#include <vector>
+
+#include "xv_internal.h"
+
+namespace xv {
+namespace {
+
+struct Dims {
+    int H, V, F, L;
+    int gh, dk, dv, gin, ginner;
+    int hq, hkv, hd, ain, ainner;
+};
+
+xv_status check_cfg(const xv_block_config* c, Dims* d) {
+    if (!c) return fail(XV_ERR_ARG, "block: null config");
+    if (c->hidden < 64 || c->hidden % 64 || c->vocab < 1 || c->mlp < 64 || c->mlp % 64 || c->n_layers < 1 || !c->layer_kind)
+        return fail(XV_ERR_ARG, "block: hidden and mlp must be positive multiples of 64, vocab and n_layers >= 1");
+    bool has_gdn = false, has_attn = false;
+    for (int l = 0; l < c->n_layers; ++l) {
+        if (c->layer_kind[l] == 0) has_gdn = true;
+        else if (c->layer_kind[l] == 1) has_attn = true;
+        else return fail(XV_ERR_ARG, "block: layer_kind[%d] must be 0 (GDN) or 1 (attention)", l);
+    }
+    d->H = c->hidden; d->V = c->vocab; d->F = c->mlp; d->L = c->n_layers;
+    d->gh = c->gdn_heads; d->dk = c->gdn_dk; d->dv = c->gdn_dv;
+    d->hq = c->attn_hq; d->hkv = c->attn_hkv; d->hd = c->attn_hd;
+    d->gin = d->gh * (2 * d->dk + d->dv) + 2 * d->gh;
+    d->ginner = d->gh * d->dv;
+    d->ain = 2 * d->hq * d->hd + 2 * d->hkv * d->hd;
+    d->ainner = d->hq * d->hd;
+    if (has_gdn) {
+        if ((d->dk != 64 && d->dk != 128) || d->dv < 16 || d->dv % 16 || d->gh < 1)
+            return fail(XV_ERR_UNSUPPORTED, "block: GDN needs dk in {64,128}, dv a multiple of 16");
+        if (d->gin % 8 || d->ginner % 8) return fail(XV_ERR_UNSUPPORTED, "block: GDN widths must be multiples of 8");
+    } else {
+        d->gin = d->ginner = 0;
+    }
+    if (has_attn) {
+        if ((d->hd != 64 && d->hd != 256) || d->hkv < 1 || d->hq % d->hkv)
+            return fail(XV_ERR_UNSUPPORTED, "block: attention needs hd in {64,256} and Hq a multiple of Hkv");
+    } else {
+        d->ain = d->ainner = 0;
+    }
+    return XV_OK;
+}
+
+inline size_t r256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Carves the block workspace; returns the total size when base is null.
+struct Carve {
+    uint16_t *x, *xn, *proj, *obuf, *y, *gu, *act;
+    float* logits;
+    void* gemm_ws;
+    size_t gemm_ws_bytes;
+    void* attn_ws;
+    size_t attn_ws_bytes;
+    size_t total;
+};
+
+Carve carve(const Dims& d, int B, int kmax, int Lmax, uint8_t* base) {
+    Carve c{};
+    const int M = B * kmax;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += r256(bytes); return p; };
+    c.x = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.H * 2));
+    c.xn = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.H * 2));
+    c.proj = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * (d.ain > 0 ? d.ain : 8) * 2));
+    const int inner = d.ginner > d.ainner ? d.ginner : d.ainner;
+    c.obuf = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * inner * 2));
+    c.y = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.H * 2));
+    c.gu = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * 2 * d.F * 2));
+    c.act = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.F * 2));
+    c.logits = reinterpret_cast<float*>(take(static_cast<size_t>(M) * d.V * 4));
+    size_t g = 0;
+    auto gm = [&](int N, int K) { size_t s = gemm_workspace_size(M, N, K); if (s > g) g = s; };
+    if (d.gin) { gm(d.gin, d.H); gm(d.H, d.ginner); }
+    if (d.ain) { gm(d.ain, d.H); gm(d.H, d.ainner); }
+    gm(2 * d.F, d.H); gm(d.H, d.F); gm(d.V, d.H);
+    c.gemm_ws_bytes = g;
+    c.gemm_ws = take(g > 0 ? g : 256);
+    c.attn_ws_bytes = d.ain ? attn_workspace_size(B, kmax, d.hq, d.hd, Lmax) : 0;
+    c.attn_ws = take(c.attn_ws_bytes > 0 ? c.attn_ws_bytes : 256);
+    c.total = off;
+    return c;
+}
+
+}  // namespace
+}  // namespace xv
+
+using namespace xv;
+
+extern "C" {
+
+int xv_gdn_in_dim(const xv_block_config* cfg) {
+    Dims d{};
+    return check_cfg(cfg, &d) ? -1 : d.gin;
+}
+
+int xv_attn_in_dim(const xv_block_config* cfg) {
+    Dims d{};
+    return check_cfg(cfg, &d) ? -1 : d.ain;
+}
+
+size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax) {
+    Dims d{};
+    if (check_cfg(cfg, &d) || B < 1 || kmax < 1 || Lmax < 1) return 0;
+    return carve(d, B, kmax, Lmax, nullptr).total;
+}
+
+static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv_block_state* st) {
+    if (!st || !st->ctx_len || !st->n_commit || !st->layers) return fail(XV_ERR_ARG, "block: incomplete state");
+    if (st->B < 1 || st->kmax < 1 || st->kmax > XV_KMAX || st->Lmax < 1)
+        return fail(XV_ERR_ARG, "block: state needs B >= 1, 1 <= kmax <= %d, Lmax >= 1", XV_KMAX);
+    for (int l = 0; l < d.L; ++l) {
+        const xv_layer_state& ls = st->layers[l];
+        if (cfg->layer_kind[l] == 0) {
+            if (!ls.gdn_state || !ls.gdn_hist[0] || !ls.gdn_hist[1] || !ls.gdn_gates[0] || !ls.gdn_gates[1])
+                return fail(XV_ERR_ARG, "block: GDN layer %d state incomplete", l);
+            if (!aligned16(ls.gdn_hist[0]) || !aligned16(ls.gdn_hist[1]))
+                return fail(XV_ERR_UNSUPPORTED, "block: GDN history must be 16-byte aligned");
+        } else {
+            if (!ls.k_cache || !ls.v_cache) return fail(XV_ERR_ARG, "block: attention layer %d cache missing", l);
+            if (!aligned16(ls.k_cache) || !aligned16(ls.v_cache))
+                return fail(XV_ERR_UNSUPPORTED, "block: caches must be 16-byte aligned");
+        }
+    }
+    return XV_OK;
+}
+
+xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                          const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept, void* ws,
+                          size_t ws_bytes, xv_stream stream) {
+    Dims d{};
+    if (xv_status e = check_cfg(cfg, &d)) return e;
+    if (xv_status e = check_state(d, cfg, st)) return e;
+    if (!w || !w->embed || !w->layers || !w->final_norm || !w->lm_head) return fail(XV_ERR_ARG, "block: incomplete weights");
+    for (int l = 0; l < d.L; ++l) {
+        const xv_layer_weights& lw = w->layers[l];
+        if (!lw.norm1 || !lw.w_in || !lw.w_out || !lw.norm2 || !lw.w_gate_up || !lw.w_down)
+            return fail(XV_ERR_ARG, "block: layer %d weights incomplete", l);
+    }
+    if (!tokens || !argmax || !n_accept) return fail(XV_ERR_ARG, "block: null tokens, argmax or n_accept");
+    const int B = st->B;
+    if (k < 1 || k > st->kmax) return fail(XV_ERR_ARG, "block: k = %d outside [1, kmax = %d]", k, st->kmax);
+    const int M = B * k;
+    if (M > XV_GEMM_M_MAX) return fail(XV_ERR_UNSUPPORTED, "block: B*k = %d exceeds %d", M, XV_GEMM_M_MAX);
+    if (d.ain && k * (d.hq / d.hkv) > 64)
+        return fail(XV_ERR_UNSUPPORTED, "block: k * Hq/Hkv = %d exceeds 64", k * (d.hq / d.hkv));
+    if (st->max_ctx < 0 || st->max_ctx + k > st->Lmax)
+        return fail(XV_ERR_ARG, "block: max_ctx + k (%d) exceeds Lmax (%d)", st->max_ctx + k, st->Lmax);
+    if (st->pending_rows < 1 || st->pending_rows > st->kmax) return fail(XV_ERR_ARG, "block: pending_rows out of range");
+    const Carve need = carve(d, B, st->kmax, st->Lmax, nullptr);
+    if (!ws || ws_bytes < need.total) return fail(XV_ERR_WORKSPACE, "block: workspace of %zu bytes needed", need.total);
+    const Carve c = carve(d, B, st->kmax, st->Lmax, static_cast<uint8_t*>(ws));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float* lg = logits ? logits : c.logits;
+    const float eps = cfg->rms_eps;
+    const int par = st->parity & 1;
+    const int attn_len = st->max_ctx + k;   // bound on ctx_len + 1 + (k - 1)
+
+#define XV_TRY(expr) do { if (xv_status e_ = (expr)) return e_; } while (0)
+    XV_TRY(embed_launch(tokens, M, w->embed, d.V, d.H, c.x, s));
+    XV_TRY(rmsnorm_launch(c.x, w->layers[0].norm1, M, d.H, eps, c.xn, s));
+    for (int l = 0; l < d.L; ++l) {
+        const xv_layer_weights& lw = w->layers[l];
+        xv_layer_state& ls = st->layers[l];
+        if (cfg->layer_kind[l] == 0) {
+            uint16_t* hist = ls.gdn_hist[par];
+            uint16_t* gates = ls.gdn_gates[par];
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, hist, d.gin, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(gdn_gates_launch(hist, d.gin, d.gh * (2 * d.dk + d.dv), M, d.gh, gates, s));
+            const uint16_t* ph = ls.gdn_hist[par ^ 1];
+            const uint16_t* pg = ls.gdn_gates[par ^ 1];
+            GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gin, 2 * d.gh, st->pending_rows};
+            GdnStepsDev draft{hist, hist + d.gh * d.dk, hist + 2 * d.gh * d.dk, gates, gates + d.gh, d.gin, 2 * d.gh, k};
+            XV_TRY(gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, draft, k, c.obuf, d.ginner, B,
+                              d.gh, d.dk, d.dv, 1, s));
+            XV_TRY(gemm_launch(c.obuf, d.ginner, lw.w_out, c.y, d.H, false, M, d.H, d.ginner, c.gemm_ws, c.gemm_ws_bytes, s));
+        } else {
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, c.proj, d.ain, false, M, d.ain, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(kv_append_launch(c.proj + 2 * d.ainner, d.ain, st->ctx_len, 0, k, B, d.hkv, d.hd, st->Lmax, ls.k_cache,
+                                    ls.v_cache, s));
+            XV_TRY(attn_launch(c.proj, d.ain, ls.k_cache, ls.v_cache, st->ctx_len, 1, k, B, d.hq, d.hkv, d.hd, st->Lmax,
+                               attn_len, 1.0f / sqrtf(static_cast<float>(d.hd)), c.proj + d.ainner, d.ain, c.obuf,
+                               d.ainner, c.attn_ws, c.attn_ws_bytes, s));
+            XV_TRY(gemm_launch(c.obuf, d.ainner, lw.w_out, c.y, d.H, false, M, d.H, d.ainner, c.gemm_ws, c.gemm_ws_bytes, s));
+        }
+        XV_TRY(residual_rmsnorm_launch(c.x, c.y, lw.norm2, M, d.H, eps, c.xn, s));
+        XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, c.gu, 2 * d.F, false, M, 2 * d.F, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+        XV_TRY(swiglu_launch(c.gu, M, d.F, c.act, s));
+        XV_TRY(gemm_launch(c.act, d.F, lw.w_down, c.y, d.H, false, M, d.H, d.F, c.gemm_ws, c.gemm_ws_bytes, s));
+        const uint16_t* next_norm = (l + 1 < d.L) ? w->layers[l + 1].norm1 : w->final_norm;
+        XV_TRY(residual_rmsnorm_launch(c.x, c.y, next_norm, M, d.H, eps, c.xn, s));
+    }
+    XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+    XV_TRY(argmax_launch(lg, M, d.V, argmax, s));
+    XV_TRY(accept_launch(tokens, argmax, B, k, n_accept, s));
+#undef XV_TRY
+    st->last_k = k;
+    return XV_OK;
+}
+
+xv_status xv_block_commit(xv_block_state* st, const int32_t* n_keep, xv_stream stream) {
+    if (!st || !st->ctx_len || !st->n_commit || !n_keep) return fail(XV_ERR_ARG, "commit: null argument");
+    if (st->last_k < 1) return fail(XV_ERR_ARG, "commit: no verify to commit");
+    xv_status e = commit_launch(n_keep, 0, st->B, st->last_k, st->ctx_len, st->n_commit, reinterpret_cast<cudaStream_t>(stream));
+    if (e) return e;
+    st->parity ^= 1;
+    st->pending_rows = st->last_k;
+    st->max_ctx += st->last_k;
+    st->last_k = 0;
+    return XV_OK;
+}
+
+xv_status xv_block_commit_accepted(xv_block_state* st, const int32_t* n_accept, xv_stream stream) {
+    if (!st || !st->ctx_len || !st->n_commit || !n_accept) return fail(XV_ERR_ARG, "commit: null argument");
+    if (st->last_k < 1) return fail(XV_ERR_ARG, "commit: no verify to commit");
+    xv_status e = commit_launch(n_accept, 1, st->B, st->last_k, st->ctx_len, st->n_commit, reinterpret_cast<cudaStream_t>(stream));
+    if (e) return e;
+    st->parity ^= 1;
+    st->pending_rows = st->last_k;
+    st->max_ctx += st->last_k;
+    st->last_k = 0;
+    return XV_OK;
+}
+
+xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stream stream) {
+    Dims d{};
+    if (xv_status e = check_cfg(cfg, &d)) return e;
+    if (xv_status e = check_state(d, cfg, st)) return e;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int par = st->parity & 1;
+    for (int l = 0; l < d.L; ++l) {
+        if (cfg->layer_kind[l] != 0) continue;
+        xv_layer_state& ls = st->layers[l];
+        const uint16_t* ph = ls.gdn_hist[par ^ 1];
+        const uint16_t* pg = ls.gdn_gates[par ^ 1];
+        GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gin, 2 * d.gh, st->pending_rows};
+        GdnStepsDev none{};
+        if (xv_status e = gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, none, 0, nullptr, 0,
+                                     st->B, d.gh, d.dk, d.dv, 1, s))
+            return e;
+    }
+    return zero_i32_launch(st->n_commit, st->B, s);
+}
+
+}  // extern "C"

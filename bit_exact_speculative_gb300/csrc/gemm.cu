@@ -1,0 +1,246 @@
+// Small-M bf16 weight-streaming GEMM on the 5th-generation tensor cores.
+//
+//   Y[M, N] = X[M, K] . W[N, K]^T, fp32 accumulate, bf16 (or fp32) out.
+//
+// Why it exists ("Follow-up to my earlier post on Qwen3.8-27B decode speed",
+// r/LocalLLaMA post, and the recipe card's summary): at decode and verify
+// batch sizes the projection GEMMs must (1) give the same bits for a row
+// whatever the number of rows, so that verifying k tokens at once equals
+// decoding them one by one, and (2) stream the weights near DRAM speed
+// (the post measured the previous small-batch kernel at about a third).
+//
+// Design (GB300, sm_103a):
+//   - Swap-AB: a CTA owns 128 weight rows (the MMA's M side); the tokens are
+//     the MMA's N side, ALWAYS padded to 64 columns whatever M is, so every
+//     call issues the identical tcgen05.mma sequence.  Each output element is
+//     the dot product of one weight row with one token row: no element reads
+//     another row's data, which makes row i independent of M and of its
+//     position (the padding rows are TMA zero fill).
+//   - Weights and tokens arrive by TMA (cp.async.bulk.tensor, 128-byte
+//     swizzle) into a 4-stage shared-memory ring, 64 K-elements per stage;
+//     one thread issues TMA, one thread issues tcgen05.mma, the accumulator
+//     (128 x 64 fp32) lives in TMEM and is read back with tcgen05.ld.
+//   - Split-K over S segments with S a function of (N, K) only; a segment
+//     covers K-blocks [s*nkb/S, (s+1)*nkb/S).  Segment partials go to the
+//     workspace; the last-arriving CTA of a tile (atomic counter after a
+//     __threadfence) adds them in segment order 0..S-1 — the same order
+//     whichever CTA is last — rounds once and resets the counter.
+//   - Every mbarrier wait is bounded; a timeout records an error bit and
+//     the CTA drains its copies in flight, frees TMEM and returns.
+#include "xv_internal.h"
+#include "xv_ptx.cuh"
+
+namespace xv {
+
+namespace {
+constexpr int STAGES = 4;
+constexpr int A_BYTES = GEMM_BN * GEMM_BK * 2;   // 16 KB of weights per stage
+constexpr int B_BYTES = GEMM_TOK * GEMM_BK * 2;  //  8 KB of tokens per stage
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 64;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BN, GEMM_TOK);
+constexpr int SM_COUNT_TARGET = 152;   // GB300
+constexpr int RESIDENT_PER_SM = 2;
+
+template <bool F32OUT>
+__global__ void __launch_bounds__(128, RESIDENT_PER_SM)
+    gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                        void* __restrict__ Y, int ldy, int M, int N, int nkb, int S, float* __restrict__ part,
+                        unsigned* __restrict__ cnt, unsigned* __restrict__ err) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_last;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + STAGES * A_BYTES;
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;      // full[STAGES], empty[STAGES], done
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t done = bar0 + 8u * (2 * STAGES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 1));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x, seg = blockIdx.y;
+    const int kb0 = static_cast<int>(static_cast<long long>(seg) * nkb / S);
+    const int kb1 = static_cast<int>(static_cast<long long>(seg + 1) * nkb / S);
+    const int nk = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    bool ok = true;
+    if (warp == 0 && lane == 0) {
+        // ---- producer: TMA into the ring
+        int issued = 0;
+        for (int i = 0; i < nk; ++i) {
+            const int st = i % STAGES;
+            const uint32_t ph = (i / STAGES) & 1u;
+            if (i >= STAGES && !mbar_wait(empty(st), ph ^ 1u, err)) { ok = false; break; }
+            mbar_arrive_expect_tx(full(st), STAGE_BYTES);
+            tma_load_2d(sA + st * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(st));
+            tma_load_2d(sB + st * B_BYTES, &tmX, (kb0 + i) * GEMM_BK, 0, full(st));
+            issued = i + 1;
+        }
+        if (!ok) {  // drain: every issued copy must land before the CTA may exit
+            for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+                mbar_wait(full(j % STAGES), (j / STAGES) & 1u, err);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer: 4 MMAs of K = 16 per stage, accumulate in TMEM
+        for (int i = 0; i < nk; ++i) {
+            const int st = i % STAGES;
+            const uint32_t ph = (i / STAGES) & 1u;
+            if (!mbar_wait(full(st), ph, err)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
+                const uint64_t ad = sw128_kmajor_desc(sA + st * A_BYTES + kk * 32);
+                const uint64_t bd = sw128_kmajor_desc(sB + st * B_BYTES + kk * 32);
+                tc_mma_bf16(tmem, ad, bd, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(empty(st));   // the stage is free once these MMAs have read it
+        }
+        tc_commit(done);            // all MMAs issued by this thread are complete
+    }
+    __syncwarp();
+
+    // ---- epilogue: TMEM -> registers; warp w owns weight rows 32w..32w+31
+    if (!mbar_wait(done, 0, err)) ok = false;
+    tc_fence_after();
+    float acc[GEMM_TOK];
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll
+    for (int c = 0; c < GEMM_TOK / 16; ++c)
+        if (c * 16 < M) tmem_ld16(trow + c * 16, acc + c * 16);
+    tmem_ld_wait();
+
+    const int n = tile * GEMM_BN + warp * 32 + lane;
+    const bool live = n < N;
+    if (S == 1) {
+        if (live) {
+#pragma unroll
+            for (int m = 0; m < GEMM_TOK; ++m) {
+                if (m < M) {
+                    if (F32OUT) static_cast<float*>(Y)[static_cast<size_t>(m) * ldy + n] = acc[m];
+                    else static_cast<uint16_t*>(Y)[static_cast<size_t>(m) * ldy + n] = f32_to_bf16(acc[m]);
+                }
+            }
+        }
+    } else {
+        if (live) {
+#pragma unroll
+            for (int m = 0; m < GEMM_TOK; ++m)
+                if (m < M) part[(static_cast<size_t>(seg) * M + m) * N + n] = acc[m];
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = (atomicAdd(&cnt[tile], 1u) == static_cast<unsigned>(S - 1));
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            if (live) {
+#pragma unroll
+                for (int m = 0; m < GEMM_TOK; ++m) {
+                    if (m < M) {
+                        float r = 0.f;
+                        for (int s2 = 0; s2 < S; ++s2) {
+                            const float v = (s2 == seg) ? acc[m] : __ldcg(&part[(static_cast<size_t>(s2) * M + m) * N + n]);
+                            r = (s2 == 0) ? v : __fadd_rn(r, v);
+                        }
+                        if (F32OUT) static_cast<float*>(Y)[static_cast<size_t>(m) * ldy + n] = r;
+                        else static_cast<uint16_t*>(Y)[static_cast<size_t>(m) * ldy + n] = f32_to_bf16(r);
+                    }
+                }
+            }
+            if (threadIdx.x == 0) cnt[tile] = 0u;   // every segment has arrived: ready for the next call
+        }
+    }
+    (void)ok;
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+inline int num_tiles(int N) { return ceil_div(N, GEMM_BN); }
+inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+int gemm_splits(int N, int K) {
+    const int tiles = num_tiles(N);
+    const int nkb = ceil_div(K, GEMM_BK);
+    int s = (SM_COUNT_TARGET * RESIDENT_PER_SM) / tiles;
+    if (s < 1) s = 1;
+    if (s > 16) s = 16;
+    while (s > 1 && nkb / s < 4) --s;
+    return s;
+}
+
+size_t gemm_workspace_size(int M, int N, int K) {
+    const int S = gemm_splits(N, K);
+    if (S == 1) return 0;
+    return round256(static_cast<size_t>(S) * M * N * sizeof(float)) + round256(num_tiles(N) * sizeof(unsigned));
+}
+
+xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, int ldy, bool f32out, int M, int N, int K,
+                      void* ws, size_t ws_bytes, cudaStream_t s) {
+    (void)ws_bytes;
+    unsigned* err = device_error_word();
+    if (!err) return fail(XV_ERR_CUDA, "gemm: device error word unavailable");
+    CUtensorMap tmW, tmX;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+        const uint32_t box[2] = {GEMM_BK, GEMM_BN};
+        if (xv_status st = encode_tiled(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
+                                        CU_TENSOR_MAP_SWIZZLE_128B))
+            return st;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(ldx) * 2};
+        const uint32_t box[2] = {GEMM_BK, GEMM_TOK};
+        if (xv_status st = encode_tiled(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dims, strides, box,
+                                        CU_TENSOR_MAP_SWIZZLE_128B))
+            return st;
+    }
+    const int tiles = num_tiles(N), S = gemm_splits(N, K), nkb = ceil_div(K, GEMM_BK);
+    float* part = nullptr;
+    unsigned* cnt = nullptr;
+    if (S > 1) {
+        part = static_cast<float*>(ws);
+        cnt = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + round256(static_cast<size_t>(S) * M * N * 4));
+    }
+    static bool attr_set[2] = {false, false};
+    auto kern = f32out ? gemm_small_m_kernel<true> : gemm_small_m_kernel<false>;
+    if (!attr_set[f32out]) {
+        if (xv_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES),
+                                      "gemm: set shared memory size"))
+            return st;
+        attr_set[f32out] = true;
+    }
+    dim3 grid(tiles, S);
+    kern<<<grid, 128, SMEM_BYTES, s>>>(tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err);
+    return launched("gemm_small_m_kernel");
+}
+
+}  // namespace xv

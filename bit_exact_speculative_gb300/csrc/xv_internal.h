@@ -1,0 +1,87 @@
+// Host-side internals shared by the translation units of libxv.so.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/xv.h"
+
+namespace xv {
+
+// Records the message for xv_last_error() and returns `code`.
+xv_status fail(xv_status code, const char* fmt, ...);
+// Checks a CUDA runtime result; on failure records it and returns XV_ERR_CUDA.
+xv_status cuda_check(cudaError_t e, const char* what);
+// Checks the launch just made on the calling thread and counts it.
+xv_status launched(const char* what);
+// Device address of the library's device-side error word for the current device.
+unsigned* device_error_word();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+xv_status encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// ---- GEMM (gemm.cu)
+constexpr int GEMM_BN = 128;   // weight rows per CTA (MMA M)
+constexpr int GEMM_BK = 64;    // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int GEMM_TOK = 64;   // token columns of every MMA (MMA N), whatever M is
+int gemm_splits(int N, int K);
+size_t gemm_workspace_size(int M, int N, int K);
+xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, int ldy, bool f32out, int M, int N,
+                      int K, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// ---- GDN (gdn.cu)
+struct GdnStepsDev {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const uint16_t* beta;
+    const uint16_t* gate;
+    long long qkv_stride;
+    long long gate_stride;
+    int rows_per_seq;
+};
+// Replays n_commit[b] (or n_fixed when n_commit is null) pending steps into
+// the state, writing o for them when emit_replay; then k speculative steps of
+// `draft` writing o rows b*k + t.
+xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_commit, int n_fixed, int max_commit,
+                     bool emit_replay, const GdnStepsDev& draft, int k, uint16_t* o, long long o_stride, int B, int H,
+                     int dk, int dv, int qk_l2norm, cudaStream_t s);
+
+// ---- attention (attn.cu)
+constexpr int ATTN_SPLIT = 512;   // positions per split, fixed absolute boundaries
+constexpr int ATTN_TILE = 64;     // positions per tile inside a split
+size_t attn_workspace_size(int B, int R, int Hq, int hd, int max_len);
+// Row r of sequence b sees ctx_len[b] + len_bias + r positions; max_len bounds every such length.
+xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
+                      const int32_t* ctx_len, int len_bias, int R, int B, int Hq, int Hkv, int hd, int Lmax,
+                      int max_len, float scale, const uint16_t* gate, long long gate_stride, uint16_t* out,
+                      long long out_stride, void* ws, size_t ws_bytes, cudaStream_t s);
+// Row (b, r) of src goes to position ctx_len[b] + pos_bias + r.
+xv_status kv_append_launch(const uint16_t* src, long long src_stride, const int32_t* ctx_len, int pos_bias, int R,
+                           int B, int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, cudaStream_t s);
+
+// ---- glue (glue.cu)
+xv_status embed_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, uint16_t* x, cudaStream_t s);
+xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s);
+// x <- bf16(x + y); xn <- rmsnorm(x, w)
+xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps,
+                                  uint16_t* xn, cudaStream_t s);
+// act[m][i] = bf16(silu(gu[m][i]) * gu[m][F + i])
+xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s);
+// gates[m] = [beta(H) | gate(H)] from the b and a columns of proj row m
+xv_status gdn_gates_launch(const uint16_t* proj, long long proj_stride, int b_col, int M, int H, uint16_t* gates,
+                           cudaStream_t s);
+xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, cudaStream_t s);
+xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s);
+// ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (keep checked to lie in [1, k])
+xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,
+                        cudaStream_t s);
+xv_status zero_i32_launch(int32_t* p, int n, cudaStream_t s);
+
+}  // namespace xv

@@ -1,0 +1,273 @@
+"""Python binding of libxv.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/xv.h) and
+takes torch CUDA tensors (any 2-byte dtype for bf16 data, int32, float32);
+every step of the computation runs in the library's kernels.  A missing
+library raises at import of the first call: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libxv.so")
+
+vp = ctypes.c_void_p
+c_int, c_ll, c_sz, c_float = ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t, ctypes.c_float
+
+XV_OK, XV_ERR_ARG, XV_ERR_UNSUPPORTED, XV_ERR_WORKSPACE, XV_ERR_CUDA, XV_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
+XV_GEMM_M_MAX = 64
+XV_KMAX = 16
+
+
+class XVError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"xv error {code}: {msg}")
+        self.code = code
+
+
+class GdnSteps(ctypes.Structure):
+    _fields_ = [("q", vp), ("k", vp), ("v", vp), ("beta", vp), ("gate", vp),
+                ("qkv_stride", c_ll), ("gate_stride", c_ll), ("rows_per_seq", c_int)]
+
+
+class BlockConfig(ctypes.Structure):
+    _fields_ = [("hidden", c_int), ("vocab", c_int), ("mlp", c_int), ("n_layers", c_int), ("layer_kind", vp),
+                ("gdn_heads", c_int), ("gdn_dk", c_int), ("gdn_dv", c_int),
+                ("attn_hq", c_int), ("attn_hkv", c_int), ("attn_hd", c_int), ("rms_eps", c_float)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("norm1", vp), ("w_in", vp), ("w_out", vp), ("norm2", vp), ("w_gate_up", vp), ("w_down", vp)]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [("embed", vp), ("layers", vp), ("final_norm", vp), ("lm_head", vp)]
+
+
+class LayerState(ctypes.Structure):
+    _fields_ = [("gdn_state", vp), ("gdn_hist", vp * 2), ("gdn_gates", vp * 2), ("k_cache", vp), ("v_cache", vp)]
+
+
+class BlockState(ctypes.Structure):
+    _fields_ = [("B", c_int), ("kmax", c_int), ("Lmax", c_int), ("ctx_len", vp), ("n_commit", vp),
+                ("parity", c_int), ("pending_rows", c_int), ("max_ctx", c_int), ("last_k", c_int), ("layers", vp)]
+
+
+_lib = None
+
+_SIGS = {
+    "xv_abi_version": ([], c_int),
+    "xv_last_error": ([], ctypes.c_char_p),
+    "xv_device_check": ([vp, ctypes.POINTER(ctypes.c_uint)], c_int),
+    "xv_launch_count": ([], ctypes.c_ulonglong),
+    "xv_gemm_workspace_size": ([c_int, c_int, c_int], c_sz),
+    "xv_gemm_small_m": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
+    "xv_gemm_small_m_f32out": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
+    "xv_gemm_splits": ([c_int, c_int], c_int),
+    "xv_gdn_decode_step": ([vp, ctypes.POINTER(GdnSteps), vp, c_ll, c_int, c_int, c_int, c_int, c_int, vp], c_int),
+    "xv_gdn_verify": ([vp, ctypes.POINTER(GdnSteps), vp, c_int, ctypes.POINTER(GdnSteps), c_int, vp, c_ll,
+                       c_int, c_int, c_int, c_int, c_int, vp], c_int),
+    "xv_attn_split_size": ([], c_int),
+    "xv_attn_workspace_size": ([c_int, c_int, c_int, c_int, c_int], c_sz),
+    "xv_attn_decode_rows": ([vp, c_ll, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                             vp, c_ll, vp, c_ll, vp, c_sz, vp], c_int),
+    "xv_kv_append": ([vp, c_ll, vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp], c_int),
+    "xv_gdn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
+    "xv_attn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
+    "xv_block_workspace_size": ([ctypes.POINTER(BlockConfig), c_int, c_int, c_int], c_sz),
+    "xv_verify_block": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState),
+                         vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
+    "xv_block_commit": ([ctypes.POINTER(BlockState), vp, vp], c_int),
+    "xv_block_commit_accepted": ([ctypes.POINTER(BlockState), vp, vp], c_int),
+    "xv_block_flush": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockState), vp], c_int),
+}
+
+
+def lib():
+    """The loaded libxv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with bit_exact_speculative_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes, f.restype = args, res
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _check(code: int):
+    if code != XV_OK:
+        raise XVError(code, lib().xv_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _row_stride(t: torch.Tensor) -> int:
+    assert t.dim() >= 2 and t.stride(-1) == 1, "rows must be contiguous"
+    return t.stride(-2) if t.dim() == 2 else t.stride(0)
+
+
+# ------------------------------------------------------------------ misc
+
+def xv_abi_version() -> int:
+    return lib().xv_abi_version()
+
+
+def xv_device_check(stream=None) -> int:
+    code = ctypes.c_uint(0)
+    _check(lib().xv_device_check(_stream(stream), ctypes.byref(code)))
+    return code.value
+
+
+def xv_launch_count() -> int:
+    return int(lib().xv_launch_count())
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace tensor of at least nbytes (the library's workspaces start zeroed)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ GEMM
+
+def xv_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().xv_gemm_workspace_size(M, N, K))
+
+
+def xv_gemm_splits(N: int, K: int) -> int:
+    return int(lib().xv_gemm_splits(N, K))
+
+
+def xv_gemm_small_m(X, W, Y, ws, stream=None):
+    M, K = X.shape[0], X.shape[1]
+    N = W.shape[0]
+    fn = lib().xv_gemm_small_m_f32out if Y.dtype == torch.float32 else lib().xv_gemm_small_m
+    _check(fn(_ptr(X), _row_stride(X), _ptr(W), _ptr(Y), _row_stride(Y), M, N, K, _ptr(ws),
+              0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+    return Y
+
+
+# ------------------------------------------------------------------- GDN
+
+def gdn_steps(q, k, v, beta, gate, qkv_stride: int, gate_stride: int, rows_per_seq: int) -> GdnSteps:
+    return GdnSteps(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), gate.data_ptr(),
+                    qkv_stride, gate_stride, rows_per_seq)
+
+
+def xv_gdn_decode_step(state, step: GdnSteps, o, o_stride: int, B, H, dk, dv, qk_l2norm: bool, stream=None):
+    _check(lib().xv_gdn_decode_step(_ptr(state), ctypes.byref(step), _ptr(o), o_stride, B, H, dk, dv,
+                                    int(qk_l2norm), _stream(stream)))
+
+
+def xv_gdn_verify(state, pending, n_commit, max_commit: int, draft, k: int, o, o_stride: int, B, H, dk, dv,
+                  qk_l2norm: bool, stream=None):
+    _check(lib().xv_gdn_verify(_ptr(state), None if pending is None else ctypes.byref(pending), _ptr(n_commit),
+                               max_commit, None if draft is None else ctypes.byref(draft), k, _ptr(o), o_stride,
+                               B, H, dk, dv, int(qk_l2norm), _stream(stream)))
+
+
+# ------------------------------------------------------------- attention
+
+def xv_attn_split_size() -> int:
+    return int(lib().xv_attn_split_size())
+
+
+def xv_attn_workspace_size(B, R, Hq, hd, max_ctx) -> int:
+    return int(lib().xv_attn_workspace_size(B, R, Hq, hd, max_ctx))
+
+
+def xv_attn_decode_rows(q, q_stride, kc, vc, ctx_len, R, B, Hq, Hkv, hd, Lmax, max_ctx, scale, out, out_stride, ws,
+                        gate=None, gate_stride=0, stream=None):
+    _check(lib().xv_attn_decode_rows(_ptr(q), q_stride, _ptr(kc), _ptr(vc), _ptr(ctx_len), R, B, Hq, Hkv, hd, Lmax,
+                                     max_ctx, float(scale), _ptr(gate), gate_stride, _ptr(out), out_stride, _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def xv_kv_append(kv_src, src_stride, ctx_len, R, B, Hkv, hd, Lmax, kc, vc, stream=None):
+    _check(lib().xv_kv_append(_ptr(kv_src), src_stride, _ptr(ctx_len), R, B, Hkv, hd, Lmax, _ptr(kc), _ptr(vc),
+                              _stream(stream)))
+
+
+# ------------------------------------------------------------------ block
+
+class Block:
+    """Holds the ctypes structs of one model (config, weights, state) over caller-owned tensors.
+
+    ``cfg`` is a dict (hidden, vocab, mlp, kinds, gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv,
+    attn_hd, rms_eps); ``weights`` a dict of device tensors (embed, final_norm, lm_head and per
+    layer ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``);
+    ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1``,
+    ``.gates0``, ``.gates1`` or ``.kc``, ``.vc``).  Tensors are kept referenced here.
+    """
+
+    def __init__(self, cfg: dict, weights: dict, state: dict, B: int, kmax: int, Lmax: int, ctx0: int):
+        kinds = list(cfg["kinds"])
+        self._kinds = (ctypes.c_int32 * len(kinds))(*kinds)
+        self.cfg = BlockConfig(cfg["hidden"], cfg["vocab"], cfg["mlp"], len(kinds),
+                               ctypes.cast(self._kinds, vp).value, cfg.get("gdn_heads", 0), cfg.get("gdn_dk", 0),
+                               cfg.get("gdn_dv", 0), cfg.get("attn_hq", 0), cfg.get("attn_hkv", 0),
+                               cfg.get("attn_hd", 0), float(cfg.get("rms_eps", 1e-6)))
+        self._keep = [weights, state]
+        lw = [LayerWeights(*[weights[f"{l}.{n}"].data_ptr() for n in ("norm1", "w_in", "w_out", "norm2", "w_gu",
+                                                                        "w_down")]) for l in range(len(kinds))]
+        self._lw = (LayerWeights * len(kinds))(*lw)
+        self.weights = BlockWeights(weights["embed"].data_ptr(), ctypes.cast(self._lw, vp).value,
+                                    weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr())
+        ls = []
+        for l, kd in enumerate(kinds):
+            if kd == 0:
+                ls.append(LayerState(state[f"{l}.state"].data_ptr(),
+                                     (vp * 2)(state[f"{l}.hist0"].data_ptr(), state[f"{l}.hist1"].data_ptr()),
+                                     (vp * 2)(state[f"{l}.gates0"].data_ptr(), state[f"{l}.gates1"].data_ptr()),
+                                     None, None))
+            else:
+                ls.append(LayerState(None, (vp * 2)(None, None), (vp * 2)(None, None), state[f"{l}.kc"].data_ptr(),
+                                     state[f"{l}.vc"].data_ptr()))
+        self._ls = (LayerState * len(kinds))(*ls)
+        self.state = BlockState(B, kmax, Lmax, state["ctx_len"].data_ptr(), state["n_commit"].data_ptr(), 0, kmax,
+                                ctx0, 0, ctypes.cast(self._ls, vp).value)
+        self.ws_bytes = int(lib().xv_block_workspace_size(ctypes.byref(self.cfg), B, kmax, Lmax))
+        if self.ws_bytes == 0:
+            _check(XV_ERR_ARG)
+
+    def gdn_in_dim(self) -> int:
+        return int(lib().xv_gdn_in_dim(ctypes.byref(self.cfg)))
+
+    def attn_in_dim(self) -> int:
+        return int(lib().xv_attn_in_dim(ctypes.byref(self.cfg)))
+
+
+def xv_verify_block(blk: Block, tokens, k: int, logits, argmax, n_accept, ws, stream=None):
+    _check(lib().xv_verify_block(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
+                                 _ptr(tokens), k, _ptr(logits), _ptr(argmax), _ptr(n_accept), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def xv_block_commit(blk: Block, n_keep, stream=None):
+    _check(lib().xv_block_commit(ctypes.byref(blk.state), _ptr(n_keep), _stream(stream)))
+
+
+def xv_block_commit_accepted(blk: Block, n_accept, stream=None):
+    _check(lib().xv_block_commit_accepted(ctypes.byref(blk.state), _ptr(n_accept), _stream(stream)))
+
+
+def xv_block_flush(blk: Block, stream=None):
+    _check(lib().xv_block_flush(ctypes.byref(blk.cfg), ctypes.byref(blk.state), _stream(stream)))

@@ -1,0 +1,279 @@
+/*
+ * xv — exact speculative verify for hybrid gated-delta-net / attention decoders
+ * on one GB300 (sm_103a).  C ABI of libxv.so.
+ *
+ * The operations follow a recipe described on these pages:
+ *   [post]  "Follow-up to my earlier post on Qwen3.8-27B decode speed"
+ *           (r/LocalLLaMA post, feedman.me copy)
+ *   [card]  "Qwen3.8-27B Bit-Exact Spec-Decode 1x RTX PRO 6000 SGLang"
+ *           (localairecipes recipe card), summary and install notes
+ *   [digest] "Bit-exact speculative decoding hits 106 t/s on Qwen3.8-27B with
+ *           one RTX PRO 6000" (agihunt digest), Key findings
+ * Their claim, which this library is built to: checking k draft tokens in one
+ * verify pass gives exactly the bits (token ids and logprobs) of decoding the
+ * same tokens one at a time.  Three parts make that so ([post]): the small-M
+ * projection GEMMs reduce in an order that does not depend on the row count;
+ * verify steps the GDN recurrence with the decode step's own code, tiling and
+ * rounding (beta and gate in the decode dtype, bf16); verify attention runs
+ * each draft position as its own decode row.
+ *
+ * Conventions (all entry points):
+ *   - bf16 tensors are passed as uint16_t* bit patterns; fp32 as float*.
+ *   - Every pointer argument is DEVICE memory owned by the caller unless it is
+ *     documented as host memory.  The library allocates nothing, frees
+ *     nothing and never synchronises the stream; work is enqueued on the
+ *     caller's stream `s` (0 = legacy default stream).
+ *   - Scratch space comes from a caller workspace `ws` of `ws_bytes` bytes,
+ *     sized by the matching *_workspace_size() query.  A workspace must be
+ *     zero-filled once before its first use (e.g. cudaMemsetAsync); every call
+ *     leaves its internal counters at zero again.  Calls that run at the same
+ *     time must use distinct workspaces.
+ *   - Arguments are validated on the host before anything is enqueued; on an
+ *     error nothing is launched and the return code says why.  Kernel waits
+ *     are bounded; a wait that runs out records a device-side error that
+ *     xv_device_check() reports.
+ *   - Layout of the row dimension: a batch of B sequences with R rows each is
+ *     stored row (b, r) at index b*R + r.
+ */
+#ifndef XV_H_
+#define XV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* xv_stream;   /* same type as cudaStream_t */
+typedef int xv_status;
+
+#define XV_OK               0
+#define XV_ERR_ARG         -1   /* null pointer, bad shape or inconsistent sizes */
+#define XV_ERR_UNSUPPORTED -2   /* size or alignment outside what the kernels handle */
+#define XV_ERR_WORKSPACE   -3   /* workspace missing or too small */
+#define XV_ERR_CUDA        -4   /* a CUDA runtime call or launch failed */
+#define XV_ERR_DEVICE_CHECK -5  /* a kernel recorded a device-side error (see xv_device_check) */
+
+#define XV_ABI_VERSION 1
+#define XV_GEMM_M_MAX 64        /* rows per small-M GEMM call */
+#define XV_KMAX 16              /* draft tokens per sequence per verify call */
+
+/* Version of this header's ABI (XV_ABI_VERSION). */
+int xv_abi_version(void);
+
+/* Message for the last error returned on the calling host thread ("" if none).
+ * The string is owned by the library and valid until the next call on the thread. */
+const char* xv_last_error(void);
+
+/* Synchronises `s`, then reads and clears the device-side error word of the
+ * current device.  Returns XV_OK, or XV_ERR_DEVICE_CHECK with *code set to the
+ * recorded bits (code may be NULL).  The only call in the library that
+ * synchronises. */
+xv_status xv_device_check(xv_stream s, unsigned* code);
+
+/* Number of kernels this library has launched in this process (host counter). */
+unsigned long long xv_launch_count(void);
+
+/* ------------------------------------------------------------------ GEMM
+ * Small-M bf16 GEMM  Y[M,N] = X[M,K] . W[N,K]^T  with fp32 accumulation.
+ * [post] and [card] summary: at small batch the projection GEMMs of decode
+ * and verify go to a tile that yields the same bits whatever the row count,
+ * and it must stream the weights near DRAM speed ([post]: the previous kernel
+ * read them at about a third of it).
+ *
+ * Contract: row i of Y is bit-identical for every M in 1..XV_GEMM_M_MAX and
+ * for every position of that row inside X, and identical from run to run.
+ * The reduction order over K is a function of (N, K) only.
+ *
+ *   X   [M, ldx] bf16, row-major, 16-byte aligned, ldx % 8 == 0, ldx >= K
+ *   W   [N, K]  bf16, row-major (the weight layout), 16-byte aligned, K % 8 == 0
+ *   Y   [M, ldy] bf16 (xv_gemm_small_m) or fp32 (xv_gemm_small_m_f32out), ldy >= N
+ *   1 <= M <= XV_GEMM_M_MAX, N >= 1, K >= 8
+ * Errors: XV_ERR_ARG (null pointer, M/N/K/ld out of range), XV_ERR_UNSUPPORTED
+ * (alignment, M > XV_GEMM_M_MAX), XV_ERR_WORKSPACE (ws_bytes below
+ * xv_gemm_workspace_size(M, N, K)), XV_ERR_CUDA. */
+size_t xv_gemm_workspace_size(int M, int N, int K);
+xv_status xv_gemm_small_m(const uint16_t* X, int ldx, const uint16_t* W, uint16_t* Y, int ldy,
+                          int M, int N, int K, void* ws, size_t ws_bytes, xv_stream s);
+xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, float* Y, int ldy,
+                                 int M, int N, int K, void* ws, size_t ws_bytes, xv_stream s);
+/* Number of K-segments the GEMM uses for (N, K) (a pure function of N and K). */
+int xv_gemm_splits(int N, int K);
+
+/* ------------------------------------------------------------------- GDN
+ * Gated delta rule, per sequence b and head h, state S [dv][dk] in fp32:
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T ,   o_t = S_t q_t
+ * [post]: verify runs the recurrence through the decode kernel (the faulty
+ * verify tiled the state differently and kept beta in fp32).  Here decode and
+ * verify are the same kernel and the same step function; a step computes, in
+ * fp32 with every operation rounded once:  S <- a S;  r = S k;
+ * u = beta (v - r);  S <- S + u k^T;  o = S q  (o rounded to bf16).
+ *
+ * Step inputs for a set of steps, row (b, t) at index b*rows_per_seq + t:
+ *   q, k  [rows, H, dk] bf16 and v [rows, H, dv] bf16, consecutive rows
+ *         qkv_stride elements apart (heads contiguous inside a row);
+ *   beta, gate [rows, H] bf16 (beta = sigmoid(.), gate = exp(-softplus(.))
+ *         already rounded to bf16), rows gate_stride elements apart.
+ * With qk_l2norm != 0 the kernel normalises q and k per head in fp32
+ * (x / sqrt(sum x^2 + 1e-6)); with 0 they are used as given. */
+typedef struct {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const uint16_t* beta;
+    const uint16_t* gate;
+    long long qkv_stride;
+    long long gate_stride;
+    int rows_per_seq;
+} xv_gdn_steps;
+
+/* One decode step for B sequences: state [B, H, dv, dk] fp32 is updated in
+ * place, o [B, H, dv] bf16 (row b at b*o_stride) receives o_t.
+ * dk in {64, 128}; dv a multiple of 16; 1 <= B, 1 <= H. */
+xv_status xv_gdn_decode_step(float* state, const xv_gdn_steps* step, uint16_t* o, long long o_stride,
+                             int B, int H, int dk, int dv, int qk_l2norm, xv_stream s);
+
+/* Verify with deferred commit.  For each sequence b:
+ *   1. replay n_commit[b] steps of `pending` (rows b*pending.rows_per_seq + 0..)
+ *      into `state` and write the state back (nothing written if 0);
+ *   2. run k speculative steps of `draft` from that state, writing only
+ *      o [B, k, H, dv] bf16 (row (b,t) at (b*k + t)*o_stride).
+ * k = 0 is a pure commit.  After the call the caller keeps `draft` alive: it
+ * becomes the next call's `pending`, with n_commit = the number of positions
+ * kept.  Bit-exactness: o of step t equals the o of decode step t from the
+ * same committed state, and the state after replaying j steps equals j
+ * decode steps.  n_commit is device memory [B] with 0 <= n_commit[b] <= max_commit;
+ * 0 <= k <= XV_KMAX, max_commit <= XV_KMAX. */
+xv_status xv_gdn_verify(float* state, const xv_gdn_steps* pending, const int32_t* n_commit, int max_commit,
+                        const xv_gdn_steps* draft, int k, uint16_t* o, long long o_stride,
+                        int B, int H, int dk, int dv, int qk_l2norm, xv_stream s);
+
+/* ------------------------------------------------------------- attention
+ * Decode-row attention over a bf16 KV cache.  [post]: verify attention runs
+ * as decode rows, one per draft position.  Row r of sequence b is the query
+ * at position ctx_len[b] - 1 + r and attends to positions [0, ctx_len[b] + r):
+ *   out = softmax(q . K^T * scale) V      per query head h, kv head h / (Hq/Hkv).
+ * The positions are cut into splits of xv_attn_split_size() tokens at fixed
+ * absolute boundaries, each split is reduced with an fp32 online softmax over
+ * fixed 64-position tiles, and the splits are combined in split order; a row
+ * therefore gets the same bits as an R = 1 call with ctx_len[b] + r.
+ *
+ *   q     [B*R rows, Hq*hd] bf16, row stride q_stride elements (16-byte aligned rows)
+ *   kc,vc [B, Hkv, Lmax, hd] bf16 (16-byte aligned)
+ *   ctx_len [B] int32 device: visible length of row 0 (includes its own token),
+ *         1 <= ctx_len[b] and ctx_len[b] + R - 1 <= max_ctx <= Lmax
+ *   max_ctx host int: upper bound used to size the grid (a larger value only
+ *         launches blocks that exit at once)
+ *   out   [B*R rows, Hq*hd] bf16, row stride out_stride
+ *   gate  optional [B*R rows, Hq*hd] bf16 with row stride gate_stride, or NULL:
+ *         when given, out = bf16( bf16(attn) * sigmoid(gate) ) (the gated
+ *         attention layer's output gate), else out = bf16(attn)
+ *   hd = 256 or 64 (hd % 64 == 0), Hq % Hkv == 0, R*(Hq/Hkv) <= 64, 1 <= R <= XV_KMAX
+ * Workspace: xv_attn_workspace_size(B, R, Hq, hd, max_ctx) bytes. */
+int xv_attn_split_size(void);
+size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx);
+xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
+                              const int32_t* ctx_len, int R, int B, int Hq, int Hkv, int hd, int Lmax,
+                              int max_ctx, float scale, const uint16_t* gate, long long gate_stride,
+                              uint16_t* out, long long out_stride, void* ws, size_t ws_bytes, xv_stream s);
+
+/* Writes the K and V rows of a verify block into the caches: row (b, r) of
+ * kv_src (k at column offset 0, v at column offset Hkv*hd, row stride
+ * src_stride) goes to position ctx_len[b] - 1 + r of sequence b. */
+xv_status xv_kv_append(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B,
+                       int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, xv_stream s);
+
+/* ------------------------------------------------------------ the block
+ * A stack of decoder layers (each: x + mixer(rmsnorm(x)), then
+ * h + SwiGLU-MLP(rmsnorm(h))), mixers being GDN or gated attention layers,
+ * under an embedding and an LM head with a final RMSNorm.  Verify takes k
+ * token ids per sequence (the last committed token, then k-1 drafts) and
+ * returns the fp32 logits of the k positions, their argmax (lowest index on
+ * ties) and the greedy acceptance count ([post]: temperature 0, every draft
+ * compared with the target's argmax).  Decode is k = 1 through the same path.
+ *
+ * Column layouts of the input projections (rows of w_in):
+ *   GDN:       [ q (H*dk) | k (H*dk) | v (H*dv) | b (H) | a (H) ]
+ *   attention: [ q (Hq*hd) | gate (Hq*hd) | k (Hkv*hd) | v (Hkv*hd) ]
+ * RMSNorm: y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ). */
+typedef struct {
+    int hidden;               /* H */
+    int vocab;                /* V */
+    int mlp;                  /* F */
+    int n_layers;
+    const int32_t* layer_kind;/* HOST array [n_layers]: 0 = GDN, 1 = attention */
+    int gdn_heads, gdn_dk, gdn_dv;
+    int attn_hq, attn_hkv, attn_hd;
+    float rms_eps;
+} xv_block_config;
+
+typedef struct {
+    const uint16_t* norm1;    /* [H] */
+    const uint16_t* w_in;     /* [in_dim, H] */
+    const uint16_t* w_out;    /* [H, inner] (inner = gdn_heads*gdn_dv or attn_hq*attn_hd) */
+    const uint16_t* norm2;    /* [H] */
+    const uint16_t* w_gate_up;/* [2F, H]: F gate rows, then F up rows */
+    const uint16_t* w_down;   /* [H, F] */
+} xv_layer_weights;
+
+typedef struct {
+    const uint16_t* embed;            /* [V, H] */
+    const xv_layer_weights* layers;   /* HOST array [n_layers] of device pointers */
+    const uint16_t* final_norm;       /* [H] */
+    const uint16_t* lm_head;          /* [V, H] */
+} xv_block_weights;
+
+typedef struct {
+    float* gdn_state;         /* GDN layer: [B, heads, dv, dk] fp32 */
+    uint16_t* gdn_hist[2];    /* GDN layer: two [B*kmax, gdn_in_dim] bf16 projection buffers */
+    uint16_t* gdn_gates[2];   /* GDN layer: two [B*kmax, 2*heads] bf16 (beta | gate) */
+    uint16_t* k_cache;        /* attention layer: [B, Hkv, Lmax, hd] bf16 */
+    uint16_t* v_cache;
+} xv_layer_state;
+
+typedef struct {
+    int B, kmax, Lmax;
+    int32_t* ctx_len;         /* [B] device: tokens committed to the KV cache */
+    int32_t* n_commit;        /* [B] device: pending GDN steps (set by commit) */
+    int parity;               /* host: which history buffer the next verify writes */
+    int pending_rows;         /* host: rows per sequence of the pending history (k of the last verify) */
+    int max_ctx;              /* host: upper bound of every ctx_len[b] (grid sizing) */
+    int last_k;               /* host: k of the last verify not yet committed (0 = none) */
+    xv_layer_state* layers;   /* HOST array [n_layers] */
+} xv_block_state;
+
+int xv_gdn_in_dim(const xv_block_config* cfg);
+int xv_attn_in_dim(const xv_block_config* cfg);
+
+/* Workspace for xv_verify_block with B sequences of up to kmax tokens. */
+size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);
+
+/* tokens [B, k] int32 device; logits [B*k, V] fp32 device or NULL; argmax
+ * [B*k] int32; n_accept [B] int32 = leading drafts equal to the argmax of the
+ * position before them (0..k-1).  Requires 1 <= k <= st->kmax, B == st->B,
+ * B*k <= XV_GEMM_M_MAX, st->max_ctx + k <= Lmax.  Appends the k rows to the KV
+ * caches (uncommitted), replays the pending GDN steps into the states and
+ * records this call's GDN inputs as the next pending steps. */
+xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                          const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept,
+                          void* ws, size_t ws_bytes, xv_stream s);
+
+/* Commit n_keep[b] (device, 1..k) positions of the last verify: ctx_len += n_keep,
+ * n_commit = n_keep; flips the history parity and advances max_ctx by the k of
+ * that verify.  [post]: the result must also be exact with every draft forced
+ * to reject (n_keep = 1). */
+xv_status xv_block_commit(xv_block_state* st, const int32_t* n_keep, xv_stream s);
+
+/* Standard commit: n_keep = n_accept + 1 (device arrays). */
+xv_status xv_block_commit_accepted(xv_block_state* st, const int32_t* n_accept, xv_stream s);
+
+/* Replays the pending GDN steps of every GDN layer into its state (k = 0
+ * verify per layer) and zeroes n_commit, so the states hold the committed
+ * position.  Needs the same cfg as the verify calls. */
+xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stream s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XV_H_ */

@@ -1,0 +1,120 @@
+"""The C-ABI library loads without a GPU, exports every declared entry point,
+and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def xv():
+    from bit_exact_speculative_gb300 import build
+    build.build()
+    from bit_exact_speculative_gb300 import xv as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "xv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(xv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(xv):
+    lib = ctypes.CDLL(xv.LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 20
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(names) == set(xv.exported_symbols())
+
+
+def test_abi_version(xv):
+    assert xv.xv_abi_version() == 1
+
+
+def _code(fn, *args):
+    return fn(*args)
+
+
+def test_gemm_validation_without_gpu(xv):
+    L = xv.lib()
+    p = ctypes.c_void_p(0x10000)
+    assert L.xv_gemm_small_m(None, 64, p, p, 64, 1, 64, 64, None, 0, None) == xv.XV_ERR_ARG
+    assert b"null" in L.xv_last_error()
+    assert L.xv_gemm_small_m(p, 64, p, p, 64, 65, 64, 64, None, 0, None) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_gemm_small_m(p, 64, p, p, 64, 0, 64, 64, None, 0, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_small_m(p, 60, p, p, 64, 1, 64, 64, None, 0, None) == xv.XV_ERR_ARG          # ldx < K
+    assert L.xv_gemm_small_m(p, 68, p, p, 64, 1, 64, 68, None, 0, None) == xv.XV_ERR_UNSUPPORTED  # K % 8
+    odd = ctypes.c_void_p(0x10002)
+    assert L.xv_gemm_small_m(odd, 64, p, p, 64, 1, 64, 64, None, 0, None) == xv.XV_ERR_UNSUPPORTED
+    # a split-K shape needs a workspace
+    assert xv.xv_gemm_splits(5120, 17408) > 1
+    assert xv.xv_gemm_workspace_size(8, 5120, 17408) > 0
+    assert L.xv_gemm_small_m(p, 17408, p, p, 5120, 8, 5120, 17408, None, 0, None) == xv.XV_ERR_WORKSPACE
+
+
+def test_gemm_splits_depend_on_shape_only(xv):
+    for N, K in [(5120, 4096), (5120, 6144), (5120, 17408), (12352, 5120), (14336, 5120), (34816, 5120), (151936, 5120)]:
+        s = xv.xv_gemm_splits(N, K)
+        assert 1 <= s <= 16
+        assert -(-K // 64) // s >= 4 or s == 1
+        assert xv.xv_gemm_workspace_size(1, N, K) <= xv.xv_gemm_workspace_size(64, N, K)
+
+
+def test_gdn_validation_without_gpu(xv):
+    L = xv.lib()
+    p = 0x10000
+    st = xv.GdnSteps(p, p, p, p, p, 128 * 3, 2, 8)
+    assert L.xv_gdn_decode_step(None, ctypes.byref(st), ctypes.c_void_p(p), 128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_ARG
+    assert L.xv_gdn_decode_step(ctypes.c_void_p(p), ctypes.byref(st), ctypes.c_void_p(p), 128, 1, 1, 96, 128, 1, None) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_gdn_decode_step(ctypes.c_void_p(p), ctypes.byref(st), ctypes.c_void_p(p), 128, 1, 1, 128, 40, 1, None) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_gdn_verify(ctypes.c_void_p(p), ctypes.byref(st), None, 4, ctypes.byref(st), 8, ctypes.c_void_p(p),
+                           128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_ARG  # n_commit missing
+    assert L.xv_gdn_verify(ctypes.c_void_p(p), None, None, 0, ctypes.byref(st), 17, ctypes.c_void_p(p),
+                           128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_UNSUPPORTED  # k > 16
+    short = xv.GdnSteps(p, p, p, p, p, 128 * 3, 2, 4)
+    assert L.xv_gdn_verify(ctypes.c_void_p(p), None, None, 0, ctypes.byref(short), 8, ctypes.c_void_p(p),
+                           128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_ARG  # draft rows < k
+
+
+def test_attn_validation_without_gpu(xv):
+    L = xv.lib()
+    p = ctypes.c_void_p(0x10000)
+    args = lambda **kw: [kw.get("q", p), 6144, p, p, p, kw.get("R", 8), 1, kw.get("Hq", 24), kw.get("Hkv", 4),
+                         kw.get("hd", 256), 4096, kw.get("max_ctx", 3000), 0.0625, None, 0, p, 6144,
+                         kw.get("ws", p), kw.get("wsb", 1 << 30), None]
+    assert L.xv_attn_decode_rows(*args(q=None)) == xv.XV_ERR_ARG
+    assert L.xv_attn_decode_rows(*args(hd=128)) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_attn_decode_rows(*args(Hq=25)) == xv.XV_ERR_ARG
+    assert L.xv_attn_decode_rows(*args(R=17)) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_attn_decode_rows(*args(Hq=80, Hkv=4)) == xv.XV_ERR_UNSUPPORTED      # 8 rows x 20 heads > 64
+    assert L.xv_attn_decode_rows(*args(max_ctx=5000)) == xv.XV_ERR_ARG              # beyond Lmax
+    assert L.xv_attn_decode_rows(*args(ws=None)) == xv.XV_ERR_WORKSPACE
+    assert xv.xv_attn_split_size() == 512
+    assert xv.xv_attn_workspace_size(1, 8, 24, 256, 2183) >= 8 * 24 * 5 * 256 * 4
+
+
+def _cfg(xv, kinds=(0, 0, 0, 1)):
+    kinds_arr = (ctypes.c_int32 * len(kinds))(*kinds)
+    c = xv.BlockConfig(5120, 151936, 17408, len(kinds), ctypes.cast(kinds_arr, ctypes.c_void_p).value,
+                       32, 128, 128, 24, 4, 256, 1e-6)
+    return c, kinds_arr
+
+
+def test_block_dims_and_validation_without_gpu(xv):
+    L = xv.lib()
+    c, keep = _cfg(xv)
+    assert L.xv_gdn_in_dim(ctypes.byref(c)) == 12352
+    assert L.xv_attn_in_dim(ctypes.byref(c)) == 14336
+    assert L.xv_block_workspace_size(ctypes.byref(c), 1, 8, 4096) > 0
+    bad, keep2 = _cfg(xv, kinds=(0, 2))
+    assert L.xv_gdn_in_dim(ctypes.byref(bad)) == -1
+    st = xv.BlockState()
+    w = xv.BlockWeights()
+    assert L.xv_verify_block(ctypes.byref(c), ctypes.byref(w), ctypes.byref(st), None, 8, None, None, None, None, 0,
+                             None) == xv.XV_ERR_ARG
+    assert L.xv_block_commit(ctypes.byref(st), None, None) == xv.XV_ERR_ARG
