@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
 
     // ---- epilogue: TMEM -> registers; warp w owns weight rows 32w..32w+31
     if (!mbar_wait(done, 0, err)) ok = false;
+    __syncwarp();   // tcgen05.ld is warp-collective: reconverge after the wait loop
     tc_fence_after();
     float acc[GEMM_TOK];
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);

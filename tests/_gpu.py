@@ -1,0 +1,77 @@
+"""Helpers shared by the GPU tests: host<->device copies of bit patterns and the tolerances.
+
+Tolerances (stated once, used everywhere):
+  - bf16 outputs vs the oracle: max|err| <= 2e-2 * RMS(reference);
+  - fp32 GDN state vs the oracle (same bf16 inputs on both sides):
+    max_i |d_i| / max(|ref_i|, RMS(ref)) <= 1e-4;
+  - fp32 logits vs the oracle: max|err| <= 2e-2 * RMS(reference);
+  - GPU vs GPU comparisons: 0 differing bits.
+"""
+import numpy as np
+import torch
+
+BF16_REL = 2e-2
+STATE_REL = 1e-4
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def host_u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def f64(u16: np.ndarray) -> np.ndarray:
+    return (np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rms(x) -> float:
+    x = np.asarray(x, dtype=np.float64)
+    return float(np.sqrt(np.mean(x * x)))
+
+
+def assert_bf16_close(got_u16, ref, rel=BF16_REL, what=""):
+    """got: bf16 bits; ref: bf16 bits (uint16) or float values."""
+    g = f64(got_u16)
+    r = f64(ref) if np.asarray(ref).dtype == np.uint16 else np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = float(np.max(np.abs(g - r))) if g.size else 0.0
+    bound = rel * rms(r)
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {rel} * RMS = {bound:.3e}"
+    return err / max(rms(r), 1e-300)
+
+
+def assert_f32_close(got, ref, rel=BF16_REL, what=""):
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = float(np.max(np.abs(g - r)))
+    bound = rel * rms(r)
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {rel} * RMS = {bound:.3e}"
+
+
+def assert_state_close(got, ref, rel=STATE_REL, what="state"):
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    floor = np.maximum(np.abs(r), rms(r))
+    worst = float(np.max(np.abs(g - r) / floor))
+    assert worst <= rel, f"{what}: max rel err {worst:.3e} > {rel}"
+    return worst
+
+
+def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
+    if a.shape != b.shape:
+        return False
+    if a.dtype in (torch.float32,):
+        return torch.equal(a.view(torch.int32), b.view(torch.int32))
+    if a.element_size() == 2:
+        return torch.equal(a.view(torch.int16), b.view(torch.int16))
+    return torch.equal(a, b)

@@ -1,0 +1,134 @@
+"""Decode-row attention: parity with the oracle (explicit fp64 softmax), every
+verify row bit-identical to a single decode row at its position, 8 sequences
+in flight, cache garbage past the visible length ignored, run-to-run
+repeatability; GQA 24/4 heads of 256 at 640, 2183 and 131072 positions."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import assert_bf16_close, dev, f64, host_u16, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def xv():
+    from bit_exact_speculative_gb300 import build
+    build.build()
+    from bit_exact_speculative_gb300 import xv as m
+    return m
+
+
+def make(seed, B, R, Hq, Hkv, hd, Lmax, name="a"):
+    q = synth.normal_bf16(seed, synth.tid(f"{name}.q"), (B * R, Hq * hd))
+    kc = synth.normal_bf16(seed, synth.tid(f"{name}.k"), (B, Hkv, Lmax, hd))
+    vc = synth.normal_bf16(seed, synth.tid(f"{name}.v"), (B, Hkv, Lmax, hd))
+    return q, kc, vc
+
+
+def attn(xv, q, kc, vc, ctx, R, B, Hq, Hkv, hd, Lmax, max_ctx, gate=None):
+    out = torch.empty((B * R, Hq * hd), dtype=torch.int16, device="cuda")
+    ws = xv.workspace(xv.xv_attn_workspace_size(B, R, Hq, hd, max_ctx))
+    xv.xv_attn_decode_rows(q, q.stride(0), kc, vc, ctx, R, B, Hq, Hkv, hd, Lmax, max_ctx, hd ** -0.5, out,
+                           out.stride(0), ws, gate=gate, gate_stride=0 if gate is None else gate.stride(0))
+    return out
+
+
+@pytest.mark.parametrize("hd,Hq,Hkv,R,lens", [(256, 4, 2, 3, [700, 1100]), (64, 2, 1, 4, [128, 1]),
+                                               (256, 24, 4, 8, [2183]), (64, 6, 2, 1, [63, 64, 65, 513])])
+def test_parity_with_oracle(xv, hd, Hq, Hkv, R, lens):
+    B = len(lens)
+    Lmax = max(lens) + R + 64
+    q, kc, vc = make(1, B, R, Hq, Hkv, hd, Lmax, name=f"p{hd}{Hq}{R}")
+    ctx = np.array(lens, dtype=np.int32)
+    out = host_u16(attn(xv, dev(q), dev(kc), dev(vc), dev(ctx), R, B, Hq, Hkv, hd, Lmax, max(lens) + R - 1))
+    for b in range(B):
+        ref = oracle.attn_rows(q[b * R:(b + 1) * R].reshape(R, Hq, hd), kc[b], vc[b], lens[b], hd ** -0.5)
+        assert_bf16_close(out[b * R:(b + 1) * R].reshape(R, Hq, hd), ref, what=f"attn b{b} len{lens[b]}")
+    assert xv.xv_device_check() == 0
+
+
+def test_gated_output_parity(xv):
+    B, R, Hq, Hkv, hd, L = 1, 4, 4, 1, 256, 900
+    Lmax = 1024
+    q, kc, vc = make(2, B, R, Hq, Hkv, hd, Lmax, name="gate")
+    g = synth.normal_bf16(2, synth.tid("gate.g"), (B * R, Hq * hd))
+    out = host_u16(attn(xv, dev(q), dev(kc), dev(vc), dev(np.array([L], np.int32)), R, B, Hq, Hkv, hd, Lmax, L + R,
+                        gate=dev(g)))
+    ref = oracle.attn_rows(q.reshape(R, Hq, hd), kc[0], vc[0], L, hd ** -0.5).reshape(R, -1)
+    gated = oracle.round_bf16(f64(ref) / (1.0 + np.exp(-f64(g))))
+    assert_bf16_close(out, gated, what="gated")
+
+
+@pytest.mark.parametrize("L", [640, 2183, 131072])
+def test_verify_rows_equal_decode_rows(xv, L):
+    """Row r of an R=8 call equals an R=1 call with ctx_len + r (GQA 24/4, hd 256)."""
+    B, R, Hq, Hkv, hd = 1, 8, 24, 4, 256
+    Lmax = L + R
+    q, kc, vc = make(3, B, R, Hq, Hkv, hd, Lmax, name=f"rows{L}")
+    Q, K, V = dev(q), dev(kc), dev(vc)
+    out = attn(xv, Q, K, V, dev(np.array([L], np.int32)), R, B, Hq, Hkv, hd, Lmax, L + R - 1)
+    for r in range(R):
+        one = attn(xv, Q[r:r + 1], K, V, dev(np.array([L + r], np.int32)), 1, B, Hq, Hkv, hd, Lmax, L + r)
+        assert same_bits(out[r:r + 1], one), f"row {r} differs from the decode row at length {L + r}"
+    # sampled parity with the oracle at this size: first and last row, three heads
+    o = host_u16(out).reshape(R, Hq, hd)
+    for r in (0, R - 1):
+        for h in (0, 5, 23):
+            g = h // (Hq // Hkv)
+            ref = oracle.attn_row(q[r, h * hd:(h + 1) * hd], kc[0, g], vc[0, g], L + r, hd ** -0.5)
+            assert_bf16_close(o[r, h], ref, what=f"L{L} r{r} h{h}")
+
+
+def test_eight_in_flight_equal_alone(xv):
+    B, R, Hq, Hkv, hd = 8, 8, 24, 4, 256
+    lens = np.array([640, 2183, 1, 513, 1024, 100, 2000, 511], dtype=np.int32)
+    Lmax = 2304
+    q, kc, vc = make(4, B, R, Hq, Hkv, hd, Lmax, name="flight")
+    Q, K, V = dev(q), dev(kc), dev(vc)
+    out = attn(xv, Q, K, V, dev(lens), R, B, Hq, Hkv, hd, Lmax, int(lens.max()) + R - 1)
+    for b in range(B):
+        one = attn(xv, Q[b * R:(b + 1) * R], K[b:b + 1], V[b:b + 1], dev(lens[b:b + 1]), R, 1, Hq, Hkv, hd, Lmax,
+                   int(lens[b]) + R - 1)
+        assert same_bits(out[b * R:(b + 1) * R], one), f"sequence {b} differs when batched"
+
+
+def test_garbage_past_length_is_ignored(xv):
+    """NaN and Inf bit patterns past the last visible position change nothing."""
+    B, R, Hq, Hkv, hd, L, Lmax = 1, 8, 24, 4, 256, 1000, 1152
+    q, kc, vc = make(5, B, R, Hq, Hkv, hd, Lmax, name="nan")
+    Q = dev(q)
+    clean = attn(xv, Q, dev(kc), dev(vc), dev(np.array([L], np.int32)), R, B, Hq, Hkv, hd, Lmax, L + R - 1)
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[:, :, L + R - 1:] = 0x7FC0   # NaN
+    vc2[:, :, L + R - 1:] = 0x7F80   # +Inf
+    dirty = attn(xv, Q, dev(kc2), dev(vc2), dev(np.array([L], np.int32)), R, B, Hq, Hkv, hd, Lmax, L + R - 1)
+    assert same_bits(clean, dirty)
+
+
+def test_hundred_runs_identical(xv):
+    B, R, Hq, Hkv, hd, Lmax = 2, 8, 24, 4, 256, 4096
+    q, kc, vc = make(6, B, R, Hq, Hkv, hd, Lmax, name="rep")
+    Q, K, V, ctx = dev(q), dev(kc), dev(vc), dev(np.array([3000, 1700], np.int32))
+    ref = attn(xv, Q, K, V, ctx, R, B, Hq, Hkv, hd, Lmax, 3007)
+    for _ in range(100):
+        assert same_bits(attn(xv, Q, K, V, ctx, R, B, Hq, Hkv, hd, Lmax, 3007), ref)
+    assert xv.xv_device_check() == 0
+
+
+def test_kv_append_places_rows(xv):
+    B, R, Hkv, hd, Lmax = 2, 3, 4, 256, 64
+    src = synth.normal_bf16(7, synth.tid("kvsrc"), (B * R, 2 * Hkv * hd))
+    kc = torch.zeros((B, Hkv, Lmax, hd), dtype=torch.int16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ctx = np.array([10, 40], dtype=np.int32)      # visible length of row 0: row r lands at ctx - 1 + r
+    xv.xv_kv_append(dev(src), 2 * Hkv * hd, dev(ctx), R, B, Hkv, hd, Lmax, kc, vc)
+    k, v = host_u16(kc), host_u16(vc)
+    for b in range(B):
+        for r in range(R):
+            row = src[b * R + r]
+            assert np.array_equal(k[b, :, ctx[b] - 1 + r].reshape(-1), row[:Hkv * hd])
+            assert np.array_equal(v[b, :, ctx[b] - 1 + r].reshape(-1), row[Hkv * hd:])
+    assert int((k != 0).sum()) == B * R * Hkv * hd - int((src[:, :Hkv * hd] == 0).sum())

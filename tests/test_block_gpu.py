@@ -1,0 +1,217 @@
+"""The verify block end to end: verify(k) gives the logits and argmax of k
+sequential decodes bit for bit, also after forced rejects and with 8
+sequences in flight; logits match the oracle's sequential decode within the
+stated tolerance.  Tiny hybrid block and the 4-layer 5120-wide stack."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import workloads
+from _block import gpu_stack, oracle_stack
+from _gpu import assert_f32_close, assert_bf16_close, dev, host, rms, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def built():
+    from bit_exact_speculative_gb300 import build
+    build.build()
+    from bit_exact_speculative_gb300 import xv
+    return xv
+
+
+def sequential(stk, toks, B):
+    """Decode each column of toks (k = 1 verify + keep 1); returns logits [B, T, V], argmax [B, T]."""
+    T = toks.shape[1]
+    lgs, ams = [], []
+    one = torch.ones(B, dtype=torch.int32, device="cuda")
+    for t in range(T):
+        lg, am, _ = stk.verify(dev(np.ascontiguousarray(toks[:, t:t + 1])), 1)
+        lgs.append(lg.clone())
+        ams.append(am.clone())
+        stk.commit(one)
+    return torch.stack(lgs, 1), torch.stack(ams, 1)
+
+
+def check_argmax_vs_oracle(am_gpu, ref_logits, tol):
+    """Argmax ids must agree wherever the oracle's top-1/top-2 margin exceeds the logit tolerance."""
+    checked = 0
+    for row, ref in zip(am_gpu, ref_logits):
+        top2 = np.sort(ref)[-2:]
+        if top2[1] - top2[0] > tol:
+            assert int(row) == int(np.argmax(ref))
+            checked += 1
+    return checked
+
+
+# ------------------------------------------------------------ tiny block
+
+@pytest.fixture(scope="module")
+def tiny(built):
+    cfg = workloads.TINY
+    return cfg, workloads.weights(cfg, seed=0)
+
+
+def test_tiny_verify_equals_sequential_decode_and_oracle(tiny):
+    cfg, w = tiny
+    B, k, L, Lmax = 1, 4, 128, 256
+    toks = workloads.draft_tokens(cfg, 0, 0, B, k)
+    A = gpu_stack(cfg, w, B, k, Lmax, [L])
+    lg, am, na = A.verify(dev(toks), k)
+    lgA, amA = lg.clone(), am.clone()
+    S = gpu_stack(cfg, w, B, k, Lmax, [L])
+    lgS, amS = sequential(S, toks, B)
+    assert same_bits(lgA.view(B, k, -1), lgS), "verify logits differ from sequential decode"
+    assert torch.equal(amA.view(B, k), amS)
+    ref = oracle_stack(cfg, w, 0, B, [L], Lmax).verify(toks[0])
+    assert_f32_close(host(lgA), ref, what="tiny logits vs oracle")
+    check_argmax_vs_oracle(host(amA), ref, 8 * 2e-2 * rms(ref) / 8)
+    # n_accept follows the rule on the GPU's own argmax
+    assert int(na[0]) == oracle.accept(toks[0], host(amA))
+
+
+@pytest.mark.parametrize("keep", [1, 2, 3, 4])
+def test_tiny_forced_reject_then_next_round(tiny, keep):
+    """Keep `keep` positions of a verify (keep = 1 is every draft rejected), verify 4 more tokens:
+    logits equal decoding the kept tokens and then the new ones; GDN state after a flush matches."""
+    cfg, w = tiny
+    B, k, L, Lmax = 1, 4, 128, 256
+    t1 = workloads.draft_tokens(cfg, 0, 1, B, k)
+    t2 = workloads.draft_tokens(cfg, 0, 2, B, k)
+    A = gpu_stack(cfg, w, B, k, Lmax, [L])
+    A.verify(dev(t1), k)
+    A.commit(torch.full((B,), keep, dtype=torch.int32, device="cuda"))
+    lg, am, _ = A.verify(dev(t2), k)
+    lgA = lg.clone()
+    S = gpu_stack(cfg, w, B, k, Lmax, [L])
+    sequential(S, t1[:, :keep], B)
+    lgS, _ = sequential(S, t2, B)
+    assert same_bits(lgA.view(B, k, -1), lgS)
+    # commit all of round 2 and flush both: GDN states and lengths agree bit for bit
+    A.commit(torch.full((B,), k, dtype=torch.int32, device="cuda"))
+    A.flush()
+    S.flush()
+    assert torch.equal(A.state["ctx_len"], S.state["ctx_len"])
+    assert same_bits(A.state["0.state"], S.state["0.state"])
+    # and the oracle, decoding the same kept tokens, agrees within tolerance
+    ost = oracle_stack(cfg, w, 0, B, [L], Lmax)
+    ost.verify(t1[0, :keep])
+    ref = ost.verify(t2[0])
+    assert_f32_close(host(lgA), ref, what="after rollback vs oracle")
+    Sg = host(A.state["0.state"])[0]
+    assert float(np.max(np.abs(Sg - ost.S[0]))) <= 2e-2 * rms(ost.S[0])
+
+
+def test_tiny_speculative_rounds_emit_greedy_decode(tiny):
+    """Verify/accept/commit rounds with drafts partly right: the emitted tokens are exactly
+    the target's greedy decode, and each round accepts at least the right drafts."""
+    cfg, w = tiny
+    B, k, L, Lmax = 1, 4, 128, 512
+    S = gpu_stack(cfg, w, B, k, Lmax, [L])
+    first = int(workloads.draft_tokens(cfg, 0, 99, 1, 1)[0, 0])
+    greedy, t = [], first
+    for _ in range(40):
+        _, am, _ = S.verify(dev(np.array([[t]], dtype=np.int32)), 1)
+        S.commit(torch.ones(1, dtype=torch.int32, device="cuda"))
+        t = int(host(am)[0])
+        greedy.append(t)
+    A = gpu_stack(cfg, w, B, k, Lmax, [L])
+    rng = np.random.default_rng(0)
+    prev, pos, rnd = first, 0, 0
+    while pos + k <= len(greedy):
+        n_right = int(rng.integers(0, k))
+        junk = list(workloads.draft_tokens(cfg, 0, 200 + rnd, 1, k)[0])
+        drafts = greedy[pos:pos + n_right] + [(x + 1) % cfg["vocab"] if x == g else x
+                                               for x, g in zip(junk, greedy[pos + n_right:])][: k - 1 - n_right]
+        toks = np.array([[prev] + drafts], dtype=np.int32)
+        _, am, na = A.verify(dev(toks), k)
+        n = int(host(na)[0])
+        assert n == n_right
+        out = [int(x) for x in host(am)[: n + 1]]
+        assert out == greedy[pos:pos + n + 1], f"round {rnd}"
+        A.commit()
+        prev, pos, rnd = out[-1], pos + n + 1, rnd + 1
+    assert int(host(A.state["ctx_len"])[0]) == L + pos
+
+
+# ------------------------------------------------------ 4-layer stack
+
+@pytest.fixture(scope="module")
+def stack(built):
+    cfg = workloads.STACK
+    w = workloads.weights(cfg, seed=0)
+    wd = {k: dev(v) for k, v in w.items()}
+    return cfg, w, wd
+
+
+def test_stack_verify_equals_sequential_decode(stack):
+    cfg, w, wd = stack
+    B, k, L = 1, 8, 2183
+    Lmax = L + 64
+    toks = workloads.draft_tokens(cfg, 0, 0, B, k)
+    A = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lg, am, na = A.verify(dev(toks), k)
+    lgA, amA = lg.clone(), am.clone()
+    S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lgS, amS = sequential(S, toks, B)
+    assert same_bits(lgA.view(B, k, -1), lgS)
+    assert torch.equal(amA.view(B, k), amS)
+    # oracle parity on the first two positions (each oracle decode streams 6 GB of weights)
+    ost = oracle_stack(cfg, w, 0, B, [L], Lmax)
+    ref = ost.verify(toks[0, :2])
+    assert_f32_close(host(lgA)[:2], ref, what="stack logits vs oracle")
+    check_argmax_vs_oracle(host(amA)[:2], ref, 2e-2 * rms(ref))
+
+
+def test_stack_forced_reject_every_j(stack):
+    cfg, w, wd = stack
+    B, k, L = 1, 8, 2183
+    Lmax = L + 64
+    t1 = workloads.draft_tokens(cfg, 0, 1, B, k)
+    t2 = workloads.draft_tokens(cfg, 0, 2, B, k)
+    S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    for keep in range(1, k + 1):
+        A = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+        A.verify(dev(t1), k)
+        A.commit(torch.full((B,), keep, dtype=torch.int32, device="cuda"))
+        lgA = A.verify(dev(t2), k)[0].clone()
+        S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+        sequential(S, t1[:, :keep], B)
+        lgS, _ = sequential(S, t2, B)
+        assert same_bits(lgA.view(B, k, -1), lgS), f"keep={keep}"
+        del A, S
+        torch.cuda.empty_cache()
+
+
+def test_stack_eight_in_flight_equal_alone(stack):
+    cfg, w, wd = stack
+    B, k = 8, 8
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500]
+    Lmax = 2304
+    toks = workloads.draft_tokens(cfg, 0, 3, B, k)
+    A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd)
+    lgA = A.verify(dev(toks), k)[0].clone().view(B, k, -1)
+    for b in (0, 3, 7):
+        # sequence b alone: same recipe restricted to b
+        one = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd)
+        # run the batch with every other sequence's tokens changed: b's rows must not move
+        toks2 = workloads.draft_tokens(cfg, 0, 4, B, k)
+        toks2[b] = toks[b]
+        lg2 = one.verify(dev(toks2), k)[0].view(B, k, -1)
+        assert same_bits(lg2[b], lgA[b]), f"sequence {b} depends on its neighbours"
+        del one
+        torch.cuda.empty_cache()
+
+
+def test_stack_long_context(stack):
+    cfg, w, wd = stack
+    B, k, L = 1, 8, 131072
+    Lmax = L + 64
+    toks = workloads.draft_tokens(cfg, 0, 5, B, k)
+    A = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lgA = A.verify(dev(toks), k)[0].clone()
+    S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lgS, _ = sequential(S, toks, B)
+    assert same_bits(lgA.view(B, k, -1), lgS)

@@ -1,0 +1,105 @@
+"""Small-M GEMM: parity with the oracle, row bits independent of M and of row
+position, run-to-run repeatability — at small ragged shapes and at the
+5120 x 17408 gate/up and down projection shapes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import assert_bf16_close, assert_f32_close, dev, host, host_u16, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def xv():
+    from bit_exact_speculative_gb300 import build
+    build.build()
+    from bit_exact_speculative_gb300 import xv as m
+    return m
+
+
+def run(xv, X, W, M=None, f32=False):
+    M = X.shape[0] if M is None else M
+    N, K = W.shape
+    Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.int16, device="cuda")
+    ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K))
+    xv.xv_gemm_small_m(X[:M], W, Y, ws)
+    return Y
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1000), (5, 300, 1000), (64, 300, 1000), (3, 256, 4096), (17, 131, 72),
+                                   (8, 1024, 640)])
+def test_parity_small_shapes(xv, M, N, K):
+    X = synth.normal_bf16(0, synth.tid(f"gx{M}.{N}.{K}"), (M, K))
+    W = synth.normal_bf16(0, synth.tid(f"gw{M}.{N}.{K}"), (N, K), sigma=0.02)
+    ref = oracle.gemm(X, W)
+    Y = run(xv, dev(X), dev(W))
+    assert_bf16_close(host_u16(Y), oracle.round_bf16(ref), what=f"gemm {M}x{N}x{K}")
+    Yf = run(xv, dev(X), dev(W), f32=True)
+    assert_f32_close(host(Yf), ref, rel=1e-3, what="gemm f32 out")
+    assert xv.xv_device_check() == 0
+
+
+@pytest.fixture(scope="module")
+def big(xv):
+    """The gate/up [17408, 5120] and down [5120, 17408] weights, activations N(0,1)."""
+    Wgu = synth.normal_bf16(0, synth.tid("sweep.w_gate_up"), (17408, 5120), sigma=0.02)
+    Wd = synth.normal_bf16(0, synth.tid("sweep.w_down"), (5120, 17408), sigma=0.02)
+    Xgu = synth.normal_bf16(0, synth.tid("sweep.x_gate_up"), (64, 5120))
+    Xd = synth.normal_bf16(0, synth.tid("sweep.x_down"), (64, 17408))
+    return {"gu": (Xgu, Wgu, dev(Xgu), dev(Wgu)), "down": (Xd, Wd, dev(Xd), dev(Wd))}
+
+
+@pytest.mark.parametrize("which", ["gu", "down"])
+def test_row_bits_independent_of_M(xv, big, which):
+    _, _, X, W = big[which]
+    ref = run(xv, X, W, M=16)
+    for M in (1, 2, 4, 8, 9, 16, 64):
+        Y = run(xv, X, W, M=M)
+        m = min(M, 16)
+        assert same_bits(Y[:m], ref[:m]), f"M={M}: rows differ from the M=16 call"
+
+
+@pytest.mark.parametrize("which", ["gu", "down"])
+def test_row_bits_independent_of_position(xv, big, which):
+    _, _, X, W = big[which]
+    perm = torch.tensor([5, 0, 7, 3, 1, 6, 2, 4], device="cuda")
+    Y = run(xv, X[:8], W)
+    Yp = run(xv, X[:8][perm].contiguous(), W)
+    assert same_bits(Yp, Y[perm])
+
+
+@pytest.mark.parametrize("which", ["gu", "down"])
+def test_full_size_parity_sampled(xv, big, which):
+    Xh, Wh, X, W = big[which]
+    M = 16
+    Y = host_u16(run(xv, X, W, M=M))
+    cols = np.sort(np.random.default_rng(0).choice(Wh.shape[0], 96, replace=False))
+    cols = np.unique(np.concatenate([cols, [0, Wh.shape[0] - 1]]))
+    ref = oracle.gemm(Xh[:M], Wh[cols])
+    assert_bf16_close(Y[:, cols], oracle.round_bf16(ref), what=f"{which} sampled")
+
+
+@pytest.mark.parametrize("which", ["gu", "down"])
+def test_hundred_runs_identical(xv, big, which):
+    _, _, X, W = big[which]
+    ref = run(xv, X, W, M=16)
+    N, K = W.shape
+    ws = xv.workspace(xv.xv_gemm_workspace_size(16, N, K))
+    Y = torch.empty_like(ref)
+    for _ in range(100):
+        xv.xv_gemm_small_m(X[:16], W, Y, ws)
+        assert same_bits(Y, ref)
+    assert xv.xv_device_check() == 0
+
+
+def test_lm_head_shape_f32(xv):
+    """The LM head shape (151936 x 5120, fp32 out) on a sample of rows."""
+    N, K = 151936, 5120
+    Wh = synth.normal_bf16(0, synth.tid("lm_head_test"), (N, K), sigma=0.02)
+    Xh = synth.normal_bf16(0, synth.tid("lm_x"), (8, K))
+    Y = host(run(xv, dev(Xh), dev(Wh), f32=True))
+    cols = np.random.default_rng(1).choice(N, 64, replace=False)
+    assert_f32_close(Y[:, cols], oracle.gemm(Xh, Wh[cols]), rel=1e-3, what="lm head")
