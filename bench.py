@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark: exact verify throughput of the 4-layer hybrid stack on GB300.
+
+A step is one full verify round of the hot path over one batch: xv_verify_block
+(embedding, 4 x [RMSNorm, input GEMM, GDN verify or KV append + decode-row
+attention, output GEMM, residual + RMSNorm, gate/up GEMM, SwiGLU, down GEMM,
+residual + RMSNorm], LM head, argmax, acceptance) followed by the commit of
+the accepted positions.  Workload: hidden 5120, 3 GDN layers (32 x 128 x 128
+fp32 state) + 1 gated attention layer (24/4 heads of 256), MLP 17408, vocab
+151936, k = 8 tokens per sequence, batch 1, context 2183, all inputs seeded
+and synthetic.  Metric: verified tokens per second (k * B per step).
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead.
+Multi-GPU (torchrun): each rank runs its own independent sequence (weak
+scaling, no collective on the data path); the job value is the sum of tokens
+over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "exact verify tok/s (k=8, 1 stream) per hybrid block"
+UNIT = "tok/s"
+WORKLOAD = ("4-layer hybrid stack (3 GDN + 1 gated attention), hidden 5120, MLP 17408, vocab 151936; "
+            "verify k=8 draft tokens, batch 1, context 2183")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="xv", choices=["xv", "reference"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--k", type=int, default=8)
+    ap.add_argument("--context", type=int, default=2183)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------------- setup
+
+def make_stack(args, device):
+    import torch
+    from synth import workloads
+    from bit_exact_speculative_gb300.model import HybridStack
+
+    cfg = workloads.STACK
+    w = workloads.weights(cfg, seed=0)
+    wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
+    B, k, L = args.batch, args.k, args.context
+    rounds = 3 * (args.steps + args.warmup) + 8
+    Lmax = L + k * rounds + 64
+    stk = HybridStack(cfg, wd, B, k, Lmax, device=device)
+    for l, kd in enumerate(cfg["kinds"]):
+        if kd == 0:
+            stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, 0, l, B)))
+        else:
+            kc, vc = workloads.kv_cache(cfg, 0, l, B, [L] * B, Lmax)
+            stk.state[f"{l}.kc"].copy_(torch.from_numpy(kc.view(np.int16)))
+            stk.state[f"{l}.vc"].copy_(torch.from_numpy(vc.view(np.int16)))
+    stk.set_context([L] * B)
+    toks = np.stack([workloads.draft_tokens(cfg, 0, r, B, k) for r in range(rounds)])
+    return cfg, w, stk, toks
+
+
+def gemm_shapes(cfg, M):
+    """(N, K) of every GEMM in one verify step, with its output element size."""
+    H, F, V = cfg["hidden"], cfg["mlp"], cfg["vocab"]
+    gin = cfg["gdn_heads"] * (2 * cfg["gdn_dk"] + cfg["gdn_dv"]) + 2 * cfg["gdn_heads"]
+    ain = 2 * cfg["attn_hq"] * cfg["attn_hd"] + 2 * cfg["attn_hkv"] * cfg["attn_hd"]
+    out = []
+    for kd in cfg["kinds"]:
+        if kd == 0:
+            out += [(gin, H, 2), (H, cfg["gdn_heads"] * cfg["gdn_dv"], 2)]
+        else:
+            out += [(ain, H, 2), (H, cfg["attn_hq"] * cfg["attn_hd"], 2)]
+        out += [(2 * F, H, 2), (H, F, 2)]
+    out.append((V, H, 4))
+    return out
+
+
+def traffic_from_profile(kernel_src: str):
+    """ncu DRAM bytes per launch for the GEMM kernel, if the committed capture matches this source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    e = d.get("gemm_small_m")
+    if not e or e.get("source_sha") != h:
+        return None
+    return e.get("dram_bytes_per_step")
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from bit_exact_speculative_gb300 import build
+    from bit_exact_speculative_gb300 import xv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    xv.lib()
+
+    cfg, w_host, stk, toks = make_stack(args, device)
+    B, k = args.batch, args.k
+    tok_dev = torch.from_numpy(toks).to(device)
+    stream = torch.cuda.current_stream()
+    rnd = 0
+
+    def step(i):
+        stk.verify(tok_dev[i], k, logits=False)
+        stk.commit()
+
+    for _ in range(args.warmup):
+        step(rnd)
+        rnd += 1
+    xv.xv_device_check()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- timed region: K steps on device-resident inputs
+    launches0 = xv.xv_launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(rnd)
+            rnd += 1
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    launches = xv.xv_launch_count() - launches0
+    ms = e0.elapsed_time(e1)
+    t = torch.tensor([ms], device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * B * k * args.steps / (ms_max / 1e3)
+    code = xv.xv_device_check()
+
+    # ---- per-kernel durations: the same steps with every launch bracketed by events
+    xv.xv_trace_enable(64 * args.steps)
+    for _ in range(args.steps):
+        step(rnd)
+        rnd += 1
+    torch.cuda.synchronize()
+    recs = xv.xv_trace_read()
+    xv.xv_trace_disable()
+    per_kind = {}
+    for name, tms, nb in recs:
+        d = per_kind.setdefault(name, [0, 0.0, 0])
+        d[0] += 1
+        d[1] += tms
+        d[2] += nb
+    g = per_kind.get("gemm_small_m", [0, 0.0, 0])
+    gemm_ms_per_launch = g[1] / max(g[0], 1)
+    gemm_bytes_per_launch = g[2] / max(g[0], 1)
+    achieved = gemm_bytes_per_launch / (gemm_ms_per_launch / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    gemm_bytes_step = sum(2 * N * K + 2 * B * k * K + B * k * N * o for N, K, o in gemm_shapes(cfg, B * k))
+    traffic_step = traffic_from_profile(os.path.join(ROOT, "bit_exact_speculative_gb300", "csrc", "gemm.cu"))
+    n_gemm = len(gemm_shapes(cfg, B * k))
+
+    # ---- end to end through the public API: pinned host tokens in, results out, every step
+    h_tok = torch.from_numpy(toks[rnd: rnd + args.steps].copy()).pin_memory()
+    d_tok = torch.empty((B, k), dtype=torch.int32, device=device)
+    h_am = torch.empty((B * k,), dtype=torch.int32).pin_memory()
+    h_na = torch.empty((B,), dtype=torch.int32).pin_memory()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        d_tok.copy_(h_tok[i], non_blocking=True)
+        _, am, na = stk.verify(d_tok, k, logits=False)
+        h_am.copy_(am, non_blocking=True)
+        h_na.copy_(na, non_blocking=True)
+        stk.commit()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    t2 = torch.tensor([e2e_s], device=device)
+    if world > 1:
+        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+        barrier()
+    e2e_value = world * B * k * args.steps / float(t2.item())
+
+    out = None
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch_per_gpu": B, "k": k, "context": args.context,
+                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
+            "gpu_launches": int(launches),
+            "roofline": {"bound": "hbm", "kernel": "gemm_small_m", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": (round(traffic_step / n_gemm) if traffic_step else None),
+                         "algorithmic_bytes_per_launch": round(gemm_bytes_per_launch),
+                         "launches_per_step": n_gemm, "ms_per_launch": round(gemm_ms_per_launch, 5)},
+            "step_roofline": {"algorithmic_bytes": gemm_bytes_step,
+                              "achieved_gbs": round(gemm_bytes_step / (ms_max / args.steps / 1e3) / 1e9, 1),
+                              "frac": round(gemm_bytes_step / (ms_max / args.steps / 1e3) / 1e9 / peak, 4)},
+            "kernels": {n: {"launches": v[0], "ms_total": round(v[1], 4),
+                            "share": round(v[1] / max(sum(x[1] for x in per_kind.values()), 1e-9), 4)}
+                        for n, v in sorted(per_kind.items(), key=lambda kv: -kv[1][1])},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(B * k * 4),
+                    "d2h_bytes_per_step": int(B * k * 4 + B * 4)},
+            "clocks": clk.summary(),
+            "device_error_bits": code,
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return out, (cfg, w_host)
+
+
+# ------------------------------------------------------------- CPU side
+
+def oracle_session(args, cfg, w):
+    """The oracle holding sequence 0 of the same workload (weights, caches, states, context)."""
+    import oracle
+    from synth import workloads
+    L = args.context
+    Lmax = L + 4 * (args.steps + args.warmup) + 64
+    oracle.build()
+    st = oracle.Stack(workloads.oracle_cfg(cfg), w, Lmax)
+    for l, kd in enumerate(cfg["kinds"]):
+        if kd == 0:
+            st.S[l][...] = workloads.gdn_state(cfg, 0, l, 1)[0]
+        else:
+            kc, vc = workloads.kv_cache(cfg, 0, l, 1, [L], Lmax)
+            st.kc[l][...], st.vc[l][...] = kc[0], vc[0]
+    st.len = L
+    toks = workloads.draft_tokens(cfg, 0, 0, 1, 4 * (args.steps + args.warmup) + 8)[0]
+    return st, toks
+
+
+def cores_used():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def oracle_sample(args, cfg, w, budget_s=12.0):
+    """The oracle decoding verify positions of the same workload until ~budget_s of CPU time."""
+    st, toks = oracle_session(args, cfg, w)
+    n, t0 = 0, time.perf_counter()
+    while n < args.k and (n == 0 or time.perf_counter() - t0 < budget_s):
+        st.decode(int(toks[n]))
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 4), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+            "sample": f"{n} of the {args.k} verify positions of one sequence (the oracle verifies by decoding "
+                      f"them one at a time), context {args.context}, full-size weights; {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step verifies one position of the workload on the host
+    cores (verify = sequential decode by definition); value = positions per second."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    from synth import workloads
+    cfg = workloads.STACK
+    w = workloads.weights(cfg, seed=0)
+    st, toks = oracle_session(args, cfg, w)
+    i = 0
+    for _ in range(args.warmup):
+        st.decode(int(toks[i]))
+        i += 1
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.decode(int(toks[i]))
+        i += 1
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    cb = {"value": round(value, 4), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+          "sample": f"{args.steps} verify positions of one sequence decoded one at a time, context "
+                    f"{args.context}, full-size weights; {dt:.1f} s"}
+    return {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "batch_per_gpu": 1, "k": args.k, "context": args.context},
+            "cpu_baseline": cb, "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        out = run_reference(args)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    out, (cfg, w) = run_gpu(args)
+    rank, world, _ = dist_env()
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = oracle_sample(args, cfg, w)
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -357,8 +357,12 @@ xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const Att
         attr_done[dev] = true;
     }
     dim3 grid(a.nsplit, a.Hkv, B);
+    trace_pre(s);
     attn_split_kernel<HD><<<grid, nw * 32, smem, s>>>(tmK, tmV, a);
-    return launched("attn_split_kernel");
+    // bound: every sequence at the longest length the launch is sized for
+    const long long bytes = 4ll * B * a.Hkv * a.max_len * HD + 2ll * B * a.R * a.Hq * HD +
+                            4ll * B * a.R * a.Hq * a.nsplit * (HD + 2);
+    return launched("attn_split_kernel", s, K_ATTN_SPLIT, bytes);
 }
 
 }  // namespace
@@ -392,16 +396,19 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
     xv_status st = hd == 256 ? launch_split<256>(tmK, tmV, a, B, s) : launch_split<64>(tmK, tmV, a, B, s);
     if (st) return st;
     CombineArgs c{ctx_len, len_bias, R, Hq, nsplit, max_len, hd, opart, ml, gate, gate_stride, out, out_stride, err};
+    trace_pre(s);
     attn_combine_kernel<<<B * R * Hq, hd / 2, 0, s>>>(c);
-    return launched("attn_combine_kernel");
+    return launched("attn_combine_kernel", s, K_ATTN_COMBINE,
+                    4ll * B * R * Hq * nsplit * (hd + 2) + 2ll * B * R * Hq * hd * (gate ? 2 : 1));
 }
 
 xv_status kv_append_launch(const uint16_t* src, long long src_stride, const int32_t* ctx_len, int pos_bias, int R, int B,
                            int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "kv_append: device error word unavailable");
+    trace_pre(s);
     kv_append_kernel<<<B * R, 128, 0, s>>>(src, src_stride, ctx_len, pos_bias, R, Hkv, hd, Lmax, kc, vc, err);
-    return launched("kv_append_kernel");
+    return launched("kv_append_kernel", s, K_KV_APPEND, 8ll * B * R * Hkv * hd);
 }
 
 }  // namespace xv

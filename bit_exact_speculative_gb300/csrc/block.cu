@@ -46,7 +46,7 @@ xv_status check_cfg(const xv_block_config* c, Dims* d) {
     if (has_gdn) {
         if ((d->dk != 64 && d->dk != 128) || d->dv < 16 || d->dv % 16 || d->gh < 1)
             return fail(XV_ERR_UNSUPPORTED, "block: GDN needs dk in {64,128}, dv a multiple of 16");
-        if (d->gin % 8 || d->ginner % 8) return fail(XV_ERR_UNSUPPORTED, "block: GDN widths must be multiples of 8");
+        if (d->ginner % 8) return fail(XV_ERR_UNSUPPORTED, "block: GDN heads*dv must be a multiple of 8");
     } else {
         d->gin = d->ginner = 0;
     }
@@ -131,8 +131,6 @@ static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv
         if (cfg->layer_kind[l] == 0) {
             if (!ls.gdn_state || !ls.gdn_hist[0] || !ls.gdn_hist[1] || !ls.gdn_gates[0] || !ls.gdn_gates[1])
                 return fail(XV_ERR_ARG, "block: GDN layer %d state incomplete", l);
-            if (!aligned16(ls.gdn_hist[0]) || !aligned16(ls.gdn_hist[1]))
-                return fail(XV_ERR_UNSUPPORTED, "block: GDN history must be 16-byte aligned");
         } else {
             if (!ls.k_cache || !ls.v_cache) return fail(XV_ERR_ARG, "block: attention layer %d cache missing", l);
             if (!aligned16(ls.k_cache) || !aligned16(ls.v_cache))

@@ -216,6 +216,7 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
               qk_l2norm ? 1 : 0, err};
     const int max_steps = max_commit + k;
     dim3 grid(dv / ROWS_PER_CTA, H, B);
+    trace_pre(s);
     if (dk == 128) {
         const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
         gdn_kernel<128><<<grid, THREADS, sm, s>>>(a);
@@ -223,7 +224,13 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
         const size_t sm = sizeof(StepSmem<64>) * (max_steps > 0 ? max_steps : 1);
         gdn_kernel<64><<<grid, THREADS, sm, s>>>(a);
     }
-    return launched("gdn_kernel");
+    // algorithmic bytes with every sequence replaying max_commit steps: the state
+    // read (and written back after a replay), the step inputs, the outputs
+    const long long state_bytes = 4ll * B * H * dv * dk;
+    const long long per_step = 2ll * B * H * (2 * dk + dv + 2);
+    const long long outs = 2ll * B * H * dv * (k + (emit_replay ? max_commit : 0));
+    const long long bytes = state_bytes * (max_commit > 0 ? 2 : 1) + per_step * (max_commit + k) + outs;
+    return launched("gdn_kernel", s, K_GDN, bytes);
 }
 
 }  // namespace xv

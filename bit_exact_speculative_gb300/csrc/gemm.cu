@@ -196,10 +196,17 @@ int gemm_splits(int N, int K) {
     return s;
 }
 
+// Workspace layout: [tile counters, COUNTER_BYTES at offset 0][segment partials].
+// The counters sit at the same place for every shape, so one zeroed workspace
+// can serve GEMMs of different shapes in turn (each call leaves them zero).
+// A split GEMM has at most SM_COUNT_TARGET * RESIDENT_PER_SM / 2 tiles.
+constexpr size_t COUNTER_BYTES = 1024;
+static_assert(COUNTER_BYTES / sizeof(unsigned) >= SM_COUNT_TARGET * RESIDENT_PER_SM / 2, "counter region too small");
+
 size_t gemm_workspace_size(int M, int N, int K) {
     const int S = gemm_splits(N, K);
     if (S == 1) return 0;
-    return round256(static_cast<size_t>(S) * M * N * sizeof(float)) + round256(num_tiles(N) * sizeof(unsigned));
+    return COUNTER_BYTES + round256(static_cast<size_t>(S) * M * N * sizeof(float));
 }
 
 xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, int ldy, bool f32out, int M, int N, int K,
@@ -228,8 +235,8 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     float* part = nullptr;
     unsigned* cnt = nullptr;
     if (S > 1) {
-        part = static_cast<float*>(ws);
-        cnt = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + round256(static_cast<size_t>(S) * M * N * 4));
+        cnt = static_cast<unsigned*>(ws);
+        part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + COUNTER_BYTES);
     }
     static bool attr_set[2] = {false, false};
     auto kern = f32out ? gemm_small_m_kernel<true> : gemm_small_m_kernel<false>;
@@ -240,8 +247,10 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
         attr_set[f32out] = true;
     }
     dim3 grid(tiles, S);
+    trace_pre(s);
     kern<<<grid, 128, SMEM_BYTES, s>>>(tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err);
-    return launched("gemm_small_m_kernel");
+    const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
+    return launched("gemm_small_m_kernel", s, K_GEMM, bytes);
 }
 
 }  // namespace xv

@@ -167,54 +167,63 @@ __global__ void zero_i32_kernel(int32_t* p, int n) {
 xv_status embed_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, uint16_t* x, cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "embed: device error word unavailable");
+    trace_pre(s);
     embed_kernel<<<M, 128, 0, s>>>(tokens, E, V, H, x, err);
-    return launched("embed_kernel");
+    return launched("embed_kernel", s, K_EMBED, 4ll * M * H + 4ll * M);
 }
 
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s) {
+    trace_pre(s);
     rmsnorm_kernel<<<M, NORM_THREADS, 0, s>>>(const_cast<uint16_t*>(x), nullptr, w, H, eps, y);
-    return launched("rmsnorm_kernel");
+    return launched("rmsnorm_kernel", s, K_RMSNORM, 4ll * M * H + 2ll * H);
 }
 
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps, uint16_t* xn,
                                   cudaStream_t s) {
+    trace_pre(s);
     rmsnorm_kernel<<<M, NORM_THREADS, 0, s>>>(x, y, w, H, eps, xn);
-    return launched("rmsnorm_kernel(residual)");
+    return launched("rmsnorm_kernel(residual)", s, K_RMSNORM, 8ll * M * H + 2ll * H);
 }
 
 xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s) {
     dim3 grid(ceil_div(F, 256 * 4), M);
+    trace_pre(s);
     swiglu_kernel<<<grid, 256, 0, s>>>(gu, F, act);
-    return launched("swiglu_kernel");
+    return launched("swiglu_kernel", s, K_SWIGLU, 6ll * M * F);
 }
 
 xv_status gdn_gates_launch(const uint16_t* proj, long long proj_stride, int b_col, int M, int H, uint16_t* gates,
                            cudaStream_t s) {
+    trace_pre(s);
     gdn_gates_kernel<<<M, 64, 0, s>>>(proj, proj_stride, b_col, H, gates);
-    return launched("gdn_gates_kernel");
+    return launched("gdn_gates_kernel", s, K_GATES, 8ll * M * H);
 }
 
 xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, cudaStream_t s) {
+    trace_pre(s);
     argmax_kernel<<<M, 1024, 0, s>>>(logits, V, idx);
-    return launched("argmax_kernel");
+    return launched("argmax_kernel", s, K_ARGMAX, 4ll * M * V + 4ll * M);
 }
 
 xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s) {
+    trace_pre(s);
     accept_kernel<<<ceil_div(B, 128), 128, 0, s>>>(tokens, pred, B, k, n_accept);
-    return launched("accept_kernel");
+    return launched("accept_kernel", s, K_ACCEPT, 8ll * B * k + 4ll * B);
 }
 
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,
                         cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "commit: device error word unavailable");
+    trace_pre(s);
     commit_kernel<<<ceil_div(B, 128), 128, 0, s>>>(keep, keep_bias, B, k, ctx_len, n_commit, err);
-    return launched("commit_kernel");
+    return launched("commit_kernel", s, K_COMMIT, 16ll * B);
 }
 
 xv_status zero_i32_launch(int32_t* p, int n, cudaStream_t s) {
+    trace_pre(s);
     zero_i32_kernel<<<ceil_div(n, 256), 256, 0, s>>>(p, n);
-    return launched("zero_i32_kernel");
+    return launched("zero_i32_kernel", s, K_ZERO, 4ll * n);
 }
 
 }  // namespace xv

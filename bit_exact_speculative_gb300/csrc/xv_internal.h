@@ -13,8 +13,13 @@ namespace xv {
 xv_status fail(xv_status code, const char* fmt, ...);
 // Checks a CUDA runtime result; on failure records it and returns XV_ERR_CUDA.
 xv_status cuda_check(cudaError_t e, const char* what);
-// Checks the launch just made on the calling thread and counts it.
-xv_status launched(const char* what);
+// Kernel kinds of the launch trace.
+enum Kind : int { K_GEMM = 0, K_GDN, K_ATTN_SPLIT, K_ATTN_COMBINE, K_KV_APPEND, K_EMBED, K_RMSNORM, K_SWIGLU,
+                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_COUNT };
+// Call right before a launch on stream s (records the opening trace event when tracing).
+void trace_pre(cudaStream_t s);
+// Checks the launch just made on the calling thread, counts it and closes its trace record.
+xv_status launched(const char* what, cudaStream_t s, int kind, long long bytes);
 // Device address of the library's device-side error word for the current device.
 unsigned* device_error_word();
 

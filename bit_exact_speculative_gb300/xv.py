@@ -64,6 +64,11 @@ _SIGS = {
     "xv_last_error": ([], ctypes.c_char_p),
     "xv_device_check": ([vp, ctypes.POINTER(ctypes.c_uint)], c_int),
     "xv_launch_count": ([], ctypes.c_ulonglong),
+    "xv_trace_enable": ([c_int], c_int),
+    "xv_trace_disable": ([], c_int),
+    "xv_trace_count": ([], c_int),
+    "xv_trace_read": ([vp, vp, vp, c_int], c_int),
+    "xv_trace_kind_name": ([c_int], ctypes.c_char_p),
     "xv_gemm_workspace_size": ([c_int, c_int, c_int], c_sz),
     "xv_gemm_small_m": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
     "xv_gemm_small_m_f32out": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
@@ -139,6 +144,25 @@ def xv_device_check(stream=None) -> int:
 
 def xv_launch_count() -> int:
     return int(lib().xv_launch_count())
+
+
+def xv_trace_enable(capacity: int):
+    _check(lib().xv_trace_enable(capacity))
+
+
+def xv_trace_disable():
+    _check(lib().xv_trace_disable())
+
+
+def xv_trace_read():
+    """Returns a list of (kind name, milliseconds, algorithmic bytes) for every traced launch."""
+    import numpy as np
+    n = int(lib().xv_trace_count())
+    ms = np.zeros(n, np.float32)
+    kind = np.zeros(n, np.int32)
+    nb = np.zeros(n, np.int64)
+    _check(lib().xv_trace_read(ms.ctypes.data, kind.ctypes.data, nb.ctypes.data, n))
+    return [(lib().xv_trace_kind_name(int(k)).decode(), float(t), int(b)) for k, t, b in zip(kind, ms, nb)]
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

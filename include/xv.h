@@ -75,6 +75,22 @@ xv_status xv_device_check(xv_stream s, unsigned* code);
 /* Number of kernels this library has launched in this process (host counter). */
 unsigned long long xv_launch_count(void);
 
+/* Launch trace, a profiling hook outside the verify method.  While enabled,
+ * every kernel the library launches is bracketed by two CUDA events recorded
+ * on its stream, and the launch's kind and algorithmic bytes (inputs read
+ * plus outputs written, as the op defines them; 0 where the host cannot know
+ * them) are noted.  xv_trace_enable creates 2*capacity events on the current
+ * device the first time (or when capacity grows) and restarts the record;
+ * launches beyond capacity are not traced.  xv_trace_read synchronises the
+ * recorded events and fills, for the first n launches, the elapsed
+ * milliseconds, the kind (see xv_trace_kind_name) and the bytes (all host
+ * arrays, any may be NULL).  Not thread-safe; for benchmarks. */
+xv_status xv_trace_enable(int capacity);
+xv_status xv_trace_disable(void);
+int xv_trace_count(void);
+xv_status xv_trace_read(float* ms, int* kind, long long* bytes, int n);
+const char* xv_trace_kind_name(int kind);
+
 /* ------------------------------------------------------------------ GEMM
  * Small-M bf16 GEMM  Y[M,N] = X[M,K] . W[N,K]^T  with fp32 accumulation.
  * [post] and [card] summary: at small batch the projection GEMMs of decode

@@ -4,7 +4,14 @@ Tolerances (stated once, used everywhere):
   - bf16 outputs vs the oracle: max|err| <= 2e-2 * RMS(reference);
   - fp32 GDN state vs the oracle (same bf16 inputs on both sides):
     max_i |d_i| / max(|ref_i|, RMS(ref)) <= 1e-4;
-  - fp32 logits vs the oracle: max|err| <= 2e-2 * RMS(reference);
+  - fp32 logits of the whole block vs the oracle's sequential decode:
+    RMS(err) <= 2e-2 * RMS(ref) and max|err| <= 1e-1 * RMS(ref), and the argmax
+    ids agree wherever the oracle's top-1/top-2 margin exceeds 0.25.  A block
+    output has passed through ~8 bf16 storage points per layer; each GEMM
+    output that lands within the fp32 accumulation error of a bf16 rounding
+    boundary rounds the other way on one side (about 0.3% of elements,
+    measured), and those 1-ulp differences propagate.  The 0.25 margin is the
+    recipe card's own figure for where divergent tokens cluster;
   - GPU vs GPU comparisons: 0 differing bits.
 """
 import numpy as np
@@ -56,6 +63,32 @@ def assert_f32_close(got, ref, rel=BF16_REL, what=""):
     err = float(np.max(np.abs(g - r)))
     bound = rel * rms(r)
     assert err <= bound, f"{what}: max|err| {err:.3e} > {rel} * RMS = {bound:.3e}"
+
+
+BLOCK_RMS_REL = 2e-2
+BLOCK_MAX_REL = 1e-1
+ARGMAX_MARGIN = 0.25
+
+
+def assert_block_close(got, ref, what=""):
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    e = np.abs(g - r)
+    scale = rms(r)
+    assert rms(e) <= BLOCK_RMS_REL * scale, f"{what}: RMS err {rms(e):.3e} > {BLOCK_RMS_REL} * RMS {scale:.3e}"
+    assert e.max() <= BLOCK_MAX_REL * scale, f"{what}: max err {e.max():.3e} > {BLOCK_MAX_REL} * RMS {scale:.3e}"
+
+
+def assert_argmax_agrees(ids, ref_logits, margin=ARGMAX_MARGIN):
+    """ids [n]; ref_logits [n, V].  Returns how many rows had a decisive margin."""
+    checked = 0
+    for i, ref in zip(ids, ref_logits):
+        top2 = np.partition(ref, -2)[-2:]
+        if top2[1] - top2[0] > margin:
+            assert int(i) == int(np.argmax(ref)), f"argmax {int(i)} != oracle {int(np.argmax(ref))} (margin {top2[1] - top2[0]:.3f})"
+            checked += 1
+    return checked
 
 
 def assert_state_close(got, ref, rel=STATE_REL, what="state"):

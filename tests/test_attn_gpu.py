@@ -28,6 +28,16 @@ def make(seed, B, R, Hq, Hkv, hd, Lmax, name="a"):
     return q, kc, vc
 
 
+def exact_rows(q, kc, vc, len0, scale, R, Hq, Hkv, hd):
+    """The oracle's fp64 decode rows (before the output's bf16 storage rounding): [R, Hq, hd]."""
+    out = np.empty((R, Hq, hd))
+    for r in range(R):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            out[r, h] = oracle.attn_row(q[r, h * hd:(h + 1) * hd], kc[g], vc[g], len0 + r, scale)
+    return out
+
+
 def attn(xv, q, kc, vc, ctx, R, B, Hq, Hkv, hd, Lmax, max_ctx, gate=None):
     out = torch.empty((B * R, Hq * hd), dtype=torch.int16, device="cuda")
     ws = xv.workspace(xv.xv_attn_workspace_size(B, R, Hq, hd, max_ctx))
@@ -45,7 +55,7 @@ def test_parity_with_oracle(xv, hd, Hq, Hkv, R, lens):
     ctx = np.array(lens, dtype=np.int32)
     out = host_u16(attn(xv, dev(q), dev(kc), dev(vc), dev(ctx), R, B, Hq, Hkv, hd, Lmax, max(lens) + R - 1))
     for b in range(B):
-        ref = oracle.attn_rows(q[b * R:(b + 1) * R].reshape(R, Hq, hd), kc[b], vc[b], lens[b], hd ** -0.5)
+        ref = exact_rows(q[b * R:(b + 1) * R], kc[b], vc[b], lens[b], hd ** -0.5, R, Hq, Hkv, hd)
         assert_bf16_close(out[b * R:(b + 1) * R].reshape(R, Hq, hd), ref, what=f"attn b{b} len{lens[b]}")
     assert xv.xv_device_check() == 0
 
@@ -57,9 +67,11 @@ def test_gated_output_parity(xv):
     g = synth.normal_bf16(2, synth.tid("gate.g"), (B * R, Hq * hd))
     out = host_u16(attn(xv, dev(q), dev(kc), dev(vc), dev(np.array([L], np.int32)), R, B, Hq, Hkv, hd, Lmax, L + R,
                         gate=dev(g)))
+    # the output crosses two bf16 storage points (attention output, gated product): the
+    # per-point bound 2e-2 * RMS applies once per point
     ref = oracle.attn_rows(q.reshape(R, Hq, hd), kc[0], vc[0], L, hd ** -0.5).reshape(R, -1)
-    gated = oracle.round_bf16(f64(ref) / (1.0 + np.exp(-f64(g))))
-    assert_bf16_close(out, gated, what="gated")
+    gated = f64(ref) / (1.0 + np.exp(-f64(g)))
+    assert_bf16_close(out, gated, rel=2 * 2e-2, what="gated")
 
 
 @pytest.mark.parametrize("L", [640, 2183, 131072])
