@@ -73,6 +73,7 @@ _SIGS = {
     "xv_gemm_small_m": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
     "xv_gemm_small_m_f32out": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
     "xv_gemm_splits": ([c_int, c_int], c_int),
+    "xv_gemm_small_m_noalloc": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp], c_int),
     "xv_gdn_decode_step": ([vp, ctypes.POINTER(GdnSteps), vp, c_ll, c_int, c_int, c_int, c_int, c_int, vp], c_int),
     "xv_gdn_verify": ([vp, ctypes.POINTER(GdnSteps), vp, c_int, ctypes.POINTER(GdnSteps), c_int, vp, c_ll,
                        c_int, c_int, c_int, c_int, c_int, vp], c_int),
@@ -186,6 +187,14 @@ def xv_gemm_small_m(X, W, Y, ws, stream=None):
     fn = lib().xv_gemm_small_m_f32out if Y.dtype == torch.float32 else lib().xv_gemm_small_m
     _check(fn(_ptr(X), _row_stride(X), _ptr(W), _ptr(Y), _row_stride(Y), M, N, K, _ptr(ws),
               0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+    return Y
+
+
+def xv_gemm_small_m_noalloc(X, W, Y, stream=None):
+    """Same GEMM with the library's own fixed scratch (no workspace argument)."""
+    M, K = X.shape[0], X.shape[1]
+    _check(lib().xv_gemm_small_m_noalloc(_ptr(X), _row_stride(X), _ptr(W), _ptr(Y), _row_stride(Y), M, W.shape[0], K,
+                                         _stream(stream)))
     return Y
 
 

@@ -117,6 +117,24 @@ xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, 
 /* Number of K-segments the GEMM uses for (N, K) (a pure function of N and K). */
 int xv_gemm_splits(int N, int K);
 
+/* The same GEMM (bf16 out) for callers that cannot allocate device memory or
+ * pass a workspace: code running under another framework's memory pool,
+ * plugins inside a host process that owns every device allocation, loops
+ * where an allocation is not allowed.  The paper has no counterpart; this is
+ * a convenience of this library.  Its scratch (split-K partial sums and tile
+ * counters) is a fixed array of XV_GEMM_NOALLOC_SCRATCH_BYTES that every GPU
+ * loading the library holds until the process exits.  The first call on a
+ * device looks up that array's device address (and clears its counters), so
+ * make the first call on each device before any stream capture.  Shapes whose
+ * scratch need (xv_gemm_workspace_size) exceeds the array are rejected with
+ * XV_ERR_UNSUPPORTED; with this size every shape with M <= XV_GEMM_M_MAX fits.
+ * All calls share the array: calls that overlap on the GPU race, so callers
+ * serialise them (one stream, or events).  Allocates nothing.  Arguments and
+ * bits of Y are as for xv_gemm_small_m. */
+#define XV_GEMM_NOALLOC_SCRATCH_BYTES (10u * 1024u * 1024u)
+xv_status xv_gemm_small_m_noalloc(const uint16_t* X, int ldx, const uint16_t* W, uint16_t* Y, int ldy,
+                                  int M, int N, int K, xv_stream s);
+
 /* ------------------------------------------------------------------- GDN
  * Gated delta rule, per sequence b and head h, state S [dv][dk] in fp32:
  *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T ,   o_t = S_t q_t
