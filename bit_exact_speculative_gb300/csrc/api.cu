@@ -14,6 +14,7 @@ namespace xv {
 namespace {
 thread_local char g_msg[512] = "";
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<bool> g_overlap{true};
 
 // One error word per device; kernels OR error bits into it.
 __device__ unsigned g_dev_err;
@@ -27,6 +28,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 }  // namespace
+
+bool overlap_enabled() { return g_overlap.load(std::memory_order_relaxed); }
 
 xv_status fail(xv_status code, const char* fmt, ...) {
     va_list ap;
@@ -118,6 +121,11 @@ int xv_abi_version(void) { return XV_ABI_VERSION; }
 const char* xv_last_error(void) { return g_msg; }
 
 unsigned long long xv_launch_count(void) { return g_launches.load(); }
+
+xv_status xv_set_overlap(int enable) {
+    g_overlap.store(enable != 0);
+    return XV_OK;
+}
 
 xv_status xv_trace_enable(int capacity) {
     if (capacity < 1) return fail(XV_ERR_ARG, "trace: capacity must be >= 1");

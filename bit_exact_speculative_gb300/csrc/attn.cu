@@ -59,6 +59,8 @@ struct AttnArgs {
 template <int HD>
 __global__ void __launch_bounds__(128, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs A) {
+    griddep_launch();
+    griddep_wait();
     using S = AttnShape<HD>;
     constexpr int CB = S::CB, STAGES = S::STAGES, TILE_BYTES = S::TILE_BYTES;
     extern __shared__ uint8_t smem_raw[];
@@ -283,6 +285,8 @@ struct CombineArgs {
 
 // One CTA per (row, q head); thread t owns output elements 2t and 2t+1.
 __global__ void attn_combine_kernel(CombineArgs C) {
+    griddep_launch();
+    griddep_wait();
     const int hq = blockIdx.x % C.Hq;
     const long long br = blockIdx.x / C.Hq;
     const int b = static_cast<int>(br / C.R), r = static_cast<int>(br % C.R);
@@ -319,6 +323,8 @@ __global__ void attn_combine_kernel(CombineArgs C) {
 __global__ void kv_append_kernel(const uint16_t* __restrict__ src, long long src_stride, const int32_t* __restrict__ ctx_len,
                                  int pos_bias, int R, int Hkv, int hd, int Lmax, uint16_t* __restrict__ kc,
                                  uint16_t* __restrict__ vc, unsigned* err) {
+    griddep_launch();
+    griddep_wait();
     const int row = blockIdx.x, b = row / R, r = row % R;
     const int pos = ctx_len[b] + pos_bias + r;
     if (pos < 0 || pos >= Lmax) {
@@ -358,7 +364,7 @@ xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const Att
     }
     dim3 grid(a.nsplit, a.Hkv, B);
     trace_pre(s);
-    attn_split_kernel<HD><<<grid, nw * 32, smem, s>>>(tmK, tmV, a);
+    launch_k(attn_split_kernel<HD>, dim3(grid), dim3(nw * 32), smem, s, tmK, tmV, a);
     // bound: every sequence at the longest length the launch is sized for
     const long long bytes = 4ll * B * a.Hkv * a.max_len * HD + 2ll * B * a.R * a.Hq * HD +
                             4ll * B * a.R * a.Hq * a.nsplit * (HD + 2);
@@ -397,7 +403,7 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
     if (st) return st;
     CombineArgs c{ctx_len, len_bias, R, Hq, nsplit, max_len, hd, opart, ml, gate, gate_stride, out, out_stride, err};
     trace_pre(s);
-    attn_combine_kernel<<<B * R * Hq, hd / 2, 0, s>>>(c);
+    launch_k(attn_combine_kernel, dim3(B * R * Hq), dim3(hd / 2), 0, s, c);
     return launched("attn_combine_kernel", s, K_ATTN_COMBINE,
                     4ll * B * R * Hq * nsplit * (hd + 2) + 2ll * B * R * Hq * hd * (gate ? 2 : 1));
 }
@@ -407,7 +413,7 @@ xv_status kv_append_launch(const uint16_t* src, long long src_stride, const int3
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "kv_append: device error word unavailable");
     trace_pre(s);
-    kv_append_kernel<<<B * R, 128, 0, s>>>(src, src_stride, ctx_len, pos_bias, R, Hkv, hd, Lmax, kc, vc, err);
+    launch_k(kv_append_kernel, dim3(B * R), dim3(128), 0, s, src, src_stride, ctx_len, pos_bias, R, Hkv, hd, Lmax, kc, vc, err);
     return launched("kv_append_kernel", s, K_KV_APPEND, 8ll * B * R * Hkv * hd);
 }
 

@@ -65,6 +65,7 @@ inline size_t r256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct Carve {
     uint16_t *x, *xn, *proj, *obuf, *y, *gu, *act;
     float* logits;
+    void* argmax_ws;
     void* gemm_ws;
     size_t gemm_ws_bytes;
     void* attn_ws;
@@ -86,6 +87,7 @@ Carve carve(const Dims& d, int B, int kmax, int Lmax, uint8_t* base) {
     c.gu = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * 2 * d.F * 2));
     c.act = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.F * 2));
     c.logits = reinterpret_cast<float*>(take(static_cast<size_t>(M) * d.V * 4));
+    c.argmax_ws = take(argmax_workspace_size(M, d.V));
     size_t g = 0;
     auto gm = [&](int N, int K) { size_t s = gemm_workspace_size(M, N, K); if (s > g) g = s; };
     if (d.gin) { gm(d.gin, d.H); gm(d.H, d.ginner); }
@@ -206,7 +208,7 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
         XV_TRY(residual_rmsnorm_launch(c.x, c.y, next_norm, M, d.H, eps, c.xn, s));
     }
     XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-    XV_TRY(argmax_launch(lg, M, d.V, argmax, s));
+    XV_TRY(argmax_launch(lg, M, d.V, argmax, c.argmax_ws, s));
     XV_TRY(accept_launch(tokens, argmax, B, k, n_accept, s));
 #undef XV_TRY
     st->last_k = k;

@@ -153,6 +153,8 @@ __device__ __forceinline__ float gdn_step(float (&s)[DK / 8], const StepSmem<DK>
 
 template <int DK>
 __global__ void __launch_bounds__(THREADS) gdn_kernel(GdnArgs A) {
+    griddep_launch();
+    griddep_wait();
     constexpr int EPL = DK / 8;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw);
@@ -219,10 +221,10 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     trace_pre(s);
     if (dk == 128) {
         const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
-        gdn_kernel<128><<<grid, THREADS, sm, s>>>(a);
+        launch_k(gdn_kernel<128>, dim3(grid), dim3(THREADS), sm, s, a);
     } else {
         const size_t sm = sizeof(StepSmem<64>) * (max_steps > 0 ? max_steps : 1);
-        gdn_kernel<64><<<grid, THREADS, sm, s>>>(a);
+        launch_k(gdn_kernel<64>, dim3(grid), dim3(THREADS), sm, s, a);
     }
     // algorithmic bytes with every sequence replaying max_commit steps: the state
     // read (and written back after a replay), the step inputs, the outputs

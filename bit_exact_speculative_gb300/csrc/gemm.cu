@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     const int kb1 = static_cast<int>(static_cast<long long>(seg + 1) * nkb / S);
     const int nk = kb1 - kb0;
 
+    griddep_launch();
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
@@ -88,9 +89,18 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
 
     bool ok = true;
     if (warp == 0 && lane == 0) {
-        // ---- producer: TMA into the ring
-        int issued = 0;
-        for (int i = 0; i < nk; ++i) {
+        // ---- producer: TMA into the ring.  The weights of the first stages are requested
+        // before waiting for the previous kernel (they do not depend on it); the token rows
+        // only after.
+        const int pre = nk < STAGES ? nk : STAGES;
+        for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(full(i), STAGE_BYTES);
+            tma_load_2d(sA + i * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(i));
+        }
+        griddep_wait();
+        for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * B_BYTES, &tmX, (kb0 + i) * GEMM_BK, 0, full(i));
+        int issued = pre;
+        for (int i = pre; i < nk; ++i) {
             const int st = i % STAGES;
             const uint32_t ph = (i / STAGES) & 1u;
             if (i >= STAGES && !mbar_wait(empty(st), ph ^ 1u, err)) { ok = false; break; }
@@ -103,7 +113,10 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
             for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
                 mbar_wait(full(j % STAGES), (j / STAGES) & 1u, err);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else {
+        griddep_wait();   // before any read or write of activations, partials or counters
+    }
+    if (warp == 1 && lane == 0) {
         // ---- MMA issuer: 4 MMAs of K = 16 per stage, accumulate in TMEM
         for (int i = 0; i < nk; ++i) {
             const int st = i % STAGES;
@@ -158,16 +171,26 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
         if (s_last) {
             __threadfence();
             if (live) {
+                // r = p_0 + p_1 + ... + p_{S-1} in segment order (this CTA's own partial is read
+                // back too, so every load is unconditional).  16 rows per batch: each segment's
+                // 16 loads are independent and in flight together.
+                for (int mc = 0; mc < M; mc += 16) {
+                    float r[16];
+                    for (int s2 = 0; s2 < S; ++s2) {
+                        const float* ps = part + (static_cast<size_t>(s2) * M + mc) * N + n;
+                        float v[16];
 #pragma unroll
-                for (int m = 0; m < GEMM_TOK; ++m) {
-                    if (m < M) {
-                        float r = 0.f;
-                        for (int s2 = 0; s2 < S; ++s2) {
-                            const float v = (s2 == seg) ? acc[m] : __ldcg(&part[(static_cast<size_t>(s2) * M + m) * N + n]);
-                            r = (s2 == 0) ? v : __fadd_rn(r, v);
+                        for (int j = 0; j < 16; ++j) v[j] = (mc + j < M) ? __ldcg(ps + static_cast<size_t>(j) * N) : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) r[j] = (s2 == 0) ? v[j] : __fadd_rn(r[j], v[j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (mc + j < M) {
+                            const size_t o = static_cast<size_t>(mc + j) * ldy + n;
+                            if (F32OUT) static_cast<float*>(Y)[o] = r[j];
+                            else static_cast<uint16_t*>(Y)[o] = f32_to_bf16(r[j]);
                         }
-                        if (F32OUT) static_cast<float*>(Y)[static_cast<size_t>(m) * ldy + n] = r;
-                        else static_cast<uint16_t*>(Y)[static_cast<size_t>(m) * ldy + n] = f32_to_bf16(r);
                     }
                 }
             }
@@ -248,7 +271,7 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     }
     dim3 grid(tiles, S);
     trace_pre(s);
-    kern<<<grid, 128, SMEM_BYTES, s>>>(tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err);
+    launch_k(kern, grid, dim3(128), SMEM_BYTES, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err);
     const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
     return launched("gemm_small_m_kernel", s, K_GEMM, bytes);
 }

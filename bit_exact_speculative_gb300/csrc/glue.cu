@@ -14,7 +14,6 @@
 namespace xv {
 
 namespace {
-constexpr int NORM_THREADS = 256;
 
 // Sum of v over the block in a fixed tree: xor-shuffle inside each warp, then
 // warp partials added in warp order by warp 0.
@@ -38,6 +37,8 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 
 __global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ E, int V, int H,
                              uint16_t* __restrict__ x, unsigned* err) {
+    griddep_launch();
+    griddep_wait();
     const int m = blockIdx.x;
     int t = tokens[m];
     if (t < 0 || t >= V) {
@@ -50,45 +51,96 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint16_t*
 }
 
 // y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ); with y_res != null first x <- bf16(x + y_res).
-__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(uint16_t* __restrict__ x, const uint16_t* __restrict__ y_res,
-                                                               const uint16_t* __restrict__ w, int H, float eps,
-                                                               uint16_t* __restrict__ out) {
+// One CTA per row; thread t owns the 8-element chunks t, t + blockDim, ... (at most NORM_MAXC),
+// so the per-thread sum order and the tree below are fixed by H alone.
+constexpr int NORM_MAXC = 4;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = static_cast<uint32_t>(f32_to_bf16(f[2 * i])) | (static_cast<uint32_t>(f32_to_bf16(f[2 * i + 1])) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x, const uint16_t* __restrict__ y_res,
+                                                       const uint16_t* __restrict__ w, int H, float eps,
+                                                       uint16_t* __restrict__ out) {
+    griddep_launch();
+    griddep_wait();
     __shared__ float red[33];
     const long long row = blockIdx.x;
-    uint16_t* xr = x + row * H;
+    const int nch = H / 8;
+    uint4* xr = reinterpret_cast<uint4*>(x + row * H);
+    const uint4* yr = y_res ? reinterpret_cast<const uint4*>(y_res + row * H) : nullptr;
+    float v[NORM_MAXC][8];
     float ss = 0.f;
     bool first = true;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        float v = bf16_to_f32(xr[i]);
-        if (y_res) {
-            v = bf16_to_f32(f32_to_bf16(__fadd_rn(v, bf16_to_f32(y_res[row * H + i]))));
-            xr[i] = f32_to_bf16(v);
+#pragma unroll
+    for (int j = 0; j < NORM_MAXC; ++j) {
+        const int c = threadIdx.x + j * blockDim.x;
+        if (c < nch) {
+            unpack8(xr[c], v[j]);
+            if (yr) {
+                float t[8];
+                unpack8(yr[c], t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[j][e] = bf16_to_f32(f32_to_bf16(__fadd_rn(v[j][e], t[e])));
+                xr[c] = pack8(v[j]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                ss = first ? __fmul_rn(v[j][e], v[j][e]) : __fmaf_rn(v[j][e], v[j][e], ss);
+                first = false;
+            }
         }
-        ss = first ? __fmul_rn(v, v) : __fmaf_rn(v, v, ss);
-        first = false;
     }
     ss = block_sum_fixed(ss, red);
     const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), eps)));
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        const float v = bf16_to_f32(xr[i]);
-        out[row * H + i] = f32_to_bf16(__fmul_rn(__fmul_rn(v, inv), __fadd_rn(1.f, bf16_to_f32(w[i]))));
+    const uint4* wr = reinterpret_cast<const uint4*>(w);
+    uint4* orow = reinterpret_cast<uint4*>(out + row * H);
+#pragma unroll
+    for (int j = 0; j < NORM_MAXC; ++j) {
+        const int c = threadIdx.x + j * blockDim.x;
+        if (c < nch) {
+            float wf[8], o[8];
+            unpack8(wr[c], wf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(v[j][e], inv), __fadd_rn(1.f, wf[e]));
+            orow[c] = pack8(o);
+        }
     }
 }
 
 __device__ __forceinline__ float sigmoid_f(float x) { return __frcp_rn(__fadd_rn(1.f, expf(-x))); }
 
+// act = bf16(silu(g) * u), 8 elements per thread
 __global__ void swiglu_kernel(const uint16_t* __restrict__ gu, int F, uint16_t* __restrict__ act) {
+    griddep_launch();
+    griddep_wait();
     const long long row = blockIdx.y;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < F; i += gridDim.x * blockDim.x) {
-        const float g = bf16_to_f32(gu[row * 2 * F + i]);
-        const float u = bf16_to_f32(gu[row * 2 * F + F + i]);
-        act[row * F + i] = f32_to_bf16(__fmul_rn(__fmul_rn(g, sigmoid_f(g)), u));
-    }
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= F / 8) return;
+    float g[8], u[8], o[8];
+    unpack8(reinterpret_cast<const uint4*>(gu + row * 2 * F)[c], g);
+    unpack8(reinterpret_cast<const uint4*>(gu + row * 2 * F + F)[c], u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(g[e], sigmoid_f(g[e])), u[e]);
+    reinterpret_cast<uint4*>(act + row * F)[c] = pack8(o);
 }
 
 // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
 __global__ void gdn_gates_kernel(const uint16_t* __restrict__ proj, long long stride, int b_col, int H,
                                  uint16_t* __restrict__ gates) {
+    griddep_launch();
+    griddep_wait();
     const long long m = blockIdx.x;
     for (int h = threadIdx.x; h < H; h += blockDim.x) {
         const float bb = bf16_to_f32(proj[m * stride + b_col + h]);
@@ -99,44 +151,82 @@ __global__ void gdn_gates_kernel(const uint16_t* __restrict__ proj, long long st
     }
 }
 
-// Lowest index among the maxima of each row (fixed-order tree; ties and NaN-free).
-__global__ void argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ idx) {
-    __shared__ float sv[32];
-    __shared__ int si[32];
-    const long long row = blockIdx.x;
-    const float* x = logits + row * V;
-    float best = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int i = threadIdx.x; i < V; i += blockDim.x) {
-        const float v = x[i];
-        if (v > best) { best = v; bi = i; }   // i increases, so ties keep the lower index
-    }
+// Argmax, lowest index among the maxima.  Pass 1: CTA (chunk, row) takes ARGMAX_CHUNK
+// consecutive logits (thread t: elements t*4 .. t*4+3 of every 1024-element stripe, in
+// increasing order) and writes its (max, index); pass 2 reduces a row's chunk results.
+// (value, -index) is a total order, so the result does not depend on the reduction order.
+constexpr int ARGMAX_THREADS = 256;
+constexpr int ARGMAX_CHUNK = 8192;
+
+__device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
+    if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+}
+__device__ __forceinline__ void warp_best(float& bv, int& bi) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+        better(bv, bi, ov, oi);
     }
+}
+
+__global__ void __launch_bounds__(ARGMAX_THREADS) argmax_chunk_kernel(const float* __restrict__ logits, int V,
+                                                                       float2* __restrict__ part, int nchunk) {
+    griddep_launch();
+    griddep_wait();
+    __shared__ float sv[ARGMAX_THREADS / 32];
+    __shared__ int si[ARGMAX_THREADS / 32];
+    const long long row = blockIdx.y;
+    const int base = blockIdx.x * ARGMAX_CHUNK;
+    const float* x = logits + row * V;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    const bool vec = (V % 4) == 0;
+#pragma unroll
+    for (int j = 0; j < ARGMAX_CHUNK / (ARGMAX_THREADS * 4); ++j) {
+        const int i0 = base + j * ARGMAX_THREADS * 4 + threadIdx.x * 4;
+        if (vec && i0 + 3 < V) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(x + i0));
+            better(bv, bi, f.x, i0);
+            better(bv, bi, f.y, i0 + 1);
+            better(bv, bi, f.z, i0 + 2);
+            better(bv, bi, f.w, i0 + 3);
+        } else {
+            for (int e = 0; e < 4; ++e)
+                if (i0 + e < V) better(bv, bi, x[i0 + e], i0 + e);
+        }
+    }
+    warp_best(bv, bi);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) { sv[warp] = best; si[warp] = bi; }
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
     __syncthreads();
     if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        best = lane < nw ? sv[lane] : -INFINITY;
-        bi = lane < nw ? si[lane] : 0x7fffffff;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
-        }
-        if (lane == 0) idx[row] = bi == 0x7fffffff ? 0 : bi;
+        bv = lane < ARGMAX_THREADS / 32 ? sv[lane] : -INFINITY;
+        bi = lane < ARGMAX_THREADS / 32 ? si[lane] : 0x7fffffff;
+        warp_best(bv, bi);
+        if (lane == 0) part[row * nchunk + blockIdx.x] = make_float2(bv, __int_as_float(bi));
     }
+}
+
+__global__ void argmax_final_kernel(const float2* __restrict__ part, int nchunk, int32_t* __restrict__ idx) {
+    griddep_launch();
+    griddep_wait();
+    const long long row = blockIdx.x;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = threadIdx.x; c < nchunk; c += 32) {
+        const float2 p = part[row * nchunk + c];
+        better(bv, bi, p.x, __float_as_int(p.y));
+    }
+    warp_best(bv, bi);
+    if (threadIdx.x == 0) idx[row] = bi == 0x7fffffff ? 0 : bi;
 }
 
 // n_accept[b] = number of leading drafts tokens[b][j+1] equal to pred[b][j]
 __global__ void accept_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ pred, int B, int k,
                               int32_t* __restrict__ n_accept) {
+    griddep_launch();
+    griddep_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int n = 0;
@@ -146,6 +236,8 @@ __global__ void accept_kernel(const int32_t* __restrict__ tokens, const int32_t*
 
 __global__ void commit_kernel(const int32_t* __restrict__ keep, int keep_bias, int B, int k, int32_t* __restrict__ ctx_len,
                               int32_t* __restrict__ n_commit, unsigned* err) {
+    griddep_launch();
+    griddep_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int n = keep[b] + keep_bias;
@@ -158,6 +250,8 @@ __global__ void commit_kernel(const int32_t* __restrict__ keep, int keep_bias, i
 }
 
 __global__ void zero_i32_kernel(int32_t* p, int n) {
+    griddep_launch();
+    griddep_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) p[i] = 0;
 }
@@ -168,46 +262,60 @@ xv_status embed_launch(const int32_t* tokens, int M, const uint16_t* E, int V, i
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "embed: device error word unavailable");
     trace_pre(s);
-    embed_kernel<<<M, 128, 0, s>>>(tokens, E, V, H, x, err);
+    launch_k(embed_kernel, dim3(M), dim3(128), 0, s, tokens, E, V, H, x, err);
     return launched("embed_kernel", s, K_EMBED, 4ll * M * H + 4ll * M);
+}
+
+static int norm_threads(int H) {
+    int t = ((H / 8 + NORM_MAXC - 1) / NORM_MAXC + 31) / 32 * 32;
+    const int want = (H / 8 + 31) / 32 * 32;       // one chunk per thread when it fits
+    if (want <= 1024) t = want;
+    return t < 32 ? 32 : t;
 }
 
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s) {
     trace_pre(s);
-    rmsnorm_kernel<<<M, NORM_THREADS, 0, s>>>(const_cast<uint16_t*>(x), nullptr, w, H, eps, y);
+    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y);
     return launched("rmsnorm_kernel", s, K_RMSNORM, 4ll * M * H + 2ll * H);
 }
 
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps, uint16_t* xn,
                                   cudaStream_t s) {
     trace_pre(s);
-    rmsnorm_kernel<<<M, NORM_THREADS, 0, s>>>(x, y, w, H, eps, xn);
+    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, x, y, w, H, eps, xn);
     return launched("rmsnorm_kernel(residual)", s, K_RMSNORM, 8ll * M * H + 2ll * H);
 }
 
 xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s) {
-    dim3 grid(ceil_div(F, 256 * 4), M);
+    dim3 grid(ceil_div(F / 8, 256), M);
     trace_pre(s);
-    swiglu_kernel<<<grid, 256, 0, s>>>(gu, F, act);
+    launch_k(swiglu_kernel, grid, dim3(256), 0, s, gu, F, act);
     return launched("swiglu_kernel", s, K_SWIGLU, 6ll * M * F);
 }
 
 xv_status gdn_gates_launch(const uint16_t* proj, long long proj_stride, int b_col, int M, int H, uint16_t* gates,
                            cudaStream_t s) {
     trace_pre(s);
-    gdn_gates_kernel<<<M, 64, 0, s>>>(proj, proj_stride, b_col, H, gates);
+    launch_k(gdn_gates_kernel, dim3(M), dim3(64), 0, s, proj, proj_stride, b_col, H, gates);
     return launched("gdn_gates_kernel", s, K_GATES, 8ll * M * H);
 }
 
-xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, cudaStream_t s) {
+size_t argmax_workspace_size(int M, int V) { return static_cast<size_t>(M) * ceil_div(V, ARGMAX_CHUNK) * sizeof(float2); }
+
+xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, void* ws, cudaStream_t s) {
+    const int nchunk = ceil_div(V, ARGMAX_CHUNK);
+    float2* part = static_cast<float2*>(ws);
     trace_pre(s);
-    argmax_kernel<<<M, 1024, 0, s>>>(logits, V, idx);
-    return launched("argmax_kernel", s, K_ARGMAX, 4ll * M * V + 4ll * M);
+    launch_k(argmax_chunk_kernel, dim3(nchunk, M), dim3(ARGMAX_THREADS), 0, s, logits, V, part, nchunk);
+    if (xv_status st = launched("argmax_chunk_kernel", s, K_ARGMAX, 4ll * M * V)) return st;
+    trace_pre(s);
+    launch_k(argmax_final_kernel, dim3(M), dim3(32), 0, s, part, nchunk, idx);
+    return launched("argmax_final_kernel", s, K_ARGMAX, 8ll * M * nchunk + 4ll * M);
 }
 
 xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s) {
     trace_pre(s);
-    accept_kernel<<<ceil_div(B, 128), 128, 0, s>>>(tokens, pred, B, k, n_accept);
+    launch_k(accept_kernel, dim3(ceil_div(B, 128)), dim3(128), 0, s, tokens, pred, B, k, n_accept);
     return launched("accept_kernel", s, K_ACCEPT, 8ll * B * k + 4ll * B);
 }
 
@@ -216,13 +324,13 @@ xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "commit: device error word unavailable");
     trace_pre(s);
-    commit_kernel<<<ceil_div(B, 128), 128, 0, s>>>(keep, keep_bias, B, k, ctx_len, n_commit, err);
+    launch_k(commit_kernel, dim3(ceil_div(B, 128)), dim3(128), 0, s, keep, keep_bias, B, k, ctx_len, n_commit, err);
     return launched("commit_kernel", s, K_COMMIT, 16ll * B);
 }
 
 xv_status zero_i32_launch(int32_t* p, int n, cudaStream_t s) {
     trace_pre(s);
-    zero_i32_kernel<<<ceil_div(n, 256), 256, 0, s>>>(p, n);
+    launch_k(zero_i32_kernel, dim3(ceil_div(n, 256)), dim3(256), 0, s, p, n);
     return launched("zero_i32_kernel", s, K_ZERO, 4ll * n);
 }
 

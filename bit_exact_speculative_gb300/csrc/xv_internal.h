@@ -20,6 +20,26 @@ enum Kind : int { K_GEMM = 0, K_GDN, K_ATTN_SPLIT, K_ATTN_COMBINE, K_KV_APPEND, 
 void trace_pre(cudaStream_t s);
 // Checks the launch just made on the calling thread, counts it and closes its trace record.
 xv_status launched(const char* what, cudaStream_t s, int kind, long long bytes);
+// Programmatic dependent launch between the library's kernels (on by default).
+bool overlap_enabled();
+// Launches `kern` on stream s with the programmatic-serialization attribute when
+// overlap is enabled: the kernel may start before its predecessor ends, and it
+// calls griddep_wait() before touching memory that earlier kernels produce or read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = overlap_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 // Device address of the library's device-side error word for the current device.
 unsigned* device_error_word();
 
@@ -82,7 +102,8 @@ xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStr
 // gates[m] = [beta(H) | gate(H)] from the b and a columns of proj row m
 xv_status gdn_gates_launch(const uint16_t* proj, long long proj_stride, int b_col, int M, int H, uint16_t* gates,
                            cudaStream_t s);
-xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, cudaStream_t s);
+size_t argmax_workspace_size(int M, int V);
+xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, void* ws, cudaStream_t s);
 xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s);
 // ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (keep checked to lie in [1, k])
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,

@@ -30,6 +30,13 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
+// ----------------------------------------------- programmatic dependent launch
+// Lets the next kernel in the stream start its independent prologue now.
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Waits until every earlier kernel of the stream has completed and its writes are visible
+// (a no-op when the kernel was launched without the programmatic attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

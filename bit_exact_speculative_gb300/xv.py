@@ -64,6 +64,7 @@ _SIGS = {
     "xv_last_error": ([], ctypes.c_char_p),
     "xv_device_check": ([vp, ctypes.POINTER(ctypes.c_uint)], c_int),
     "xv_launch_count": ([], ctypes.c_ulonglong),
+    "xv_set_overlap": ([c_int], c_int),
     "xv_trace_enable": ([c_int], c_int),
     "xv_trace_disable": ([], c_int),
     "xv_trace_count": ([], c_int),
@@ -145,6 +146,10 @@ def xv_device_check(stream=None) -> int:
 
 def xv_launch_count() -> int:
     return int(lib().xv_launch_count())
+
+
+def xv_set_overlap(enable: bool):
+    _check(lib().xv_set_overlap(int(enable)))
 
 
 def xv_trace_enable(capacity: int):

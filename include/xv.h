@@ -75,6 +75,13 @@ xv_status xv_device_check(xv_stream s, unsigned* code);
 /* Number of kernels this library has launched in this process (host counter). */
 unsigned long long xv_launch_count(void);
 
+/* Programmatic dependent launch between consecutive kernels of this library
+ * (default on): a kernel may start its independent prologue (barrier set-up,
+ * TMEM allocation, prefetch of weights) while its predecessor in the stream
+ * finishes, and waits for the predecessor before touching activations.
+ * Results are identical either way; 0 turns it off (for timing comparisons). */
+xv_status xv_set_overlap(int enable);
+
 /* Launch trace, a profiling hook outside the verify method.  While enabled,
  * every kernel the library launches is bracketed by two CUDA events recorded
  * on its stream, and the launch's kind and algorithmic bytes (inputs read
