@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--k", type=int, default=8)
     ap.add_argument("--context", type=int, default=2183)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true", help="launch kernels without programmatic dependent launch")
     return ap.parse_args()
 
 
@@ -186,6 +187,7 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     xv.lib()
+    xv.xv_set_overlap(not args.no_overlap)
 
     cfg, w_host, stk, toks = make_stack(args, device)
     B, k = args.batch, args.k
@@ -280,7 +282,7 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch_per_gpu": B, "k": k, "context": args.context,
-                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
+                       "parallelism": f"replicas x{world}", "overlap": not args.no_overlap, "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
             "gpu_launches": int(launches),
             "roofline": {"bound": "hbm", "kernel": "gemm_small_m", "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),

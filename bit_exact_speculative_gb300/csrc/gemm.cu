@@ -41,13 +41,22 @@ constexpr int TMEM_COLS = 64;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BN, GEMM_TOK);
 constexpr int SM_COUNT_TARGET = 152;   // GB300
+// K-blocks of its weight slice, beyond the first STAGES, that a CTA asks L2 to prefetch
+// before it waits for the previous kernel: while earlier kernels that move little data
+// run (GDN, attention, norms), HBM keeps streaming this GEMM's weights.
+constexpr int L2_PREFETCH_BLOCKS = 8;
+// Splits of 2..CLUSTER_MAX segments are combined inside a thread-block cluster through
+// distributed shared memory (no workspace); larger ones, used only by narrow shapes with
+// too few tiles to fill the GPU otherwise, go through the workspace.
+constexpr int CLUSTER_MAX = 4;
 constexpr int RESIDENT_PER_SM = 2;
 
 template <bool F32OUT>
 __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         void* __restrict__ Y, int ldy, int M, int N, int nkb, int S, float* __restrict__ part,
-                        unsigned* __restrict__ cnt, unsigned* __restrict__ err) {
+                        unsigned* __restrict__ cnt, unsigned* __restrict__ err, const uint16_t* __restrict__ W,
+                        int K, int cluster_combine) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_last;
     const uint32_t raw = smem_u32(smem_raw);
@@ -92,10 +101,11 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
         // ---- producer: TMA into the ring.  The weights of the first stages are requested
         // before waiting for the previous kernel (they do not depend on it); the token rows
         // only after.
+        const uint64_t stream_policy = l2_policy_evict_first();   // each weight is read once
         const int pre = nk < STAGES ? nk : STAGES;
         for (int i = 0; i < pre; ++i) {
             mbar_arrive_expect_tx(full(i), STAGE_BYTES);
-            tma_load_2d(sA + i * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(i));
+            tma_load_2d_hint(sA + i * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(i), stream_policy);
         }
         griddep_wait();
         for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * B_BYTES, &tmX, (kb0 + i) * GEMM_BK, 0, full(i));
@@ -105,7 +115,7 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
             const uint32_t ph = (i / STAGES) & 1u;
             if (i >= STAGES && !mbar_wait(empty(st), ph ^ 1u, err)) { ok = false; break; }
             mbar_arrive_expect_tx(full(st), STAGE_BYTES);
-            tma_load_2d(sA + st * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(st));
+            tma_load_2d_hint(sA + st * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(st), stream_policy);
             tma_load_2d(sB + st * B_BYTES, &tmX, (kb0 + i) * GEMM_BK, 0, full(st));
             issued = i + 1;
         }
@@ -114,6 +124,18 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
                 mbar_wait(full(j % STAGES), (j / STAGES) & 1u, err);
         }
     } else {
+        if (warp == 2) {
+            // L2 prefetch of the next K-blocks of this CTA's 128 weight rows (weights only)
+            const int k_first = kb0 + STAGES, k_last = min(kb1, kb0 + STAGES + L2_PREFETCH_BLOCKS);
+            if (k_first < k_last) {
+                const int k_end = min(k_last * GEMM_BK, K);
+                const uint32_t bytes = static_cast<uint32_t>(k_end - k_first * GEMM_BK) * 2u;
+                for (int r = lane; r < GEMM_BN; r += 32) {
+                    const int row = tile * GEMM_BN + r;
+                    if (row < N) l2_prefetch(W + static_cast<size_t>(row) * K + static_cast<size_t>(k_first) * GEMM_BK, bytes);
+                }
+            }
+        }
         griddep_wait();   // before any read or write of activations, partials or counters
     }
     if (warp == 1 && lane == 0) {
@@ -148,7 +170,55 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
 
     const int n = tile * GEMM_BN + warp * 32 + lane;
     const bool live = n < N;
-    if (S == 1) {
+    if (cluster_combine) {
+        // The S segments of this tile form one cluster.  Each CTA parks its partial in its own
+        // shared memory (the drained stage ring) as [m][row]; after a cluster barrier, CTA q
+        // finishes the rows r = q, q + S, ... by reading every segment's partial over DSMEM and
+        // adding them in segment order 0..S-1 — the same sum, in the same order, as the
+        // workspace path below, so the bits do not depend on the path.
+        float* pbuf = reinterpret_cast<float*>(smem);
+        const int r_local = warp * 32 + lane;
+#pragma unroll
+        for (int m = 0; m < GEMM_TOK; ++m)
+            if (m < M) pbuf[m * GEMM_BN + r_local] = acc[m];
+        __syncwarp();
+        cluster_sync();
+        const uint32_t q = cluster_ctarank();
+        const int rows_q = (GEMM_BN - static_cast<int>(q) + S - 1) / S;
+        const int total = rows_q * M;
+        const uint32_t pbase = smem_u32(pbuf);
+        // 8 elements per thread per batch, all their DSMEM loads in flight together
+        for (int e0 = threadIdx.x; e0 < total; e0 += 8 * blockDim.x) {
+            float v[8][CLUSTER_MAX];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + j * blockDim.x;
+                const int r = static_cast<int>(q) + S * (e / M), m = e % M;
+                const uint32_t off = static_cast<uint32_t>((m * GEMM_BN + r) * 4);
+#pragma unroll
+                for (int s2 = 0; s2 < CLUSTER_MAX; ++s2)
+                    v[j][s2] = (e < total && s2 < S) ? ld_dsmem(mapa_shared(pbase + off, s2)) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + j * blockDim.x;
+                if (e >= total) continue;
+                const int r = static_cast<int>(q) + S * (e / M), m = e % M;
+                float sum = v[j][0];
+#pragma unroll
+                for (int s2 = 1; s2 < CLUSTER_MAX; ++s2)
+                    if (s2 < S) sum = __fadd_rn(sum, v[j][s2]);
+                const int row = tile * GEMM_BN + r;
+                if (row < N) {
+                    const size_t o = static_cast<size_t>(m) * ldy + row;
+                    if (F32OUT) static_cast<float*>(Y)[o] = sum;
+                    else static_cast<uint16_t*>(Y)[o] = f32_to_bf16(sum);
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+    } else if (S == 1) {
         if (live) {
 #pragma unroll
             for (int m = 0; m < GEMM_TOK; ++m) {
@@ -172,20 +242,30 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
             __threadfence();
             if (live) {
                 // r = p_0 + p_1 + ... + p_{S-1} in segment order (this CTA's own partial is read
-                // back too, so every load is unconditional).  16 rows per batch: each segment's
-                // 16 loads are independent and in flight together.
-                for (int mc = 0; mc < M; mc += 16) {
-                    float r[16];
-                    for (int s2 = 0; s2 < S; ++s2) {
-                        const float* ps = part + (static_cast<size_t>(s2) * M + mc) * N + n;
-                        float v[16];
+                // back too, so every load is unconditional).  Rows go in batches of 8 and the
+                // loads of up to 8 segments are issued together before any add, so a batch
+                // costs one round trip to L2 per 8 segments.
+                for (int mc = 0; mc < M; mc += 8) {
+                    float r[8];
+                    for (int sg = 0; sg < S; sg += 8) {
+                        float v[8][8];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = (mc + j < M) ? __ldcg(ps + static_cast<size_t>(j) * N) : 0.f;
+                        for (int q = 0; q < 8; ++q) {
+                            const float* ps = part + (static_cast<size_t>(sg + q) * M + mc) * N + n;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) r[j] = (s2 == 0) ? v[j] : __fadd_rn(r[j], v[j]);
+                            for (int j = 0; j < 8; ++j)
+                                v[q][j] = (sg + q < S && mc + j < M) ? __ldcg(ps + static_cast<size_t>(j) * N) : 0.f;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            if (sg + q < S) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) r[j] = (sg + q == 0) ? v[q][j] : __fadd_rn(r[j], v[q][j]);
+                            }
+                        }
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         if (mc + j < M) {
                             const size_t o = static_cast<size_t>(mc + j) * ldy + n;
                             if (F32OUT) static_cast<float*>(Y)[o] = r[j];
@@ -215,6 +295,7 @@ int gemm_splits(int N, int K) {
     int s = (SM_COUNT_TARGET * RESIDENT_PER_SM) / tiles;
     if (s < 1) s = 1;
     if (s > 16) s = 16;
+    if (s > CLUSTER_MAX && tiles * CLUSTER_MAX >= SM_COUNT_TARGET) s = CLUSTER_MAX;
     while (s > 1 && nkb / s < 4) --s;
     return s;
 }
@@ -228,7 +309,7 @@ static_assert(COUNTER_BYTES / sizeof(unsigned) >= SM_COUNT_TARGET * RESIDENT_PER
 
 size_t gemm_workspace_size(int M, int N, int K) {
     const int S = gemm_splits(N, K);
-    if (S == 1) return 0;
+    if (S <= CLUSTER_MAX) return 0;
     return COUNTER_BYTES + round256(static_cast<size_t>(S) * M * N * sizeof(float));
 }
 
@@ -257,7 +338,7 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     const int tiles = num_tiles(N), S = gemm_splits(N, K), nkb = ceil_div(K, GEMM_BK);
     float* part = nullptr;
     unsigned* cnt = nullptr;
-    if (S > 1) {
+    if (S > CLUSTER_MAX) {
         cnt = static_cast<unsigned*>(ws);
         part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + COUNTER_BYTES);
     }
@@ -270,8 +351,13 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
         attr_set[f32out] = true;
     }
     dim3 grid(tiles, S);
+    const int cluster = (S > 1 && S <= CLUSTER_MAX) ? 1 : 0;
     trace_pre(s);
-    launch_k(kern, grid, dim3(128), SMEM_BYTES, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err);
+    if (cluster)
+        launch_k_cluster(kern, grid, dim3(128), SMEM_BYTES, s, dim3(1, S, 1), tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt,
+                         err, W, K, cluster);
+    else
+        launch_k(kern, grid, dim3(128), SMEM_BYTES, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, W, K, cluster);
     const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
     return launched("gemm_small_m_kernel", s, K_GEMM, bytes);
 }

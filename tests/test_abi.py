@@ -51,10 +51,12 @@ def test_gemm_validation_without_gpu(xv):
     assert L.xv_gemm_small_m(p, 68, p, p, 64, 1, 64, 68, None, 0, None) == xv.XV_ERR_UNSUPPORTED  # K % 8
     odd = ctypes.c_void_p(0x10002)
     assert L.xv_gemm_small_m(odd, 64, p, p, 64, 1, 64, 64, None, 0, None) == xv.XV_ERR_UNSUPPORTED
-    # a split-K shape needs a workspace
-    assert xv.xv_gemm_splits(5120, 17408) > 1
-    assert xv.xv_gemm_workspace_size(8, 5120, 17408) > 0
-    assert L.xv_gemm_small_m(p, 17408, p, p, 5120, 8, 5120, 17408, None, 0, None) == xv.XV_ERR_WORKSPACE
+    # a narrow shape split into more segments than a cluster combines needs a workspace
+    assert xv.xv_gemm_splits(1024, 8192) > 4
+    assert xv.xv_gemm_workspace_size(8, 1024, 8192) > 0
+    assert L.xv_gemm_small_m(p, 8192, p, p, 1024, 8, 1024, 8192, None, 0, None) == xv.XV_ERR_WORKSPACE
+    # the projection shapes combine their splits in clusters and need none
+    assert 1 < xv.xv_gemm_splits(5120, 17408) <= 4 and xv.xv_gemm_workspace_size(64, 5120, 17408) == 0
 
 
 def test_gemm_splits_depend_on_shape_only(xv):

@@ -49,10 +49,21 @@ def big(xv):
     Wd = synth.normal_bf16(0, synth.tid("sweep.w_down"), (5120, 17408), sigma=0.02)
     Xgu = synth.normal_bf16(0, synth.tid("sweep.x_gate_up"), (64, 5120))
     Xd = synth.normal_bf16(0, synth.tid("sweep.x_down"), (64, 17408))
-    return {"gu": (Xgu, Wgu, dev(Xgu), dev(Wgu)), "down": (Xd, Wd, dev(Xd), dev(Wd))}
+    # a narrow, deep shape whose K split (16 segments) is combined through the workspace
+    Wn = synth.normal_bf16(0, synth.tid("sweep.w_narrow"), (1024, 8192), sigma=0.02)
+    Xn = synth.normal_bf16(0, synth.tid("sweep.x_narrow"), (64, 8192))
+    return {"gu": (Xgu, Wgu, dev(Xgu), dev(Wgu)), "down": (Xd, Wd, dev(Xd), dev(Wd)),
+            "narrow": (Xn, Wn, dev(Xn), dev(Wn))}
 
 
-@pytest.mark.parametrize("which", ["gu", "down"])
+def test_split_paths(xv):
+    """gate/up: no split; down: 4 segments combined in a cluster; narrow: 16 through the workspace."""
+    assert xv.xv_gemm_splits(34816, 5120) == 1
+    assert 2 <= xv.xv_gemm_splits(5120, 17408) <= 4
+    assert xv.xv_gemm_splits(1024, 8192) > 4 and xv.xv_gemm_workspace_size(8, 1024, 8192) > 0
+
+
+@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
 def test_row_bits_independent_of_M(xv, big, which):
     _, _, X, W = big[which]
     ref = run(xv, X, W, M=16)
@@ -62,7 +73,7 @@ def test_row_bits_independent_of_M(xv, big, which):
         assert same_bits(Y[:m], ref[:m]), f"M={M}: rows differ from the M=16 call"
 
 
-@pytest.mark.parametrize("which", ["gu", "down"])
+@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
 def test_row_bits_independent_of_position(xv, big, which):
     _, _, X, W = big[which]
     perm = torch.tensor([5, 0, 7, 3, 1, 6, 2, 4], device="cuda")
@@ -71,7 +82,7 @@ def test_row_bits_independent_of_position(xv, big, which):
     assert same_bits(Yp, Y[perm])
 
 
-@pytest.mark.parametrize("which", ["gu", "down"])
+@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
 def test_full_size_parity_sampled(xv, big, which):
     Xh, Wh, X, W = big[which]
     M = 16
@@ -82,7 +93,7 @@ def test_full_size_parity_sampled(xv, big, which):
     assert_bf16_close(Y[:, cols], ref, what=f"{which} sampled")
 
 
-@pytest.mark.parametrize("which", ["gu", "down"])
+@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
 def test_hundred_runs_identical(xv, big, which):
     _, _, X, W = big[which]
     ref = run(xv, X, W, M=16)

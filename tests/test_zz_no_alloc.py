@@ -29,8 +29,9 @@ def xv():
     return m
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 5120, 17408), (8, 17408, 5120), (64, 5120, 4096), (5, 300, 1000)])
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 8192), (64, 1024, 8192), (16, 5120, 17408), (5, 300, 1000)])
 def test_noalloc_matches_workspace_entry_point_twice(xv, M, N, K):
+    # the first two shapes split K into 16 segments, whose partial sums go through the scratch
     X = dev(synth.normal_bf16(0, synth.tid(f"na.x.{M}.{N}.{K}"), (M, K)))
     W = dev(synth.normal_bf16(0, synth.tid(f"na.w.{M}.{N}.{K}"), (N, K), sigma=0.02))
     ref = torch.empty((M, N), dtype=torch.int16, device="cuda")
