@@ -39,7 +39,7 @@ WORKLOAD = ("4-layer hybrid stack (3 GDN + 1 gated attention), hidden 5120, MLP 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="xv", choices=["xv", "reference"])
     ap.add_argument("--batch", type=int, default=1)
@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--context", type=int, default=2183)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="launch kernels without programmatic dependent launch")
+    ap.add_argument("--no-kernel-rooflines", action="store_true", help="skip the per-kernel measurements")
     return ap.parse_args()
 
 
@@ -81,6 +82,12 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_first(self, timeout=5.0):
+        """Blocks until the sampler has produced a line (so the timed region is covered)."""
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
 
     def __exit__(self, *a):
         if self.proc:
@@ -169,6 +176,115 @@ def traffic_from_profile(kernel_src: str):
     return e.get("dram_bytes_per_step")
 
 
+# ------------------------------------------------------ per-kernel rooflines
+
+def _traced_median_ms(xv, launch, n):
+    """Median device time of n launches (each bracketed by events on its stream)."""
+    import torch
+    xv.xv_trace_enable(4 * n)
+    for i in range(n):
+        launch(i)
+    torch.cuda.synchronize()
+    recs = xv.xv_trace_read()
+    xv.xv_trace_disable()
+    return recs
+
+
+def kernel_rooflines(xv, device, peak):
+    """The three hot kernels alone, L2-cold (inputs rotated through more than 3x L2), timed per launch."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    out = {}
+
+    def rnd(shape, scale=1.0, dtype=torch.bfloat16):
+        return (torch.randn(shape, generator=g, device=device) * scale).to(dtype)
+
+    def copies_for(nbytes):
+        return max(2, int(np.ceil(400e6 / max(nbytes, 1))))
+
+    # small-M GEMM, every projection shape of the stack
+    gem = {}
+    for M in (8, 64):
+        for N, K, name, f32 in [(12352, 5120, "gdn_in", False), (5120, 4096, "gdn_out", False),
+                                (14336, 5120, "attn_in", False), (5120, 6144, "attn_out", False),
+                                (34816, 5120, "gate_up", False), (5120, 17408, "down", False),
+                                (151936, 5120, "lm_head", True)]:
+            nc = copies_for(2 * N * K)
+            Ws = [rnd((N, K), 0.02) for _ in range(nc)]
+            X = rnd((M, K))
+            Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
+            ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K), device=device)
+            for i in range(nc):
+                xv.xv_gemm_small_m(X, Ws[i], Y, ws)
+            recs = _traced_median_ms(xv, lambda i: xv.xv_gemm_small_m(X, Ws[i % nc], Y, ws), 3 * nc)
+            ms = float(np.median([t for k, t, _ in recs if k == "gemm_small_m"]))
+            nbytes = 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)
+            gem[f"{name}_M{M}"] = {"N": N, "K": K, "splits": xv.xv_gemm_splits(N, K), "us": round(ms * 1e3, 2),
+                                   "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                                   "frac": round(nbytes / ms / 1e6 / peak, 4)}
+            del Ws
+            torch.cuda.empty_cache()
+    out["gemm_small_m"] = gem
+
+    # GDN verify: 32 heads of 128 x 128 fp32, k = 8 speculative steps after 1 replayed step
+    H, D, k = 32, 128, 8
+    gd = {}
+    for B in (1, 8):
+        state_bytes = 4 * B * H * D * D
+        nc = copies_for(state_bytes)
+        states = [torch.randn((B, H, D, D), generator=g, device=device) * 0.1 for _ in range(nc)]
+        rows = B * k
+        qkv = rnd((rows, H * 3 * D))
+        gates = torch.rand((rows, 2 * H), generator=g, device=device).to(torch.bfloat16)
+        st = xv.gdn_steps(qkv, qkv[:, H * D:], qkv[:, 2 * H * D:], gates, gates[:, H:], 3 * H * D, 2 * H, k)
+        n = torch.ones(B, dtype=torch.int32, device=device)
+        o = torch.empty((rows, H * D), dtype=torch.bfloat16, device=device)
+        launch = lambda i: xv.xv_gdn_verify(states[i % nc], st, n, k, st, k, o, H * D, B, H, D, D, True)
+        for i in range(nc):
+            launch(i)
+        recs = _traced_median_ms(xv, launch, 3 * nc)
+        ms = float(np.median([t for kk, t, _ in recs if kk == "gdn"]))
+        nbytes = 2 * state_bytes + 2 * (1 + k) * B * H * (3 * D + 2) + 2 * k * B * H * D
+        gd[f"B{B}"] = {"us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                       "frac": round(nbytes / ms / 1e6 / peak, 4)}
+        del states
+        torch.cuda.empty_cache()
+    out["gdn_verify"] = gd
+
+    # decode-row attention: 24 q / 4 kv heads of 256, 8 rows per sequence
+    Hq, Hkv, hd, R = 24, 4, 256, 8
+    at = {}
+    for L in (640, 2183, 131072):
+        for B in (1, 8):
+            Lmax = L + R
+            cache_bytes = 2 * B * Hkv * Lmax * hd * 2
+            nc = copies_for(cache_bytes) if L < 131072 else 1
+            kcs = [rnd((B, Hkv, Lmax, hd)) for _ in range(nc)]
+            vcs = [rnd((B, Hkv, Lmax, hd)) for _ in range(nc)]
+            q = rnd((B * R, Hq * hd))
+            outb = torch.empty((B * R, Hq * hd), dtype=torch.bfloat16, device=device)
+            ctx = torch.full((B,), L, dtype=torch.int32, device=device)
+            ws = xv.workspace(xv.xv_attn_workspace_size(B, R, Hq, hd, L + R - 1), device=device)
+            launch = lambda i: xv.xv_attn_decode_rows(q, q.stride(0), kcs[i % nc], vcs[i % nc], ctx, R, B, Hq, Hkv, hd,
+                                                      Lmax, L + R - 1, hd ** -0.5, outb, outb.stride(0), ws)
+            for i in range(nc):
+                launch(i)
+            reps = max(3 * nc, 5)
+            recs = _traced_median_ms(xv, launch, reps)
+            split = [t for kk, t, _ in recs if kk == "attn_split"]
+            comb = [t for kk, t, _ in recs if kk == "attn_combine"]
+            ms = float(np.median(split)) + float(np.median(comb))
+            nbytes = B * (4 * Hkv * (L + R - 1) * hd + 2 * 2 * R * Hq * hd)   # K+V of every visible position, q, out
+            at[f"L{L}_B{B}"] = {"us": round(ms * 1e3, 2), "split_us": round(float(np.median(split)) * 1e3, 2),
+                                "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                                "frac": round(nbytes / ms / 1e6 / peak, 4)}
+            del kcs, vcs
+            torch.cuda.empty_cache()
+    out["attn_decode_rows"] = at
+    return out
+
+
 # ------------------------------------------------------------ GPU arm
 
 def run_gpu(args):
@@ -211,6 +327,7 @@ def run_gpu(args):
     # ---- timed region: K steps on device-resident inputs
     launches0 = xv.xv_launch_count()
     with ClockSampler(local) as clk:
+        clk.wait_first()
         barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -221,6 +338,7 @@ def run_gpu(args):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        time.sleep(0.25)   # one more sample after the region
     launches = xv.xv_launch_count() - launches0
     ms = e0.elapsed_time(e1)
     t = torch.tensor([ms], device=device)
@@ -275,6 +393,12 @@ def run_gpu(args):
         barrier()
     e2e_value = world * B * k * args.steps / float(t2.item())
 
+    rooflines = None
+    if rank == 0 and world == 1 and not args.no_kernel_rooflines:
+        del stk
+        torch.cuda.empty_cache()
+        rooflines = kernel_rooflines(xv, device, peak)
+
     out = None
     if rank == 0:
         out = {
@@ -298,6 +422,7 @@ def run_gpu(args):
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(B * k * 4),
                     "d2h_bytes_per_step": int(B * k * 4 + B * 4)},
             "clocks": clk.summary(),
+            "kernel_rooflines": rooflines,
             "device_error_bits": code,
         }
     if world > 1:

@@ -173,9 +173,10 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     if (cluster_combine) {
         // The S segments of this tile form one cluster.  Each CTA parks its partial in its own
         // shared memory (the drained stage ring) as [m][row]; after a cluster barrier, CTA q
-        // finishes the rows r = q, q + S, ... by reading every segment's partial over DSMEM and
-        // adding them in segment order 0..S-1 — the same sum, in the same order, as the
-        // workspace path below, so the bits do not depend on the path.
+        // finishes the contiguous rows [q*128/S, (q+1)*128/S) by reading every segment's partial
+        // over DSMEM and adding them in segment order 0..S-1 — the same sum, in the same order,
+        // as the workspace path below, so the bits do not depend on the path.  Consecutive
+        // threads take consecutive rows: conflict-free DSMEM reads, coalesced stores.
         float* pbuf = reinterpret_cast<float*>(smem);
         const int r_local = warp * 32 + lane;
 #pragma unroll
@@ -184,8 +185,9 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
         __syncwarp();
         cluster_sync();
         const uint32_t q = cluster_ctarank();
-        const int rows_q = (GEMM_BN - static_cast<int>(q) + S - 1) / S;
-        const int total = rows_q * M;
+        const int r0 = static_cast<int>(q) * GEMM_BN / S, r1 = (static_cast<int>(q) + 1) * GEMM_BN / S;
+        const int nr = r1 - r0;
+        const int total = nr * M;
         const uint32_t pbase = smem_u32(pbuf);
         // 8 elements per thread per batch, all their DSMEM loads in flight together
         for (int e0 = threadIdx.x; e0 < total; e0 += 8 * blockDim.x) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int e = e0 + j * blockDim.x;
-                const int r = static_cast<int>(q) + S * (e / M), m = e % M;
+                const int r = r0 + e % nr, m = e / nr;
                 const uint32_t off = static_cast<uint32_t>((m * GEMM_BN + r) * 4);
 #pragma unroll
                 for (int s2 = 0; s2 < CLUSTER_MAX; ++s2)
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
             for (int j = 0; j < 8; ++j) {
                 const int e = e0 + j * blockDim.x;
                 if (e >= total) continue;
-                const int r = static_cast<int>(q) + S * (e / M), m = e % M;
+                const int r = r0 + e % nr, m = e / nr;
                 float sum = v[j][0];
 #pragma unroll
                 for (int s2 = 1; s2 < CLUSTER_MAX; ++s2)
