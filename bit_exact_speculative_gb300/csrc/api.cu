@@ -225,7 +225,7 @@ xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, 
 static xv_status gdn_dims(int B, int H, int dk, int dv) {
     if (B < 1 || H < 1) return fail(XV_ERR_ARG, "gdn: need B >= 1 and H >= 1");
     if (dk != 64 && dk != 128) return fail(XV_ERR_UNSUPPORTED, "gdn: dk must be 64 or 128 (got %d)", dk);
-    if (dv < 16 || dv % 16) return fail(XV_ERR_UNSUPPORTED, "gdn: dv must be a positive multiple of 16 (got %d)", dv);
+    if (dv < 32 || dv % 32) return fail(XV_ERR_UNSUPPORTED, "gdn: dv must be a positive multiple of 32 (got %d)", dv);
     if (B > 65535 || H > 65535) return fail(XV_ERR_UNSUPPORTED, "gdn: B and H must be below 65536");
     return XV_OK;
 }
@@ -235,6 +235,8 @@ static xv_status gdn_steps_ok(const xv_gdn_steps* st, const char* which, int dk,
     if (!st->q || !st->k || !st->v || !st->beta || !st->gate) return fail(XV_ERR_ARG, "gdn: null pointer in %s", which);
     if (st->rows_per_seq < 1) return fail(XV_ERR_ARG, "gdn: %s.rows_per_seq must be >= 1", which);
     if (st->qkv_stride < 0 || st->gate_stride < H) return fail(XV_ERR_ARG, "gdn: bad strides in %s", which);
+    if (!aligned16(st->q) || !aligned16(st->k) || !aligned16(st->v) || (st->qkv_stride % 8))
+        return fail(XV_ERR_UNSUPPORTED, "gdn: q, k and v of %s must be 16-byte aligned with qkv_stride %% 8 == 0", which);
     (void)dk;
     return XV_OK;
 }

@@ -22,7 +22,7 @@ namespace {
 
 struct Dims {
     int H, V, F, L;
-    int gh, dk, dv, gin, ginner;
+    int gh, dk, dv, gin, ginner, gstride;
     int hq, hkv, hd, ain, ainner;
 };
 
@@ -40,12 +40,13 @@ xv_status check_cfg(const xv_block_config* c, Dims* d) {
     d->gh = c->gdn_heads; d->dk = c->gdn_dk; d->dv = c->gdn_dv;
     d->hq = c->attn_hq; d->hkv = c->attn_hkv; d->hd = c->attn_hd;
     d->gin = d->gh * (2 * d->dk + d->dv) + 2 * d->gh;
+    d->gstride = (d->gin + 7) / 8 * 8;
     d->ginner = d->gh * d->dv;
     d->ain = 2 * d->hq * d->hd + 2 * d->hkv * d->hd;
     d->ainner = d->hq * d->hd;
     if (has_gdn) {
-        if ((d->dk != 64 && d->dk != 128) || d->dv < 16 || d->dv % 16 || d->gh < 1)
-            return fail(XV_ERR_UNSUPPORTED, "block: GDN needs dk in {64,128}, dv a multiple of 16");
+        if ((d->dk != 64 && d->dk != 128) || d->dv < 32 || d->dv % 32 || d->gh < 1)
+            return fail(XV_ERR_UNSUPPORTED, "block: GDN needs dk in {64,128}, dv a multiple of 32");
         if (d->ginner % 8) return fail(XV_ERR_UNSUPPORTED, "block: GDN heads*dv must be a multiple of 8");
     } else {
         d->gin = d->ginner = 0;
@@ -113,6 +114,11 @@ int xv_gdn_in_dim(const xv_block_config* cfg) {
     return check_cfg(cfg, &d) ? -1 : d.gin;
 }
 
+int xv_gdn_hist_stride(const xv_block_config* cfg) {
+    Dims d{};
+    return check_cfg(cfg, &d) ? -1 : d.gstride;
+}
+
 int xv_attn_in_dim(const xv_block_config* cfg) {
     Dims d{};
     return check_cfg(cfg, &d) ? -1 : d.ain;
@@ -133,6 +139,8 @@ static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv
         if (cfg->layer_kind[l] == 0) {
             if (!ls.gdn_state || !ls.gdn_hist[0] || !ls.gdn_hist[1] || !ls.gdn_gates[0] || !ls.gdn_gates[1])
                 return fail(XV_ERR_ARG, "block: GDN layer %d state incomplete", l);
+            if (!aligned16(ls.gdn_hist[0]) || !aligned16(ls.gdn_hist[1]))
+                return fail(XV_ERR_UNSUPPORTED, "block: GDN history buffers must be 16-byte aligned");
         } else {
             if (!ls.k_cache || !ls.v_cache) return fail(XV_ERR_ARG, "block: attention layer %d cache missing", l);
             if (!aligned16(ls.k_cache) || !aligned16(ls.v_cache))
@@ -182,12 +190,12 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
         if (cfg->layer_kind[l] == 0) {
             uint16_t* hist = ls.gdn_hist[par];
             uint16_t* gates = ls.gdn_gates[par];
-            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, hist, d.gin, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-            XV_TRY(gdn_gates_launch(hist, d.gin, d.gh * (2 * d.dk + d.dv), M, d.gh, gates, s));
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, hist, d.gstride, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(gdn_gates_launch(hist, d.gstride, d.gh * (2 * d.dk + d.dv), M, d.gh, gates, s));
             const uint16_t* ph = ls.gdn_hist[par ^ 1];
             const uint16_t* pg = ls.gdn_gates[par ^ 1];
-            GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gin, 2 * d.gh, st->pending_rows};
-            GdnStepsDev draft{hist, hist + d.gh * d.dk, hist + 2 * d.gh * d.dk, gates, gates + d.gh, d.gin, 2 * d.gh, k};
+            GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gstride, 2 * d.gh, st->pending_rows};
+            GdnStepsDev draft{hist, hist + d.gh * d.dk, hist + 2 * d.gh * d.dk, gates, gates + d.gh, d.gstride, 2 * d.gh, k};
             XV_TRY(gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, draft, k, c.obuf, d.ginner, B,
                               d.gh, d.dk, d.dv, 1, s));
             XV_TRY(gemm_launch(c.obuf, d.ginner, lw.w_out, c.y, d.H, false, M, d.H, d.ginner, c.gemm_ws, c.gemm_ws_bytes, s));
@@ -250,7 +258,7 @@ xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stre
         xv_layer_state& ls = st->layers[l];
         const uint16_t* ph = ls.gdn_hist[par ^ 1];
         const uint16_t* pg = ls.gdn_gates[par ^ 1];
-        GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gin, 2 * d.gh, st->pending_rows};
+        GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gstride, 2 * d.gh, st->pending_rows};
         GdnStepsDev none{};
         if (xv_status e = gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, none, 0, nullptr, 0,
                                      st->B, d.gh, d.dk, d.dv, 1, s))

@@ -14,21 +14,29 @@
 // rounded once (explicit _rn intrinsics, so no contraction can differ):
 //     S <- a S;  r = S k;  u = b (v - r);  S <- S + u k^T;  o = S q.
 //
-// Tiling: a CTA owns (sequence b, head h, 16 state rows); each row is split
-// over 8 consecutive lanes, lane g holding float4 chunks g, g+8, g+16, ... of
-// the row (coalesced 128-byte segments per 8 lanes).  Row dot products are a
-// fixed two-chain sum over the lane's elements, then an xor-shuffle tree over
-// the 8 lanes (offsets 1, 2, 4): every lane ends with the same bits.  The
-// state lives in registers across all replay and speculative steps; it is
-// read once and (after a replay) written once.
+// Tiling: a CTA owns (sequence b, head h, 32 state rows) with 64 threads; a
+// row is split over 4 consecutive lanes (lane g holds float4 chunks g, g+4,
+// g+8, ... of the row) and each thread carries 2 rows, so the staged k and q
+// slices are loaded once for both and the two rows' dependency chains run
+// side by side.  Row dot products: two packed f32x2 accumulators (even and
+// odd pairs), a fixed sum of their four lanes, then an xor-shuffle tree over
+// the row's 4 lanes (offsets 1, 2): every lane ends with the same bits.  The
+// state lives in registers across all replay and speculative steps; it is read
+// once (its loads issued before the step inputs are staged) and, after a
+// replay, written once.  All step inputs are staged in one round of
+// independent loads, then normalised from shared memory.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
 namespace xv {
 
 namespace {
-constexpr int ROWS_PER_CTA = 16;
-constexpr int THREADS = 128;        // 4 warps x 4 rows x 8 lanes
+constexpr int LPR = 4;                          // lanes per state row
+constexpr int RPT = 2;                          // state rows per thread
+constexpr int WARPS = 2;
+constexpr int ROWS_PER_WARP = 32 / LPR * RPT;   // 16
+constexpr int ROWS_PER_CTA = ROWS_PER_WARP * WARPS;
+constexpr int THREADS = 32 * WARPS;
 
 struct GdnArgs {
     float* state;
@@ -45,8 +53,8 @@ struct GdnArgs {
     unsigned* err;
 };
 
-// Per-step inputs staged in shared memory: normalised q and k (fp32), this
-// CTA's 16 v entries, beta and gate.
+// Per-step inputs staged in shared memory: q and k (fp32, normalised in place), this
+// CTA's v entries, beta and gate.
 template <int DK>
 struct StepSmem {
     float q[DK];
@@ -56,154 +64,268 @@ struct StepSmem {
     float pad[2];
 };
 
-// Loads one step's inputs for (row index `row`, head h) and normalises q, k
-// with a fixed reduction (one warp per step: lane j sums elements j, j+32,
-// ... in order, then an xor tree over 32 lanes).
+// Source of staged slot t for sequence b: slots [0, max_commit) hold pending rows 0.., slots
+// [max_commit, max_commit + k) the draft rows.  All are staged whatever n_commit[b] is, so
+// staging never waits for it; only the first n_commit[b] pending slots are replayed.
+__device__ __forceinline__ const GdnStepsDev& step_src(const GdnArgs& A, int b, int t, long long* row) {
+    if (t < A.max_commit) {
+        *row = static_cast<long long>(b) * A.pend.rows_per_seq + t;
+        return A.pend;
+    }
+    *row = static_cast<long long>(b) * A.draft.rows_per_seq + (t - A.max_commit);
+    return A.draft;
+}
+
+__device__ __forceinline__ void store8(float* dst, const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float4 a = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
+                           __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+    float4 b = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
+                           __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+    *reinterpret_cast<float4*>(dst) = a;
+    *reinterpret_cast<float4*>(dst + 4) = b;
+}
+
+// Every step's raw inputs, converted to fp32 in shared memory.  q, k and this CTA's v slab
+// go as 16-byte chunks, STAGE_BATCH per thread issued back to back before any is used (one
+// round trip to memory for a verify's worth of steps); beta and gate are scalars.
+constexpr int STAGE_BATCH = 10;
+
 template <int DK>
-__device__ __forceinline__ void stage_step(StepSmem<DK>& dst, const GdnStepsDev& src, long long row, int h, int dv,
-                                           int row0, int l2, int lane) {
-    const uint16_t* q = src.q + row * src.qkv_stride + static_cast<long long>(h) * DK;
-    const uint16_t* k = src.k + row * src.qkv_stride + static_cast<long long>(h) * DK;
-    const uint16_t* v = src.v + row * src.qkv_stride + static_cast<long long>(h) * dv + row0;
-    constexpr int PER = DK / 32;
-    float qv[PER], kv[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        qv[e] = bf16_to_f32(q[lane + 32 * e]);
-        kv[e] = bf16_to_f32(k[lane + 32 * e]);
-    }
-    if (l2) {
-        float sq = __fmul_rn(qv[0], qv[0]), sk = __fmul_rn(kv[0], kv[0]);
-#pragma unroll
-        for (int e = 1; e < PER; ++e) {
-            sq = __fmaf_rn(qv[e], qv[e], sq);
-            sk = __fmaf_rn(kv[e], kv[e], sk);
+__device__ __forceinline__ const uint16_t* chunk_addr(const GdnArgs& A, int b, int h, int row0, int idx) {
+    constexpr int CH = DK / 8, VCH = ROWS_PER_CTA / 8, PER = 2 * CH + VCH;
+    const int t = idx / PER, j = idx - t * PER;
+    long long row;
+    const GdnStepsDev& src = step_src(A, b, t, &row);
+    const long long base = row * src.qkv_stride;
+    if (j < CH) return src.q + base + static_cast<long long>(h) * DK + 8 * j;
+    if (j < 2 * CH) return src.k + base + static_cast<long long>(h) * DK + 8 * (j - CH);
+    return src.v + base + static_cast<long long>(h) * A.dv + row0 + 8 * (j - 2 * CH);
+}
+
+// Shared-memory destination of chunk idx (q, k and v of a slot are contiguous floats).
+template <int DK>
+__device__ __forceinline__ float* chunk_dst(StepSmem<DK>* steps, int idx) {
+    constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
+    const int t = idx / PER, j = idx - t * PER;
+    return reinterpret_cast<float*>(&steps[t]) + 8 * j;
+}
+
+// One round of staging for thread slot `base`: issue() starts the loads (a beta/gate scalar
+// and up to STAGE_BATCH chunks) into registers, commit() converts and stores them.
+template <int DK>
+struct StageRound {
+    uint4 v[STAGE_BATCH];
+    uint16_t bg;
+    int base;
+
+    __device__ __forceinline__ void issue(StepSmem<DK>* steps, const GdnArgs& A, int b, int h, int row0, int total,
+                                          int base_) {
+        constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
+        base = base_;
+        const int n = total * PER;
+        if (base < 2 * total) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, base >> 1, &row);
+            bg = (base & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
         }
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
-            sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, off));
-        }
-        const float iq = __frcp_rn(__fsqrt_rn(__fadd_rn(sq, 1e-6f)));
-        const float ik = __frcp_rn(__fsqrt_rn(__fadd_rn(sk, 1e-6f)));
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            qv[e] = __fmul_rn(qv[e], iq);
-            kv[e] = __fmul_rn(kv[e], ik);
+        for (int u = 0; u < STAGE_BATCH; ++u) {
+            const int idx = base + u * THREADS;
+            if (idx < n) v[u] = *reinterpret_cast<const uint4*>(chunk_addr<DK>(A, b, h, row0, idx));
         }
     }
+    __device__ __forceinline__ void commit(StepSmem<DK>* steps, int total) {
+        constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
+        const int n = total * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        dst.q[lane + 32 * e] = qv[e];
-        dst.k[lane + 32 * e] = kv[e];
+        for (int u = 0; u < STAGE_BATCH; ++u)
+            if (base + u * THREADS < n) store8(chunk_dst<DK>(steps, base + u * THREADS), v[u]);
+        if (base < 2 * total) {
+            if (base & 1) steps[base >> 1].gate = bf16_to_f32(bg);
+            else steps[base >> 1].beta = bf16_to_f32(bg);
+        }
     }
-    if (lane < ROWS_PER_CTA) dst.v[lane] = bf16_to_f32(v[lane]);
-    if (lane == 0) {
-        dst.beta = bf16_to_f32(src.beta[row * src.gate_stride + h]);
-        dst.gate = bf16_to_f32(src.gate[row * src.gate_stride + h]);
+};
+
+// Per-head L2 normalisation of q and k in shared memory: x / sqrt(sum x^2 + 1e-6).
+// Vector w (slot w/2, q for even w, k for odd) belongs to the thread pair (2w', 2w'+1) with
+// w' = w mod (THREADS/2); thread p of the pair sums elements p*DK/2 .. (p+1)*DK/2 - 1 in four
+// interleaved chains (e mod 4), adds them as (c0 + c1) + (c2 + c3), the pair adds its two
+// halves (one shuffle), and each thread scales its half.
+template <int DK>
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total) {
+    constexpr int HALF = DK / 2;
+    const int p = threadIdx.x & 1;
+    for (int w0 = 0; w0 < 2 * total; w0 += THREADS / 2) {   // same trip count for every thread
+        const int w = w0 + (threadIdx.x >> 1);
+        const bool act = w < 2 * total;
+        float* x = (w & 1) ? steps[act ? w >> 1 : 0].k : steps[act ? w >> 1 : 0].q;
+        float* h = x + p * HALF;
+        float c[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) c[q4] = __fmul_rn(h[q4], h[q4]);
+#pragma unroll
+        for (int e = 4; e < HALF; e += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(h + e);
+            c[0] = __fmaf_rn(v.x, v.x, c[0]);
+            c[1] = __fmaf_rn(v.y, v.y, c[1]);
+            c[2] = __fmaf_rn(v.z, v.z, c[2]);
+            c[3] = __fmaf_rn(v.w, v.w, c[3]);
+        }
+        float ss = __fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3]));
+        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
+        const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ss, 1e-6f)));
+        if (!act) continue;
+#pragma unroll
+        for (int e = 0; e < HALF; e += 4) {
+            float4 v = *reinterpret_cast<const float4*>(h + e);
+            v.x = __fmul_rn(v.x, inv);
+            v.y = __fmul_rn(v.y, inv);
+            v.z = __fmul_rn(v.z, inv);
+            v.w = __fmul_rn(v.w, inv);
+            *reinterpret_cast<float4*>(h + e) = v;
+        }
     }
 }
 
-// The step function shared by decode, replay and verify.  s[] holds this
-// lane's EPL state entries of row `r`; kk/qq point at the staged step.
+// Sum over the LPR lanes of a row (xor 1, 2): every lane gets the same bits.
+__device__ __forceinline__ float row_sum(float v) {
+    v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
+    return v;
+}
+
+// Dot product of a lane's row slice with a staged vector: packed pair j = elements
+// (2j, 2j+1) of the slice; two packed accumulators over even and odd pairs, then
+// (A.x + A.y) + (B.x + B.y), then the lanes of the row.
+template <int NP>
+__device__ __forceinline__ float slice_dot(const float2 (&s)[NP], const float2 (&v)[NP]) {
+    float2 a = __fmul2_rn(s[0], v[0]);
+    float2 c = __fmul2_rn(s[1], v[1]);
+#pragma unroll
+    for (int j = 2; j < NP; j += 2) {
+        a = __ffma2_rn(s[j], v[j], a);
+        c = __ffma2_rn(s[j + 1], v[j + 1], c);
+    }
+    return row_sum(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(c.x, c.y)));
+}
+
+// Lane g of a row holds the 16-byte chunks g, g + LPR, g + 2 LPR, ... of the row.
 template <int DK>
-__device__ __forceinline__ float gdn_step(float (&s)[DK / 8], const StepSmem<DK>& in, int g, int r, bool want_o) {
-    constexpr int EPL = DK / 8;
-    float kk[EPL];
+__device__ __forceinline__ void load_slice(float2 (&d)[DK / (2 * LPR)], const float* src, int g) {
 #pragma unroll
-    for (int u = 0; u < EPL / 4; ++u) {
-        const float4 t = *reinterpret_cast<const float4*>(&in.k[4 * (g + 8 * u)]);
-        kk[4 * u] = t.x; kk[4 * u + 1] = t.y; kk[4 * u + 2] = t.z; kk[4 * u + 3] = t.w;
+    for (int u = 0; u < DK / (4 * LPR); ++u) {
+        const float4 t = *reinterpret_cast<const float4*>(src + 4 * (g + LPR * u));
+        d[2 * u] = make_float2(t.x, t.y);
+        d[2 * u + 1] = make_float2(t.z, t.w);
     }
-    const float a = in.gate, b = in.beta;
+}
+
+// The step function shared by decode, replay and verify, for this thread's RPT rows:
+//   S <- a S;  r = S k;  u = beta (v - r);  S <- S + u k^T;  o = S q
+// each operation rounded once (packed f32x2 lanes are independent IEEE fp32 ops).
+template <int DK>
+__device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const StepSmem<DK>& in, int g,
+                                         const int (&r)[RPT], bool want_o, float (&o)[RPT]) {
+    constexpr int NP = DK / (2 * LPR);
+    float2 kk[NP];
+    load_slice<DK>(kk, in.k, g);
+    const float2 a2 = make_float2(in.gate, in.gate);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) s[e] = __fmul_rn(a, s[e]);
-    float r0 = __fmul_rn(s[0], kk[0]), r1 = __fmul_rn(s[1], kk[1]);
+    for (int x = 0; x < RPT; ++x) {
 #pragma unroll
-    for (int e = 2; e < EPL; e += 2) {
-        r0 = __fmaf_rn(s[e], kk[e], r0);
-        r1 = __fmaf_rn(s[e + 1], kk[e + 1], r1);
+        for (int j = 0; j < NP; ++j) s[x][j] = __fmul2_rn(a2, s[x][j]);
     }
-    float rr = __fadd_rn(r0, r1);
-    rr = __fadd_rn(rr, __shfl_xor_sync(0xffffffffu, rr, 1));
-    rr = __fadd_rn(rr, __shfl_xor_sync(0xffffffffu, rr, 2));
-    rr = __fadd_rn(rr, __shfl_xor_sync(0xffffffffu, rr, 4));
-    const float uu = __fmul_rn(b, __fsub_rn(in.v[r], rr));
+    float rr[RPT];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) s[e] = __fmaf_rn(uu, kk[e], s[e]);
-    if (!want_o) return 0.f;
-    float qq[EPL];
+    for (int x = 0; x < RPT; ++x) rr[x] = slice_dot<NP>(s[x], kk);
 #pragma unroll
-    for (int u = 0; u < EPL / 4; ++u) {
-        const float4 t = *reinterpret_cast<const float4*>(&in.q[4 * (g + 8 * u)]);
-        qq[4 * u] = t.x; qq[4 * u + 1] = t.y; qq[4 * u + 2] = t.z; qq[4 * u + 3] = t.w;
+    for (int x = 0; x < RPT; ++x) {
+        const float uu = __fmul_rn(in.beta, __fsub_rn(in.v[r[x]], rr[x]));
+        const float2 u2 = make_float2(uu, uu);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) s[x][j] = __ffma2_rn(u2, kk[j], s[x][j]);
     }
-    float o0 = __fmul_rn(s[0], qq[0]), o1 = __fmul_rn(s[1], qq[1]);
+    if (!want_o) return;
+    float2 qq[NP];
+    load_slice<DK>(qq, in.q, g);
 #pragma unroll
-    for (int e = 2; e < EPL; e += 2) {
-        o0 = __fmaf_rn(s[e], qq[e], o0);
-        o1 = __fmaf_rn(s[e + 1], qq[e + 1], o1);
-    }
-    float oo = __fadd_rn(o0, o1);
-    oo = __fadd_rn(oo, __shfl_xor_sync(0xffffffffu, oo, 1));
-    oo = __fadd_rn(oo, __shfl_xor_sync(0xffffffffu, oo, 2));
-    oo = __fadd_rn(oo, __shfl_xor_sync(0xffffffffu, oo, 4));
-    return oo;
+    for (int x = 0; x < RPT; ++x) o[x] = slice_dot<NP>(s[x], qq);
 }
 
 template <int DK>
-__global__ void __launch_bounds__(THREADS) gdn_kernel(GdnArgs A) {
+__global__ void __launch_bounds__(THREADS, 8) gdn_kernel(GdnArgs A) {
     griddep_launch();
     griddep_wait();
-    constexpr int EPL = DK / 8;
+    constexpr int NP = DK / (2 * LPR);
     extern __shared__ __align__(16) uint8_t smem_raw[];
     StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw);
 
     const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = warp * 4 + (lane >> 3);        // row within the slab
-    const int g = lane & 7;                      // lane within the row group
+    const int g = lane % LPR;
+    int r[RPT];                                           // rows within the slab
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) r[x] = warp * ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
     const int row0 = slab * ROWS_PER_CTA;
-    const int i = row0 + r;                      // state row (v index)
 
+    // Loads in flight together: the first staging round (the step inputs gate the start of
+    // the recurrence), then the state rows, which arrive while the inputs are normalised.
+    const int total = A.max_commit + A.k;
+    constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
+    const int n_items = total * PER > 2 * total ? total * PER : 2 * total;
+    StageRound<DK> first;
+    first.issue(steps, A, b, h, row0, total, threadIdx.x);
+    float2 s[RPT][NP];
+#pragma unroll
+    for (int x = 0; x < RPT; ++x)
+        load_slice<DK>(s[x], A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0 + r[x]) * DK, g);
+    first.commit(steps, total);
+    for (int base = threadIdx.x + THREADS * STAGE_BATCH; base < n_items; base += THREADS * STAGE_BATCH) {
+        StageRound<DK> more;   // long verify blocks only: further rounds
+        more.issue(steps, A, b, h, row0, total, base);
+        more.commit(steps, total);
+    }
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
     if (nc < 0 || nc > A.max_commit) {
         if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
     }
-    const int total = nc + A.k;
-
-    // stage every step's inputs (warp w takes steps w, w+4, ...)
-    for (int t = warp; t < total; t += THREADS / 32) {
-        if (t < nc) stage_step<DK>(steps[t], A.pend, static_cast<long long>(b) * A.pend.rows_per_seq + t, h, A.dv, row0, A.l2, lane);
-        else stage_step<DK>(steps[t], A.draft, static_cast<long long>(b) * A.draft.rows_per_seq + (t - nc), h, A.dv, row0, A.l2, lane);
-    }
+    __syncthreads();
+    if (A.l2) normalise_all<DK>(steps, total);
     __syncthreads();
 
-    float* srow = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + i) * DK;
-    float s[EPL];
-#pragma unroll
-    for (int u = 0; u < EPL / 4; ++u) {
-        const float4 t = *reinterpret_cast<const float4*>(srow + 4 * (g + 8 * u));
-        s[4 * u] = t.x; s[4 * u + 1] = t.y; s[4 * u + 2] = t.z; s[4 * u + 3] = t.w;
-    }
-
+    float o[RPT];
     // replay the committed steps (these change the stored state)
     for (int t = 0; t < nc; ++t) {
-        const float o = gdn_step<DK>(s, steps[t], g, r, A.emit_replay != 0);
-        if (A.emit_replay && g == 0)
-            A.o[(static_cast<long long>(b) * nc + t) * A.o_stride + static_cast<long long>(h) * A.dv + i] = f32_to_bf16(o);
+        gdn_step<DK>(s, steps[t], g, r, A.emit_replay != 0, o);
+        if (A.emit_replay && g == 0) {
+#pragma unroll
+            for (int x = 0; x < RPT; ++x)
+                A.o[(static_cast<long long>(b) * nc + t) * A.o_stride + static_cast<long long>(h) * A.dv + row0 + r[x]] =
+                    f32_to_bf16(o[x]);
+        }
     }
     if (nc > 0) {
 #pragma unroll
-        for (int u = 0; u < EPL / 4; ++u)
-            *reinterpret_cast<float4*>(srow + 4 * (g + 8 * u)) = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+        for (int x = 0; x < RPT; ++x) {
+            float* srow = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0 + r[x]) * DK;
+#pragma unroll
+            for (int u = 0; u < NP / 2; ++u)
+                *reinterpret_cast<float4*>(srow + 4 * (g + LPR * u)) =
+                    make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
+        }
     }
     // speculative steps: outputs only, the state in memory stays committed
     for (int t = 0; t < A.k; ++t) {
-        const float o = gdn_step<DK>(s, steps[nc + t], g, r, true);
-        if (g == 0)
-            A.o[(static_cast<long long>(b) * A.k + t) * A.o_stride + static_cast<long long>(h) * A.dv + i] = f32_to_bf16(o);
+        gdn_step<DK>(s, steps[A.max_commit + t], g, r, true, o);
+        if (g == 0) {
+#pragma unroll
+            for (int x = 0; x < RPT; ++x)
+                A.o[(static_cast<long long>(b) * A.k + t) * A.o_stride + static_cast<long long>(h) * A.dv + row0 + r[x]] =
+                    f32_to_bf16(o[x]);
+        }
     }
 }
 
@@ -217,8 +339,15 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
               qk_l2norm ? 1 : 0, err};
     const int max_steps = max_commit + k;
-    dim3 grid(dv / ROWS_PER_CTA, H, B);
+    dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
     trace_pre(s);
+    static bool carve[2] = {false, false};
+    if (!carve[dk == 128]) {
+        // as much shared memory as possible for the carveout: 8 CTAs per SM need ~150 KB
+        if (dk == 128) cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        else cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        carve[dk == 128] = true;
+    }
     if (dk == 128) {
         const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
         launch_k(gdn_kernel<128>, dim3(grid), dim3(THREADS), sm, s, a);

@@ -22,6 +22,11 @@ def gdn_in_dim(cfg: dict) -> int:
     return cfg["gdn_heads"] * (2 * cfg["gdn_dk"] + cfg["gdn_dv"]) + 2 * cfg["gdn_heads"]
 
 
+def gdn_hist_stride(cfg: dict) -> int:
+    """Row stride of the GDN step-history buffers (the input width rounded up to 8)."""
+    return (gdn_in_dim(cfg) + 7) // 8 * 8
+
+
 def attn_in_dim(cfg: dict) -> int:
     return 2 * cfg["attn_hq"] * cfg["attn_hd"] + 2 * cfg["attn_hkv"] * cfg["attn_hd"]
 
@@ -49,7 +54,7 @@ class HybridStack:
                 h, dk, dv = cfg["gdn_heads"], cfg["gdn_dk"], cfg["gdn_dv"]
                 st[f"{l}.state"] = torch.zeros((B, h, dv, dk), dtype=torch.float32, device=d)
                 for p in (0, 1):
-                    st[f"{l}.hist{p}"] = torch.zeros((B * kmax, gdn_in_dim(cfg)), dtype=torch.int16, device=d)
+                    st[f"{l}.hist{p}"] = torch.zeros((B * kmax, gdn_hist_stride(cfg)), dtype=torch.int16, device=d)
                     st[f"{l}.gates{p}"] = torch.zeros((B * kmax, 2 * h), dtype=torch.int16, device=d)
             else:
                 shape = (B, cfg["attn_hkv"], Lmax, cfg["attn_hd"])

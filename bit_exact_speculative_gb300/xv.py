@@ -84,6 +84,7 @@ _SIGS = {
                              vp, c_ll, vp, c_ll, vp, c_sz, vp], c_int),
     "xv_kv_append": ([vp, c_ll, vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp], c_int),
     "xv_gdn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
+    "xv_gdn_hist_stride": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_attn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_block_workspace_size": ([ctypes.POINTER(BlockConfig), c_int, c_int, c_int], c_sz),
     "xv_verify_block": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState),

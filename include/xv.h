@@ -153,7 +153,8 @@ xv_status xv_gemm_small_m_noalloc(const uint16_t* X, int ldx, const uint16_t* W,
  *
  * Step inputs for a set of steps, row (b, t) at index b*rows_per_seq + t:
  *   q, k  [rows, H, dk] bf16 and v [rows, H, dv] bf16, consecutive rows
- *         qkv_stride elements apart (heads contiguous inside a row);
+ *         qkv_stride elements apart (heads contiguous inside a row); q, k
+ *         and v 16-byte aligned and qkv_stride a multiple of 8;
  *   beta, gate [rows, H] bf16 (beta = sigmoid(.), gate = exp(-softplus(.))
  *         already rounded to bf16), rows gate_stride elements apart.
  * With qk_l2norm != 0 the kernel normalises q and k per head in fp32
@@ -171,7 +172,7 @@ typedef struct {
 
 /* One decode step for B sequences: state [B, H, dv, dk] fp32 is updated in
  * place, o [B, H, dv] bf16 (row b at b*o_stride) receives o_t.
- * dk in {64, 128}; dv a multiple of 16; 1 <= B, 1 <= H. */
+ * dk in {64, 128}; dv a multiple of 32; 1 <= B, 1 <= H. */
 xv_status xv_gdn_decode_step(float* state, const xv_gdn_steps* step, uint16_t* o, long long o_stride,
                              int B, int H, int dk, int dv, int qk_l2norm, xv_stream s);
 
@@ -267,7 +268,7 @@ typedef struct {
 
 typedef struct {
     float* gdn_state;         /* GDN layer: [B, heads, dv, dk] fp32 */
-    uint16_t* gdn_hist[2];    /* GDN layer: two [B*kmax, gdn_in_dim] bf16 projection buffers */
+    uint16_t* gdn_hist[2];    /* GDN layer: two [B*kmax, xv_gdn_hist_stride(cfg)] bf16 projection buffers */
     uint16_t* gdn_gates[2];   /* GDN layer: two [B*kmax, 2*heads] bf16 (beta | gate) */
     uint16_t* k_cache;        /* attention layer: [B, Hkv, Lmax, hd] bf16 */
     uint16_t* v_cache;
@@ -285,6 +286,8 @@ typedef struct {
 } xv_block_state;
 
 int xv_gdn_in_dim(const xv_block_config* cfg);
+/* Row stride (elements) of the GDN step-history buffers: xv_gdn_in_dim rounded up to 8. */
+int xv_gdn_hist_stride(const xv_block_config* cfg);
 int xv_attn_in_dim(const xv_block_config* cfg);
 
 /* Workspace for xv_verify_block with B sequences of up to kmax tokens. */
