@@ -48,6 +48,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="launch kernels without programmatic dependent launch")
     ap.add_argument("--no-kernel-rooflines", action="store_true", help="skip the per-kernel measurements")
+    ap.add_argument("--kernel", choices=["gemm", "gdn", "attn"], default=None,
+                    help="time one hot kernel alone on one workload shape (for profiler captures) instead of the step")
+    ap.add_argument("--shape", default=None, help="with --kernel: gemm gdn_in|gdn_out|attn_in|attn_out|gate_up|down|"
+                    "lm_head (M = --batch * --k); gdn: B = --batch; attn: context --context, B = --batch")
+    ap.add_argument("--launches", type=int, default=4, help="with --kernel: launches to run")
     return ap.parse_args()
 
 
@@ -162,8 +167,10 @@ def gemm_shapes(cfg, M):
     return out
 
 
-def traffic_from_profile(kernel_src: str):
-    """ncu DRAM bytes per launch for the GEMM kernel, if the committed capture matches this source."""
+def traffic_ratio_from_profile(kernel_src: str):
+    """ncu DRAM bytes (read + write) per algorithmic byte of the GEMM kernel, from the committed
+    capture of one projection shape (profiles/traffic.json), if that capture matches this source;
+    else None.  The GEMM streams each weight once, so its traffic scales with the bytes it moves."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -173,7 +180,7 @@ def traffic_from_profile(kernel_src: str):
     e = d.get("gemm_small_m")
     if not e or e.get("source_sha") != h:
         return None
-    return e.get("dram_bytes_per_step")
+    return float(e["ratio"])
 
 
 # ------------------------------------------------------ per-kernel rooflines
@@ -285,6 +292,72 @@ def kernel_rooflines(xv, device, peak):
     return out
 
 
+# ------------------------------------------------------ one kernel alone
+
+GEMM_SHAPES = {"gdn_in": (12352, 5120), "gdn_out": (5120, 4096), "attn_in": (14336, 5120), "attn_out": (5120, 6144),
+               "gate_up": (34816, 5120), "down": (5120, 17408), "lm_head": (151936, 5120)}
+
+
+def run_one_kernel(args):
+    """--kernel: `launches` launches of one hot kernel on one stack shape, inputs resident (a fresh
+    weight or state copy per launch up to 3 copies), for profiler captures; prints one JSON line."""
+    import torch
+    from bit_exact_speculative_gb300 import build
+    from bit_exact_speculative_gb300 import xv
+    build.build()
+    device = torch.device("cuda", 0)
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+
+    def rnd(shape, scale=1.0):
+        return (torch.randn(shape, generator=g, device=device) * scale).to(torch.bfloat16)
+
+    B, k, n = args.batch, args.k, args.launches
+    if args.kernel == "gemm":
+        N, K = GEMM_SHAPES[args.shape]
+        M = B * k
+        Ws = [rnd((N, K), 0.02) for _ in range(3)]
+        X = rnd((M, K))
+        Y = torch.empty((M, N), dtype=torch.float32 if args.shape == "lm_head" else torch.bfloat16, device=device)
+        ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K), device=device)
+        launch = lambda i: xv.xv_gemm_small_m(X, Ws[i % 3], Y, ws)
+        desc = {"M": M, "N": N, "K": K}
+    elif args.kernel == "gdn":
+        H, D = 32, 128
+        states = [torch.randn((B, H, D, D), generator=g, device=device) * 0.1 for _ in range(3)]
+        qkv = rnd((B * k, H * 3 * D))
+        gates = torch.rand((B * k, 2 * H), generator=g, device=device).to(torch.bfloat16)
+        st = xv.gdn_steps(qkv, qkv[:, H * D:], qkv[:, 2 * H * D:], gates, gates[:, H:], 3 * H * D, 2 * H, k)
+        nc = torch.ones(B, dtype=torch.int32, device=device)
+        o = torch.empty((B * k, H * D), dtype=torch.bfloat16, device=device)
+        launch = lambda i: xv.xv_gdn_verify(states[i % 3], st, nc, k, st, k, o, H * D, B, H, D, D, True)
+        desc = {"B": B, "heads": H, "dk": D, "dv": D, "k": k}
+    else:
+        Hq, Hkv, hd, L = 24, 4, 256, args.context
+        Lmax = L + k
+        kcs = [rnd((B, Hkv, Lmax, hd)) for _ in range(2)]
+        vcs = [rnd((B, Hkv, Lmax, hd)) for _ in range(2)]
+        q = rnd((B * k, Hq * hd))
+        out = torch.empty((B * k, Hq * hd), dtype=torch.bfloat16, device=device)
+        ctx = torch.full((B,), L, dtype=torch.int32, device=device)
+        ws = xv.workspace(xv.xv_attn_workspace_size(B, k, Hq, hd, L + k - 1), device=device)
+        launch = lambda i: xv.xv_attn_decode_rows(q, q.stride(0), kcs[i % 2], vcs[i % 2], ctx, k, B, Hq, Hkv, hd, Lmax,
+                                                  L + k - 1, hd ** -0.5, out, out.stride(0), ws)
+        desc = {"B": B, "rows": k, "context": L, "hq": Hq, "hkv": Hkv, "hd": hd}
+    launch(0)   # the first launch also loads the module: not timed
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(1, n):
+        launch(i)
+    e1.record()
+    torch.cuda.synchronize()
+    code = xv.xv_device_check()
+    print(json.dumps({"kernel": args.kernel, "shape": args.shape, **desc, "launches": n,
+                      "us_per_launch": round(e0.elapsed_time(e1) / max(n - 1, 1) * 1e3, 2),
+                      "device_error_bits": code}), flush=True)
+
+
 # ------------------------------------------------------------ GPU arm
 
 def run_gpu(args):
@@ -368,7 +441,7 @@ def run_gpu(args):
     achieved = gemm_bytes_per_launch / (gemm_ms_per_launch / 1e3) / 1e9
     peak, peak_kind = peaks()
     gemm_bytes_step = sum(2 * N * K + 2 * B * k * K + B * k * N * o for N, K, o in gemm_shapes(cfg, B * k))
-    traffic_step = traffic_from_profile(os.path.join(ROOT, "bit_exact_speculative_gb300", "csrc", "gemm.cu"))
+    traffic_ratio = traffic_ratio_from_profile(os.path.join(ROOT, "bit_exact_speculative_gb300", "csrc", "gemm.cu"))
     n_gemm = len(gemm_shapes(cfg, B * k))
 
     # ---- end to end through the public API: pinned host tokens in, results out, every step
@@ -410,7 +483,9 @@ def run_gpu(args):
             "gpu_launches": int(launches),
             "roofline": {"bound": "hbm", "kernel": "gemm_small_m", "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": (round(traffic_step / n_gemm) if traffic_step else None),
+                         "traffic": (round(traffic_ratio * gemm_bytes_per_launch) if traffic_ratio else None),
+                         "traffic_source": ("ncu dram bytes per algorithmic byte of the down projection (M=8) "
+                                            "x this launch average" if traffic_ratio else None),
                          "algorithmic_bytes_per_launch": round(gemm_bytes_per_launch),
                          "launches_per_step": n_gemm, "ms_per_launch": round(gemm_ms_per_launch, 5)},
             "step_roofline": {"algorithmic_bytes": gemm_bytes_step,
@@ -502,6 +577,9 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.kernel:
+        run_one_kernel(args)
+        return
     if args.impl == "reference":
         out = run_reference(args)
         if out is not None:
