@@ -14,17 +14,17 @@
 // rounded once (explicit _rn intrinsics, so no contraction can differ):
 //     S <- a S;  r = S k;  u = b (v - r);  S <- S + u k^T;  o = S q.
 //
-// Tiling: a CTA owns (sequence b, head h, 32 state rows) with 64 threads; a
+// Tiling: a CTA owns (sequence b, head h, 32 state rows) with 128 threads; a
 // row is split over 4 consecutive lanes (lane g holds float4 chunks g, g+4,
-// g+8, ... of the row) and each thread carries 2 rows, so the staged k and q
-// slices are loaded once for both and the two rows' dependency chains run
-// side by side.  Row dot products: two packed f32x2 accumulators (even and
-// odd pairs), a fixed sum of their four lanes, then an xor-shuffle tree over
-// the row's 4 lanes (offsets 1, 2): every lane ends with the same bits.  The
-// state lives in registers across all replay and speculative steps; it is read
-// once (its loads issued before the step inputs are staged) and, after a
-// replay, written once.  All step inputs are staged in one round of
-// independent loads, then normalised from shared memory.
+// g+8, ... of the row).  Row dot products: two packed f32x2 accumulators (even
+// and odd pairs), a fixed sum of their four lanes, then an xor-shuffle tree
+// over the row's 4 lanes (offsets 1, 2): every lane ends with the same bits.
+// The state lives in registers across all replay and speculative steps; it is
+// read once (plain loads issued first) and, after a replay, written once.
+// The step inputs (per step: q and k of the head, this CTA's slice of v) come
+// by bulk asynchronous copies that one thread issues on one mbarrier, so the
+// whole verify's inputs arrive in a single round trip; beta and gate are plain
+// loads.  q and k are then L2-normalised by 4 threads per vector into fp32.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
@@ -32,11 +32,12 @@ namespace xv {
 
 namespace {
 constexpr int LPR = 4;                          // lanes per state row
-constexpr int RPT = 2;                          // state rows per thread
-constexpr int WARPS = 2;
-constexpr int ROWS_PER_WARP = 32 / LPR * RPT;   // 16
+constexpr int RPT = 1;                          // state rows per thread
+constexpr int WARPS = 4;
+constexpr int ROWS_PER_WARP = 32 / LPR * RPT;   // 8
 constexpr int ROWS_PER_CTA = ROWS_PER_WARP * WARPS;
 constexpr int THREADS = 32 * WARPS;
+constexpr int NORM_LANES = 4;                   // threads per q or k vector in the normalisation
 
 struct GdnArgs {
     float* state;
@@ -76,116 +77,74 @@ __device__ __forceinline__ const GdnStepsDev& step_src(const GdnArgs& A, int b, 
     return A.draft;
 }
 
-__device__ __forceinline__ void store8(float* dst, const uint4& v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float4 a = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
-                           __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
-    float4 b = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
-                           __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
-    *reinterpret_cast<float4*>(dst) = a;
-    *reinterpret_cast<float4*>(dst + 4) = b;
-}
-
-// Every step's raw inputs, converted to fp32 in shared memory.  q, k and this CTA's v slab
-// go as 16-byte chunks, STAGE_BATCH per thread issued back to back before any is used (one
-// round trip to memory for a verify's worth of steps); beta and gate are scalars.
-constexpr int STAGE_BATCH = 10;
-
+// Raw step inputs as they arrive: bf16 q and k of the head, then this CTA's bf16 slice of v.
 template <int DK>
-__device__ __forceinline__ const uint16_t* chunk_addr(const GdnArgs& A, int b, int h, int row0, int idx) {
-    constexpr int CH = DK / 8, VCH = ROWS_PER_CTA / 8, PER = 2 * CH + VCH;
-    const int t = idx / PER, j = idx - t * PER;
-    long long row;
-    const GdnStepsDev& src = step_src(A, b, t, &row);
-    const long long base = row * src.qkv_stride;
-    if (j < CH) return src.q + base + static_cast<long long>(h) * DK + 8 * j;
-    if (j < 2 * CH) return src.k + base + static_cast<long long>(h) * DK + 8 * (j - CH);
-    return src.v + base + static_cast<long long>(h) * A.dv + row0 + 8 * (j - 2 * CH);
-}
-
-// Shared-memory destination of chunk idx (q, k and v of a slot are contiguous floats).
-template <int DK>
-__device__ __forceinline__ float* chunk_dst(StepSmem<DK>* steps, int idx) {
-    constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
-    const int t = idx / PER, j = idx - t * PER;
-    return reinterpret_cast<float*>(&steps[t]) + 8 * j;
-}
-
-// One round of staging for thread slot `base`: issue() starts the loads (a beta/gate scalar
-// and up to STAGE_BATCH chunks) into registers, commit() converts and stores them.
-template <int DK>
-struct StageRound {
-    uint4 v[STAGE_BATCH];
-    uint16_t bg;
-    int base;
-
-    __device__ __forceinline__ void issue(StepSmem<DK>* steps, const GdnArgs& A, int b, int h, int row0, int total,
-                                          int base_) {
-        constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
-        base = base_;
-        const int n = total * PER;
-        if (base < 2 * total) {
-            long long row;
-            const GdnStepsDev& src = step_src(A, b, base >> 1, &row);
-            bg = (base & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
-        }
-#pragma unroll
-        for (int u = 0; u < STAGE_BATCH; ++u) {
-            const int idx = base + u * THREADS;
-            if (idx < n) v[u] = *reinterpret_cast<const uint4*>(chunk_addr<DK>(A, b, h, row0, idx));
-        }
-    }
-    __device__ __forceinline__ void commit(StepSmem<DK>* steps, int total) {
-        constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
-        const int n = total * PER;
-#pragma unroll
-        for (int u = 0; u < STAGE_BATCH; ++u)
-            if (base + u * THREADS < n) store8(chunk_dst<DK>(steps, base + u * THREADS), v[u]);
-        if (base < 2 * total) {
-            if (base & 1) steps[base >> 1].gate = bf16_to_f32(bg);
-            else steps[base >> 1].beta = bf16_to_f32(bg);
-        }
-    }
+struct StepRaw {
+    uint16_t q[DK];
+    uint16_t k[DK];
+    uint16_t v[ROWS_PER_CTA];
 };
+static_assert(sizeof(StepRaw<64>) % 16 == 0 && sizeof(StepRaw<128>) % 16 == 0, "bulk copies need 16-byte slots");
 
-// Per-head L2 normalisation of q and k in shared memory: x / sqrt(sum x^2 + 1e-6).
-// Vector w (slot w/2, q for even w, k for odd) belongs to the thread pair (2w', 2w'+1) with
-// w' = w mod (THREADS/2); thread p of the pair sums elements p*DK/2 .. (p+1)*DK/2 - 1 in four
-// interleaved chains (e mod 4), adds them as (c0 + c1) + (c2 + c3), the pair adds its two
-// halves (one shuffle), and each thread scales its half.
+__device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+
+// Global address of a step's q, k or v piece (all 16-byte aligned: checked by the callers).
+__device__ __forceinline__ const uint16_t* piece(const GdnStepsDev& src, long long row, int h, int dk, int dv,
+                                                 int row0, int which) {
+    const long long base = row * src.qkv_stride;
+    if (which == 0) return src.q + base + static_cast<long long>(h) * dk;
+    if (which == 1) return src.k + base + static_cast<long long>(h) * dk;
+    return src.v + base + static_cast<long long>(h) * dv + row0;
+}
+
+// Vector w of the staged steps (slot w / 2; q for even w, k for odd) to fp32, L2-normalised when
+// l2 (x / sqrt(sum x^2 + 1e-6)): thread j of the vector's group of NORM_LANES takes elements
+// [j DK/4, (j+1) DK/4), sums their squares in four interleaved chains (e mod 4) added as
+// (c0 + c1) + (c2 + c3), the group adds its partials by an xor tree (1, 2), and every thread
+// scales its own elements.
 template <int DK>
-__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total) {
-    constexpr int HALF = DK / 2;
-    const int p = threadIdx.x & 1;
-    for (int w0 = 0; w0 < 2 * total; w0 += THREADS / 2) {   // same trip count for every thread
-        const int w = w0 + (threadIdx.x >> 1);
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const StepRaw<DK>* raw, int total, bool l2) {
+    constexpr int PART = DK / NORM_LANES;
+    const int jl = threadIdx.x % NORM_LANES;
+    for (int w0 = 0; w0 < 2 * total; w0 += THREADS / NORM_LANES) {   // same trip count for every thread
+        const int w = w0 + static_cast<int>(threadIdx.x) / NORM_LANES;
         const bool act = w < 2 * total;
-        float* x = (w & 1) ? steps[act ? w >> 1 : 0].k : steps[act ? w >> 1 : 0].q;
-        float* h = x + p * HALF;
-        float c[4];
+        const int t = act ? w >> 1 : 0;
+        const uint16_t* x = ((w & 1) ? raw[t].k : raw[t].q) + jl * PART;
+        float* y = ((w & 1) ? steps[t].k : steps[t].q) + jl * PART;
+        float f[PART];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) c[q4] = __fmul_rn(h[q4], h[q4]);
+        for (int c = 0; c < PART / 8; ++c) {
+            const uint4 u = *reinterpret_cast<const uint4*>(x + 8 * c);
+            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int e = 4; e < HALF; e += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(h + e);
-            c[0] = __fmaf_rn(v.x, v.x, c[0]);
-            c[1] = __fmaf_rn(v.y, v.y, c[1]);
-            c[2] = __fmaf_rn(v.z, v.z, c[2]);
-            c[3] = __fmaf_rn(v.w, v.w, c[3]);
+            for (int e = 0; e < 4; ++e) {
+                f[8 * c + 2 * e] = __uint_as_float(wd[e] << 16);
+                f[8 * c + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+            }
         }
-        float ss = __fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3]));
-        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
-        const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ss, 1e-6f)));
+        float inv = 1.f;
+        if (l2) {
+            float c[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) c[q4] = __fmul_rn(f[q4], f[q4]);
+#pragma unroll
+            for (int e = 4; e < PART; e += 4) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) c[q4] = __fmaf_rn(f[e + q4], f[e + q4], c[q4]);
+            }
+            float ss = __fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3]));
+            ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
+            ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
+            inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ss, 1e-6f)));
+        }
         if (!act) continue;
 #pragma unroll
-        for (int e = 0; e < HALF; e += 4) {
-            float4 v = *reinterpret_cast<const float4*>(h + e);
-            v.x = __fmul_rn(v.x, inv);
-            v.y = __fmul_rn(v.y, inv);
-            v.z = __fmul_rn(v.z, inv);
-            v.w = __fmul_rn(v.w, inv);
-            *reinterpret_cast<float4*>(h + e) = v;
-        }
+        for (int e = 0; e < PART; e += 4)
+            *reinterpret_cast<float4*>(y + e) =
+                l2 ? make_float4(__fmul_rn(f[e], inv), __fmul_rn(f[e + 1], inv), __fmul_rn(f[e + 2], inv),
+                                 __fmul_rn(f[e + 3], inv))
+                   : make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
     }
 }
 
@@ -255,12 +214,15 @@ __device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const
 }
 
 template <int DK>
-__global__ void __launch_bounds__(THREADS, 8) gdn_kernel(GdnArgs A) {
+__global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
     griddep_launch();
-    griddep_wait();
     constexpr int NP = DK / (2 * LPR);
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw);
+    const int total = A.max_commit + A.k;
+    StepRaw<DK>* raw = reinterpret_cast<StepRaw<DK>*>(smem_raw);
+    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw + sizeof(StepRaw<DK>) * total);
+    __shared__ __align__(8) uint64_t bar_mem;
+    const uint32_t bar = smem_u32(&bar_mem);
 
     const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,31 +231,57 @@ __global__ void __launch_bounds__(THREADS, 8) gdn_kernel(GdnArgs A) {
 #pragma unroll
     for (int x = 0; x < RPT; ++x) r[x] = warp * ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
     const int row0 = slab * ROWS_PER_CTA;
+    float* srow0 = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0) * DK;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        l2_prefetch(srow0, ROWS_PER_CTA * DK * 4);   // a hint only: the loads come after the wait
+    }
+    __syncthreads();
+    griddep_wait();
 
-    // Loads in flight together: the first staging round (the step inputs gate the start of
-    // the recurrence), then the state rows, which arrive while the inputs are normalised.
-    const int total = A.max_commit + A.k;
-    constexpr int PER = 2 * (DK / 8) + ROWS_PER_CTA / 8;
-    const int n_items = total * PER > 2 * total ? total * PER : 2 * total;
-    StageRound<DK> first;
-    first.issue(steps, A, b, h, row0, total, threadIdx.x);
+    // Every load of the CTA in flight at once: first each thread's state row (the longest
+    // trip), then one thread's bulk copies of every step's q, k and v slice on one barrier,
+    // the commit count and one beta or gate scalar per thread (2 * total <= 2 * 32 <= THREADS).
     float2 s[RPT][NP];
 #pragma unroll
-    for (int x = 0; x < RPT; ++x)
-        load_slice<DK>(s[x], A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0 + r[x]) * DK, g);
-    first.commit(steps, total);
-    for (int base = threadIdx.x + THREADS * STAGE_BATCH; base < n_items; base += THREADS * STAGE_BATCH) {
-        StageRound<DK> more;   // long verify blocks only: further rounds
-        more.issue(steps, A, b, h, row0, total, base);
-        more.commit(steps, total);
+    for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], srow0 + static_cast<size_t>(r[x]) * DK, g);
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(sizeof(StepRaw<DK>)) * total);
+        for (int t = 0; t < total; ++t) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, t, &row);
+            const uint32_t d = smem_u32(&raw[t]);
+            bulk_load(d, piece(src, row, h, DK, A.dv, row0, 0), DK * 2, bar);
+            bulk_load(d + DK * 2, piece(src, row, h, DK, A.dv, row0, 1), DK * 2, bar);
+            bulk_load(d + DK * 4, piece(src, row, h, DK, A.dv, row0, 2), ROWS_PER_CTA * 2, bar);
+        }
     }
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
+    const int bg_idx = threadIdx.x;
+    uint16_t bg = 0;
+    if (bg_idx < 2 * total) {
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
+        bg = (bg_idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
+    }
+    const bool landed = mbar_wait(bar, 0, A.err);
+    if (!__syncthreads_and(landed)) {   // the same verdict for every thread
+        mbar_wait(bar, 0, A.err);       // the copies must land before the CTA may leave
+        return;
+    }
     if (nc < 0 || nc > A.max_commit) {
         if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
     }
-    __syncthreads();
-    if (A.l2) normalise_all<DK>(steps, total);
+    if (bg_idx < 2 * total) {
+        if (bg_idx & 1) steps[bg_idx >> 1].gate = bf16f(bg);
+        else steps[bg_idx >> 1].beta = bf16f(bg);
+    }
+    // v slices to fp32, q and k normalised
+    for (int idx = threadIdx.x; idx < total * ROWS_PER_CTA; idx += THREADS)
+        steps[idx / ROWS_PER_CTA].v[idx % ROWS_PER_CTA] = bf16f(raw[idx / ROWS_PER_CTA].v[idx % ROWS_PER_CTA]);
+    normalise_all<DK>(steps, raw, total, A.l2 != 0);
     __syncthreads();
 
     float o[RPT];
@@ -317,7 +305,9 @@ __global__ void __launch_bounds__(THREADS, 8) gdn_kernel(GdnArgs A) {
                     make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
         }
     }
-    // speculative steps: outputs only, the state in memory stays committed
+    // speculative steps: outputs only, the state in memory stays committed (unrolled by 2 so
+    // that one step's output product can overlap the next step's decay and key product)
+#pragma unroll 2
     for (int t = 0; t < A.k; ++t) {
         gdn_step<DK>(s, steps[A.max_commit + t], g, r, true, o);
         if (g == 0) {
@@ -339,20 +329,21 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
               qk_l2norm ? 1 : 0, err};
     const int max_steps = max_commit + k;
+    if (max_steps > THREADS / 2) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS / 2);
     dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
     trace_pre(s);
     static bool carve[2] = {false, false};
     if (!carve[dk == 128]) {
-        // as much shared memory as possible for the carveout: 8 CTAs per SM need ~150 KB
+        // as much shared memory as possible for the carveout: several CTAs per SM at B = 8
         if (dk == 128) cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         else cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         carve[dk == 128] = true;
     }
     if (dk == 128) {
-        const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
+        const size_t sm = (sizeof(StepRaw<128>) + sizeof(StepSmem<128>)) * (max_steps > 0 ? max_steps : 1);
         launch_k(gdn_kernel<128>, dim3(grid), dim3(THREADS), sm, s, a);
     } else {
-        const size_t sm = sizeof(StepSmem<64>) * (max_steps > 0 ? max_steps : 1);
+        const size_t sm = (sizeof(StepRaw<64>) + sizeof(StepSmem<64>)) * (max_steps > 0 ? max_steps : 1);
         launch_k(gdn_kernel<64>, dim3(grid), dim3(THREADS), sm, s, a);
     }
     // algorithmic bytes with every sequence replaying max_commit steps: the state

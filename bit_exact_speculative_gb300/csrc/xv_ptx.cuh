@@ -122,6 +122,13 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
         : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from global to shared memory, both 16-byte aligned,
+// completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 // L2 policy: lines brought in by this access are the first candidates for eviction.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
