@@ -137,7 +137,7 @@ static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv
     for (int l = 0; l < d.L; ++l) {
         const xv_layer_state& ls = st->layers[l];
         if (cfg->layer_kind[l] == 0) {
-            if (!ls.gdn_state || !ls.gdn_hist[0] || !ls.gdn_hist[1] || !ls.gdn_gates[0] || !ls.gdn_gates[1])
+            if (!ls.gdn_state || !ls.gdn_hist[0] || !ls.gdn_hist[1])
                 return fail(XV_ERR_ARG, "block: GDN layer %d state incomplete", l);
             if (!aligned16(ls.gdn_hist[0]) || !aligned16(ls.gdn_hist[1]))
                 return fail(XV_ERR_UNSUPPORTED, "block: GDN history buffers must be 16-byte aligned");
@@ -189,13 +189,14 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
         xv_layer_state& ls = st->layers[l];
         if (cfg->layer_kind[l] == 0) {
             uint16_t* hist = ls.gdn_hist[par];
-            uint16_t* gates = ls.gdn_gates[par];
             XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, hist, d.gstride, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-            XV_TRY(gdn_gates_launch(hist, d.gstride, d.gh * (2 * d.dk + d.dv), M, d.gh, gates, s));
+            // the recurrence kernel reads q, k, v and the raw b, a columns of the history rows
+            const int bc = d.gh * (2 * d.dk + d.dv);
             const uint16_t* ph = ls.gdn_hist[par ^ 1];
-            const uint16_t* pg = ls.gdn_gates[par ^ 1];
-            GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gstride, 2 * d.gh, st->pending_rows};
-            GdnStepsDev draft{hist, hist + d.gh * d.dk, hist + 2 * d.gh * d.dk, gates, gates + d.gh, d.gstride, 2 * d.gh, k};
+            GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, ph + bc, ph + bc + d.gh, d.gstride, d.gstride,
+                             st->pending_rows, 1};
+            GdnStepsDev draft{hist, hist + d.gh * d.dk, hist + 2 * d.gh * d.dk, hist + bc, hist + bc + d.gh, d.gstride,
+                              d.gstride, k, 1};
             XV_TRY(gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, draft, k, c.obuf, d.ginner, B,
                               d.gh, d.dk, d.dv, 1, s));
             XV_TRY(gemm_launch(c.obuf, d.ginner, lw.w_out, c.y, d.H, false, M, d.H, d.ginner, c.gemm_ws, c.gemm_ws_bytes, s));
@@ -257,8 +258,9 @@ xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stre
         if (cfg->layer_kind[l] != 0) continue;
         xv_layer_state& ls = st->layers[l];
         const uint16_t* ph = ls.gdn_hist[par ^ 1];
-        const uint16_t* pg = ls.gdn_gates[par ^ 1];
-        GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, pg, pg + d.gh, d.gstride, 2 * d.gh, st->pending_rows};
+        const int bc = d.gh * (2 * d.dk + d.dv);
+        GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, ph + bc, ph + bc + d.gh, d.gstride, d.gstride,
+                         st->pending_rows, 1};
         GdnStepsDev none{};
         if (xv_status e = gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, none, 0, nullptr, 0,
                                      st->B, d.gh, d.dk, d.dv, 1, s))

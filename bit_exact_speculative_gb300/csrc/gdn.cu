@@ -275,8 +275,16 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
         nc = nc < 0 ? 0 : A.max_commit;
     }
     if (bg_idx < 2 * total) {
-        if (bg_idx & 1) steps[bg_idx >> 1].gate = bf16f(bg);
-        else steps[bg_idx >> 1].beta = bf16f(bg);
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
+        float x = bf16f(bg);
+        if (src.raw_gates) {
+            // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
+            if (bg_idx & 1) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
+            else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
+        }
+        if (bg_idx & 1) steps[bg_idx >> 1].gate = x;
+        else steps[bg_idx >> 1].beta = x;
     }
     // v slices to fp32, q and k normalised
     for (int idx = threadIdx.x; idx < total * ROWS_PER_CTA; idx += THREADS)

@@ -1,5 +1,5 @@
 // Row-wise glue of the verify block: embedding gather, RMSNorm (fused with the
-// residual add), SwiGLU, GDN gates, argmax, greedy acceptance and commit.
+// residual add), SwiGLU, argmax, greedy acceptance and commit.
 //
 // Every kernel here computes each row from that row alone, with a reduction
 // tree fixed by the row length, so a row's bits do not depend on how many
@@ -134,21 +134,6 @@ __global__ void swiglu_kernel(const uint16_t* __restrict__ gu, int F, uint16_t* 
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(g[e], sigmoid_f(g[e])), u[e]);
     reinterpret_cast<uint4*>(act + row * F)[c] = pack8(o);
-}
-
-// beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
-__global__ void gdn_gates_kernel(const uint16_t* __restrict__ proj, long long stride, int b_col, int H,
-                                 uint16_t* __restrict__ gates) {
-    griddep_launch();
-    griddep_wait();
-    const long long m = blockIdx.x;
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        const float bb = bf16_to_f32(proj[m * stride + b_col + h]);
-        const float aa = bf16_to_f32(proj[m * stride + b_col + H + h]);
-        const float sp = aa > 20.f ? aa : log1pf(expf(aa));
-        gates[m * 2 * H + h] = f32_to_bf16(sigmoid_f(bb));
-        gates[m * 2 * H + H + h] = f32_to_bf16(expf(-sp));
-    }
 }
 
 // Argmax, lowest index among the maxima.  Pass 1: CTA (chunk, row) takes ARGMAX_CHUNK
@@ -291,13 +276,6 @@ xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStr
     trace_pre(s);
     launch_k(swiglu_kernel, grid, dim3(256), 0, s, gu, F, act);
     return launched("swiglu_kernel", s, K_SWIGLU, 6ll * M * F);
-}
-
-xv_status gdn_gates_launch(const uint16_t* proj, long long proj_stride, int b_col, int M, int H, uint16_t* gates,
-                           cudaStream_t s) {
-    trace_pre(s);
-    launch_k(gdn_gates_kernel, dim3(M), dim3(64), 0, s, proj, proj_stride, b_col, H, gates);
-    return launched("gdn_gates_kernel", s, K_GATES, 8ll * M * H);
 }
 
 size_t argmax_workspace_size(int M, int V) { return static_cast<size_t>(M) * ceil_div(V, ARGMAX_CHUNK) * sizeof(float2); }

@@ -90,6 +90,9 @@ struct GdnStepsDev {
     long long qkv_stride;
     long long gate_stride;
     int rows_per_seq;
+    // 0: beta and gate hold bf16 beta = sigmoid(b) and gate = exp(-softplus(a));
+    // 1: they point at the raw b and a projection columns and the kernel applies those maps
+    int raw_gates;
 };
 // Replays n_commit[b] (or n_fixed when n_commit is null) pending steps into
 // the state, writing o for them when emit_replay; then k speculative steps of
@@ -119,9 +122,6 @@ xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t
                                   uint16_t* xn, cudaStream_t s);
 // act[m][i] = bf16(silu(gu[m][i]) * gu[m][F + i])
 xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s);
-// gates[m] = [beta(H) | gate(H)] from the b and a columns of proj row m
-xv_status gdn_gates_launch(const uint16_t* proj, long long proj_stride, int b_col, int M, int H, uint16_t* gates,
-                           cudaStream_t s);
 size_t argmax_workspace_size(int M, int V);
 xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, void* ws, cudaStream_t s);
 xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s);

@@ -55,7 +55,6 @@ class HybridStack:
                 st[f"{l}.state"] = torch.zeros((B, h, dv, dk), dtype=torch.float32, device=d)
                 for p in (0, 1):
                     st[f"{l}.hist{p}"] = torch.zeros((B * kmax, gdn_hist_stride(cfg)), dtype=torch.int16, device=d)
-                    st[f"{l}.gates{p}"] = torch.zeros((B * kmax, 2 * h), dtype=torch.int16, device=d)
             else:
                 shape = (B, cfg["attn_hkv"], Lmax, cfg["attn_hd"])
                 st[f"{l}.kc"] = torch.zeros(shape, dtype=torch.int16, device=d)

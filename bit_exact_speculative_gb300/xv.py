@@ -49,7 +49,7 @@ class BlockWeights(ctypes.Structure):
 
 
 class LayerState(ctypes.Structure):
-    _fields_ = [("gdn_state", vp), ("gdn_hist", vp * 2), ("gdn_gates", vp * 2), ("k_cache", vp), ("v_cache", vp)]
+    _fields_ = [("gdn_state", vp), ("gdn_hist", vp * 2), ("k_cache", vp), ("v_cache", vp)]
 
 
 class BlockState(ctypes.Structure):
@@ -253,8 +253,8 @@ class Block:
     ``cfg`` is a dict (hidden, vocab, mlp, kinds, gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv,
     attn_hd, rms_eps); ``weights`` a dict of device tensors (embed, final_norm, lm_head and per
     layer ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``);
-    ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1``,
-    ``.gates0``, ``.gates1`` or ``.kc``, ``.vc``).  Tensors are kept referenced here.
+    ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1`` or
+    ``.kc``, ``.vc``).  Tensors are kept referenced here.
     """
 
     def __init__(self, cfg: dict, weights: dict, state: dict, B: int, kmax: int, Lmax: int, ctx0: int):
@@ -275,11 +275,9 @@ class Block:
             if kd == 0:
                 ls.append(LayerState(state[f"{l}.state"].data_ptr(),
                                      (vp * 2)(state[f"{l}.hist0"].data_ptr(), state[f"{l}.hist1"].data_ptr()),
-                                     (vp * 2)(state[f"{l}.gates0"].data_ptr(), state[f"{l}.gates1"].data_ptr()),
                                      None, None))
             else:
-                ls.append(LayerState(None, (vp * 2)(None, None), (vp * 2)(None, None), state[f"{l}.kc"].data_ptr(),
-                                     state[f"{l}.vc"].data_ptr()))
+                ls.append(LayerState(None, (vp * 2)(None, None), state[f"{l}.kc"].data_ptr(), state[f"{l}.vc"].data_ptr()))
         self._ls = (LayerState * len(kinds))(*ls)
         self.state = BlockState(B, kmax, Lmax, state["ctx_len"].data_ptr(), state["n_commit"].data_ptr(), 0, kmax,
                                 ctx0, 0, ctypes.cast(self._ls, vp).value)

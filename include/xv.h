@@ -269,7 +269,6 @@ typedef struct {
 typedef struct {
     float* gdn_state;         /* GDN layer: [B, heads, dv, dk] fp32 */
     uint16_t* gdn_hist[2];    /* GDN layer: two [B*kmax, xv_gdn_hist_stride(cfg)] bf16 projection buffers */
-    uint16_t* gdn_gates[2];   /* GDN layer: two [B*kmax, 2*heads] bf16 (beta | gate) */
     uint16_t* k_cache;        /* attention layer: [B, Hkv, Lmax, hd] bf16 */
     uint16_t* v_cache;
 } xv_layer_state;
