@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--shape", default=None, help="with --kernel: gemm gdn_in|gdn_out|attn_in|attn_out|gate_up|down|"
                     "lm_head (M = --batch * --k); gdn: B = --batch; attn: context --context, B = --batch")
     ap.add_argument("--launches", type=int, default=4, help="with --kernel: launches to run")
+    ap.add_argument("--speculative", type=float, default=None, metavar="ACCEPT",
+                    help="run greedy speculative decoding rounds (verify k, accept, commit) with a stand-in drafter "
+                         "whose drafts are right with probability ACCEPT, and report committed tokens per second")
+    ap.add_argument("--tokens", type=int, default=128, help="with --speculative: tokens to emit")
     return ap.parse_args()
 
 
@@ -127,27 +131,36 @@ def dist_env():
 
 # ----------------------------------------------------------------- setup
 
-def make_stack(args, device):
+def make_stack(args, device, rank=0, extra_rounds=0):
+    """The 4-layer stack with its weights (the same on every rank: replicas of one model) and
+    rank's own sequences (caches, GDN states and draft tokens from the rank's seed)."""
     import torch
     from synth import workloads
     from bit_exact_speculative_gb300.model import HybridStack
+    from bit_exact_speculative_gb300.replicas import rank_seed
 
     cfg = workloads.STACK
     w = workloads.weights(cfg, seed=0)
     wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
     B, k, L = args.batch, args.k, args.context
-    rounds = 3 * (args.steps + args.warmup) + 8
+    seq = rank_seed(0, rank)
+    rounds = 3 * (args.steps + args.warmup) + 8 + extra_rounds
     Lmax = L + k * rounds + 64
     stk = HybridStack(cfg, wd, B, k, Lmax, device=device)
-    for l, kd in enumerate(cfg["kinds"]):
-        if kd == 0:
-            stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, 0, l, B)))
-        else:
-            kc, vc = workloads.kv_cache(cfg, 0, l, B, [L] * B, Lmax)
-            stk.state[f"{l}.kc"].copy_(torch.from_numpy(kc.view(np.int16)))
-            stk.state[f"{l}.vc"].copy_(torch.from_numpy(vc.view(np.int16)))
-    stk.set_context([L] * B)
-    toks = np.stack([workloads.draft_tokens(cfg, 0, r, B, k) for r in range(rounds)])
+
+    def reset():
+        for l, kd in enumerate(cfg["kinds"]):
+            if kd == 0:
+                stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seq, l, B)))
+            else:
+                kc, vc = workloads.kv_cache(cfg, seq, l, B, [L] * B, Lmax)
+                stk.state[f"{l}.kc"].copy_(torch.from_numpy(kc.view(np.int16)))
+                stk.state[f"{l}.vc"].copy_(torch.from_numpy(vc.view(np.int16)))
+        stk.set_context([L] * B)
+
+    reset()
+    stk.reset = reset
+    toks = np.stack([workloads.draft_tokens(cfg, seq, r, B, k) for r in range(rounds)])
     return cfg, w, stk, toks
 
 
@@ -358,6 +371,52 @@ def run_one_kernel(args):
                       "device_error_bits": code}), flush=True)
 
 
+# ------------------------------------------------------- speculative rounds
+
+def run_speculative(args):
+    """Greedy speculative decoding of one sequence on the 4-layer stack: first the target's own
+    greedy decode (k = 1 steps) as the reference, then rounds of verify k / accept / commit from
+    the same state with drafts taken from that reference and corrupted at rate 1 - ACCEPT.  The
+    emitted tokens must equal the reference exactly; the metric is committed tokens per second."""
+    import torch
+    from bit_exact_speculative_gb300 import build
+    from bit_exact_speculative_gb300.speculative import ReplayDrafter, greedy_decode, speculative_decode
+    build.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    args.batch = 1
+    n, k = args.tokens, args.k
+    cfg, _, stk, toks = make_stack(args, device, 0, extra_rounds=(2 * n + 4 * k) // k + 1)
+    first = int(toks[0, 0, 0])
+    greedy_decode(stk, first, 4)                         # warm-up, then start over
+    stk.reset()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ref = greedy_decode(stk, first, n)
+    t_dec = time.perf_counter() - t0
+    stk.reset()
+    torch.cuda.synchronize()
+    drafter = ReplayDrafter(ref, cfg["vocab"], args.speculative, seed=1)
+    t0 = time.perf_counter()
+    emitted, accepted = speculative_decode(stk, first, n, k, drafter)
+    t_spec = time.perf_counter() - t0
+    exact = emitted[:n] == ref[1:n + 1]
+    value = len(emitted) / t_spec
+    print(json.dumps({
+        "metric": f"greedy speculative decode, committed tok/s (k={k}, 1 stream, draft acceptance {args.speculative})",
+        "value": round(value, 1), "unit": UNIT, "n_gpus": 1, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": WORKLOAD.replace("verify k=8 draft tokens, batch 1",
+                                                                      f"speculative rounds k={k}, batch 1"),
+                                        "tokens": len(emitted), "context": args.context},
+        "exact": bool(exact), "rounds": len(accepted),
+        "mean_accepted_drafts": round(float(np.mean(accepted)), 3),
+        "decode_tok_s": round(n / t_dec, 1), "speedup_vs_decode": round(value / (n / t_dec), 3),
+        "timing": "host wall clock, one synchronisation per round (the next round's first token is read back)"}),
+        flush=True)
+    if not exact:
+        raise SystemExit("speculative decoding diverged from the greedy decode")
+
+
 # ------------------------------------------------------------ GPU arm
 
 def run_gpu(args):
@@ -365,6 +424,7 @@ def run_gpu(args):
     import torch.distributed as dist
     from bit_exact_speculative_gb300 import build
     from bit_exact_speculative_gb300 import xv
+    from bit_exact_speculative_gb300.replicas import job_throughput
 
     rank, world, local = dist_env()
     if world > 1:
@@ -378,7 +438,7 @@ def run_gpu(args):
     xv.lib()
     xv.xv_set_overlap(not args.no_overlap)
 
-    cfg, w_host, stk, toks = make_stack(args, device)
+    cfg, w_host, stk, toks = make_stack(args, device, rank)
     B, k = args.batch, args.k
     tok_dev = torch.from_numpy(toks).to(device)
     stream = torch.cuda.current_stream()
@@ -414,11 +474,8 @@ def run_gpu(args):
         time.sleep(0.25)   # one more sample after the region
     launches = xv.xv_launch_count() - launches0
     ms = e0.elapsed_time(e1)
-    t = torch.tensor([ms], device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * B * k * args.steps / (ms_max / 1e3)
+    value, s_max, _ = job_throughput(ms / 1e3, B * k * args.steps, device)   # all ranks' tokens / slowest
+    ms_max = s_max * 1e3
     code = xv.xv_device_check()
 
     # ---- per-kernel durations: the same steps with every launch bracketed by events
@@ -460,11 +517,8 @@ def run_gpu(args):
         stk.commit()
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    t2 = torch.tensor([e2e_s], device=device)
-    if world > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-        barrier()
-    e2e_value = world * B * k * args.steps / float(t2.item())
+    e2e_value, _, _ = job_throughput(e2e_s, B * k * args.steps, device)
+    barrier()
 
     rooflines = None
     if rank == 0 and world == 1 and not args.no_kernel_rooflines:
@@ -579,6 +633,9 @@ def main():
     args = parse()
     if args.kernel:
         run_one_kernel(args)
+        return
+    if args.speculative is not None:
+        run_speculative(args)
         return
     if args.impl == "reference":
         out = run_reference(args)

@@ -93,3 +93,9 @@ class HybridStack:
     @property
     def max_ctx(self) -> int:
         return self.blk.state.max_ctx
+
+    def tighten_context(self, longest: int):
+        """Lowers the host bound on the committed lengths to ``longest``, the longest ctx_len the
+        caller has read back (a commit raises the bound by k whatever was accepted)."""
+        if longest < self.blk.state.max_ctx:
+            self.blk.state.max_ctx = int(longest)

@@ -279,7 +279,10 @@ typedef struct {
     int32_t* n_commit;        /* [B] device: pending GDN steps (set by commit) */
     int parity;               /* host: which history buffer the next verify writes */
     int pending_rows;         /* host: rows per sequence of the pending history (k of the last verify) */
-    int max_ctx;              /* host: upper bound of every ctx_len[b] (grid sizing) */
+    int max_ctx;              /* host: upper bound of every ctx_len[b] (grid sizing and the Lmax
+                                 check); a commit raises it by the verify's k, as the accepted
+                                 counts stay on the device; a caller that has read the lengths
+                                 back may lower it to their maximum (never below it) */
     int last_k;               /* host: k of the last verify not yet committed (0 = none) */
     xv_layer_state* layers;   /* HOST array [n_layers] */
 } xv_block_state;

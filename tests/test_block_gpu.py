@@ -204,3 +204,20 @@ def test_stack_long_context(stack):
     S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
     lgS, _ = sequential(S, toks, B)
     assert same_bits(lgA.view(B, k, -1), lgS)
+
+
+def test_stack_speculative_rounds_emit_greedy_decode(stack):
+    """Greedy speculative rounds (verify 8 / accept / commit) on the 4-layer stack emit exactly the
+    target's k=1 greedy decode, for drafts that are always, sometimes and never right."""
+    from bit_exact_speculative_gb300.speculative import ReplayDrafter, greedy_decode, speculative_decode
+    cfg, w, wd = stack
+    B, k, L, n = 1, 8, 2183, 40
+    Lmax = L + 3 * n + 4 * k
+    first = int(workloads.draft_tokens(cfg, 0, 77, 1, 1)[0, 0])
+    ref = greedy_decode(gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd), first, n)
+    for accept, lo, hi in [(1.0, 6.0, 7.0), (0.6, 0.1, 6.0), (0.0, 0.0, 0.0)]:
+        S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+        out, acc = speculative_decode(S, first, n, k, ReplayDrafter(ref, cfg["vocab"], accept, seed=3))
+        assert out[:n] == ref[1:n + 1], f"accept {accept}: emitted tokens differ from the greedy decode"
+        assert lo <= float(np.mean(acc)) <= hi, (accept, acc)
+        assert int(host(S.state["ctx_len"])[0]) == L + len(out)
