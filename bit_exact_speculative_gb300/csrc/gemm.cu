@@ -41,10 +41,6 @@ constexpr int TMEM_COLS = 64;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BN, GEMM_TOK);
 constexpr int SM_COUNT_TARGET = 152;   // GB300
-// K-blocks of its weight slice, beyond the first STAGES, that a CTA asks L2 to prefetch
-// before it waits for the previous kernel: while earlier kernels that move little data
-// run (GDN, attention, norms), HBM keeps streaming this GEMM's weights.
-constexpr int L2_PREFETCH_BLOCKS = 8;
 // Splits of 2..CLUSTER_MAX segments are combined inside a thread-block cluster through
 // distributed shared memory (no workspace); larger ones, used only by narrow shapes with
 // too few tiles to fill the GPU otherwise, go through the workspace.
@@ -55,8 +51,7 @@ template <bool F32OUT>
 __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         void* __restrict__ Y, int ldy, int M, int N, int nkb, int S, float* __restrict__ part,
-                        unsigned* __restrict__ cnt, unsigned* __restrict__ err, const uint16_t* __restrict__ W,
-                        int K, int cluster_combine) {
+                        unsigned* __restrict__ cnt, unsigned* __restrict__ err, int cluster_combine) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_last;
     const uint32_t raw = smem_u32(smem_raw);
@@ -124,18 +119,9 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
                 mbar_wait(full(j % STAGES), (j / STAGES) & 1u, err);
         }
     } else {
-        if (warp == 2) {
-            // L2 prefetch of the next K-blocks of this CTA's 128 weight rows (weights only)
-            const int k_first = kb0 + STAGES, k_last = min(kb1, kb0 + STAGES + L2_PREFETCH_BLOCKS);
-            if (k_first < k_last) {
-                const int k_end = min(k_last * GEMM_BK, K);
-                const uint32_t bytes = static_cast<uint32_t>(k_end - k_first * GEMM_BK) * 2u;
-                for (int r = lane; r < GEMM_BN; r += 32) {
-                    const int row = tile * GEMM_BN + r;
-                    if (row < N) l2_prefetch(W + static_cast<size_t>(row) * K + static_cast<size_t>(k_first) * GEMM_BK, bytes);
-                }
-            }
-        }
+        // An L2 prefetch of this CTA's K-blocks beyond the ring, issued here before the wait, was
+        // measured to slow the verify step down (897 -> 908 us with 8 blocks, 962 with 24): the
+        // ring's own early weight loads are the useful prefetch.
         griddep_wait();   // before any read or write of activations, partials or counters
     }
     if (warp == 1 && lane == 0) {
@@ -357,9 +343,9 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     trace_pre(s);
     if (cluster)
         launch_k_cluster(kern, grid, dim3(128), SMEM_BYTES, s, dim3(1, S, 1), tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt,
-                         err, W, K, cluster);
+                         err, cluster);
     else
-        launch_k(kern, grid, dim3(128), SMEM_BYTES, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, W, K, cluster);
+        launch_k(kern, grid, dim3(128), SMEM_BYTES, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster);
     const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
     return launched("gemm_small_m_kernel", s, K_GEMM, bytes);
 }
