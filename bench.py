@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--k", type=int, default=8)
     ap.add_argument("--context", type=int, default=2183)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lmax", type=int, default=None,
+                    help="KV-cache capacity per sequence (default: enough for every step the run makes)")
     ap.add_argument("--no-overlap", action="store_true", help="launch kernels without programmatic dependent launch")
     ap.add_argument("--no-kernel-rooflines", action="store_true", help="skip the per-kernel measurements")
     ap.add_argument("--kernel", choices=["gemm", "gdn", "attn"], default=None,
@@ -146,6 +148,10 @@ def make_stack(args, device, rank=0, extra_rounds=0):
     seq = rank_seed(0, rank)
     rounds = 3 * (args.steps + args.warmup) + 8 + extra_rounds
     Lmax = L + k * rounds + 64
+    if args.lmax:
+        if args.lmax < Lmax:
+            raise SystemExit(f"--lmax {args.lmax} is below the {Lmax} positions this run needs")
+        Lmax = args.lmax
     stk = HybridStack(cfg, wd, B, k, Lmax, device=device)
 
     def reset():
@@ -347,7 +353,7 @@ def run_one_kernel(args):
         desc = {"B": B, "heads": H, "dk": D, "dv": D, "k": k}
     else:
         Hq, Hkv, hd, L = 24, 4, 256, args.context
-        Lmax = L + k
+        Lmax = max(L + k, args.lmax or 0)
         kcs = [rnd((B, Hkv, Lmax, hd)) for _ in range(2)]
         vcs = [rnd((B, Hkv, Lmax, hd)) for _ in range(2)]
         q = rnd((B * k, Hq * hd))

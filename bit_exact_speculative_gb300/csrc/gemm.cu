@@ -35,10 +35,21 @@ namespace xv {
 namespace {
 constexpr int STAGES = 4;
 constexpr int A_BYTES = GEMM_BN * GEMM_BK * 2;   // 16 KB of weights per stage
-constexpr int B_BYTES = GEMM_TOK * GEMM_BK * 2;  //  8 KB of tokens per stage
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int B_BYTES = GEMM_TOK * GEMM_BK * 2;  //  8 KB: 64 token rows of one K-block
+// Token rows have a ring of their own.  For M > 8 it holds STAGES slots of 64 rows (8 KB) and
+// advances with the weights.  For M <= 8 a slot is the 8 rows of one K-block (one 1 KB swizzle
+// atom) and the ring has X_RING slots, so the tokens are requested up to X_RING - STAGES
+// K-blocks ahead of the weights: every CTA re-reads them from L2 on every stage, and measured
+// on GB300 that read stalls the 4-stage weight ring whenever the activation buffer sits at an
+// unlucky place in memory (up to +14% per GEMM).  The MMA still sees 64 token rows: its 8-row
+// groups all read the one atom (group stride 0), so columns 8..63 repeat columns 0..7.
+constexpr int X_RING = 16;
+constexpr int X_SMALL_M = 8;
+constexpr int N_BARS = 2 * STAGES + 2 * X_RING + 1;   // full, empty, xfull, xempty, done
 constexpr int TMEM_COLS = 64;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int smem_bytes(int xb, int xr) { return 1024 + STAGES * A_BYTES + xr * xb + 8 * N_BARS + 16; }
+constexpr int SMEM_MAX = smem_bytes(B_BYTES, STAGES) > smem_bytes(1024, X_RING) ? smem_bytes(B_BYTES, STAGES)
+                                                                                   : smem_bytes(1024, X_RING);
 constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BN, GEMM_TOK);
 constexpr int SM_COUNT_TARGET = 152;   // GB300
 // Splits of 2..CLUSTER_MAX segments are combined inside a thread-block cluster through
@@ -51,19 +62,23 @@ template <bool F32OUT>
 __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         void* __restrict__ Y, int ldy, int M, int N, int nkb, int S, float* __restrict__ part,
-                        unsigned* __restrict__ cnt, unsigned* __restrict__ err, int cluster_combine) {
+                        unsigned* __restrict__ cnt, unsigned* __restrict__ err, int cluster_combine, int xb,
+                        int xr) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_last;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw);
     const uint32_t sA = base;
-    const uint32_t sB = base + STAGES * A_BYTES;
-    const uint32_t bar0 = base + STAGES * STAGE_BYTES;      // full[STAGES], empty[STAGES], done
+    const uint32_t sX = base + STAGES * A_BYTES;            // token ring: xr slots of xb bytes
+    const uint32_t bar0 = sX + xr * xb;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t done = bar0 + 8u * (2 * STAGES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 1));
+    auto xfull = [&](int j) { return bar0 + 8u * (2 * STAGES + j); };
+    auto xempty = [&](int j) { return bar0 + 8u * (2 * STAGES + X_RING + j); };
+    const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * X_RING);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar0 - base) + 8 * N_BARS);
+    const uint32_t xgroup = xb == B_BYTES ? 1024u : 0u;   // 8-row group stride of the token operand
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, seg = blockIdx.y;
@@ -78,6 +93,10 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
+        }
+        for (int j = 0; j < xr; ++j) {
+            mbar_init(xfull(j), 1);
+            mbar_init(xempty(j), 1);
         }
         mbar_init(done, 1);
         fence_mbar_init();
@@ -99,24 +118,37 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
         const uint64_t stream_policy = l2_policy_evict_first();   // each weight is read once
         const int pre = nk < STAGES ? nk : STAGES;
         for (int i = 0; i < pre; ++i) {
-            mbar_arrive_expect_tx(full(i), STAGE_BYTES);
+            mbar_arrive_expect_tx(full(i), A_BYTES);
             tma_load_2d_hint(sA + i * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(i), stream_policy);
         }
         griddep_wait();
-        for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * B_BYTES, &tmX, (kb0 + i) * GEMM_BK, 0, full(i));
+        // token K-blocks up to (but not including) `lim`; slot reuse waits for the MMAs of the
+        // K-block xr earlier, never stricter than the weight ring's own wait
+        int xi = 0;
+        auto issue_x = [&](int lim) -> bool {
+            for (; xi < lim; ++xi) {
+                const int js = xi % xr;
+                if (xi >= xr && !mbar_wait(xempty(js), ((xi / xr) & 1u) ^ 1u, err)) return false;
+                mbar_arrive_expect_tx(xfull(js), xb);
+                tma_load_2d(sX + js * xb, &tmX, (kb0 + xi) * GEMM_BK, 0, xfull(js));
+            }
+            return true;
+        };
+        ok = issue_x(min(nk, xr));
         int issued = pre;
-        for (int i = pre; i < nk; ++i) {
+        for (int i = pre; ok && i < nk; ++i) {
             const int st = i % STAGES;
             const uint32_t ph = (i / STAGES) & 1u;
             if (i >= STAGES && !mbar_wait(empty(st), ph ^ 1u, err)) { ok = false; break; }
-            mbar_arrive_expect_tx(full(st), STAGE_BYTES);
+            mbar_arrive_expect_tx(full(st), A_BYTES);
             tma_load_2d_hint(sA + st * A_BYTES, &tmW, (kb0 + i) * GEMM_BK, tile * GEMM_BN, full(st), stream_policy);
-            tma_load_2d(sB + st * B_BYTES, &tmX, (kb0 + i) * GEMM_BK, 0, full(st));
             issued = i + 1;
+            ok = issue_x(min(nk, i + 1 + xr - STAGES));
         }
         if (!ok) {  // drain: every issued copy must land before the CTA may exit
             for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
                 mbar_wait(full(j % STAGES), (j / STAGES) & 1u, err);
+            for (int j = xi > xr ? xi - xr : 0; j < xi; ++j) mbar_wait(xfull(j % xr), (j / xr) & 1u, err);
         }
     } else {
         // An L2 prefetch of this CTA's K-blocks beyond the ring, issued here before the wait, was
@@ -127,17 +159,18 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     if (warp == 1 && lane == 0) {
         // ---- MMA issuer: 4 MMAs of K = 16 per stage, accumulate in TMEM
         for (int i = 0; i < nk; ++i) {
-            const int st = i % STAGES;
-            const uint32_t ph = (i / STAGES) & 1u;
-            if (!mbar_wait(full(st), ph, err)) { ok = false; break; }
+            const int st = i % STAGES, js = i % xr;
+            if (!mbar_wait(full(st), (i / STAGES) & 1u, err)) { ok = false; break; }
+            if (!mbar_wait(xfull(js), (i / xr) & 1u, err)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
                 const uint64_t ad = sw128_kmajor_desc(sA + st * A_BYTES + kk * 32);
-                const uint64_t bd = sw128_kmajor_desc(sB + st * B_BYTES + kk * 32);
+                const uint64_t bd = sw128_kmajor_desc(sX + js * xb + kk * 32, xgroup);
                 tc_mma_bf16(tmem, ad, bd, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
             }
-            tc_commit(empty(st));   // the stage is free once these MMAs have read it
+            tc_commit(empty(st));   // the stage and the token slot are free once these MMAs have read them
+            tc_commit(xempty(js));
         }
         tc_commit(done);            // all MMAs issued by this thread are complete
     }
@@ -277,13 +310,23 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 }  // namespace
 
+// Narrow shapes (at most half an SM's worth of tiles per SM) split K to fill the GPU; every wider
+// shape splits K in two.  Measured on the 17 GEMMs of a verify step (same GPU, back to back):
+// the two-way split of the gate/up projection (544 CTAs instead of 272, about 1.8 waves of 2 CTAs
+// per SM, so the hardware evens out SMs that stream at different rates) took the step from 895
+// to 862 us; two-way splits of the input projections (instead of 3 and 2) and of the LM head a
+// further 5 us; 3 or 4 segments, or clusters of up to 8 for the narrow shapes, were slower.
 int gemm_splits(int N, int K) {
     const int tiles = num_tiles(N);
     const int nkb = ceil_div(K, GEMM_BK);
-    int s = (SM_COUNT_TARGET * RESIDENT_PER_SM) / tiles;
-    if (s < 1) s = 1;
-    if (s > 16) s = 16;
-    if (s > CLUSTER_MAX && tiles * CLUSTER_MAX >= SM_COUNT_TARGET) s = CLUSTER_MAX;
+    int s;
+    if (2 * tiles > SM_COUNT_TARGET) {
+        s = 2;
+    } else {
+        s = (SM_COUNT_TARGET * RESIDENT_PER_SM) / tiles;
+        if (s > 16) s = 16;
+        if (s > CLUSTER_MAX && tiles * CLUSTER_MAX >= SM_COUNT_TARGET) s = CLUSTER_MAX;
+    }
     while (s > 1 && nkb / s < 4) --s;
     return s;
 }
@@ -318,7 +361,7 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
         const uint64_t strides[1] = {static_cast<uint64_t>(ldx) * 2};
-        const uint32_t box[2] = {GEMM_BK, GEMM_TOK};
+        const uint32_t box[2] = {GEMM_BK, static_cast<uint32_t>(M <= X_SMALL_M ? X_SMALL_M : GEMM_TOK)};
         if (xv_status st = encode_tiled(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dims, strides, box,
                                         CU_TENSOR_MAP_SWIZZLE_128B))
             return st;
@@ -333,19 +376,21 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     static bool attr_set[2] = {false, false};
     auto kern = f32out ? gemm_small_m_kernel<true> : gemm_small_m_kernel<false>;
     if (!attr_set[f32out]) {
-        if (xv_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES),
+        if (xv_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX),
                                       "gemm: set shared memory size"))
             return st;
         attr_set[f32out] = true;
     }
+    const int xb = M <= X_SMALL_M ? 1024 : B_BYTES, xr = M <= X_SMALL_M ? X_RING : STAGES;
+    const int smem = smem_bytes(xb, xr);
     dim3 grid(tiles, S);
     const int cluster = (S > 1 && S <= CLUSTER_MAX) ? 1 : 0;
     trace_pre(s);
     if (cluster)
-        launch_k_cluster(kern, grid, dim3(128), SMEM_BYTES, s, dim3(1, S, 1), tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt,
-                         err, cluster);
+        launch_k_cluster(kern, grid, dim3(128), smem, s, dim3(1, S, 1), tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt,
+                         err, cluster, xb, xr);
     else
-        launch_k(kern, grid, dim3(128), SMEM_BYTES, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster);
+        launch_k(kern, grid, dim3(128), smem, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster, xb, xr);
     const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
     return launched("gemm_small_m_kernel", s, K_GEMM, bytes);
 }

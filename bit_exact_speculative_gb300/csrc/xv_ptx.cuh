@@ -184,12 +184,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand stored with the
-// 128-byte swizzle (rows of 128 bytes, groups of 8 rows 1024 bytes apart).
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+// 128-byte swizzle (rows of 128 bytes, groups of 8 rows `group_stride` bytes
+// apart: 1024 for a dense tile; 0 makes every 8-row group read the first one).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr, uint32_t group_stride = 1024u) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);      // start address
     d |= static_cast<uint64_t>(16u >> 4) << 16;               // leading byte offset (unused for this layout)
-    d |= static_cast<uint64_t>(1024u >> 4) << 32;             // stride byte offset: next 8-row group
+    d |= static_cast<uint64_t>(group_stride >> 4) << 32;      // stride byte offset: next 8-row group
     d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
     d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
     return d;
