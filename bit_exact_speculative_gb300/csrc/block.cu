@@ -182,8 +182,7 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
     const int attn_len = st->max_ctx + k;   // bound on ctx_len + 1 + (k - 1)
 
 #define XV_TRY(expr) do { if (xv_status e_ = (expr)) return e_; } while (0)
-    XV_TRY(embed_launch(tokens, M, w->embed, d.V, d.H, c.x, s));
-    XV_TRY(rmsnorm_launch(c.x, w->layers[0].norm1, M, d.H, eps, c.xn, s));
+    XV_TRY(embed_rmsnorm_launch(tokens, M, w->embed, d.V, d.H, w->layers[0].norm1, eps, c.x, c.xn, s));
     for (int l = 0; l < d.L; ++l) {
         const xv_layer_weights& lw = w->layers[l];
         xv_layer_state& ls = st->layers[l];
@@ -217,8 +216,7 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
         XV_TRY(residual_rmsnorm_launch(c.x, c.y, next_norm, M, d.H, eps, c.xn, s));
     }
     XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-    XV_TRY(argmax_launch(lg, M, d.V, argmax, c.argmax_ws, s));
-    XV_TRY(accept_launch(tokens, argmax, B, k, n_accept, s));
+    XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, n_accept, s));
 #undef XV_TRY
     st->last_k = k;
     return XV_OK;

@@ -35,22 +35,8 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
     return r;
 }
 
-__global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ E, int V, int H,
-                             uint16_t* __restrict__ x, unsigned* err) {
-    griddep_launch();
-    griddep_wait();
-    const int m = blockIdx.x;
-    int t = tokens[m];
-    if (t < 0 || t >= V) {
-        if (threadIdx.x == 0) atomicOr(err, ERR_BAD_TOKEN);
-        t = 0;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(E + static_cast<long long>(t) * H);
-    uint4* dst = reinterpret_cast<uint4*>(x + static_cast<long long>(m) * H);
-    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
-}
-
-// y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ); with y_res != null first x <- bf16(x + y_res).
+// y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ); with y_res != null first x <- bf16(x + y_res);
+// with tokens != null the row is first gathered from the embedding, x <- E[tokens[row]].
 // One CTA per row; thread t owns the 8-element chunks t, t + blockDim, ... (at most NORM_MAXC),
 // so the per-thread sum order and the tree below are fixed by H alone.
 constexpr int NORM_MAXC = 4;
@@ -72,13 +58,23 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 
 __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x, const uint16_t* __restrict__ y_res,
                                                        const uint16_t* __restrict__ w, int H, float eps,
-                                                       uint16_t* __restrict__ out) {
+                                                       uint16_t* __restrict__ out, const int32_t* __restrict__ tokens,
+                                                       const uint16_t* __restrict__ E, int V, unsigned* err) {
     griddep_launch();
     griddep_wait();
     __shared__ float red[33];
     const long long row = blockIdx.x;
     const int nch = H / 8;
     uint4* xr = reinterpret_cast<uint4*>(x + row * H);
+    const uint4* src = xr;
+    if (tokens) {
+        int t = tokens[row];
+        if (t < 0 || t >= V) {
+            if (threadIdx.x == 0) atomicOr(err, ERR_BAD_TOKEN);
+            t = 0;
+        }
+        src = reinterpret_cast<const uint4*>(E + static_cast<long long>(t) * H);
+    }
     const uint4* yr = y_res ? reinterpret_cast<const uint4*>(y_res + row * H) : nullptr;
     float v[NORM_MAXC][8];
     float ss = 0.f;
@@ -87,7 +83,9 @@ __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x,
     for (int j = 0; j < NORM_MAXC; ++j) {
         const int c = threadIdx.x + j * blockDim.x;
         if (c < nch) {
-            unpack8(xr[c], v[j]);
+            const uint4 raw = src[c];
+            if (tokens) xr[c] = raw;
+            unpack8(raw, v[j]);
             if (yr) {
                 float t[8];
                 unpack8(yr[c], t);
@@ -193,30 +191,34 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_chunk_kernel(const floa
     }
 }
 
-__global__ void argmax_final_kernel(const float2* __restrict__ part, int nchunk, int32_t* __restrict__ idx) {
+// Pass 2 and the greedy acceptance of one sequence per CTA: warp j reduces the chunk results of
+// row b*k + j into idx[b*k + j]; then n_accept[b] = the number of leading drafts tokens[b][j+1]
+// equal to idx[b*k + j].
+__global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk, int k, int32_t* __restrict__ idx,
+                                     const int32_t* __restrict__ tokens, int32_t* __restrict__ n_accept) {
     griddep_launch();
     griddep_wait();
-    const long long row = blockIdx.x;
+    __shared__ int pred[XV_KMAX];
+    const int b = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(b) * k + j;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int c = threadIdx.x; c < nchunk; c += 32) {
+    for (int c = lane; c < nchunk; c += 32) {
         const float2 p = part[row * nchunk + c];
         better(bv, bi, p.x, __float_as_int(p.y));
     }
     warp_best(bv, bi);
-    if (threadIdx.x == 0) idx[row] = bi == 0x7fffffff ? 0 : bi;
-}
-
-// n_accept[b] = number of leading drafts tokens[b][j+1] equal to pred[b][j]
-__global__ void accept_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ pred, int B, int k,
-                              int32_t* __restrict__ n_accept) {
-    griddep_launch();
-    griddep_wait();
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    int n = 0;
-    while (n < k - 1 && pred[b * k + n] == tokens[b * k + n + 1]) ++n;
-    n_accept[b] = n;
+    if (lane == 0) {
+        const int id = bi == 0x7fffffff ? 0 : bi;
+        idx[row] = id;
+        pred[j] = id;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = 0;
+        while (n < k - 1 && pred[n] == tokens[static_cast<long long>(b) * k + n + 1]) ++n;
+        n_accept[b] = n;
+    }
 }
 
 __global__ void commit_kernel(const int32_t* __restrict__ keep, int keep_bias, int B, int k, int32_t* __restrict__ ctx_len,
@@ -243,13 +245,6 @@ __global__ void zero_i32_kernel(int32_t* p, int n) {
 
 }  // namespace
 
-xv_status embed_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, uint16_t* x, cudaStream_t s) {
-    unsigned* err = device_error_word();
-    if (!err) return fail(XV_ERR_CUDA, "embed: device error word unavailable");
-    trace_pre(s);
-    launch_k(embed_kernel, dim3(M), dim3(128), 0, s, tokens, E, V, H, x, err);
-    return launched("embed_kernel", s, K_EMBED, 4ll * M * H + 4ll * M);
-}
 
 static int norm_threads(int H) {
     int t = ((H / 8 + NORM_MAXC - 1) / NORM_MAXC + 31) / 32 * 32;
@@ -260,14 +255,24 @@ static int norm_threads(int H) {
 
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s) {
     trace_pre(s);
-    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y);
+    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y,
+             nullptr, nullptr, 0, nullptr);
     return launched("rmsnorm_kernel", s, K_RMSNORM, 4ll * M * H + 2ll * H);
+}
+
+xv_status embed_rmsnorm_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, const uint16_t* w,
+                               float eps, uint16_t* x, uint16_t* xn, cudaStream_t s) {
+    unsigned* err = device_error_word();
+    if (!err) return fail(XV_ERR_CUDA, "embed: device error word unavailable");
+    trace_pre(s);
+    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, x, nullptr, w, H, eps, xn, tokens, E, V, err);
+    return launched("rmsnorm_kernel(embed)", s, K_EMBED, 6ll * M * H + 2ll * H + 4ll * M);
 }
 
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps, uint16_t* xn,
                                   cudaStream_t s) {
     trace_pre(s);
-    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, x, y, w, H, eps, xn);
+    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, x, y, w, H, eps, xn, nullptr, nullptr, 0, nullptr);
     return launched("rmsnorm_kernel(residual)", s, K_RMSNORM, 8ll * M * H + 2ll * H);
 }
 
@@ -280,21 +285,18 @@ xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStr
 
 size_t argmax_workspace_size(int M, int V) { return static_cast<size_t>(M) * ceil_div(V, ARGMAX_CHUNK) * sizeof(float2); }
 
-xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, void* ws, cudaStream_t s) {
+xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
+                               const int32_t* tokens, int32_t* n_accept, cudaStream_t s) {
+    if (k < 1 || k > XV_KMAX) return fail(XV_ERR_ARG, "argmax: k = %d outside [1, %d]", k, XV_KMAX);
+    const int M = B * k;
     const int nchunk = ceil_div(V, ARGMAX_CHUNK);
     float2* part = static_cast<float2*>(ws);
     trace_pre(s);
     launch_k(argmax_chunk_kernel, dim3(nchunk, M), dim3(ARGMAX_THREADS), 0, s, logits, V, part, nchunk);
     if (xv_status st = launched("argmax_chunk_kernel", s, K_ARGMAX, 4ll * M * V)) return st;
     trace_pre(s);
-    launch_k(argmax_final_kernel, dim3(M), dim3(32), 0, s, part, nchunk, idx);
-    return launched("argmax_final_kernel", s, K_ARGMAX, 8ll * M * nchunk + 4ll * M);
-}
-
-xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s) {
-    trace_pre(s);
-    launch_k(accept_kernel, dim3(ceil_div(B, 128)), dim3(128), 0, s, tokens, pred, B, k, n_accept);
-    return launched("accept_kernel", s, K_ACCEPT, 8ll * B * k + 4ll * B);
+    launch_k(argmax_accept_kernel, dim3(B), dim3(32 * k), 0, s, part, nchunk, k, idx, tokens, n_accept);
+    return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
 }
 
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,

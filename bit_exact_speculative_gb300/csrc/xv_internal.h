@@ -115,16 +115,20 @@ xv_status kv_append_launch(const uint16_t* src, long long src_stride, const int3
                            int B, int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, cudaStream_t s);
 
 // ---- glue (glue.cu)
-xv_status embed_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, uint16_t* x, cudaStream_t s);
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s);
+// x[m] <- E[tokens[m]]; xn[m] = rmsnorm(x[m], w) (one kernel)
+xv_status embed_rmsnorm_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, const uint16_t* w,
+                               float eps, uint16_t* x, uint16_t* xn, cudaStream_t s);
 // x <- bf16(x + y); xn <- rmsnorm(x, w)
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps,
                                   uint16_t* xn, cudaStream_t s);
 // act[m][i] = bf16(silu(gu[m][i]) * gu[m][F + i])
 xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s);
 size_t argmax_workspace_size(int M, int V);
-xv_status argmax_launch(const float* logits, int M, int V, int32_t* idx, void* ws, cudaStream_t s);
-xv_status accept_launch(const int32_t* tokens, const int32_t* pred, int B, int k, int32_t* n_accept, cudaStream_t s);
+// idx[b*k + j] = argmax of logits row b*k + j (lowest index among equal maxima);
+// n_accept[b] = leading drafts tokens[b][j+1] equal to idx[b*k + j] (two kernels)
+xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
+                               const int32_t* tokens, int32_t* n_accept, cudaStream_t s);
 // ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (keep checked to lie in [1, k])
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,
                         cudaStream_t s);
