@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lmax", type=int, default=None,
                     help="KV-cache capacity per sequence (default: enough for every step the run makes)")
+    ap.add_argument("--page-size", type=int, default=None,
+                    help="paged KV cache with pages of this many positions (a multiple of 64)")
     ap.add_argument("--no-overlap", action="store_true", help="launch kernels without programmatic dependent launch")
     ap.add_argument("--no-kernel-rooflines", action="store_true", help="skip the per-kernel measurements")
     ap.add_argument("--kernel", choices=["gemm", "gdn", "attn"], default=None,
@@ -152,17 +154,22 @@ def make_stack(args, device, rank=0, extra_rounds=0):
         if args.lmax < Lmax:
             raise SystemExit(f"--lmax {args.lmax} is below the {Lmax} positions this run needs")
         Lmax = args.lmax
-    stk = HybridStack(cfg, wd, B, k, Lmax, device=device)
+    paged = {}
+    if args.page_size:
+        # a pool with room for every sequence at Lmax, its pages handed out in a seeded random order
+        n_pages = B * (-(-Lmax // args.page_size))
+        paged = dict(page_size=args.page_size, n_pages=n_pages,
+                     page_order=np.random.default_rng(seq).permutation(n_pages))
+    stk = HybridStack(cfg, wd, B, k, Lmax, device=device, **paged)
 
     def reset():
+        stk.set_context([L] * B)
         for l, kd in enumerate(cfg["kinds"]):
             if kd == 0:
                 stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seq, l, B)))
             else:
                 kc, vc = workloads.kv_cache(cfg, seq, l, B, [L] * B, Lmax)
-                stk.state[f"{l}.kc"].copy_(torch.from_numpy(kc.view(np.int16)))
-                stk.state[f"{l}.vc"].copy_(torch.from_numpy(vc.view(np.int16)))
-        stk.set_context([L] * B)
+                stk.load_kv(l, torch.from_numpy(kc.view(np.int16)), torch.from_numpy(vc.view(np.int16)))
 
     reset()
     stk.reset = reset
@@ -539,7 +546,9 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch_per_gpu": B, "k": k, "context": args.context,
-                       "parallelism": f"replicas x{world}", "overlap": not args.no_overlap, "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
+                       "parallelism": f"replicas x{world}", "overlap": not args.no_overlap,
+                       "kv_cache": f"paged, {args.page_size}-position pages" if args.page_size else "contiguous",
+                       "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
             "gpu_launches": int(launches),
             "roofline": {"bound": "hbm", "kernel": "gemm_small_m", "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -319,8 +319,43 @@ xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint1
         return st;
     size_t need = attn_workspace_size(B, R, Hq, hd, max_ctx);
     if (!ws || ws_bytes < need) return fail(XV_ERR_WORKSPACE, "attn: workspace of %zu bytes needed", need);
-    return attn_launch(q, q_stride, kc, vc, ctx_len, 0, R, B, Hq, Hkv, hd, Lmax, max_ctx, scale, gate, gate_stride, out,
-                       out_stride, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return attn_launch(q, q_stride, kc, vc, kv_contiguous(B, Lmax), ctx_len, 0, R, B, Hq, Hkv, hd, max_ctx, scale, gate,
+                       gate_stride, out, out_stride, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+// A page table and its sizes as the kernels take them; Lmax = the positions a sequence can hold.
+static xv_status kv_pages_check(const xv_kv_pages* pages, int Hkv, int hd, KvPages* kv, int* Lmax) {
+    if (!pages || !pages->page_table) return fail(XV_ERR_ARG, "paged KV: null page table");
+    if (pages->page_size < 64 || pages->page_size % 64)
+        return fail(XV_ERR_UNSUPPORTED, "paged KV: page_size must be a positive multiple of 64 (got %d)", pages->page_size);
+    if (pages->max_pages < 1 || pages->n_pages < 1) return fail(XV_ERR_ARG, "paged KV: max_pages and n_pages must be positive");
+    if (static_cast<long long>(pages->page_size) * pages->max_pages > (1ll << 30))
+        return fail(XV_ERR_UNSUPPORTED, "paged KV: page_size * max_pages exceeds 2^30 positions");
+    if (static_cast<long long>(pages->n_pages) * Hkv * pages->page_size * hd > (1ll << 40))
+        return fail(XV_ERR_UNSUPPORTED, "paged KV: pool too large");
+    if (static_cast<long long>(pages->n_pages) * Hkv > (1ll << 31)) return fail(XV_ERR_UNSUPPORTED, "paged KV: too many pages");
+    *kv = KvPages{pages->page_table, pages->page_size, pages->max_pages, pages->n_pages};
+    *Lmax = pages->page_size * pages->max_pages;
+    return XV_OK;
+}
+
+xv_status xv_attn_decode_rows_paged(const uint16_t* q, long long q_stride, const uint16_t* kpool, const uint16_t* vpool,
+                                    const xv_kv_pages* pages, const int32_t* ctx_len, int R, int B, int Hq, int Hkv,
+                                    int hd, int max_ctx, float scale, const uint16_t* gate, long long gate_stride,
+                                    uint16_t* out, long long out_stride, void* ws, size_t ws_bytes, xv_stream s) {
+    KvPages kv{};
+    int Lmax = 0;
+    if (xv_status st = kv_pages_check(pages, Hkv, hd, &kv, &Lmax)) return st;
+    // the pool is addressed as one cache of n_pages sequences of page_size positions
+    if (xv_status st = attn_checks(q, q_stride, kpool, vpool, ctx_len, R, 1, Hq, Hkv, hd, kv.page, R, gate, gate_stride,
+                                   out, out_stride))
+        return st;
+    if (B < 1 || B > 65535) return fail(XV_ERR_ARG, "attn: B must lie in [1, 65535]");
+    if (max_ctx < R || max_ctx > Lmax) return fail(XV_ERR_ARG, "attn: need R <= max_ctx <= page_size * max_pages");
+    size_t need = attn_workspace_size(B, R, Hq, hd, max_ctx);
+    if (!ws || ws_bytes < need) return fail(XV_ERR_WORKSPACE, "attn: workspace of %zu bytes needed", need);
+    return attn_launch(q, q_stride, kpool, vpool, kv, ctx_len, 0, R, B, Hq, Hkv, hd, max_ctx, scale, gate, gate_stride,
+                       out, out_stride, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 xv_status xv_kv_append(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B, int Hkv,
@@ -330,7 +365,21 @@ xv_status xv_kv_append(const uint16_t* kv_src, long long src_stride, const int32
     if (src_stride < 2ll * Hkv * hd) return fail(XV_ERR_ARG, "kv_append: src_stride below 2*Hkv*hd");
     if (!aligned16(kv_src) || (src_stride % 8) || !aligned16(kc) || !aligned16(vc))
         return fail(XV_ERR_UNSUPPORTED, "kv_append: 16-byte alignment required");
-    return kv_append_launch(kv_src, src_stride, ctx_len, -1, R, B, Hkv, hd, Lmax, kc, vc,
+    return kv_append_launch(kv_src, src_stride, ctx_len, -1, R, B, Hkv, hd, kv_contiguous(B, Lmax), kc, vc,
+                            reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_kv_append_paged(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B, int Hkv,
+                             int hd, const xv_kv_pages* pages, uint16_t* kpool, uint16_t* vpool, xv_stream s) {
+    if (!kv_src || !ctx_len || !kpool || !vpool) return fail(XV_ERR_ARG, "kv_append: null pointer");
+    if (R < 1 || B < 1 || Hkv < 1 || hd < 8 || hd % 8) return fail(XV_ERR_ARG, "kv_append: bad sizes");
+    KvPages kv{};
+    int Lmax = 0;
+    if (xv_status st = kv_pages_check(pages, Hkv, hd, &kv, &Lmax)) return st;
+    if (src_stride < 2ll * Hkv * hd) return fail(XV_ERR_ARG, "kv_append: src_stride below 2*Hkv*hd");
+    if (!aligned16(kv_src) || (src_stride % 8) || !aligned16(kpool) || !aligned16(vpool))
+        return fail(XV_ERR_UNSUPPORTED, "kv_append: 16-byte alignment required");
+    return kv_append_launch(kv_src, src_stride, ctx_len, -1, R, B, Hkv, hd, kv, kpool, vpool,
                             reinterpret_cast<cudaStream_t>(s));
 }
 

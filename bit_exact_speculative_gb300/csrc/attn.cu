@@ -19,8 +19,11 @@
 // is the dot product of its own row and column.
 //
 // Kernel 1 (attn_split_kernel), one CTA per (split, kv head, sequence):
-// K and V tiles arrive by TMA (3-D tensor map over [B*Hkv, Lmax, hd], 128-byte
-// swizzle) into a 3-stage shared-memory ring; QK^T and PV run on mma.sync
+// K and V tiles arrive by TMA (3-D tensor map over [pages*Hkv, page, hd], 128-byte
+// swizzle; a contiguous cache is one page of Lmax positions per sequence, a
+// paged one pages of a multiple of 64 positions, so a tile never straddles two
+// pages and the page a tile comes from changes nothing in its arithmetic)
+// into a 3-stage shared-memory ring; QK^T and PV run on mma.sync
 // m16n8k16 bf16 -> fp32 with P rounded to bf16; one warp owns 16 query rows.
 // Kernel 2 (attn_combine_kernel), one CTA per (row, q head): fixed-order
 // split combine, normalisation, optional output gate, bf16 store.
@@ -35,6 +38,23 @@ namespace {
 constexpr int T = ATTN_TILE;
 constexpr float NEG_INF = -INFINITY;
 
+// Page of position p of sequence b (row *row inside it); an entry outside the pool is
+// recorded and replaced by page 0, so no copy leaves the pool.  p < page * max_pages.
+__device__ __forceinline__ int kv_page(const KvPages& kv, int b, int p, int* row, unsigned* err) {
+    if (!kv.table) {
+        *row = p;
+        return b;
+    }
+    const int j = p / kv.page;
+    *row = p - j * kv.page;
+    int pg = kv.table[static_cast<long long>(b) * kv.max_pages + j];
+    if (pg < 0 || pg >= kv.n_pages) {
+        atomicOr(err, ERR_BAD_PAGE);
+        pg = 0;
+    }
+    return pg;
+}
+
 template <int HD>
 struct AttnShape {
     static constexpr int CB = HD / 64;                   // 128-byte column blocks per row
@@ -47,6 +67,7 @@ struct AttnShape {
 struct AttnArgs {
     const uint16_t* q;
     long long q_stride;
+    KvPages kv;
     const int32_t* ctx_len;
     int len_bias;
     int R, G, Hq, Hkv, nsplit, max_len;
@@ -89,20 +110,30 @@ __global__ void __launch_bounds__(128, 1)
     const int p_end = min(p_begin + ATTN_SPLIT, maxlen);
     const int ntiles = (p_end - p_begin + T - 1) / T;
 
+    // page and row of every tile of the split, looked up once by thread 0 (all loads in flight together)
+    __shared__ int tile_z[ATTN_SPLIT / T], tile_row[ATTN_SPLIT / T];
     auto issue = [&](int i) {
         const int st = i % STAGES;
         mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES);
-        const int p0 = p_begin + i * T, z = b * A.Hkv + g;
+        const int z = tile_z[i], row = tile_row[i];
 #pragma unroll
         for (int cb = 0; cb < CB; ++cb) {
-            tma_load_3d(sK(st) + cb * T * 128, &tmK, cb * 64, p0, z, full(st));
-            tma_load_3d(sV(st) + cb * T * 128, &tmV, cb * 64, p0, z, full(st));
+            tma_load_3d(sK(st) + cb * T * 128, &tmK, cb * 64, row, z, full(st));
+            tma_load_3d(sV(st) + cb * T * 128, &tmV, cb * 64, row, z, full(st));
         }
     };
     int issued = 0;   // tiles whose copies thread 0 has started
     if (tid == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+#pragma unroll
+        for (int i = 0; i < ATTN_SPLIT / T; ++i) {
+            if (i < ntiles) {
+                int row;
+                tile_z[i] = kv_page(A.kv, b, p_begin + i * T, &row, A.err) * A.Hkv + g;
+                tile_row[i] = row;
+            }
+        }
         for (int st = 0; st < STAGES; ++st) mbar_init(full(st), 1);
         fence_mbar_init();
         for (; issued < STAGES && issued < ntiles; ++issued) issue(issued);
@@ -321,15 +352,26 @@ __global__ void attn_combine_kernel(CombineArgs C) {
 }
 
 __global__ void kv_append_kernel(const uint16_t* __restrict__ src, long long src_stride, const int32_t* __restrict__ ctx_len,
-                                 int pos_bias, int R, int Hkv, int hd, int Lmax, uint16_t* __restrict__ kc,
+                                 int pos_bias, int R, int Hkv, int hd, KvPages kv, uint16_t* __restrict__ kc,
                                  uint16_t* __restrict__ vc, unsigned* err) {
     griddep_launch();
     griddep_wait();
     const int row = blockIdx.x, b = row / R, r = row % R;
     const int pos = ctx_len[b] + pos_bias + r;
-    if (pos < 0 || pos >= Lmax) {
+    if (pos < 0 || pos >= kv.page * kv.max_pages) {
         if (threadIdx.x == 0) atomicOr(err, ERR_BAD_LENGTH);
         return;
+    }
+    int prow = pos;
+    int pg = b;
+    if (kv.table) {
+        const int j = pos / kv.page;
+        prow = pos - j * kv.page;
+        pg = kv.table[static_cast<long long>(b) * kv.max_pages + j];
+        if (pg < 0 || pg >= kv.n_pages) {
+            if (threadIdx.x == 0) atomicOr(err, ERR_BAD_PAGE);
+            return;
+        }
     }
     const int chunks = Hkv * hd / 8;
     for (int c = threadIdx.x; c < 2 * chunks; c += blockDim.x) {
@@ -337,7 +379,7 @@ __global__ void kv_append_kernel(const uint16_t* __restrict__ src, long long src
         const int cc = is_v ? c - chunks : c;
         const int h = cc / (hd / 8), d = (cc % (hd / 8)) * 8;
         const uint4 v = *reinterpret_cast<const uint4*>(src + row * src_stride + (is_v ? Hkv * hd : 0) + h * hd + d);
-        uint16_t* dst = (is_v ? vc : kc) + ((static_cast<long long>(b) * Hkv + h) * Lmax + pos) * hd + d;
+        uint16_t* dst = (is_v ? vc : kc) + ((static_cast<long long>(pg) * Hkv + h) * kv.page + prow) * hd + d;
         *reinterpret_cast<uint4*>(dst) = v;
     }
 }
@@ -378,16 +420,17 @@ size_t attn_workspace_size(int B, int R, int Hq, int hd, int max_len) {
     return round256(rows * hd * sizeof(float)) + round256(rows * sizeof(float2));
 }
 
-xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
-                      const int32_t* ctx_len, int len_bias, int R, int B, int Hq, int Hkv, int hd, int Lmax, int max_len,
+xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc, const KvPages& kv,
+                      const int32_t* ctx_len, int len_bias, int R, int B, int Hq, int Hkv, int hd, int max_len,
                       float scale, const uint16_t* gate, long long gate_stride, uint16_t* out, long long out_stride,
                       void* ws, size_t ws_bytes, cudaStream_t s) {
     (void)ws_bytes;
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "attn: device error word unavailable");
     CUtensorMap tmK, tmV;
-    const uint64_t dims[3] = {static_cast<uint64_t>(hd), static_cast<uint64_t>(Lmax), static_cast<uint64_t>(B) * Hkv};
-    const uint64_t strides[2] = {static_cast<uint64_t>(hd) * 2, static_cast<uint64_t>(Lmax) * hd * 2};
+    const uint64_t dims[3] = {static_cast<uint64_t>(hd), static_cast<uint64_t>(kv.page),
+                              static_cast<uint64_t>(kv.n_pages) * Hkv};
+    const uint64_t strides[2] = {static_cast<uint64_t>(hd) * 2, static_cast<uint64_t>(kv.page) * hd * 2};
     const uint32_t box[3] = {64, static_cast<uint32_t>(T), 1};
     if (xv_status st = encode_tiled(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return st;
@@ -397,7 +440,7 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
     const size_t rows = static_cast<size_t>(B) * R * Hq * nsplit;
     float* opart = static_cast<float*>(ws);
     float2* ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + round256(rows * hd * sizeof(float)));
-    AttnArgs a{q, q_stride, ctx_len, len_bias, R, Hq / Hkv, Hq, Hkv, nsplit, max_len,
+    AttnArgs a{q, q_stride, kv, ctx_len, len_bias, R, Hq / Hkv, Hq, Hkv, nsplit, max_len,
                scale * 1.4426950408889634f, opart, ml, err};
     xv_status st = hd == 256 ? launch_split<256>(tmK, tmV, a, B, s) : launch_split<64>(tmK, tmV, a, B, s);
     if (st) return st;
@@ -409,11 +452,11 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
 }
 
 xv_status kv_append_launch(const uint16_t* src, long long src_stride, const int32_t* ctx_len, int pos_bias, int R, int B,
-                           int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, cudaStream_t s) {
+                           int Hkv, int hd, const KvPages& kv, uint16_t* kc, uint16_t* vc, cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "kv_append: device error word unavailable");
     trace_pre(s);
-    launch_k(kv_append_kernel, dim3(B * R), dim3(128), 0, s, src, src_stride, ctx_len, pos_bias, R, Hkv, hd, Lmax, kc, vc, err);
+    launch_k(kv_append_kernel, dim3(B * R), dim3(128), 0, s, src, src_stride, ctx_len, pos_bias, R, Hkv, hd, kv, kc, vc, err);
     return launched("kv_append_kernel", s, K_KV_APPEND, 8ll * B * R * Hkv * hd);
 }
 

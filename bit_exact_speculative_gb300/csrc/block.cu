@@ -134,6 +134,15 @@ static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv
     if (!st || !st->ctx_len || !st->n_commit || !st->layers) return fail(XV_ERR_ARG, "block: incomplete state");
     if (st->B < 1 || st->kmax < 1 || st->kmax > XV_KMAX || st->Lmax < 1)
         return fail(XV_ERR_ARG, "block: state needs B >= 1, 1 <= kmax <= %d, Lmax >= 1", XV_KMAX);
+    const xv_kv_pages& pg = st->kv_pages;
+    if (pg.page_table) {
+        if (pg.page_size < 64 || pg.page_size % 64 || pg.max_pages < 1 || pg.n_pages < 1)
+            return fail(XV_ERR_ARG, "block: paged KV needs page_size a positive multiple of 64, max_pages, n_pages >= 1");
+        if (static_cast<long long>(pg.page_size) * pg.max_pages < st->Lmax)
+            return fail(XV_ERR_ARG, "block: Lmax exceeds page_size * max_pages");
+        if (static_cast<long long>(pg.n_pages) * d.hkv > (1ll << 31))
+            return fail(XV_ERR_UNSUPPORTED, "block: too many KV pages");
+    }
     for (int l = 0; l < d.L; ++l) {
         const xv_layer_state& ls = st->layers[l];
         if (cfg->layer_kind[l] == 0) {
@@ -150,9 +159,14 @@ static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv
     return XV_OK;
 }
 
-xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
-                          const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept, void* ws,
-                          size_t ws_bytes, xv_stream stream) {
+static KvPages state_pages(const xv_block_state* st) {
+    const xv_kv_pages& pg = st->kv_pages;
+    return pg.page_table ? KvPages{pg.page_table, pg.page_size, pg.max_pages, pg.n_pages} : kv_contiguous(st->B, st->Lmax);
+}
+
+xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                                 const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
+                                 int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream) {
     Dims d{};
     if (xv_status e = check_cfg(cfg, &d)) return e;
     if (xv_status e = check_state(d, cfg, st)) return e;
@@ -180,6 +194,7 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
     const float eps = cfg->rms_eps;
     const int par = st->parity & 1;
     const int attn_len = st->max_ctx + k;   // bound on ctx_len + 1 + (k - 1)
+    const KvPages kv = state_pages(st);
 
 #define XV_TRY(expr) do { if (xv_status e_ = (expr)) return e_; } while (0)
     XV_TRY(embed_rmsnorm_launch(tokens, M, w->embed, d.V, d.H, w->layers[0].norm1, eps, c.x, c.xn, s));
@@ -201,9 +216,9 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
             XV_TRY(gemm_launch(c.obuf, d.ginner, lw.w_out, c.y, d.H, false, M, d.H, d.ginner, c.gemm_ws, c.gemm_ws_bytes, s));
         } else {
             XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, c.proj, d.ain, false, M, d.ain, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-            XV_TRY(kv_append_launch(c.proj + 2 * d.ainner, d.ain, st->ctx_len, 0, k, B, d.hkv, d.hd, st->Lmax, ls.k_cache,
+            XV_TRY(kv_append_launch(c.proj + 2 * d.ainner, d.ain, st->ctx_len, 0, k, B, d.hkv, d.hd, kv, ls.k_cache,
                                     ls.v_cache, s));
-            XV_TRY(attn_launch(c.proj, d.ain, ls.k_cache, ls.v_cache, st->ctx_len, 1, k, B, d.hq, d.hkv, d.hd, st->Lmax,
+            XV_TRY(attn_launch(c.proj, d.ain, ls.k_cache, ls.v_cache, kv, st->ctx_len, 1, k, B, d.hq, d.hkv, d.hd,
                                attn_len, 1.0f / sqrtf(static_cast<float>(d.hd)), c.proj + d.ainner, d.ain, c.obuf,
                                d.ainner, c.attn_ws, c.attn_ws_bytes, s));
             XV_TRY(gemm_launch(c.obuf, d.ainner, lw.w_out, c.y, d.H, false, M, d.H, d.ainner, c.gemm_ws, c.gemm_ws_bytes, s));
@@ -216,33 +231,44 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
         XV_TRY(residual_rmsnorm_launch(c.x, c.y, next_norm, M, d.H, eps, c.xn, s));
     }
     XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-    XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, n_accept, s));
+    XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
 #undef XV_TRY
     st->last_k = k;
+    st->last_k_seq = k_seq;
     return XV_OK;
+}
+
+xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                          const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept, void* ws,
+                          size_t ws_bytes, xv_stream stream) {
+    return xv_verify_block_ragged(cfg, w, st, tokens, k, nullptr, logits, argmax, n_accept, ws, ws_bytes, stream);
 }
 
 xv_status xv_block_commit(xv_block_state* st, const int32_t* n_keep, xv_stream stream) {
     if (!st || !st->ctx_len || !st->n_commit || !n_keep) return fail(XV_ERR_ARG, "commit: null argument");
     if (st->last_k < 1) return fail(XV_ERR_ARG, "commit: no verify to commit");
-    xv_status e = commit_launch(n_keep, 0, st->B, st->last_k, st->ctx_len, st->n_commit, reinterpret_cast<cudaStream_t>(stream));
+    xv_status e = commit_launch(n_keep, 0, st->B, st->last_k, st->last_k_seq, st->ctx_len, st->n_commit,
+                                reinterpret_cast<cudaStream_t>(stream));
     if (e) return e;
     st->parity ^= 1;
     st->pending_rows = st->last_k;
     st->max_ctx += st->last_k;
     st->last_k = 0;
+    st->last_k_seq = nullptr;
     return XV_OK;
 }
 
 xv_status xv_block_commit_accepted(xv_block_state* st, const int32_t* n_accept, xv_stream stream) {
     if (!st || !st->ctx_len || !st->n_commit || !n_accept) return fail(XV_ERR_ARG, "commit: null argument");
     if (st->last_k < 1) return fail(XV_ERR_ARG, "commit: no verify to commit");
-    xv_status e = commit_launch(n_accept, 1, st->B, st->last_k, st->ctx_len, st->n_commit, reinterpret_cast<cudaStream_t>(stream));
+    xv_status e = commit_launch(n_accept, 1, st->B, st->last_k, st->last_k_seq, st->ctx_len, st->n_commit,
+                                reinterpret_cast<cudaStream_t>(stream));
     if (e) return e;
     st->parity ^= 1;
     st->pending_rows = st->last_k;
     st->max_ctx += st->last_k;
     st->last_k = 0;
+    st->last_k_seq = nullptr;
     return XV_OK;
 }
 

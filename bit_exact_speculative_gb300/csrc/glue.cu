@@ -193,9 +193,10 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_chunk_kernel(const floa
 
 // Pass 2 and the greedy acceptance of one sequence per CTA: warp j reduces the chunk results of
 // row b*k + j into idx[b*k + j]; then n_accept[b] = the number of leading drafts tokens[b][j+1]
-// equal to idx[b*k + j].
+// equal to idx[b*k + j], over the sequence's own k_b <= k rows.
 __global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk, int k, int32_t* __restrict__ idx,
-                                     const int32_t* __restrict__ tokens, int32_t* __restrict__ n_accept) {
+                                     const int32_t* __restrict__ tokens, const int32_t* __restrict__ k_seq,
+                                     int32_t* __restrict__ n_accept, unsigned* err) {
     griddep_launch();
     griddep_wait();
     __shared__ int pred[XV_KMAX];
@@ -215,22 +216,39 @@ __global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        int kb = k;
+        if (k_seq) {
+            kb = k_seq[b];
+            if (kb < 1 || kb > k) {
+                atomicOr(err, ERR_BAD_COUNT);
+                kb = kb < 1 ? 1 : k;
+            }
+        }
         int n = 0;
-        while (n < k - 1 && pred[n] == tokens[static_cast<long long>(b) * k + n + 1]) ++n;
+        while (n < kb - 1 && pred[n] == tokens[static_cast<long long>(b) * k + n + 1]) ++n;
         n_accept[b] = n;
     }
 }
 
-__global__ void commit_kernel(const int32_t* __restrict__ keep, int keep_bias, int B, int k, int32_t* __restrict__ ctx_len,
+__global__ void commit_kernel(const int32_t* __restrict__ keep, int keep_bias, int B, int k,
+                              const int32_t* __restrict__ k_seq, int32_t* __restrict__ ctx_len,
                               int32_t* __restrict__ n_commit, unsigned* err) {
     griddep_launch();
     griddep_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
+    int kb = k;
+    if (k_seq) {
+        kb = k_seq[b];
+        if (kb < 1 || kb > k) {
+            atomicOr(err, ERR_BAD_COUNT);
+            kb = kb < 1 ? 1 : k;
+        }
+    }
     int n = keep[b] + keep_bias;
-    if (n < 1 || n > k) {
+    if (n < 1 || n > kb) {
         atomicOr(err, ERR_BAD_COUNT);
-        n = n < 1 ? 1 : k;
+        n = n < 1 ? 1 : kb;
     }
     ctx_len[b] += n;
     n_commit[b] = n;
@@ -286,7 +304,9 @@ xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStr
 size_t argmax_workspace_size(int M, int V) { return static_cast<size_t>(M) * ceil_div(V, ARGMAX_CHUNK) * sizeof(float2); }
 
 xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
-                               const int32_t* tokens, int32_t* n_accept, cudaStream_t s) {
+                               const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s) {
+    unsigned* err = device_error_word();
+    if (!err) return fail(XV_ERR_CUDA, "argmax: device error word unavailable");
     if (k < 1 || k > XV_KMAX) return fail(XV_ERR_ARG, "argmax: k = %d outside [1, %d]", k, XV_KMAX);
     const int M = B * k;
     const int nchunk = ceil_div(V, ARGMAX_CHUNK);
@@ -295,16 +315,17 @@ xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t
     launch_k(argmax_chunk_kernel, dim3(nchunk, M), dim3(ARGMAX_THREADS), 0, s, logits, V, part, nchunk);
     if (xv_status st = launched("argmax_chunk_kernel", s, K_ARGMAX, 4ll * M * V)) return st;
     trace_pre(s);
-    launch_k(argmax_accept_kernel, dim3(B), dim3(32 * k), 0, s, part, nchunk, k, idx, tokens, n_accept);
+    launch_k(argmax_accept_kernel, dim3(B), dim3(32 * k), 0, s, part, nchunk, k, idx, tokens, k_seq, n_accept, err);
     return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
 }
 
-xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,
+xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, const int32_t* k_seq, int32_t* ctx_len,
+                        int32_t* n_commit,
                         cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "commit: device error word unavailable");
     trace_pre(s);
-    launch_k(commit_kernel, dim3(ceil_div(B, 128)), dim3(128), 0, s, keep, keep_bias, B, k, ctx_len, n_commit, err);
+    launch_k(commit_kernel, dim3(ceil_div(B, 128)), dim3(128), 0, s, keep, keep_bias, B, k, k_seq, ctx_len, n_commit, err);
     return launched("commit_kernel", s, K_COMMIT, 16ll * B);
 }
 

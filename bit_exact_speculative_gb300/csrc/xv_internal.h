@@ -105,14 +105,24 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
 constexpr int ATTN_SPLIT = 512;   // positions per split, fixed absolute boundaries
 constexpr int ATTN_TILE = 64;     // positions per tile inside a split
 size_t attn_workspace_size(int B, int R, int Hq, int hd, int max_len);
+// Where position p of sequence b lives in a K or V cache of Hkv heads: page
+// table[b * max_pages + p / page], row p % page, in a pool [n_pages, Hkv, page, hd].
+// A contiguous cache [B, Hkv, Lmax, hd] is one page of Lmax positions per sequence
+// (table == nullptr, page = Lmax, max_pages = 1, n_pages = B).  Positions run to
+// page * max_pages.
+struct KvPages {
+    const int32_t* table;
+    int page, max_pages, n_pages;
+};
+inline KvPages kv_contiguous(int B, int Lmax) { return KvPages{nullptr, Lmax, 1, B}; }
 // Row r of sequence b sees ctx_len[b] + len_bias + r positions; max_len bounds every such length.
-xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
-                      const int32_t* ctx_len, int len_bias, int R, int B, int Hq, int Hkv, int hd, int Lmax,
-                      int max_len, float scale, const uint16_t* gate, long long gate_stride, uint16_t* out,
-                      long long out_stride, void* ws, size_t ws_bytes, cudaStream_t s);
+xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc, const KvPages& kv,
+                      const int32_t* ctx_len, int len_bias, int R, int B, int Hq, int Hkv, int hd, int max_len,
+                      float scale, const uint16_t* gate, long long gate_stride, uint16_t* out, long long out_stride,
+                      void* ws, size_t ws_bytes, cudaStream_t s);
 // Row (b, r) of src goes to position ctx_len[b] + pos_bias + r.
 xv_status kv_append_launch(const uint16_t* src, long long src_stride, const int32_t* ctx_len, int pos_bias, int R,
-                           int B, int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, cudaStream_t s);
+                           int B, int Hkv, int hd, const KvPages& kv, uint16_t* kc, uint16_t* vc, cudaStream_t s);
 
 // ---- glue (glue.cu)
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s);
@@ -126,12 +136,14 @@ xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t
 xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s);
 size_t argmax_workspace_size(int M, int V);
 // idx[b*k + j] = argmax of logits row b*k + j (lowest index among equal maxima);
-// n_accept[b] = leading drafts tokens[b][j+1] equal to idx[b*k + j] (two kernels)
+// n_accept[b] = leading drafts tokens[b][j+1] (j + 1 < k_b) equal to idx[b*k + j], where
+// k_b = k_seq[b] (k when k_seq is null) (two kernels)
 xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
-                               const int32_t* tokens, int32_t* n_accept, cudaStream_t s);
-// ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (keep checked to lie in [1, k])
-xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, int32_t* ctx_len, int32_t* n_commit,
-                        cudaStream_t s);
+                               const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s);
+// ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (checked to lie in [1, k_b],
+// k_b = k_seq[b] or k)
+xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, const int32_t* k_seq, int32_t* ctx_len,
+                        int32_t* n_commit, cudaStream_t s);
 xv_status zero_i32_launch(int32_t* p, int n, cudaStream_t s);
 
 }  // namespace xv

@@ -13,7 +13,8 @@ enum : unsigned {
     ERR_WAIT_TIMEOUT = 1u << 0,   // an mbarrier wait gave up
     ERR_BAD_TOKEN = 1u << 1,      // a token id outside [0, vocab)
     ERR_BAD_LENGTH = 1u << 2,     // a context length outside the range the launch was sized for
-    ERR_BAD_COUNT = 1u << 3,      // a commit/keep count outside its range
+    ERR_BAD_COUNT = 1u << 3,      // a commit/keep count or a per-sequence k outside its range
+    ERR_BAD_PAGE = 1u << 4,       // a KV page table entry outside the pool
 };
 
 // Upper bound on the time one mbarrier wait may take before it records an

@@ -7,12 +7,17 @@ lengths, workspace) with torch, and calls ``xv_verify_block`` /
 
 Config keys: hidden, vocab, mlp, kinds (0 = GDN, 1 = gated attention),
 gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv, attn_hd, rms_eps.
+
+With ``page_size`` the attention caches are page pools shared by the
+sequences (:class:`KvPagePool` hands pages out); without, each sequence has a
+contiguous [Hkv, Lmax, hd] cache.  Both give the same bits.
 Weight keys: embed, final_norm, lm_head and per layer ``f"{l}.norm1"``,
 ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down`` (bf16 bit patterns in
 any 2-byte torch dtype, on the device).
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import xv
@@ -42,13 +47,90 @@ def weight_shapes(cfg: dict) -> dict:
     return shapes
 
 
+class KvPagePool:
+    """Hands out the pages of a paged KV pool to the sequences of a stack.
+
+    Entry ``[b, j]`` of the page table names the page that holds positions
+    ``[j * page, (j + 1) * page)`` of sequence b (-1: none yet).  Pages come off
+    a free list, so the pages of one sequence are scattered through the pool in
+    the order the list gives (``order``, default 0, 1, 2, ...).  ``table`` is the
+    device copy the kernels read; :meth:`sync` refreshes it after changes with a
+    stream-ordered copy from one of two pinned staging buffers, so the host never
+    waits for the device to drain (it waits only for the copy made two syncs
+    earlier from the same buffer).
+    """
+
+    def __init__(self, n_pages: int, page: int, B: int, max_pages: int, device="cuda", order=None):
+        self.n_pages, self.page, self.B, self.max_pages = int(n_pages), int(page), int(B), int(max_pages)
+        order = list(range(n_pages)) if order is None else [int(x) for x in order]
+        if sorted(order) != list(range(n_pages)):
+            raise ValueError("order must be a permutation of the pool's pages")
+        self.free = order[::-1]           # pop() hands out order[0] first
+        self.host = np.full((B, max_pages), -1, dtype=np.int32)
+        self.held = [0] * B
+        self.table = torch.full((B, max_pages), -1, dtype=torch.int32, device=device)
+        self.dirty = False
+        self._cuda = self.table.is_cuda
+        if self._cuda:
+            self._stage = [torch.empty((B, max_pages), dtype=torch.int32).pin_memory() for _ in range(2)]
+            self._copied = [None, None]
+            self._flip = 0
+
+    def ensure(self, b: int, length: int):
+        """Gives sequence b pages for positions [0, length)."""
+        need = -(-int(length) // self.page)
+        if need > self.max_pages:
+            raise ValueError(f"sequence {b}: {length} positions exceed {self.max_pages} pages of {self.page}")
+        while self.held[b] < need:
+            if not self.free:
+                raise MemoryError("KV page pool exhausted")
+            self.host[b, self.held[b]] = self.free.pop()
+            self.held[b] += 1
+            self.dirty = True
+
+    def release(self, b: int):
+        """Returns every page of sequence b to the pool."""
+        for j in range(self.held[b] - 1, -1, -1):
+            self.free.append(int(self.host[b, j]))
+        self.host[b, :] = -1
+        self.held[b] = 0
+        self.dirty = True
+
+    def sync(self, stream=None):
+        """Enqueues the table update on ``stream`` (default: the current stream)."""
+        if not self.dirty:
+            return
+        if not self._cuda:
+            self.table.copy_(torch.from_numpy(self.host))
+        else:
+            i = self._flip
+            self._flip ^= 1
+            if self._copied[i] is not None:
+                self._copied[i].synchronize()
+            self._stage[i].copy_(torch.from_numpy(self.host))
+            stream = torch.cuda.current_stream(self.table.device) if stream is None else stream
+            with torch.cuda.stream(stream):
+                self.table.copy_(self._stage[i], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+            self._copied[i] = ev
+        self.dirty = False
+
+
 class HybridStack:
-    def __init__(self, cfg: dict, weights: dict, B: int, kmax: int, Lmax: int, device="cuda"):
+    def __init__(self, cfg: dict, weights: dict, B: int, kmax: int, Lmax: int, device="cuda",
+                 page_size: int | None = None, n_pages: int | None = None, page_order=None):
         self.cfg, self.B, self.kmax, self.Lmax = dict(cfg), B, kmax, Lmax
         self.weights = weights
         d = device
         st = {"ctx_len": torch.zeros(B, dtype=torch.int32, device=d),
               "n_commit": torch.zeros(B, dtype=torch.int32, device=d)}
+        self.pool = None
+        if page_size is not None:
+            max_pages = -(-Lmax // page_size)
+            n_pages = B * max_pages if n_pages is None else n_pages
+            self.pool = KvPagePool(n_pages, page_size, B, max_pages, device=d, order=page_order)
+            st["page_table"] = self.pool.table
         for l, kd in enumerate(cfg["kinds"]):
             if kd == 0:
                 h, dk, dv = cfg["gdn_heads"], cfg["gdn_dk"], cfg["gdn_dv"]
@@ -56,11 +138,18 @@ class HybridStack:
                 for p in (0, 1):
                     st[f"{l}.hist{p}"] = torch.zeros((B * kmax, gdn_hist_stride(cfg)), dtype=torch.int16, device=d)
             else:
-                shape = (B, cfg["attn_hkv"], Lmax, cfg["attn_hd"])
+                if self.pool is None:
+                    shape = (B, cfg["attn_hkv"], Lmax, cfg["attn_hd"])
+                else:
+                    shape = (self.pool.n_pages, cfg["attn_hkv"], page_size, cfg["attn_hd"])
                 st[f"{l}.kc"] = torch.zeros(shape, dtype=torch.int16, device=d)
                 st[f"{l}.vc"] = torch.zeros(shape, dtype=torch.int16, device=d)
         self.state = st
-        self.blk = xv.Block(cfg, weights, st, B, kmax, Lmax, ctx0=0)
+        pages = None if self.pool is None else xv.kv_pages(self.pool.table, page_size, self.pool.n_pages)
+        self.blk = xv.Block(cfg, weights, st, B, kmax, Lmax, ctx0=0, pages=pages)
+        self._bound = [0] * B          # host upper bound of each ctx_len (page allocation)
+        self._k_seq = None             # the k_seq of a ragged verify, kept alive until its commit
+        self._last_k = 0
         self.ws = xv.workspace(self.blk.ws_bytes, device=d)
         self.logits = torch.empty((B * kmax, cfg["vocab"]), dtype=torch.float32, device=d)
         self.argmax = torch.empty(B * kmax, dtype=torch.int32, device=d)
@@ -68,16 +157,55 @@ class HybridStack:
 
     def set_context(self, ctx_len):
         """Sets every sequence's committed length (host list); the caller has filled the caches/states."""
-        t = torch.as_tensor(list(ctx_len), dtype=torch.int32)
+        lens = [int(x) for x in ctx_len]
+        t = torch.as_tensor(lens, dtype=torch.int32)
         self.state["ctx_len"].copy_(t)
         self.state["n_commit"].zero_()
         self.blk.state.max_ctx = int(t.max())
         self.blk.state.last_k = 0
+        self._bound = lens
+        if self.pool is not None:
+            for b, n in enumerate(lens):
+                self.pool.ensure(b, n)
+            self.pool.sync()
 
-    def verify(self, tokens: torch.Tensor, k: int, logits: bool = True, stream=None):
-        """tokens: int32 [B, k] on the device.  Returns (logits [B*k, V] or None, argmax [B*k], n_accept [B])."""
+    def load_kv(self, layer: int, kc, vc):
+        """Writes contiguous caches kc, vc ([B, Hkv, Lmax, hd], 2-byte dtype, host or device) into
+        attention layer ``layer``: copied as they are, or scattered into the pages the pool holds."""
+        kd, vd = self.state[f"{layer}.kc"], self.state[f"{layer}.vc"]
+        kc = torch.as_tensor(kc).view(torch.int16)
+        vc = torch.as_tensor(vc).view(torch.int16)
+        if self.pool is None:
+            kd.copy_(kc)
+            vd.copy_(vc)
+            return
+        P = self.pool.page
+        for b in range(self.B):
+            for j in range(self.pool.held[b]):
+                pg = int(self.pool.host[b, j])
+                n = min(P, self.Lmax - j * P)
+                kd[pg, :, :n].copy_(kc[b, :, j * P:j * P + n])
+                vd[pg, :, :n].copy_(vc[b, :, j * P:j * P + n])
+
+    def _prepare(self, k: int, stream=None):
+        if self.pool is not None:
+            for b in range(self.B):
+                self.pool.ensure(b, min(self._bound[b] + k, self.Lmax))
+            self.pool.sync(stream)
+
+    def verify(self, tokens: torch.Tensor, k: int, logits: bool = True, stream=None, k_seq=None):
+        """tokens: int32 [B, k] on the device; k_seq: optional int32 [B] device tensor of per-sequence
+        token counts (1..k; rows past k_seq[b] are padding).  Returns (logits [B*k, V] or None,
+        argmax [B*k], n_accept [B])."""
+        self._prepare(k, stream)
         lg = self.logits[: self.B * k] if logits else None
-        xv.xv_verify_block(self.blk, tokens, k, lg, self.argmax, self.n_accept, self.ws, stream=stream)
+        if k_seq is None:
+            xv.xv_verify_block(self.blk, tokens, k, lg, self.argmax, self.n_accept, self.ws, stream=stream)
+        else:
+            xv.xv_verify_block_ragged(self.blk, tokens, k, k_seq, lg, self.argmax, self.n_accept, self.ws,
+                                      stream=stream)
+        self._k_seq = k_seq
+        self._last_k = k
         return lg, self.argmax[: self.B * k], self.n_accept
 
     def commit(self, n_keep: torch.Tensor | None = None, stream=None):
@@ -86,6 +214,8 @@ class HybridStack:
             xv.xv_block_commit_accepted(self.blk, self.n_accept, stream=stream)
         else:
             xv.xv_block_commit(self.blk, n_keep, stream=stream)
+        self._bound = [n + self._last_k for n in self._bound]
+        self._k_seq = None
 
     def flush(self, stream=None):
         xv.xv_block_flush(self.blk, stream=stream)
@@ -99,3 +229,4 @@ class HybridStack:
         caller has read back (a commit raises the bound by k whatever was accepted)."""
         if longest < self.blk.state.max_ctx:
             self.blk.state.max_ctx = int(longest)
+        self._bound = [min(n, int(longest)) for n in self._bound]

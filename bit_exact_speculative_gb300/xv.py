@@ -52,9 +52,14 @@ class LayerState(ctypes.Structure):
     _fields_ = [("gdn_state", vp), ("gdn_hist", vp * 2), ("k_cache", vp), ("v_cache", vp)]
 
 
+class KvPages(ctypes.Structure):
+    _fields_ = [("page_table", vp), ("page_size", c_int), ("max_pages", c_int), ("n_pages", c_int)]
+
+
 class BlockState(ctypes.Structure):
     _fields_ = [("B", c_int), ("kmax", c_int), ("Lmax", c_int), ("ctx_len", vp), ("n_commit", vp),
-                ("parity", c_int), ("pending_rows", c_int), ("max_ctx", c_int), ("last_k", c_int), ("layers", vp)]
+                ("parity", c_int), ("pending_rows", c_int), ("max_ctx", c_int), ("last_k", c_int), ("layers", vp),
+                ("kv_pages", KvPages), ("last_k_seq", vp)]
 
 
 _lib = None
@@ -83,12 +88,17 @@ _SIGS = {
     "xv_attn_decode_rows": ([vp, c_ll, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                              vp, c_ll, vp, c_ll, vp, c_sz, vp], c_int),
     "xv_kv_append": ([vp, c_ll, vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp], c_int),
+    "xv_attn_decode_rows_paged": ([vp, c_ll, vp, vp, ctypes.POINTER(KvPages), vp, c_int, c_int, c_int, c_int, c_int,
+                                   c_int, c_float, vp, c_ll, vp, c_ll, vp, c_sz, vp], c_int),
+    "xv_kv_append_paged": ([vp, c_ll, vp, c_int, c_int, c_int, c_int, ctypes.POINTER(KvPages), vp, vp, vp], c_int),
     "xv_gdn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_gdn_hist_stride": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_attn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_block_workspace_size": ([ctypes.POINTER(BlockConfig), c_int, c_int, c_int], c_sz),
     "xv_verify_block": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState),
                          vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
+    "xv_verify_block_ragged": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
+                                ctypes.POINTER(BlockState), vp, c_int, vp, vp, vp, vp, vp, c_sz, vp], c_int),
     "xv_block_commit": ([ctypes.POINTER(BlockState), vp, vp], c_int),
     "xv_block_commit_accepted": ([ctypes.POINTER(BlockState), vp, vp], c_int),
     "xv_block_flush": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockState), vp], c_int),
@@ -245,6 +255,27 @@ def xv_kv_append(kv_src, src_stride, ctx_len, R, B, Hkv, hd, Lmax, kc, vc, strea
                               _stream(stream)))
 
 
+def kv_pages(page_table, page_size: int, n_pages: int) -> KvPages:
+    """The page description of a paged KV pool: page_table int32 [B, max_pages] on the device
+    (kept referenced by the returned struct)."""
+    pages = KvPages(page_table.data_ptr(), int(page_size), int(page_table.shape[1]), int(n_pages))
+    pages._table = page_table
+    return pages
+
+
+def xv_attn_decode_rows_paged(q, q_stride, kpool, vpool, pages: KvPages, ctx_len, R, B, Hq, Hkv, hd, max_ctx, scale,
+                              out, out_stride, ws, gate=None, gate_stride=0, stream=None):
+    _check(lib().xv_attn_decode_rows_paged(_ptr(q), q_stride, _ptr(kpool), _ptr(vpool), ctypes.byref(pages),
+                                           _ptr(ctx_len), R, B, Hq, Hkv, hd, max_ctx, float(scale), _ptr(gate),
+                                           gate_stride, _ptr(out), out_stride, _ptr(ws),
+                                           ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def xv_kv_append_paged(kv_src, src_stride, ctx_len, R, B, Hkv, hd, pages: KvPages, kpool, vpool, stream=None):
+    _check(lib().xv_kv_append_paged(_ptr(kv_src), src_stride, _ptr(ctx_len), R, B, Hkv, hd, ctypes.byref(pages),
+                                    _ptr(kpool), _ptr(vpool), _stream(stream)))
+
+
 # ------------------------------------------------------------------ block
 
 class Block:
@@ -254,10 +285,12 @@ class Block:
     attn_hd, rms_eps); ``weights`` a dict of device tensors (embed, final_norm, lm_head and per
     layer ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``);
     ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1`` or
-    ``.kc``, ``.vc``).  Tensors are kept referenced here.
+    ``.kc``, ``.vc``).  With ``pages`` (a :class:`KvPages` over ``state["page_table"]``) the
+    attention caches are page pools.  Tensors are kept referenced here.
     """
 
-    def __init__(self, cfg: dict, weights: dict, state: dict, B: int, kmax: int, Lmax: int, ctx0: int):
+    def __init__(self, cfg: dict, weights: dict, state: dict, B: int, kmax: int, Lmax: int, ctx0: int,
+                 pages: KvPages | None = None):
         kinds = list(cfg["kinds"])
         self._kinds = (ctypes.c_int32 * len(kinds))(*kinds)
         self.cfg = BlockConfig(cfg["hidden"], cfg["vocab"], cfg["mlp"], len(kinds),
@@ -280,7 +313,8 @@ class Block:
                 ls.append(LayerState(None, (vp * 2)(None, None), state[f"{l}.kc"].data_ptr(), state[f"{l}.vc"].data_ptr()))
         self._ls = (LayerState * len(kinds))(*ls)
         self.state = BlockState(B, kmax, Lmax, state["ctx_len"].data_ptr(), state["n_commit"].data_ptr(), 0, kmax,
-                                ctx0, 0, ctypes.cast(self._ls, vp).value)
+                                ctx0, 0, ctypes.cast(self._ls, vp).value, pages if pages is not None else KvPages(),
+                                None)
         self.ws_bytes = int(lib().xv_block_workspace_size(ctypes.byref(self.cfg), B, kmax, Lmax))
         if self.ws_bytes == 0:
             _check(XV_ERR_ARG)
@@ -296,6 +330,12 @@ def xv_verify_block(blk: Block, tokens, k: int, logits, argmax, n_accept, ws, st
     _check(lib().xv_verify_block(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
                                  _ptr(tokens), k, _ptr(logits), _ptr(argmax), _ptr(n_accept), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def xv_verify_block_ragged(blk: Block, tokens, k: int, k_seq, logits, argmax, n_accept, ws, stream=None):
+    _check(lib().xv_verify_block_ragged(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
+                                        _ptr(tokens), k, _ptr(k_seq), _ptr(logits), _ptr(argmax), _ptr(n_accept),
+                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def xv_block_commit(blk: Block, n_keep, stream=None):

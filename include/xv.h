@@ -55,7 +55,7 @@ typedef int xv_status;
 #define XV_ERR_CUDA        -4   /* a CUDA runtime call or launch failed */
 #define XV_ERR_DEVICE_CHECK -5  /* a kernel recorded a device-side error (see xv_device_check) */
 
-#define XV_ABI_VERSION 1
+#define XV_ABI_VERSION 2
 #define XV_GEMM_M_MAX 64        /* rows per small-M GEMM call */
 #define XV_KMAX 16              /* draft tokens per sequence per verify call */
 
@@ -68,7 +68,10 @@ const char* xv_last_error(void);
 
 /* Synchronises `s`, then reads and clears the device-side error word of the
  * current device.  Returns XV_OK, or XV_ERR_DEVICE_CHECK with *code set to the
- * recorded bits (code may be NULL).  The only call in the library that
+ * recorded bits (code may be NULL): 1 a bounded wait gave up, 2 a token id
+ * outside [0, vocab), 4 a context length outside what the launch was sized
+ * for, 8 a commit count or per-sequence k outside its range, 16 a KV page
+ * table entry outside the pool.  The only call in the library that
  * synchronises. */
 xv_status xv_device_check(xv_stream s, unsigned* code);
 
@@ -226,6 +229,34 @@ xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint1
 xv_status xv_kv_append(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B,
                        int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, xv_stream s);
 
+/* Paged KV cache.  The K and V pools are [n_pages, Hkv, page_size, hd] bf16
+ * (16-byte aligned); position p of sequence b is row p % page_size of page
+ * page_table[b * max_pages + p / page_size], so a sequence holds up to
+ * page_size * max_pages positions and pages are handed out by the caller
+ * (pages of one pool may be shared out among the sequences in any order).
+ * page_size is a positive multiple of 64: a page holds whole 64-position
+ * tiles, so the split/tile schedule, and with it every bit of the result, is
+ * the one of a contiguous cache holding the same values.  Every table entry
+ * that a call reads (positions below ctx_len[b] + R - 1) must name a page in
+ * [0, n_pages); an entry outside it is recorded as device error bit 16 and
+ * replaced by page 0 (attention) or skipped (append). */
+typedef struct {
+    const int32_t* page_table;   /* [B, max_pages] int32 device */
+    int page_size;               /* positions per page, a multiple of 64 */
+    int max_pages;               /* table entries per sequence */
+    int n_pages;                 /* pages in each pool */
+} xv_kv_pages;
+
+/* xv_attn_decode_rows over paged pools; R <= max_ctx <= page_size * max_pages. */
+xv_status xv_attn_decode_rows_paged(const uint16_t* q, long long q_stride, const uint16_t* kpool, const uint16_t* vpool,
+                                    const xv_kv_pages* pages, const int32_t* ctx_len, int R, int B, int Hq, int Hkv,
+                                    int hd, int max_ctx, float scale, const uint16_t* gate, long long gate_stride,
+                                    uint16_t* out, long long out_stride, void* ws, size_t ws_bytes, xv_stream s);
+
+/* xv_kv_append into paged pools. */
+xv_status xv_kv_append_paged(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B,
+                             int Hkv, int hd, const xv_kv_pages* pages, uint16_t* kpool, uint16_t* vpool, xv_stream s);
+
 /* ------------------------------------------------------------ the block
  * A stack of decoder layers (each: x + mixer(rmsnorm(x)), then
  * h + SwiGLU-MLP(rmsnorm(h))), mixers being GDN or gated attention layers,
@@ -269,7 +300,8 @@ typedef struct {
 typedef struct {
     float* gdn_state;         /* GDN layer: [B, heads, dv, dk] fp32 */
     uint16_t* gdn_hist[2];    /* GDN layer: two [B*kmax, xv_gdn_hist_stride(cfg)] bf16 projection buffers */
-    uint16_t* k_cache;        /* attention layer: [B, Hkv, Lmax, hd] bf16 */
+    uint16_t* k_cache;        /* attention layer: [B, Hkv, Lmax, hd] bf16, or a pool
+                                 [kv_pages.n_pages, Hkv, page_size, hd] when the state is paged */
     uint16_t* v_cache;
 } xv_layer_state;
 
@@ -285,6 +317,10 @@ typedef struct {
                                  back may lower it to their maximum (never below it) */
     int last_k;               /* host: k of the last verify not yet committed (0 = none) */
     xv_layer_state* layers;   /* HOST array [n_layers] */
+    xv_kv_pages kv_pages;     /* page_table NULL: contiguous caches; else every attention layer's
+                                 caches are pools addressed by this one table, and
+                                 Lmax <= page_size * max_pages */
+    const int32_t* last_k_seq;/* host: the k_seq of the last verify not yet committed (NULL = k) */
 } xv_block_state;
 
 int xv_gdn_in_dim(const xv_block_config* cfg);
@@ -304,6 +340,19 @@ size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int 
 xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
                           const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept,
                           void* ws, size_t ws_bytes, xv_stream s);
+
+/* Verify with a number of tokens per sequence: sequence b verifies k_b =
+ * k_seq[b] tokens (device [B] int32, 1 <= k_b <= k), laid out as the first
+ * k_b of its k rows in tokens [B, k]; rows k_b..k-1 are padding (any valid
+ * token ids).  Rows below k_b get the bits a call with k = k_b (or k_b
+ * decode steps) gives them; the outputs of padding rows are unspecified.
+ * n_accept[b] counts drafts among the k_b - 1 of sequence b.  k_seq must
+ * stay unchanged until the commit, which keeps 1..k_b positions of sequence
+ * b (a count outside is recorded as device error bit 8 and clamped).
+ * k_seq = NULL is xv_verify_block. */
+xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                                 const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
+                                 int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream s);
 
 /* Commit n_keep[b] (device, 1..k) positions of the last verify: ctx_len += n_keep,
  * n_commit = n_keep; flips the history parity and advances max_ctx by the k of

@@ -7,18 +7,23 @@ from synth import workloads
 from _gpu import dev
 
 
-def gpu_stack(cfg, w_np, B, kmax, Lmax, ctx_lens, seed=0, weights_dev=None):
+def gpu_stack(cfg, w_np, B, kmax, Lmax, ctx_lens, seed=0, weights_dev=None, page_size=None, n_pages=None,
+              page_order=None, only=None):
+    """The stack of the seeded recipe for B sequences of lengths ctx_lens; with ``only`` = b a B = 1
+    stack holding sequence b of that recipe.  page_size / n_pages / page_order make the KV caches
+    a page pool."""
     from bit_exact_speculative_gb300.model import HybridStack
     weights = weights_dev if weights_dev is not None else {k: dev(v) for k, v in w_np.items()}
-    stk = HybridStack(cfg, weights, B, kmax, Lmax)
+    sel = slice(None) if only is None else slice(only, only + 1)
+    nb = B if only is None else 1
+    stk = HybridStack(cfg, weights, nb, kmax, Lmax, page_size=page_size, n_pages=n_pages, page_order=page_order)
+    stk.set_context(list(ctx_lens)[sel])
     for l, kd in enumerate(cfg["kinds"]):
         if kd == 0:
-            stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seed, l, B)))
+            stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seed, l, B)[sel]))
         else:
             kc, vc = workloads.kv_cache(cfg, seed, l, B, ctx_lens, Lmax)
-            stk.state[f"{l}.kc"].copy_(torch.from_numpy(kc.view(np.int16)))
-            stk.state[f"{l}.vc"].copy_(torch.from_numpy(vc.view(np.int16)))
-    stk.set_context(ctx_lens)
+            stk.load_kv(l, torch.from_numpy(kc[sel].view(np.int16)), torch.from_numpy(vc[sel].view(np.int16)))
     torch.cuda.synchronize()
     return stk
 

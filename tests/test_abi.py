@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(xv):
 
 
 def test_abi_version(xv):
-    assert xv.xv_abi_version() == 1
+    assert xv.xv_abi_version() == 2
 
 
 def _code(fn, *args):
@@ -120,3 +120,24 @@ def test_block_dims_and_validation_without_gpu(xv):
     assert L.xv_verify_block(ctypes.byref(c), ctypes.byref(w), ctypes.byref(st), None, 8, None, None, None, None, 0,
                              None) == xv.XV_ERR_ARG
     assert L.xv_block_commit(ctypes.byref(st), None, None) == xv.XV_ERR_ARG
+
+
+def test_paged_validation_without_gpu(xv):
+    """Paged KV calls check the page description on the host before anything reaches the device."""
+    L = xv.lib()
+    p = ctypes.c_void_p(0x10000)
+    bad = xv.KvPages(0x10000, 96, 4, 8)       # page size not a multiple of 64
+    good = xv.KvPages(0x10000, 64, 4, 8)
+    args = lambda pages, max_ctx: (p, 256, p, p, ctypes.byref(pages), p, 2, 1, 4, 2, 64, max_ctx, 0.125, None, 0, p,
+                                   256, p, 1 << 20, None)
+    assert L.xv_attn_decode_rows_paged(*args(bad, 100)) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_attn_decode_rows_paged(*args(good, 257)) == xv.XV_ERR_ARG      # beyond 4 pages of 64
+    assert L.xv_attn_decode_rows_paged(*args(xv.KvPages(None, 64, 4, 8), 100)) == xv.XV_ERR_ARG
+    assert L.xv_kv_append_paged(p, 256, p, 2, 1, 2, 64, ctypes.byref(bad), p, p, None) == xv.XV_ERR_UNSUPPORTED
+
+
+def test_block_state_layout(xv):
+    """The binding's state struct ends with the page description and the ragged k pointer."""
+    names = [f[0] for f in xv.BlockState._fields_]
+    assert names[-2:] == ["kv_pages", "last_k_seq"]
+    assert ctypes.sizeof(xv.KvPages) == 8 + 3 * 4 + 4     # pointer, three ints, tail padding

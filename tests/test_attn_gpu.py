@@ -144,3 +144,88 @@ def test_kv_append_places_rows(xv):
             assert np.array_equal(k[b, :, ctx[b] - 1 + r].reshape(-1), row[:Hkv * hd])
             assert np.array_equal(v[b, :, ctx[b] - 1 + r].reshape(-1), row[Hkv * hd:])
     assert int((k != 0).sum()) == B * R * Hkv * hd - int((src[:, :Hkv * hd] == 0).sum())
+
+
+def to_pages(c, table, page, n_pages):
+    """Scatters contiguous caches [B, Hkv, Lmax, hd] into a pool [n_pages, Hkv, page, hd] by table."""
+    B, Hkv, Lmax, hd = c.shape
+    pool = np.zeros((n_pages, Hkv, page, hd), dtype=c.dtype)
+    for b in range(B):
+        for j in range(table.shape[1]):
+            n = min(page, Lmax - j * page)
+            if n > 0 and table[b, j] >= 0:
+                pool[table[b, j], :, :n] = c[b, :, j * page:j * page + n]
+    return pool
+
+
+def scattered_table(seed, B, max_pages, n_pages):
+    """Every sequence's pages drawn without replacement from a pool larger than needed."""
+    perm = np.random.default_rng(seed).permutation(n_pages)[: B * max_pages]
+    return perm.reshape(B, max_pages).astype(np.int32)
+
+
+@pytest.mark.parametrize("hd,Hq,Hkv,R,page,lens", [(256, 24, 4, 8, 64, [2183, 1, 640, 1500]),
+                                                    (256, 24, 4, 9, 256, [513, 2047]),
+                                                    (64, 6, 2, 4, 128, [63, 64, 65, 700])])
+def test_paged_equals_contiguous(xv, hd, Hq, Hkv, R, page, lens):
+    """The same values in scattered pages give the bits of the contiguous cache (and the oracle)."""
+    B = len(lens)
+    Lmax = (max(lens) + R + page - 1) // page * page
+    max_pages = Lmax // page
+    n_pages = B * max_pages + 5
+    q, kc, vc = make(11, B, R, Hq, Hkv, hd, Lmax, name=f"pg{hd}{page}")
+    table = scattered_table(page, B, max_pages, n_pages)
+    ctx = np.array(lens, dtype=np.int32)
+    max_ctx = max(lens) + R - 1
+    ref = attn(xv, dev(q), dev(kc), dev(vc), dev(ctx), R, B, Hq, Hkv, hd, Lmax, max_ctx)
+    kp, vp = dev(to_pages(kc, table, page, n_pages)), dev(to_pages(vc, table, page, n_pages))
+    tab = dev(table)
+    pages = xv.kv_pages(tab, page, n_pages)
+    out = torch.empty((B * R, Hq * hd), dtype=torch.int16, device="cuda")
+    ws = xv.workspace(xv.xv_attn_workspace_size(B, R, Hq, hd, max_ctx))
+    xv.xv_attn_decode_rows_paged(dev(q), Hq * hd, kp, vp, pages, dev(ctx), R, B, Hq, Hkv, hd, max_ctx, hd ** -0.5,
+                                 out, out.stride(0), ws)
+    assert same_bits(out, ref), "paged attention differs from the contiguous cache"
+    assert xv.xv_device_check() == 0
+    b = 0
+    exp = exact_rows(q[b * R:(b + 1) * R], kc[b], vc[b], lens[b], hd ** -0.5, R, Hq, Hkv, hd)
+    assert_bf16_close(host_u16(out)[b * R:(b + 1) * R].reshape(R, Hq, hd), exp, what="paged attn vs oracle")
+
+
+def test_kv_append_paged_places_rows(xv):
+    B, R, Hkv, hd, page, max_pages = 2, 9, 4, 256, 64, 3
+    n_pages = 8
+    src = synth.normal_bf16(8, synth.tid("kvsrc_paged"), (B * R, 2 * Hkv * hd))
+    table = np.array([[5, 2, 7], [0, 6, 3]], dtype=np.int32)
+    kp = torch.zeros((n_pages, Hkv, page, hd), dtype=torch.int16, device="cuda")
+    vp = torch.zeros_like(kp)
+    ctx = np.array([60, 128], dtype=np.int32)     # sequence 0 crosses from its page 0 into page 1
+    tab = dev(table)
+    pages = xv.kv_pages(tab, page, n_pages)
+    xv.xv_kv_append_paged(dev(src), 2 * Hkv * hd, dev(ctx), R, B, Hkv, hd, pages, kp, vp)
+    k, v = host_u16(kp), host_u16(vp)
+    for b in range(B):
+        for r in range(R):
+            p = ctx[b] - 1 + r
+            pg, row = table[b, p // page], p % page
+            assert np.array_equal(k[pg, :, row].reshape(-1), src[b * R + r, :Hkv * hd])
+            assert np.array_equal(v[pg, :, row].reshape(-1), src[b * R + r, Hkv * hd:])
+    assert int((k != 0).sum()) == B * R * Hkv * hd - int((src[:, :Hkv * hd] == 0).sum())
+    assert xv.xv_device_check() == 0
+
+
+def test_paged_arguments_rejected(xv):
+    """Host checks: a page size that is not a multiple of 64, or max_ctx beyond the table's reach."""
+    B, R, Hq, Hkv, hd = 1, 2, 4, 2, 64
+    tab = torch.zeros((B, 2), dtype=torch.int32, device="cuda")
+    kp = torch.zeros((2, Hkv, 96, hd), dtype=torch.int16, device="cuda")
+    q = torch.zeros((B * R, Hq * hd), dtype=torch.int16, device="cuda")
+    out = torch.empty_like(q)
+    ctx = torch.ones(B, dtype=torch.int32, device="cuda")
+    ws = xv.workspace(xv.xv_attn_workspace_size(B, R, Hq, hd, 256))
+    with pytest.raises(xv.XVError):
+        xv.xv_attn_decode_rows_paged(q, Hq * hd, kp, kp, xv.kv_pages(tab, 96, 2), ctx, R, B, Hq, Hkv, hd, 100, 0.125,
+                                     out, Hq * hd, ws)
+    with pytest.raises(xv.XVError):
+        xv.xv_attn_decode_rows_paged(q, Hq * hd, kp, kp, xv.kv_pages(tab, 64, 2), ctx, R, B, Hq, Hkv, hd, 129, 0.125,
+                                     out, Hq * hd, ws)

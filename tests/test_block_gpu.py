@@ -221,3 +221,93 @@ def test_stack_speculative_rounds_emit_greedy_decode(stack):
         assert out[:n] == ref[1:n + 1], f"accept {accept}: emitted tokens differ from the greedy decode"
         assert lo <= float(np.mean(acc)) <= hi, (accept, acc)
         assert int(host(S.state["ctx_len"])[0]) == L + len(out)
+
+
+def test_stack_verify_k9_equals_sequential_decode(stack):
+    """k = 9 (one more than the 8 the fused kernels' row count was sized around): bit-exact too."""
+    cfg, w, wd = stack
+    B, k, L = 1, 9, 2183
+    Lmax = L + 64
+    toks = workloads.draft_tokens(cfg, 0, 9, B, k)
+    A = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lg, am, _ = A.verify(dev(toks), k)
+    lgA, amA = lg.clone(), am.clone()
+    S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lgS, amS = sequential(S, toks, B)
+    assert same_bits(lgA.view(B, k, -1), lgS)
+    assert torch.equal(amA.view(B, k), amS)
+
+
+@pytest.mark.parametrize("page", [64, 256])
+def test_stack_paged_kv_equals_contiguous(stack, page):
+    """8 sequences over one scattered page pool: two rounds of verify/commit give the logits and
+    lengths of contiguous caches bit for bit."""
+    from bit_exact_speculative_gb300 import xv
+    cfg, w, wd = stack
+    B, k = 8, 8
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500]
+    Lmax = 2304
+    n_pages = B * (Lmax // page) + 3
+    order = np.random.default_rng(page).permutation(n_pages)
+    A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd)
+    P = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd, page_size=page, n_pages=n_pages, page_order=order)
+    for rnd, keep in ((0, [3, 1, 8, 2, 5, 8, 1, 4]), (1, [8, 8, 1, 1, 2, 7, 3, 6])):
+        toks = dev(workloads.draft_tokens(cfg, 0, 10 + rnd, B, k))
+        lgA = A.verify(toks, k)[0].clone()
+        lgP = P.verify(toks, k)[0].clone()
+        assert same_bits(lgA, lgP), f"round {rnd}: paged logits differ"
+        kp = torch.tensor(keep, dtype=torch.int32, device="cuda")
+        A.commit(kp)
+        P.commit(kp)
+    assert torch.equal(A.state["ctx_len"], P.state["ctx_len"])
+    assert xv.xv_device_check() == 0
+
+
+def test_stack_ragged_k_per_sequence(stack):
+    """Four sequences verifying 1, 9, 5 and 3 tokens in one call, then (after keeping 1..k_b of
+    each) 9, 2, 1 and 6: each sequence's rows equal its own sequential decode bit for bit, and
+    n_accept counts only its own drafts."""
+    from bit_exact_speculative_gb300 import xv
+    cfg, w, wd = stack
+    B, kmax, Lmax = 4, 9, 2304
+    lens = [2183, 640, 1, 1500]
+    ks1, keep, ks2 = [1, 9, 5, 3], [1, 4, 5, 2], [9, 2, 1, 6]
+    t1 = workloads.draft_tokens(cfg, 0, 6, B, kmax)
+    t2 = workloads.draft_tokens(cfg, 0, 7, B, kmax)
+    A = gpu_stack(cfg, w, B, kmax, Lmax, lens, weights_dev=wd)
+    k1 = torch.tensor(ks1, dtype=torch.int32, device="cuda")
+    lg, am, na = A.verify(dev(t1), kmax, k_seq=k1)
+    lg1, am1, na1 = lg.clone().view(B, kmax, -1), host(am).reshape(B, kmax), host(na).copy()
+    A.commit(torch.tensor(keep, dtype=torch.int32, device="cuda"))
+    k2 = torch.tensor(ks2, dtype=torch.int32, device="cuda")
+    lg2 = A.verify(dev(t2), kmax, k_seq=k2)[0].clone().view(B, kmax, -1)
+    assert xv.xv_device_check() == 0
+    for b in range(B):
+        S = gpu_stack(cfg, w, B, kmax, Lmax, lens, weights_dev=wd, only=b)
+        lgS, amS = sequential(S, t1[b:b + 1, :ks1[b]], 1)
+        assert same_bits(lg1[b, :ks1[b]], lgS[0]), f"sequence {b}, round 1"
+        assert np.array_equal(am1[b, :ks1[b]], host(amS[0]))
+        assert int(na1[b]) == oracle.accept(t1[b, :ks1[b]], am1[b, :ks1[b]])
+        del S
+        S = gpu_stack(cfg, w, B, kmax, Lmax, lens, weights_dev=wd, only=b)
+        sequential(S, t1[b:b + 1, :keep[b]], 1)
+        lgS, _ = sequential(S, t2[b:b + 1, :ks2[b]], 1)
+        assert same_bits(lg2[b, :ks2[b]], lgS[0]), f"sequence {b}, round 2"
+        del S
+        torch.cuda.empty_cache()
+
+
+def test_ragged_commit_beyond_k_seq_is_flagged(tiny):
+    """Keeping more positions than a sequence verified is recorded (device error bit 8) and clamped."""
+    from bit_exact_speculative_gb300 import xv
+    cfg, w = tiny
+    B, k, Lmax = 2, 4, 256
+    A = gpu_stack(cfg, w, B, k, Lmax, [128, 100])
+    toks = workloads.draft_tokens(cfg, 0, 1, B, k)
+    A.verify(dev(toks), k, k_seq=torch.tensor([2, 4], dtype=torch.int32, device="cuda"))
+    A.commit(torch.tensor([3, 4], dtype=torch.int32, device="cuda"))
+    with pytest.raises(xv.XVError) as e:
+        xv.xv_device_check()
+    assert e.value.code == xv.XV_ERR_DEVICE_CHECK and "bits 0x8" in str(e.value)
+    assert xv.xv_device_check() == 0          # read and cleared
+    assert host(A.state["ctx_len"]).tolist() == [130, 104]
