@@ -39,16 +39,17 @@ def build(force: bool = False) -> str:
 class _Cfg(ctypes.Structure):
     _fields_ = [("H", i32), ("V", i32), ("F", i32), ("n_layers", i32), ("kind", vp),
                 ("gdn_h", i32), ("gdn_dk", i32), ("gdn_dv", i32),
-                ("at_hq", i32), ("at_hkv", i32), ("at_hd", i32), ("eps", dbl)]
+                ("at_hq", i32), ("at_hkv", i32), ("at_hd", i32), ("eps", dbl),
+                ("gdn_hk", i32), ("gdn_conv", i32), ("gdn_onorm", i32)]
 
 
 class _Weights(ctypes.Structure):
     _fields_ = [("embed", vp), ("norm1", vp), ("w_in", vp), ("w_out", vp), ("norm2", vp),
-                ("w_gu", vp), ("w_down", vp), ("final_norm", vp), ("lm_head", vp)]
+                ("w_gu", vp), ("w_down", vp), ("final_norm", vp), ("lm_head", vp), ("conv_w", vp), ("onorm", vp)]
 
 
 class _Seq(ctypes.Structure):
-    _fields_ = [("S", vp), ("kc", vp), ("vc", vp), ("Lmax", i32), ("len", i32)]
+    _fields_ = [("S", vp), ("kc", vp), ("vc", vp), ("Lmax", i32), ("len", i32), ("conv", vp)]
 
 
 def lib():
@@ -68,6 +69,10 @@ def lib():
         L.orc_gdn_step.argtypes = [vp, vp, vp, vp, dbl, dbl, i32, i32, vp]
         L.orc_gdn_step_bf16.argtypes = [vp, vp, vp, vp, u16, u16, i32, i32, i32, vp]
         L.orc_gdn_step_heads.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        L.orc_gdn_step_heads_grouped.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        L.orc_conv_step.argtypes = [vp, vp, vp, i32, i32, vp]
+        L.orc_gated_norm.argtypes = [vp, vp, vp, i32, dbl, vp]
+        L.orc_gdn_conv_dim.argtypes, L.orc_gdn_conv_dim.restype = [vp], i32
         L.orc_attn_row.argtypes = [vp, vp, vp, i64, i32, i32, dbl, vp]
         L.orc_attn_rows.argtypes = [vp, i64, vp, vp, i32, i32, i32, i32, i32, i32, dbl, vp, i64]
         L.orc_argmax.argtypes, L.orc_argmax.restype = [vp, i32], i32
@@ -179,6 +184,39 @@ def gdn_step_heads(S: np.ndarray, q, k, v, beta, gate, l2: bool) -> np.ndarray:
     return o
 
 
+def gdn_step_heads_grouped(S: np.ndarray, q, k, v, beta, gate, l2: bool) -> np.ndarray:
+    """Like :func:`gdn_step_heads` with Hk = q.shape[0] q/k heads for the Hv = S.shape[0] v heads."""
+    assert S.dtype == np.float64 and S.flags["C_CONTIGUOUS"]
+    Hv, dv, dk = S.shape
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    beta, gate = _c(beta, np.uint16), _c(gate, np.uint16)
+    Hk = q.shape[0]
+    o = np.empty((Hv, dv), dtype=np.uint16)
+    lib().orc_gdn_step_heads_grouped(_p(S), _p(q), _p(k), _p(v), _p(beta), _p(gate), Hv, Hk, dk, dv, int(l2), _p(o))
+    return o
+
+
+def conv_step(state: np.ndarray, x, w) -> np.ndarray:
+    """One causal-convolution step: state [Kc-1, C] bf16 (updated in place), x [C] bf16, w [C, Kc]
+    bf16 -> y [C] bf16."""
+    assert state.dtype == np.uint16 and state.flags["C_CONTIGUOUS"]
+    x, w = _c(x, np.uint16), _c(w, np.uint16)
+    C, Kc = w.shape
+    y = np.empty(C, dtype=np.uint16)
+    lib().orc_conv_step(_p(state), _p(x), _p(w), C, Kc, _p(y))
+    return y
+
+
+def gated_norm(o, z, w, eps: float = 1e-6) -> np.ndarray:
+    """Rows of o [..., n] normalised and gated by silu(z) with gain (1 + w)."""
+    o, z, w = _c(o, np.uint16), _c(z, np.uint16), _c(w, np.uint16)
+    n = o.shape[-1]
+    y = np.empty_like(o)
+    for r in range(o.size // n):
+        lib().orc_gated_norm(_p(o) + 2 * r * n, _p(z) + 2 * r * n, _p(w), n, eps, _p(y) + 2 * r * n)
+    return y
+
+
 def attn_row(q, K, V, length: int, scale: float) -> np.ndarray:
     q, K, V = _c(q, np.uint16), _c(K, np.uint16), _c(V, np.uint16)
     hd = q.shape[-1]
@@ -213,9 +251,13 @@ class Stack:
     """The hybrid decoder for ONE sequence, with its own fp64 GDN states and bf16 KV caches.
 
     ``cfg`` is a dict with H, V, F, kinds (list of 0 = GDN, 1 = attention),
-    gdn_h, gdn_dk, gdn_dv, at_hq, at_hkv, at_hd, eps.  ``weights`` maps
-    names to bf16 arrays: embed, final_norm, lm_head and per layer l the keys
-    ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``.
+    gdn_h, gdn_dk, gdn_dv, at_hq, at_hkv, at_hd, eps, and optionally gdn_hk
+    (q/k heads, default gdn_h), gdn_conv (convolution width, default 0 = none),
+    gdn_onorm (gated output norm, default 0).  ``weights`` maps names to bf16
+    arrays: embed, final_norm, lm_head and per layer l the keys
+    ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``
+    (and ``.conv_w`` [C, Kc], ``.onorm`` [dv] for GDN layers that use them).
+    The convolution states ``conv[l]`` [Kc-1, C] start at zero.
     """
 
     def __init__(self, cfg: dict, weights: dict, Lmax: int):
@@ -223,18 +265,23 @@ class Stack:
         L = len(cfg["kinds"])
         self._kind = np.asarray(cfg["kinds"], dtype=np.int32)
         self._c = _Cfg(cfg["H"], cfg["V"], cfg["F"], L, _p(self._kind), cfg["gdn_h"], cfg["gdn_dk"],
-                       cfg["gdn_dv"], cfg["at_hq"], cfg["at_hkv"], cfg["at_hd"], float(cfg.get("eps", 1e-6)))
+                       cfg["gdn_dv"], cfg["at_hq"], cfg["at_hkv"], cfg["at_hd"], float(cfg.get("eps", 1e-6)),
+                       cfg.get("gdn_hk", cfg["gdn_h"]), cfg.get("gdn_conv", 0), int(cfg.get("gdn_onorm", 0)))
         self._w = {k: _c(v, np.uint16) for k, v in weights.items()}
-        self._tabs = {n: (vp * L)(*[_p(self._w[f"{l}.{n}"]) for l in range(L)])
-                      for n in ("norm1", "w_in", "w_out", "norm2", "w_gu", "w_down")}
+        self._tabs = {n: (vp * L)(*[_p(self._w[f"{l}.{n}"]) if f"{l}.{n}" in self._w else None for l in range(L)])
+                      for n in ("norm1", "w_in", "w_out", "norm2", "w_gu", "w_down", "conv_w", "onorm")}
         addr = {n: ctypes.cast(t, vp).value for n, t in self._tabs.items()}
         self._W = _Weights(_p(self._w["embed"]), addr["norm1"], addr["w_in"], addr["w_out"], addr["norm2"],
-                           addr["w_gu"], addr["w_down"], _p(self._w["final_norm"]), _p(self._w["lm_head"]))
+                           addr["w_gu"], addr["w_down"], _p(self._w["final_norm"]), _p(self._w["lm_head"]),
+                           addr["conv_w"], addr["onorm"])
         self.Lmax = Lmax
-        self.S, self.kc, self.vc = {}, {}, {}
+        self.S, self.kc, self.vc, self.conv = {}, {}, {}, {}
+        Kc = self._c.gdn_conv
         for l, kd in enumerate(cfg["kinds"]):
             if kd == 0:
                 self.S[l] = np.zeros((cfg["gdn_h"], cfg["gdn_dv"], cfg["gdn_dk"]), dtype=np.float64)
+                if Kc > 0:
+                    self.conv[l] = np.zeros((Kc - 1, self.gdn_conv_dim), dtype=np.uint16)
             else:
                 self.kc[l] = np.zeros((cfg["at_hkv"], Lmax, cfg["at_hd"]), dtype=np.uint16)
                 self.vc[l] = np.zeros((cfg["at_hkv"], Lmax, cfg["at_hd"]), dtype=np.uint16)
@@ -242,10 +289,12 @@ class Stack:
 
     def snapshot(self):
         return ({l: s.copy() for l, s in self.S.items()}, {l: a.copy() for l, a in self.kc.items()},
-                {l: a.copy() for l, a in self.vc.items()}, self.len)
+                {l: a.copy() for l, a in self.vc.items()}, self.len, {l: a.copy() for l, a in self.conv.items()})
 
     def restore(self, snap):
-        S, kc, vc, n = snap
+        S, kc, vc, n, conv = snap
+        for l in conv:
+            self.conv[l][...] = conv[l]
         for l in S:
             self.S[l][...] = S[l]
         for l in kc:
@@ -259,8 +308,9 @@ class Stack:
         Sp = (vp * L)(*[_p(self.S[l]) if l in self.S else None for l in range(L)])
         Kp = (vp * L)(*[_p(self.kc[l]) if l in self.kc else None for l in range(L)])
         Vp = (vp * L)(*[_p(self.vc[l]) if l in self.vc else None for l in range(L)])
+        Cp = (vp * L)(*[_p(self.conv[l]) if l in self.conv else None for l in range(L)])
         seq = _Seq(ctypes.cast(Sp, vp).value, ctypes.cast(Kp, vp).value, ctypes.cast(Vp, vp).value,
-                   self.Lmax, self.len)
+                   self.Lmax, self.len, ctypes.cast(Cp, vp).value)
         logits = np.empty(self.cfg["V"], dtype=np.float64)
         lib().orc_decode_token(ctypes.byref(self._c), ctypes.byref(self._W), ctypes.byref(seq),
                                int(token), _p(logits))
@@ -278,3 +328,7 @@ class Stack:
     @property
     def attn_in_dim(self) -> int:
         return int(lib().orc_attn_in_dim(ctypes.byref(self._c)))
+
+    @property
+    def gdn_conv_dim(self) -> int:
+        return int(lib().orc_gdn_conv_dim(ctypes.byref(self._c)))

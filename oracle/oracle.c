@@ -36,8 +36,14 @@
  *   - rmsnorm(x) = x / sqrt(mean(x^2) + eps) * (1 + w);
  *   - GDN input projection columns = [q | k | v | b | a]; q and k are
  *     L2-normalised per head (x / sqrt(sum x^2 + 1e-6)); beta = sigmoid(b),
- *     gate = exp(-softplus(a)), both rounded to bf16 before use; no conv1d,
- *     no output norm, no q scale;
+ *     gate = exp(-softplus(a)), both rounded to bf16 before use; no q scale;
+ *   - the complete GDN layer (optional, off in the configurations the pages'
+ *     measurements concern) adds, as in gated-delta-net decoders: fewer q/k
+ *     heads than v heads (v head h reads q/k head h / (Hv/Hk)); a depthwise
+ *     causal convolution of width Kc with SiLU over the q|k|v channels, whose
+ *     state is the Kc-1 previous inputs; and an output RMSNorm per v head
+ *     gated by silu(z), z a further Hv*dv projection columns placed after v,
+ *     with the (1 + w) gain of the block's other norms;
  *   - attention input projection columns = [q | gate | k | v]; no RoPE;
  *     scale 1/sqrt(hd); output rounded to bf16, then times sigmoid(gate);
  *   - softplus(x) = x for x > 20, else log1p(exp(x));
@@ -50,7 +56,11 @@
  * integer products; the GDN step against the 1x1 closed form, a brute-force
  * 2x2 case in exact rationals, and the delta-rule invariants; attention
  * against L=1, identical keys, a dominant key and scipy's softmax; RMSNorm,
- * SwiGLU and the gates against constant-vector closed forms and scipy.
+ * SwiGLU and the gates against constant-vector closed forms and scipy; the
+ * causal convolution against numpy's convolution, its impulse response and
+ * its state; the gated norm against closed forms; grouped heads against the
+ * ungrouped step on repeated q/k; the complete GDN layer's column layout
+ * against repeated projection rows, a zeroed z block and a numpy composition.
  * orc_decode_token composes pinned functions; its composition is pinned only
  * structurally (identity path, KV append position), so its exact operation
  * order is "parity unpinned".
@@ -220,6 +230,44 @@ void orc_gdn_step_heads(double* S, const uint16_t* q, const uint16_t* k, const u
                           v + (int64_t)h * dv, beta[h], gate[h], dk, dv, l2, o + (int64_t)h * dv);
 }
 
+/* Grouped heads: v head h (of Hv) reads q and k of head h / (Hv / Hk).
+ * S [Hv][dv][dk], q/k [Hk][dk], v [Hv][dv], beta/gate [Hv], o [Hv][dv]. */
+void orc_gdn_step_heads_grouped(double* S, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const uint16_t* beta, const uint16_t* gate, int Hv, int Hk, int dk, int dv,
+                                int l2, uint16_t* o) {
+    int group = Hv / Hk;
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < Hv; ++h)
+        orc_gdn_step_bf16(S + (int64_t)h * dv * dk, q + (int64_t)(h / group) * dk, k + (int64_t)(h / group) * dk,
+                          v + (int64_t)h * dv, beta[h], gate[h], dk, dv, l2, o + (int64_t)h * dv);
+}
+
+/* One step of a depthwise causal convolution of width Kc over C channels,
+ * then SiLU.  The window of channel c is its Kc-1 previous inputs (state,
+ * [Kc-1][C], oldest row first) followed by x[c]; tap j = 0 meets the oldest:
+ *     y[c] = bf16( silu( sum_j w[c][j] * window_c[j] ) ).
+ * Afterwards the state forgets its oldest row and keeps x as its newest, so
+ * it always holds the last Kc-1 inputs (bf16 values moved, never rounded). */
+void orc_conv_step(uint16_t* state, const uint16_t* x, const uint16_t* w, int C, int Kc, uint16_t* y) {
+    for (int c = 0; c < C; ++c) {
+        double acc = 0.0;
+        for (int j = 0; j < Kc - 1; ++j) acc += orc_bf16_val(w[(int64_t)c * Kc + j]) * orc_bf16_val(state[(int64_t)j * C + c]);
+        acc += orc_bf16_val(w[(int64_t)c * Kc + Kc - 1]) * orc_bf16_val(x[c]);
+        y[c] = orc_bf16_rne(silu(acc));
+    }
+    for (int j = 0; j + 1 < Kc - 1; ++j) memcpy(state + (int64_t)j * C, state + (int64_t)(j + 1) * C, sizeof(uint16_t) * C);
+    if (Kc > 1) memcpy(state + (int64_t)(Kc - 2) * C, x, sizeof(uint16_t) * C);
+}
+
+/* The gated output norm of one head: y = bf16( o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z) ). */
+void orc_gated_norm(const uint16_t* o, const uint16_t* z, const uint16_t* w, int n, double eps, uint16_t* y) {
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += orc_bf16_val(o[i]) * orc_bf16_val(o[i]);
+    double inv = 1.0 / sqrt(ss / n + eps);
+    for (int i = 0; i < n; ++i)
+        y[i] = orc_bf16_rne(orc_bf16_val(o[i]) * inv * (1.0 + orc_bf16_val(w[i])) * silu(orc_bf16_val(z[i])));
+}
+
 /* ---------------------------------------------------------- attention */
 
 /* One decode row: softmax(q K^T * scale) V over positions [0, len), explicit
@@ -292,6 +340,9 @@ typedef struct {
     int gdn_h, gdn_dk, gdn_dv;
     int at_hq, at_hkv, at_hd;
     double eps;
+    int gdn_hk;                 /* q/k heads of a GDN layer (gdn_h v heads) */
+    int gdn_conv;               /* causal convolution width Kc (0: none) */
+    int gdn_onorm;              /* 1: gated output norm with z columns */
 } orc_cfg;
 
 typedef struct {
@@ -304,6 +355,8 @@ typedef struct {
     const uint16_t* const* w_down;     /* [L] -> [H][F] */
     const uint16_t* final_norm;        /* [H] */
     const uint16_t* lm_head;           /* [V][H] */
+    const uint16_t* const* conv_w;     /* [L] -> [C][Kc] (GDN layers with a convolution) */
+    const uint16_t* const* onorm;      /* [L] -> [dv] (GDN layers with the gated output norm) */
 } orc_weights;
 
 typedef struct {
@@ -312,6 +365,7 @@ typedef struct {
     uint16_t* const* vc;
     int Lmax;
     int len;                 /* tokens already in the KV cache */
+    uint16_t* const* conv;   /* [L] -> convolution state [Kc-1][C] bf16 (GDN layers with a convolution) */
 } orc_seq;
 
 /* y = bf16(x @ W^T) for one row */
@@ -327,27 +381,41 @@ static void residual(uint16_t* x, const uint16_t* y, int n) {
 }
 
 /* Input-projection widths (columns of w_in). */
-int orc_gdn_in_dim(const orc_cfg* c) { return c->gdn_h * (2 * c->gdn_dk + c->gdn_dv) + 2 * c->gdn_h; }
+int orc_gdn_in_dim(const orc_cfg* c) {
+    return 2 * c->gdn_hk * c->gdn_dk + c->gdn_h * c->gdn_dv * (c->gdn_onorm ? 2 : 1) + 2 * c->gdn_h;
+}
+/* Channels the convolution runs over: q | k | v. */
+int orc_gdn_conv_dim(const orc_cfg* c) { return 2 * c->gdn_hk * c->gdn_dk + c->gdn_h * c->gdn_dv; }
 int orc_attn_in_dim(const orc_cfg* c) { return 2 * c->at_hq * c->at_hd + 2 * c->at_hkv * c->at_hd; }
 
-static void gdn_mixer(const orc_cfg* c, double* S, const uint16_t* xn, const uint16_t* Win,
-                      const uint16_t* Wout, uint16_t* y) {
-    int Hg = c->gdn_h, dk = c->gdn_dk, dv = c->gdn_dv;
-    int in = orc_gdn_in_dim(c), inner = Hg * dv;
+static void gdn_mixer(const orc_cfg* c, double* S, uint16_t* conv_state, const uint16_t* conv_w,
+                      const uint16_t* onorm, const uint16_t* xn, const uint16_t* Win, const uint16_t* Wout,
+                      uint16_t* y) {
+    int Hg = c->gdn_h, Hk = c->gdn_hk, dk = c->gdn_dk, dv = c->gdn_dv;
+    int in = orc_gdn_in_dim(c), inner = Hg * dv, C = orc_gdn_conv_dim(c);
     uint16_t* p = (uint16_t*)malloc(sizeof(uint16_t) * in);
+    uint16_t* u = (uint16_t*)malloc(sizeof(uint16_t) * C);
     uint16_t* beta = (uint16_t*)malloc(sizeof(uint16_t) * Hg);
     uint16_t* gate = (uint16_t*)malloc(sizeof(uint16_t) * Hg);
     uint16_t* o = (uint16_t*)malloc(sizeof(uint16_t) * inner);
     proj(xn, Win, in, c->H, p);
-    const uint16_t* q = p;
-    const uint16_t* k = p + Hg * dk;
-    const uint16_t* v = p + 2 * Hg * dk;
-    const uint16_t* b = p + Hg * (2 * dk + dv);
+    const uint16_t* qkv = p;
+    if (c->gdn_conv > 0) {
+        orc_conv_step(conv_state, p, conv_w, C, c->gdn_conv, u);
+        qkv = u;
+    }
+    const uint16_t* q = qkv;
+    const uint16_t* k = qkv + Hk * dk;
+    const uint16_t* v = qkv + 2 * Hk * dk;
+    const uint16_t* z = p + C;                       /* only with the gated output norm */
+    const uint16_t* b = p + C + (c->gdn_onorm ? inner : 0);
     const uint16_t* a = b + Hg;
     orc_gdn_gates(b, a, Hg, beta, gate);
-    orc_gdn_step_heads(S, q, k, v, beta, gate, Hg, dk, dv, 1, o);
+    orc_gdn_step_heads_grouped(S, q, k, v, beta, gate, Hg, Hk, dk, dv, 1, o);
+    if (c->gdn_onorm)
+        for (int h = 0; h < Hg; ++h) orc_gated_norm(o + h * dv, z + h * dv, onorm, dv, c->eps, o + h * dv);
     proj(o, Wout, c->H, inner, y);
-    free(p); free(beta); free(gate); free(o);
+    free(p); free(u); free(beta); free(gate); free(o);
 }
 
 static void attn_mixer(const orc_cfg* c, orc_seq* s, int layer, const uint16_t* xn,
@@ -386,7 +454,9 @@ void orc_decode_token(const orc_cfg* c, const orc_weights* w, orc_seq* s, int32_
     memcpy(x, w->embed + (int64_t)token * H, sizeof(uint16_t) * H);
     for (int l = 0; l < c->n_layers; ++l) {
         orc_rmsnorm(x, w->norm1[l], H, c->eps, xn);
-        if (c->kind[l] == 0) gdn_mixer(c, s->S[l], xn, w->w_in[l], w->w_out[l], y);
+        if (c->kind[l] == 0)
+            gdn_mixer(c, s->S[l], c->gdn_conv > 0 ? s->conv[l] : NULL, c->gdn_conv > 0 ? w->conv_w[l] : NULL,
+                      c->gdn_onorm ? w->onorm[l] : NULL, xn, w->w_in[l], w->w_out[l], y);
         else attn_mixer(c, s, l, xn, w->w_in[l], w->w_out[l], y);
         residual(x, y, H);
         orc_rmsnorm(x, w->norm2[l], H, c->eps, xn);

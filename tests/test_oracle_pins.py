@@ -440,3 +440,201 @@ def test_stack_verify_is_sequential_decode_and_state_advances():
     assert not np.array_equal(a.S[0], snap[0][0])
     a.restore(snap)
     assert np.array_equal(a.S[0], snap[0][0]) and a.len == 3
+
+
+# ------------------------------------------------ complete GDN layer parts
+
+def test_conv_step_matches_numpy_convolve():
+    """Stepping a sequence through the convolution from a zero state is numpy's full convolution
+    with the taps reversed (tap Kc-1 meets the newest input), then SiLU, then bf16; the state
+    ends as the last Kc-1 inputs, oldest first."""
+    rng = np.random.default_rng(5)
+    C, Kc, T = 6, 4, 12
+    w = bf(rng.normal(0, 0.5, (C, Kc)))
+    xs = bf(rng.normal(0, 1, (T, C)))
+    st = np.zeros((Kc - 1, C), np.uint16)
+    ys = np.stack([oracle.conv_step(st, xs[t], w) for t in range(T)])
+    wf, xf = oracle.bf16_to_f64(w), oracle.bf16_to_f64(xs)
+    for c in range(C):
+        full = np.convolve(xf[:, c], wf[c, ::-1])[:T]
+        assert np.array_equal(ys[:, c], bf(full * sp.expit(full))), c
+    assert np.array_equal(st, xs[T - Kc + 1:])
+
+
+def test_conv_impulse_response_reads_taps_newest_last():
+    C, Kc = 3, 4
+    w = bf(np.array([[0.5, -1.0, 2.0, 3.0], [1.0, 1.0, 1.0, 1.0], [0.0, 0.0, 0.0, -2.0]]))
+    st = np.zeros((Kc - 1, C), np.uint16)
+    one, zero = bf(np.ones(C)), bf(np.zeros(C))
+    outs = [oracle.conv_step(st, one if t == 0 else zero, w) for t in range(Kc + 1)]
+    wf = oracle.bf16_to_f64(w)
+    for t in range(Kc):
+        tap = wf[:, Kc - 1 - t]
+        assert np.array_equal(outs[t], bf(tap * sp.expit(tap))), t
+    assert np.all(oracle.bf16_to_f64(outs[Kc]) == 0.0)
+
+
+def test_conv_state_is_the_prior_inputs():
+    """A state holding inputs x0, x1, x2 (oldest first) continues exactly as stepping them would."""
+    rng = np.random.default_rng(6)
+    C, Kc = 5, 4
+    w = bf(rng.normal(0, 0.5, (C, Kc)))
+    xs = bf(rng.normal(0, 1, (5, C)))
+    a = np.zeros((Kc - 1, C), np.uint16)
+    for t in range(3):
+        oracle.conv_step(a, xs[t], w)
+    b = xs[:3].copy()
+    assert np.array_equal(a, b)
+    assert np.array_equal(oracle.conv_step(a, xs[3], w), oracle.conv_step(b, xs[3], w))
+    # a width-1 convolution has no state: y = bf16(silu(w x))
+    w1 = bf(np.array([[2.0], [-0.5], [1.0], [0.0], [3.0]]))
+    y = oracle.conv_step(np.zeros((0, C), np.uint16), xs[4], w1)
+    v = oracle.bf16_to_f64(w1[:, 0]) * oracle.bf16_to_f64(xs[4])
+    assert np.array_equal(oracle.bf16_to_f64(y), oracle.bf16_to_f64(bf(v * sp.expit(v))))   # -0 == +0
+
+
+def test_gated_norm_closed_forms():
+    n = 16
+    w0 = bf(np.zeros(n))
+    o = bf(np.full(n, 2.0))
+    assert np.all(oracle.bf16_to_f64(oracle.gated_norm(o, bf(np.zeros(n)), w0)) == 0.0)      # silu(0) = 0
+    z30 = bf(np.full(n, 30.0))                         # silu(30) = 30 - 3e-12
+    assert np.all(oracle.bf16_to_f64(oracle.gated_norm(o, z30, w0, eps=0.0)) == 30.0)
+    assert np.all(oracle.bf16_to_f64(oracle.gated_norm(bf(np.full(n, -0.75)), z30, w0, eps=0.0)) == -30.0)
+    # the 3-4 pattern: mean square 12.5, eps 0.5 -> divide by sqrt(13); gain 1.25; z = 1 -> silu(1)
+    o34 = bf(np.array([3.0, 4.0] * 4))
+    y = oracle.bf16_to_f64(oracle.gated_norm(o34, bf(np.ones(8)), bf(np.full(8, 0.25)), eps=0.5))
+    exp = np.array([3.0, 4.0] * 4) / np.sqrt(13.0) * 1.25 * sp.expit(1.0)
+    assert np.array_equal(y, oracle.bf16_to_f64(bf(exp)))
+    # z = -1 at one position only flips that output's sign against z = 1 scaled by sigmoid(-1)/sigmoid(1)
+    z = bf(np.array([1.0] * 7 + [-1.0]))
+    y2 = oracle.bf16_to_f64(oracle.gated_norm(o34, z, bf(np.full(8, 0.25)), eps=0.5))
+    assert np.array_equal(y2[:7], y[:7])
+    assert y2[7] == oracle.bf16_to_f64(bf(-4.0 / np.sqrt(13.0) * 1.25 * sp.expit(-1.0)))
+
+
+def test_grouped_heads_equal_repeated_qk():
+    """v head h reads q/k head h // (Hv/Hk): the same as the ungrouped step with each q/k head
+    repeated Hv/Hk times in a row (and not as repeating the whole q/k block)."""
+    rng = np.random.default_rng(7)
+    Hv, Hk, dk, dv = 4, 2, 8, 8
+    S0 = rng.normal(0, 0.1, (Hv, dv, dk))
+    q, k = bf(rng.normal(0, 1, (Hk, dk))), bf(rng.normal(0, 1, (Hk, dk)))
+    v = bf(rng.normal(0, 1, (Hv, dv)))
+    beta, gate = bf(rng.uniform(0.1, 0.9, Hv)), bf(rng.uniform(0.5, 1.0, Hv))
+    S1, S2, S3 = S0.copy(), S0.copy(), S0.copy()
+    o1 = oracle.gdn_step_heads_grouped(S1, q, k, v, beta, gate, True)
+    o2 = oracle.gdn_step_heads(S2, np.repeat(q, 2, axis=0), np.repeat(k, 2, axis=0), v, beta, gate, True)
+    o3 = oracle.gdn_step_heads(S3, np.tile(q, (2, 1)), np.tile(k, (2, 1)), v, beta, gate, True)
+    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
+    assert not np.array_equal(o1, o3)
+
+
+def _full_tiny_cfg(**kw):
+    c = dict(_tiny_cfg(), gdn_h=4, gdn_hk=2, gdn_conv=4, gdn_onorm=1)
+    c.update(kw)
+    return c
+
+
+def _gdn_in(cfg):
+    hk = cfg.get("gdn_hk", cfg["gdn_h"])
+    return 2 * hk * cfg["gdn_dk"] + cfg["gdn_h"] * cfg["gdn_dv"] * (2 if cfg.get("gdn_onorm") else 1) + 2 * cfg["gdn_h"]
+
+
+def _full_weights(cfg, seed=0, zero_mlp=False):
+    H, F, V = cfg["H"], cfg["F"], cfg["V"]
+    ain = 2 * cfg["at_hq"] * cfg["at_hd"] + 2 * cfg["at_hkv"] * cfg["at_hd"]
+    hk = cfg.get("gdn_hk", cfg["gdn_h"])
+    C = 2 * hk * cfg["gdn_dk"] + cfg["gdn_h"] * cfg["gdn_dv"]
+    w = {"embed": synth.normal_bf16(seed, 1, (V, H)), "final_norm": synth.normal_bf16(seed, 2, H, sigma=0.02),
+         "lm_head": synth.normal_bf16(seed, 3, (V, H), sigma=0.02)}
+    for l, kd in enumerate(cfg["kinds"]):
+        inn = _gdn_in(cfg) if kd == 0 else ain
+        inner = cfg["gdn_h"] * cfg["gdn_dv"] if kd == 0 else cfg["at_hq"] * cfg["at_hd"]
+        w[f"{l}.norm1"] = synth.normal_bf16(seed, 10 + l, H, sigma=0.02)
+        w[f"{l}.w_in"] = synth.normal_bf16(seed, 20 + l, (inn, H), sigma=0.2)
+        w[f"{l}.w_out"] = synth.normal_bf16(seed, 30 + l, (H, inner), sigma=0.2)
+        w[f"{l}.norm2"] = synth.normal_bf16(seed, 40 + l, H, sigma=0.02)
+        w[f"{l}.w_gu"] = synth.normal_bf16(seed, 50 + l, (2 * F, H), sigma=0.2)
+        w[f"{l}.w_down"] = synth.normal_bf16(seed, 60 + l, (H, F), sigma=0.2)
+        if kd == 0 and cfg.get("gdn_conv"):
+            w[f"{l}.conv_w"] = synth.normal_bf16(seed, 70 + l, (C, cfg["gdn_conv"]), sigma=0.5)
+        if kd == 0 and cfg.get("gdn_onorm"):
+            w[f"{l}.onorm"] = synth.normal_bf16(seed, 80 + l, cfg["gdn_dv"], sigma=0.02)
+        if zero_mlp:
+            w[f"{l}.w_down"][...] = 0
+    return w
+
+
+def test_full_gdn_grouped_layout_equals_repeated_rows():
+    """Grouped q/k heads in the stack: the logits equal those of the ungrouped layer whose q and
+    k projection rows repeat each head's rows Hv/Hk times in a row (a column-layout pin)."""
+    cfg_g = _full_tiny_cfg(gdn_conv=0, gdn_onorm=0)
+    w_g = _full_weights(cfg_g)
+    cfg_p = _full_tiny_cfg(gdn_hk=4, gdn_conv=0, gdn_onorm=0)
+    w_p = dict(w_g)
+    dk, hk = cfg_g["gdn_dk"], cfg_g["gdn_hk"]
+    Win = w_g["0.w_in"]
+    qg = Win[:hk * dk].reshape(hk, dk, -1)
+    kg = Win[hk * dk:2 * hk * dk].reshape(hk, dk, -1)
+    rest = Win[2 * hk * dk:]
+    w_p["0.w_in"] = np.concatenate([np.repeat(qg, 2, axis=0).reshape(-1, Win.shape[1]),
+                                    np.repeat(kg, 2, axis=0).reshape(-1, Win.shape[1]), rest])
+    a, b = oracle.Stack(cfg_g, w_g, Lmax=16), oracle.Stack(cfg_p, w_p, Lmax=16)
+    for tok in (4, 9, 1):
+        assert np.array_equal(a.decode(tok), b.decode(tok))
+
+
+def test_full_gdn_z_columns_follow_v():
+    """With the z rows of the projection zeroed, silu(z) = 0 silences the GDN layer: the logits
+    equal those of the same stack with the GDN output projection zeroed."""
+    cfg = _full_tiny_cfg()
+    w = _full_weights(cfg)
+    C = 2 * cfg["gdn_hk"] * cfg["gdn_dk"] + cfg["gdn_h"] * cfg["gdn_dv"]
+    inner = cfg["gdn_h"] * cfg["gdn_dv"]
+    wz = dict(w)
+    wz["0.w_in"] = w["0.w_in"].copy()
+    wz["0.w_in"][C:C + inner] = 0
+    wo = dict(w)
+    wo["0.w_out"] = np.zeros_like(w["0.w_out"])
+    a, b = oracle.Stack(cfg, wz, Lmax=16), oracle.Stack(cfg, wo, Lmax=16)
+    for tok in (3, 8):
+        assert np.array_equal(a.decode(tok), b.decode(tok))
+    # the z block shifted by one head (head 0 keeps its z, the b rows lose theirs) leaves the layer active
+    wv = dict(w)
+    wv["0.w_in"] = w["0.w_in"].copy()
+    wv["0.w_in"][C + cfg["gdn_dv"]:C + inner + cfg["gdn_dv"]] = 0
+    assert not np.array_equal(oracle.Stack(cfg, wv, Lmax=16).decode(3), oracle.Stack(cfg, wo, Lmax=16).decode(3))
+
+
+def test_full_gdn_layer_composition_and_conv_state():
+    """One complete GDN layer (MLP silenced): the logits equal lm_head @ rmsnorm(x + W_out g),
+    with the projection done by numpy and g composed from the separately pinned convolution,
+    gates, grouped recurrence and gated norm; the convolution state holds the projected q|k|v
+    of the tokens seen, newest last."""
+    cfg = _full_tiny_cfg(kinds=[0])
+    w = _full_weights(cfg, zero_mlp=True)
+    st = oracle.Stack(cfg, w, Lmax=16)
+    H, h, hk, dk, dv, Kc = cfg["H"], cfg["gdn_h"], cfg["gdn_hk"], cfg["gdn_dk"], cfg["gdn_dv"], cfg["gdn_conv"]
+    C, inner = 2 * hk * dk + h * dv, h * dv
+    f = oracle.bf16_to_f64
+    S = np.zeros((h, dv, dk))
+    conv = np.zeros((Kc - 1, C), np.uint16)
+    proj_rows = []
+    for tok in (5, 2, 7):
+        logits = st.decode(tok)
+        x = f(w["embed"][tok])
+        xn = f(bf(x / np.sqrt(np.mean(x * x) + 1e-6) * (1 + f(w["0.norm1"]))))
+        p = bf(f(w["0.w_in"]) @ xn)
+        proj_rows.append(p[:C])
+        u = oracle.conv_step(conv, p[:C], w["0.conv_w"])
+        z = p[C:C + inner]
+        beta, gate = oracle.gdn_gates(p[C + inner:C + inner + h], p[C + inner + h:])
+        o = oracle.gdn_step_heads_grouped(S, u[:hk * dk].reshape(hk, dk), u[hk * dk:2 * hk * dk].reshape(hk, dk),
+                                          u[2 * hk * dk:].reshape(h, dv), beta, gate, True)
+        g = oracle.gated_norm(o, z.reshape(h, dv), w["0.onorm"])
+        y = bf(f(w["0.w_out"]) @ f(g.reshape(-1)))
+        r = f(bf(x + f(y)))
+        rn = f(bf(r / np.sqrt(np.mean(r * r) + 1e-6) * (1 + f(w["final_norm"]))))
+        np.testing.assert_allclose(logits, f(w["lm_head"]) @ rn, rtol=1e-12, atol=1e-13)
+    assert np.array_equal(st.conv[0], np.stack(proj_rows))
