@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lmax", type=int, default=None,
                     help="KV-cache capacity per sequence (default: enough for every step the run makes)")
+    ap.add_argument("--full-gdn", action="store_true",
+                    help="complete GDN layers: 16 q/k heads for the 32 v heads, width-4 causal convolution, "
+                         "gated output norm")
     ap.add_argument("--page-size", type=int, default=None,
                     help="paged KV cache with pages of this many positions (a multiple of 64)")
     ap.add_argument("--no-overlap", action="store_true", help="launch kernels without programmatic dependent launch")
@@ -143,7 +146,7 @@ def make_stack(args, device, rank=0, extra_rounds=0):
     from bit_exact_speculative_gb300.model import HybridStack
     from bit_exact_speculative_gb300.replicas import rank_seed
 
-    cfg = workloads.STACK
+    cfg = workloads.STACK_FULL if args.full_gdn else workloads.STACK
     w = workloads.weights(cfg, seed=0)
     wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
     B, k, L = args.batch, args.k, args.context
@@ -167,6 +170,8 @@ def make_stack(args, device, rank=0, extra_rounds=0):
         for l, kd in enumerate(cfg["kinds"]):
             if kd == 0:
                 stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seq, l, B)))
+                if cfg.get("gdn_conv"):
+                    stk.state[f"{l}.conv"].copy_(torch.from_numpy(workloads.conv_state(cfg, seq, l, B).view(np.int16)))
             else:
                 kc, vc = workloads.kv_cache(cfg, seq, l, B, [L] * B, Lmax)
                 stk.load_kv(l, torch.from_numpy(kc.view(np.int16)), torch.from_numpy(vc.view(np.int16)))
@@ -180,7 +185,8 @@ def make_stack(args, device, rank=0, extra_rounds=0):
 def gemm_shapes(cfg, M):
     """(N, K) of every GEMM in one verify step, with its output element size."""
     H, F, V = cfg["hidden"], cfg["mlp"], cfg["vocab"]
-    gin = cfg["gdn_heads"] * (2 * cfg["gdn_dk"] + cfg["gdn_dv"]) + 2 * cfg["gdn_heads"]
+    from bit_exact_speculative_gb300.model import gdn_in_dim
+    gin = gdn_in_dim(cfg)
     ain = 2 * cfg["attn_hq"] * cfg["attn_hd"] + 2 * cfg["attn_hkv"] * cfg["attn_hd"]
     out = []
     for kd in cfg["kinds"]:
@@ -548,6 +554,8 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD, "batch_per_gpu": B, "k": k, "context": args.context,
                        "parallelism": f"replicas x{world}", "overlap": not args.no_overlap,
                        "kv_cache": f"paged, {args.page_size}-position pages" if args.page_size else "contiguous",
+                       "gdn_layer": "complete (conv 4, gated norm, 16 q/k heads)" if args.full_gdn else
+                                    "recurrence only (32 q/k/v heads)",
                        "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
             "gpu_launches": int(launches),
             "roofline": {"bound": "hbm", "kernel": "gemm_small_m", "achieved": round(achieved, 1),

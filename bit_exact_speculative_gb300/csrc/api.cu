@@ -53,7 +53,8 @@ struct Trace {
     std::vector<long long> bytes;
 } g_trace;
 const char* const KIND_NAMES[K_COUNT] = {"gemm_small_m", "gdn", "attn_split", "attn_combine", "kv_append", "embed",
-                                         "rmsnorm", "swiglu", "gdn_gates", "argmax", "accept", "commit", "zero"};
+                                         "rmsnorm", "swiglu", "gdn_gates", "argmax", "accept", "commit", "zero",
+                                         "conv", "gated_norm"};
 }  // namespace
 
 void trace_pre(cudaStream_t s) {
@@ -252,14 +253,22 @@ xv_status xv_gdn_decode_step(float* state, const xv_gdn_steps* step, uint16_t* o
     if (xv_status st = gdn_steps_ok(step, "step", dk, H)) return st;
     if (o_stride < (long long)H * dv) return fail(XV_ERR_ARG, "gdn: o_stride below H*dv");
     GdnStepsDev p = to_dev(*step), none{};
-    return gdn_launch(state, p, nullptr, 1, 1, true, none, 0, o, o_stride, B, H, dk, dv, qk_l2norm,
+    return gdn_launch(state, p, nullptr, 1, 1, true, none, 0, o, o_stride, B, H, H, dk, dv, qk_l2norm,
                       reinterpret_cast<cudaStream_t>(s));
 }
 
 xv_status xv_gdn_verify(float* state, const xv_gdn_steps* pending, const int32_t* n_commit, int max_commit,
                         const xv_gdn_steps* draft, int k, uint16_t* o, long long o_stride, int B, int H, int dk, int dv,
                         int qk_l2norm, xv_stream s) {
+    return xv_gdn_verify_grouped(state, pending, n_commit, max_commit, draft, k, o, o_stride, B, H, H, dk, dv, qk_l2norm,
+                                 s);
+}
+
+xv_status xv_gdn_verify_grouped(float* state, const xv_gdn_steps* pending, const int32_t* n_commit, int max_commit,
+                                const xv_gdn_steps* draft, int k, uint16_t* o, long long o_stride, int B, int H, int Hk,
+                                int dk, int dv, int qk_l2norm, xv_stream s) {
     if (xv_status st = gdn_dims(B, H, dk, dv)) return st;
+    if (Hk < 1 || H % Hk) return fail(XV_ERR_ARG, "gdn: H = %d is not a multiple of Hk = %d", H, Hk);
     if (!state) return fail(XV_ERR_ARG, "gdn: null state");
     if (k < 0 || k > XV_KMAX) return fail(XV_ERR_UNSUPPORTED, "gdn: k = %d outside [0, %d]", k, XV_KMAX);
     if (max_commit < 0 || max_commit > XV_KMAX)
@@ -278,8 +287,38 @@ xv_status xv_gdn_verify(float* state, const xv_gdn_steps* pending, const int32_t
     if (k == 0 && max_commit == 0) return XV_OK;
     GdnStepsDev p = max_commit > 0 ? to_dev(*pending) : GdnStepsDev{};
     GdnStepsDev d = k > 0 ? to_dev(*draft) : GdnStepsDev{};
-    return gdn_launch(state, p, max_commit > 0 ? n_commit : nullptr, 0, max_commit, false, d, k, o, o_stride, B, H, dk,
-                      dv, qk_l2norm, reinterpret_cast<cudaStream_t>(s));
+    return gdn_launch(state, p, max_commit > 0 ? n_commit : nullptr, 0, max_commit, false, d, k, o, o_stride, B, H, Hk,
+                      dk, dv, qk_l2norm, reinterpret_cast<cudaStream_t>(s));
+}
+
+// ------------------------------------------------ complete GDN layer parts
+
+xv_status xv_gdn_conv(uint16_t* state, const uint16_t* pend, long long pend_stride, int pend_rows,
+                      const int32_t* n_commit, int max_commit, const uint16_t* x, long long x_stride, int x_rows, int k,
+                      const uint16_t* w, int C, int Kc, int B, uint16_t* y, long long y_stride, xv_stream s) {
+    if (!state || (k > 0 && !w)) return fail(XV_ERR_ARG, "conv: null state or taps");
+    if (B < 1 || B > 65535 || C < 1) return fail(XV_ERR_ARG, "conv: need 1 <= B <= 65535 and C >= 1");
+    if (Kc < 2 || Kc > XV_CONV_MAX) return fail(XV_ERR_UNSUPPORTED, "conv: width %d outside [2, %d]", Kc, XV_CONV_MAX);
+    if (k < 0 || k > XV_KMAX || max_commit < 0 || max_commit > XV_KMAX)
+        return fail(XV_ERR_UNSUPPORTED, "conv: k and max_commit must lie in [0, %d]", XV_KMAX);
+    if (max_commit > 0 && (!pend || !n_commit || pend_rows < max_commit || pend_stride < C))
+        return fail(XV_ERR_ARG, "conv: pending rows need pend, n_commit, pend_rows >= max_commit, pend_stride >= C");
+    if (k > 0 && (!x || !y || x_rows < k || x_stride < C || y_stride < C))
+        return fail(XV_ERR_ARG, "conv: the k rows need x, y, x_rows >= k and strides >= C");
+    if (k == 0 && max_commit == 0) return XV_OK;
+    return conv_launch(state, pend, pend_stride, pend_rows, n_commit, max_commit, x, x_stride, x_rows, k, w, C, Kc, B, y,
+                       y_stride, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z, long long z_stride, const uint16_t* w,
+                        int M, int H, int dv, float eps, uint16_t* y, long long y_stride, xv_stream s) {
+    if (!o || !z || !w || !y) return fail(XV_ERR_ARG, "gated norm: null pointer");
+    if (M < 1 || H < 1) return fail(XV_ERR_ARG, "gated norm: need M >= 1 and H >= 1");
+    if (dv < 32 || dv % 32 || dv > 256) return fail(XV_ERR_UNSUPPORTED, "gated norm: dv must be a multiple of 32 up to 256");
+    const long long row = static_cast<long long>(H) * dv;
+    if (o_stride < row || z_stride < row || y_stride < row) return fail(XV_ERR_ARG, "gated norm: row strides below H*dv");
+    if (static_cast<long long>(M) * H > (1ll << 30)) return fail(XV_ERR_UNSUPPORTED, "gated norm: too many rows");
+    return gated_norm_launch(o, o_stride, z, z_stride, w, M, H, dv, eps, y, y_stride, reinterpret_cast<cudaStream_t>(s));
 }
 
 // ------------------------------------------------------------- attention

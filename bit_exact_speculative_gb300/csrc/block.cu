@@ -23,6 +23,7 @@ namespace {
 struct Dims {
     int H, V, F, L;
     int gh, dk, dv, gin, ginner, gstride;
+    int hk, kc, onorm, cdim, cstride, bcol;   // q/k heads, conv width, gated norm, conv channels, b column
     int hq, hkv, hd, ain, ainner;
 };
 
@@ -39,17 +40,29 @@ xv_status check_cfg(const xv_block_config* c, Dims* d) {
     d->H = c->hidden; d->V = c->vocab; d->F = c->mlp; d->L = c->n_layers;
     d->gh = c->gdn_heads; d->dk = c->gdn_dk; d->dv = c->gdn_dv;
     d->hq = c->attn_hq; d->hkv = c->attn_hkv; d->hd = c->attn_hd;
-    d->gin = d->gh * (2 * d->dk + d->dv) + 2 * d->gh;
-    d->gstride = (d->gin + 7) / 8 * 8;
+    d->hk = c->gdn_qk_heads > 0 ? c->gdn_qk_heads : c->gdn_heads;
+    d->kc = c->gdn_conv;
+    d->onorm = c->gdn_out_norm ? 1 : 0;
     d->ginner = d->gh * d->dv;
+    d->cdim = 2 * d->hk * d->dk + d->ginner;
+    d->cstride = (d->cdim + 7) / 8 * 8;
+    d->bcol = d->cdim + (d->onorm ? d->ginner : 0);
+    d->gin = d->bcol + 2 * d->gh;
+    d->gstride = (d->gin + 7) / 8 * 8;
     d->ain = 2 * d->hq * d->hd + 2 * d->hkv * d->hd;
     d->ainner = d->hq * d->hd;
     if (has_gdn) {
         if ((d->dk != 64 && d->dk != 128) || d->dv < 32 || d->dv % 32 || d->gh < 1)
             return fail(XV_ERR_UNSUPPORTED, "block: GDN needs dk in {64,128}, dv a multiple of 32");
         if (d->ginner % 8) return fail(XV_ERR_UNSUPPORTED, "block: GDN heads*dv must be a multiple of 8");
+        if (d->hk < 1 || d->gh % d->hk) return fail(XV_ERR_ARG, "block: gdn_qk_heads must divide gdn_heads");
+        if (d->kc != 0 && (d->kc < 2 || d->kc > XV_CONV_MAX))
+            return fail(XV_ERR_UNSUPPORTED, "block: gdn_conv must be 0 or lie in [2, %d]", XV_CONV_MAX);
+        if (c->gdn_out_norm != 0 && c->gdn_out_norm != 1) return fail(XV_ERR_ARG, "block: gdn_out_norm must be 0 or 1");
+        if (d->onorm && d->dv > 256) return fail(XV_ERR_UNSUPPORTED, "block: the gated output norm needs dv <= 256");
     } else {
-        d->gin = d->ginner = 0;
+        d->gin = d->ginner = d->cdim = 0;
+        d->kc = d->onorm = 0;
     }
     if (has_attn) {
         if ((d->hd != 64 && d->hd != 256) || d->hkv < 1 || d->hq % d->hkv)
@@ -124,6 +137,16 @@ int xv_attn_in_dim(const xv_block_config* cfg) {
     return check_cfg(cfg, &d) ? -1 : d.ain;
 }
 
+int xv_gdn_conv_dim(const xv_block_config* cfg) {
+    Dims d{};
+    return check_cfg(cfg, &d) ? -1 : d.cdim;
+}
+
+int xv_gdn_conv_stride(const xv_block_config* cfg) {
+    Dims d{};
+    return check_cfg(cfg, &d) ? -1 : d.cstride;
+}
+
 size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax) {
     Dims d{};
     if (check_cfg(cfg, &d) || B < 1 || kmax < 1 || Lmax < 1) return 0;
@@ -150,6 +173,12 @@ static xv_status check_state(const Dims& d, const xv_block_config* cfg, const xv
                 return fail(XV_ERR_ARG, "block: GDN layer %d state incomplete", l);
             if (!aligned16(ls.gdn_hist[0]) || !aligned16(ls.gdn_hist[1]))
                 return fail(XV_ERR_UNSUPPORTED, "block: GDN history buffers must be 16-byte aligned");
+            if (d.kc) {
+                if (!ls.gdn_conv_state || !ls.gdn_conv_out[0] || !ls.gdn_conv_out[1])
+                    return fail(XV_ERR_ARG, "block: GDN layer %d convolution state or outputs missing", l);
+                if (!aligned16(ls.gdn_conv_out[0]) || !aligned16(ls.gdn_conv_out[1]))
+                    return fail(XV_ERR_UNSUPPORTED, "block: GDN convolution output buffers must be 16-byte aligned");
+            }
         } else {
             if (!ls.k_cache || !ls.v_cache) return fail(XV_ERR_ARG, "block: attention layer %d cache missing", l);
             if (!aligned16(ls.k_cache) || !aligned16(ls.v_cache))
@@ -175,8 +204,11 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
         const xv_layer_weights& lw = w->layers[l];
         if (!lw.norm1 || !lw.w_in || !lw.w_out || !lw.norm2 || !lw.w_gate_up || !lw.w_down)
             return fail(XV_ERR_ARG, "block: layer %d weights incomplete", l);
+        if (cfg->layer_kind[l] == 0 && ((d.kc && !lw.conv_w) || (d.onorm && !lw.out_norm)))
+            return fail(XV_ERR_ARG, "block: GDN layer %d convolution taps or output norm weights missing", l);
     }
     if (!tokens || !argmax || !n_accept) return fail(XV_ERR_ARG, "block: null tokens, argmax or n_accept");
+    if (st->last_k != 0) return fail(XV_ERR_ARG, "block: the previous verify has not been committed");
     const int B = st->B;
     if (k < 1 || k > st->kmax) return fail(XV_ERR_ARG, "block: k = %d outside [1, kmax = %d]", k, st->kmax);
     const int M = B * k;
@@ -204,15 +236,29 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
         if (cfg->layer_kind[l] == 0) {
             uint16_t* hist = ls.gdn_hist[par];
             XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, hist, d.gstride, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-            // the recurrence kernel reads q, k, v and the raw b, a columns of the history rows
-            const int bc = d.gh * (2 * d.dk + d.dv);
+            // the recurrence kernel reads q, k, v (the convolution's outputs, or the history rows
+            // themselves) and the raw b, a columns of the history rows
             const uint16_t* ph = ls.gdn_hist[par ^ 1];
-            GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, ph + bc, ph + bc + d.gh, d.gstride, d.gstride,
-                             st->pending_rows, 1};
-            GdnStepsDev draft{hist, hist + d.gh * d.dk, hist + 2 * d.gh * d.dk, hist + bc, hist + bc + d.gh, d.gstride,
+            const uint16_t* qkv_pend = ph;
+            const uint16_t* qkv_cur = hist;
+            long long qstride = d.gstride;
+            if (d.kc) {
+                XV_TRY(conv_launch(ls.gdn_conv_state, ph, d.gstride, st->pending_rows, st->n_commit, st->pending_rows,
+                                   hist, d.gstride, k, k, lw.conv_w, d.cdim, d.kc, B, ls.gdn_conv_out[par], d.cstride, s));
+                qkv_pend = ls.gdn_conv_out[par ^ 1];
+                qkv_cur = ls.gdn_conv_out[par];
+                qstride = d.cstride;
+            }
+            const int qk = d.hk * d.dk;
+            GdnStepsDev pend{qkv_pend, qkv_pend + qk, qkv_pend + 2 * qk, ph + d.bcol, ph + d.bcol + d.gh, qstride,
+                             d.gstride, st->pending_rows, 1};
+            GdnStepsDev draft{qkv_cur, qkv_cur + qk, qkv_cur + 2 * qk, hist + d.bcol, hist + d.bcol + d.gh, qstride,
                               d.gstride, k, 1};
             XV_TRY(gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, draft, k, c.obuf, d.ginner, B,
-                              d.gh, d.dk, d.dv, 1, s));
+                              d.gh, d.hk, d.dk, d.dv, 1, s));
+            if (d.onorm)
+                XV_TRY(gated_norm_launch(c.obuf, d.ginner, hist + d.cdim, d.gstride, lw.out_norm, M, d.gh, d.dv, eps,
+                                         c.obuf, d.ginner, s));
             XV_TRY(gemm_launch(c.obuf, d.ginner, lw.w_out, c.y, d.H, false, M, d.H, d.ginner, c.gemm_ws, c.gemm_ws_bytes, s));
         } else {
             XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, c.proj, d.ain, false, M, d.ain, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
@@ -276,18 +322,29 @@ xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stre
     Dims d{};
     if (xv_status e = check_cfg(cfg, &d)) return e;
     if (xv_status e = check_state(d, cfg, st)) return e;
+    if (st->last_k != 0) return fail(XV_ERR_ARG, "flush: the last verify has not been committed");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int par = st->parity & 1;
     for (int l = 0; l < d.L; ++l) {
         if (cfg->layer_kind[l] != 0) continue;
         xv_layer_state& ls = st->layers[l];
         const uint16_t* ph = ls.gdn_hist[par ^ 1];
-        const int bc = d.gh * (2 * d.dk + d.dv);
-        GdnStepsDev pend{ph, ph + d.gh * d.dk, ph + 2 * d.gh * d.dk, ph + bc, ph + bc + d.gh, d.gstride, d.gstride,
+        const uint16_t* qkv_pend = ph;
+        long long qstride = d.gstride;
+        if (d.kc) {
+            // the state takes the kept rows; no taps are needed without rows to convolve
+            if (xv_status e = conv_launch(ls.gdn_conv_state, ph, d.gstride, st->pending_rows, st->n_commit,
+                                          st->pending_rows, nullptr, 0, 0, 0, nullptr, d.cdim, d.kc, st->B, nullptr, 0, s))
+                return e;
+            qkv_pend = ls.gdn_conv_out[par ^ 1];
+            qstride = d.cstride;
+        }
+        const int qk = d.hk * d.dk;
+        GdnStepsDev pend{qkv_pend, qkv_pend + qk, qkv_pend + 2 * qk, ph + d.bcol, ph + d.bcol + d.gh, qstride, d.gstride,
                          st->pending_rows, 1};
         GdnStepsDev none{};
         if (xv_status e = gdn_launch(ls.gdn_state, pend, st->n_commit, 0, st->pending_rows, false, none, 0, nullptr, 0,
-                                     st->B, d.gh, d.dk, d.dv, 1, s))
+                                     st->B, d.gh, d.hk, d.dk, d.dv, 1, s))
             return e;
     }
     return zero_i32_launch(st->n_commit, st->B, s);

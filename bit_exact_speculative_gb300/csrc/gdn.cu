@@ -14,6 +14,9 @@
 // rounded once (explicit _rn intrinsics, so no contraction can differ):
 //     S <- a S;  r = S k;  u = b (v - r);  S <- S + u k^T;  o = S q.
 //
+// Grouped heads: with fewer q/k heads than v heads, v head h reads q/k head
+// h / qk_group (the state and v, beta, gate are per v head).
+//
 // Tiling: a CTA owns (sequence b, head h, 32 state rows) with 128 threads; a
 // row is split over 4 consecutive lanes (lane g holds float4 chunks g, g+4,
 // g+8, ... of the row).  Row dot products: two packed f32x2 accumulators (even
@@ -50,7 +53,7 @@ struct GdnArgs {
     int k;
     uint16_t* o;
     long long o_stride;
-    int H, dv, l2;
+    int H, dv, l2, qk_group;
     unsigned* err;
 };
 
@@ -89,11 +92,12 @@ static_assert(sizeof(StepRaw<64>) % 16 == 0 && sizeof(StepRaw<128>) % 16 == 0, "
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
 // Global address of a step's q, k or v piece (all 16-byte aligned: checked by the callers).
-__device__ __forceinline__ const uint16_t* piece(const GdnStepsDev& src, long long row, int h, int dk, int dv,
+// hk is the q/k head of v head h.
+__device__ __forceinline__ const uint16_t* piece(const GdnStepsDev& src, long long row, int h, int hk, int dk, int dv,
                                                  int row0, int which) {
     const long long base = row * src.qkv_stride;
-    if (which == 0) return src.q + base + static_cast<long long>(h) * dk;
-    if (which == 1) return src.k + base + static_cast<long long>(h) * dk;
+    if (which == 0) return src.q + base + static_cast<long long>(hk) * dk;
+    if (which == 1) return src.k + base + static_cast<long long>(hk) * dk;
     return src.v + base + static_cast<long long>(h) * dv + row0;
 }
 
@@ -248,13 +252,14 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
     for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], srow0 + static_cast<size_t>(r[x]) * DK, g);
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(sizeof(StepRaw<DK>)) * total);
+        const int hk = h / A.qk_group;
         for (int t = 0; t < total; ++t) {
             long long row;
             const GdnStepsDev& src = step_src(A, b, t, &row);
             const uint32_t d = smem_u32(&raw[t]);
-            bulk_load(d, piece(src, row, h, DK, A.dv, row0, 0), DK * 2, bar);
-            bulk_load(d + DK * 2, piece(src, row, h, DK, A.dv, row0, 1), DK * 2, bar);
-            bulk_load(d + DK * 4, piece(src, row, h, DK, A.dv, row0, 2), ROWS_PER_CTA * 2, bar);
+            bulk_load(d, piece(src, row, h, hk, DK, A.dv, row0, 0), DK * 2, bar);
+            bulk_load(d + DK * 2, piece(src, row, h, hk, DK, A.dv, row0, 1), DK * 2, bar);
+            bulk_load(d + DK * 4, piece(src, row, h, hk, DK, A.dv, row0, 2), ROWS_PER_CTA * 2, bar);
         }
     }
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
@@ -331,11 +336,12 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
 
 xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_commit, int n_fixed, int max_commit,
                      bool emit_replay, const GdnStepsDev& draft, int k, uint16_t* o, long long o_stride, int B, int H,
-                     int dk, int dv, int qk_l2norm, cudaStream_t s) {
+                     int Hk, int dk, int dv, int qk_l2norm, cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "gdn: device error word unavailable");
+    if (Hk < 1 || H % Hk) return fail(XV_ERR_ARG, "gdn: %d v heads are not a multiple of %d q/k heads", H, Hk);
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
-              qk_l2norm ? 1 : 0, err};
+              qk_l2norm ? 1 : 0, H / Hk, err};
     const int max_steps = max_commit + k;
     if (max_steps > THREADS / 2) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS / 2);
     dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
@@ -357,7 +363,7 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     // algorithmic bytes with every sequence replaying max_commit steps: the state
     // read (and written back after a replay), the step inputs, the outputs
     const long long state_bytes = 4ll * B * H * dv * dk;
-    const long long per_step = 2ll * B * H * (2 * dk + dv + 2);
+    const long long per_step = 2ll * B * (2 * Hk * dk + H * (dv + 2));
     const long long outs = 2ll * B * H * dv * (k + (emit_replay ? max_commit : 0));
     const long long bytes = state_bytes * (max_commit > 0 ? 2 : 1) + per_step * (max_commit + k) + outs;
     return launched("gdn_kernel", s, K_GDN, bytes);

@@ -15,7 +15,7 @@ xv_status fail(xv_status code, const char* fmt, ...);
 xv_status cuda_check(cudaError_t e, const char* what);
 // Kernel kinds of the launch trace.
 enum Kind : int { K_GEMM = 0, K_GDN, K_ATTN_SPLIT, K_ATTN_COMBINE, K_KV_APPEND, K_EMBED, K_RMSNORM, K_SWIGLU,
-                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_COUNT };
+                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_CONV, K_GNORM, K_COUNT };
 // Call right before a launch on stream s (records the opening trace event when tracing).
 void trace_pre(cudaStream_t s);
 // Checks the launch just made on the calling thread, counts it and closes its trace record.
@@ -99,7 +99,19 @@ struct GdnStepsDev {
 // `draft` writing o rows b*k + t.
 xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_commit, int n_fixed, int max_commit,
                      bool emit_replay, const GdnStepsDev& draft, int k, uint16_t* o, long long o_stride, int B, int H,
+                     int Hk,
                      int dk, int dv, int qk_l2norm, cudaStream_t s);
+
+// ---- complete GDN layer parts (gdn_layer.cu)
+// Shifts the n_commit[b] pending rows into the state [B, Kc-1, C], then convolves the k rows of x
+// (row b*x_rows + t) into y (row b*k + t): y = bf16(silu(taps . window)).
+xv_status conv_launch(uint16_t* state, const uint16_t* pend, long long pend_stride, int pend_rows,
+                      const int32_t* n_commit, int max_commit, const uint16_t* x, long long x_stride, int x_rows, int k,
+                      const uint16_t* w, int C, int Kc, int B, uint16_t* y, long long y_stride, cudaStream_t s);
+// y = bf16(o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z)) per (row, head) of dv values; y may be o.
+xv_status gated_norm_launch(const uint16_t* o, long long o_stride, const uint16_t* z, long long z_stride,
+                            const uint16_t* w, int M, int H, int dv, float eps, uint16_t* y, long long y_stride,
+                            cudaStream_t s);
 
 // ---- attention (attn.cu)
 constexpr int ATTN_SPLIT = 512;   // positions per split, fixed absolute boundaries

@@ -6,14 +6,17 @@ lengths, workspace) with torch, and calls ``xv_verify_block`` /
 ``xv_block_commit`` for each round.  All arithmetic happens in libxv.so.
 
 Config keys: hidden, vocab, mlp, kinds (0 = GDN, 1 = gated attention),
-gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv, attn_hd, rms_eps.
+gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv, attn_hd, rms_eps, and for a
+complete GDN layer gdn_qk_heads (default gdn_heads), gdn_conv (convolution
+width, default 0 = none) and gdn_out_norm (gated output norm, default 0).
 
 With ``page_size`` the attention caches are page pools shared by the
 sequences (:class:`KvPagePool` hands pages out); without, each sequence has a
 contiguous [Hkv, Lmax, hd] cache.  Both give the same bits.
 Weight keys: embed, final_norm, lm_head and per layer ``f"{l}.norm1"``,
-``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down`` (bf16 bit patterns in
-any 2-byte torch dtype, on the device).
+``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``, and ``.conv_w``
+[C, Kc] / ``.onorm`` [dv] for complete GDN layers (bf16 bit patterns in any
+2-byte torch dtype, on the device).
 """
 from __future__ import annotations
 
@@ -23,8 +26,18 @@ import torch
 from . import xv
 
 
+def gdn_qk_heads(cfg: dict) -> int:
+    return cfg.get("gdn_qk_heads") or cfg["gdn_heads"]
+
+
+def gdn_conv_dim(cfg: dict) -> int:
+    """Channels of the GDN convolution: q | k | v."""
+    return 2 * gdn_qk_heads(cfg) * cfg["gdn_dk"] + cfg["gdn_heads"] * cfg["gdn_dv"]
+
+
 def gdn_in_dim(cfg: dict) -> int:
-    return cfg["gdn_heads"] * (2 * cfg["gdn_dk"] + cfg["gdn_dv"]) + 2 * cfg["gdn_heads"]
+    z = cfg["gdn_heads"] * cfg["gdn_dv"] if cfg.get("gdn_out_norm") else 0
+    return gdn_conv_dim(cfg) + z + 2 * cfg["gdn_heads"]
 
 
 def gdn_hist_stride(cfg: dict) -> int:
@@ -44,6 +57,10 @@ def weight_shapes(cfg: dict) -> dict:
         inner = cfg["gdn_heads"] * cfg["gdn_dv"] if kd == 0 else cfg["attn_hq"] * cfg["attn_hd"]
         shapes.update({f"{l}.norm1": (H,), f"{l}.w_in": (inn, H), f"{l}.w_out": (H, inner), f"{l}.norm2": (H,),
                        f"{l}.w_gu": (2 * F, H), f"{l}.w_down": (H, F)})
+        if kd == 0 and cfg.get("gdn_conv"):
+            shapes[f"{l}.conv_w"] = (gdn_conv_dim(cfg), cfg["gdn_conv"])
+        if kd == 0 and cfg.get("gdn_out_norm"):
+            shapes[f"{l}.onorm"] = (cfg["gdn_dv"],)
     return shapes
 
 
@@ -137,6 +154,11 @@ class HybridStack:
                 st[f"{l}.state"] = torch.zeros((B, h, dv, dk), dtype=torch.float32, device=d)
                 for p in (0, 1):
                     st[f"{l}.hist{p}"] = torch.zeros((B * kmax, gdn_hist_stride(cfg)), dtype=torch.int16, device=d)
+                if cfg.get("gdn_conv"):
+                    C = gdn_conv_dim(cfg)
+                    st[f"{l}.conv"] = torch.zeros((B, cfg["gdn_conv"] - 1, C), dtype=torch.int16, device=d)
+                    for p in (0, 1):
+                        st[f"{l}.cout{p}"] = torch.zeros((B * kmax, (C + 7) // 8 * 8), dtype=torch.int16, device=d)
             else:
                 if self.pool is None:
                     shape = (B, cfg["attn_hkv"], Lmax, cfg["attn_hd"])

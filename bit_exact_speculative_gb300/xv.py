@@ -37,11 +37,13 @@ class GdnSteps(ctypes.Structure):
 class BlockConfig(ctypes.Structure):
     _fields_ = [("hidden", c_int), ("vocab", c_int), ("mlp", c_int), ("n_layers", c_int), ("layer_kind", vp),
                 ("gdn_heads", c_int), ("gdn_dk", c_int), ("gdn_dv", c_int),
-                ("attn_hq", c_int), ("attn_hkv", c_int), ("attn_hd", c_int), ("rms_eps", c_float)]
+                ("attn_hq", c_int), ("attn_hkv", c_int), ("attn_hd", c_int), ("rms_eps", c_float),
+                ("gdn_qk_heads", c_int), ("gdn_conv", c_int), ("gdn_out_norm", c_int)]
 
 
 class LayerWeights(ctypes.Structure):
-    _fields_ = [("norm1", vp), ("w_in", vp), ("w_out", vp), ("norm2", vp), ("w_gate_up", vp), ("w_down", vp)]
+    _fields_ = [("norm1", vp), ("w_in", vp), ("w_out", vp), ("norm2", vp), ("w_gate_up", vp), ("w_down", vp),
+                ("conv_w", vp), ("out_norm", vp)]
 
 
 class BlockWeights(ctypes.Structure):
@@ -49,7 +51,8 @@ class BlockWeights(ctypes.Structure):
 
 
 class LayerState(ctypes.Structure):
-    _fields_ = [("gdn_state", vp), ("gdn_hist", vp * 2), ("k_cache", vp), ("v_cache", vp)]
+    _fields_ = [("gdn_state", vp), ("gdn_hist", vp * 2), ("gdn_conv_state", vp), ("gdn_conv_out", vp * 2),
+                ("k_cache", vp), ("v_cache", vp)]
 
 
 class KvPages(ctypes.Structure):
@@ -83,6 +86,11 @@ _SIGS = {
     "xv_gdn_decode_step": ([vp, ctypes.POINTER(GdnSteps), vp, c_ll, c_int, c_int, c_int, c_int, c_int, vp], c_int),
     "xv_gdn_verify": ([vp, ctypes.POINTER(GdnSteps), vp, c_int, ctypes.POINTER(GdnSteps), c_int, vp, c_ll,
                        c_int, c_int, c_int, c_int, c_int, vp], c_int),
+    "xv_gdn_verify_grouped": ([vp, ctypes.POINTER(GdnSteps), vp, c_int, ctypes.POINTER(GdnSteps), c_int, vp, c_ll,
+                               c_int, c_int, c_int, c_int, c_int, c_int, vp], c_int),
+    "xv_gdn_conv": ([vp, vp, c_ll, c_int, vp, c_int, vp, c_ll, c_int, c_int, vp, c_int, c_int, c_int, vp, c_ll, vp],
+                    c_int),
+    "xv_gated_norm": ([vp, c_ll, vp, c_ll, vp, c_int, c_int, c_int, c_float, vp, c_ll, vp], c_int),
     "xv_attn_split_size": ([], c_int),
     "xv_attn_workspace_size": ([c_int, c_int, c_int, c_int, c_int], c_sz),
     "xv_attn_decode_rows": ([vp, c_ll, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
@@ -94,6 +102,8 @@ _SIGS = {
     "xv_gdn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_gdn_hist_stride": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_attn_in_dim": ([ctypes.POINTER(BlockConfig)], c_int),
+    "xv_gdn_conv_dim": ([ctypes.POINTER(BlockConfig)], c_int),
+    "xv_gdn_conv_stride": ([ctypes.POINTER(BlockConfig)], c_int),
     "xv_block_workspace_size": ([ctypes.POINTER(BlockConfig), c_int, c_int, c_int], c_sz),
     "xv_verify_block": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState),
                          vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
@@ -233,6 +243,28 @@ def xv_gdn_verify(state, pending, n_commit, max_commit: int, draft, k: int, o, o
                                B, H, dk, dv, int(qk_l2norm), _stream(stream)))
 
 
+def xv_gdn_verify_grouped(state, pending, n_commit, max_commit: int, draft, k: int, o, o_stride: int, B, H, Hk, dk,
+                          dv, qk_l2norm: bool, stream=None):
+    _check(lib().xv_gdn_verify_grouped(_ptr(state), None if pending is None else ctypes.byref(pending), _ptr(n_commit),
+                                       max_commit, None if draft is None else ctypes.byref(draft), k, _ptr(o),
+                                       o_stride, B, H, Hk, dk, dv, int(qk_l2norm), _stream(stream)))
+
+
+def xv_gdn_conv(state, pend, pend_stride: int, pend_rows: int, n_commit, max_commit: int, x, x_stride: int,
+                x_rows: int, k: int, w, B: int, y, y_stride: int, stream=None):
+    """state [B, Kc-1, C], w [C, Kc] (2-byte dtypes; w may be None when k = 0); see the C header
+    for the rows."""
+    C, Kc = state.shape[-1], state.shape[-2] + 1
+    _check(lib().xv_gdn_conv(_ptr(state), _ptr(pend), pend_stride, pend_rows, _ptr(n_commit), max_commit, _ptr(x),
+                             x_stride, x_rows, k, _ptr(w), C, Kc, B, _ptr(y), y_stride, _stream(stream)))
+
+
+def xv_gated_norm(o, o_stride: int, z, z_stride: int, w, M: int, H: int, dv: int, eps: float, y, y_stride: int,
+                  stream=None):
+    _check(lib().xv_gated_norm(_ptr(o), o_stride, _ptr(z), z_stride, _ptr(w), M, H, dv, float(eps), _ptr(y),
+                               y_stride, _stream(stream)))
+
+
 # ------------------------------------------------------------- attention
 
 def xv_attn_split_size() -> int:
@@ -283,9 +315,10 @@ class Block:
 
     ``cfg`` is a dict (hidden, vocab, mlp, kinds, gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv,
     attn_hd, rms_eps); ``weights`` a dict of device tensors (embed, final_norm, lm_head and per
-    layer ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``);
-    ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1`` or
-    ``.kc``, ``.vc``).  With ``pages`` (a :class:`KvPages` over ``state["page_table"]``) the
+    layer ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down`` and, for complete GDN
+    layers, ``.conv_w``, ``.onorm``);
+    ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1`` (and
+    ``.conv``, ``.cout0``, ``.cout1`` with a convolution) or ``.kc``, ``.vc``).  With ``pages`` (a :class:`KvPages` over ``state["page_table"]``) the
     attention caches are page pools.  Tensors are kept referenced here.
     """
 
@@ -296,21 +329,27 @@ class Block:
         self.cfg = BlockConfig(cfg["hidden"], cfg["vocab"], cfg["mlp"], len(kinds),
                                ctypes.cast(self._kinds, vp).value, cfg.get("gdn_heads", 0), cfg.get("gdn_dk", 0),
                                cfg.get("gdn_dv", 0), cfg.get("attn_hq", 0), cfg.get("attn_hkv", 0),
-                               cfg.get("attn_hd", 0), float(cfg.get("rms_eps", 1e-6)))
+                               cfg.get("attn_hd", 0), float(cfg.get("rms_eps", 1e-6)), cfg.get("gdn_qk_heads", 0),
+                               cfg.get("gdn_conv", 0), int(cfg.get("gdn_out_norm", 0)))
         self._keep = [weights, state]
-        lw = [LayerWeights(*[weights[f"{l}.{n}"].data_ptr() for n in ("norm1", "w_in", "w_out", "norm2", "w_gu",
-                                                                        "w_down")]) for l in range(len(kinds))]
+        names = ("norm1", "w_in", "w_out", "norm2", "w_gu", "w_down", "conv_w", "onorm")
+        lw = [LayerWeights(*[weights[f"{l}.{n}"].data_ptr() if f"{l}.{n}" in weights else None for n in names])
+              for l in range(len(kinds))]
         self._lw = (LayerWeights * len(kinds))(*lw)
         self.weights = BlockWeights(weights["embed"].data_ptr(), ctypes.cast(self._lw, vp).value,
                                     weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr())
         ls = []
         for l, kd in enumerate(kinds):
             if kd == 0:
+                conv = f"{l}.conv" in state
                 ls.append(LayerState(state[f"{l}.state"].data_ptr(),
                                      (vp * 2)(state[f"{l}.hist0"].data_ptr(), state[f"{l}.hist1"].data_ptr()),
-                                     None, None))
+                                     state[f"{l}.conv"].data_ptr() if conv else None,
+                                     (vp * 2)(state[f"{l}.cout0"].data_ptr(), state[f"{l}.cout1"].data_ptr())
+                                     if conv else (vp * 2)(None, None), None, None))
             else:
-                ls.append(LayerState(None, (vp * 2)(None, None), state[f"{l}.kc"].data_ptr(), state[f"{l}.vc"].data_ptr()))
+                ls.append(LayerState(None, (vp * 2)(None, None), None, (vp * 2)(None, None), state[f"{l}.kc"].data_ptr(),
+                                     state[f"{l}.vc"].data_ptr()))
         self._ls = (LayerState * len(kinds))(*ls)
         self.state = BlockState(B, kmax, Lmax, state["ctx_len"].data_ptr(), state["n_commit"].data_ptr(), 0, kmax,
                                 ctx0, 0, ctypes.cast(self._ls, vp).value, pages if pages is not None else KvPages(),
@@ -324,6 +363,9 @@ class Block:
 
     def attn_in_dim(self) -> int:
         return int(lib().xv_attn_in_dim(ctypes.byref(self.cfg)))
+
+    def gdn_conv_stride(self) -> int:
+        return int(lib().xv_gdn_conv_stride(ctypes.byref(self.cfg)))
 
 
 def xv_verify_block(blk: Block, tokens, k: int, logits, argmax, n_accept, ws, stream=None):

@@ -58,6 +58,7 @@ typedef int xv_status;
 #define XV_ABI_VERSION 2
 #define XV_GEMM_M_MAX 64        /* rows per small-M GEMM call */
 #define XV_KMAX 16              /* draft tokens per sequence per verify call */
+#define XV_CONV_MAX 8           /* widest causal convolution of a complete GDN layer */
 
 /* Version of this header's ABI (XV_ABI_VERSION). */
 int xv_abi_version(void);
@@ -194,6 +195,41 @@ xv_status xv_gdn_verify(float* state, const xv_gdn_steps* pending, const int32_t
                         const xv_gdn_steps* draft, int k, uint16_t* o, long long o_stride,
                         int B, int H, int dk, int dv, int qk_l2norm, xv_stream s);
 
+/* xv_gdn_verify with grouped heads: H v heads (state, v, beta, gate, o per v
+ * head) over Hk q/k heads, H a multiple of Hk; v head h reads q and k of head
+ * h / (H / Hk) (q and k rows hold Hk*dk values). */
+xv_status xv_gdn_verify_grouped(float* state, const xv_gdn_steps* pending, const int32_t* n_commit, int max_commit,
+                                const xv_gdn_steps* draft, int k, uint16_t* o, long long o_stride,
+                                int B, int H, int Hk, int dk, int dv, int qk_l2norm, xv_stream s);
+
+/* ------------------------------------------ complete GDN layer parts
+ * Not on the pages (which measure GDN layers without them); the complete
+ * layer of gated-delta-net decoders adds a depthwise causal convolution over
+ * the q|k|v projection channels and a per-head output RMSNorm gated by
+ * silu(z).  Both are computed per output from its own inputs in a fixed
+ * order, so verify rows get the bits of decode steps.
+ *
+ * Convolution of width Kc (2..XV_CONV_MAX) over C channels for B sequences.
+ * state [B, Kc-1, C] bf16 holds each sequence's Kc-1 previous inputs, oldest
+ * first.  The call first shifts the n_commit[b] (device, 0..max_commit)
+ * pending rows pend[b*pend_rows + t] into the state and writes it back, then
+ * convolves the k rows x[b*x_rows + t]:
+ *     y[b*k + t][c] = bf16( silu( sum_j w[c][j] * window[j] ) ),
+ * the window being the Kc-1 prior inputs then x (tap Kc-1 meets the newest).
+ * The k rows do not enter the state: the caller passes them as the next
+ * call's pending rows (deferred commit, as for the recurrence).  Strides are
+ * in elements; w is [C, Kc] bf16. */
+xv_status xv_gdn_conv(uint16_t* state, const uint16_t* pend, long long pend_stride, int pend_rows,
+                      const int32_t* n_commit, int max_commit, const uint16_t* x, long long x_stride, int x_rows,
+                      int k, const uint16_t* w, int C, int Kc, int B, uint16_t* y, long long y_stride, xv_stream s);
+
+/* Gated output norm over M rows of H heads of dv values (dv a multiple of 32
+ * up to 256): y = bf16( o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z) ), w
+ * [dv]; y may be o. */
+xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z, long long z_stride,
+                        const uint16_t* w, int M, int H, int dv, float eps, uint16_t* y, long long y_stride,
+                        xv_stream s);
+
 /* ------------------------------------------------------------- attention
  * Decode-row attention over a bf16 KV cache.  [post]: verify attention runs
  * as decode rows, one per draft position.  Row r of sequence b is the query
@@ -267,8 +303,13 @@ xv_status xv_kv_append_paged(const uint16_t* kv_src, long long src_stride, const
  * compared with the target's argmax).  Decode is k = 1 through the same path.
  *
  * Column layouts of the input projections (rows of w_in):
- *   GDN:       [ q (H*dk) | k (H*dk) | v (H*dv) | b (H) | a (H) ]
+ *   GDN:       [ q (Hk*dk) | k (Hk*dk) | v (H*dv) | z (H*dv, with the gated
+ *                output norm only) | b (H) | a (H) ]   (H = gdn_heads v heads,
+ *                Hk = gdn_qk_heads q/k heads, Hk = H unless set)
  *   attention: [ q (Hq*hd) | gate (Hq*hd) | k (Hkv*hd) | v (Hkv*hd) ]
+ * A complete GDN layer (gdn_conv > 0 and/or gdn_out_norm) runs the q|k|v
+ * columns through the causal convolution (xv_gdn_conv) before the
+ * recurrence and its output through the gated norm (xv_gated_norm).
  * RMSNorm: y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ). */
 typedef struct {
     int hidden;               /* H */
@@ -279,6 +320,9 @@ typedef struct {
     int gdn_heads, gdn_dk, gdn_dv;
     int attn_hq, attn_hkv, attn_hd;
     float rms_eps;
+    int gdn_qk_heads;         /* q/k heads of a GDN layer (0: gdn_heads); divides gdn_heads */
+    int gdn_conv;             /* causal convolution width over q|k|v (0: none, else 2..XV_CONV_MAX) */
+    int gdn_out_norm;         /* 1: z columns after v and the gated output norm */
 } xv_block_config;
 
 typedef struct {
@@ -288,6 +332,8 @@ typedef struct {
     const uint16_t* norm2;    /* [H] */
     const uint16_t* w_gate_up;/* [2F, H]: F gate rows, then F up rows */
     const uint16_t* w_down;   /* [H, F] */
+    const uint16_t* conv_w;   /* GDN layer with a convolution: [C, Kc], C = xv_gdn_conv_dim(cfg) */
+    const uint16_t* out_norm; /* GDN layer with the gated output norm: [dv] */
 } xv_layer_weights;
 
 typedef struct {
@@ -300,6 +346,9 @@ typedef struct {
 typedef struct {
     float* gdn_state;         /* GDN layer: [B, heads, dv, dk] fp32 */
     uint16_t* gdn_hist[2];    /* GDN layer: two [B*kmax, xv_gdn_hist_stride(cfg)] bf16 projection buffers */
+    uint16_t* gdn_conv_state; /* GDN layer with a convolution: [B, Kc-1, C] bf16, prior inputs, oldest first */
+    uint16_t* gdn_conv_out[2];/* GDN layer with a convolution: two [B*kmax, xv_gdn_conv_stride(cfg)] bf16
+                                 buffers of convolution outputs (this call's and the pending ones) */
     uint16_t* k_cache;        /* attention layer: [B, Hkv, Lmax, hd] bf16, or a pool
                                  [kv_pages.n_pages, Hkv, page_size, hd] when the state is paged */
     uint16_t* v_cache;
@@ -327,6 +376,10 @@ int xv_gdn_in_dim(const xv_block_config* cfg);
 /* Row stride (elements) of the GDN step-history buffers: xv_gdn_in_dim rounded up to 8. */
 int xv_gdn_hist_stride(const xv_block_config* cfg);
 int xv_attn_in_dim(const xv_block_config* cfg);
+/* Channels of a GDN layer's convolution (q|k|v: 2*Hk*dk + H*dv) and the row stride of its output
+ * buffers (rounded up to 8). */
+int xv_gdn_conv_dim(const xv_block_config* cfg);
+int xv_gdn_conv_stride(const xv_block_config* cfg);
 
 /* Workspace for xv_verify_block with B sequences of up to kmax tokens. */
 size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);

@@ -21,6 +21,8 @@ def gpu_stack(cfg, w_np, B, kmax, Lmax, ctx_lens, seed=0, weights_dev=None, page
     for l, kd in enumerate(cfg["kinds"]):
         if kd == 0:
             stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seed, l, B)[sel]))
+            if cfg.get("gdn_conv"):
+                stk.state[f"{l}.conv"].copy_(torch.from_numpy(workloads.conv_state(cfg, seed, l, B)[sel].view(np.int16)))
         else:
             kc, vc = workloads.kv_cache(cfg, seed, l, B, ctx_lens, Lmax)
             stk.load_kv(l, torch.from_numpy(kc[sel].view(np.int16)), torch.from_numpy(vc[sel].view(np.int16)))
@@ -34,6 +36,8 @@ def oracle_stack(cfg, w_np, b, B, ctx_lens, Lmax, seed=0):
     for l, kd in enumerate(cfg["kinds"]):
         if kd == 0:
             st.S[l][...] = workloads.gdn_state(cfg, seed, l, B)[b].astype(np.float64)
+            if cfg.get("gdn_conv"):
+                st.conv[l][...] = workloads.conv_state(cfg, seed, l, B)[b]
         else:
             kc, vc = workloads.kv_cache(cfg, seed, l, B, ctx_lens, Lmax)
             st.kc[l][...] = kc[b]
