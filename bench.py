@@ -257,7 +257,14 @@ def kernel_rooflines(xv, device, peak):
             for i in range(nc):
                 xv.xv_gemm_small_m(X, Ws[i], Y, ws)
             recs = _traced_median_ms(xv, lambda i: xv.xv_gemm_small_m(X, Ws[i % nc], Y, ws), 3 * nc)
-            ms = float(np.median([t for k, t, _ in recs if k == "gemm_small_m"]))
+            # a launch's time includes its split-K combine kernel where it has one (M > 8, > 4 segments)
+            per_launch = []
+            for k_, t_, _ in recs:
+                if k_ == "gemm_small_m":
+                    per_launch.append(t_)
+                elif k_ == "gemm_combine" and per_launch:
+                    per_launch[-1] += t_
+            ms = float(np.median(per_launch))
             nbytes = 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)
             gem[f"{name}_M{M}"] = {"N": N, "K": K, "splits": xv.xv_gemm_splits(N, K), "us": round(ms * 1e3, 2),
                                    "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
@@ -512,7 +519,8 @@ def run_gpu(args):
         d[1] += tms
         d[2] += nb
     g = per_kind.get("gemm_small_m", [0, 0.0, 0])
-    gemm_ms_per_launch = g[1] / max(g[0], 1)
+    gc = per_kind.get("gemm_combine", [0, 0.0, 0])    # split-K combines of the M > 8 narrow shapes
+    gemm_ms_per_launch = (g[1] + gc[1]) / max(g[0], 1)
     gemm_bytes_per_launch = g[2] / max(g[0], 1)
     achieved = gemm_bytes_per_launch / (gemm_ms_per_launch / 1e3) / 1e9
     peak, peak_kind = peaks()

@@ -54,7 +54,7 @@ struct Trace {
 } g_trace;
 const char* const KIND_NAMES[K_COUNT] = {"gemm_small_m", "gdn", "attn_split", "attn_combine", "kv_append", "embed",
                                          "rmsnorm", "swiglu", "gdn_gates", "argmax", "accept", "commit", "zero",
-                                         "conv", "gated_norm"};
+                                         "conv", "gated_norm", "gemm_combine"};
 }  // namespace
 
 void trace_pre(cudaStream_t s) {

@@ -249,6 +249,13 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
                 }
             }
         }
+    } else if (!cnt) {
+        // the partials are combined by gemm_combine_kernel, launched next on the stream
+        if (live) {
+#pragma unroll
+            for (int m = 0; m < GEMM_TOK; ++m)
+                if (m < M) part[(static_cast<size_t>(seg) * M + m) * N + n] = acc[m];
+        }
     } else {
         if (live) {
 #pragma unroll
@@ -305,6 +312,29 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Y[m][n] = p_0 + p_1 + ... + p_{S-1} (segment order, the sum of the in-kernel combines) of the
+// partials part[(seg*M + m)*N + n]; one thread per output, every segment's load in flight at once.
+constexpr int COMBINE_THREADS = 256;
+template <bool F32OUT>
+__global__ void __launch_bounds__(COMBINE_THREADS)
+    gemm_combine_kernel(const float* __restrict__ part, void* __restrict__ Y, int ldy, int M, int N, int S) {
+    griddep_launch();
+    griddep_wait();
+    const long long idx = static_cast<long long>(blockIdx.x) * COMBINE_THREADS + threadIdx.x;
+    if (idx >= static_cast<long long>(M) * N) return;
+    const int m = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = q < S ? __ldcg(part + (static_cast<size_t>(q) * M + m) * N + n) : 0.f;
+    float r = v[0];
+#pragma unroll
+    for (int q = 1; q < 16; ++q)
+        if (q < S) r = __fadd_rn(r, v[q]);
+    const size_t o = static_cast<size_t>(m) * ldy + n;
+    if (F32OUT) static_cast<float*>(Y)[o] = r;
+    else static_cast<uint16_t*>(Y)[o] = f32_to_bf16(r);
+}
+
 inline int num_tiles(int N) { return ceil_div(N, GEMM_BN); }
 inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -315,7 +345,11 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // the two-way split of the gate/up projection (544 CTAs instead of 272, about 1.8 waves of 2 CTAs
 // per SM, so the hardware evens out SMs that stream at different rates) took the step from 895
 // to 862 us; two-way splits of the input projections (instead of 3 and 2) and of the LM head a
-// further 5 us; 3 or 4 segments, or clusters of up to 8 for the narrow shapes, were slower.
+// further 5 us; 3 segments for the GDN input projection were slower.  The narrow shapes take as
+// many segments as fit in one wave of 2 CTAs per SM (the three N = 5120 projections: 7 segments,
+// 280 CTAs, combined through the workspace): 909.5 -> 889.4 us per step against 4 segments in
+// clusters (160 CTAs); 3 segments (120 CTAs) 967 us, 8 (320 CTAs, a second wave) 984 us; the
+// workspace combine instead of clusters for the splits of 2..4 cost 30 us.
 int gemm_splits(int N, int K) {
     const int tiles = num_tiles(N);
     const int nkb = ceil_div(K, GEMM_BK);
@@ -325,7 +359,6 @@ int gemm_splits(int N, int K) {
     } else {
         s = (SM_COUNT_TARGET * RESIDENT_PER_SM) / tiles;
         if (s > 16) s = 16;
-        if (s > CLUSTER_MAX && tiles * CLUSTER_MAX >= SM_COUNT_TARGET) s = CLUSTER_MAX;
     }
     while (s > 1 && nkb / s < 4) --s;
     return s;
@@ -369,8 +402,11 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     const int tiles = num_tiles(N), S = gemm_splits(N, K), nkb = ceil_div(K, GEMM_BK);
     float* part = nullptr;
     unsigned* cnt = nullptr;
+    // Past 8 token rows the last-arriving CTA's combine is a long serial tail (one round trip per
+    // 8 rows); a separate kernel with a thread per output combines them in one round trip.
+    const bool sep_combine = S > CLUSTER_MAX && M > X_SMALL_M;
     if (S > CLUSTER_MAX) {
-        cnt = static_cast<unsigned*>(ws);
+        cnt = sep_combine ? nullptr : static_cast<unsigned*>(ws);
         part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + COUNTER_BYTES);
     }
     static bool attr_set[2] = {false, false};
@@ -392,7 +428,15 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
     else
         launch_k(kern, grid, dim3(128), smem, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster, xb, xr);
     const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
-    return launched("gemm_small_m_kernel", s, K_GEMM, bytes);
+    if (xv_status st = launched("gemm_small_m_kernel", s, K_GEMM, bytes)) return st;
+    if (sep_combine) {
+        trace_pre(s);
+        const long long outs = static_cast<long long>(M) * N;
+        auto ck = f32out ? gemm_combine_kernel<true> : gemm_combine_kernel<false>;
+        launch_k(ck, dim3(ceil_div(outs, COMBINE_THREADS)), dim3(COMBINE_THREADS), 0, s, part, Y, ldy, M, N, S);
+        return launched("gemm_combine_kernel", s, K_GEMM_COMBINE, 4ll * S * outs + outs * (f32out ? 4 : 2));
+    }
+    return XV_OK;
 }
 
 }  // namespace xv

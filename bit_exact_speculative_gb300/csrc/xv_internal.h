@@ -15,7 +15,7 @@ xv_status fail(xv_status code, const char* fmt, ...);
 xv_status cuda_check(cudaError_t e, const char* what);
 // Kernel kinds of the launch trace.
 enum Kind : int { K_GEMM = 0, K_GDN, K_ATTN_SPLIT, K_ATTN_COMBINE, K_KV_APPEND, K_EMBED, K_RMSNORM, K_SWIGLU,
-                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_CONV, K_GNORM, K_COUNT };
+                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_CONV, K_GNORM, K_GEMM_COMBINE, K_COUNT };
 // Call right before a launch on stream s (records the opening trace event when tracing).
 void trace_pre(cudaStream_t s);
 // Checks the launch just made on the calling thread, counts it and closes its trace record.

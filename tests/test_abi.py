@@ -55,8 +55,13 @@ def test_gemm_validation_without_gpu(xv):
     assert xv.xv_gemm_splits(1024, 8192) > 4
     assert xv.xv_gemm_workspace_size(8, 1024, 8192) > 0
     assert L.xv_gemm_small_m(p, 8192, p, p, 1024, 8, 1024, 8192, None, 0, None) == xv.XV_ERR_WORKSPACE
-    # the projection shapes combine their splits in clusters and need none
-    assert 1 < xv.xv_gemm_splits(5120, 17408) <= 4 and xv.xv_gemm_workspace_size(64, 5120, 17408) == 0
+    # the wide shapes split in two, combined in clusters, and need none; the narrow projections fill
+    # one wave of 2 CTAs per SM and combine through the workspace
+    assert xv.xv_gemm_splits(34816, 5120) == 2 and xv.xv_gemm_workspace_size(64, 34816, 5120) == 0
+    assert xv.xv_gemm_splits(5120, 17408) == 7 and xv.xv_gemm_workspace_size(64, 5120, 17408) > 0
+    # every shape's workspace fits the allocation-free entry point's 10 MiB scratch
+    for N in (1024, 4096, 5120, 9728):
+        assert xv.xv_gemm_workspace_size(64, N, 17408) <= 10 << 20
 
 
 def test_gemm_splits_depend_on_shape_only(xv):

@@ -57,11 +57,12 @@ def big(xv):
 
 
 def test_split_paths(xv):
-    """gate/up: 2 segments; down: 4 combined in a cluster; narrow: 16 through the workspace;
-    a deep shape too short in K for two segments stays whole."""
+    """gate/up: 2 segments combined in a cluster; down: 7 (one wave of 2 CTAs per SM) through the
+    workspace; narrow: 16 through the workspace; a deep shape too short in K for two segments
+    stays whole."""
     assert xv.xv_gemm_splits(34816, 5120) == 2
     assert xv.xv_gemm_splits(34816, 256) == 1
-    assert 2 <= xv.xv_gemm_splits(5120, 17408) <= 4
+    assert xv.xv_gemm_splits(5120, 17408) == 7 and xv.xv_gemm_workspace_size(8, 5120, 17408) > 0
     assert xv.xv_gemm_splits(1024, 8192) > 4 and xv.xv_gemm_workspace_size(8, 1024, 8192) > 0
 
 
