@@ -326,16 +326,29 @@ __global__ void attn_combine_kernel(CombineArgs C) {
     const int ns = (len + ATTN_SPLIT - 1) / ATTN_SPLIT;
     const long long idx0 = (br * C.Hq + hq) * C.nsplit;
     float M = NEG_INF;
+#pragma unroll 8
     for (int s = 0; s < ns; ++s) M = fmaxf(M, C.ml[idx0 + s].x);
     const int d = 2 * threadIdx.x;
     float L = 0.f, acc0 = 0.f, acc1 = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float2 ml = C.ml[idx0 + s];
-        const float w = exp2f(__fsub_rn(ml.x, M));
-        const float2 o = *reinterpret_cast<const float2*>(C.opart + (idx0 + s) * C.hd + d);
-        L = __fadd_rn(L, __fmul_rn(w, ml.y));
-        acc0 = __fadd_rn(acc0, __fmul_rn(w, o.x));
-        acc1 = __fadd_rn(acc1, __fmul_rn(w, o.y));
+    // chunks of CH splits: every load of a chunk is issued before its adds, which stay in split order
+    constexpr int CH = 16;
+    for (int s0 = 0; s0 < ns; s0 += CH) {
+        float2 ml[CH], o[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int s = s0 + j < ns ? s0 + j : ns - 1;
+            ml[j] = C.ml[idx0 + s];
+            o[j] = *reinterpret_cast<const float2*>(C.opart + (idx0 + s) * C.hd + d);
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (s0 + j < ns) {
+                const float w = exp2f(__fsub_rn(ml[j].x, M));
+                L = __fadd_rn(L, __fmul_rn(w, ml[j].y));
+                acc0 = __fadd_rn(acc0, __fmul_rn(w, o[j].x));
+                acc1 = __fadd_rn(acc1, __fmul_rn(w, o[j].y));
+            }
+        }
     }
     float y0 = __fdiv_rn(acc0, L), y1 = __fdiv_rn(acc1, L);
     if (C.gate) {
