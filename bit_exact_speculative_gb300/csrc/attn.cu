@@ -9,8 +9,8 @@
 //     boundaries, and each split into tiles of 64 positions;
 //   - inside a split, an fp32 online softmax (log2 domain) runs over the
 //     split's tiles in order; a tile or position past the row's length is
-//     masked to -inf, contributes p = 0, and leaves the running max, sum and
-//     output bit-for-bit unchanged (correction factor exp2(0) = 1);
+//     masked to -inf, contributes p = 0, and leaves the reference max, sum and
+//     output bit-for-bit unchanged;
 //   - the splits 0..ceil(len/ATTN_SPLIT)-1 are combined in split order by a
 //     second kernel.
 // The rows of a verify block share the K/V tiles (loaded once per CTA, for
@@ -23,8 +23,9 @@
 // swizzle; a contiguous cache is one page of Lmax positions per sequence, a
 // paged one pages of a multiple of 64 positions, so a tile never straddles two
 // pages and the page a tile comes from changes nothing in its arithmetic)
-// into a 3-stage shared-memory ring; QK^T and PV run on mma.sync
-// m16n8k16 bf16 -> fp32 with P rounded to bf16; one warp owns 16 query rows.
+// into a shared-memory ring; QK^T and PV run on tcgen05 (fp32 accumulators in
+// tensor memory, bf16 operands in shared memory, P rounded to bf16); the
+// softmax is one thread per query row, reading its S row from tensor memory.
 // Kernel 2 (attn_combine_kernel), one CTA per (row, q head): fixed-order
 // split combine, normalisation, optional output gate, bf16 store.
 #include <cmath>
@@ -55,13 +56,31 @@ __device__ __forceinline__ int kv_page(const KvPages& kv, int b, int p, int* row
     return pg;
 }
 
+// Shared-memory plan of the split kernel (offsets from a 1024-byte aligned base):
+//   Q      CB blocks of [64 rows][64 dims], 128-byte swizzle: the A operand of Q K^T.  The MMA
+//          reads 128 rows: rows 64..127 of a block are the 8 KB that follow it (the next block,
+//          then P), and land in TMEM lanes nobody reads
+//   P[2]   [64 rows][64 positions] bf16, the A operand of P V, double-buffered (rows 64..127
+//          of P[0] read P[1], of P[1] the K ring)
+//   K ring SK stages of a K tile: CB blocks of [64 positions][64 dims] (B of Q K^T, K-major)
+//   V ring SV stages of a V tile, same layout, read as the MN-major B operand of P V
+//   barriers
 template <int HD>
 struct AttnShape {
     static constexpr int CB = HD / 64;                   // 128-byte column blocks per row
-    static constexpr int TILE_BYTES = T * HD * 2;        // one K or V tile
-    static constexpr int STAGES = HD == 256 ? 3 : 4;
-    static constexpr int RING_BYTES = STAGES * 2 * TILE_BYTES;
-    static int smem_bytes(int rows_pad) { return 1024 + RING_BYTES + rows_pad * HD * 2 + 8 * STAGES + 64; }
+    static constexpr int BLK = T * 128;                  // one [64][64] bf16 block: 8 KB
+    static constexpr int TILE_BYTES = CB * BLK;          // one K or V tile
+    static constexpr int SK = HD == 256 ? 3 : 4;
+    static constexpr int SV = HD == 256 ? 2 : 4;
+    static constexpr int Q_OFF = 0;
+    static constexpr int P_OFF = Q_OFF + CB * BLK;
+    static constexpr int K_OFF = P_OFF + 2 * BLK;
+    static constexpr int V_OFF = K_OFF + SK * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + SV * TILE_BYTES;
+    // fullK, emptyK, fullV, emptyV, sbar[2], sfree[2], pready[2], pfree[2], done, vfix
+    static constexpr int N_BARS = 2 * SK + 2 * SV + 10;
+    static constexpr int SMEM = 1024 + BAR_OFF + 8 * N_BARS;
+    static constexpr uint32_t TMEM_COLS = HD == 256 ? 512 : 256;   // S[2] (64 columns each) + O (HD)
 };
 
 struct AttnArgs {
@@ -73,32 +92,58 @@ struct AttnArgs {
     int R, G, Hq, Hkv, nsplit, max_len;
     float sl2;          // scale * log2(e)
     float* opart;       // [B*R*Hq][nsplit][HD]
-    float2* ml;         // [B*R*Hq][nsplit] (running max in log2 units, sum)
+    float2* ml;         // [B*R*Hq][nsplit] (reference max in log2 units, sum)
     unsigned* err;
 };
 
+constexpr int ATTN_THREADS = 160;   // warps 0-1 softmax, 2 K loads, 3 V loads, 4 MMA
+constexpr float RESCALE_SLACK = 2.f;
+
+// One CTA per (split, kv head, sequence).  Per 64-position tile i of the split:
+//   MMA warp   S[i%2] = Q K_i^T on tcgen05 (M = 128 rows, N = 64 positions, fp32 in TMEM), issued
+//              one tile ahead
+//   softmax    thread = query row: its S row from TMEM, mask, scale; the reference max m moves
+//              to the tile's max when that exceeds it by more than RESCALE_SLACK (log2 units) or
+//              at the row's first live tile, and then O (TMEM) and the sum l are rescaled by
+//              exp2(m_old - m_new); P = bf16(exp2(s - m)) into shared memory, l += its fp32
+//              values in position order (exp2 by the hardware approximation)
+//   MMA warp   O += P V_i (N = HD; V straight from its TMA stage as an MN-major operand)
+// A row's operations depend on its own length and the absolute tile positions only, so a verify
+// row gets the bits of the decode row at its position.
 template <int HD>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs A) {
     griddep_launch();
-    griddep_wait();
     using S = AttnShape<HD>;
-    constexpr int CB = S::CB, STAGES = S::STAGES, TILE_BYTES = S::TILE_BYTES;
+    constexpr int CB = S::CB, SK = S::SK, SV = S::SV, TILE_BYTES = S::TILE_BYTES, BLK = S::BLK;
     extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int s_abort;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw);
-    const int nw = blockDim.x >> 5;
-    const int rows_pad = nw * 16;
-    const uint32_t sQ = base + S::RING_BYTES;
-    const uint32_t bar0 = sQ + rows_pad * HD * 2;
-    auto sK = [&](int st) { return base + st * 2 * TILE_BYTES; };
-    auto sV = [&](int st) { return base + st * 2 * TILE_BYTES + TILE_BYTES; };
-    auto full = [&](int st) { return bar0 + 8u * st; };
+    const uint32_t sQ = base + S::Q_OFF, sP = base + S::P_OFF;
+    auto sK = [&](int st) { return base + S::K_OFF + st * TILE_BYTES; };
+    auto sV = [&](int st) { return base + S::V_OFF + st * TILE_BYTES; };
+    const uint32_t bar0 = base + S::BAR_OFF;
+    auto fullK = [&](int st) { return bar0 + 8u * st; };
+    auto emptyK = [&](int st) { return bar0 + 8u * (SK + st); };
+    auto fullV = [&](int st) { return bar0 + 8u * (2 * SK + st); };
+    auto emptyV = [&](int st) { return bar0 + 8u * (2 * SK + SV + st); };
+    const uint32_t bx = bar0 + 8u * (2 * SK + 2 * SV);
+    auto sbar = [&](int j) { return bx + 8u * j; };
+    auto sfree = [&](int j) { return bx + 8u * (2 + j); };
+    auto pready = [&](int j) { return bx + 8u * (4 + j); };
+    // pfree[j]: P V of tile k (k % 2 == j) has completed (so have all MMAs before it); a wait for
+    // P V of tile k only ever happens once that of tile k - 2 is known complete, so the barrier is
+    // never two phases away from the one waited for
+    auto pfree = [&](int j) { return bx + 8u * (6 + j); };
+    const uint32_t done = bx + 8u * 8, vfix = bx + 8u * 9;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = A.R * A.G;
+    griddep_wait();
     const int L0 = A.ctx_len[b] + A.len_bias;     // visible length of row 0
     const int maxlen = L0 + A.R - 1;
     if (L0 < 1 || maxlen > A.max_len) {
@@ -110,36 +155,35 @@ __global__ void __launch_bounds__(128, 1)
     const int p_end = min(p_begin + ATTN_SPLIT, maxlen);
     const int ntiles = (p_end - p_begin + T - 1) / T;
 
-    // page and row of every tile of the split, looked up once by thread 0 (all loads in flight together)
-    __shared__ int tile_z[ATTN_SPLIT / T], tile_row[ATTN_SPLIT / T];
-    auto issue = [&](int i) {
-        const int st = i % STAGES;
-        mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES);
-        const int z = tile_z[i], row = tile_row[i];
-#pragma unroll
-        for (int cb = 0; cb < CB; ++cb) {
-            tma_load_3d(sK(st) + cb * T * 128, &tmK, cb * 64, row, z, full(st));
-            tma_load_3d(sV(st) + cb * T * 128, &tmV, cb * 64, row, z, full(st));
-        }
-    };
-    int issued = 0;   // tiles whose copies thread 0 has started
     if (tid == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-#pragma unroll
-        for (int i = 0; i < ATTN_SPLIT / T; ++i) {
-            if (i < ntiles) {
-                int row;
-                tile_z[i] = kv_page(A.kv, b, p_begin + i * T, &row, A.err) * A.Hkv + g;
-                tile_row[i] = row;
-            }
+        for (int st = 0; st < SK; ++st) {
+            mbar_init(fullK(st), 1);
+            mbar_init(emptyK(st), 1);
         }
-        for (int st = 0; st < STAGES; ++st) mbar_init(full(st), 1);
+        for (int st = 0; st < SV; ++st) {
+            mbar_init(fullV(st), 1);
+            mbar_init(emptyV(st), 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(sbar(j), 1);
+            mbar_init(sfree(j), 64);
+            mbar_init(pready(j), 64);
+            mbar_init(pfree(j), 1);
+        }
+        mbar_init(done, 1);
+        mbar_init(vfix, 1);
         fence_mbar_init();
-        for (; issued < STAGES && issued < ntiles; ++issued) issue(issued);
+        s_abort = 0;
     }
-    // Q rows (r, gh) -> tile row r*G + gh, 16-byte chunks XOR-swizzled by row
-    for (int idx = tid; idx < rows_pad * (HD / 8); idx += blockDim.x) {
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_slot), S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Q rows (r, gh) -> tile row r*G + gh, 16-byte chunks XOR-swizzled by row; rows past `rows` zero.
+    // (Starting the K/V copies before this, in parallel with it, was measured slower.)
+    for (int idx = tid; idx < 64 * (HD / 8); idx += ATTN_THREADS) {
         const int row = idx / (HD / 8), ch = idx % (HD / 8);
         uint4 v = make_uint4(0, 0, 0, 0);
         if (row < rows) {
@@ -147,158 +191,199 @@ __global__ void __launch_bounds__(128, 1)
             v = *reinterpret_cast<const uint4*>(A.q + (static_cast<long long>(b) * A.R + r) * A.q_stride +
                                                 static_cast<long long>(h) * HD + ch * 8);
         }
-        *reinterpret_cast<uint4*>(smem + (sQ - base) + row * HD * 2 + ((ch ^ (row & 7)) * 16)) = v;
+        *reinterpret_cast<uint4*>(smem + S::Q_OFF + (ch >> 3) * BLK + row * 128 + (((ch & 7) ^ (row & 7)) * 16)) = v;
     }
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
 
-    const int rho0 = warp * 16 + (lane >> 2), rho1 = rho0 + 8;
-    const int len0 = rho0 < rows ? L0 + rho0 / A.G : 0;
-    const int len1 = rho1 < rows ? L0 + rho1 / A.G : 0;
-    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-    float O[HD / 8][4];
-#pragma unroll
-    for (int j = 0; j < HD / 8; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.f;
+    // bounded waits, sleeping between tests (a waiting warp leaves the issue slots to the softmax
+    // warps that share its scheduler); after the first one that gives up, every later wait
+    // returns at once
+    auto W = [&](uint32_t bar, uint32_t par) -> bool {
+        if (s_abort) return false;
+        if (!mbar_wait_sleep(bar, par, A.err)) {
+            s_abort = 1;
+            return false;
+        }
+        return true;
+    };
+    // the same verdict for every lane of a warp that goes on to warp-collective instructions
+    auto WW = [&](uint32_t bar, uint32_t par) -> bool { return __all_sync(0xffffffffu, W(bar, par)); };
 
-    bool ok = true;
-    for (int i = 0; i < ntiles; ++i) {
-        const int st = i % STAGES;
-        if (!mbar_wait(full(st), (i / STAGES) & 1u, A.err)) { ok = false; }
-        if (!__syncthreads_and(ok)) { ok = false; break; }
-        const int p0 = p_begin + i * T;
-        if (p0 + T > maxlen) {
-            // positions past every row's length: zero V so that p = 0 never meets a non-finite value
-            const int first = maxlen - p0;
-            for (int idx = tid; idx < (T - first) * CB * 8; idx += blockDim.x) {
-                const int prow = first + idx / (CB * 8), rem = idx % (CB * 8);
-                *reinterpret_cast<uint4*>(smem + (sV(st) - base) + (rem >> 3) * T * 128 + prow * 128 + (rem & 7) * 16) =
-                    make_uint4(0, 0, 0, 0);
-            }
-            __syncthreads();
-        }
+    const uint32_t tS = tmem, tO = tmem + 128;   // columns: S[0] 0..63, S[1] 64..127, O 128..128+HD-1
 
-        // ---- S = Q K^T for this warp's 16 rows and the tile's 64 positions
-        float sacc[8][4];
+    if (warp == 2 || warp == 3) {
+        // ---- TMA producers: warp 2 the K tiles, warp 3 the V tiles
+        if (lane == 0) {
+            const bool isK = warp == 2;
+            const int NS = isK ? SK : SV;
+            const CUtensorMap* map = isK ? &tmK : &tmV;
+            int issued = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % NS;
+                if (i >= NS && !W(isK ? emptyK(st) : emptyV(st), ((i / NS) & 1u) ^ 1u)) break;
+                const uint32_t fb = isK ? fullK(st) : fullV(st);
+                const uint32_t dst = isK ? sK(st) : sV(st);
+                mbar_arrive_expect_tx(fb, TILE_BYTES);
+                int row;
+                const int z = kv_page(A.kv, b, p_begin + i * T, &row, A.err) * A.Hkv + g;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-#pragma unroll 4
-        for (int ks = 0; ks < HD / 16; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            {
-                const int qr = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int qc = ks * 2 + (lane >> 4);
-                ldsm_x4(sQ + qr * HD * 2 + ((qc ^ (qr & 7)) * 16), a0, a1, a2, a3);
+                for (int cb = 0; cb < CB; ++cb) tma_load_3d(dst + cb * BLK, map, cb * 64, row, z, fb);
+                issued = i + 1;
             }
-            const int chunk = ks * 2 + ((lane >> 3) & 1);
-            const int cb = chunk >> 3, cic = chunk & 7;
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                const int pos = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(sK(st) + cb * T * 128 + pos * 128 + ((cic ^ (pos & 7)) * 16), b0, b1, b2, b3);
-                mma_16816(sacc[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_16816(sacc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-            }
+            // every issued copy lands before the CTA may leave
+            for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
+                mbar_wait(isK ? fullK(j % NS) : fullV(j % NS), (j / NS) & 1u, A.err);
         }
-
-        // ---- online softmax (row stats held by the 4 lanes of a quad)
-        float mx0 = NEG_INF, mx1 = NEG_INF;
+        if (warp == 3 && p_begin + ntiles * T > maxlen) {
+            // V rows of the last tile past every row's length are zeroed once they have landed, so
+            // that p = 0 never meets a non-finite value there; P V of that tile waits for vfix
+            const int il = ntiles - 1, st = il % SV;
+            const int first = maxlen - (p_begin + il * T);
+            if (WW(fullV(st), (il / SV) & 1u)) {
+                for (int idx = first * 8 + lane; idx < T * 8; idx += 32)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int pos = p0 + nt * 8 + 2 * (lane & 3) + j;
-                const float v0 = pos < len0 ? __fmul_rn(sacc[nt][j], A.sl2) : NEG_INF;
-                const float v1 = pos < len1 ? __fmul_rn(sacc[nt][2 + j], A.sl2) : NEG_INF;
-                sacc[nt][j] = v0;
-                sacc[nt][2 + j] = v1;
-                mx0 = fmaxf(mx0, v0);
-                mx1 = fmaxf(mx1, v1);
-            }
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const bool dead0 = mn0 == NEG_INF, dead1 = mn1 == NEG_INF;
-        const float al0 = dead0 ? 1.f : exp2f(__fsub_rn(m0, mn0));
-        const float al1 = dead1 ? 1.f : exp2f(__fsub_rn(m1, mn1));
-        float ts0 = 0.f, ts1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float p0v = dead0 ? 0.f : exp2f(__fsub_rn(sacc[nt][j], mn0));
-                const float p1v = dead1 ? 0.f : exp2f(__fsub_rn(sacc[nt][2 + j], mn1));
-                sacc[nt][j] = p0v;
-                sacc[nt][2 + j] = p1v;
-                ts0 = __fadd_rn(ts0, p0v);
-                ts1 = __fadd_rn(ts1, p1v);
+                    for (int cb = 0; cb < CB; ++cb)
+                        *reinterpret_cast<uint4*>(smem + (sV(st) - base) + cb * BLK + idx * 16) = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(vfix);
             }
         }
-        l0 = __fadd_rn(__fmul_rn(l0, al0), ts0);
-        l1 = __fadd_rn(__fmul_rn(l1, al1), ts1);
-        m0 = mn0;
-        m1 = mn1;
+    } else if (warp == 4) {
+        // ---- MMA issuer: Q K^T of tile i+1 goes out before P V of tile i
+        if (lane == 0) {
+            constexpr uint32_t IDS = idesc_bf16_f32(128, T), IDO = idesc_bf16_f32(128, HD, true);
+            // the next 64 dims of V sit one block further; with a single block the field is never
+            // used and holds the group stride, which keeps every address of the operand inside
+            // its stage under either reading of the two fields
+            constexpr uint32_t VBLK = CB > 1 ? BLK : 1024;
+            auto qk = [&](int i) -> bool {
+                const int st = i % SK;
+                if (!W(fullK(st), (i / SK) & 1u)) return false;
+                if (i >= 2 && !W(sfree(i & 1), ((i - 2) >> 1) & 1u)) return false;
+                tc_fence_after();
 #pragma unroll
-        for (int j = 0; j < HD / 8; ++j) {
-            O[j][0] = __fmul_rn(O[j][0], al0);
-            O[j][1] = __fmul_rn(O[j][1], al0);
-            O[j][2] = __fmul_rn(O[j][2], al1);
-            O[j][3] = __fmul_rn(O[j][3], al1);
-        }
-
-        // ---- O += P V  (P rounded to bf16)
+                for (int ks = 0; ks < HD / 16; ++ks) {
+                    const uint64_t ad = sw128_kmajor_desc(sQ + (ks >> 2) * BLK + (ks & 3) * 32);
+                    const uint64_t bd = sw128_kmajor_desc(sK(st) + (ks >> 2) * BLK + (ks & 3) * 32);
+                    tc_mma_bf16(tS + (i & 1) * T, ad, bd, IDS, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(sbar(i & 1));
+                tc_commit(emptyK(st));
+                return true;
+            };
+            bool ok = qk(0);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                if (i + 1 < ntiles && !qk(i + 1)) break;
+                const int sv = i % SV;
+                const bool fix = i == ntiles - 1 && p_begin + ntiles * T > maxlen;
+                if (!W(pready(i & 1), (i >> 1) & 1u) || !W(fix ? vfix : fullV(sv), fix ? 0u : (i / SV) & 1u)) break;
+                tc_fence_after();
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-            const uint32_t a0 = pack_bf16x2(sacc[2 * kp][0], sacc[2 * kp][1]);
-            const uint32_t a1 = pack_bf16x2(sacc[2 * kp][2], sacc[2 * kp][3]);
-            const uint32_t a2 = pack_bf16x2(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1]);
-            const uint32_t a3 = pack_bf16x2(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3]);
-            const int pos = kp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int dp = 0; dp < HD / 16; ++dp) {
-                const int chunk = dp * 2 + (lane >> 4);
-                const int cb = chunk >> 3, cic = chunk & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(sV(st) + cb * T * 128 + pos * 128 + ((cic ^ (pos & 7)) * 16), b0, b1, b2, b3);
-                mma_16816(O[2 * dp], a0, a1, a2, a3, b0, b1);
-                mma_16816(O[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+                for (int kk = 0; kk < T / 16; ++kk)   // 16 positions = two 8-row groups of the V tile
+                    tc_mma_bf16(tO, sw128_kmajor_desc(sP + (i & 1) * BLK + kk * 32),
+                                sw128_mnmajor_desc(sV(sv) + kk * 2048, VBLK, 1024), IDO, (i > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(pfree(i & 1));
+                tc_commit(emptyV(sv));
             }
+            tc_commit(done);   // every MMA issued is complete before the CTA may leave
+            mbar_wait(done, 0u, A.err);
         }
-        __syncthreads();   // every warp is done with stage st
-        if (tid == 0 && i + STAGES < ntiles) {
+    } else {
+        // ---- softmax: thread = tile row rho (TMEM lane rho)
+        const int rho = tid;
+        const int len = rho < rows ? L0 + rho / A.G : 0;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        float m = NEG_INF, l = 0.f;
+        for (int i = 0; i < ntiles; ++i) {
+            if (!WW(sbar(i & 1), (i >> 1) & 1u)) break;
+            tc_fence_after();
+            float s[T];
+#pragma unroll
+            for (int c = 0; c < T / 16; ++c) tmem_ld16(tS + lane_off + (i & 1) * T + c * 16, s + c * 16);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(sfree(i & 1));
+            const int p0 = p_begin + i * T;
+            float mx = NEG_INF;
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                s[j] = p0 + j < len ? __fmul_rn(s[j], A.sl2) : NEG_INF;
+                mx = fmaxf(mx, s[j]);
+            }
+            const float mn = (m == NEG_INF || mx > __fadd_rn(m, RESCALE_SLACK)) ? mx : m;
+            const bool dead = mn == NEG_INF;
+            const float al = (dead || mn == m) ? 1.f : ex2_approx(__fsub_rn(m, mn));
+            float ts = 0.f;
+            uint32_t pk[T / 2];
+#pragma unroll
+            for (int j = 0; j < T; j += 2) {
+                const float a0 = dead ? 0.f : ex2_approx(__fsub_rn(s[j], mn));
+                const float a1 = dead ? 0.f : ex2_approx(__fsub_rn(s[j + 1], mn));
+                ts = __fadd_rn(__fadd_rn(ts, a0), a1);
+                pk[j / 2] = pack_bf16x2(a0, a1);
+            }
+            l = __fadd_rn(__fmul_rn(l, al), ts);
+            m = mn;
+            // O is rescaled once P V of tile i-1 has completed (tcgen05.ld/st are warp-collective)
+            if (i >= 1 && __any_sync(0xffffffffu, al != 1.f)) {
+                if (!WW(pfree((i - 1) & 1), ((i - 1) >> 1) & 1u)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < HD / 64; ++c) {
+                    float o[64];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) o[e] = __fmul_rn(o[e], al);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) tmem_st16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+                }
+                tmem_st_wait();
+            }
+            // P buffer i%2 was last read by P V of tile i-2
+            if (i >= 2 && !WW(pfree(i & 1), ((i - 2) >> 1) & 1u)) break;
+#pragma unroll
+            for (int c = 0; c < T / 8; ++c)
+                *reinterpret_cast<uint4*>(smem + S::P_OFF + (i & 1) * BLK + rho * 128 + ((c ^ (rho & 7)) * 16)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             fence_proxy_async_smem();
-            issue(i + STAGES);
-            ++issued;
+            tc_fence_before();
+            mbar_arrive(pready(i & 1));
+        }
+        // ---- epilogue: O after the last tile's P V
+        if (WW(pfree((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1u)) {
+            tc_fence_after();
+            // tcgen05.ld is warp-collective: every lane loads, the live rows store
+            const bool live = rho < rows && len > p_begin;
+            const int r = rho / A.G, h = g * A.G + rho % A.G;
+            const long long idx = ((static_cast<long long>(b) * A.R + r) * A.Hq + h) * A.nsplit + split;
+            float* op = A.opart + idx * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD / 64; ++c) {
+                float o[64];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+                tmem_ld_wait();
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < 64; e += 4)
+                        *reinterpret_cast<float4*>(op + c * 64 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                }
+            }
+            if (live) A.ml[idx] = make_float2(m, l);
         }
     }
-    if (!ok) {
-        // drain copies still in flight before the CTA leaves
-        if (tid == 0)
-            for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
-                mbar_wait(full(j % STAGES), (j / STAGES) & 1u, A.err);
-        return;
-    }
-
-    l0 = __fadd_rn(l0, __shfl_xor_sync(0xffffffffu, l0, 1));
-    l0 = __fadd_rn(l0, __shfl_xor_sync(0xffffffffu, l0, 2));
-    l1 = __fadd_rn(l1, __shfl_xor_sync(0xffffffffu, l1, 1));
-    l1 = __fadd_rn(l1, __shfl_xor_sync(0xffffffffu, l1, 2));
-
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int rho = half ? rho1 : rho0;
-        const int len = half ? len1 : len0;
-        if (rho >= rows || len <= p_begin) continue;
-        const int r = rho / A.G, h = g * A.G + rho % A.G;
-        const long long idx = ((static_cast<long long>(b) * A.R + r) * A.Hq + h) * A.nsplit + split;
-        float* op = A.opart + idx * HD;
-#pragma unroll
-        for (int j = 0; j < HD / 8; ++j)
-            *reinterpret_cast<float2*>(op + j * 8 + 2 * (lane & 3)) =
-                half ? make_float2(O[j][2], O[j][3]) : make_float2(O[j][0], O[j][1]);
-        if ((lane & 3) == 0) A.ml[idx] = half ? make_float2(m1, l1) : make_float2(m0, l0);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, S::TMEM_COLS);
     }
 }
 
@@ -403,23 +488,20 @@ inline int nsplit_for(int max_len) { return (max_len + ATTN_SPLIT - 1) / ATTN_SP
 template <int HD>
 xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int B, cudaStream_t s) {
     using S = AttnShape<HD>;
-    const int rows = a.R * a.G;
-    const int nw = (rows + 15) / 16;
-    const int smem = S::smem_bytes(nw * 16);
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "attn: device ordinal out of range");
     if (!attr_done[dev]) {
-        const int maxsm = S::smem_bytes(64);
-        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, maxsm),
+        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           S::SMEM),
                                       "attn: set shared memory size"))
             return st;
         attr_done[dev] = true;
     }
     dim3 grid(a.nsplit, a.Hkv, B);
     trace_pre(s);
-    launch_k(attn_split_kernel<HD>, dim3(grid), dim3(nw * 32), smem, s, tmK, tmV, a);
+    launch_k(attn_split_kernel<HD>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
     // bound: every sequence at the longest length the launch is sized for
     const long long bytes = 4ll * B * a.Hkv * a.max_len * HD + 2ll * B * a.R * a.Hq * HD +
                             4ll * B * a.R * a.Hq * a.nsplit * (HD + 2);

@@ -88,6 +88,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, letting the thread sleep up to `hint_ns` (or until the phase completes) before
+// it returns false: a waiting warp then takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait with sleeping tests.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, unsigned* err) {
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(err, ERR_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+// 2^x by the hardware's approximate exponential (results below 2^-126 flush to 0, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // Waits for the phase with the given parity to complete; gives up after
 // WAIT_LIMIT_NS, records ERR_WAIT_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
@@ -183,6 +214,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 32 bits, 16 consecutive columns per thread, stored.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle (rows of 128 bytes, groups of 8 rows `group_stride` bytes
@@ -197,10 +239,24 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr, uint32_t g
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, A K-major, B K-major (or, with
+// b_mn_major, MN-major: N contiguous).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for an MN-major operand stored with the 128-byte swizzle:
+// rows of 128 bytes hold 64 consecutive N elements, consecutive rows are consecutive K, 8-row
+// groups `group_stride` bytes apart; the next 64 N elements sit `block_stride` bytes further.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t block_stride, uint32_t group_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);      // start address
+    d |= static_cast<uint64_t>(block_stride >> 4) << 16;      // leading byte offset: next 64 N elements
+    d |= static_cast<uint64_t>(group_stride >> 4) << 32;      // stride byte offset: next 8 K rows
+    d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
+    return d;
 }
 
 // ---------------------------------------------------- ldmatrix / mma.sync
