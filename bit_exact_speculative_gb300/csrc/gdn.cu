@@ -24,10 +24,10 @@
 // over the row's 4 lanes (offsets 1, 2): every lane ends with the same bits.
 // The state lives in registers across all replay and speculative steps; it is
 // read once (plain loads issued first) and, after a replay, written once.
-// The step inputs (per step: q and k of the head, this CTA's slice of v) come
-// by bulk asynchronous copies that one thread issues on one mbarrier, so the
-// whole verify's inputs arrive in a single round trip; beta and gate are plain
-// loads.  q and k are then L2-normalised by 4 threads per vector into fp32.
+// The step inputs (per step: q and k of the head, this CTA's slice of v, beta
+// and gate) are plain 16-byte loads spread over the CTA's threads and issued
+// together with the state loads, so the whole verify's inputs arrive in a
+// single round trip.  q and k are then L2-normalised by 4 threads per vector into fp32.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
@@ -80,15 +80,6 @@ __device__ __forceinline__ const GdnStepsDev& step_src(const GdnArgs& A, int b, 
     return A.draft;
 }
 
-// Raw step inputs as they arrive: bf16 q and k of the head, then this CTA's bf16 slice of v.
-template <int DK>
-struct StepRaw {
-    uint16_t q[DK];
-    uint16_t k[DK];
-    uint16_t v[ROWS_PER_CTA];
-};
-static_assert(sizeof(StepRaw<64>) % 16 == 0 && sizeof(StepRaw<128>) % 16 == 0, "bulk copies need 16-byte slots");
-
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
 // Global address of a step's q, k or v piece (all 16-byte aligned: checked by the callers).
@@ -101,20 +92,23 @@ __device__ __forceinline__ const uint16_t* piece(const GdnStepsDev& src, long lo
     return src.v + base + static_cast<long long>(h) * dv + row0;
 }
 
-// Vector w of the staged steps (slot w / 2; q for even w, k for odd) to fp32, L2-normalised when
-// l2 (x / sqrt(sum x^2 + 1e-6)): thread j of the vector's group of NORM_LANES takes elements
-// [j DK/4, (j+1) DK/4), sums their squares in four interleaved chains (e mod 4) added as
-// (c0 + c1) + (c2 + c3), the group adds its partials by an xor tree (1, 2), and every thread
-// scales its own elements.
+// Vector w of the steps (step w / 2; q for even w, k for odd) read from global memory to fp32,
+// L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)): thread j of the vector's group of
+// NORM_LANES takes elements [j DK/4, (j+1) DK/4), sums their squares in four interleaved chains
+// (e mod 4) added as (c0 + c1) + (c2 + c3), the group adds its partials by an xor tree (1, 2),
+// and every thread scales its own elements.
 template <int DK>
-__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const StepRaw<DK>* raw, int total, bool l2) {
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const GdnArgs& A, int b, int h, int hk, int total,
+                                              bool l2) {
     constexpr int PART = DK / NORM_LANES;
     const int jl = threadIdx.x % NORM_LANES;
     for (int w0 = 0; w0 < 2 * total; w0 += THREADS / NORM_LANES) {   // same trip count for every thread
         const int w = w0 + static_cast<int>(threadIdx.x) / NORM_LANES;
         const bool act = w < 2 * total;
         const int t = act ? w >> 1 : 0;
-        const uint16_t* x = ((w & 1) ? raw[t].k : raw[t].q) + jl * PART;
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, t, &row);
+        const uint16_t* x = piece(src, row, h, hk, DK, A.dv, 0, w & 1) + jl * PART;
         float* y = ((w & 1) ? steps[t].k : steps[t].q) + jl * PART;
         float f[PART];
 #pragma unroll
@@ -223,10 +217,7 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
     constexpr int NP = DK / (2 * LPR);
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int total = A.max_commit + A.k;
-    StepRaw<DK>* raw = reinterpret_cast<StepRaw<DK>*>(smem_raw);
-    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw + sizeof(StepRaw<DK>) * total);
-    __shared__ __align__(8) uint64_t bar_mem;
-    const uint32_t bar = smem_u32(&bar_mem);
+    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw);
 
     const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -236,32 +227,16 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
     for (int x = 0; x < RPT; ++x) r[x] = warp * ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
     const int row0 = slab * ROWS_PER_CTA;
     float* srow0 = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0) * DK;
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        l2_prefetch(srow0, ROWS_PER_CTA * DK * 4);   // a hint only: the loads come after the wait
-    }
-    __syncthreads();
+    if (threadIdx.x == 0) l2_prefetch(srow0, ROWS_PER_CTA * DK * 4);   // a hint only: the loads come after the wait
     griddep_wait();
 
-    // Every load of the CTA in flight at once: first each thread's state row (the longest
-    // trip), then one thread's bulk copies of every step's q, k and v slice on one barrier,
-    // the commit count and one beta or gate scalar per thread (2 * total <= 2 * 32 <= THREADS).
+    // Every load of the CTA in flight at once, each thread's own: its state row (the longest
+    // trip), the commit count, one beta or gate scalar (2 * total <= THREADS), one 16-byte chunk
+    // of a step's v slice, then the q / k chunks its normalisation group reads.  (Bulk copies
+    // of the same pieces, 3 per step, took 2 us to issue for 16 steps.)
     float2 s[RPT][NP];
 #pragma unroll
     for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], srow0 + static_cast<size_t>(r[x]) * DK, g);
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(sizeof(StepRaw<DK>)) * total);
-        const int hk = h / A.qk_group;
-        for (int t = 0; t < total; ++t) {
-            long long row;
-            const GdnStepsDev& src = step_src(A, b, t, &row);
-            const uint32_t d = smem_u32(&raw[t]);
-            bulk_load(d, piece(src, row, h, hk, DK, A.dv, row0, 0), DK * 2, bar);
-            bulk_load(d + DK * 2, piece(src, row, h, hk, DK, A.dv, row0, 1), DK * 2, bar);
-            bulk_load(d + DK * 4, piece(src, row, h, hk, DK, A.dv, row0, 2), ROWS_PER_CTA * 2, bar);
-        }
-    }
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
     const int bg_idx = threadIdx.x;
     uint16_t bg = 0;
@@ -270,11 +245,20 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
         const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
         bg = (bg_idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
     }
-    const bool landed = mbar_wait(bar, 0, A.err);
-    if (!__syncthreads_and(landed)) {   // the same verdict for every thread
-        mbar_wait(bar, 0, A.err);       // the copies must land before the CTA may leave
-        return;
+    constexpr int VCH = ROWS_PER_CTA / 8;   // 16-byte chunks of a step's v slice
+    for (int idx = threadIdx.x; idx < total * VCH; idx += THREADS) {
+        const int t = idx / VCH, c = idx % VCH;
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, t, &row);
+        const uint4 u = *reinterpret_cast<const uint4*>(piece(src, row, h, 0, DK, A.dv, row0, 2) + 8 * c);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            steps[t].v[8 * c + 2 * e] = __uint_as_float(wd[e] << 16);
+            steps[t].v[8 * c + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+        }
     }
+    normalise_all<DK>(steps, A, b, h, h / A.qk_group, total, A.l2 != 0);
     if (nc < 0 || nc > A.max_commit) {
         if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
@@ -291,10 +275,6 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
         if (bg_idx & 1) steps[bg_idx >> 1].gate = x;
         else steps[bg_idx >> 1].beta = x;
     }
-    // v slices to fp32, q and k normalised
-    for (int idx = threadIdx.x; idx < total * ROWS_PER_CTA; idx += THREADS)
-        steps[idx / ROWS_PER_CTA].v[idx % ROWS_PER_CTA] = bf16f(raw[idx / ROWS_PER_CTA].v[idx % ROWS_PER_CTA]);
-    normalise_all<DK>(steps, raw, total, A.l2 != 0);
     __syncthreads();
 
     float o[RPT];
@@ -354,10 +334,10 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
         carve[dk == 128] = true;
     }
     if (dk == 128) {
-        const size_t sm = (sizeof(StepRaw<128>) + sizeof(StepSmem<128>)) * (max_steps > 0 ? max_steps : 1);
+        const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
         launch_k(gdn_kernel<128>, dim3(grid), dim3(THREADS), sm, s, a);
     } else {
-        const size_t sm = (sizeof(StepRaw<64>) + sizeof(StepSmem<64>)) * (max_steps > 0 ? max_steps : 1);
+        const size_t sm = sizeof(StepSmem<64>) * (max_steps > 0 ? max_steps : 1);
         launch_k(gdn_kernel<64>, dim3(grid), dim3(THREADS), sm, s, a);
     }
     // algorithmic bytes with every sequence replaying max_commit steps: the state
