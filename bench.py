@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lmax", type=int, default=None,
                     help="KV-cache capacity per sequence (default: enough for every step the run makes)")
+    ap.add_argument("--prefill", type=int, default=None, metavar="T",
+                    help="time an exact chunked prefill of T prompt tokens instead of the verify step")
     ap.add_argument("--full-gdn", action="store_true",
                     help="complete GDN layers: 16 q/k heads for the 32 v heads, width-4 causal convolution, "
                          "gated output norm")
@@ -399,6 +401,44 @@ def run_one_kernel(args):
 
 # ------------------------------------------------------- speculative rounds
 
+def run_prefill(args):
+    """Exact chunked prefill of a T-token prompt from an empty context on the 4-layer stack (verify
+    passes of k tokens, every position committed), timed with CUDA events: time to the first token
+    and prompt tokens per second.  The caches and states it leaves are those of T decode steps."""
+    import torch
+    from synth import workloads
+    from bit_exact_speculative_gb300 import build
+    from bit_exact_speculative_gb300.model import HybridStack
+    build.build()
+    device = torch.device("cuda", 0)
+    cfg = workloads.STACK_FULL if args.full_gdn else workloads.STACK
+    w = workloads.weights(cfg, seed=0)
+    wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
+    B, k, T = args.batch, args.k, args.prefill
+    stk = HybridStack(cfg, wd, B, k, T + 64, device=device)
+    prompt = torch.from_numpy(np.concatenate([workloads.draft_tokens(cfg, 0, 1000 + i % 97, B, 1) for i in range(T)],
+                                             axis=1)).to(device)
+    times = []
+    for rep in range(2):   # the first run warms up
+        stk.set_context([0] * B)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        stk.prefill(prompt, k)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    t = times[-1]
+    print(json.dumps({
+        "metric": f"exact chunked prefill, prompt tok/s (chunks of {k}, batch {B})", "value": round(B * T / t, 1),
+        "unit": "tok/s", "n_gpus": 1, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD.replace("verify k=8 draft tokens, batch 1, context 2183",
+                                                f"prefill of {T} tokens from an empty context"),
+                   "prompt_tokens": T, "batch": B, "chunk": k},
+        "ttft_s": round(t, 4), "verify_passes": -(-T // k),
+        "timing": "CUDA events around the whole prefill (second run)"}), flush=True)
+
+
 def run_speculative(args):
     """Greedy speculative decoding of one sequence on the 4-layer stack: first the target's own
     greedy decode (k = 1 steps) as the reference, then rounds of verify k / accept / commit from
@@ -667,6 +707,9 @@ def main():
         return
     if args.speculative is not None:
         run_speculative(args)
+        return
+    if args.prefill:
+        run_prefill(args)
         return
     if args.impl == "reference":
         out = run_reference(args)

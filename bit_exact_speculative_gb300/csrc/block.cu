@@ -318,6 +318,71 @@ xv_status xv_block_commit_accepted(xv_block_state* st, const int32_t* n_accept, 
     return XV_OK;
 }
 
+// Prefill scratch after the verify workspace: the chunk's tokens [B, kmax], argmax [B, kmax],
+// n_accept [B] and a zero array [B] (the commit keeps 0 + k positions).
+static size_t prefill_extra(int B, int kmax) { return r256(8ull * B * kmax) + 2 * r256(4ull * B); }
+
+size_t xv_block_prefill_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax) {
+    const size_t v = xv_block_workspace_size(cfg, B, kmax, Lmax);
+    return v ? r256(v) + prefill_extra(B, kmax) : 0;
+}
+
+xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                           const int32_t* tokens, int T, int chunk, float* last_logits, int32_t* last_argmax, void* ws,
+                           size_t ws_bytes, xv_stream stream) {
+    Dims d{};
+    if (xv_status e = check_cfg(cfg, &d)) return e;
+    if (xv_status e = check_state(d, cfg, st)) return e;
+    if (!tokens || T < 1) return fail(XV_ERR_ARG, "prefill: need tokens and T >= 1");
+    if (chunk < 1 || chunk > st->kmax) return fail(XV_ERR_ARG, "prefill: chunk = %d outside [1, kmax = %d]", chunk, st->kmax);
+    if (st->last_k != 0) return fail(XV_ERR_ARG, "prefill: the previous verify has not been committed");
+    if (st->max_ctx < 0 || static_cast<long long>(st->max_ctx) + T > st->Lmax)
+        return fail(XV_ERR_ARG, "prefill: max_ctx + T exceeds Lmax (%d)", st->Lmax);
+    const int B = st->B;
+    const size_t vbytes = r256(carve(d, B, st->kmax, st->Lmax, nullptr).total);
+    if (!ws || ws_bytes < vbytes + prefill_extra(B, st->kmax))
+        return fail(XV_ERR_WORKSPACE, "prefill: workspace of %zu bytes needed", vbytes + prefill_extra(B, st->kmax));
+    uint8_t* extra = static_cast<uint8_t*>(ws) + vbytes;
+    int32_t* tok = reinterpret_cast<int32_t*>(extra);
+    int32_t* am = tok + static_cast<size_t>(B) * st->kmax;
+    int32_t* na = reinterpret_cast<int32_t*>(extra + r256(8ull * B * st->kmax));
+    int32_t* zeros = reinterpret_cast<int32_t*>(extra + r256(8ull * B * st->kmax) + r256(4ull * B));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (xv_status e = zero_i32_launch(zeros, B, s)) return e;
+    const Carve c = carve(d, B, st->kmax, st->Lmax, static_cast<uint8_t*>(ws));
+    xv_status e_check = XV_OK;
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        const int k = T - t0 < chunk ? T - t0 : chunk;
+        const bool last = t0 + k == T;
+        // the chunk of every sequence, [B, k]
+        if (xv_status e = cuda_check(cudaMemcpy2DAsync(tok, 4ull * k, tokens + t0, 4ull * T, 4ull * k, B,
+                                                       cudaMemcpyDeviceToDevice, s),
+                                     "prefill: gather the chunk"))
+            return e;
+        if (xv_status e = xv_verify_block(cfg, w, st, tok, k, nullptr, am, na, ws, vbytes, stream)) return e;
+        if (last) {
+            // the last position of each sequence: row b*k + k - 1
+            if (last_logits &&
+                (e_check = cuda_check(cudaMemcpy2DAsync(last_logits, 4ull * d.V, c.logits + static_cast<size_t>(k - 1) * d.V,
+                                                        4ull * k * d.V, 4ull * d.V, B, cudaMemcpyDeviceToDevice, s),
+                                      "prefill: last logits")))
+                return e_check;
+            if (last_argmax &&
+                (e_check = cuda_check(cudaMemcpy2DAsync(last_argmax, 4, am + (k - 1), 4ull * k, 4, B,
+                                                        cudaMemcpyDeviceToDevice, s),
+                                      "prefill: last argmax")))
+                return e_check;
+        }
+        if (xv_status e = commit_launch(zeros, k, B, k, nullptr, st->ctx_len, st->n_commit, s)) return e;
+        st->parity ^= 1;
+        st->pending_rows = k;
+        st->max_ctx += k;
+        st->last_k = 0;
+        st->last_k_seq = nullptr;
+    }
+    return XV_OK;
+}
+
 xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stream stream) {
     Dims d{};
     if (xv_status e = check_cfg(cfg, &d)) return e;

@@ -173,6 +173,7 @@ class HybridStack:
         self._k_seq = None             # the k_seq of a ragged verify, kept alive until its commit
         self._last_k = 0
         self.ws = xv.workspace(self.blk.ws_bytes, device=d)
+        self._pf_ws = None           # the prefill workspace, made on first use
         self.logits = torch.empty((B * kmax, cfg["vocab"]), dtype=torch.float32, device=d)
         self.argmax = torch.empty(B * kmax, dtype=torch.int32, device=d)
         self.n_accept = torch.empty(B, dtype=torch.int32, device=d)
@@ -238,6 +239,26 @@ class HybridStack:
             xv.xv_block_commit(self.blk, n_keep, stream=stream)
         self._bound = [n + self._last_k for n in self._bound]
         self._k_seq = None
+
+    def prefill(self, tokens: torch.Tensor, chunk: int | None = None, stream=None):
+        """Feeds tokens [B, T] (int32, device) through verify + commit-all in chunks of ``chunk``
+        (default kmax); the caches and states end bit-identical to T decode steps.  Returns
+        (logits [B, V] fp32, argmax [B]) after each sequence's last token."""
+        B, T = tokens.shape
+        chunk = self.kmax if chunk is None else int(chunk)
+        if self._pf_ws is None:
+            n = int(xv.lib().xv_block_prefill_workspace_size(xv.ctypes.byref(self.blk.cfg), self.B, self.kmax,
+                                                             self.Lmax))
+            self._pf_ws = xv.workspace(n, device=self.argmax.device)
+        if self.pool is not None:
+            for b in range(self.B):
+                self.pool.ensure(b, min(self._bound[b] + T, self.Lmax))
+            self.pool.sync(stream)
+        lg = torch.empty((B, self.cfg["vocab"]), dtype=torch.float32, device=self.argmax.device)
+        am = torch.empty(B, dtype=torch.int32, device=self.argmax.device)
+        xv.xv_block_prefill(self.blk, tokens.contiguous(), T, chunk, lg, am, self._pf_ws, stream=stream)
+        self._bound = [n + T for n in self._bound]
+        return lg, am
 
     def flush(self, stream=None):
         xv.xv_block_flush(self.blk, stream=stream)

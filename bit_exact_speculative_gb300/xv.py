@@ -112,6 +112,9 @@ _SIGS = {
     "xv_block_commit": ([ctypes.POINTER(BlockState), vp, vp], c_int),
     "xv_block_commit_accepted": ([ctypes.POINTER(BlockState), vp, vp], c_int),
     "xv_block_flush": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockState), vp], c_int),
+    "xv_block_prefill_workspace_size": ([ctypes.POINTER(BlockConfig), c_int, c_int, c_int], c_sz),
+    "xv_block_prefill": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState), vp,
+                          c_int, c_int, vp, vp, vp, c_sz, vp], c_int),
 }
 
 
@@ -386,6 +389,12 @@ def xv_block_commit(blk: Block, n_keep, stream=None):
 
 def xv_block_commit_accepted(blk: Block, n_accept, stream=None):
     _check(lib().xv_block_commit_accepted(ctypes.byref(blk.state), _ptr(n_accept), _stream(stream)))
+
+
+def xv_block_prefill(blk: Block, tokens, T: int, chunk: int, last_logits, last_argmax, ws, stream=None):
+    _check(lib().xv_block_prefill(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
+                                  _ptr(tokens), T, chunk, _ptr(last_logits), _ptr(last_argmax), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def xv_block_flush(blk: Block, stream=None):

@@ -421,6 +421,24 @@ xv_status xv_block_commit_accepted(xv_block_state* st, const int32_t* n_accept, 
  * position.  Needs the same cfg as the verify calls. */
 xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stream s);
 
+/* Exact chunked prefill.  Feeds tokens [B, T] (int32 device, row b = the
+ * next T tokens of sequence b) through the verify pass in chunks of `chunk`
+ * tokens (the last one shorter if T % chunk != 0) and commits every
+ * position, all enqueued on `s` without a host synchronisation.  Because a
+ * verify gives the bits of decoding its tokens one at a time and a commit
+ * of all k positions is the same state as k decode steps, the KV caches,
+ * GDN (and convolution) states and lengths afterwards are bit-identical to T
+ * decode steps, for every chunk size: batch-invariant by construction.
+ * last_logits [B, V] fp32 and last_argmax [B] int32 (device, each may be
+ * NULL) receive the logits and greedy token after each sequence's last
+ * prompt token.  1 <= chunk <= st->kmax; the last verify must have been
+ * committed; st->max_ctx + T <= Lmax.  Workspace:
+ * xv_block_prefill_workspace_size(cfg, B, kmax, Lmax). */
+size_t xv_block_prefill_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);
+xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                           const int32_t* tokens, int T, int chunk, float* last_logits, int32_t* last_argmax,
+                           void* ws, size_t ws_bytes, xv_stream s);
+
 #ifdef __cplusplus
 }
 #endif

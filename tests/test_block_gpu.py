@@ -311,3 +311,62 @@ def test_ragged_commit_beyond_k_seq_is_flagged(tiny):
     assert e.value.code == xv.XV_ERR_DEVICE_CHECK and "bits 0x8" in str(e.value)
     assert xv.xv_device_check() == 0          # read and cleared
     assert host(A.state["ctx_len"]).tolist() == [130, 104]
+
+
+# ------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("cfg_name", ["TINY", "TINY_FULL"])
+def test_prefill_any_chunk_equals_decode(built, cfg_name):
+    """Prefill of 37 tokens in chunks of 4 or 3 leaves the states of 37 decode steps bit for bit:
+    the same last logits, the same GDN/convolution states and the same next verify."""
+    cfg = getattr(workloads, cfg_name)
+    w = workloads.weights(cfg, seed=0)
+    B, k, Lmax, T = 2, 4, 256, 37
+    lens = [100, 41]
+    prompt = np.concatenate([workloads.draft_tokens(cfg, 0, 30 + i, B, 1) for i in range(T)], axis=1)
+    nxt = workloads.draft_tokens(cfg, 0, 90, B, k)
+    outs = []
+    for chunk in (4, 3):
+        A = gpu_stack(cfg, w, B, k, Lmax, lens)
+        lg, am = A.prefill(dev(prompt), chunk)
+        lgv = A.verify(dev(nxt), k)[0].clone()
+        A.commit(torch.full((B,), k, dtype=torch.int32, device="cuda"))
+        A.flush()
+        outs.append((lg.clone(), am.clone(), lgv, A.state["0.state"].clone(),
+                     A.state["0.conv"].clone() if "0.conv" in A.state else None, A.state["ctx_len"].clone()))
+    S = gpu_stack(cfg, w, B, k, Lmax, lens)
+    lgS, amS = sequential(S, prompt, B)
+    lgvS = S.verify(dev(nxt), k)[0].clone()
+    S.commit(torch.full((B,), k, dtype=torch.int32, device="cuda"))
+    S.flush()
+    for lg, am, lgv, st, cv, ctx in outs:
+        assert same_bits(lg, lgS[:, -1])
+        assert torch.equal(am, amS[:, -1])
+        assert same_bits(lgv, lgvS)
+        assert same_bits(st, S.state["0.state"])
+        if cv is not None:
+            assert same_bits(cv, S.state["0.conv"])
+        assert torch.equal(ctx, S.state["ctx_len"])
+        assert host(ctx).tolist() == [lens[0] + T + k, lens[1] + T + k]
+
+
+def test_stack_prefill_chunks_equal(stack):
+    """The 5120-wide stack: 50 prompt tokens prefilled in chunks of 8 and of 5 give the same last
+    logits and the same next verify, and match 50 decode steps."""
+    cfg, w, wd = stack
+    B, k, L, T = 1, 8, 640, 50
+    Lmax = L + T + 2 * k
+    prompt = np.concatenate([workloads.draft_tokens(cfg, 0, 300 + i, B, 1) for i in range(T)], axis=1)
+    nxt = workloads.draft_tokens(cfg, 0, 399, B, k)
+    res = []
+    for chunk in (8, 5):
+        A = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+        lg, _ = A.prefill(dev(prompt), chunk)
+        res.append((lg.clone(), A.verify(dev(nxt), k)[0].clone()))
+        del A
+    S = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    lgS, _ = sequential(S, prompt, B)
+    lgvS = S.verify(dev(nxt), k)[0].clone()
+    for lg, lgv in res:
+        assert same_bits(lg, lgS[:, -1])
+        assert same_bits(lgv, lgvS)
