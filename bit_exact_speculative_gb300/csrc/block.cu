@@ -230,6 +230,16 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
 
 #define XV_TRY(expr) do { if (xv_status e_ = (expr)) return e_; } while (0)
     XV_TRY(embed_rmsnorm_launch(tokens, M, w->embed, d.V, d.H, w->layers[0].norm1, eps, c.x, c.xn, s));
+    // a projection into the residual stream, then x <- bf16(x + y), xn <- rmsnorm(x, gain); where
+    // the GEMM would combine its split-K partials in a kernel of its own, the norm kernel sums
+    // them itself (the same sums in the same order: the same bits)
+    auto residual_gemm = [&](const uint16_t* A, int K, const uint16_t* Wt, const uint16_t* gain) -> xv_status {
+        float* part = nullptr;
+        int S = 0;
+        XV_TRY(gemm_launch(A, K, Wt, c.y, d.H, false, M, d.H, K, c.gemm_ws, c.gemm_ws_bytes, s, &part, &S));
+        if (part) return residual_rmsnorm_part_launch(c.x, part, S, gain, M, d.H, eps, c.xn, s);
+        return residual_rmsnorm_launch(c.x, c.y, gain, M, d.H, eps, c.xn, s);
+    };
     for (int l = 0; l < d.L; ++l) {
         const xv_layer_weights& lw = w->layers[l];
         xv_layer_state& ls = st->layers[l];
@@ -259,7 +269,7 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
             if (d.onorm)
                 XV_TRY(gated_norm_launch(c.obuf, d.ginner, hist + d.cdim, d.gstride, lw.out_norm, M, d.gh, d.dv, eps,
                                          c.obuf, d.ginner, s));
-            XV_TRY(gemm_launch(c.obuf, d.ginner, lw.w_out, c.y, d.H, false, M, d.H, d.ginner, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(residual_gemm(c.obuf, d.ginner, lw.w_out, lw.norm2));
         } else {
             XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, c.proj, d.ain, false, M, d.ain, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
             XV_TRY(kv_append_launch(c.proj + 2 * d.ainner, d.ain, st->ctx_len, 0, k, B, d.hkv, d.hd, kv, ls.k_cache,
@@ -267,14 +277,12 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
             XV_TRY(attn_launch(c.proj, d.ain, ls.k_cache, ls.v_cache, kv, st->ctx_len, 1, k, B, d.hq, d.hkv, d.hd,
                                attn_len, 1.0f / sqrtf(static_cast<float>(d.hd)), c.proj + d.ainner, d.ain, c.obuf,
                                d.ainner, c.attn_ws, c.attn_ws_bytes, s));
-            XV_TRY(gemm_launch(c.obuf, d.ainner, lw.w_out, c.y, d.H, false, M, d.H, d.ainner, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(residual_gemm(c.obuf, d.ainner, lw.w_out, lw.norm2));
         }
-        XV_TRY(residual_rmsnorm_launch(c.x, c.y, lw.norm2, M, d.H, eps, c.xn, s));
         XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, c.gu, 2 * d.F, false, M, 2 * d.F, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
         XV_TRY(swiglu_launch(c.gu, M, d.F, c.act, s));
-        XV_TRY(gemm_launch(c.act, d.F, lw.w_down, c.y, d.H, false, M, d.H, d.F, c.gemm_ws, c.gemm_ws_bytes, s));
         const uint16_t* next_norm = (l + 1 < d.L) ? w->layers[l + 1].norm1 : w->final_norm;
-        XV_TRY(residual_rmsnorm_launch(c.x, c.y, next_norm, M, d.H, eps, c.xn, s));
+        XV_TRY(residual_gemm(c.act, d.F, lw.w_down, next_norm));
     }
     XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
     XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));

@@ -378,8 +378,9 @@ size_t gemm_workspace_size(int M, int N, int K) {
 }
 
 xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, int ldy, bool f32out, int M, int N, int K,
-                      void* ws, size_t ws_bytes, cudaStream_t s) {
+                      void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part, int* defer_S) {
     (void)ws_bytes;
+    if (defer_part) *defer_part = nullptr;
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "gemm: device error word unavailable");
     CUtensorMap tmW, tmX;
@@ -429,6 +430,11 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
         launch_k(kern, grid, dim3(128), smem, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster, xb, xr);
     const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
     if (xv_status st = launched("gemm_small_m_kernel", s, K_GEMM, bytes)) return st;
+    if (sep_combine && defer_part) {
+        *defer_part = part;
+        if (defer_S) *defer_S = S;
+        return XV_OK;
+    }
     if (sep_combine) {
         trace_pre(s);
         const long long outs = static_cast<long long>(M) * N;

@@ -37,8 +37,13 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 
 // y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ); with y_res != null first x <- bf16(x + y_res);
 // with tokens != null the row is first gathered from the embedding, x <- E[tokens[row]].
-// One CTA per row; thread t owns the 8-element chunks t, t + blockDim, ... (at most NORM_MAXC),
+// One CTA per row; thread t < nt owns the 8-element chunks t, t + nt, ... (at most NORM_MAXC),
 // so the per-thread sum order and the tree below are fixed by H alone.
+//
+// With part != null, y_res is instead bf16(part_0 + ... + part_{S-1}), a GEMM's split-K partials
+// [S][M][H] added in segment order (the bits of the GEMM's own combine).  All blockDim threads
+// first form that row of y in shared memory; threads past nt then take no chunk, and their
+// warps add zeros after the others in the fixed tree, which leaves the sum's bits unchanged.
 constexpr int NORM_MAXC = 4;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
@@ -56,13 +61,43 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Sum of the S partials of the 8 elements of chunk c of `row`, in segment order, as bf16.
+__device__ __forceinline__ uint4 partial_sum8(const float* __restrict__ part, int S, int M, int H, long long row, int c) {
+    constexpr int G = 4;   // segments whose loads are in flight together
+    float r[8];
+    for (int q0 = 0; q0 < S; q0 += G) {
+        float4 p[G][2];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float4* pp = reinterpret_cast<const float4*>(part + (static_cast<long long>(q0 + g) * M + row) * H) + 2 * c;
+            p[g][0] = q0 + g < S ? __ldcg(pp) : make_float4(0.f, 0.f, 0.f, 0.f);
+            p[g][1] = q0 + g < S ? __ldcg(pp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float a[8] = {p[g][0].x, p[g][0].y, p[g][0].z, p[g][0].w, p[g][1].x, p[g][1].y, p[g][1].z, p[g][1].w};
+            if (q0 + g == 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r[e] = a[e];
+            } else if (q0 + g < S) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r[e] = __fadd_rn(r[e], a[e]);
+            }
+        }
+    }
+    return pack8(r);
+}
+
+template <bool PART>
 __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x, const uint16_t* __restrict__ y_res,
                                                        const uint16_t* __restrict__ w, int H, float eps,
                                                        uint16_t* __restrict__ out, const int32_t* __restrict__ tokens,
-                                                       const uint16_t* __restrict__ E, int V, unsigned* err) {
+                                                       const uint16_t* __restrict__ E, int V, unsigned* err,
+                                                       const float* __restrict__ part, int S, int M, int nt) {
     griddep_launch();
     griddep_wait();
     __shared__ float red[33];
+    extern __shared__ uint4 ysm[];
     const long long row = blockIdx.x;
     const int nch = H / 8;
     uint4* xr = reinterpret_cast<uint4*>(x + row * H);
@@ -76,13 +111,19 @@ __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x,
         src = reinterpret_cast<const uint4*>(E + static_cast<long long>(t) * H);
     }
     const uint4* yr = y_res ? reinterpret_cast<const uint4*>(y_res + row * H) : nullptr;
+    if constexpr (PART) {
+        for (int c = threadIdx.x; c < nch; c += blockDim.x) ysm[c] = partial_sum8(part, S, M, H, row, c);
+        __syncthreads();
+        yr = ysm;
+    }
+    const bool owner = !PART || threadIdx.x < nt;
     float v[NORM_MAXC][8];
     float ss = 0.f;
     bool first = true;
 #pragma unroll
     for (int j = 0; j < NORM_MAXC; ++j) {
-        const int c = threadIdx.x + j * blockDim.x;
-        if (c < nch) {
+        const int c = threadIdx.x + j * nt;
+        if (owner && c < nch) {
             const uint4 raw = src[c];
             if (tokens) xr[c] = raw;
             unpack8(raw, v[j]);
@@ -106,8 +147,8 @@ __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x,
     uint4* orow = reinterpret_cast<uint4*>(out + row * H);
 #pragma unroll
     for (int j = 0; j < NORM_MAXC; ++j) {
-        const int c = threadIdx.x + j * blockDim.x;
-        if (c < nch) {
+        const int c = threadIdx.x + j * nt;
+        if (owner && c < nch) {
             float wf[8], o[8];
             unpack8(wr[c], wf);
 #pragma unroll
@@ -273,8 +314,8 @@ static int norm_threads(int H) {
 
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s) {
     trace_pre(s);
-    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y,
-             nullptr, nullptr, 0, nullptr);
+    launch_k(rmsnorm_kernel<false>, dim3(M), dim3(norm_threads(H)), 0, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y,
+             nullptr, nullptr, 0, nullptr, nullptr, 0, 0, norm_threads(H));
     return launched("rmsnorm_kernel", s, K_RMSNORM, 4ll * M * H + 2ll * H);
 }
 
@@ -283,15 +324,31 @@ xv_status embed_rmsnorm_launch(const int32_t* tokens, int M, const uint16_t* E, 
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "embed: device error word unavailable");
     trace_pre(s);
-    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, x, nullptr, w, H, eps, xn, tokens, E, V, err);
+    launch_k(rmsnorm_kernel<false>, dim3(M), dim3(norm_threads(H)), 0, s, x, nullptr, w, H, eps, xn, tokens, E, V, err,
+             nullptr, 0, 0, norm_threads(H));
     return launched("rmsnorm_kernel(embed)", s, K_EMBED, 6ll * M * H + 2ll * H + 4ll * M);
 }
 
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps, uint16_t* xn,
                                   cudaStream_t s) {
     trace_pre(s);
-    launch_k(rmsnorm_kernel, dim3(M), dim3(norm_threads(H)), 0, s, x, y, w, H, eps, xn, nullptr, nullptr, 0, nullptr);
+    launch_k(rmsnorm_kernel<false>, dim3(M), dim3(norm_threads(H)), 0, s, x, y, w, H, eps, xn, nullptr, nullptr, 0, nullptr,
+             nullptr, 0, 0, norm_threads(H));
     return launched("rmsnorm_kernel(residual)", s, K_RMSNORM, 8ll * M * H + 2ll * H);
+}
+
+xv_status residual_rmsnorm_part_launch(uint16_t* x, const float* part, int S, const uint16_t* w, int M, int H, float eps,
+                                       uint16_t* xn, cudaStream_t s) {
+    if (S < 1 || S > 16) return fail(XV_ERR_ARG, "rmsnorm: %d partials outside [1, 16]", S);
+    if (H % 8 || H > 16384) return fail(XV_ERR_UNSUPPORTED, "rmsnorm: width %d with partials", H);
+    trace_pre(s);
+    const int nt = norm_threads(H);
+    int threads = (H / 8 + 31) / 32 * 32;
+    if (threads > 1024) threads = 1024;
+    if (threads < nt) threads = nt;
+    launch_k(rmsnorm_kernel<true>, dim3(M), dim3(threads), static_cast<size_t>(H) * 2, s, x, nullptr, w, H, eps, xn, nullptr,
+             nullptr, 0, nullptr, part, S, M, nt);
+    return launched("rmsnorm_kernel(residual, partials)", s, K_RMSNORM, 4ll * S * M * H + 6ll * M * H + 2ll * H);
 }
 
 xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStream_t s) {

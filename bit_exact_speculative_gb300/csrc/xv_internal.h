@@ -77,8 +77,11 @@ constexpr int GEMM_BK = 64;    // K elements per pipeline stage (one 128-byte sw
 constexpr int GEMM_TOK = 64;   // token columns of every MMA (MMA N), whatever M is
 int gemm_splits(int N, int K);
 size_t gemm_workspace_size(int M, int N, int K);
+// defer_part: when the GEMM would combine its partials in a separate kernel (M > 8, more segments
+// than a cluster), it skips that kernel and returns the partials [S][M][N] and S instead (else
+// *defer_part = nullptr).
 xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, int ldy, bool f32out, int M, int N,
-                      int K, void* ws, size_t ws_bytes, cudaStream_t s);
+                      int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part = nullptr, int* defer_S = nullptr);
 
 // ---- GDN (gdn.cu)
 struct GdnStepsDev {
@@ -142,6 +145,9 @@ xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, flo
 xv_status embed_rmsnorm_launch(const int32_t* tokens, int M, const uint16_t* E, int V, int H, const uint16_t* w,
                                float eps, uint16_t* x, uint16_t* xn, cudaStream_t s);
 // x <- bf16(x + y); xn <- rmsnorm(x, w)
+// the same with y = bf16(sum of a GEMM's S split-K partials [S][M][H] in segment order)
+xv_status residual_rmsnorm_part_launch(uint16_t* x, const float* part, int S, const uint16_t* w, int M, int H, float eps,
+                                       uint16_t* xn, cudaStream_t s);
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps,
                                   uint16_t* xn, cudaStream_t s);
 // act[m][i] = bf16(silu(gu[m][i]) * gu[m][F + i])
