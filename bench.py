@@ -50,6 +50,8 @@ def parse():
                     help="KV-cache capacity per sequence (default: enough for every step the run makes)")
     ap.add_argument("--prefill", type=int, default=None, metavar="T",
                     help="time an exact chunked prefill of T prompt tokens instead of the verify step")
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="with --prefill: tokens per verify pass (default 64 / batch, the most one GEMM call takes)")
     ap.add_argument("--full-gdn", action="store_true",
                     help="complete GDN layers: 16 q/k heads for the 32 v heads, width-4 causal convolution, "
                          "gated output norm")
@@ -403,8 +405,9 @@ def run_one_kernel(args):
 
 def run_prefill(args):
     """Exact chunked prefill of a T-token prompt from an empty context on the 4-layer stack (verify
-    passes of k tokens, every position committed), timed with CUDA events: time to the first token
-    and prompt tokens per second.  The caches and states it leaves are those of T decode steps."""
+    passes of `chunk` tokens, every position committed, the LM head only in the last pass), timed
+    with CUDA events: time to the first token and prompt tokens per second.  The caches and states
+    it leaves are those of T decode steps."""
     import torch
     from synth import workloads
     from bit_exact_speculative_gb300 import build
@@ -414,7 +417,8 @@ def run_prefill(args):
     cfg = workloads.STACK_FULL if args.full_gdn else workloads.STACK
     w = workloads.weights(cfg, seed=0)
     wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
-    B, k, T = args.batch, args.k, args.prefill
+    B, T = args.batch, args.prefill
+    k = args.chunk if args.chunk else max(1, 64 // B)
     stk = HybridStack(cfg, wd, B, k, T + 64, device=device)
     prompt = torch.from_numpy(np.concatenate([workloads.draft_tokens(cfg, 0, 1000 + i % 97, B, 1) for i in range(T)],
                                              axis=1)).to(device)

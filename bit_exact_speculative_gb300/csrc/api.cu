@@ -338,7 +338,6 @@ static xv_status attn_checks(const uint16_t* q, long long q_stride, const uint16
     if (R > XV_KMAX) return fail(XV_ERR_UNSUPPORTED, "attn: R = %d exceeds %d", R, XV_KMAX);
     if (Hq % Hkv) return fail(XV_ERR_ARG, "attn: Hq must be a multiple of Hkv");
     if (hd != 64 && hd != 256) return fail(XV_ERR_UNSUPPORTED, "attn: hd must be 64 or 256 (got %d)", hd);
-    if (R * (Hq / Hkv) > 64) return fail(XV_ERR_UNSUPPORTED, "attn: R * Hq/Hkv = %d exceeds 64", R * (Hq / Hkv));
     if (max_len < R || max_len > Lmax) return fail(XV_ERR_ARG, "attn: need R <= max_ctx <= Lmax");
     if (B > 65535 || Hkv > 65535) return fail(XV_ERR_UNSUPPORTED, "attn: B and Hkv must be below 65536");
     if ((long long)B * Hkv * Lmax > (1ll << 31)) return fail(XV_ERR_UNSUPPORTED, "attn: cache too large");

@@ -14,11 +14,12 @@
 //   - the splits 0..ceil(len/ATTN_SPLIT)-1 are combined in split order by a
 //     second kernel.
 // The rows of a verify block share the K/V tiles (loaded once per CTA, for
-// all q heads of a kv head and all R rows), but no arithmetic of one row
+// up to 64 rows (r, q head) of a kv head; more rows take more CTAs, which
+// read the same tiles through L2), but no arithmetic of one row
 // touches another row's data: each output element of a tensor-core product
 // is the dot product of its own row and column.
 //
-// Kernel 1 (attn_split_kernel), one CTA per (split, kv head, sequence):
+// Kernel 1 (attn_split_kernel), one CTA per (split, 64-row tile, kv head, sequence):
 // K and V tiles arrive by TMA (3-D tensor map over [pages*Hkv, page, hd], 128-byte
 // swizzle; a contiguous cache is one page of Lmax positions per sequence, a
 // paged one pages of a multiple of 64 positions, so a tile never straddles two
@@ -140,16 +141,21 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     auto pfree = [&](int j) { return bx + 8u * (6 + j); };
     const uint32_t done = bx + 8u * 8, vfix = bx + 8u * 9;
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // blockIdx.x = split * nrt + row tile: the row tiles of one split are neighbours and share
+    // its K/V tiles through L2
+    const int rows = A.R * A.G, nrt = (rows + 63) / 64;
+    const int split = blockIdx.x / nrt, row_base = (blockIdx.x % nrt) * 64;
+    const int g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rows = A.R * A.G;
     griddep_wait();
     const int L0 = A.ctx_len[b] + A.len_bias;     // visible length of row 0
-    const int maxlen = L0 + A.R - 1;
-    if (L0 < 1 || maxlen > A.max_len) {
-        if (tid == 0 && split == 0 && g == 0) atomicOr(A.err, ERR_BAD_LENGTH);
+    if (L0 < 1 || L0 + A.R - 1 > A.max_len) {
+        if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(A.err, ERR_BAD_LENGTH);
         return;
     }
+    // the longest visible length among this CTA's rows; positions past a row's own length are
+    // masked (p = 0), so how far the tile runs does not change any row's bits
+    const int maxlen = L0 + (min(rows, row_base + 64) - 1) / A.G;
     const int p_begin = split * ATTN_SPLIT;
     if (p_begin >= maxlen) return;
     const int p_end = min(p_begin + ATTN_SPLIT, maxlen);
@@ -181,13 +187,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_alloc(smem_u32(&tmem_slot), S::TMEM_COLS);
         tmem_relinquish();
     }
-    // Q rows (r, gh) -> tile row r*G + gh, 16-byte chunks XOR-swizzled by row; rows past `rows` zero.
+    // Q rows (r, gh) -> block row r*G + gh, tile row r*G + gh - row_base, 16-byte chunks
+    // XOR-swizzled by row; rows past `rows` zero.
     // (Starting the K/V copies before this, in parallel with it, was measured slower.)
     for (int idx = tid; idx < 64 * (HD / 8); idx += ATTN_THREADS) {
         const int row = idx / (HD / 8), ch = idx % (HD / 8);
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < rows) {
-            const int r = row / A.G, h = g * A.G + row % A.G;
+        if (row_base + row < rows) {
+            const int r = (row_base + row) / A.G, h = g * A.G + (row_base + row) % A.G;
             v = *reinterpret_cast<const uint4*>(A.q + (static_cast<long long>(b) * A.R + r) * A.q_stride +
                                                 static_cast<long long>(h) * HD + ch * 8);
         }
@@ -295,8 +302,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         }
     } else {
         // ---- softmax: thread = tile row rho (TMEM lane rho)
-        const int rho = tid;
-        const int len = rho < rows ? L0 + rho / A.G : 0;
+        const int rho = tid, grow = row_base + rho;   // TMEM lane, row of the verify block
+        const int len = grow < rows ? L0 + grow / A.G : 0;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         float m = NEG_INF, l = 0.f;
         for (int i = 0; i < ntiles; ++i) {
@@ -360,8 +367,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         if (WW(pfree((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1u)) {
             tc_fence_after();
             // tcgen05.ld is warp-collective: every lane loads, the live rows store
-            const bool live = rho < rows && len > p_begin;
-            const int r = rho / A.G, h = g * A.G + rho % A.G;
+            const bool live = grow < rows && len > p_begin;
+            const int r = grow / A.G, h = g * A.G + grow % A.G;
             const long long idx = ((static_cast<long long>(b) * A.R + r) * A.Hq + h) * A.nsplit + split;
             float* op = A.opart + idx * HD;
 #pragma unroll 1
@@ -499,7 +506,7 @@ xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const Att
             return st;
         attr_done[dev] = true;
     }
-    dim3 grid(a.nsplit, a.Hkv, B);
+    dim3 grid(a.nsplit * ((a.R * a.G + 63) / 64), a.Hkv, B);
     trace_pre(s);
     launch_k(attn_split_kernel<HD>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
     // bound: every sequence at the longest length the launch is sized for

@@ -193,9 +193,11 @@ static KvPages state_pages(const xv_block_state* st) {
     return pg.page_table ? KvPages{pg.page_table, pg.page_size, pg.max_pages, pg.n_pages} : kv_contiguous(st->B, st->Lmax);
 }
 
-xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
-                                 const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
-                                 int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream) {
+// The verify pass; with head = false it stops after the final RMSNorm (no LM head, argmax or
+// acceptance: a prefill chunk whose logits nobody reads).
+static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                             const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
+                             int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream, bool head) {
     Dims d{};
     if (xv_status e = check_cfg(cfg, &d)) return e;
     if (xv_status e = check_state(d, cfg, st)) return e;
@@ -207,14 +209,12 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
         if (cfg->layer_kind[l] == 0 && ((d.kc && !lw.conv_w) || (d.onorm && !lw.out_norm)))
             return fail(XV_ERR_ARG, "block: GDN layer %d convolution taps or output norm weights missing", l);
     }
-    if (!tokens || !argmax || !n_accept) return fail(XV_ERR_ARG, "block: null tokens, argmax or n_accept");
+    if (!tokens || (head && (!argmax || !n_accept))) return fail(XV_ERR_ARG, "block: null tokens, argmax or n_accept");
     if (st->last_k != 0) return fail(XV_ERR_ARG, "block: the previous verify has not been committed");
     const int B = st->B;
     if (k < 1 || k > st->kmax) return fail(XV_ERR_ARG, "block: k = %d outside [1, kmax = %d]", k, st->kmax);
     const int M = B * k;
     if (M > XV_GEMM_M_MAX) return fail(XV_ERR_UNSUPPORTED, "block: B*k = %d exceeds %d", M, XV_GEMM_M_MAX);
-    if (d.ain && k * (d.hq / d.hkv) > 64)
-        return fail(XV_ERR_UNSUPPORTED, "block: k * Hq/Hkv = %d exceeds 64", k * (d.hq / d.hkv));
     if (st->max_ctx < 0 || st->max_ctx + k > st->Lmax)
         return fail(XV_ERR_ARG, "block: max_ctx + k (%d) exceeds Lmax (%d)", st->max_ctx + k, st->Lmax);
     if (st->pending_rows < 1 || st->pending_rows > st->kmax) return fail(XV_ERR_ARG, "block: pending_rows out of range");
@@ -284,12 +284,20 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
         const uint16_t* next_norm = (l + 1 < d.L) ? w->layers[l + 1].norm1 : w->final_norm;
         XV_TRY(residual_gemm(c.act, d.F, lw.w_down, next_norm));
     }
-    XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-    XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
+    if (head) {
+        XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+        XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
+    }
 #undef XV_TRY
     st->last_k = k;
     st->last_k_seq = k_seq;
     return XV_OK;
+}
+
+xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                                 const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
+                                 int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream) {
+    return verify_impl(cfg, w, st, tokens, k, k_seq, logits, argmax, n_accept, ws, ws_bytes, stream, true);
 }
 
 xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
@@ -343,6 +351,9 @@ xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w
     if (xv_status e = check_state(d, cfg, st)) return e;
     if (!tokens || T < 1) return fail(XV_ERR_ARG, "prefill: need tokens and T >= 1");
     if (chunk < 1 || chunk > st->kmax) return fail(XV_ERR_ARG, "prefill: chunk = %d outside [1, kmax = %d]", chunk, st->kmax);
+    if (static_cast<long long>(st->B) * chunk > XV_GEMM_M_MAX)
+        return fail(XV_ERR_UNSUPPORTED, "prefill: B*chunk = %lld exceeds %d", static_cast<long long>(st->B) * chunk,
+                    XV_GEMM_M_MAX);
     if (st->last_k != 0) return fail(XV_ERR_ARG, "prefill: the previous verify has not been committed");
     if (st->max_ctx < 0 || static_cast<long long>(st->max_ctx) + T > st->Lmax)
         return fail(XV_ERR_ARG, "prefill: max_ctx + T exceeds Lmax (%d)", st->Lmax);
@@ -367,7 +378,8 @@ xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w
                                                        cudaMemcpyDeviceToDevice, s),
                                      "prefill: gather the chunk"))
             return e;
-        if (xv_status e = xv_verify_block(cfg, w, st, tok, k, nullptr, am, na, ws, vbytes, stream)) return e;
+        // only the last chunk's logits are read: the others stop before the LM head
+        if (xv_status e = verify_impl(cfg, w, st, tok, k, nullptr, nullptr, am, na, ws, vbytes, stream, last)) return e;
         if (last) {
             // the last position of each sequence: row b*k + k - 1
             if (last_logits &&

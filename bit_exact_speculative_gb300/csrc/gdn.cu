@@ -231,19 +231,22 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
     griddep_wait();
 
     // Every load of the CTA in flight at once, each thread's own: its state row (the longest
-    // trip), the commit count, one beta or gate scalar (2 * total <= THREADS), one 16-byte chunk
+    // trip), the commit count, up to two beta or gate scalars (2 * total <= 2 * THREADS), one 16-byte chunk
     // of a step's v slice, then the q / k chunks its normalisation group reads.  (Bulk copies
     // of the same pieces, 3 per step, took 2 us to issue for 16 steps.)
     float2 s[RPT][NP];
 #pragma unroll
     for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], srow0 + static_cast<size_t>(r[x]) * DK, g);
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
-    const int bg_idx = threadIdx.x;
-    uint16_t bg = 0;
-    if (bg_idx < 2 * total) {
-        long long row;
-        const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
-        bg = (bg_idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
+    uint16_t bg[2] = {0, 0};   // slots threadIdx.x and threadIdx.x + THREADS of (beta, gate) x step
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int bg_idx = threadIdx.x + q * THREADS;
+        if (bg_idx < 2 * total) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
+            bg[q] = (bg_idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
+        }
     }
     constexpr int VCH = ROWS_PER_CTA / 8;   // 16-byte chunks of a step's v slice
     for (int idx = threadIdx.x; idx < total * VCH; idx += THREADS) {
@@ -263,17 +266,21 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
         if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
     }
-    if (bg_idx < 2 * total) {
-        long long row;
-        const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
-        float x = bf16f(bg);
-        if (src.raw_gates) {
-            // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
-            if (bg_idx & 1) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
-            else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int bg_idx = threadIdx.x + q * THREADS;
+        if (bg_idx < 2 * total) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
+            float x = bf16f(bg[q]);
+            if (src.raw_gates) {
+                // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
+                if (bg_idx & 1) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
+                else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
+            }
+            if (bg_idx & 1) steps[bg_idx >> 1].gate = x;
+            else steps[bg_idx >> 1].beta = x;
         }
-        if (bg_idx & 1) steps[bg_idx >> 1].gate = x;
-        else steps[bg_idx >> 1].beta = x;
     }
     __syncthreads();
 
@@ -323,16 +330,28 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
               qk_l2norm ? 1 : 0, H / Hk, err};
     const int max_steps = max_commit + k;
-    if (max_steps > THREADS / 2) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS / 2);
+    if (max_steps > THREADS) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS);
     dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
-    trace_pre(s);
     static bool carve[2] = {false, false};
     if (!carve[dk == 128]) {
-        // as much shared memory as possible for the carveout: several CTAs per SM at B = 8
-        if (dk == 128) cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        else cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        // as much shared memory as possible for the carveout: several CTAs per SM at B = 8; up to
+        // THREADS staged steps (a prefill chunk of XV_KMAX positions after as many pending ones)
+        xv_status st;
+        if (dk == 128) {
+            cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            st = cuda_check(cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(sizeof(StepSmem<128>) * THREADS)),
+                            "gdn: set shared memory size");
+        } else {
+            cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            st = cuda_check(cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(sizeof(StepSmem<64>) * THREADS)),
+                            "gdn: set shared memory size");
+        }
+        if (st) return st;
         carve[dk == 128] = true;
     }
+    trace_pre(s);
     if (dk == 128) {
         const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
         launch_k(gdn_kernel<128>, dim3(grid), dim3(THREADS), sm, s, a);

@@ -41,10 +41,10 @@ struct ConvArgs {
     unsigned* err;
 };
 
-// One thread per (channel, sequence).  Every load is issued before the first
-// use: the new window is the last Kc-1 entries of (state ++ pending[0, n)),
-// the k input rows come in one predicated burst; the window then slides over
-// them in registers.
+// One thread per (channel, sequence).  The new window is the last Kc-1 entries
+// of (state ++ pending[0, n)); the k input rows come in predicated bursts of
+// XC rows (the first burst is issued with the window's loads); the window
+// slides over them in registers.
 template <int KC>
 __global__ void __launch_bounds__(CONV_THREADS) conv_kernel(ConvArgs A) {
     griddep_launch();
@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(CONV_THREADS) conv_kernel(ConvArgs A) {
     const int b = blockIdx.y;
     if (c >= A.C) return;
     uint16_t* st = A.state + static_cast<long long>(b) * W * A.C + c;
-    uint16_t old[W], win[W], xs[XV_KMAX];
+    constexpr int XC = 16;
+    uint16_t old[W], win[W], xs[XC];
 #pragma unroll
     for (int j = 0; j < W; ++j) old[j] = st[static_cast<long long>(j) * A.C];
     int nc = A.n_commit ? A.n_commit[b] : 0;
@@ -77,8 +78,11 @@ __global__ void __launch_bounds__(CONV_THREADS) conv_kernel(ConvArgs A) {
         }
     }
     const long long xrow = static_cast<long long>(b) * A.x_rows;
+    auto burst = [&](int t0) {
 #pragma unroll
-    for (int t = 0; t < XV_KMAX; ++t) xs[t] = t < A.k ? A.x[(xrow + t) * A.x_stride + c] : uint16_t(0);
+        for (int t = 0; t < XC; ++t) xs[t] = t0 + t < A.k ? A.x[(xrow + t0 + t) * A.x_stride + c] : uint16_t(0);
+    };
+    burst(0);
     if (nc > 0) {
 #pragma unroll
         for (int j = 0; j < W; ++j) st[static_cast<long long>(j) * A.C] = win[j];
@@ -87,17 +91,20 @@ __global__ void __launch_bounds__(CONV_THREADS) conv_kernel(ConvArgs A) {
     float w[KC];
 #pragma unroll
     for (int j = 0; j < KC; ++j) w[j] = bfv(A.w[static_cast<long long>(c) * KC + j]);
+    for (int t0 = 0; t0 < A.k; t0 += XC) {
+        if (t0 > 0) burst(t0);
 #pragma unroll
-    for (int t = 0; t < XV_KMAX; ++t) {
-        if (t < A.k) {
-            float acc = __fmul_rn(w[0], bfv(win[0]));
+        for (int t = 0; t < XC; ++t) {
+            if (t0 + t < A.k) {
+                float acc = __fmul_rn(w[0], bfv(win[0]));
 #pragma unroll
-            for (int j = 1; j < W; ++j) acc = __fmaf_rn(w[j], bfv(win[j]), acc);
-            acc = __fmaf_rn(w[W], bfv(xs[t]), acc);
-            A.y[(static_cast<long long>(b) * A.k + t) * A.y_stride + c] = f32_to_bf16(silu_f(acc));
+                for (int j = 1; j < W; ++j) acc = __fmaf_rn(w[j], bfv(win[j]), acc);
+                acc = __fmaf_rn(w[W], bfv(xs[t]), acc);
+                A.y[(static_cast<long long>(b) * A.k + t0 + t) * A.y_stride + c] = f32_to_bf16(silu_f(acc));
 #pragma unroll
-            for (int j = 0; j + 1 < W; ++j) win[j] = win[j + 1];
-            win[W - 1] = xs[t];
+                for (int j = 0; j + 1 < W; ++j) win[j] = win[j + 1];
+                win[W - 1] = xs[t];
+            }
         }
     }
 }

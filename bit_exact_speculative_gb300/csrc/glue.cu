@@ -241,19 +241,21 @@ __global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk
     griddep_launch();
     griddep_wait();
     __shared__ int pred[XV_KMAX];
-    const int b = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = static_cast<long long>(b) * k + j;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = lane; c < nchunk; c += 32) {
-        const float2 p = part[row * nchunk + c];
-        better(bv, bi, p.x, __float_as_int(p.y));
-    }
-    warp_best(bv, bi);
-    if (lane == 0) {
-        const int id = bi == 0x7fffffff ? 0 : bi;
-        idx[row] = id;
-        pred[j] = id;
+    const int b = blockIdx.x, lane = threadIdx.x & 31;
+    for (int j = threadIdx.x >> 5; j < k; j += blockDim.x >> 5) {   // warp per row
+        const long long row = static_cast<long long>(b) * k + j;
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int c = lane; c < nchunk; c += 32) {
+            const float2 p = part[row * nchunk + c];
+            better(bv, bi, p.x, __float_as_int(p.y));
+        }
+        warp_best(bv, bi);
+        if (lane == 0) {
+            const int id = bi == 0x7fffffff ? 0 : bi;
+            idx[row] = id;
+            pred[j] = id;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -372,7 +374,8 @@ xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t
     launch_k(argmax_chunk_kernel, dim3(nchunk, M), dim3(ARGMAX_THREADS), 0, s, logits, V, part, nchunk);
     if (xv_status st = launched("argmax_chunk_kernel", s, K_ARGMAX, 4ll * M * V)) return st;
     trace_pre(s);
-    launch_k(argmax_accept_kernel, dim3(B), dim3(32 * k), 0, s, part, nchunk, k, idx, tokens, k_seq, n_accept, err);
+    launch_k(argmax_accept_kernel, dim3(B), dim3(32 * (k < 32 ? k : 32)), 0, s, part, nchunk, k, idx, tokens, k_seq,
+             n_accept, err);
     return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
 }
 

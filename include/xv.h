@@ -55,9 +55,9 @@ typedef int xv_status;
 #define XV_ERR_CUDA        -4   /* a CUDA runtime call or launch failed */
 #define XV_ERR_DEVICE_CHECK -5  /* a kernel recorded a device-side error (see xv_device_check) */
 
-#define XV_ABI_VERSION 2
+#define XV_ABI_VERSION 3
 #define XV_GEMM_M_MAX 64        /* rows per small-M GEMM call */
-#define XV_KMAX 16              /* draft tokens per sequence per verify call */
+#define XV_KMAX 64              /* tokens per sequence per verify (or prefill chunk) call */
 #define XV_CONV_MAX 8           /* widest causal convolution of a complete GDN layer */
 
 /* Version of this header's ABI (XV_ABI_VERSION). */
@@ -250,7 +250,8 @@ xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z
  *   gate  optional [B*R rows, Hq*hd] bf16 with row stride gate_stride, or NULL:
  *         when given, out = bf16( bf16(attn) * sigmoid(gate) ) (the gated
  *         attention layer's output gate), else out = bf16(attn)
- *   hd = 256 or 64 (hd % 64 == 0), Hq % Hkv == 0, R*(Hq/Hkv) <= 64, 1 <= R <= XV_KMAX
+ *   hd = 256 or 64 (hd % 64 == 0), Hq % Hkv == 0, 1 <= R <= XV_KMAX (the R*(Hq/Hkv) rows of a
+ *         kv head go in tiles of 64 rows, one CTA each per split)
  * Workspace: xv_attn_workspace_size(B, R, Hq, hd, max_ctx) bytes. */
 int xv_attn_split_size(void);
 size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx);
@@ -431,8 +432,10 @@ xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stre
  * decode steps, for every chunk size: batch-invariant by construction.
  * last_logits [B, V] fp32 and last_argmax [B] int32 (device, each may be
  * NULL) receive the logits and greedy token after each sequence's last
- * prompt token.  1 <= chunk <= st->kmax; the last verify must have been
- * committed; st->max_ctx + T <= Lmax.  Workspace:
+ * prompt token; only the last chunk runs the LM head.  1 <= chunk <= st->kmax,
+ * B*chunk <= XV_GEMM_M_MAX (so a prefill of one sequence takes chunks of up to 64
+ * tokens); the last verify must have been committed; st->max_ctx + T <= Lmax.
+ * Workspace:
  * xv_block_prefill_workspace_size(cfg, B, kmax, Lmax). */
 size_t xv_block_prefill_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);
 xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(xv):
 
 
 def test_abi_version(xv):
-    assert xv.xv_abi_version() == 2
+    assert xv.xv_abi_version() == 3
 
 
 def _code(fn, *args):
@@ -81,8 +81,8 @@ def test_gdn_validation_without_gpu(xv):
     assert L.xv_gdn_decode_step(ctypes.c_void_p(p), ctypes.byref(st), ctypes.c_void_p(p), 128, 1, 1, 128, 40, 1, None) == xv.XV_ERR_UNSUPPORTED
     assert L.xv_gdn_verify(ctypes.c_void_p(p), ctypes.byref(st), None, 4, ctypes.byref(st), 8, ctypes.c_void_p(p),
                            128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_ARG  # n_commit missing
-    assert L.xv_gdn_verify(ctypes.c_void_p(p), None, None, 0, ctypes.byref(st), 17, ctypes.c_void_p(p),
-                           128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_UNSUPPORTED  # k > 16
+    assert L.xv_gdn_verify(ctypes.c_void_p(p), None, None, 0, ctypes.byref(st), xv.XV_KMAX + 1, ctypes.c_void_p(p),
+                           128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_UNSUPPORTED  # k > XV_KMAX
     short = xv.GdnSteps(p, p, p, p, p, 128 * 3, 2, 4)
     assert L.xv_gdn_verify(ctypes.c_void_p(p), None, None, 0, ctypes.byref(short), 8, ctypes.c_void_p(p),
                            128, 1, 1, 128, 128, 1, None) == xv.XV_ERR_ARG  # draft rows < k
@@ -97,8 +97,8 @@ def test_attn_validation_without_gpu(xv):
     assert L.xv_attn_decode_rows(*args(q=None)) == xv.XV_ERR_ARG
     assert L.xv_attn_decode_rows(*args(hd=128)) == xv.XV_ERR_UNSUPPORTED
     assert L.xv_attn_decode_rows(*args(Hq=25)) == xv.XV_ERR_ARG
-    assert L.xv_attn_decode_rows(*args(R=17)) == xv.XV_ERR_UNSUPPORTED
-    assert L.xv_attn_decode_rows(*args(Hq=80, Hkv=4)) == xv.XV_ERR_UNSUPPORTED      # 8 rows x 20 heads > 64
+    assert L.xv_attn_decode_rows(*args(R=xv.XV_KMAX + 1)) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_attn_decode_rows(*args(R=0)) == xv.XV_ERR_ARG
     assert L.xv_attn_decode_rows(*args(max_ctx=5000)) == xv.XV_ERR_ARG              # beyond Lmax
     assert L.xv_attn_decode_rows(*args(ws=None)) == xv.XV_ERR_WORKSPACE
     assert xv.xv_attn_split_size() == 512

@@ -94,6 +94,28 @@ def test_verify_rows_equal_decode_rows(xv, L):
             assert_bf16_close(o[r, h], ref, what=f"L{L} r{r} h{h}")
 
 
+@pytest.mark.parametrize("R,L", [(16, 2183), (64, 480), (64, 4050)])
+def test_row_tiles_equal_decode_rows(xv, R, L):
+    """Past 64 rows per kv head (R x 6 q heads) the rows go in tiles of 64, one CTA each per split;
+    every row still equals an R=1 call at its own length, also where the rows cross a split
+    boundary (480 + 63, 4050 + 63), and the oracle (GQA 24/4, hd 256)."""
+    B, Hq, Hkv, hd = 1, 24, 4, 256
+    Lmax = L + R
+    q, kc, vc = make(7, B, R, Hq, Hkv, hd, Lmax, name=f"tiles{R}.{L}")
+    Q, K, V = dev(q), dev(kc), dev(vc)
+    out = attn(xv, Q, K, V, dev(np.array([L], np.int32)), R, B, Hq, Hkv, hd, Lmax, L + R - 1)
+    for r in range(R):
+        one = attn(xv, Q[r:r + 1], K, V, dev(np.array([L + r], np.int32)), 1, B, Hq, Hkv, hd, Lmax, L + r)
+        assert same_bits(out[r:r + 1], one), f"row {r} differs from the decode row at length {L + r}"
+    o = host_u16(out).reshape(R, Hq, hd)
+    for r in (0, 10, R - 1):
+        for h in (0, 11, 23):
+            g = h // (Hq // Hkv)
+            ref = oracle.attn_row(q[r, h * hd:(h + 1) * hd], kc[0, g], vc[0, g], L + r, hd ** -0.5)
+            assert_bf16_close(o[r, h], ref, what=f"R{R} L{L} r{r} h{h}")
+    assert xv.xv_device_check() == 0
+
+
 def test_eight_in_flight_equal_alone(xv):
     B, R, Hq, Hkv, hd = 8, 8, 24, 4, 256
     lens = np.array([640, 2183, 1, 513, 1024, 100, 2000, 511], dtype=np.int32)

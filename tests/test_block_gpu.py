@@ -317,8 +317,8 @@ def test_ragged_commit_beyond_k_seq_is_flagged(tiny):
 
 @pytest.mark.parametrize("cfg_name", ["TINY", "TINY_FULL"])
 def test_prefill_any_chunk_equals_decode(built, cfg_name):
-    """Prefill of 37 tokens in chunks of 4 or 3 leaves the states of 37 decode steps bit for bit:
-    the same last logits, the same GDN/convolution states and the same next verify."""
+    """Prefill of 37 tokens in chunks of 4, 3 or 32 leaves the states of 37 decode steps bit for
+    bit: the same last logits, the same GDN/convolution states and the same next verify."""
     cfg = getattr(workloads, cfg_name)
     w = workloads.weights(cfg, seed=0)
     B, k, Lmax, T = 2, 4, 256, 37
@@ -326,8 +326,8 @@ def test_prefill_any_chunk_equals_decode(built, cfg_name):
     prompt = np.concatenate([workloads.draft_tokens(cfg, 0, 30 + i, B, 1) for i in range(T)], axis=1)
     nxt = workloads.draft_tokens(cfg, 0, 90, B, k)
     outs = []
-    for chunk in (4, 3):
-        A = gpu_stack(cfg, w, B, k, Lmax, lens)
+    for kmax, chunk in ((k, 4), (k, 3), (32, 32)):
+        A = gpu_stack(cfg, w, B, kmax, Lmax, lens)
         lg, am = A.prefill(dev(prompt), chunk)
         lgv = A.verify(dev(nxt), k)[0].clone()
         A.commit(torch.full((B,), k, dtype=torch.int32, device="cuda"))
@@ -351,16 +351,17 @@ def test_prefill_any_chunk_equals_decode(built, cfg_name):
 
 
 def test_stack_prefill_chunks_equal(stack):
-    """The 5120-wide stack: 50 prompt tokens prefilled in chunks of 8 and of 5 give the same last
-    logits and the same next verify, and match 50 decode steps."""
+    """The 5120-wide stack: 150 prompt tokens prefilled in chunks of 64 (384 attention rows per
+    kv head: 6 row tiles), 8 and 5 give the same last logits and the same next verify, and match
+    150 decode steps."""
     cfg, w, wd = stack
-    B, k, L, T = 1, 8, 640, 50
+    B, k, L, T = 1, 8, 640, 150
     Lmax = L + T + 2 * k
     prompt = np.concatenate([workloads.draft_tokens(cfg, 0, 300 + i, B, 1) for i in range(T)], axis=1)
     nxt = workloads.draft_tokens(cfg, 0, 399, B, k)
     res = []
-    for chunk in (8, 5):
-        A = gpu_stack(cfg, w, B, k, Lmax, [L], weights_dev=wd)
+    for chunk in (64, 8, 5):
+        A = gpu_stack(cfg, w, B, 64, Lmax, [L], weights_dev=wd)
         lg, _ = A.prefill(dev(prompt), chunk)
         res.append((lg.clone(), A.verify(dev(nxt), k)[0].clone()))
         del A

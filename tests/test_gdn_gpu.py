@@ -117,9 +117,8 @@ def test_dk64_tiny_heads(xv):
     assert_state_close(host(S), Sref)
 
 
-@pytest.mark.parametrize("B", [1, 8])
-def test_verify_equals_sequential_decode_and_rollback(xv, B):
-    K = 8
+@pytest.mark.parametrize("B,K", [(1, 8), (8, 8), (1, 64)])
+def test_verify_equals_sequential_decode_and_rollback(xv, B, K):
     qkv_h, gates_h = make_inputs(4, B, K)
     qkv, gates = dev(qkv_h), dev(gates_h)
     S0 = dev(init_state(4, B))
@@ -150,14 +149,15 @@ def test_verify_equals_sequential_decode_and_rollback(xv, B):
     assert xv.xv_device_check() == 0
 
 
-def test_replay_then_speculate_matches_decode(xv):
-    """Round 2 of a speculative loop: replay 3 kept steps, speculate 8 new ones."""
-    B, K = 2, 8
-    qkv_h, gates_h = make_inputs(5, B, 2 * K)          # rows b*16 + t, first 8 = round 1, last 8 = round 2
+@pytest.mark.parametrize("K,keep", [(8, 3), (64, 37), (64, 64)])
+def test_replay_then_speculate_matches_decode(xv, K, keep):
+    """Round 2 of a speculative loop: replay `keep` kept steps, speculate K new ones (up to 128
+    staged steps in one call)."""
+    B = 2
+    qkv_h, gates_h = make_inputs(5, B, 2 * K)          # rows b*2K + t: first K = round 1, last K = round 2
     qkv, gates = dev(qkv_h), dev(gates_h)
     S0 = dev(init_state(5, B))
-    keep = 3
-    # decode reference: 3 steps of round 1, then 8 of round 2
+    # decode reference: `keep` steps of round 1, then the K of round 2
     Sd = S0.clone()
     outs = []
     for t in list(range(keep)) + list(range(K, 2 * K)):

@@ -61,10 +61,11 @@ def test_conv_decode_parity_and_state(xv, Kc, C):
     assert xv.xv_device_check() == 0
 
 
-def test_conv_verify_rows_equal_decode_and_commit_any_j(xv):
+@pytest.mark.parametrize("k", [8, 64])
+def test_conv_verify_rows_equal_decode_and_commit_any_j(xv, k):
     """k rows in one call equal k one-row calls bit for bit; committing j of them shifts exactly
     those j into the state."""
-    B, k, C, Kc = 2, 8, 1024, 4
+    B, C, Kc = 2, 1024, 4
     w, x, st0 = conv_inputs(2, B, k, C, Kc)
     W, X = dev(w), dev(x)
     S = dev(st0)
