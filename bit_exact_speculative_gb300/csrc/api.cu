@@ -357,6 +357,7 @@ xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint1
         return st;
     size_t need = attn_workspace_size(B, R, Hq, hd, max_ctx);
     if (!ws || ws_bytes < need) return fail(XV_ERR_WORKSPACE, "attn: workspace of %zu bytes needed", need);
+    if (!aligned16(ws)) return fail(XV_ERR_UNSUPPORTED, "attn: workspace must be 16-byte aligned");
     return attn_launch(q, q_stride, kc, vc, kv_contiguous(B, Lmax), ctx_len, 0, R, B, Hq, Hkv, hd, max_ctx, scale, gate,
                        gate_stride, out, out_stride, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
@@ -392,6 +393,7 @@ xv_status xv_attn_decode_rows_paged(const uint16_t* q, long long q_stride, const
     if (max_ctx < R || max_ctx > Lmax) return fail(XV_ERR_ARG, "attn: need R <= max_ctx <= page_size * max_pages");
     size_t need = attn_workspace_size(B, R, Hq, hd, max_ctx);
     if (!ws || ws_bytes < need) return fail(XV_ERR_WORKSPACE, "attn: workspace of %zu bytes needed", need);
+    if (!aligned16(ws)) return fail(XV_ERR_UNSUPPORTED, "attn: workspace must be 16-byte aligned");
     return attn_launch(q, q_stride, kpool, vpool, kv, ctx_len, 0, R, B, Hq, Hkv, hd, max_ctx, scale, gate, gate_stride,
                        out, out_stride, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }

@@ -406,10 +406,24 @@ struct CombineArgs {
     unsigned* err;
 };
 
-// One CTA per (row, q head); thread t owns output elements 2t and 2t+1.
-__global__ void attn_combine_kernel(CombineArgs C) {
+// One CTA per (row, q head); thread t owns output elements 2t and 2t+1.  Per thread, in split
+// order s = 0..ns-1:  w_s = exp2(m_s - M), L += w_s l_s, acc += w_s o_s;  out = acc / L, where M
+// is the largest m_s (a maximum is exact in any order, so the CTA takes it as a tree).  The
+// split partials o_s of a (row, head) are contiguous: they stream through shared memory in
+// chunks of COMB_CH splits by bulk copies, COMB_NB chunks in flight.
+constexpr int COMB_CH = 32, COMB_NB = 3;
+
+inline size_t combine_smem(int hd, int nsplit) {
+    return static_cast<size_t>(COMB_NB) * COMB_CH * hd * 4 + static_cast<size_t>(nsplit) * 8;
+}
+
+__global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
     griddep_launch();
     griddep_wait();
+    extern __shared__ __align__(128) uint8_t csm[];
+    __shared__ __align__(8) uint64_t cbar[COMB_NB];
+    __shared__ float wmax[4];
+    __shared__ volatile int s_abort;
     const int hq = blockIdx.x % C.Hq;
     const long long br = blockIdx.x / C.Hq;
     const int b = static_cast<int>(br / C.R), r = static_cast<int>(br % C.R);
@@ -417,30 +431,70 @@ __global__ void attn_combine_kernel(CombineArgs C) {
     if (len < 1 || len - r + C.R - 1 > C.max_len) return;   // reported by the split kernel
     const int ns = (len + ATTN_SPLIT - 1) / ATTN_SPLIT;
     const long long idx0 = (br * C.Hq + hq) * C.nsplit;
-    float M = NEG_INF;
-#pragma unroll 8
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, C.ml[idx0 + s].x);
-    const int d = 2 * threadIdx.x;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    float* obuf = reinterpret_cast<float*>(csm);               // COMB_NB chunks of [COMB_CH][hd]
+    float* wv = obuf + COMB_NB * COMB_CH * C.hd;               // w_s
+    float* lv = wv + C.nsplit;                                 // l_s
+    const int nchunk = (ns + COMB_CH - 1) / COMB_CH;
+    const float* src = C.opart + idx0 * C.hd;
+    auto bar = [&](int i) { return smem_u32(&cbar[i]); };
+    auto issue = [&](int c) {
+        const int n = min(COMB_CH, ns - c * COMB_CH);
+        const uint32_t bytes = static_cast<uint32_t>(n) * C.hd * 4;
+        mbar_arrive_expect_tx(bar(c % COMB_NB), bytes);
+        bulk_load(smem_u32(obuf + (c % COMB_NB) * COMB_CH * C.hd), src + static_cast<long long>(c) * COMB_CH * C.hd,
+                  bytes, bar(c % COMB_NB));
+    };
+    int issued = 0;   // thread 0: chunks whose copies have been issued
+    if (tid == 0) {
+        for (int i = 0; i < COMB_NB; ++i) mbar_init(bar(i), 1);
+        fence_mbar_init();
+        s_abort = 0;
+        for (; issued < nchunk && issued < COMB_NB; ++issued) issue(issued);
+    }
+    float mx = NEG_INF;
+    for (int s = tid; s < ns; s += nt) {
+        const float2 v = C.ml[idx0 + s];
+        wv[s] = v.x;
+        lv[s] = v.y;
+        mx = fmaxf(mx, v.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+    __syncthreads();
+    float M = wmax[0];
+    for (int w = 1; w < (nt >> 5); ++w) M = fmaxf(M, wmax[w]);
+    for (int s = tid; s < ns; s += nt) wv[s] = exp2f(__fsub_rn(wv[s], M));
+    __syncthreads();
+    const int d = 2 * tid;
     float L = 0.f, acc0 = 0.f, acc1 = 0.f;
-    // chunks of CH splits: every load of a chunk is issued before its adds, which stay in split order
-    constexpr int CH = 16;
-    for (int s0 = 0; s0 < ns; s0 += CH) {
-        float2 ml[CH], o[CH];
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-            const int s = s0 + j < ns ? s0 + j : ns - 1;
-            ml[j] = C.ml[idx0 + s];
-            o[j] = *reinterpret_cast<const float2*>(C.opart + (idx0 + s) * C.hd + d);
-        }
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-            if (s0 + j < ns) {
-                const float w = exp2f(__fsub_rn(ml[j].x, M));
-                L = __fadd_rn(L, __fmul_rn(w, ml[j].y));
-                acc0 = __fadd_rn(acc0, __fmul_rn(w, o[j].x));
-                acc1 = __fadd_rn(acc1, __fmul_rn(w, o[j].y));
+    for (int c = 0; c < nchunk; ++c) {
+        const int st = c % COMB_NB;
+        if (!s_abort && !mbar_wait(bar(st), (c / COMB_NB) & 1u, C.err)) s_abort = 1;
+        if (!s_abort) {
+            const float* ob = obuf + st * COMB_CH * C.hd + d;
+            const int s0 = c * COMB_CH, n = min(COMB_CH, ns - s0);
+            for (int j = 0; j < n; ++j) {
+                const float w = wv[s0 + j];
+                const float2 o = *reinterpret_cast<const float2*>(ob + j * C.hd);
+                L = __fadd_rn(L, __fmul_rn(w, lv[s0 + j]));
+                acc0 = __fadd_rn(acc0, __fmul_rn(w, o.x));
+                acc1 = __fadd_rn(acc1, __fmul_rn(w, o.y));
             }
         }
+        __syncthreads();   // every thread is done with chunk c's buffer
+        if (tid == 0 && c + COMB_NB < nchunk && !s_abort) {
+            fence_proxy_async_smem();
+            issue(c + COMB_NB);
+            ++issued;
+        }
+    }
+    if (s_abort) {
+        // copies still in flight land before the CTA leaves: wait for the last one of each buffer
+        if (tid == 0)
+            for (int c = issued - 1; c >= 0 && c >= issued - COMB_NB; --c) mbar_wait(bar(c % COMB_NB), (c / COMB_NB) & 1u, C.err);
+        return;
     }
     float y0 = __fdiv_rn(acc0, L), y1 = __fdiv_rn(acc1, L);
     if (C.gate) {
@@ -547,8 +601,20 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
     xv_status st = hd == 256 ? launch_split<256>(tmK, tmV, a, B, s) : launch_split<64>(tmK, tmV, a, B, s);
     if (st) return st;
     CombineArgs c{ctx_len, len_bias, R, Hq, nsplit, max_len, hd, opart, ml, gate, gate_stride, out, out_stride, err};
+    const size_t csm = combine_smem(hd, nsplit);
+    static size_t csm_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "attn: device ordinal out of range");
+    if (csm > csm_set[dev]) {
+        if (xv_status e = cuda_check(cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          static_cast<int>(csm)),
+                                     "attn: set combine shared memory size"))
+            return e;
+        csm_set[dev] = csm;
+    }
     trace_pre(s);
-    launch_k(attn_combine_kernel, dim3(B * R * Hq), dim3(hd / 2), 0, s, c);
+    launch_k(attn_combine_kernel, dim3(B * R * Hq), dim3(hd / 2), csm, s, c);
     return launched("attn_combine_kernel", s, K_ATTN_COMBINE,
                     4ll * B * R * Hq * nsplit * (hd + 2) + 2ll * B * R * Hq * hd * (gate ? 2 : 1));
 }

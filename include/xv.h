@@ -252,7 +252,7 @@ xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z
  *         attention layer's output gate), else out = bf16(attn)
  *   hd = 256 or 64 (hd % 64 == 0), Hq % Hkv == 0, 1 <= R <= XV_KMAX (the R*(Hq/Hkv) rows of a
  *         kv head go in tiles of 64 rows, one CTA each per split)
- * Workspace: xv_attn_workspace_size(B, R, Hq, hd, max_ctx) bytes. */
+ * Workspace: xv_attn_workspace_size(B, R, Hq, hd, max_ctx) bytes, 16-byte aligned. */
 int xv_attn_split_size(void);
 size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx);
 xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,

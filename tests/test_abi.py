@@ -101,6 +101,7 @@ def test_attn_validation_without_gpu(xv):
     assert L.xv_attn_decode_rows(*args(R=0)) == xv.XV_ERR_ARG
     assert L.xv_attn_decode_rows(*args(max_ctx=5000)) == xv.XV_ERR_ARG              # beyond Lmax
     assert L.xv_attn_decode_rows(*args(ws=None)) == xv.XV_ERR_WORKSPACE
+    assert L.xv_attn_decode_rows(*args(ws=ctypes.c_void_p(0x10008))) == xv.XV_ERR_UNSUPPORTED   # misaligned
     assert xv.xv_attn_split_size() == 512
     assert xv.xv_attn_workspace_size(1, 8, 24, 256, 2183) >= 8 * 24 * 5 * 256 * 4
 
