@@ -78,8 +78,8 @@ struct AttnShape {
     static constexpr int K_OFF = P_OFF + 2 * BLK;
     static constexpr int V_OFF = K_OFF + SK * TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + SV * TILE_BYTES;
-    // fullK, emptyK, fullV, emptyV, sbar[2], sfree[2], pready[2], pfree[2], done, vfix
-    static constexpr int N_BARS = 2 * SK + 2 * SV + 10;
+    // fullK, emptyK, fullV, emptyV, vfix, sbar[2], sfree[2], pready[2], pfree[2], done, ofree, qfull
+    static constexpr int N_BARS = 2 * SK + 3 * SV + 11;
     static constexpr int SMEM = 1024 + BAR_OFF + 8 * N_BARS;
     static constexpr uint32_t TMEM_COLS = HD == 256 ? 512 : 256;   // S[2] (64 columns each) + O (HD)
 };
@@ -90,7 +90,7 @@ struct AttnArgs {
     KvPages kv;
     const int32_t* ctx_len;
     int len_bias;
-    int R, G, Hq, Hkv, nsplit, max_len;
+    int R, G, Hq, Hkv, nsplit, max_len, B;
     float sl2;          // scale * log2(e)
     float* opart;       // [B*R*Hq][nsplit][HD]
     float2* ml;         // [B*R*Hq][nsplit] (reference max in log2 units, sum)
@@ -100,18 +100,79 @@ struct AttnArgs {
 constexpr int ATTN_THREADS = 160;   // warps 0-1 softmax, 2 K loads, 3 V loads, 4 MMA
 constexpr float RESCALE_SLACK = 2.f;
 
-// One CTA per (split, kv head, sequence).  Per 64-position tile i of the split:
-//   MMA warp   S[i%2] = Q K_i^T on tcgen05 (M = 128 rows, N = 64 positions, fp32 in TMEM), issued
+// A unit of work: (split, 64-row tile, kv head, sequence), numbered with the split fastest so
+// that a CTA's consecutive items mostly share their Q tile.  Dead items (the split starts at or
+// past every row's length, or the sequence's length is out of range) are skipped by every warp.
+struct AttnItem {
+    int b, g, row_base, split, L0, maxlen, p_begin, ntiles;
+    bool live, bad;
+};
+
+__device__ __forceinline__ AttnItem attn_item(const AttnArgs& A, int it, int nrt) {
+    AttnItem I;
+    I.split = it % A.nsplit;
+    int rest = it / A.nsplit;
+    I.row_base = (rest % nrt) * 64;
+    rest /= nrt;
+    I.g = rest % A.Hkv;
+    I.b = rest / A.Hkv;
+    const int rows = A.R * A.G;
+    I.L0 = __ldg(A.ctx_len + I.b) + A.len_bias;     // visible length of row 0
+    I.bad = I.L0 < 1 || I.L0 + A.R - 1 > A.max_len;
+    // the longest visible length among the item's rows; positions past a row's own length are
+    // masked (p = 0), so how far the item runs does not change any row's bits
+    I.maxlen = I.L0 + (min(rows, I.row_base + 64) - 1) / A.G;
+    I.p_begin = I.split * ATTN_SPLIT;
+    I.live = !I.bad && I.p_begin < I.maxlen;
+    I.ntiles = I.live ? (min(I.p_begin + ATTN_SPLIT, I.maxlen) - I.p_begin + T - 1) / T : 0;
+    return I;
+}
+
+// Q rows (r, gh) of an item -> block row r*G + gh, tile row r*G + gh - row_base, 16-byte chunks
+// XOR-swizzled by row; rows past the block's R*G rows zero.  NT threads from t0, every load of a
+// thread issued before its stores.
+template <int HD, int BLK, int NT>
+__device__ __forceinline__ void load_q_tile(uint8_t* sq, const AttnArgs& A, const AttnItem& I, int t0) {
+    constexpr int N = 64 * (HD / 8), PER = (N + NT - 1) / NT;
+    const int rows = A.R * A.G;
+    uint4 v[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int idx = t0 + j * NT;
+        const int row = idx / (HD / 8), ch = idx % (HD / 8);
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (idx < N && I.row_base + row < rows) {
+            const int r = (I.row_base + row) / A.G, h = I.g * A.G + (I.row_base + row) % A.G;
+            v[j] = *reinterpret_cast<const uint4*>(A.q + (static_cast<long long>(I.b) * A.R + r) * A.q_stride +
+                                                   static_cast<long long>(h) * HD + ch * 8);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int idx = t0 + j * NT;
+        const int row = idx / (HD / 8), ch = idx % (HD / 8);
+        if (idx < N) *reinterpret_cast<uint4*>(sq + (ch >> 3) * BLK + row * 128 + (((ch & 7) ^ (row & 7)) * 16)) = v[j];
+    }
+}
+
+// Persistent CTAs (at most one per SM), each walking a contiguous range of items.  Per 64-position
+// tile of an item:
+//   MMA warp   S[t%2] = Q K_t^T on tcgen05 (M = 128 rows, N = 64 positions, fp32 in TMEM), issued
 //              one tile ahead
 //   softmax    thread = query row: its S row from TMEM, mask, scale; the reference max m moves
 //              to the tile's max when that exceeds it by more than RESCALE_SLACK (log2 units) or
 //              at the row's first live tile, and then O (TMEM) and the sum l are rescaled by
 //              exp2(m_old - m_new); P = bf16(exp2(s - m)) into shared memory, l += its fp32
 //              values in position order (exp2 by the hardware approximation)
-//   MMA warp   O += P V_i (N = HD; V straight from its TMA stage as an MN-major operand)
-// A row's operations depend on its own length and the absolute tile positions only, so a verify
-// row gets the bits of the decode row at its position.
-template <int HD>
+//   MMA warp   O += P V_t (N = HD; V straight from its TMA stage as an MN-major operand)
+// t counts the CTA's tiles across its items, so the K/V rings, the two S buffers and the two P
+// buffers keep cycling from one item to the next; an item's first P V overwrites O once the
+// softmax warps have read the previous item's O out (ofree), and Q is reloaded (qfull) only when
+// the item's (sequence, kv head, row tile) changes.  A row's operations depend on its own length
+// and the absolute tile positions only, so a verify row gets the bits of the decode row at its
+// position, whichever CTA and whichever neighbours it has.  MULTI = false is the launch with one
+// item per CTA (CTA i takes item i), with the cross-item hand-offs compiled out.
+template <int HD, bool MULTI>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs A) {
     griddep_launch();
@@ -131,7 +192,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     auto emptyK = [&](int st) { return bar0 + 8u * (SK + st); };
     auto fullV = [&](int st) { return bar0 + 8u * (2 * SK + st); };
     auto emptyV = [&](int st) { return bar0 + 8u * (2 * SK + SV + st); };
-    const uint32_t bx = bar0 + 8u * (2 * SK + 2 * SV);
+    // vfix[st]: the V rows of an item's last tile past every row's length have been zeroed in
+    // stage st (one barrier per stage: two fixes of one stage are a ring turn apart, so a wait is
+    // never two phases behind)
+    auto vfix = [&](int st) { return bar0 + 8u * (2 * SK + 2 * SV + st); };
+    const uint32_t bx = bar0 + 8u * (2 * SK + 3 * SV);
     auto sbar = [&](int j) { return bx + 8u * j; };
     auto sfree = [&](int j) { return bx + 8u * (2 + j); };
     auto pready = [&](int j) { return bx + 8u * (4 + j); };
@@ -139,27 +204,22 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     // P V of tile k only ever happens once that of tile k - 2 is known complete, so the barrier is
     // never two phases away from the one waited for
     auto pfree = [&](int j) { return bx + 8u * (6 + j); };
-    const uint32_t done = bx + 8u * 8, vfix = bx + 8u * 9;
+    const uint32_t done = bx + 8u * 8, ofree = bx + 8u * 9, qfull = bx + 8u * 10;
 
-    // blockIdx.x = split * nrt + row tile: the row tiles of one split are neighbours and share
-    // its K/V tiles through L2
-    const int rows = A.R * A.G, nrt = (rows + 63) / 64;
-    const int split = blockIdx.x / nrt, row_base = (blockIdx.x % nrt) * 64;
-    const int g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rows = A.R * A.G, nrt = (rows + 63) / 64;
+    const int n_items = A.nsplit * nrt * A.Hkv * A.B;
+    const int it0 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x) * n_items / gridDim.x) : blockIdx.x;
+    const int it1 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_items / gridDim.x) : it0 + 1;
     griddep_wait();
-    const int L0 = A.ctx_len[b] + A.len_bias;     // visible length of row 0
-    if (L0 < 1 || L0 + A.R - 1 > A.max_len) {
-        if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(A.err, ERR_BAD_LENGTH);
-        return;
-    }
-    // the longest visible length among this CTA's rows; positions past a row's own length are
-    // masked (p = 0), so how far the tile runs does not change any row's bits
-    const int maxlen = L0 + (min(rows, row_base + 64) - 1) / A.G;
-    const int p_begin = split * ATTN_SPLIT;
-    if (p_begin >= maxlen) return;
-    const int p_end = min(p_begin + ATTN_SPLIT, maxlen);
-    const int ntiles = (p_end - p_begin + T - 1) / T;
+    int first = it0;
+    while (first < it1 && !attn_item(A, first, nrt).live) ++first;
+    if (tid == 0)
+        for (int it = it0; it < it1; ++it) {
+            const AttnItem I = attn_item(A, it, nrt);
+            if (I.bad && I.split == 0 && I.row_base == 0 && I.g == 0) atomicOr(A.err, ERR_BAD_LENGTH);
+        }
+    if (first == it1) return;   // nothing live here: no barrier or tensor memory was set up
 
     if (tid == 0) {
         tma_prefetch_desc(&tmK);
@@ -171,6 +231,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         for (int st = 0; st < SV; ++st) {
             mbar_init(fullV(st), 1);
             mbar_init(emptyV(st), 1);
+            mbar_init(vfix(st), 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(sbar(j), 1);
@@ -179,7 +240,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             mbar_init(pfree(j), 1);
         }
         mbar_init(done, 1);
-        mbar_init(vfix, 1);
+        mbar_init(ofree, 64);
+        mbar_init(qfull, 64);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -187,19 +249,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_alloc(smem_u32(&tmem_slot), S::TMEM_COLS);
         tmem_relinquish();
     }
-    // Q rows (r, gh) -> block row r*G + gh, tile row r*G + gh - row_base, 16-byte chunks
-    // XOR-swizzled by row; rows past `rows` zero.
-    // (Starting the K/V copies before this, in parallel with it, was measured slower.)
-    for (int idx = tid; idx < 64 * (HD / 8); idx += ATTN_THREADS) {
-        const int row = idx / (HD / 8), ch = idx % (HD / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row_base + row < rows) {
-            const int r = (row_base + row) / A.G, h = g * A.G + (row_base + row) % A.G;
-            v = *reinterpret_cast<const uint4*>(A.q + (static_cast<long long>(b) * A.R + r) * A.q_stride +
-                                                static_cast<long long>(h) * HD + ch * 8);
-        }
-        *reinterpret_cast<uint4*>(smem + S::Q_OFF + (ch >> 3) * BLK + row * 128 + (((ch & 7) ^ (row & 7)) * 16)) = v;
-    }
+    // All threads load the first item's Q; the softmax warps reload it when an item's Q differs
+    // from the previous one's.  (Starting the K/V copies before this, in parallel with it, was
+    // measured slower.)
+    load_q_tile<HD, BLK, ATTN_THREADS>(smem + S::Q_OFF, A, attn_item(A, first, nrt), tid);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -219,157 +272,211 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     };
     // the same verdict for every lane of a warp that goes on to warp-collective instructions
     auto WW = [&](uint32_t bar, uint32_t par) -> bool { return __all_sync(0xffffffffu, W(bar, par)); };
+    auto same_q = [](const AttnItem& x, int b, int g, int rb) { return x.b == b && x.g == g && x.row_base == rb; };
 
     const uint32_t tS = tmem, tO = tmem + 128;   // columns: S[0] 0..63, S[1] 64..127, O 128..128+HD-1
 
     if (warp == 2 || warp == 3) {
-        // ---- TMA producers: warp 2 the K tiles, warp 3 the V tiles
-        if (lane == 0) {
-            const bool isK = warp == 2;
-            const int NS = isK ? SK : SV;
-            const CUtensorMap* map = isK ? &tmK : &tmV;
-            int issued = 0;
-            for (int i = 0; i < ntiles; ++i) {
-                const int st = i % NS;
-                if (i >= NS && !W(isK ? emptyK(st) : emptyV(st), ((i / NS) & 1u) ^ 1u)) break;
-                const uint32_t fb = isK ? fullK(st) : fullV(st);
-                const uint32_t dst = isK ? sK(st) : sV(st);
-                mbar_arrive_expect_tx(fb, TILE_BYTES);
-                int row;
-                const int z = kv_page(A.kv, b, p_begin + i * T, &row, A.err) * A.Hkv + g;
+        // ---- TMA producers: warp 2 the K tiles, warp 3 the V tiles (and the V fix of an item's
+        // last tile: once its copy has landed, rows past every row's length are zeroed so that
+        // p = 0 never meets a non-finite value there)
+        const bool isK = warp == 2;
+        const int NS = isK ? SK : SV;
+        const CUtensorMap* map = isK ? &tmK : &tmV;
+        int t = 0;   // tiles issued so far
+        bool ok = true;
+        for (int it = first; ok && it < it1; ++it) {
+            const AttnItem I = attn_item(A, it, nrt);
+            if (!I.live) continue;
+            if (lane == 0) {
+                for (int i = 0; i < I.ntiles; ++i) {
+                    const int st = t % NS;
+                    if (t >= NS && !W(isK ? emptyK(st) : emptyV(st), ((t / NS) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = isK ? fullK(st) : fullV(st);
+                    const uint32_t dst = isK ? sK(st) : sV(st);
+                    mbar_arrive_expect_tx(fb, TILE_BYTES);
+                    int row;
+                    const int z = kv_page(A.kv, I.b, I.p_begin + i * T, &row, A.err) * A.Hkv + I.g;
 #pragma unroll
-                for (int cb = 0; cb < CB; ++cb) tma_load_3d(dst + cb * BLK, map, cb * 64, row, z, fb);
-                issued = i + 1;
+                    for (int cb = 0; cb < CB; ++cb) tma_load_3d(dst + cb * BLK, map, cb * 64, row, z, fb);
+                    ++t;
+                }
             }
-            // every issued copy lands before the CTA may leave
-            for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
-                mbar_wait(isK ? fullK(j % NS) : fullV(j % NS), (j / NS) & 1u, A.err);
-        }
-        if (warp == 3 && p_begin + ntiles * T > maxlen) {
-            // V rows of the last tile past every row's length are zeroed once they have landed, so
-            // that p = 0 never meets a non-finite value there; P V of that tile waits for vfix
-            const int il = ntiles - 1, st = il % SV;
-            const int first = maxlen - (p_begin + il * T);
-            if (WW(fullV(st), (il / SV) & 1u)) {
-                for (int idx = first * 8 + lane; idx < T * 8; idx += 32)
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (!isK && ok && I.p_begin + I.ntiles * T > I.maxlen) {
+                const int tl = t - 1, st = tl % SV;
+                const int first_row = I.maxlen - (I.p_begin + (I.ntiles - 1) * T);
+                if (WW(fullV(st), (tl / SV) & 1u)) {
+                    for (int idx = first_row * 8 + lane; idx < T * 8; idx += 32)
 #pragma unroll
-                    for (int cb = 0; cb < CB; ++cb)
-                        *reinterpret_cast<uint4*>(smem + (sV(st) - base) + cb * BLK + idx * 16) = make_uint4(0, 0, 0, 0);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(vfix);
+                        for (int cb = 0; cb < CB; ++cb)
+                            *reinterpret_cast<uint4*>(smem + (sV(st) - base) + cb * BLK + idx * 16) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(vfix(st));
+                } else {
+                    ok = false;
+                }
             }
         }
+        // every issued copy lands before the CTA may leave
+        if (lane == 0)
+            for (int j = t > NS ? t - NS : 0; j < t; ++j) mbar_wait(isK ? fullK(j % NS) : fullV(j % NS), (j / NS) & 1u, A.err);
     } else if (warp == 4) {
-        // ---- MMA issuer: Q K^T of tile i+1 goes out before P V of tile i
+        // ---- MMA issuer: Q K^T of tile t+1 goes out before P V of tile t (within an item)
         if (lane == 0) {
             constexpr uint32_t IDS = idesc_bf16_f32(128, T), IDO = idesc_bf16_f32(128, HD, true);
             // the next 64 dims of V sit one block further; with a single block the field is never
             // used and holds the group stride, which keeps every address of the operand inside
             // its stage under either reading of the two fields
             constexpr uint32_t VBLK = CB > 1 ? BLK : 1024;
-            auto qk = [&](int i) -> bool {
-                const int st = i % SK;
-                if (!W(fullK(st), (i / SK) & 1u)) return false;
-                if (i >= 2 && !W(sfree(i & 1), ((i - 2) >> 1) & 1u)) return false;
+            auto qk = [&](int tt) -> bool {
+                const int st = tt % SK;
+                if (!W(fullK(st), (tt / SK) & 1u)) return false;
+                if (tt >= 2 && !W(sfree(tt & 1), ((tt - 2) >> 1) & 1u)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < HD / 16; ++ks) {
                     const uint64_t ad = sw128_kmajor_desc(sQ + (ks >> 2) * BLK + (ks & 3) * 32);
                     const uint64_t bd = sw128_kmajor_desc(sK(st) + (ks >> 2) * BLK + (ks & 3) * 32);
-                    tc_mma_bf16(tS + (i & 1) * T, ad, bd, IDS, ks > 0 ? 1u : 0u);
+                    tc_mma_bf16(tS + (tt & 1) * T, ad, bd, IDS, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(sbar(i & 1));
+                tc_commit(sbar(tt & 1));
                 tc_commit(emptyK(st));
                 return true;
             };
-            bool ok = qk(0);
-            for (int i = 0; ok && i < ntiles; ++i) {
-                if (i + 1 < ntiles && !qk(i + 1)) break;
-                const int sv = i % SV;
-                const bool fix = i == ntiles - 1 && p_begin + ntiles * T > maxlen;
-                if (!W(pready(i & 1), (i >> 1) & 1u) || !W(fix ? vfix : fullV(sv), fix ? 0u : (i / SV) & 1u)) break;
-                tc_fence_after();
+            int t = 0, jl = 0, nq = 0;
+            uint32_t fixpar = 0;   // bit st: parity of the next vfix phase of V stage st
+            int qb = -1, qg = -1, qrb = -1;
+            bool ok = true;
+            for (int it = first; ok && it < it1; ++it) {
+                const AttnItem I = attn_item(A, it, nrt);
+                if (!I.live) continue;
+                if (MULTI && jl > 0 && !same_q(I, qb, qg, qrb)) {
+                    if (!W(qfull, nq & 1u)) break;
+                    ++nq;
+                }
+                qb = I.b, qg = I.g, qrb = I.row_base;
+                if (!qk(t)) break;
+                for (int i = 0; i < I.ntiles; ++i) {
+                    const int tt = t + i, sv = tt % SV;
+                    if (i + 1 < I.ntiles && !qk(tt + 1)) { ok = false; break; }
+                    const bool fix = i == I.ntiles - 1 && I.p_begin + I.ntiles * T > I.maxlen;
+                    if (MULTI && i == 0 && jl > 0 && !W(ofree, (jl - 1) & 1u)) { ok = false; break; }
+                    if (!W(pready(tt & 1), (tt >> 1) & 1u) ||
+                        !W(fix ? vfix(sv) : fullV(sv), fix ? (fixpar >> sv) & 1u : (tt / SV) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (fix) fixpar ^= 1u << sv;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < T / 16; ++kk)   // 16 positions = two 8-row groups of the V tile
-                    tc_mma_bf16(tO, sw128_kmajor_desc(sP + (i & 1) * BLK + kk * 32),
-                                sw128_mnmajor_desc(sV(sv) + kk * 2048, VBLK, 1024), IDO, (i > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(pfree(i & 1));
-                tc_commit(emptyV(sv));
+                    for (int kk = 0; kk < T / 16; ++kk)   // 16 positions = two 8-row groups of the V tile
+                        tc_mma_bf16(tO, sw128_kmajor_desc(sP + (tt & 1) * BLK + kk * 32),
+                                    sw128_mnmajor_desc(sV(sv) + kk * 2048, VBLK, 1024), IDO, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(pfree(tt & 1));
+                    tc_commit(emptyV(sv));
+                }
+                t += I.ntiles;
+                ++jl;
             }
             tc_commit(done);   // every MMA issued is complete before the CTA may leave
             mbar_wait(done, 0u, A.err);
         }
     } else {
         // ---- softmax: thread = tile row rho (TMEM lane rho)
-        const int rho = tid, grow = row_base + rho;   // TMEM lane, row of the verify block
-        const int len = grow < rows ? L0 + grow / A.G : 0;
+        const int rho = tid;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        float m = NEG_INF, l = 0.f;
-        for (int i = 0; i < ntiles; ++i) {
-            if (!WW(sbar(i & 1), (i >> 1) & 1u)) break;
-            tc_fence_after();
-            float s[T];
-#pragma unroll
-            for (int c = 0; c < T / 16; ++c) tmem_ld16(tS + lane_off + (i & 1) * T + c * 16, s + c * 16);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(sfree(i & 1));
-            const int p0 = p_begin + i * T;
-            float mx = NEG_INF;
-#pragma unroll
-            for (int j = 0; j < T; ++j) {
-                s[j] = p0 + j < len ? __fmul_rn(s[j], A.sl2) : NEG_INF;
-                mx = fmaxf(mx, s[j]);
-            }
-            const float mn = (m == NEG_INF || mx > __fadd_rn(m, RESCALE_SLACK)) ? mx : m;
-            const bool dead = mn == NEG_INF;
-            const float al = (dead || mn == m) ? 1.f : ex2_approx(__fsub_rn(m, mn));
-            float ts = 0.f;
-            uint32_t pk[T / 2];
-#pragma unroll
-            for (int j = 0; j < T; j += 2) {
-                const float a0 = dead ? 0.f : ex2_approx(__fsub_rn(s[j], mn));
-                const float a1 = dead ? 0.f : ex2_approx(__fsub_rn(s[j + 1], mn));
-                ts = __fadd_rn(__fadd_rn(ts, a0), a1);
-                pk[j / 2] = pack_bf16x2(a0, a1);
-            }
-            l = __fadd_rn(__fmul_rn(l, al), ts);
-            m = mn;
-            // O is rescaled once P V of tile i-1 has completed (tcgen05.ld/st are warp-collective)
-            if (i >= 1 && __any_sync(0xffffffffu, al != 1.f)) {
-                if (!WW(pfree((i - 1) & 1), ((i - 1) >> 1) & 1u)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < HD / 64; ++c) {
-                    float o[64];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) o[e] = __fmul_rn(o[e], al);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tmem_st16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+        int t = 0, jl = 0;
+        int qb = -1, qg = -1, qrb = -1;
+        for (int it = first; it < it1; ++it) {
+            const AttnItem I = attn_item(A, it, nrt);
+            if (!I.live) continue;
+            if constexpr (MULTI) {
+                if (jl > 0 && !same_q(I, qb, qg, qrb)) {
+                    // the previous item's last P V has completed (its epilogue waited for it), and
+                    // with it every MMA that read the old Q; the MMA warp issues nothing until qfull
+                    load_q_tile<HD, BLK, 64>(smem + S::Q_OFF, A, I, rho);
+                    fence_proxy_async_smem();
+                    mbar_arrive(qfull);
                 }
-                tmem_st_wait();
             }
-            // P buffer i%2 was last read by P V of tile i-2
-            if (i >= 2 && !WW(pfree(i & 1), ((i - 2) >> 1) & 1u)) break;
+            qb = I.b, qg = I.g, qrb = I.row_base;
+            const int grow = I.row_base + rho;   // row of the verify block
+            const int len = grow < rows ? I.L0 + grow / A.G : 0;
+            float m = NEG_INF, l = 0.f;
+            bool ok = true;
+            for (int i = 0; i < I.ntiles; ++i) {
+                const int tt = t + i;
+                if (!WW(sbar(tt & 1), (tt >> 1) & 1u)) { ok = false; break; }
+                tc_fence_after();
+                float s[T];
 #pragma unroll
-            for (int c = 0; c < T / 8; ++c)
-                *reinterpret_cast<uint4*>(smem + S::P_OFF + (i & 1) * BLK + rho * 128 + ((c ^ (rho & 7)) * 16)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(pready(i & 1));
-        }
-        // ---- epilogue: O after the last tile's P V
-        if (WW(pfree((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1u)) {
+                for (int c = 0; c < T / 16; ++c) tmem_ld16(tS + lane_off + (tt & 1) * T + c * 16, s + c * 16);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(sfree(tt & 1));
+                const int p0 = I.p_begin + i * T;
+                float mx = NEG_INF;
+#pragma unroll
+                for (int j = 0; j < T; ++j) {
+                    s[j] = p0 + j < len ? __fmul_rn(s[j], A.sl2) : NEG_INF;
+                    mx = fmaxf(mx, s[j]);
+                }
+                const float mn = (m == NEG_INF || mx > __fadd_rn(m, RESCALE_SLACK)) ? mx : m;
+                const bool dead = mn == NEG_INF;
+                const float al = (dead || mn == m) ? 1.f : ex2_approx(__fsub_rn(m, mn));
+                float ts = 0.f;
+                uint32_t pk[T / 2];
+#pragma unroll
+                for (int j = 0; j < T; j += 2) {
+                    const float a0 = dead ? 0.f : ex2_approx(__fsub_rn(s[j], mn));
+                    const float a1 = dead ? 0.f : ex2_approx(__fsub_rn(s[j + 1], mn));
+                    ts = __fadd_rn(__fadd_rn(ts, a0), a1);
+                    pk[j / 2] = pack_bf16x2(a0, a1);
+                }
+                l = __fadd_rn(__fmul_rn(l, al), ts);
+                m = mn;
+                // O is rescaled once P V of tile tt-1 has completed (tcgen05.ld/st are warp-collective)
+                if (i >= 1 && __any_sync(0xffffffffu, al != 1.f)) {
+                    if (!WW(pfree((tt - 1) & 1), ((tt - 1) >> 1) & 1u)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < HD / 64; ++c) {
+                        float o[64];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) o[e] = __fmul_rn(o[e], al);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) tmem_st16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+                    }
+                    tmem_st_wait();
+                }
+                // P buffer tt%2 was last read by P V of tile tt-2
+                if (tt >= 2 && !WW(pfree(tt & 1), ((tt - 2) >> 1) & 1u)) { ok = false; break; }
+#pragma unroll
+                for (int c = 0; c < T / 8; ++c)
+                    *reinterpret_cast<uint4*>(smem + S::P_OFF + (tt & 1) * BLK + rho * 128 + ((c ^ (rho & 7)) * 16)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(pready(tt & 1));
+            }
+            if (!ok) break;
+            // ---- epilogue: O after the item's last P V
+            const int tl = t + I.ntiles - 1;
+            if (!WW(pfree(tl & 1), (tl >> 1) & 1u)) break;
             tc_fence_after();
             // tcgen05.ld is warp-collective: every lane loads, the live rows store
-            const bool live = grow < rows && len > p_begin;
-            const int r = grow / A.G, h = g * A.G + grow % A.G;
-            const long long idx = ((static_cast<long long>(b) * A.R + r) * A.Hq + h) * A.nsplit + split;
+            const bool live = grow < rows && len > I.p_begin;
+            const int r = grow / A.G, h = I.g * A.G + grow % A.G;
+            const long long idx = ((static_cast<long long>(I.b) * A.R + r) * A.Hq + h) * A.nsplit + I.split;
             float* op = A.opart + idx * HD;
 #pragma unroll 1
             for (int c = 0; c < HD / 64; ++c) {
@@ -384,6 +491,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                 }
             }
             if (live) A.ml[idx] = make_float2(m, l);
+            if constexpr (MULTI) {
+                tc_fence_before();
+                mbar_arrive(ofree);   // O may be overwritten by the next item's first P V
+            }
+            t += I.ntiles;
+            ++jl;
         }
     }
     tc_fence_before();
@@ -550,19 +663,34 @@ template <int HD>
 xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int B, cudaStream_t s) {
     using S = AttnShape<HD>;
     static bool attr_done[64] = {};
+    static int sms[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "attn: device ordinal out of range");
     if (!attr_done[dev]) {
-        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                           S::SMEM),
+        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD, true>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM),
                                       "attn: set shared memory size"))
+            return st;
+        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD, false>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM),
+                                      "attn: set shared memory size"))
+            return st;
+        if (xv_status st = cuda_check(cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev),
+                                      "attn: SM count"))
             return st;
         attr_done[dev] = true;
     }
-    dim3 grid(a.nsplit * ((a.R * a.G + 63) / 64), a.Hkv, B);
+    // past two waves of items, one persistent CTA per SM (the shared-memory plan admits one);
+    // otherwise one CTA per item (measured in the verify step: with 160 items the persistent
+    // launch was 4 us slower, with 1028 and 8224 items 15 and 218 us faster)
+    const long long n_items = static_cast<long long>(a.nsplit) * ((a.R * a.G + 63) / 64) * a.Hkv * B;
+    if (n_items > (1ll << 30)) return fail(XV_ERR_UNSUPPORTED, "attn: %lld work items", n_items);
+    const bool multi = n_items > 2ll * sms[dev];
+    dim3 grid(static_cast<unsigned>(multi ? sms[dev] : n_items));
     trace_pre(s);
-    launch_k(attn_split_kernel<HD>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
+    if (multi) launch_k(attn_split_kernel<HD, true>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
+    else launch_k(attn_split_kernel<HD, false>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
     // bound: every sequence at the longest length the launch is sized for
     const long long bytes = 4ll * B * a.Hkv * a.max_len * HD + 2ll * B * a.R * a.Hq * HD +
                             4ll * B * a.R * a.Hq * a.nsplit * (HD + 2);
@@ -596,7 +724,7 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
     const size_t rows = static_cast<size_t>(B) * R * Hq * nsplit;
     float* opart = static_cast<float*>(ws);
     float2* ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + round256(rows * hd * sizeof(float)));
-    AttnArgs a{q, q_stride, kv, ctx_len, len_bias, R, Hq / Hkv, Hq, Hkv, nsplit, max_len,
+    AttnArgs a{q, q_stride, kv, ctx_len, len_bias, R, Hq / Hkv, Hq, Hkv, nsplit, max_len, B,
                scale * 1.4426950408889634f, opart, ml, err};
     xv_status st = hd == 256 ? launch_split<256>(tmK, tmV, a, B, s) : launch_split<64>(tmK, tmV, a, B, s);
     if (st) return st;
