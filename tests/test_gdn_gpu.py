@@ -168,7 +168,7 @@ def test_replay_then_speculate_matches_decode(xv, K, keep):
         xv.xv_gdn_decode_step(Sd, st, ob, H * DV, B, H, DK, DV, False)
         outs.append(ob)
     ref = torch.stack(outs[keep:], dim=1)
-    # verify: pending = round 1 rows (rows_per_seq 16 from row 0), draft = round 2 rows (from row 8)
+    # verify: pending = round 1 rows (rows_per_seq 2K from row 0), draft = round 2 rows (from row K)
     Sv = S0.clone()
     pend = steps(xv, qkv, gates, 2 * K)
     draft = steps(xv, qkv, gates, 2 * K, row0=K)
