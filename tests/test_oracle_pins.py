@@ -276,6 +276,31 @@ def test_gdn_matches_error_correcting_form():
         np.testing.assert_allclose(o, ref @ q, rtol=1e-12, atol=1e-12)
 
 
+def test_gdn_fp32_evaluation_sizes_the_state_tolerance():
+    """The same 16 steps evaluated in fp32 (numpy float32, the order S <- a S; r = S k;
+    u = b (v - r); S <- S + u k^T) stay within 1e-5 of the fp64 oracle in the state's relative
+    measure max|dS| / max(|S|, rms S): the 1e-4 bound on the GPU's fp32 state has a factor of ten
+    of room for reduction order alone."""
+    rng = np.random.default_rng(18)
+    dk = dv = 128
+    S64 = rng.normal(size=(dv, dk)) * 0.1
+    S32 = S64.astype(np.float32)
+    for _ in range(16):
+        q, k = rng.normal(size=dk), rng.normal(size=dk)
+        q, k = q / np.linalg.norm(q), k / np.linalg.norm(k)
+        v = rng.normal(size=dv)
+        b, a = 1 / (1 + np.exp(-rng.normal())), np.exp(-np.log1p(np.exp(rng.normal())))
+        oracle.gdn_step(S64, q, k, v, b, a)
+        f = np.float32
+        S32 = S32 * f(a)
+        r = S32 @ k.astype(f)
+        u = f(b) * (v.astype(f) - r)
+        S32 = S32 + np.outer(u, k.astype(f))
+    err = np.abs(S32.astype(np.float64) - S64)
+    floor = np.sqrt(np.mean(S64 * S64))
+    assert np.max(err / np.maximum(np.abs(S64), floor)) < 1e-5
+
+
 def test_gdn_heads_bf16_path_normalises_and_rounds():
     rng = np.random.default_rng(11)
     H, dk, dv = 3, 4, 5
@@ -344,6 +369,31 @@ def test_attn_rows_gqa_mapping_and_causal_rows():
             s = oracle.bf16_to_f64(kc[g, :len0 + r]) @ oracle.bf16_to_f64(q[r, h]) * 0.35
             ref = sp.softmax(s) @ oracle.bf16_to_f64(vc[g, :len0 + r])
             assert np.max(np.abs(out[r, h] - ref)) <= 2.0 ** -8 * np.max(np.abs(ref))
+
+
+def test_attn_split_combine_identity():
+    """Softmax attention over any partition of the positions: per part the local max m_p, sum l_p
+    and unnormalised output o_p, merged with weights exp(m_p - M), equals the explicit softmax of
+    the oracle to 1e-12 (the identity the split kernels rest on), for the fixed 512-position
+    splits and for random cuts."""
+    rng = np.random.default_rng(17)
+    hd, n = 16, 1300
+    q, K, V = bf(rng.normal(size=hd)), bf(rng.normal(size=(n, hd))), bf(rng.normal(size=(n, hd)))
+    scale = 0.3
+    ref = oracle.attn_row(q, K, V, n, scale)
+    s = oracle.bf16_to_f64(K) @ oracle.bf16_to_f64(q) * scale
+    Vf = oracle.bf16_to_f64(V)
+    cuts_list = [list(range(0, n, 512)) + [n], [0] + sorted(rng.choice(np.arange(1, n), 9, replace=False).tolist()) + [n]]
+    for cuts in cuts_list:
+        parts = []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            m = s[a:b].max()
+            w = np.exp(s[a:b] - m)
+            parts.append((m, w.sum(), w @ Vf[a:b]))
+        M = max(p[0] for p in parts)
+        L = sum(np.exp(m - M) * l for m, l, _ in parts)
+        O = sum(np.exp(m - M) * o for m, _, o in parts)
+        np.testing.assert_allclose(O / L, ref, rtol=1e-12, atol=1e-14)
 
 
 # ------------------------------------------------------- argmax / accept
