@@ -78,8 +78,9 @@ struct AttnShape {
     static constexpr int K_OFF = P_OFF + 2 * BLK;
     static constexpr int V_OFF = K_OFF + SK * TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + SV * TILE_BYTES;
-    // fullK, emptyK, fullV, emptyV, vfix, sbar[2], sfree[2], pready[2], pfree[2], done, ofree, qfull
-    static constexpr int N_BARS = 2 * SK + 3 * SV + 11;
+    // fullK, emptyK, fullV, emptyV, vfix, sbar[2], sfree[2], pready[2], pfree[2], done, ofree, qfull,
+    // mlready
+    static constexpr int N_BARS = 2 * SK + 3 * SV + 12;
     static constexpr int SMEM = 1024 + BAR_OFF + 8 * N_BARS;
     static constexpr uint32_t TMEM_COLS = HD == 256 ? 512 : 256;   // S[2] (64 columns each) + O (HD)
 };
@@ -97,7 +98,8 @@ struct AttnArgs {
     unsigned* err;
 };
 
-constexpr int ATTN_THREADS = 160;   // warps 0-1 softmax, 2 K loads, 3 V loads, 4 MMA
+// warps 0-1 softmax, 2 K loads, 3 V loads, 4-5 epilogue (tensor-memory lanes 0-63, as 0-1), 6 MMA
+constexpr int ATTN_THREADS = 224;
 constexpr float RESCALE_SLACK = 2.f;
 
 // A unit of work: (split, 64-row tile, kv head, sequence), numbered with the split fastest so
@@ -165,9 +167,13 @@ __device__ __forceinline__ void load_q_tile(uint8_t* sq, const AttnArgs& A, cons
 //              exp2(m_old - m_new); P = bf16(exp2(s - m)) into shared memory, l += its fp32
 //              values in position order (exp2 by the hardware approximation)
 //   MMA warp   O += P V_t (N = HD; V straight from its TMA stage as an MN-major operand)
+//   epilogue   two warps on the softmax warps' tensor-memory lanes: once the item's last P V has
+//              completed and the softmax warps have left the item's m and l in shared memory
+//              (mlready), O is read out and written as the item's partials; meanwhile the softmax
+//              warps are already on the next item's first S
 // t counts the CTA's tiles across its items, so the K/V rings, the two S buffers and the two P
 // buffers keep cycling from one item to the next; an item's first P V overwrites O once the
-// softmax warps have read the previous item's O out (ofree), and Q is reloaded (qfull) only when
+// epilogue warps have read the previous item's O out (ofree), and Q is reloaded (qfull) only when
 // the item's (sequence, kv head, row tile) changes.  A row's operations depend on its own length
 // and the absolute tile positions only, so a verify row gets the bits of the decode row at its
 // position, whichever CTA and whichever neighbours it has.  MULTI = false is the launch with one
@@ -181,6 +187,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_abort;
+    __shared__ float2 ml_sm[64];   // (m, l) of each row of the item being written out
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw);
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     // P V of tile k only ever happens once that of tile k - 2 is known complete, so the barrier is
     // never two phases away from the one waited for
     auto pfree = [&](int j) { return bx + 8u * (6 + j); };
-    const uint32_t done = bx + 8u * 8, ofree = bx + 8u * 9, qfull = bx + 8u * 10;
+    const uint32_t done = bx + 8u * 8, ofree = bx + 8u * 9, qfull = bx + 8u * 10, mlready = bx + 8u * 11;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = A.R * A.G, nrt = (rows + 63) / 64;
@@ -242,6 +249,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         mbar_init(done, 1);
         mbar_init(ofree, 64);
         mbar_init(qfull, 64);
+        mbar_init(mlready, 64);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         // every issued copy lands before the CTA may leave
         if (lane == 0)
             for (int j = t > NS ? t - NS : 0; j < t; ++j) mbar_wait(isK ? fullK(j % NS) : fullV(j % NS), (j / NS) & 1u, A.err);
-    } else if (warp == 4) {
+    } else if (warp == 6) {
         // ---- MMA issuer: Q K^T of tile t+1 goes out before P V of tile t (within an item)
         if (lane == 0) {
             constexpr uint32_t IDS = idesc_bf16_f32(128, T), IDO = idesc_bf16_f32(128, HD, true);
@@ -387,6 +395,44 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             tc_commit(done);   // every MMA issued is complete before the CTA may leave
             mbar_wait(done, 0u, A.err);
         }
+    } else if (warp >= 4) {
+        // ---- epilogue: thread = tile row rho (TMEM lane rho, the lanes of warps 0-1)
+        const int rho = tid - 128;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        int t = 0, jl = 0;
+        for (int it = first; it < it1; ++it) {
+            const AttnItem I = attn_item(A, it, nrt);
+            if (!I.live) continue;
+            const int tl = t + I.ntiles - 1;
+            // m and l of the item (the softmax warps are done with it), then its last P V
+            if (!WW(mlready, jl & 1u) || !WW(pfree(tl & 1), (tl >> 1) & 1u)) break;
+            tc_fence_after();
+            const int grow = I.row_base + rho;
+            const int len = grow < rows ? I.L0 + grow / A.G : 0;
+            // tcgen05.ld is warp-collective: every lane loads, the live rows store
+            const bool live = grow < rows && len > I.p_begin;
+            const int r = grow / A.G, h = I.g * A.G + grow % A.G;
+            const long long idx = ((static_cast<long long>(I.b) * A.R + r) * A.Hq + h) * A.nsplit + I.split;
+            float* op = A.opart + idx * HD;
+            const float2 ml = ml_sm[rho];
+#pragma unroll 1
+            for (int c = 0; c < HD / 64; ++c) {
+                float o[64];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
+                tmem_ld_wait();
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < 64; e += 4)
+                        *reinterpret_cast<float4*>(op + c * 64 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                }
+            }
+            if (live) A.ml[idx] = ml;
+            tc_fence_before();
+            mbar_arrive(ofree);   // O (and ml_sm) may be overwritten by the next item
+            t += I.ntiles;
+            ++jl;
+        }
     } else {
         // ---- softmax: thread = tile row rho (TMEM lane rho)
         const int rho = tid;
@@ -398,8 +444,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             if (!I.live) continue;
             if constexpr (MULTI) {
                 if (jl > 0 && !same_q(I, qb, qg, qrb)) {
-                    // the previous item's last P V has completed (its epilogue waited for it), and
-                    // with it every MMA that read the old Q; the MMA warp issues nothing until qfull
+                    // every Q K^T that read the old Q has completed (this warp has seen the S of
+                    // the previous item's last tile; P V does not read Q), and the MMA warp issues
+                    // nothing for this item until qfull
                     load_q_tile<HD, BLK, 64>(smem + S::Q_OFF, A, I, rho);
                     fence_proxy_async_smem();
                     mbar_arrive(qfull);
@@ -469,32 +516,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                 mbar_arrive(pready(tt & 1));
             }
             if (!ok) break;
-            // ---- epilogue: O after the item's last P V
-            const int tl = t + I.ntiles - 1;
-            if (!WW(pfree(tl & 1), (tl >> 1) & 1u)) break;
-            tc_fence_after();
-            // tcgen05.ld is warp-collective: every lane loads, the live rows store
-            const bool live = grow < rows && len > I.p_begin;
-            const int r = grow / A.G, h = I.g * A.G + grow % A.G;
-            const long long idx = ((static_cast<long long>(I.b) * A.R + r) * A.Hq + h) * A.nsplit + I.split;
-            float* op = A.opart + idx * HD;
-#pragma unroll 1
-            for (int c = 0; c < HD / 64; ++c) {
-                float o[64];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
-                tmem_ld_wait();
-                if (live) {
-#pragma unroll
-                    for (int e = 0; e < 64; e += 4)
-                        *reinterpret_cast<float4*>(op + c * 64 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                }
-            }
-            if (live) A.ml[idx] = make_float2(m, l);
-            if constexpr (MULTI) {
-                tc_fence_before();
-                mbar_arrive(ofree);   // O may be overwritten by the next item's first P V
-            }
+            // hand m and l to the epilogue warps (once they are done with the previous item's)
+            if (MULTI && jl > 0 && !WW(ofree, (jl - 1) & 1u)) break;
+            ml_sm[rho] = make_float2(m, l);
+            mbar_arrive(mlready);
             t += I.ntiles;
             ++jl;
         }
