@@ -19,16 +19,19 @@
 // touches another row's data: each output element of a tensor-core product
 // is the dot product of its own row and column.
 //
-// Kernel 1 (attn_split_kernel), one CTA per (split, 64-row tile, kv head, sequence):
-// K and V tiles arrive by TMA (3-D tensor map over [pages*Hkv, page, hd], 128-byte
+// Kernel 1 (attn_split_kernel), work items (split, 64-row tile, kv head, sequence):
+// one CTA per item up to two waves of them, else one persistent CTA per SM
+// walking a contiguous range of items.  K and V tiles arrive by TMA (3-D tensor map over [pages*Hkv, page, hd], 128-byte
 // swizzle; a contiguous cache is one page of Lmax positions per sequence, a
 // paged one pages of a multiple of 64 positions, so a tile never straddles two
 // pages and the page a tile comes from changes nothing in its arithmetic)
 // into a shared-memory ring; QK^T and PV run on tcgen05 (fp32 accumulators in
 // tensor memory, bf16 operands in shared memory, P rounded to bf16); the
-// softmax is one thread per query row, reading its S row from tensor memory.
+// softmax is one thread per query row, reading its S row from tensor memory;
+// two epilogue warps read O out.
 // Kernel 2 (attn_combine_kernel), one CTA per (row, q head): fixed-order
-// split combine, normalisation, optional output gate, bf16 store.
+// split combine (the split partials streamed through shared memory),
+// normalisation, optional output gate, bf16 store.
 #include <cmath>
 
 #include "xv_internal.h"
