@@ -147,3 +147,36 @@ def test_block_state_layout(xv):
     names = [f[0] for f in xv.BlockState._fields_]
     assert names[-2:] == ["kv_pages", "last_k_seq"]
     assert ctypes.sizeof(xv.KvPages) == 8 + 3 * 4 + 4     # pointer, three ints, tail padding
+
+
+def _fake_state(xv, B, kmax, Lmax, n_layers=4):
+    """A block state whose pointers are aligned but point nowhere: for host validation only."""
+    p = 0x10000
+    layers = (xv.LayerState * n_layers)()
+    for ls in layers:
+        ls.gdn_state, ls.k_cache, ls.v_cache = p, p, p
+        ls.gdn_hist[0], ls.gdn_hist[1] = p, p
+    st = xv.BlockState(B, kmax, Lmax, p, p, 0, kmax, 0, 0, ctypes.cast(layers, ctypes.c_void_p).value)
+    return st, layers
+
+
+def test_prefill_limits_without_gpu(xv):
+    """Chunks beyond kmax, or beyond 64 GEMM rows over the batch, are refused before any launch."""
+    L = xv.lib()
+    c, keep = _cfg(xv)
+    w = xv.BlockWeights()
+    st, layers = _fake_state(xv, 2, xv.XV_KMAX, 4096)
+    p = ctypes.c_void_p(0x10000)
+    call = lambda T, chunk: L.xv_block_prefill(ctypes.byref(c), ctypes.byref(w), ctypes.byref(st), p, T, chunk, None,
+                                               None, p, 1 << 30, None)
+    assert call(100, xv.XV_KMAX + 1) == xv.XV_ERR_ARG             # chunk > kmax
+    assert call(100, 0) == xv.XV_ERR_ARG
+    assert call(0, 8) == xv.XV_ERR_ARG                            # no tokens
+    assert call(100, 33) == xv.XV_ERR_UNSUPPORTED                 # 2 x 33 rows > 64
+    st.last_k = 4
+    assert call(100, 8) == xv.XV_ERR_ARG                          # an uncommitted verify
+    st.last_k, st.max_ctx = 0, 4000
+    assert call(100, 8) == xv.XV_ERR_ARG                          # max_ctx + T > Lmax
+    big, layers2 = _fake_state(xv, 1, xv.XV_KMAX + 1, 4096)
+    assert L.xv_block_prefill(ctypes.byref(c), ctypes.byref(w), ctypes.byref(big), p, 100, 8, None, None, p, 1 << 30,
+                              None) == xv.XV_ERR_ARG              # kmax beyond XV_KMAX
