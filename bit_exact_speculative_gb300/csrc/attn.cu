@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             int t = 0, jl = 0, nq = 0;
             uint32_t fixpar = 0;   // bit st: parity of the next vfix phase of V stage st
             int qb = -1, qg = -1, qrb = -1;
-            bool ok = true;
+            bool ok = true, pre = false;   // pre: this item's first Q K^T went out with the last item
             for (int it = first; ok && it < it1; ++it) {
                 const AttnItem I = attn_item(A, it, nrt);
                 if (!I.live) continue;
@@ -372,10 +372,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                     ++nq;
                 }
                 qb = I.b, qg = I.g, qrb = I.row_base;
-                if (!qk(t)) break;
+                if (!pre && !qk(t)) break;
+                pre = false;
+                // the next live item: with the same Q its first Q K^T goes out before this item's
+                // last P V, so its S is ready when the softmax warps come to it
+                bool next_same = false;
+                if (MULTI) {
+                    int nx = it + 1;
+                    while (nx < it1 && !attn_item(A, nx, nrt).live) ++nx;
+                    next_same = nx < it1 && same_q(attn_item(A, nx, nrt), I.b, I.g, I.row_base);
+                }
                 for (int i = 0; i < I.ntiles; ++i) {
                     const int tt = t + i, sv = tt % SV;
-                    if (i + 1 < I.ntiles && !qk(tt + 1)) { ok = false; break; }
+                    if ((i + 1 < I.ntiles || next_same) && !qk(tt + 1)) { ok = false; break; }
+                    if (i + 1 == I.ntiles && next_same) pre = true;
                     const bool fix = i == I.ntiles - 1 && I.p_begin + I.ntiles * T > I.maxlen;
                     if (MULTI && i == 0 && jl > 0 && !W(ofree, (jl - 1) & 1u)) { ok = false; break; }
                     if (!W(pready(tt & 1), (tt >> 1) & 1u) ||
