@@ -332,8 +332,12 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     const int max_steps = max_commit + k;
     if (max_steps > THREADS) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS);
     dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
-    static bool carve[2] = {false, false};
-    if (!carve[dk == 128]) {
+    // function attributes are per device: set once on each
+    static bool carve[64][2] = {};
+    int dev = 0;
+    if (xv_status st = cuda_check(cudaGetDevice(&dev), "gdn: cudaGetDevice")) return st;
+    if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "gdn: device ordinal %d out of range", dev);
+    if (!carve[dev][dk == 128]) {
         // as much shared memory as possible for the carveout: several CTAs per SM at B = 8; up to
         // THREADS staged steps (a prefill chunk of XV_KMAX positions after as many pending ones)
         xv_status st;
@@ -349,7 +353,7 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
                             "gdn: set shared memory size");
         }
         if (st) return st;
-        carve[dk == 128] = true;
+        carve[dev][dk == 128] = true;
     }
     trace_pre(s);
     if (dk == 128) {
