@@ -94,11 +94,12 @@ def test_verify_rows_equal_decode_rows(xv, L):
             assert_bf16_close(o[r, h], ref, what=f"L{L} r{r} h{h}")
 
 
-@pytest.mark.parametrize("R,L", [(16, 2183), (64, 480), (64, 4050)])
+@pytest.mark.parametrize("R,L", [(16, 2183), (64, 480), (64, 4050), (16, 131072)])
 def test_row_tiles_equal_decode_rows(xv, R, L):
-    """Past 64 rows per kv head (R x 6 q heads) the rows go in tiles of 64, one CTA each per split;
-    every row still equals an R=1 call at its own length, also where the rows cross a split
-    boundary (480 + 63, 4050 + 63), and the oracle (GQA 24/4, hd 256)."""
+    """Past 64 rows per kv head (R x 6 q heads) the rows go in tiles of 64, one work item each per
+    split; every row still equals an R=1 call at its own length, also where the rows cross a split
+    boundary (480 + 63, 4050 + 63), and with persistent CTAs that reload Q between row tiles
+    (131072: 2056 items), and the oracle (GQA 24/4, hd 256)."""
     B, Hq, Hkv, hd = 1, 24, 4, 256
     Lmax = L + R
     q, kc, vc = make(7, B, R, Hq, Hkv, hd, Lmax, name=f"tiles{R}.{L}")
