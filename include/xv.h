@@ -218,14 +218,21 @@ xv_status xv_gdn_verify_grouped(float* state, const xv_gdn_steps* pending, const
  * the window being the Kc-1 prior inputs then x (tap Kc-1 meets the newest).
  * The k rows do not enter the state: the caller passes them as the next
  * call's pending rows (deferred commit, as for the recurrence).  Strides are
- * in elements; w is [C, Kc] bf16. */
+ * in elements; w is [C, Kc] bf16.  k = 0 with max_commit > 0 is a pure commit.
+ * Errors: XV_ERR_ARG (null state or taps, B outside [1, 65535], C < 1, pending
+ * rows or x rows fewer than max_commit or k, strides below C),
+ * XV_ERR_UNSUPPORTED (Kc outside [2, XV_CONV_MAX], k or max_commit outside
+ * [0, XV_KMAX]), XV_ERR_CUDA (launch).  A count n_commit[b] out of range is
+ * clamped on the device and reported by xv_device_check. */
 xv_status xv_gdn_conv(uint16_t* state, const uint16_t* pend, long long pend_stride, int pend_rows,
                       const int32_t* n_commit, int max_commit, const uint16_t* x, long long x_stride, int x_rows,
                       int k, const uint16_t* w, int C, int Kc, int B, uint16_t* y, long long y_stride, xv_stream s);
 
 /* Gated output norm over M rows of H heads of dv values (dv a multiple of 32
  * up to 256): y = bf16( o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z) ), w
- * [dv]; y may be o. */
+ * [dv]; y may be o.  Rows are o_stride / z_stride / y_stride elements apart.
+ * Errors: XV_ERR_ARG (null pointer, M or H < 1, a stride below H*dv),
+ * XV_ERR_UNSUPPORTED (dv, or M*H above 2^30), XV_ERR_CUDA (launch). */
 xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z, long long z_stride,
                         const uint16_t* w, int M, int H, int dv, float eps, uint16_t* y, long long y_stride,
                         xv_stream s);
