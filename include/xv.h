@@ -176,7 +176,15 @@ typedef struct {
 
 /* One decode step for B sequences: state [B, H, dv, dk] fp32 is updated in
  * place, o [B, H, dv] bf16 (row b at b*o_stride) receives o_t.
- * dk in {64, 128}; dv a multiple of 32; 1 <= B, 1 <= H. */
+ * dk in {64, 128}; dv a multiple of 32; 1 <= B, 1 <= H.
+ * Errors (for this and the two verify calls below): XV_ERR_ARG (null state,
+ * o or step pointers, B or H < 1, rows_per_seq < 1 or fewer rows than the
+ * steps used, gate_stride < H, o_stride < H*dv, n_commit missing with
+ * max_commit > 0, H not a multiple of Hk); XV_ERR_UNSUPPORTED (dk, dv, B or H
+ * above 65535, q/k/v not 16-byte aligned or qkv_stride not a multiple of 8,
+ * k or max_commit outside [0, XV_KMAX]); XV_ERR_CUDA (launch).  A count
+ * n_commit[b] outside [0, max_commit] is clamped on the device and reported
+ * by xv_device_check. */
 xv_status xv_gdn_decode_step(float* state, const xv_gdn_steps* step, uint16_t* o, long long o_stride,
                              int B, int H, int dk, int dv, int qk_l2norm, xv_stream s);
 
@@ -259,7 +267,14 @@ xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z
  *         attention layer's output gate), else out = bf16(attn)
  *   hd = 256 or 64 (hd % 64 == 0), Hq % Hkv == 0, 1 <= R <= XV_KMAX (the R*(Hq/Hkv) rows of a
  *         kv head go in tiles of 64 rows, one CTA each per split)
- * Workspace: xv_attn_workspace_size(B, R, Hq, hd, max_ctx) bytes, 16-byte aligned. */
+ * Workspace: xv_attn_workspace_size(B, R, Hq, hd, max_ctx) bytes, 16-byte aligned (0 is returned
+ * for sizes below 1).
+ * Errors: XV_ERR_ARG (null pointer, sizes < 1, Hq not a multiple of Hkv,
+ * max_ctx outside [R, Lmax], row strides below Hq*hd), XV_ERR_UNSUPPORTED (hd,
+ * R > XV_KMAX, B or Hkv above 65535, B*Hkv*Lmax above 2^31, unaligned q rows,
+ * caches or workspace), XV_ERR_WORKSPACE (missing or small workspace),
+ * XV_ERR_CUDA (launch).  A sequence whose ctx_len[b] + R - 1 falls outside
+ * [1, max_ctx] is skipped on the device and reported by xv_device_check. */
 int xv_attn_split_size(void);
 size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx);
 xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
@@ -269,7 +284,12 @@ xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint1
 
 /* Writes the K and V rows of a verify block into the caches: row (b, r) of
  * kv_src (k at column offset 0, v at column offset Hkv*hd, row stride
- * src_stride) goes to position ctx_len[b] - 1 + r of sequence b. */
+ * src_stride) goes to position ctx_len[b] - 1 + r of sequence b.
+ * Errors: XV_ERR_ARG (null pointer, sizes < 1, hd not a multiple of 8,
+ * src_stride < 2*Hkv*hd), XV_ERR_UNSUPPORTED (kv_src, kc, vc not 16-byte
+ * aligned or src_stride not a multiple of 8), XV_ERR_CUDA (launch).  A
+ * position outside [0, Lmax) is skipped on the device and reported by
+ * xv_device_check. */
 xv_status xv_kv_append(const uint16_t* kv_src, long long src_stride, const int32_t* ctx_len, int R, int B,
                        int Hkv, int hd, int Lmax, uint16_t* kc, uint16_t* vc, xv_stream s);
 
@@ -389,7 +409,8 @@ int xv_attn_in_dim(const xv_block_config* cfg);
 int xv_gdn_conv_dim(const xv_block_config* cfg);
 int xv_gdn_conv_stride(const xv_block_config* cfg);
 
-/* Workspace for xv_verify_block with B sequences of up to kmax tokens. */
+/* Workspace for xv_verify_block with B sequences of up to kmax tokens (0 for an invalid
+ * configuration or sizes below 1). */
 size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);
 
 /* tokens [B, k] int32 device; logits [B*k, V] fp32 device or NULL; argmax
@@ -397,7 +418,14 @@ size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int 
  * position before them (0..k-1).  Requires 1 <= k <= st->kmax, B == st->B,
  * B*k <= XV_GEMM_M_MAX, st->max_ctx + k <= Lmax.  Appends the k rows to the KV
  * caches (uncommitted), replays the pending GDN steps into the states and
- * records this call's GDN inputs as the next pending steps. */
+ * records this call's GDN inputs as the next pending steps.
+ * Errors: XV_ERR_ARG (invalid configuration, incomplete weights or state, null
+ * tokens/argmax/n_accept, k outside [1, kmax], the previous verify not yet
+ * committed, st->max_ctx + k > Lmax, pending_rows out of range),
+ * XV_ERR_UNSUPPORTED (B*k > XV_GEMM_M_MAX, unaligned buffers, shapes the
+ * kernels do not take), XV_ERR_WORKSPACE, XV_ERR_CUDA.  Nothing is enqueued
+ * when a host check fails; token ids or lengths found out of range on the
+ * device are clamped and reported by xv_device_check. */
 xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
                           const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept,
                           void* ws, size_t ws_bytes, xv_stream s);
@@ -418,7 +446,9 @@ xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weig
 /* Commit n_keep[b] (device, 1..k) positions of the last verify: ctx_len += n_keep,
  * n_commit = n_keep; flips the history parity and advances max_ctx by the k of
  * that verify.  [post]: the result must also be exact with every draft forced
- * to reject (n_keep = 1). */
+ * to reject (n_keep = 1).  Errors: XV_ERR_ARG (null state or counts, no
+ * uncommitted verify), XV_ERR_CUDA; a count outside 1..k is clamped on the
+ * device and reported by xv_device_check. */
 xv_status xv_block_commit(xv_block_state* st, const int32_t* n_keep, xv_stream s);
 
 /* Standard commit: n_keep = n_accept + 1 (device arrays). */
@@ -426,7 +456,8 @@ xv_status xv_block_commit_accepted(xv_block_state* st, const int32_t* n_accept, 
 
 /* Replays the pending GDN steps of every GDN layer into its state (k = 0
  * verify per layer) and zeroes n_commit, so the states hold the committed
- * position.  Needs the same cfg as the verify calls. */
+ * position.  Needs the same cfg as the verify calls.  Errors: XV_ERR_ARG
+ * (invalid configuration or state, an uncommitted verify), XV_ERR_CUDA. */
 xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stream s);
 
 /* Exact chunked prefill.  Feeds tokens [B, T] (int32 device, row b = the
@@ -442,8 +473,13 @@ xv_status xv_block_flush(const xv_block_config* cfg, xv_block_state* st, xv_stre
  * prompt token; only the last chunk runs the LM head.  1 <= chunk <= st->kmax,
  * B*chunk <= XV_GEMM_M_MAX (so a prefill of one sequence takes chunks of up to 64
  * tokens); the last verify must have been committed; st->max_ctx + T <= Lmax.
- * Workspace:
- * xv_block_prefill_workspace_size(cfg, B, kmax, Lmax). */
+ * Workspace: xv_block_prefill_workspace_size(cfg, B, kmax, Lmax) (0 for an
+ * invalid configuration).  Errors: XV_ERR_ARG (null tokens, T < 1, chunk
+ * outside [1, kmax], an uncommitted verify, st->max_ctx + T > Lmax, and every
+ * error of xv_verify_block), XV_ERR_UNSUPPORTED (B*chunk > XV_GEMM_M_MAX),
+ * XV_ERR_WORKSPACE, XV_ERR_CUDA.  The limits are checked before anything is
+ * enqueued; a failure inside a later chunk leaves the chunks before it
+ * committed. */
 size_t xv_block_prefill_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);
 xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
                            const int32_t* tokens, int T, int chunk, float* last_logits, int32_t* last_argmax,
