@@ -21,6 +21,7 @@ c_int, c_ll, c_sz, c_float = ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t, c
 XV_OK, XV_ERR_ARG, XV_ERR_UNSUPPORTED, XV_ERR_WORKSPACE, XV_ERR_CUDA, XV_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
 XV_GEMM_M_MAX = 64
 XV_KMAX = 64
+XV_CONV_MAX = 8
 
 
 class XVError(RuntimeError):

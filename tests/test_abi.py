@@ -180,3 +180,37 @@ def test_prefill_limits_without_gpu(xv):
     big, layers2 = _fake_state(xv, 1, xv.XV_KMAX + 1, 4096)
     assert L.xv_block_prefill(ctypes.byref(c), ctypes.byref(w), ctypes.byref(big), p, 100, 8, None, None, p, 1 << 30,
                               None) == xv.XV_ERR_ARG              # kmax beyond XV_KMAX
+
+
+def test_complete_gdn_dims_without_gpu(xv):
+    """Column layout of a complete GDN layer: q | k (16 q/k heads) | v | z (32 v heads) | b | a;
+    the convolution covers q | k | v; strides are rounded up to 8 columns."""
+    L = xv.lib()
+    kinds = (ctypes.c_int32 * 4)(0, 0, 0, 1)
+    c = xv.BlockConfig(5120, 151936, 17408, 4, ctypes.cast(kinds, ctypes.c_void_p).value, 32, 128, 128, 24, 4, 256,
+                       1e-6, 16, 4, 1)
+    qk, v = 16 * 128, 32 * 128
+    assert L.xv_gdn_conv_dim(ctypes.byref(c)) == 2 * qk + v
+    assert L.xv_gdn_conv_stride(ctypes.byref(c)) == (2 * qk + v + 7) // 8 * 8
+    assert L.xv_gdn_in_dim(ctypes.byref(c)) == 2 * qk + 2 * v + 2 * 32
+    assert L.xv_gdn_hist_stride(ctypes.byref(c)) % 8 == 0
+    assert L.xv_gdn_hist_stride(ctypes.byref(c)) >= L.xv_gdn_in_dim(ctypes.byref(c))
+    bad = xv.BlockConfig(5120, 151936, 17408, 4, ctypes.cast(kinds, ctypes.c_void_p).value, 32, 128, 128, 24, 4, 256,
+                         1e-6, 12, 4, 1)      # 12 q/k heads do not divide 32 v heads
+    assert L.xv_gdn_in_dim(ctypes.byref(bad)) == -1
+    wide = xv.BlockConfig(5120, 151936, 17408, 4, ctypes.cast(kinds, ctypes.c_void_p).value, 32, 128, 128, 24, 4,
+                          256, 1e-6, 16, xv.XV_CONV_MAX + 1, 1)
+    assert L.xv_gdn_in_dim(ctypes.byref(wide)) == -1
+    # the prefill workspace holds the verify workspace and its own chunk buffers
+    assert L.xv_block_prefill_workspace_size(ctypes.byref(c), 1, 64, 4096) > \
+        L.xv_block_workspace_size(ctypes.byref(c), 1, 64, 4096) > 0
+    assert L.xv_block_workspace_size(ctypes.byref(c), 0, 64, 4096) == 0
+
+
+def test_binding_constants_match_the_header(xv):
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "xv.h")).read()
+    for name in ("XV_KMAX", "XV_GEMM_M_MAX", "XV_CONV_MAX", "XV_ABI_VERSION"):
+        m = re.search(r"#define\s+%s\s+(\d+)" % name, hdr)
+        assert m, name
+        value = xv.xv_abi_version() if name == "XV_ABI_VERSION" else getattr(xv, name)
+        assert value == int(m.group(1)), name
