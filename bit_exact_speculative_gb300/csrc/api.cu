@@ -25,6 +25,17 @@ std::mutex g_err_mu;
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// Kernels whose dynamic shared-memory size has been raised, per device (function
+// attributes belong to the device that was current when they were set).
+struct AttrSet {
+    int dev;
+    const void* fn;
+    int bytes;
+};
+std::vector<AttrSet> g_attr_set;
+int g_sm_count[MAX_DEVICES] = {};
+std::mutex g_attr_mu;
+
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 }  // namespace
@@ -71,6 +82,39 @@ xv_status launched(const char* what, cudaStream_t s, int kind, long long bytes) 
         ++g_trace.count;
     }
     return st;
+}
+
+xv_status kernel_smem_once(const void* fn, int bytes, bool max_carveout, const char* what) {
+    int dev = 0;
+    if (xv_status st = cuda_check(cudaGetDevice(&dev), what)) return st;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (const AttrSet& a : g_attr_set)
+        if (a.dev == dev && a.fn == fn && a.bytes >= bytes) return XV_OK;
+    if (max_carveout)
+        if (xv_status st = cuda_check(cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100), what))
+            return st;
+    if (xv_status st = cuda_check(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), what))
+        return st;
+    for (AttrSet& a : g_attr_set)
+        if (a.dev == dev && a.fn == fn) {
+            a.bytes = bytes;
+            return XV_OK;
+        }
+    g_attr_set.push_back(AttrSet{dev, fn, bytes});
+    return XV_OK;
+}
+
+xv_status device_sm_count(int* out) {
+    int dev = 0;
+    if (xv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return st;
+    if (dev < 0 || dev >= MAX_DEVICES) return fail(XV_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (!g_sm_count[dev])
+        if (xv_status st = cuda_check(cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev),
+                                      "SM count"))
+            return st;
+    *out = g_sm_count[dev];
+    return XV_OK;
 }
 
 unsigned* device_error_word() {

@@ -700,32 +700,21 @@ inline int nsplit_for(int max_len) { return (max_len + ATTN_SPLIT - 1) / ATTN_SP
 template <int HD>
 xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int B, cudaStream_t s) {
     using S = AttnShape<HD>;
-    static bool attr_done[64] = {};
-    static int sms[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "attn: device ordinal out of range");
-    if (!attr_done[dev]) {
-        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD, true>,
-                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM),
-                                      "attn: set shared memory size"))
-            return st;
-        if (xv_status st = cuda_check(cudaFuncSetAttribute(attn_split_kernel<HD, false>,
-                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM),
-                                      "attn: set shared memory size"))
-            return st;
-        if (xv_status st = cuda_check(cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev),
-                                      "attn: SM count"))
-            return st;
-        attr_done[dev] = true;
-    }
+    int sms = 0;
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(attn_split_kernel<HD, true>), S::SMEM, false,
+                                        "attn: set shared memory size"))
+        return st;
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(attn_split_kernel<HD, false>), S::SMEM, false,
+                                        "attn: set shared memory size"))
+        return st;
+    if (xv_status st = device_sm_count(&sms)) return st;
     // past two waves of items, one persistent CTA per SM (the shared-memory plan admits one);
     // otherwise one CTA per item (measured in the verify step: with 160 items the persistent
     // launch was 4 us slower, with 1028 and 8224 items 15 and 218 us faster)
     const long long n_items = static_cast<long long>(a.nsplit) * ((a.R * a.G + 63) / 64) * a.Hkv * B;
     if (n_items > (1ll << 30)) return fail(XV_ERR_UNSUPPORTED, "attn: %lld work items", n_items);
-    const bool multi = n_items > 2ll * sms[dev];
-    dim3 grid(static_cast<unsigned>(multi ? sms[dev] : n_items));
+    const bool multi = n_items > 2ll * sms;
+    dim3 grid(static_cast<unsigned>(multi ? sms : n_items));
     trace_pre(s);
     if (multi) launch_k(attn_split_kernel<HD, true>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
     else launch_k(attn_split_kernel<HD, false>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
@@ -768,17 +757,9 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
     if (st) return st;
     CombineArgs c{ctx_len, len_bias, R, Hq, nsplit, max_len, hd, opart, ml, gate, gate_stride, out, out_stride, err};
     const size_t csm = combine_smem(hd, nsplit);
-    static size_t csm_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "attn: device ordinal out of range");
-    if (csm > csm_set[dev]) {
-        if (xv_status e = cuda_check(cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                          static_cast<int>(csm)),
-                                     "attn: set combine shared memory size"))
-            return e;
-        csm_set[dev] = csm;
-    }
+    if (xv_status e = kernel_smem_once(reinterpret_cast<const void*>(attn_combine_kernel), static_cast<int>(csm), false,
+                                       "attn: set combine shared memory size"))
+        return e;
     trace_pre(s);
     launch_k(attn_combine_kernel, dim3(B * R * Hq), dim3(hd / 2), csm, s, c);
     return launched("attn_combine_kernel", s, K_ATTN_COMBINE,

@@ -332,28 +332,13 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     const int max_steps = max_commit + k;
     if (max_steps > THREADS) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS);
     dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
-    // function attributes are per device: set once on each
-    static bool carve[64][2] = {};
-    int dev = 0;
-    if (xv_status st = cuda_check(cudaGetDevice(&dev), "gdn: cudaGetDevice")) return st;
-    if (dev < 0 || dev >= 64) return fail(XV_ERR_CUDA, "gdn: device ordinal %d out of range", dev);
-    if (!carve[dev][dk == 128]) {
-        // as much shared memory as possible for the carveout: several CTAs per SM at B = 8; up to
-        // THREADS staged steps (a prefill chunk of XV_KMAX positions after as many pending ones)
-        xv_status st;
-        if (dk == 128) {
-            cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-            st = cuda_check(cudaFuncSetAttribute(gdn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(sizeof(StepSmem<128>) * THREADS)),
-                            "gdn: set shared memory size");
-        } else {
-            cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-            st = cuda_check(cudaFuncSetAttribute(gdn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(sizeof(StepSmem<64>) * THREADS)),
-                            "gdn: set shared memory size");
-        }
-        if (st) return st;
-        carve[dev][dk == 128] = true;
+    // as much shared memory as possible for the carveout: several CTAs per SM at B = 8; up to
+    // THREADS staged steps (a prefill chunk of XV_KMAX positions after as many pending ones)
+    {
+        const void* fn = dk == 128 ? reinterpret_cast<const void*>(gdn_kernel<128>)
+                                   : reinterpret_cast<const void*>(gdn_kernel<64>);
+        const int bytes = static_cast<int>(dk == 128 ? sizeof(StepSmem<128>) * THREADS : sizeof(StepSmem<64>) * THREADS);
+        if (xv_status st = kernel_smem_once(fn, bytes, true, "gdn: set shared memory size")) return st;
     }
     trace_pre(s);
     if (dk == 128) {

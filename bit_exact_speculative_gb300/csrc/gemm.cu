@@ -368,8 +368,17 @@ int gemm_splits(int N, int K) {
 // The counters sit at the same place for every shape, so one zeroed workspace
 // can serve GEMMs of different shapes in turn (each call leaves them zero).
 // A split GEMM has at most SM_COUNT_TARGET * RESIDENT_PER_SM / 2 tiles.
-constexpr size_t COUNTER_BYTES = 1024;
+constexpr size_t COUNTER_BYTES = GEMM_COUNTER_BYTES;
 static_assert(COUNTER_BYTES / sizeof(unsigned) >= SM_COUNT_TARGET * RESIDENT_PER_SM / 2, "counter region too small");
+// The largest scratch need: a split shape has S * tiles <= SM_COUNT_TARGET * RESIDENT_PER_SM and
+// N <= tiles * GEMM_BN, so its partials take at most M_MAX * 4 bytes * that many tiles' columns;
+// the allocation-free entry point's fixed array must hold it for every M <= XV_GEMM_M_MAX.
+static_assert(COUNTER_BYTES + 256 + static_cast<size_t>(XV_GEMM_M_MAX) * sizeof(float) * SM_COUNT_TARGET *
+                                          RESIDENT_PER_SM * GEMM_BN <=
+                  XV_GEMM_NOALLOC_SCRATCH_BYTES,
+              "the allocation-free scratch array is smaller than the largest split-K need");
+
+bool gemm_uses_counters(int M, int N, int K) { return gemm_splits(N, K) > CLUSTER_MAX && M <= X_SMALL_M; }
 
 size_t gemm_workspace_size(int M, int N, int K) {
     const int S = gemm_splits(N, K);
@@ -410,14 +419,9 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
         cnt = sep_combine ? nullptr : static_cast<unsigned*>(ws);
         part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + COUNTER_BYTES);
     }
-    static bool attr_set[2] = {false, false};
     auto kern = f32out ? gemm_small_m_kernel<true> : gemm_small_m_kernel<false>;
-    if (!attr_set[f32out]) {
-        if (xv_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX),
-                                      "gemm: set shared memory size"))
-            return st;
-        attr_set[f32out] = true;
-    }
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(kern), SMEM_MAX, false, "gemm: set shared memory size"))
+        return st;
     const int xb = M <= X_SMALL_M ? 1024 : B_BYTES, xr = M <= X_SMALL_M ? X_RING : STAGES;
     const int smem = smem_bytes(xb, xr);
     dim3 grid(tiles, S);

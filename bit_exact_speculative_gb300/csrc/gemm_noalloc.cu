@@ -15,8 +15,10 @@
 // cannot use its name as a device address, so the first call on each device
 // looks the address up with cudaGetSymbolAddress (with that device current)
 // and caches it; that first call should therefore come before any stream
-// capture.  The counters it needs are zero when the module loads, the first
-// call on a device clears them once more, and every call leaves them zero.
+// capture.  The per-tile arrival counters at the start of the array must be
+// zero when a split GEMM starts; a GEMM that completes leaves them zero, but
+// one whose bounded wait gave up (xv_device_check reports bit 0) may not, so
+// every call whose shape uses them first clears them on the caller's stream.
 // All calls share the one array: calls whose kernels overlap on the GPU (other
 // streams, other host threads) race and must be serialised by the caller.
 #include <mutex>
@@ -33,7 +35,7 @@ void* g_scratch_ptr[MAX_DEVICES] = {};
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device (set-up on first use).
-xv_status scratch_address(cudaStream_t s, void** out) {
+xv_status scratch_address(void** out) {
     int dev = 0;
     if (xv_status st = cuda_check(cudaGetDevice(&dev), "gemm_noalloc: cudaGetDevice")) return st;
     if (dev < 0 || dev >= MAX_DEVICES) return fail(XV_ERR_CUDA, "gemm_noalloc: device ordinal %d out of range", dev);
@@ -42,8 +44,6 @@ xv_status scratch_address(cudaStream_t s, void** out) {
         void* p = nullptr;
         if (xv_status st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "gemm_noalloc: cudaGetSymbolAddress"))
             return st;
-        // the tile arrival counters (the first KiB of a GEMM workspace) must be zero before the first split GEMM
-        if (xv_status st = cuda_check(cudaMemsetAsync(p, 0, 1024, s), "gemm_noalloc: clear counters")) return st;
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
@@ -71,6 +71,9 @@ extern "C" xv_status xv_gemm_small_m_noalloc(const uint16_t* X, int ldx, const u
                     M, N, K, need, static_cast<size_t>(XV_GEMM_NOALLOC_SCRATCH_BYTES));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void* scratch = nullptr;
-    if (xv_status st = scratch_address(s, &scratch)) return st;
+    if (xv_status st = scratch_address(&scratch)) return st;
+    if (gemm_uses_counters(M, N, K))
+        if (xv_status st = cuda_check(cudaMemsetAsync(scratch, 0, GEMM_COUNTER_BYTES, s), "gemm_noalloc: clear counters"))
+            return st;
     return gemm_launch(X, ldx, W, Y, ldy, false, M, N, K, scratch, XV_GEMM_NOALLOC_SCRATCH_BYTES, s);
 }

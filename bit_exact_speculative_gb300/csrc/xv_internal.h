@@ -62,6 +62,11 @@ inline cudaError_t launch_k_cluster(void (*kern)(KArgs...), dim3 grid, dim3 bloc
 }
 // Device address of the library's device-side error word for the current device.
 unsigned* device_error_word();
+// Raises fn's dynamic shared-memory limit to at least `bytes` (and, with max_carveout, asks for the
+// largest shared-memory carveout) on the current device, once per device and kernel; thread-safe.
+xv_status kernel_smem_once(const void* fn, int bytes, bool max_carveout, const char* what);
+// Number of SMs of the current device (looked up once per device; thread-safe).
+xv_status device_sm_count(int* out);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 xv_status encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
@@ -77,6 +82,10 @@ constexpr int GEMM_BK = 64;    // K elements per pipeline stage (one 128-byte sw
 constexpr int GEMM_TOK = 64;   // token columns of every MMA (MMA N), whatever M is
 int gemm_splits(int N, int K);
 size_t gemm_workspace_size(int M, int N, int K);
+// Bytes at the start of a GEMM workspace that hold the tile arrival counters (zero between calls).
+constexpr size_t GEMM_COUNTER_BYTES = 1024;
+// Whether a GEMM of this shape combines its split-K partials through the workspace's tile counters.
+bool gemm_uses_counters(int M, int N, int K);
 // defer_part: when the GEMM would combine its partials in a separate kernel (M > 8, more segments
 // than a cluster), it skips that kernel and returns the partials [S][M][N] and S instead (else
 // *defer_part = nullptr).

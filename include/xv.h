@@ -135,8 +135,11 @@ int xv_gemm_splits(int N, int K);
  * a convenience of this library.  Its scratch (split-K partial sums and tile
  * counters) is a fixed array of XV_GEMM_NOALLOC_SCRATCH_BYTES that every GPU
  * loading the library holds until the process exits.  The first call on a
- * device looks up that array's device address (and clears its counters), so
- * make the first call on each device before any stream capture.  Shapes whose
+ * device looks up that array's device address, so make the first call on each
+ * device before any stream capture.  A call whose shape combines its split-K
+ * partials through the tile counters (M <= 8 and more than 4 K-segments) first
+ * clears them on the stream (a 1 KiB memset), so a call that follows one whose
+ * bounded wait gave up still starts from zero.  Shapes whose
  * scratch need (xv_gemm_workspace_size) exceeds the array are rejected with
  * XV_ERR_UNSUPPORTED; with this size every shape with M <= XV_GEMM_M_MAX fits.
  * All calls share the array: calls that overlap on the GPU race, so callers

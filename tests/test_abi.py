@@ -64,6 +64,16 @@ def test_gemm_validation_without_gpu(xv):
         assert xv.xv_gemm_workspace_size(64, N, 17408) <= 10 << 20
 
 
+def test_gemm_noalloc_scratch_holds_every_shape(xv):
+    """The allocation-free entry point's fixed scratch (10 MiB) holds the split-K need of every
+    shape it accepts (M <= 64), over a sweep of widths and depths."""
+    worst = 0
+    for N in list(range(128, 20000, 128)) + [1, 100, 300, 5120, 9728, 19455]:
+        for K in (64, 256, 1000, 4096, 8192, 17408, 65536):
+            worst = max(worst, xv.xv_gemm_workspace_size(64, N, K))
+    assert 0 < worst <= 10 << 20
+
+
 def test_gemm_splits_depend_on_shape_only(xv):
     for N, K in [(5120, 4096), (5120, 6144), (5120, 17408), (12352, 5120), (14336, 5120), (34816, 5120), (151936, 5120)]:
         s = xv.xv_gemm_splits(N, K)

@@ -5,8 +5,8 @@ running under another framework's memory pool, plugins inside a process that
 owns every device allocation, loops where allocating is not allowed).  It
 runs the same kernel as xv_gemm_small_m with its scratch in a fixed array of
 the library, so its output must match the workspace entry point's — here
-bit for bit, which is inside every tolerance the other tests use — on two
-calls in a row (the second call finds the array as the first one left it).
+bit for bit, which is inside every tolerance the other tests use — on calls
+in a row, each finding the array as the previous one left it.
 This file is collected last on purpose.
 """
 import ctypes
@@ -29,26 +29,52 @@ def xv():
     return m
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 1024, 8192), (64, 1024, 8192), (16, 5120, 17408), (5, 300, 1000)])
-def test_noalloc_matches_workspace_entry_point_twice(xv, M, N, K):
-    # the first two shapes split K into 16 segments, whose partial sums go through the scratch
+def _operands(xv, M, N, K):
     X = dev(synth.normal_bf16(0, synth.tid(f"na.x.{M}.{N}.{K}"), (M, K)))
     W = dev(synth.normal_bf16(0, synth.tid(f"na.w.{M}.{N}.{K}"), (N, K), sigma=0.02))
     ref = torch.empty((M, N), dtype=torch.int16, device="cuda")
     ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K))
     xv.xv_gemm_small_m(X, W, ref, ws)
+    return X, W, ref
+
+
+def _noalloc(xv, X, W, M, N, K):
     lib = xv.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    Y = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    code = lib.xv_gemm_small_m_noalloc(ctypes.c_void_p(X.data_ptr()), K, ctypes.c_void_p(W.data_ptr()),
+                                       ctypes.c_void_p(Y.data_ptr()), N, M, N, K, stream)
+    assert code == 0, lib.xv_last_error()
+    return Y
+
+
+# (1, 1024, 8192) and (8, 5120, 17408) split K in 16 and 7 segments with at most 8 token rows:
+# their last-arriving CTAs combine the partials through the scratch's tile counters.  (16, ...)
+# and (64, ...) split as much but combine in a separate kernel; (5, 300, 1000) takes a cluster.
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 8192), (8, 5120, 17408), (16, 1024, 8192), (64, 1024, 8192),
+                                   (16, 5120, 17408), (5, 300, 1000)])
+def test_noalloc_matches_workspace_entry_point_twice(xv, M, N, K):
+    X, W, ref = _operands(xv, M, N, K)
     for _ in range(2):
-        Y = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
-        code = lib.xv_gemm_small_m_noalloc(ctypes.c_void_p(X.data_ptr()), K, ctypes.c_void_p(W.data_ptr()),
-                                           ctypes.c_void_p(Y.data_ptr()), N, M, N, K, stream)
-        assert code == 0, lib.xv_last_error()
-        assert same_bits(Y, ref)
+        assert same_bits(_noalloc(xv, X, W, M, N, K), ref)
     assert xv.xv_device_check() == 0
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch(xv):
+def test_noalloc_alternating_counter_shapes(xv):
+    """Back-to-back calls alternating between two counter-combined shapes with different tile
+    counts (8 and 40 tiles): every call finds the counters the previous one left and still
+    gives the workspace entry point's bits."""
+    assert xv.xv_gemm_splits(1024, 8192) > 4 and xv.xv_gemm_splits(5120, 17408) > 4
+    a = (1, 1024, 8192)
+    b = (8, 5120, 17408)
+    ops = {s: _operands(xv, *s) for s in (a, b)}
+    for s in (a, b, a, b, b, a):
+        X, W, ref = ops[s]
+        assert same_bits(_noalloc(xv, X, W, *s), ref), s
+    assert xv.xv_device_check() == 0
+
+
+def test_noalloc_rejects_more_rows_than_a_call_takes(xv):
     lib = xv.lib()
     p = ctypes.c_void_p(0x10000)
     # more rows than any GEMM call takes: rejected before anything is launched
