@@ -20,20 +20,25 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_LIB32_PATH = os.path.join(_HERE, "liboracle_f32.so")
 _lib = None
+_lib32 = None
 
 vp = ctypes.c_void_p
 i32, i64, u16, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_uint16, ctypes.c_double
 
 
-def build(force: bool = False) -> str:
-    """Compile ``liboracle.so`` (gcc, OpenMP, no FP contraction) beside the source."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-                               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+def build(force: bool = False, f32: bool = False) -> str:
+    """Compile ``liboracle.so`` (gcc, OpenMP, no FP contraction) beside the source; with ``f32``
+    the single-precision evaluation ``liboracle_f32.so`` (the same source with ORC_F32 defined),
+    which only sizes tolerances and is never the reference."""
+    path = _LIB32_PATH if f32 else _LIB_PATH
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"] +
+                              (["-DORC_F32"] if f32 else []) + ["-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, path)
+    return path
 
 
 class _Cfg(ctypes.Structure):
@@ -52,10 +57,11 @@ class _Seq(ctypes.Structure):
     _fields_ = [("S", vp), ("kc", vp), ("vc", vp), ("Lmax", i32), ("len", i32), ("conv", vp)]
 
 
-def lib():
-    global _lib
-    if _lib is None:
-        L = ctypes.CDLL(build())
+def lib(f32: bool = False):
+    """The double-precision oracle (or, with ``f32``, its single-precision evaluation)."""
+    global _lib, _lib32
+    if (_lib32 if f32 else _lib) is None:
+        L = ctypes.CDLL(build(f32=f32))
         L.orc_bf16_val.argtypes, L.orc_bf16_val.restype = [u16], dbl
         L.orc_bf16_rne.argtypes, L.orc_bf16_rne.restype = [dbl], u16
         L.orc_bf16_round.argtypes, L.orc_bf16_round.restype = [dbl], dbl
@@ -80,8 +86,11 @@ def lib():
         L.orc_gdn_in_dim.argtypes, L.orc_gdn_in_dim.restype = [vp], i32
         L.orc_attn_in_dim.argtypes, L.orc_attn_in_dim.restype = [vp], i32
         L.orc_decode_token.argtypes = [vp, vp, vp, ctypes.c_int32, vp]
-        _lib = L
-    return _lib
+        if f32:
+            _lib32 = L
+        else:
+            _lib = L
+    return _lib32 if f32 else _lib
 
 
 def _p(a: np.ndarray) -> int:
@@ -258,10 +267,15 @@ class Stack:
     ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down``
     (and ``.conv_w`` [C, Kc], ``.onorm`` [dv] for GDN layers that use them).
     The convolution states ``conv[l]`` [Kc-1, C] start at zero.
+
+    With ``f32=True`` the stack runs the oracle's single-precision evaluation (every
+    accumulation in fp32, the same bf16 storage points): a second evaluation whose distance from
+    the double-precision one sizes the tolerance of whole-block comparisons.
     """
 
-    def __init__(self, cfg: dict, weights: dict, Lmax: int):
+    def __init__(self, cfg: dict, weights: dict, Lmax: int, f32: bool = False):
         self.cfg = dict(cfg)
+        self._f32 = bool(f32)
         L = len(cfg["kinds"])
         self._kind = np.asarray(cfg["kinds"], dtype=np.int32)
         self._c = _Cfg(cfg["H"], cfg["V"], cfg["F"], L, _p(self._kind), cfg["gdn_h"], cfg["gdn_dk"],
@@ -312,8 +326,8 @@ class Stack:
         seq = _Seq(ctypes.cast(Sp, vp).value, ctypes.cast(Kp, vp).value, ctypes.cast(Vp, vp).value,
                    self.Lmax, self.len, ctypes.cast(Cp, vp).value)
         logits = np.empty(self.cfg["V"], dtype=np.float64)
-        lib().orc_decode_token(ctypes.byref(self._c), ctypes.byref(self._W), ctypes.byref(seq),
-                               int(token), _p(logits))
+        lib(self._f32).orc_decode_token(ctypes.byref(self._c), ctypes.byref(self._W), ctypes.byref(seq),
+                                        int(token), _p(logits))
         self.len = seq.len
         return logits
 

@@ -61,14 +61,35 @@
  * its state; the gated norm against closed forms; grouped heads against the
  * ungrouped step on repeated q/k; the complete GDN layer's column layout
  * against repeated projection rows, a zeroed z block and a numpy composition.
- * orc_decode_token composes pinned functions; its composition is pinned only
- * structurally (identity path, KV append position), so its exact operation
- * order is "parity unpinned".
+ * orc_decode_token composes pinned functions; its composition (column blocks,
+ * gate, MLP layout, both residuals) is pinned against numpy compositions of
+ * the pinned parts.
+ *
+ * Second evaluation.  Compiled with ORC_F32 defined, every accumulation and
+ * every elementwise evaluation runs in single precision instead (the type
+ * `real` below; the GDN state is rounded to single precision after each
+ * step), with the bf16 storage points unchanged.  That build is never the
+ * reference: the tests use the distance between its results and the double
+ * build's to size the tolerance of whole-block comparisons, since it shows
+ * how far a faithful fp32 evaluation of the same arithmetic lands from the
+ * exact one.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+#ifdef ORC_F32
+typedef float real;
+#define EXP expf
+#define LOG1P log1pf
+#define SQRT sqrtf
+#else
+typedef double real;
+#define EXP exp
+#define LOG1P log1p
+#define SQRT sqrt
+#endif
 
 /* ------------------------------------------------------------------ bf16 */
 
@@ -119,9 +140,9 @@ void orc_bf16_rne_f32_range(uint64_t lo, uint64_t hi, uint16_t* out) {
 
 /* ------------------------------------------------------------ elementwise */
 
-static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
-static double softplus(double x) { return x > 20.0 ? x : log1p(exp(x)); }
-static double silu(double x) { return x * sigmoid(x); }
+static real sigmoid(real x) { return (real)1 / ((real)1 + EXP(-x)); }
+static real softplus(real x) { return x > (real)20 ? x : LOG1P(EXP(x)); }
+static real silu(real x) { return x * sigmoid(x); }
 
 /* ----------------------------------------------------------------- GEMM */
 
@@ -135,8 +156,8 @@ void orc_gemm(const uint16_t* X, int64_t ldx, const uint16_t* W, int M, int N, i
         const uint16_t* w = W + (int64_t)n * K;
         for (int m = 0; m < M; ++m) {
             const uint16_t* x = X + (int64_t)m * ldx;
-            double acc = 0.0;
-            for (int k = 0; k < K; ++k) acc += orc_bf16_val(x[k]) * orc_bf16_val(w[k]);
+            real acc = 0;
+            for (int k = 0; k < K; ++k) acc += (real)orc_bf16_val(x[k]) * (real)orc_bf16_val(w[k]);
             Y[(int64_t)m * N + n] = acc;
         }
     }
@@ -146,32 +167,33 @@ void orc_gemm(const uint16_t* X, int64_t ldx, const uint16_t* W, int M, int N, i
 
 /* y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ) */
 void orc_rmsnorm(const uint16_t* x, const uint16_t* w, int H, double eps, uint16_t* y) {
-    double ss = 0.0;
-    for (int i = 0; i < H; ++i) ss += orc_bf16_val(x[i]) * orc_bf16_val(x[i]);
-    double inv = 1.0 / sqrt(ss / H + eps);
-    for (int i = 0; i < H; ++i) y[i] = orc_bf16_rne(orc_bf16_val(x[i]) * inv * (1.0 + orc_bf16_val(w[i])));
+    real ss = 0;
+    for (int i = 0; i < H; ++i) ss += (real)orc_bf16_val(x[i]) * (real)orc_bf16_val(x[i]);
+    real inv = (real)1 / SQRT(ss / (real)H + (real)eps);
+    for (int i = 0; i < H; ++i)
+        y[i] = orc_bf16_rne((real)orc_bf16_val(x[i]) * inv * ((real)1 + (real)orc_bf16_val(w[i])));
 }
 
 /* y = bf16( silu(g) * u ) */
 void orc_swiglu(const uint16_t* g, const uint16_t* u, int n, uint16_t* y) {
-    for (int i = 0; i < n; ++i) y[i] = orc_bf16_rne(silu(orc_bf16_val(g[i])) * orc_bf16_val(u[i]));
+    for (int i = 0; i < n; ++i) y[i] = orc_bf16_rne(silu((real)orc_bf16_val(g[i])) * (real)orc_bf16_val(u[i]));
 }
 
 /* beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))): the decode dtype
  * for both ([post]: the faulty verify kept beta in fp32). */
 void orc_gdn_gates(const uint16_t* b, const uint16_t* a, int n, uint16_t* beta, uint16_t* gate) {
     for (int i = 0; i < n; ++i) {
-        beta[i] = orc_bf16_rne(sigmoid(orc_bf16_val(b[i])));
-        gate[i] = orc_bf16_rne(exp(-softplus(orc_bf16_val(a[i]))));
+        beta[i] = orc_bf16_rne(sigmoid((real)orc_bf16_val(b[i])));
+        gate[i] = orc_bf16_rne(EXP(-softplus((real)orc_bf16_val(a[i]))));
     }
 }
 
 /* y = x / sqrt(sum x^2 + eps) */
 void orc_l2norm(const double* x, int n, double eps, double* y) {
-    double ss = 0.0;
-    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
-    double d = sqrt(ss + eps);
-    for (int i = 0; i < n; ++i) y[i] = x[i] / d;
+    real ss = 0;
+    for (int i = 0; i < n; ++i) ss += (real)x[i] * (real)x[i];
+    real d = SQRT(ss + (real)eps);
+    for (int i = 0; i < n; ++i) y[i] = (real)x[i] / d;
 }
 
 /* ---------------------------------------------------------------- GDN */
@@ -182,20 +204,21 @@ void orc_l2norm(const double* x, int n, double eps, double* y) {
  * doubles (unrounded).  O(dv dk^2): slow on purpose, no refactoring. */
 void orc_gdn_step(double* S, const double* q, const double* k, const double* v,
                   double beta, double gate, int dk, int dv, double* o) {
-    double* P = (double*)malloc(sizeof(double) * (size_t)dk * dk);   /* I - b k k^T */
-    double* T = (double*)malloc(sizeof(double) * (size_t)dv * dk);
+    real* P = (real*)malloc(sizeof(real) * (size_t)dk * dk);   /* I - b k k^T */
+    real* T = (real*)malloc(sizeof(real) * (size_t)dv * dk);
+    const real b = (real)beta, a = (real)gate;
     for (int i = 0; i < dk; ++i)
-        for (int j = 0; j < dk; ++j) P[i * dk + j] = (i == j ? 1.0 : 0.0) - beta * k[i] * k[j];
+        for (int j = 0; j < dk; ++j) P[i * dk + j] = (real)(i == j ? 1 : 0) - b * (real)k[i] * (real)k[j];
     for (int r = 0; r < dv; ++r)
         for (int j = 0; j < dk; ++j) {
-            double acc = 0.0;
-            for (int i = 0; i < dk; ++i) acc += S[r * dk + i] * P[i * dk + j];
-            T[r * dk + j] = gate * acc + beta * v[r] * k[j];
+            real acc = 0;
+            for (int i = 0; i < dk; ++i) acc += (real)S[r * dk + i] * P[i * dk + j];
+            T[r * dk + j] = a * acc + b * (real)v[r] * (real)k[j];
         }
-    memcpy(S, T, sizeof(double) * (size_t)dv * dk);
+    for (int i = 0; i < dv * dk; ++i) S[i] = T[i];
     for (int r = 0; r < dv; ++r) {
-        double acc = 0.0;
-        for (int j = 0; j < dk; ++j) acc += S[r * dk + j] * q[j];
+        real acc = 0;
+        for (int j = 0; j < dk; ++j) acc += (real)S[r * dk + j] * (real)q[j];
         o[r] = acc;
     }
     free(P);
@@ -250,9 +273,10 @@ void orc_gdn_step_heads_grouped(double* S, const uint16_t* q, const uint16_t* k,
  * it always holds the last Kc-1 inputs (bf16 values moved, never rounded). */
 void orc_conv_step(uint16_t* state, const uint16_t* x, const uint16_t* w, int C, int Kc, uint16_t* y) {
     for (int c = 0; c < C; ++c) {
-        double acc = 0.0;
-        for (int j = 0; j < Kc - 1; ++j) acc += orc_bf16_val(w[(int64_t)c * Kc + j]) * orc_bf16_val(state[(int64_t)j * C + c]);
-        acc += orc_bf16_val(w[(int64_t)c * Kc + Kc - 1]) * orc_bf16_val(x[c]);
+        real acc = 0;
+        for (int j = 0; j < Kc - 1; ++j)
+            acc += (real)orc_bf16_val(w[(int64_t)c * Kc + j]) * (real)orc_bf16_val(state[(int64_t)j * C + c]);
+        acc += (real)orc_bf16_val(w[(int64_t)c * Kc + Kc - 1]) * (real)orc_bf16_val(x[c]);
         y[c] = orc_bf16_rne(silu(acc));
     }
     for (int j = 0; j + 1 < Kc - 1; ++j) memcpy(state + (int64_t)j * C, state + (int64_t)(j + 1) * C, sizeof(uint16_t) * C);
@@ -261,11 +285,12 @@ void orc_conv_step(uint16_t* state, const uint16_t* x, const uint16_t* w, int C,
 
 /* The gated output norm of one head: y = bf16( o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z) ). */
 void orc_gated_norm(const uint16_t* o, const uint16_t* z, const uint16_t* w, int n, double eps, uint16_t* y) {
-    double ss = 0.0;
-    for (int i = 0; i < n; ++i) ss += orc_bf16_val(o[i]) * orc_bf16_val(o[i]);
-    double inv = 1.0 / sqrt(ss / n + eps);
+    real ss = 0;
+    for (int i = 0; i < n; ++i) ss += (real)orc_bf16_val(o[i]) * (real)orc_bf16_val(o[i]);
+    real inv = (real)1 / SQRT(ss / (real)n + (real)eps);
     for (int i = 0; i < n; ++i)
-        y[i] = orc_bf16_rne(orc_bf16_val(o[i]) * inv * (1.0 + orc_bf16_val(w[i])) * silu(orc_bf16_val(z[i])));
+        y[i] = orc_bf16_rne((real)orc_bf16_val(o[i]) * inv * ((real)1 + (real)orc_bf16_val(w[i])) *
+                            silu((real)orc_bf16_val(z[i])));
 }
 
 /* ---------------------------------------------------------- attention */
@@ -276,19 +301,19 @@ void orc_gated_norm(const uint16_t* o, const uint16_t* z, const uint16_t* w, int
  * attention as one decode row per draft position; a decode row is this. */
 void orc_attn_row(const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t ld,
                   int len, int hd, double scale, double* out) {
-    double* s = (double*)malloc(sizeof(double) * (len > 0 ? len : 1));
-    double m = -INFINITY;
+    real* s = (real*)malloc(sizeof(real) * (len > 0 ? len : 1));
+    real m = -INFINITY;
     for (int j = 0; j < len; ++j) {
-        double acc = 0.0;
-        for (int d = 0; d < hd; ++d) acc += orc_bf16_val(q[d]) * orc_bf16_val(K[(int64_t)j * ld + d]);
-        s[j] = acc * scale;
+        real acc = 0;
+        for (int d = 0; d < hd; ++d) acc += (real)orc_bf16_val(q[d]) * (real)orc_bf16_val(K[(int64_t)j * ld + d]);
+        s[j] = acc * (real)scale;
         if (s[j] > m) m = s[j];
     }
-    double l = 0.0;
-    for (int j = 0; j < len; ++j) { s[j] = exp(s[j] - m); l += s[j]; }
+    real l = 0;
+    for (int j = 0; j < len; ++j) { s[j] = EXP(s[j] - m); l += s[j]; }
     for (int d = 0; d < hd; ++d) {
-        double acc = 0.0;
-        for (int j = 0; j < len; ++j) acc += s[j] * orc_bf16_val(V[(int64_t)j * ld + d]);
+        real acc = 0;
+        for (int j = 0; j < len; ++j) acc += s[j] * (real)orc_bf16_val(V[(int64_t)j * ld + d]);
         out[d] = acc / l;
     }
     free(s);
@@ -436,7 +461,7 @@ static void attn_mixer(const orc_cfg* c, orc_seq* s, int layer, const uint16_t* 
         memcpy(vc + ((int64_t)h * s->Lmax + s->len) * hd, v + h * hd, sizeof(uint16_t) * hd);
     }
     orc_attn_rows(q, inner, kc, vc, s->Lmax, s->len + 1, 1, Hq, Hkv, hd, 1.0 / sqrt((double)hd), o, inner);
-    for (int i = 0; i < inner; ++i) o[i] = orc_bf16_rne(orc_bf16_val(o[i]) * sigmoid(orc_bf16_val(g[i])));
+    for (int i = 0; i < inner; ++i) o[i] = orc_bf16_rne((real)orc_bf16_val(o[i]) * sigmoid((real)orc_bf16_val(g[i])));
     proj(o, Wout, c->H, inner, y);
     free(p); free(o);
 }

@@ -5,13 +5,20 @@ Tolerances (stated once, used everywhere):
   - fp32 GDN state vs the oracle (same bf16 inputs on both sides):
     max_i |d_i| / max(|ref_i|, RMS(ref)) <= 1e-4;
   - fp32 logits of the whole block vs the oracle's sequential decode:
-    RMS(err) <= 2e-2 * RMS(ref) and max|err| <= 1e-1 * RMS(ref), and the argmax
-    ids agree wherever the oracle's top-1/top-2 margin exceeds 0.25.  A block
-    output has passed through ~8 bf16 storage points per layer; each GEMM
-    output that lands within the fp32 accumulation error of a bf16 rounding
-    boundary rounds the other way on one side (about 0.3% of elements,
-    measured), and those 1-ulp differences propagate.  The 0.25 margin is the
-    recipe card's own figure for where divergent tokens cluster;
+    RMS(err) <= 3 * RMS(spread) and max|err| <= 3 * max|spread|, where spread
+    is the oracle's own single-precision evaluation minus its double one on
+    the same inputs (the same rows, extended on the tiny blocks to 16
+    positions of the same sequence).  A block output has passed through ~8
+    bf16 storage points per layer; a value that lands within the fp32
+    accumulation error of a bf16 rounding boundary rounds the other way in
+    any fp32 evaluation, and those 1-ulp differences propagate: the spread
+    measures how far a faithful fp32 evaluation lands from the exact one, and
+    the factor 3 leaves room for the device's different (equally valid)
+    accumulation order.  Argmax ids equal the lowest-index maximum of the
+    GPU's own logits row (exactly), and the oracle's argmax wherever the
+    oracle's top-1/top-2 margin exceeds twice the max bound (no pair of
+    logits within the bound can swap there); each such check must find a
+    decisive row;
   - GPU vs GPU comparisons: 0 differing bits.
 """
 import numpy as np
@@ -65,30 +72,40 @@ def assert_f32_close(got, ref, rel=BF16_REL, what=""):
     assert err <= bound, f"{what}: max|err| {err:.3e} > {rel} * RMS = {bound:.3e}"
 
 
-BLOCK_RMS_REL = 2e-2
-BLOCK_MAX_REL = 1e-1
-ARGMAX_MARGIN = 0.25
+SPREAD_FACTOR = 3.0
 
 
-def assert_block_close(got, ref, what=""):
+def assert_block_close(got, ref, spread, what=""):
+    """got, ref: fp32/fp64 logits [n, V]; spread: f32-oracle minus f64-oracle logits on the same
+    inputs (at least the compared rows).  Returns the max-error bound."""
     g = np.asarray(got, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
+    sp = np.asarray(spread, dtype=np.float64)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    rms_bound, max_bound = SPREAD_FACTOR * rms(sp), SPREAD_FACTOR * float(np.max(np.abs(sp)))
+    assert rms_bound > 0 and max_bound > 0, f"{what}: degenerate spread"
     e = np.abs(g - r)
-    scale = rms(r)
-    assert rms(e) <= BLOCK_RMS_REL * scale, f"{what}: RMS err {rms(e):.3e} > {BLOCK_RMS_REL} * RMS {scale:.3e}"
-    assert e.max() <= BLOCK_MAX_REL * scale, f"{what}: max err {e.max():.3e} > {BLOCK_MAX_REL} * RMS {scale:.3e}"
+    assert rms(e) <= rms_bound, f"{what}: RMS err {rms(e):.3e} > {SPREAD_FACTOR} * RMS(spread) = {rms_bound:.3e}"
+    assert e.max() <= max_bound, f"{what}: max err {e.max():.3e} > {SPREAD_FACTOR} * max|spread| = {max_bound:.3e}"
+    return max_bound
 
 
-def assert_argmax_agrees(ids, ref_logits, margin=ARGMAX_MARGIN):
-    """ids [n]; ref_logits [n, V].  Returns how many rows had a decisive margin."""
-    checked = 0
-    for i, ref in zip(ids, ref_logits):
-        top2 = np.partition(ref, -2)[-2:]
-        if top2[1] - top2[0] > margin:
-            assert int(i) == int(np.argmax(ref)), f"argmax {int(i)} != oracle {int(np.argmax(ref))} (margin {top2[1] - top2[0]:.3f})"
-            checked += 1
-    return checked
+def assert_argmax(ids, got, ref, max_bound, min_decisive=1):
+    """ids: GPU argmax [n]; got: the GPU logits [n, V] they came from; ref: oracle logits [n, V].
+    Every id is the lowest-index maximum of its GPU row; where the oracle's top-1/top-2 margin
+    exceeds 2 * max_bound it is also the oracle's argmax.  Returns the number of such rows, which
+    must be at least min_decisive."""
+    ids = np.asarray(ids).reshape(-1)
+    got = np.asarray(got)
+    assert np.array_equal(ids, np.argmax(got, axis=1)), "argmax is not the lowest-index maximum of the logits"
+    decisive = 0
+    for i, r in zip(ids, np.asarray(ref, dtype=np.float64)):
+        top2 = np.partition(r, -2)[-2:]
+        if top2[1] - top2[0] > 2 * max_bound:
+            assert int(i) == int(np.argmax(r)), f"argmax {int(i)} != oracle {int(np.argmax(r))} (margin {top2[1] - top2[0]:.3f})"
+            decisive += 1
+    assert decisive >= min_decisive, f"{decisive} decisive rows (margin > {2 * max_bound:.3e}), {min_decisive} needed"
+    return decisive
 
 
 def assert_state_close(got, ref, rel=STATE_REL, what="state"):

@@ -130,6 +130,29 @@ def test_eight_in_flight_equal_alone(xv):
         assert same_bits(out[b * R:(b + 1) * R], one), f"sequence {b} differs when batched"
 
 
+def test_eight_in_flight_long_mixed_lengths(xv):
+    """8 sequences at up to 131072 positions with mixed lengths (more than two waves of items:
+    persistent CTAs whose ranges of items cross sequences of different lengths): each sequence's
+    rows equal the same rows computed alone, bit for bit, and sampled rows match the oracle."""
+    B, R, Hq, Hkv, hd = 8, 8, 24, 4, 256
+    lens = np.array([131072, 70001, 1, 513, 131000, 2183, 64, 99999], dtype=np.int32)
+    Lmax = 131072 + 64
+    q, kc, vc = make(8, B, R, Hq, Hkv, hd, Lmax, name="flightlong")
+    Q, K, V = dev(q), dev(kc), dev(vc)
+    out = attn(xv, Q, K, V, dev(lens), R, B, Hq, Hkv, hd, Lmax, int(lens.max()) + R - 1)
+    for b in range(B):
+        one = attn(xv, Q[b * R:(b + 1) * R], K[b:b + 1], V[b:b + 1], dev(lens[b:b + 1]), R, 1, Hq, Hkv, hd, Lmax,
+                   int(lens[b]) + R - 1)
+        assert same_bits(out[b * R:(b + 1) * R], one), f"sequence {b} (length {lens[b]}) differs when batched"
+    o = host_u16(out).reshape(B, R, Hq, hd)
+    for b in (1, 2, 7):
+        for r, h in ((0, 0), (R - 1, 23)):
+            g = h // (Hq // Hkv)
+            ref = oracle.attn_row(q[b * R + r, h * hd:(h + 1) * hd], kc[b, g], vc[b, g], int(lens[b]) + r, hd ** -0.5)
+            assert_bf16_close(o[b, r, h], ref, what=f"b{b} r{r} h{h}")
+    assert xv.xv_device_check() == 0
+
+
 def test_garbage_past_length_is_ignored(xv):
     """NaN and Inf bit patterns past the last visible position change nothing."""
     B, R, Hq, Hkv, hd, L, Lmax = 1, 8, 24, 4, 256, 1000, 1152

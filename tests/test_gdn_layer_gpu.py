@@ -11,8 +11,8 @@ import torch
 import oracle
 import synth
 from synth import workloads
-from _block import gpu_stack, oracle_stack
-from _gpu import assert_argmax_agrees, assert_bf16_close, assert_block_close, assert_state_close, dev, host, \
+from _block import gpu_stack, oracle_logits, oracle_stack
+from _gpu import assert_argmax, assert_bf16_close, assert_block_close, assert_state_close, dev, host, \
     host_u16, rms, same_bits
 
 pytestmark = pytest.mark.gpu
@@ -161,9 +161,9 @@ def test_tiny_full_verify_equals_decode_and_oracle(tiny_full):
     lgS, amS = sequential(S, toks, B)
     assert same_bits(lgA.view(B, k, -1), lgS)
     assert torch.equal(amA.view(B, k), amS)
-    ref = oracle_stack(cfg, w, 0, B, [L], Lmax).verify(toks[0])
-    assert_block_close(host(lgA), ref, what="complete GDN tiny logits vs oracle")
-    assert_argmax_agrees(host(amA), ref)
+    ref, spread, _ = oracle_logits(cfg, w, 0, B, [L], Lmax, toks[0], extra=12)
+    mb = assert_block_close(host(lgA), ref, spread, what="complete GDN tiny logits vs oracle")
+    assert_argmax(host(amA), host(lgA), ref, mb)
 
 
 @pytest.mark.parametrize("keep", [1, 2, 4])
@@ -188,10 +188,8 @@ def test_tiny_full_forced_reject_then_next_round(tiny_full, keep):
     S.flush()
     assert same_bits(A.state["0.state"], S.state["0.state"])
     assert same_bits(A.state["0.conv"], S.state["0.conv"])
-    ost = oracle_stack(cfg, w, 0, B, lens, Lmax)
-    ost.verify(t1[0, :keep])
-    ref = ost.verify(t2[0])
-    assert_block_close(host(lgA)[:k], ref, what="after rollback vs oracle")
+    ref, spread, ost = oracle_logits(cfg, w, 0, B, lens, Lmax, t2[0], before=t1[0, :keep], extra=12)
+    assert_block_close(host(lgA)[:k], ref, spread, what="after rollback vs oracle")
     assert np.array_equal(host_u16(A.state["0.conv"])[0], ost.conv[0])     # data movement only: exact
     assert_state_close(host(A.state["0.state"])[0], ost.S[0], rel=2e-2)
 
@@ -230,7 +228,7 @@ def test_stack_full_verify_equals_decode_and_in_flight(xv):
     C = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd)
     lgC = C.verify(dev(toks2), k)[0].view(B, k, -1)
     assert same_bits(lgC[0], lgA.view(B, k, -1)[0])
-    ref = oracle_stack(cfg, w, 0, B, lens, Lmax).verify(toks[0, :1])
-    assert_block_close(host(lgA)[:1], ref, what="complete GDN stack vs oracle")
+    ref, spread, _ = oracle_logits(cfg, w, 0, B, lens, Lmax, toks[0, :1])
+    assert_block_close(host(lgA)[:1], ref, spread, what="complete GDN stack vs oracle")
     from bit_exact_speculative_gb300 import xv as m
     assert m.xv_device_check() == 0

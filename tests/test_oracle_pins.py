@@ -688,3 +688,123 @@ def test_full_gdn_layer_composition_and_conv_state():
         rn = f(bf(r / np.sqrt(np.mean(r * r) + 1e-6) * (1 + f(w["final_norm"]))))
         np.testing.assert_allclose(logits, f(w["lm_head"]) @ rn, rtol=1e-12, atol=1e-13)
     assert np.array_equal(st.conv[0], np.stack(proj_rows))
+
+
+# ---------------------------------------- stack composition (attention layer, MLP, residuals)
+
+def _np_norm(x, w, eps=1e-6):
+    """bf16 bits of rmsnorm(x) with the (1 + w) gain, composed in numpy."""
+    return bf(x / np.sqrt(np.mean(x * x) + eps) * (1 + oracle.bf16_to_f64(w)))
+
+
+def _np_attn_layer(w, l, x, cfg, K, V, pos):
+    """The gated attention mixer in numpy: projection columns [q | gate | k | v], the new k/v at
+    position pos, explicit softmax over positions 0..pos per q head h against kv head h // (Hq/Hkv),
+    output rounded to bf16, times sigmoid(gate) rounded again, then the output projection."""
+    f = oracle.bf16_to_f64
+    Hq, Hkv, hd = cfg["at_hq"], cfg["at_hkv"], cfg["at_hd"]
+    inner = Hq * hd
+    xn = f(_np_norm(x, w[f"{l}.norm1"]))
+    p = f(bf(f(w[f"{l}.w_in"]) @ xn))
+    q = p[:inner].reshape(Hq, hd)
+    gate = p[inner:2 * inner]
+    K[:, pos] = p[2 * inner:2 * inner + Hkv * hd].reshape(Hkv, hd)
+    V[:, pos] = p[2 * inner + Hkv * hd:].reshape(Hkv, hd)
+    att = np.empty((Hq, hd))
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        att[h] = sp.softmax(K[g, :pos + 1] @ q[h] / np.sqrt(hd)) @ V[g, :pos + 1]
+    gated = f(bf(f(bf(att.reshape(-1))) * sp.expit(gate)))
+    return f(bf(f(w[f"{l}.w_out"]) @ gated))
+
+
+def _np_mlp(w, l, h, F):
+    """SwiGLU MLP in numpy on rmsnorm(h, norm2): g = the first F rows of w_gu, u = the next F,
+    act = bf16(silu(g) u), y = bf16(W_down act)."""
+    f = oracle.bf16_to_f64
+    hn = f(_np_norm(h, w[f"{l}.norm2"]))
+    gu = f(bf(f(w[f"{l}.w_gu"]) @ hn))
+    g, u = gu[:F], gu[F:]
+    act = f(bf(g * sp.expit(g) * u))
+    return f(bf(f(w[f"{l}.w_down"]) @ act))
+
+
+def _np_logits(w, x):
+    f = oracle.bf16_to_f64
+    return f(w["lm_head"]) @ f(_np_norm(x, w["final_norm"]))
+
+
+def test_attention_layer_composition_with_mlp_silenced():
+    """One gated attention layer (MLP output zeroed), four tokens: the logits equal
+    lm_head @ rmsnorm(x + W_o bf16(bf16(attn) * sigmoid(gate))) composed in numpy, with q, gate, k
+    and v taken from the projection's column blocks in that order, 4 q heads over 2 kv heads, and
+    the KV cache filled position by position.  A swapped block, a wrong GQA map, a gate applied
+    before the output rounding or a missing residual fails it."""
+    cfg = dict(_tiny_cfg(), kinds=[1], at_hq=4, at_hkv=2)
+    w = _tiny_weights(cfg, zero_mlp=True)
+    st = oracle.Stack(cfg, w, Lmax=8)
+    f = oracle.bf16_to_f64
+    K = np.zeros((cfg["at_hkv"], 8, cfg["at_hd"]))
+    V = np.zeros_like(K)
+    for pos, tok in enumerate((5, 2, 7, 7)):
+        logits = st.decode(tok)
+        x = f(w["embed"][tok])
+        r = f(bf(x + _np_attn_layer(w, 0, x, cfg, K, V, pos)))
+        np.testing.assert_allclose(logits, _np_logits(w, r), rtol=1e-12, atol=1e-13)
+    assert np.array_equal(f(st.kc[0][:, :4]), K[:, :4]) and np.array_equal(f(st.vc[0][:, :4]), V[:, :4])
+
+
+def test_mlp_composition_and_residual_chain_with_mixers_silenced():
+    """Two layers whose mixer outputs are zeroed: each layer is h + W_down bf16(silu(g) u) on
+    rmsnorm(h) with its norm2 gain, g the first F rows of the gate|up projection and u the next F,
+    and the second layer reads the first one's residual output (numpy composition)."""
+    cfg = _tiny_cfg()
+    w = _tiny_weights(cfg, zero_mixers=True)
+    st = oracle.Stack(cfg, w, Lmax=8)
+    f = oracle.bf16_to_f64
+    for tok in (3, 9):
+        logits = st.decode(tok)
+        h = f(w["embed"][tok])
+        for l in range(len(cfg["kinds"])):
+            h = f(bf(h + _np_mlp(w, l, h, cfg["F"])))
+        np.testing.assert_allclose(logits, _np_logits(w, h), rtol=1e-12, atol=1e-13)
+    # gate and up rows swapped in the weight give other logits: the layout is pinned, not symmetric
+    ws = dict(w)
+    ws["0.w_gu"] = np.concatenate([w["0.w_gu"][cfg["F"]:], w["0.w_gu"][:cfg["F"]]])
+    assert not np.allclose(oracle.Stack(cfg, ws, Lmax=8).decode(3), oracle.Stack(cfg, w, Lmax=8).decode(3))
+
+
+def test_full_attention_layer_composition():
+    """One attention layer with both sublayers live: x1 = bf16(x + attention mixer), then
+    x2 = bf16(x1 + MLP(rmsnorm(x1, norm2))): the MLP reads the residual after the mixer, and the
+    logits are lm_head @ rmsnorm(x2, final_norm) (numpy composition of the two pinned halves)."""
+    cfg = dict(_tiny_cfg(), kinds=[1], at_hq=4, at_hkv=2)
+    w = _tiny_weights(cfg)
+    st = oracle.Stack(cfg, w, Lmax=8)
+    f = oracle.bf16_to_f64
+    K = np.zeros((cfg["at_hkv"], 8, cfg["at_hd"]))
+    V = np.zeros_like(K)
+    for pos, tok in enumerate((1, 4, 4)):
+        logits = st.decode(tok)
+        x = f(w["embed"][tok])
+        x1 = f(bf(x + _np_attn_layer(w, 0, x, cfg, K, V, pos)))
+        x2 = f(bf(x1 + _np_mlp(w, 0, x1, cfg["F"])))
+        np.testing.assert_allclose(logits, _np_logits(w, x2), rtol=1e-12, atol=1e-13)
+
+
+def test_single_precision_evaluation_is_close_but_distinct():
+    """The single-precision build (the same source with ORC_F32) that sizes block tolerances:
+    on the tiny stack its logits stay within 1% RMS of the double build's yet differ (it is a
+    second evaluation, not a copy), and with every bf16 storage point shared, exact small-integer
+    GEMMs agree bit for bit."""
+    cfg = _tiny_cfg()
+    w = _tiny_weights(cfg)
+    a, b = oracle.Stack(cfg, w, Lmax=16), oracle.Stack(cfg, w, Lmax=16, f32=True)
+    la, lb = a.verify([4, 9, 1, 7, 7, 3]), b.verify([4, 9, 1, 7, 7, 3])
+    d = lb - la
+    assert 0 < np.sqrt(np.mean(d * d)) <= 1e-2 * np.sqrt(np.mean(la * la))
+    X = bf(np.arange(-8, 8).reshape(2, 8))
+    W = bf(np.arange(24).reshape(3, 8) % 5)
+    y32 = np.empty((2, 3))
+    oracle.lib(True).orc_gemm(X.ctypes.data, 8, W.ctypes.data, 2, 3, 8, y32.ctypes.data)
+    assert np.array_equal(y32, oracle.gemm(X, W))
