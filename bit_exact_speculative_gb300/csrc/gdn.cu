@@ -17,17 +17,25 @@
 // Grouped heads: with fewer q/k heads than v heads, v head h reads q/k head
 // h / qk_group (the state and v, beta, gate are per v head).
 //
-// Tiling: a CTA owns (sequence b, head h, 32 state rows) with 128 threads; a
-// row is split over 4 consecutive lanes (lane g holds float4 chunks g, g+4,
-// g+8, ... of the row).  Row dot products: two packed f32x2 accumulators (even
-// and odd pairs), a fixed sum of their four lanes, then an xor-shuffle tree
-// over the row's 4 lanes (offsets 1, 2): every lane ends with the same bits.
-// The state lives in registers across all replay and speculative steps; it is
+// Arithmetic of a row (fixed): a row is split over 4 consecutive lanes (lane g
+// holds float4 chunks g, g+4, g+8, ... of the row).  Row dot products: two
+// packed f32x2 accumulators (even and odd pairs), a fixed sum of their four
+// lanes, then an xor-shuffle tree over the row's 4 lanes (offsets 1, 2): every
+// lane ends with the same bits.  Nothing a row computes depends on which
+// thread, warp or CTA holds it.
+//
+// Tiling (free, chosen per launch): a thread holds RPT rows (rows lane/4,
+// lane/4 + 8, ... of its warp's 8 * RPT), a CTA WARPS warps.  Every step reads
+// the whole k and q vectors from shared memory into each row's lanes; with
+// one row per thread that read (1 KB per row per step) is the bound, so wide
+// launches hold 4 rows per thread and read each slice once for the four.  The
+// state lives in registers across all replay and speculative steps; it is
 // read once (plain loads issued first) and, after a replay, written once.
 // The step inputs (per step: q and k of the head, this CTA's slice of v, beta
-// and gate) are plain 16-byte loads spread over the CTA's threads and issued
-// together with the state loads, so the whole verify's inputs arrive in a
-// single round trip.  q and k are then L2-normalised by 4 threads per vector into fp32.
+// and gate) are staged by 16-byte asynchronous copies spread over the CTA's
+// threads and issued together with the state loads, so the whole verify's
+// inputs arrive in a single round trip without holding registers; q and k are
+// then L2-normalised by 4 threads per vector into fp32.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
@@ -35,12 +43,22 @@ namespace xv {
 
 namespace {
 constexpr int LPR = 4;                          // lanes per state row
-constexpr int RPT = 1;                          // state rows per thread
-constexpr int WARPS = 4;
-constexpr int ROWS_PER_WARP = 32 / LPR * RPT;   // 8
-constexpr int ROWS_PER_CTA = ROWS_PER_WARP * WARPS;
-constexpr int THREADS = 32 * WARPS;
 constexpr int NORM_LANES = 4;                   // threads per q or k vector in the normalisation
+
+// A launch shape: RPT state rows per thread, WARPS warps per CTA, at least MIN_BLOCKS CTAs per SM.
+template <int RPT_, int WARPS_, int MIN_BLOCKS_>
+struct Tiling {
+    static constexpr int RPT = RPT_;
+    static constexpr int WARPS = WARPS_;
+    static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
+    static constexpr int ROWS_PER_WARP = 32 / LPR * RPT;
+    static constexpr int ROWS = ROWS_PER_WARP * WARPS;   // state rows per CTA
+    static constexpr int THREADS = 32 * WARPS;
+};
+using NarrowTiling = Tiling<1, 4, 4>;   // 32 rows, 128 threads: few CTAs (latency-bound launches)
+using WideTiling = Tiling<4, 1, 8>;     // 32 rows, 32 threads: many CTAs (shared-memory reads amortised)
+static_assert(NarrowTiling::ROWS == WideTiling::ROWS, "both tilings cut a head into the same slabs");
+constexpr int SLAB = NarrowTiling::ROWS;
 
 struct GdnArgs {
     float* state;
@@ -57,16 +75,24 @@ struct GdnArgs {
     unsigned* err;
 };
 
-// Per-step inputs staged in shared memory: q and k (fp32, normalised in place), this
-// CTA's v entries, beta and gate.
+// Per-step inputs staged in shared memory: q and k (fp32, normalised), this CTA's v entries,
+// beta and gate; and the raw bf16 q, k, v the asynchronous copies land in.
 template <int DK>
 struct StepSmem {
     float q[DK];
     float k[DK];
-    float v[ROWS_PER_CTA];
+    float v[SLAB];
     float beta, gate;
     float pad[2];
 };
+template <int DK>
+struct RawStep {
+    uint16_t q[DK];
+    uint16_t k[DK];
+    uint16_t v[SLAB];
+};
+template <int DK>
+constexpr size_t step_smem_bytes() { return sizeof(StepSmem<DK>) + sizeof(RawStep<DK>); }
 
 // Source of staged slot t for sequence b: slots [0, max_commit) hold pending rows 0.., slots
 // [max_commit, max_commit + k) the draft rows.  All are staged whatever n_commit[b] is, so
@@ -82,33 +108,46 @@ __device__ __forceinline__ const GdnStepsDev& step_src(const GdnArgs& A, int b, 
 
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
-// Global address of a step's q, k or v piece (all 16-byte aligned: checked by the callers).
-// hk is the q/k head of v head h.
-__device__ __forceinline__ const uint16_t* piece(const GdnStepsDev& src, long long row, int h, int hk, int dk, int dv,
-                                                 int row0, int which) {
-    const long long base = row * src.qkv_stride;
-    if (which == 0) return src.q + base + static_cast<long long>(hk) * dk;
-    if (which == 1) return src.k + base + static_cast<long long>(hk) * dk;
-    return src.v + base + static_cast<long long>(h) * dv + row0;
+// Issues the asynchronous copies of every staged step's raw q, k (of q/k head hk) and this
+// CTA's v slice (rows row0.., of v head h): 16-byte pieces spread over the CTA's threads.
+template <int DK, int THREADS>
+__device__ __forceinline__ void stage_raw(RawStep<DK>* raw, const GdnArgs& A, int b, int h, int hk, int row0,
+                                          int total) {
+    constexpr int QC = DK / 8, VC = SLAB / 8, PER_STEP = 2 * QC + VC;
+    for (int idx = threadIdx.x; idx < total * PER_STEP; idx += THREADS) {
+        const int t = idx / PER_STEP, c = idx % PER_STEP;
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, t, &row);
+        const uint16_t* g;
+        uint16_t* d;
+        if (c < QC) {
+            g = src.q + row * src.qkv_stride + static_cast<long long>(hk) * DK + 8 * c;
+            d = raw[t].q + 8 * c;
+        } else if (c < 2 * QC) {
+            g = src.k + row * src.qkv_stride + static_cast<long long>(hk) * DK + 8 * (c - QC);
+            d = raw[t].k + 8 * (c - QC);
+        } else {
+            g = src.v + row * src.qkv_stride + static_cast<long long>(h) * A.dv + row0 + 8 * (c - 2 * QC);
+            d = raw[t].v + 8 * (c - 2 * QC);
+        }
+        cp_async16(d, g);
+    }
 }
 
-// Vector w of the steps (step w / 2; q for even w, k for odd) read from global memory to fp32,
-// L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)): thread j of the vector's group of
+// Vector w of the staged steps (step w / 2; q for even w, k for odd) from its raw bf16 copy to
+// fp32, L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)): thread j of the vector's group of
 // NORM_LANES takes elements [j DK/4, (j+1) DK/4), sums their squares in four interleaved chains
 // (e mod 4) added as (c0 + c1) + (c2 + c3), the group adds its partials by an xor tree (1, 2),
 // and every thread scales its own elements.
-template <int DK>
-__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const GdnArgs& A, int b, int h, int hk, int total,
-                                              bool l2) {
+template <int DK, int THREADS>
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const RawStep<DK>* raw, int total, bool l2) {
     constexpr int PART = DK / NORM_LANES;
     const int jl = threadIdx.x % NORM_LANES;
     for (int w0 = 0; w0 < 2 * total; w0 += THREADS / NORM_LANES) {   // same trip count for every thread
         const int w = w0 + static_cast<int>(threadIdx.x) / NORM_LANES;
         const bool act = w < 2 * total;
         const int t = act ? w >> 1 : 0;
-        long long row;
-        const GdnStepsDev& src = step_src(A, b, t, &row);
-        const uint16_t* x = piece(src, row, h, hk, DK, A.dv, 0, w & 1) + jl * PART;
+        const uint16_t* x = ((w & 1) ? raw[t].k : raw[t].q) + jl * PART;
         float* y = ((w & 1) ? steps[t].k : steps[t].q) + jl * PART;
         float f[PART];
 #pragma unroll
@@ -179,10 +218,11 @@ __device__ __forceinline__ void load_slice(float2 (&d)[DK / (2 * LPR)], const fl
     }
 }
 
-// The step function shared by decode, replay and verify, for this thread's RPT rows:
+// The step function shared by decode, replay and verify, for this thread's RPT rows (each
+// row's operations are the same whatever RPT is):
 //   S <- a S;  r = S k;  u = beta (v - r);  S <- S + u k^T;  o = S q
 // each operation rounded once (packed f32x2 lanes are independent IEEE fp32 ops).
-template <int DK>
+template <int DK, int RPT>
 __device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const StepSmem<DK>& in, int g,
                                          const int (&r)[RPT], bool want_o, float (&o)[RPT]) {
     constexpr int NP = DK / (2 * LPR);
@@ -211,83 +251,62 @@ __device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const
     for (int x = 0; x < RPT; ++x) o[x] = slice_dot<NP>(s[x], qq);
 }
 
-template <int DK>
-__global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
+template <int DK, class T>
+__global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs A) {
     griddep_launch();
     constexpr int NP = DK / (2 * LPR);
+    constexpr int RPT = T::RPT, THREADS = T::THREADS;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int total = A.max_commit + A.k;
     StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw);
+    RawStep<DK>* raw = reinterpret_cast<RawStep<DK>*>(smem_raw + sizeof(StepSmem<DK>) * (total > 0 ? total : 1));
 
     const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane % LPR;
     int r[RPT];                                           // rows within the slab
 #pragma unroll
-    for (int x = 0; x < RPT; ++x) r[x] = warp * ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
-    const int row0 = slab * ROWS_PER_CTA;
+    for (int x = 0; x < RPT; ++x) r[x] = warp * T::ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
+    const int row0 = slab * SLAB;
     float* srow0 = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0) * DK;
-    if (threadIdx.x == 0) l2_prefetch(srow0, ROWS_PER_CTA * DK * 4);   // a hint only: the loads come after the wait
+    if (threadIdx.x == 0) l2_prefetch(srow0, SLAB * DK * 4);   // a hint only: the loads come after the wait
     griddep_wait();
 
-    // Every load of the CTA in flight at once, each thread's own: its state row (the longest
-    // trip), the commit count, up to two beta or gate scalars (2 * total <= 2 * THREADS), one 16-byte chunk
-    // of a step's v slice, then the q / k chunks its normalisation group reads.  (Bulk copies
-    // of the same pieces, 3 per step, took 2 us to issue for 16 steps.)
+    // Every load of the CTA in flight at once: each thread's state rows (the longest trip, into
+    // registers), the asynchronous copies of the steps' q, k, v, the commit count and the beta
+    // and gate scalars.
     float2 s[RPT][NP];
 #pragma unroll
     for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], srow0 + static_cast<size_t>(r[x]) * DK, g);
+    stage_raw<DK, THREADS>(raw, A, b, h, h / A.qk_group, row0, total);
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
-    uint16_t bg[2] = {0, 0};   // slots threadIdx.x and threadIdx.x + THREADS of (beta, gate) x step
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int bg_idx = threadIdx.x + q * THREADS;
-        if (bg_idx < 2 * total) {
-            long long row;
-            const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
-            bg[q] = (bg_idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
-        }
-    }
-    constexpr int VCH = ROWS_PER_CTA / 8;   // 16-byte chunks of a step's v slice
-    for (int idx = threadIdx.x; idx < total * VCH; idx += THREADS) {
-        const int t = idx / VCH, c = idx % VCH;
+    for (int idx = threadIdx.x; idx < 2 * total; idx += THREADS) {
         long long row;
-        const GdnStepsDev& src = step_src(A, b, t, &row);
-        const uint4 u = *reinterpret_cast<const uint4*>(piece(src, row, h, 0, DK, A.dv, row0, 2) + 8 * c);
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            steps[t].v[8 * c + 2 * e] = __uint_as_float(wd[e] << 16);
-            steps[t].v[8 * c + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+        const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
+        float x = bf16f((idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h]);
+        if (src.raw_gates) {
+            // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
+            if (idx & 1) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
+            else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
         }
+        if (idx & 1) steps[idx >> 1].gate = x;
+        else steps[idx >> 1].beta = x;
     }
-    normalise_all<DK>(steps, A, b, h, h / A.qk_group, total, A.l2 != 0);
     if (nc < 0 || nc > A.max_commit) {
         if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
     }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int bg_idx = threadIdx.x + q * THREADS;
-        if (bg_idx < 2 * total) {
-            long long row;
-            const GdnStepsDev& src = step_src(A, b, bg_idx >> 1, &row);
-            float x = bf16f(bg[q]);
-            if (src.raw_gates) {
-                // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
-                if (bg_idx & 1) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
-                else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
-            }
-            if (bg_idx & 1) steps[bg_idx >> 1].gate = x;
-            else steps[bg_idx >> 1].beta = x;
-        }
-    }
+    cp_async_wait_all();
+    __syncthreads();
+    normalise_all<DK, THREADS>(steps, raw, total, A.l2 != 0);
+    for (int idx = threadIdx.x; idx < total * SLAB; idx += THREADS)
+        steps[idx / SLAB].v[idx % SLAB] = bf16f(raw[idx / SLAB].v[idx % SLAB]);
     __syncthreads();
 
     float o[RPT];
     // replay the committed steps (these change the stored state)
     for (int t = 0; t < nc; ++t) {
-        gdn_step<DK>(s, steps[t], g, r, A.emit_replay != 0, o);
+        gdn_step<DK, RPT>(s, steps[t], g, r, A.emit_replay != 0, o);
         if (A.emit_replay && g == 0) {
 #pragma unroll
             for (int x = 0; x < RPT; ++x)
@@ -305,11 +324,12 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
                     make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
         }
     }
-    // speculative steps: outputs only, the state in memory stays committed (unrolled by 2 so
-    // that one step's output product can overlap the next step's decay and key product)
-#pragma unroll 2
+    // speculative steps: outputs only, the state in memory stays committed (with one row per
+    // thread unrolled by 2 so that one step's output product can overlap the next step's decay
+    // and key product; with several rows per thread those give the overlap)
+#pragma unroll(RPT == 1 ? 2 : 1)
     for (int t = 0; t < A.k; ++t) {
-        gdn_step<DK>(s, steps[A.max_commit + t], g, r, true, o);
+        gdn_step<DK, RPT>(s, steps[A.max_commit + t], g, r, true, o);
         if (g == 0) {
 #pragma unroll
             for (int x = 0; x < RPT; ++x)
@@ -317,6 +337,18 @@ __global__ void __launch_bounds__(THREADS, 4) gdn_kernel(GdnArgs A) {
                     f32_to_bf16(o[x]);
         }
     }
+}
+
+template <int DK, class T>
+xv_status launch_tiled(const GdnArgs& a, int B, int H, int dv, int total, cudaStream_t s) {
+    const size_t per_step = step_smem_bytes<DK>();
+    const int max_bytes = static_cast<int>(per_step * XV_GDN_MAX_STAGED);
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_kernel<DK, T>), max_bytes, true,
+                                        "gdn: set shared memory size"))
+        return st;
+    const dim3 grid(dv / SLAB, H, B);   // dv is a multiple of SLAB (checked)
+    launch_k(gdn_kernel<DK, T>, grid, dim3(T::THREADS), per_step * (total > 0 ? total : 1), s, a);
+    return XV_OK;
 }
 
 }  // namespace
@@ -330,24 +362,25 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
               qk_l2norm ? 1 : 0, H / Hk, err};
     const int max_steps = max_commit + k;
-    if (max_steps > THREADS) return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, THREADS);
-    dim3 grid(dv / ROWS_PER_CTA, H, B);   // dv is a multiple of ROWS_PER_CTA (checked)
-    // as much shared memory as possible for the carveout: several CTAs per SM at B = 8; up to
-    // THREADS staged steps (a prefill chunk of XV_KMAX positions after as many pending ones)
-    {
-        const void* fn = dk == 128 ? reinterpret_cast<const void*>(gdn_kernel<128>)
-                                   : reinterpret_cast<const void*>(gdn_kernel<64>);
-        const int bytes = static_cast<int>(dk == 128 ? sizeof(StepSmem<128>) * THREADS : sizeof(StepSmem<64>) * THREADS);
-        if (xv_status st = kernel_smem_once(fn, bytes, true, "gdn: set shared memory size")) return st;
-    }
+    if (max_steps > XV_GDN_MAX_STAGED)
+        return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, XV_GDN_MAX_STAGED);
+    // Slabs of 32 rows: with at least two per SM the wide tiling (4 rows per thread, one warp per
+    // slab) reads each k and q slice once for four rows; below that the narrow one (one row per
+    // thread, four warps per slab) keeps more warps per SM on the latency-bound chain.  Every row's
+    // arithmetic is the same in both.
+    int sms = 0;
+    if (xv_status st = device_sm_count(&sms)) return st;
+    const long long slabs = static_cast<long long>(B) * H * (dv / SLAB);
+    const bool wide = slabs >= 2ll * sms;
     trace_pre(s);
-    if (dk == 128) {
-        const size_t sm = sizeof(StepSmem<128>) * (max_steps > 0 ? max_steps : 1);
-        launch_k(gdn_kernel<128>, dim3(grid), dim3(THREADS), sm, s, a);
-    } else {
-        const size_t sm = sizeof(StepSmem<64>) * (max_steps > 0 ? max_steps : 1);
-        launch_k(gdn_kernel<64>, dim3(grid), dim3(THREADS), sm, s, a);
-    }
+    xv_status st;
+    if (dk == 128)
+        st = wide ? launch_tiled<128, WideTiling>(a, B, H, dv, max_steps, s)
+                  : launch_tiled<128, NarrowTiling>(a, B, H, dv, max_steps, s);
+    else
+        st = wide ? launch_tiled<64, WideTiling>(a, B, H, dv, max_steps, s)
+                  : launch_tiled<64, NarrowTiling>(a, B, H, dv, max_steps, s);
+    if (st) return st;
     // algorithmic bytes with every sequence replaying max_commit steps: the state
     // read (and written back after a replay), the step inputs, the outputs
     const long long state_bytes = 4ll * B * H * dv * dk;

@@ -93,6 +93,8 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
                       int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part = nullptr, int* defer_S = nullptr);
 
 // ---- GDN (gdn.cu)
+// Steps one GDN call stages: up to XV_KMAX replayed ones and XV_KMAX speculative ones.
+constexpr int XV_GDN_MAX_STAGED = 2 * XV_KMAX;
 struct GdnStepsDev {
     const uint16_t* q;
     const uint16_t* k;

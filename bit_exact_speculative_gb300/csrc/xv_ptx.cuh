@@ -38,6 +38,13 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // (a no-op when the kernel was launched without the programmatic attribute).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ------------------------------------------------------- cp.async (16 B)
+// One 16-byte global -> shared copy through L2 (not L1), completed by cp_async_wait_all().
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

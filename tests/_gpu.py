@@ -5,10 +5,11 @@ Tolerances (stated once, used everywhere):
   - fp32 GDN state vs the oracle (same bf16 inputs on both sides):
     max_i |d_i| / max(|ref_i|, RMS(ref)) <= 1e-4;
   - fp32 logits of the whole block vs the oracle's sequential decode:
-    RMS(err) <= 3 * RMS(spread) and max|err| <= 3 * max|spread|, where spread
-    is the oracle's own single-precision evaluation minus its double one on
-    the same inputs (the same rows, extended on the tiny blocks to 16
-    positions of the same sequence).  A block output has passed through ~8
+    every row's RMS(err) <= 3 * the largest row RMS(spread) and max|err| <=
+    3 * max|spread|, where spread is the oracle's own single-precision
+    evaluation minus its double one on the same inputs (the same rows,
+    extended on the tiny blocks to 64 positions of the same sequence, whose
+    few rounding flips per row otherwise leave rows without any).  A block output has passed through ~8
     bf16 storage points per layer; a value that lands within the fp32
     accumulation error of a bf16 rounding boundary rounds the other way in
     any fp32 evaluation, and those 1-ulp differences propagate: the spread
@@ -82,10 +83,12 @@ def assert_block_close(got, ref, spread, what=""):
     r = np.asarray(ref, dtype=np.float64)
     sp = np.asarray(spread, dtype=np.float64)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
-    rms_bound, max_bound = SPREAD_FACTOR * rms(sp), SPREAD_FACTOR * float(np.max(np.abs(sp)))
+    row_rms = lambda x: np.sqrt(np.mean(x.reshape(x.shape[0], -1) ** 2, axis=1))
+    rms_bound, max_bound = SPREAD_FACTOR * float(row_rms(sp).max()), SPREAD_FACTOR * float(np.max(np.abs(sp)))
     assert rms_bound > 0 and max_bound > 0, f"{what}: degenerate spread"
-    e = np.abs(g - r)
-    assert rms(e) <= rms_bound, f"{what}: RMS err {rms(e):.3e} > {SPREAD_FACTOR} * RMS(spread) = {rms_bound:.3e}"
+    e = np.abs(g - r).reshape(g.shape[0] if g.ndim > 1 else 1, -1)
+    worst = float(row_rms(e).max())
+    assert worst <= rms_bound, f"{what}: row RMS err {worst:.3e} > {SPREAD_FACTOR} * max row RMS(spread) = {rms_bound:.3e}"
     assert e.max() <= max_bound, f"{what}: max err {e.max():.3e} > {SPREAD_FACTOR} * max|spread| = {max_bound:.3e}"
     return max_bound
 
