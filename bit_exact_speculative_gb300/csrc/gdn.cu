@@ -25,17 +25,23 @@
 // thread, warp or CTA holds it.
 //
 // Tiling (free, chosen per launch): a thread holds RPT rows (rows lane/4,
-// lane/4 + 8, ... of its warp's 8 * RPT), a CTA WARPS warps.  Every step reads
-// the whole k and q vectors from shared memory into each row's lanes; with
-// one row per thread that read (1 KB per row per step) is the bound, so wide
-// launches hold 4 rows per thread and read each slice once for the four.  The
-// state lives in registers across all replay and speculative steps; it is
-// read once (plain loads issued first) and, after a replay, written once.
-// The step inputs (per step: q and k of the head, this CTA's slice of v, beta
-// and gate) are staged by 16-byte asynchronous copies spread over the CTA's
-// threads and issued together with the state loads, so the whole verify's
-// inputs arrive in a single round trip without holding registers; q and k are
-// then L2-normalised by 4 threads per vector into fp32.
+// lane/4 + 8, ... of its warp's 8 * RPT), a CTA WARPS warps, and a CTA owns one
+// slab of 32 rows of one head.  Every step reads the whole k and q vectors
+// from shared memory into each row's lanes; with one row per thread that read
+// (1 KB per row per step) is the bound, so wide launches hold 4 rows per
+// thread and read each slice once for the four.
+//
+// Data movement: everything a CTA reads arrives by bulk asynchronous copies on
+// one mbarrier, issued by all threads right after the dependency wait: its
+// 16 KB slab of the state (contiguous rows) and, per staged step, the raw q and
+// k of its head and its slice of v.  Plain per-thread loads of the state, one
+// 16-byte piece at a time, queued behind each other in the load/store unit
+// and held the shared-memory traffic of the steps behind them.  The state then
+// lives in registers across all replay and speculative steps; after a replay
+// it goes back through shared memory and one bulk store, and the outputs of
+// every step are gathered in shared memory and written in 16-byte pieces at
+// the end.  q and k are L2-normalised in place (the raw bf16 vector lands in
+// the upper half of its fp32 array) by 4 threads per vector.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
@@ -73,10 +79,11 @@ struct GdnArgs {
     long long o_stride;
     int H, dv, l2, qk_group;
     unsigned* err;
+    int o_vec;   // o and o_stride allow 16-byte stores
 };
 
-// Per-step inputs staged in shared memory: q and k (fp32, normalised), this CTA's v entries,
-// beta and gate; and the raw bf16 q, k, v the asynchronous copies land in.
+// Per-step inputs staged in shared memory: q and k (fp32, normalised; their raw bf16 copies land in
+// the upper halves), this CTA's v entries, beta and gate.
 template <int DK>
 struct StepSmem {
     float q[DK];
@@ -85,14 +92,21 @@ struct StepSmem {
     float beta, gate;
     float pad[2];
 };
+static_assert(sizeof(StepSmem<128>) % 16 == 0 && sizeof(StepSmem<64>) % 16 == 0, "16-byte aligned steps");
+
+// Shared-memory plan of a CTA: the state slab, the staged steps, the raw v slices, the outputs of
+// every step (replayed ones first when they are emitted), the mbarrier.
 template <int DK>
-struct RawStep {
-    uint16_t q[DK];
-    uint16_t k[DK];
-    uint16_t v[SLAB];
+struct GdnSmem {
+    size_t steps, rawv, obuf, bar, total;
+    __host__ __device__ GdnSmem(int n_steps, int n_out) {
+        steps = static_cast<size_t>(SLAB) * DK * 4;
+        rawv = steps + sizeof(StepSmem<DK>) * n_steps;
+        obuf = rawv + static_cast<size_t>(SLAB) * 2 * n_steps;
+        bar = (obuf + static_cast<size_t>(SLAB) * 2 * n_out + 15) & ~static_cast<size_t>(15);
+        total = bar + 16;
+    }
 };
-template <int DK>
-constexpr size_t step_smem_bytes() { return sizeof(StepSmem<DK>) + sizeof(RawStep<DK>); }
 
 // Source of staged slot t for sequence b: slots [0, max_commit) hold pending rows 0.., slots
 // [max_commit, max_commit + k) the draft rows.  All are staged whatever n_commit[b] is, so
@@ -108,47 +122,22 @@ __device__ __forceinline__ const GdnStepsDev& step_src(const GdnArgs& A, int b, 
 
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
-// Issues the asynchronous copies of every staged step's raw q, k (of q/k head hk) and this
-// CTA's v slice (rows row0.., of v head h): 16-byte pieces spread over the CTA's threads.
+// Vector w of the staged steps (step w / 2; q for even w, k for odd) from its raw bf16 copy (upper
+// half of the fp32 array) to fp32 in place, L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)):
+// thread j of the vector's group of NORM_LANES takes elements [j DK/4, (j+1) DK/4), sums their
+// squares in four interleaved chains (e mod 4) added as (c0 + c1) + (c2 + c3), the group adds its
+// partials by an xor tree (1, 2), and every thread scales its own elements.
 template <int DK, int THREADS>
-__device__ __forceinline__ void stage_raw(RawStep<DK>* raw, const GdnArgs& A, int b, int h, int hk, int row0,
-                                          int total) {
-    constexpr int QC = DK / 8, VC = SLAB / 8, PER_STEP = 2 * QC + VC;
-    for (int idx = threadIdx.x; idx < total * PER_STEP; idx += THREADS) {
-        const int t = idx / PER_STEP, c = idx % PER_STEP;
-        long long row;
-        const GdnStepsDev& src = step_src(A, b, t, &row);
-        const uint16_t* g;
-        uint16_t* d;
-        if (c < QC) {
-            g = src.q + row * src.qkv_stride + static_cast<long long>(hk) * DK + 8 * c;
-            d = raw[t].q + 8 * c;
-        } else if (c < 2 * QC) {
-            g = src.k + row * src.qkv_stride + static_cast<long long>(hk) * DK + 8 * (c - QC);
-            d = raw[t].k + 8 * (c - QC);
-        } else {
-            g = src.v + row * src.qkv_stride + static_cast<long long>(h) * A.dv + row0 + 8 * (c - 2 * QC);
-            d = raw[t].v + 8 * (c - 2 * QC);
-        }
-        cp_async16(d, g);
-    }
-}
-
-// Vector w of the staged steps (step w / 2; q for even w, k for odd) from its raw bf16 copy to
-// fp32, L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)): thread j of the vector's group of
-// NORM_LANES takes elements [j DK/4, (j+1) DK/4), sums their squares in four interleaved chains
-// (e mod 4) added as (c0 + c1) + (c2 + c3), the group adds its partials by an xor tree (1, 2),
-// and every thread scales its own elements.
-template <int DK, int THREADS>
-__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const RawStep<DK>* raw, int total, bool l2) {
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bool l2) {
     constexpr int PART = DK / NORM_LANES;
     const int jl = threadIdx.x % NORM_LANES;
     for (int w0 = 0; w0 < 2 * total; w0 += THREADS / NORM_LANES) {   // same trip count for every thread
         const int w = w0 + static_cast<int>(threadIdx.x) / NORM_LANES;
         const bool act = w < 2 * total;
         const int t = act ? w >> 1 : 0;
-        const uint16_t* x = ((w & 1) ? raw[t].k : raw[t].q) + jl * PART;
-        float* y = ((w & 1) ? steps[t].k : steps[t].q) + jl * PART;
+        float* y = (w & 1) ? steps[t].k : steps[t].q;
+        const uint16_t* x = reinterpret_cast<const uint16_t*>(y + DK / 2) + jl * PART;
+        y += jl * PART;
         float f[PART];
 #pragma unroll
         for (int c = 0; c < PART / 8; ++c) {
@@ -175,6 +164,7 @@ __device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const RawStep
             ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
             inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ss, 1e-6f)));
         }
+        __syncwarp();   // the group's raw halves are read before any fp32 element overwrites them
         if (!act) continue;
 #pragma unroll
         for (int e = 0; e < PART; e += 4)
@@ -183,6 +173,17 @@ __device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const RawStep
                                  __fmul_rn(f[e + 3], inv))
                    : make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
     }
+}
+
+// beta = bf16(sigmoid(b)) (odd idx: gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20)
+// from the raw projection column when the source holds raw values, else the bf16 value itself.
+__device__ __forceinline__ float gate_value(uint16_t raw, bool is_gate, bool raw_gates) {
+    float x = bf16f(raw);
+    if (raw_gates) {
+        if (is_gate) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
+        else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
+    }
+    return x;
 }
 
 // Sum over the LPR lanes of a row (xor 1, 2): every lane gets the same bits.
@@ -256,72 +257,111 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
     griddep_launch();
     constexpr int NP = DK / (2 * LPR);
     constexpr int RPT = T::RPT, THREADS = T::THREADS;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     const int total = A.max_commit + A.k;
-    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw);
-    RawStep<DK>* raw = reinterpret_cast<RawStep<DK>*>(smem_raw + sizeof(StepSmem<DK>) * (total > 0 ? total : 1));
+    const int n_out = A.k + (A.emit_replay ? A.max_commit : 0);
+    const GdnSmem<DK> L(total, n_out);
+    float* sstate = reinterpret_cast<float*>(smem_raw);
+    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw + L.steps);
+    uint16_t* rawv = reinterpret_cast<uint16_t*>(smem_raw + L.rawv);
+    uint16_t* obuf = reinterpret_cast<uint16_t*>(smem_raw + L.obuf);
+    const uint32_t bar = smem_u32(smem_raw + L.bar);
 
-    const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / A.qk_group;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane % LPR;
     int r[RPT];                                           // rows within the slab
 #pragma unroll
     for (int x = 0; x < RPT; ++x) r[x] = warp * T::ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
     const int row0 = slab * SLAB;
-    float* srow0 = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0) * DK;
-    if (threadIdx.x == 0) l2_prefetch(srow0, SLAB * DK * 4);   // a hint only: the loads come after the wait
+    float* gslab = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0) * DK;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        l2_prefetch(gslab, SLAB * DK * 4);   // a hint only: the copies come after the wait
+    }
+    __syncthreads();
     griddep_wait();
 
-    // Every load of the CTA in flight at once: each thread's state rows (the longest trip, into
-    // registers), the asynchronous copies of the steps' q, k, v, the commit count and the beta
-    // and gate scalars.
-    float2 s[RPT][NP];
-#pragma unroll
-    for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], srow0 + static_cast<size_t>(r[x]) * DK, g);
-    stage_raw<DK, THREADS>(raw, A, b, h, h / A.qk_group, row0, total);
-    int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
-    for (int idx = threadIdx.x; idx < 2 * total; idx += THREADS) {
-        long long row;
-        const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
-        float x = bf16f((idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h]);
-        if (src.raw_gates) {
-            // beta = bf16(sigmoid(b)), gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20
-            if (idx & 1) x = bf16f(f32_to_bf16(expf(-(x > 20.f ? x : log1pf(expf(x))))));
-            else x = bf16f(f32_to_bf16(__frcp_rn(__fadd_rn(1.f, expf(-x)))));
+    // Every copy of the CTA in flight at once, spread over its threads: the state slab, then per
+    // staged step its raw q and k (into the upper halves of the fp32 arrays) and its v slice.
+    // The beta and gate scalars and the commit count are plain loads issued alongside.
+    constexpr uint32_t QK_BYTES = DK * 2, V_BYTES = SLAB * 2;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, SLAB * DK * 4 + total * (2 * QK_BYTES + V_BYTES));
+    for (int c = threadIdx.x; c < 1 + 3 * total; c += THREADS) {
+        if (c == 0) {
+            bulk_load(smem_u32(sstate), gslab, SLAB * DK * 4, bar);
+            continue;
         }
-        if (idx & 1) steps[idx >> 1].gate = x;
-        else steps[idx >> 1].beta = x;
+        const int t = (c - 1) / 3, which = (c - 1) % 3;
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, t, &row);
+        const long long base = row * src.qkv_stride;
+        if (which == 0)
+            bulk_load(smem_u32(steps[t].q + DK / 2), src.q + base + static_cast<long long>(hk) * DK, QK_BYTES, bar);
+        else if (which == 1)
+            bulk_load(smem_u32(steps[t].k + DK / 2), src.k + base + static_cast<long long>(hk) * DK, QK_BYTES, bar);
+        else
+            bulk_load(smem_u32(rawv + t * SLAB), src.v + base + static_cast<long long>(h) * A.dv + row0, V_BYTES, bar);
     }
+    uint16_t bg[2] = {0, 0};   // entries threadIdx.x and threadIdx.x + THREADS of (beta, gate) x step
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int idx = threadIdx.x + q * THREADS;
+        if (idx < 2 * total) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
+            bg[q] = (idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
+        }
+    }
+    int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
     if (nc < 0 || nc > A.max_commit) {
         if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
     }
-    cp_async_wait_all();
-    __syncthreads();
-    normalise_all<DK, THREADS>(steps, raw, total, A.l2 != 0);
-    for (int idx = threadIdx.x; idx < total * SLAB; idx += THREADS)
-        steps[idx / SLAB].v[idx % SLAB] = bf16f(raw[idx / SLAB].v[idx % SLAB]);
+    mbar_wait(bar, 0, A.err);
+
+    normalise_all<DK, THREADS>(steps, total, A.l2 != 0);
+    for (int idx = threadIdx.x; idx < total * SLAB; idx += THREADS) steps[idx / SLAB].v[idx % SLAB] = bf16f(rawv[idx]);
+    for (int idx = threadIdx.x; idx < 2 * total; idx += THREADS) {
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
+        const uint16_t raw = idx < 2 * THREADS ? (idx >= THREADS ? bg[1] : bg[0])
+                                               : ((idx & 1) ? src.gate[row * src.gate_stride + h]
+                                                            : src.beta[row * src.gate_stride + h]);
+        const float x = gate_value(raw, idx & 1, src.raw_gates != 0);
+        if (idx & 1) steps[idx >> 1].gate = x;
+        else steps[idx >> 1].beta = x;
+    }
+    float2 s[RPT][NP];
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], sstate + r[x] * DK, g);
     __syncthreads();
 
     float o[RPT];
     // replay the committed steps (these change the stored state)
+    const int orow_spec = A.emit_replay ? nc : 0;
     for (int t = 0; t < nc; ++t) {
         gdn_step<DK, RPT>(s, steps[t], g, r, A.emit_replay != 0, o);
         if (A.emit_replay && g == 0) {
 #pragma unroll
-            for (int x = 0; x < RPT; ++x)
-                A.o[(static_cast<long long>(b) * nc + t) * A.o_stride + static_cast<long long>(h) * A.dv + row0 + r[x]] =
-                    f32_to_bf16(o[x]);
+            for (int x = 0; x < RPT; ++x) obuf[t * SLAB + r[x]] = f32_to_bf16(o[x]);
         }
     }
     if (nc > 0) {
+        // the committed state goes back through shared memory and one bulk store
 #pragma unroll
         for (int x = 0; x < RPT; ++x) {
-            float* srow = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0 + r[x]) * DK;
 #pragma unroll
             for (int u = 0; u < NP / 2; ++u)
-                *reinterpret_cast<float4*>(srow + 4 * (g + LPR * u)) =
+                *reinterpret_cast<float4*>(sstate + r[x] * DK + 4 * (g + LPR * u)) =
                     make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bulk_store(gslab, smem_u32(sstate), SLAB * DK * 4);
+            bulk_commit();
         }
     }
     // speculative steps: outputs only, the state in memory stays committed (with one row per
@@ -332,22 +372,42 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
         gdn_step<DK, RPT>(s, steps[A.max_commit + t], g, r, true, o);
         if (g == 0) {
 #pragma unroll
-            for (int x = 0; x < RPT; ++x)
-                A.o[(static_cast<long long>(b) * A.k + t) * A.o_stride + static_cast<long long>(h) * A.dv + row0 + r[x]] =
-                    f32_to_bf16(o[x]);
+            for (int x = 0; x < RPT; ++x) obuf[(orow_spec + t) * SLAB + r[x]] = f32_to_bf16(o[x]);
         }
     }
+    __syncthreads();
+    // outputs: row t of the buffer is the slab's 32 values of output row (b, t) (replayed rows
+    // first when emitted, then the speculative ones), 16 bytes per thread
+    const int rows_out = orow_spec + A.k;
+    constexpr int CH = SLAB / 8;
+    for (int idx = threadIdx.x; idx < rows_out * CH; idx += THREADS) {
+        const int t = idx / CH, c = idx % CH;
+        const long long orow = t < orow_spec ? static_cast<long long>(b) * nc + t
+                                             : static_cast<long long>(b) * A.k + (t - orow_spec);
+        uint16_t* dst = A.o + orow * A.o_stride + static_cast<long long>(h) * A.dv + row0 + 8 * c;
+        const uint4 v = *reinterpret_cast<const uint4*>(obuf + t * SLAB + 8 * c);
+        if (A.o_vec) {
+            *reinterpret_cast<uint4*>(dst) = v;
+        } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dst[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+                dst[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+            }
+        }
+    }
+    if (nc > 0 && threadIdx.x == 0) bulk_wait_read();   // the state slab stays in shared memory until read
 }
 
 template <int DK, class T>
-xv_status launch_tiled(const GdnArgs& a, int B, int H, int dv, int total, cudaStream_t s) {
-    const size_t per_step = step_smem_bytes<DK>();
-    const int max_bytes = static_cast<int>(per_step * XV_GDN_MAX_STAGED);
-    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_kernel<DK, T>), max_bytes, true,
-                                        "gdn: set shared memory size"))
+xv_status launch_tiled(const GdnArgs& a, int B, int H, int dv, int total, int n_out, cudaStream_t s) {
+    const GdnSmem<DK> most(XV_GDN_MAX_STAGED, XV_GDN_MAX_STAGED);
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_kernel<DK, T>), static_cast<int>(most.total),
+                                        true, "gdn: set shared memory size"))
         return st;
     const dim3 grid(dv / SLAB, H, B);   // dv is a multiple of SLAB (checked)
-    launch_k(gdn_kernel<DK, T>, grid, dim3(T::THREADS), per_step * (total > 0 ? total : 1), s, a);
+    launch_k(gdn_kernel<DK, T>, grid, dim3(T::THREADS), GdnSmem<DK>(total, n_out).total, s, a);
     return XV_OK;
 }
 
@@ -359,9 +419,11 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "gdn: device error word unavailable");
     if (Hk < 1 || H % Hk) return fail(XV_ERR_ARG, "gdn: %d v heads are not a multiple of %d q/k heads", H, Hk);
+    if (!aligned16(state)) return fail(XV_ERR_UNSUPPORTED, "gdn: the state must be 16-byte aligned");
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
-              qk_l2norm ? 1 : 0, H / Hk, err};
+              qk_l2norm ? 1 : 0, H / Hk, err, (aligned16(o) && o_stride % 8 == 0) ? 1 : 0};
     const int max_steps = max_commit + k;
+    const int n_out = k + (emit_replay ? max_commit : 0);
     if (max_steps > XV_GDN_MAX_STAGED)
         return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, XV_GDN_MAX_STAGED);
     // Slabs of 32 rows: with at least two per SM the wide tiling (4 rows per thread, one warp per
@@ -375,11 +437,11 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     trace_pre(s);
     xv_status st;
     if (dk == 128)
-        st = wide ? launch_tiled<128, WideTiling>(a, B, H, dv, max_steps, s)
-                  : launch_tiled<128, NarrowTiling>(a, B, H, dv, max_steps, s);
+        st = wide ? launch_tiled<128, WideTiling>(a, B, H, dv, max_steps, n_out, s)
+                  : launch_tiled<128, NarrowTiling>(a, B, H, dv, max_steps, n_out, s);
     else
-        st = wide ? launch_tiled<64, WideTiling>(a, B, H, dv, max_steps, s)
-                  : launch_tiled<64, NarrowTiling>(a, B, H, dv, max_steps, s);
+        st = wide ? launch_tiled<64, WideTiling>(a, B, H, dv, max_steps, n_out, s)
+                  : launch_tiled<64, NarrowTiling>(a, B, H, dv, max_steps, n_out, s);
     if (st) return st;
     // algorithmic bytes with every sequence replaying max_commit steps: the state
     // read (and written back after a replay), the step inputs, the outputs
