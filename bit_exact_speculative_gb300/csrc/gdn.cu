@@ -24,21 +24,25 @@
 // lane ends with the same bits.  Nothing a row computes depends on which
 // thread, warp or CTA holds it.
 //
-// Tiling (free, chosen per launch): a thread holds RPT rows (rows lane/4,
-// lane/4 + 8, ... of its warp's 8 * RPT), a CTA WARPS warps, and a CTA owns one
-// slab of 32 rows of one head.  Every step reads the whole k and q vectors
-// from shared memory into each row's lanes; with one row per thread that read
-// (1 KB per row per step) is the bound, so wide launches hold 4 rows per
-// thread and read each slice once for the four.
+// Tiling (free, chosen per launch): a "team" of threads owns one slab of 32
+// state rows of one head; a thread holds RPT rows of it (rows lane/4,
+// lane/4 + 8, ... of its warp's 8 * RPT).  Every step reads the whole k and q
+// vectors from shared memory into each row's lanes; with one row per thread
+// that read (1 KB per row per step) is the bound, so wide launches hold 4 rows
+// per thread (a team is one warp) and read each slice once for the four.  A
+// wide CTA holds several such warps, each with its own slab, barrier and
+// staging, and there is at most one CTA per SM, so the whole call is one wave;
+// a narrow CTA (few slabs: a latency-bound call) is one team of 4 warps with
+// one row per thread.
 //
-// Data movement: everything a CTA reads arrives by bulk asynchronous copies on
-// one mbarrier, issued by all threads right after the dependency wait: its
-// 16 KB slab of the state (contiguous rows) and, per staged step, the raw q and
-// k of its head and its slice of v.  Plain per-thread loads of the state, one
-// 16-byte piece at a time, queued behind each other in the load/store unit
-// and held the shared-memory traffic of the steps behind them.  The state then
-// lives in registers across all replay and speculative steps; after a replay
-// it goes back through shared memory and one bulk store, and the outputs of
+// Data movement: everything a team reads arrives by bulk asynchronous copies
+// on one mbarrier, issued right after the dependency wait: its 16 KB slab of
+// the state (contiguous rows) and, per staged step, the raw q and k of its
+// head and its slice of v.  (Plain per-thread loads of the state, one 16-byte
+// piece at a time, queued behind each other in the load/store unit and held
+// the shared-memory traffic of the steps behind them.)  The state then lives
+// in registers across all replay and speculative steps; after a replay it
+// goes back through shared memory and one bulk store, and the outputs of
 // every step are gathered in shared memory and written in 16-byte pieces at
 // the end.  q and k are L2-normalised in place (the raw bf16 vector lands in
 // the upper half of its fp32 array) by 4 threads per vector.
@@ -50,21 +54,19 @@ namespace xv {
 namespace {
 constexpr int LPR = 4;                          // lanes per state row
 constexpr int NORM_LANES = 4;                   // threads per q or k vector in the normalisation
+constexpr int SLAB = 32;                        // state rows per team
+constexpr int MAX_TEAMS = 8;                    // slabs (warps) per wide CTA
 
-// A launch shape: RPT state rows per thread, WARPS warps per CTA, at least MIN_BLOCKS CTAs per SM.
-template <int RPT_, int WARPS_, int MIN_BLOCKS_>
+// A launch shape: RPT state rows per thread, TEAM threads per slab.
+template <int RPT_>
 struct Tiling {
     static constexpr int RPT = RPT_;
-    static constexpr int WARPS = WARPS_;
-    static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
+    static constexpr int TEAM = SLAB * LPR / RPT;        // threads sharing one slab
     static constexpr int ROWS_PER_WARP = 32 / LPR * RPT;
-    static constexpr int ROWS = ROWS_PER_WARP * WARPS;   // state rows per CTA
-    static constexpr int THREADS = 32 * WARPS;
 };
-using NarrowTiling = Tiling<1, 4, 4>;   // 32 rows, 128 threads: few CTAs (latency-bound launches)
-using WideTiling = Tiling<4, 1, 8>;     // 32 rows, 32 threads: many CTAs (shared-memory reads amortised)
-static_assert(NarrowTiling::ROWS == WideTiling::ROWS, "both tilings cut a head into the same slabs");
-constexpr int SLAB = NarrowTiling::ROWS;
+using NarrowTiling = Tiling<1>;   // 128 threads per slab, one CTA each: few slabs (latency-bound calls)
+using WideTiling = Tiling<4>;     // one warp per slab, up to MAX_TEAMS per CTA: shared-memory reads amortised
+static_assert(WideTiling::TEAM == 32, "a wide team is one warp");
 
 struct GdnArgs {
     float* state;
@@ -79,23 +81,24 @@ struct GdnArgs {
     long long o_stride;
     int H, dv, l2, qk_group;
     unsigned* err;
-    int o_vec;   // o and o_stride allow 16-byte stores
+    int o_vec;     // o and o_stride allow 16-byte stores
+    int n_slabs;   // B * H * dv / SLAB
+    int teams;     // slabs per CTA (blockDim.x / TEAM)
 };
 
 // Per-step inputs staged in shared memory: q and k (fp32, normalised; their raw bf16 copies land in
-// the upper halves), this CTA's v entries, beta and gate.
+// the upper halves), beta and gate.
 template <int DK>
 struct StepSmem {
     float q[DK];
     float k[DK];
-    float v[SLAB];
     float beta, gate;
     float pad[2];
 };
 static_assert(sizeof(StepSmem<128>) % 16 == 0 && sizeof(StepSmem<64>) % 16 == 0, "16-byte aligned steps");
 
-// Shared-memory plan of a CTA: the state slab, the staged steps, the raw v slices, the outputs of
-// every step (replayed ones first when they are emitted), the mbarrier.
+// Shared-memory plan of one team: the state slab, the staged steps, the raw v slices, the outputs
+// of every step (replayed ones first when they are emitted), the mbarrier.
 template <int DK>
 struct GdnSmem {
     size_t steps, rawv, obuf, bar, total;
@@ -104,7 +107,7 @@ struct GdnSmem {
         rawv = steps + sizeof(StepSmem<DK>) * n_steps;
         obuf = rawv + static_cast<size_t>(SLAB) * 2 * n_steps;
         bar = (obuf + static_cast<size_t>(SLAB) * 2 * n_out + 15) & ~static_cast<size_t>(15);
-        total = bar + 16;
+        total = (bar + 16 + 127) & ~static_cast<size_t>(127);
     }
 };
 
@@ -122,31 +125,38 @@ __device__ __forceinline__ const GdnStepsDev& step_src(const GdnArgs& A, int b, 
 
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
+// Synchronises the threads of a team: a wide team is one warp, a narrow one the whole CTA.
+template <int TEAM>
+__device__ __forceinline__ void team_sync() {
+    if constexpr (TEAM == 32) __syncwarp();
+    else __syncthreads();
+}
+
 // Vector w of the staged steps (step w / 2; q for even w, k for odd) from its raw bf16 copy (upper
 // half of the fp32 array) to fp32 in place, L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)):
-// thread j of the vector's group of NORM_LANES takes elements [j DK/4, (j+1) DK/4), sums their
-// squares in four interleaved chains (e mod 4) added as (c0 + c1) + (c2 + c3), the group adds its
-// partials by an xor tree (1, 2), and every thread scales its own elements.
-template <int DK, int THREADS>
-__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bool l2) {
-    constexpr int PART = DK / NORM_LANES;
-    const int jl = threadIdx.x % NORM_LANES;
-    for (int w0 = 0; w0 < 2 * total; w0 += THREADS / NORM_LANES) {   // same trip count for every thread
-        const int w = w0 + static_cast<int>(threadIdx.x) / NORM_LANES;
+// thread j of the vector's group of NORM_LANES takes the 16-byte raw pieces j, j + 4, j + 8, ...
+// (8 elements each, so the group's reads and writes fall in distinct banks), sums their squares
+// in four interleaved chains (element index mod 4) added as (c0 + c1) + (c2 + c3), the group adds
+// its partials by an xor tree (1, 2), and every thread scales its own elements.
+template <int DK, int TEAM>
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bool l2, int tid) {
+    constexpr int PIECES = DK / 8 / NORM_LANES;   // raw 16-byte pieces per thread
+    const int jl = tid % NORM_LANES;
+    for (int w0 = 0; w0 < 2 * total; w0 += TEAM / NORM_LANES) {   // same trip count for every thread
+        const int w = w0 + tid / NORM_LANES;
         const bool act = w < 2 * total;
         const int t = act ? w >> 1 : 0;
         float* y = (w & 1) ? steps[t].k : steps[t].q;
-        const uint16_t* x = reinterpret_cast<const uint16_t*>(y + DK / 2) + jl * PART;
-        y += jl * PART;
-        float f[PART];
+        const uint16_t* x = reinterpret_cast<const uint16_t*>(y + DK / 2);
+        float f[8 * PIECES];
 #pragma unroll
-        for (int c = 0; c < PART / 8; ++c) {
-            const uint4 u = *reinterpret_cast<const uint4*>(x + 8 * c);
+        for (int i = 0; i < PIECES; ++i) {
+            const uint4 u = *reinterpret_cast<const uint4*>(x + 8 * (jl + NORM_LANES * i));
             const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                f[8 * c + 2 * e] = __uint_as_float(wd[e] << 16);
-                f[8 * c + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+                f[8 * i + 2 * e] = __uint_as_float(wd[e] << 16);
+                f[8 * i + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
             }
         }
         float inv = 1.f;
@@ -155,7 +165,7 @@ __device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bo
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) c[q4] = __fmul_rn(f[q4], f[q4]);
 #pragma unroll
-            for (int e = 4; e < PART; e += 4) {
+            for (int e = 4; e < 8 * PIECES; e += 4) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) c[q4] = __fmaf_rn(f[e + q4], f[e + q4], c[q4]);
             }
@@ -167,15 +177,23 @@ __device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bo
         __syncwarp();   // the group's raw halves are read before any fp32 element overwrites them
         if (!act) continue;
 #pragma unroll
-        for (int e = 0; e < PART; e += 4)
-            *reinterpret_cast<float4*>(y + e) =
-                l2 ? make_float4(__fmul_rn(f[e], inv), __fmul_rn(f[e + 1], inv), __fmul_rn(f[e + 2], inv),
-                                 __fmul_rn(f[e + 3], inv))
-                   : make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        for (int i = 0; i < PIECES; ++i) {
+            float* d = y + 8 * (jl + NORM_LANES * i);
+            const float* v = f + 8 * i;
+            if (l2) {
+                *reinterpret_cast<float4*>(d) =
+                    make_float4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
+                *reinterpret_cast<float4*>(d + 4) =
+                    make_float4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
+            } else {
+                *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        }
     }
 }
 
-// beta = bf16(sigmoid(b)) (odd idx: gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20)
+// beta = bf16(sigmoid(b)) (is_gate: gate = bf16(exp(-softplus(a))), softplus(x) = x for x > 20)
 // from the raw projection column when the source holds raw values, else the bf16 value itself.
 __device__ __forceinline__ float gate_value(uint16_t raw, bool is_gate, bool raw_gates) {
     float x = bf16f(raw);
@@ -224,8 +242,8 @@ __device__ __forceinline__ void load_slice(float2 (&d)[DK / (2 * LPR)], const fl
 //   S <- a S;  r = S k;  u = beta (v - r);  S <- S + u k^T;  o = S q
 // each operation rounded once (packed f32x2 lanes are independent IEEE fp32 ops).
 template <int DK, int RPT>
-__device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const StepSmem<DK>& in, int g,
-                                         const int (&r)[RPT], bool want_o, float (&o)[RPT]) {
+__device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const StepSmem<DK>& in,
+                                         const uint16_t* v, int g, const int (&r)[RPT], bool want_o, float (&o)[RPT]) {
     constexpr int NP = DK / (2 * LPR);
     float2 kk[NP];
     load_slice<DK>(kk, in.k, g);
@@ -240,7 +258,7 @@ __device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const
     for (int x = 0; x < RPT; ++x) rr[x] = slice_dot<NP>(s[x], kk);
 #pragma unroll
     for (int x = 0; x < RPT; ++x) {
-        const float uu = __fmul_rn(in.beta, __fsub_rn(in.v[r[x]], rr[x]));
+        const float uu = __fmul_rn(in.beta, __fsub_rn(bf16f(v[r[x]]), rr[x]));
         const float2 u2 = make_float2(uu, uu);
 #pragma unroll
         for (int j = 0; j < NP; ++j) s[x][j] = __ffma2_rn(u2, kk[j], s[x][j]);
@@ -253,42 +271,48 @@ __device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const
 }
 
 template <int DK, class T>
-__global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs A) {
+__global__ void __launch_bounds__(T::TEAM == 32 ? 32 * MAX_TEAMS : T::TEAM, T::TEAM == 32 ? 1 : 2) gdn_kernel(GdnArgs A) {
     griddep_launch();
     constexpr int NP = DK / (2 * LPR);
-    constexpr int RPT = T::RPT, THREADS = T::THREADS;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
+    constexpr int RPT = T::RPT, TEAM = T::TEAM;
+    extern __shared__ __align__(128) uint8_t smem_all[];
     const int total = A.max_commit + A.k;
     const int n_out = A.k + (A.emit_replay ? A.max_commit : 0);
     const GdnSmem<DK> L(total, n_out);
+    const int team = static_cast<int>(threadIdx.x) / TEAM, tid = static_cast<int>(threadIdx.x) % TEAM;
+    const int slab_id = blockIdx.x * A.teams + team;
+    if (slab_id >= A.n_slabs) return;   // a whole team (a warp, or the CTA) leaves together
+    uint8_t* smem_raw = smem_all + L.total * team;
     float* sstate = reinterpret_cast<float*>(smem_raw);
     StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw + L.steps);
     uint16_t* rawv = reinterpret_cast<uint16_t*>(smem_raw + L.rawv);
     uint16_t* obuf = reinterpret_cast<uint16_t*>(smem_raw + L.obuf);
     const uint32_t bar = smem_u32(smem_raw + L.bar);
 
-    const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / A.qk_group;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slabs_per_head = A.dv / SLAB;
+    const int slab = slab_id % slabs_per_head, h = (slab_id / slabs_per_head) % A.H;
+    const int b = slab_id / (slabs_per_head * A.H), hk = h / A.qk_group;
+    const int warp = tid >> 5, lane = tid & 31;
     const int g = lane % LPR;
     int r[RPT];                                           // rows within the slab
 #pragma unroll
     for (int x = 0; x < RPT; ++x) r[x] = warp * T::ROWS_PER_WARP + x * (32 / LPR) + lane / LPR;
     const int row0 = slab * SLAB;
     float* gslab = A.state + ((static_cast<size_t>(b) * A.H + h) * A.dv + row0) * DK;
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
         l2_prefetch(gslab, SLAB * DK * 4);   // a hint only: the copies come after the wait
     }
-    __syncthreads();
+    team_sync<TEAM>();
     griddep_wait();
 
-    // Every copy of the CTA in flight at once, spread over its threads: the state slab, then per
+    // Every copy of the team in flight at once, spread over its threads: the state slab, then per
     // staged step its raw q and k (into the upper halves of the fp32 arrays) and its v slice.
     // The beta and gate scalars and the commit count are plain loads issued alongside.
     constexpr uint32_t QK_BYTES = DK * 2, V_BYTES = SLAB * 2;
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, SLAB * DK * 4 + total * (2 * QK_BYTES + V_BYTES));
-    for (int c = threadIdx.x; c < 1 + 3 * total; c += THREADS) {
+    if (tid == 0) mbar_arrive_expect_tx(bar, SLAB * DK * 4 + total * (2 * QK_BYTES + V_BYTES));
+    for (int c = tid; c < 1 + 3 * total; c += TEAM) {
         if (c == 0) {
             bulk_load(smem_u32(sstate), gslab, SLAB * DK * 4, bar);
             continue;
@@ -304,10 +328,10 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
         else
             bulk_load(smem_u32(rawv + t * SLAB), src.v + base + static_cast<long long>(h) * A.dv + row0, V_BYTES, bar);
     }
-    uint16_t bg[2] = {0, 0};   // entries threadIdx.x and threadIdx.x + THREADS of (beta, gate) x step
+    uint16_t bg[2] = {0, 0};   // entries tid and tid + TEAM of (beta, gate) x step
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-        const int idx = threadIdx.x + q * THREADS;
+        const int idx = tid + q * TEAM;
         if (idx < 2 * total) {
             long long row;
             const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
@@ -316,19 +340,18 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
     }
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
     if (nc < 0 || nc > A.max_commit) {
-        if (threadIdx.x == 0) atomicOr(A.err, ERR_BAD_COUNT);
+        if (tid == 0) atomicOr(A.err, ERR_BAD_COUNT);
         nc = nc < 0 ? 0 : A.max_commit;
     }
     mbar_wait(bar, 0, A.err);
 
-    normalise_all<DK, THREADS>(steps, total, A.l2 != 0);
-    for (int idx = threadIdx.x; idx < total * SLAB; idx += THREADS) steps[idx / SLAB].v[idx % SLAB] = bf16f(rawv[idx]);
-    for (int idx = threadIdx.x; idx < 2 * total; idx += THREADS) {
+    normalise_all<DK, TEAM>(steps, total, A.l2 != 0, tid);
+    for (int idx = tid; idx < 2 * total; idx += TEAM) {
         long long row;
         const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
-        const uint16_t raw = idx < 2 * THREADS ? (idx >= THREADS ? bg[1] : bg[0])
-                                               : ((idx & 1) ? src.gate[row * src.gate_stride + h]
-                                                            : src.beta[row * src.gate_stride + h]);
+        const uint16_t raw = idx < 2 * TEAM ? (idx >= TEAM ? bg[1] : bg[0])
+                                            : ((idx & 1) ? src.gate[row * src.gate_stride + h]
+                                                         : src.beta[row * src.gate_stride + h]);
         const float x = gate_value(raw, idx & 1, src.raw_gates != 0);
         if (idx & 1) steps[idx >> 1].gate = x;
         else steps[idx >> 1].beta = x;
@@ -336,13 +359,13 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
     float2 s[RPT][NP];
 #pragma unroll
     for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], sstate + r[x] * DK, g);
-    __syncthreads();
+    team_sync<TEAM>();
 
     float o[RPT];
     // replay the committed steps (these change the stored state)
     const int orow_spec = A.emit_replay ? nc : 0;
     for (int t = 0; t < nc; ++t) {
-        gdn_step<DK, RPT>(s, steps[t], g, r, A.emit_replay != 0, o);
+        gdn_step<DK, RPT>(s, steps[t], rawv + t * SLAB, g, r, A.emit_replay != 0, o);
         if (A.emit_replay && g == 0) {
 #pragma unroll
             for (int x = 0; x < RPT; ++x) obuf[t * SLAB + r[x]] = f32_to_bf16(o[x]);
@@ -358,8 +381,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
                     make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
         }
         fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
+        team_sync<TEAM>();
+        if (tid == 0) {
             bulk_store(gslab, smem_u32(sstate), SLAB * DK * 4);
             bulk_commit();
         }
@@ -369,18 +392,18 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
     // and key product; with several rows per thread those give the overlap)
 #pragma unroll(RPT == 1 ? 2 : 1)
     for (int t = 0; t < A.k; ++t) {
-        gdn_step<DK, RPT>(s, steps[A.max_commit + t], g, r, true, o);
+        gdn_step<DK, RPT>(s, steps[A.max_commit + t], rawv + (A.max_commit + t) * SLAB, g, r, true, o);
         if (g == 0) {
 #pragma unroll
             for (int x = 0; x < RPT; ++x) obuf[(orow_spec + t) * SLAB + r[x]] = f32_to_bf16(o[x]);
         }
     }
-    __syncthreads();
+    team_sync<TEAM>();
     // outputs: row t of the buffer is the slab's 32 values of output row (b, t) (replayed rows
     // first when emitted, then the speculative ones), 16 bytes per thread
     const int rows_out = orow_spec + A.k;
     constexpr int CH = SLAB / 8;
-    for (int idx = threadIdx.x; idx < rows_out * CH; idx += THREADS) {
+    for (int idx = tid; idx < rows_out * CH; idx += TEAM) {
         const int t = idx / CH, c = idx % CH;
         const long long orow = t < orow_spec ? static_cast<long long>(b) * nc + t
                                              : static_cast<long long>(b) * A.k + (t - orow_spec);
@@ -397,17 +420,18 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS) gdn_kernel(GdnArgs 
             }
         }
     }
-    if (nc > 0 && threadIdx.x == 0) bulk_wait_read();   // the state slab stays in shared memory until read
+    if (nc > 0 && tid == 0) bulk_wait_read();   // the state slab stays in shared memory until read
 }
 
 template <int DK, class T>
-xv_status launch_tiled(const GdnArgs& a, int B, int H, int dv, int total, int n_out, cudaStream_t s) {
-    const GdnSmem<DK> most(XV_GDN_MAX_STAGED, XV_GDN_MAX_STAGED);
-    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_kernel<DK, T>), static_cast<int>(most.total),
-                                        true, "gdn: set shared memory size"))
+xv_status launch_tiled(GdnArgs a, int teams, int total, int n_out, cudaStream_t s) {
+    const size_t per_team = GdnSmem<DK>(total, n_out).total;
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_kernel<DK, T>), XV_GDN_SMEM_MAX, true,
+                                        "gdn: set shared memory size"))
         return st;
-    const dim3 grid(dv / SLAB, H, B);   // dv is a multiple of SLAB (checked)
-    launch_k(gdn_kernel<DK, T>, grid, dim3(T::THREADS), GdnSmem<DK>(total, n_out).total, s, a);
+    a.teams = teams;
+    const int grid = (a.n_slabs + teams - 1) / teams;
+    launch_k(gdn_kernel<DK, T>, dim3(grid), dim3(T::TEAM * teams), per_team * teams, s, a);
     return XV_OK;
 }
 
@@ -420,28 +444,34 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     if (!err) return fail(XV_ERR_CUDA, "gdn: device error word unavailable");
     if (Hk < 1 || H % Hk) return fail(XV_ERR_ARG, "gdn: %d v heads are not a multiple of %d q/k heads", H, Hk);
     if (!aligned16(state)) return fail(XV_ERR_UNSUPPORTED, "gdn: the state must be 16-byte aligned");
+    const long long slabs = static_cast<long long>(B) * H * (dv / SLAB);   // dv is a multiple of SLAB (checked)
+    if (slabs > (1ll << 30)) return fail(XV_ERR_UNSUPPORTED, "gdn: %lld slabs", slabs);
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
-              qk_l2norm ? 1 : 0, H / Hk, err, (aligned16(o) && o_stride % 8 == 0) ? 1 : 0};
+              qk_l2norm ? 1 : 0, H / Hk, err, (aligned16(o) && o_stride % 8 == 0) ? 1 : 0, static_cast<int>(slabs), 1};
     const int max_steps = max_commit + k;
-    const int n_out = k + (emit_replay ? max_commit : 0);
     if (max_steps > XV_GDN_MAX_STAGED)
         return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, XV_GDN_MAX_STAGED);
-    // Slabs of 32 rows: with at least two per SM the wide tiling (4 rows per thread, one warp per
-    // slab) reads each k and q slice once for four rows; below that the narrow one (one row per
-    // thread, four warps per slab) keeps more warps per SM on the latency-bound chain.  Every row's
-    // arithmetic is the same in both.
+    const int n_out = k + (emit_replay ? max_commit : 0);
+    // With at least two slabs per SM the wide tiling (4 rows per thread, a warp per slab, the
+    // slabs of an SM in one CTA: one wave) reads each k and q slice once for four rows; below that
+    // the narrow one (a row per thread, four warps per slab) keeps more warps on each slab's
+    // latency-bound chain.  Every row's arithmetic is the same in both.
     int sms = 0;
     if (xv_status st = device_sm_count(&sms)) return st;
-    const long long slabs = static_cast<long long>(B) * H * (dv / SLAB);
     const bool wide = slabs >= 2ll * sms;
     trace_pre(s);
     xv_status st;
-    if (dk == 128)
-        st = wide ? launch_tiled<128, WideTiling>(a, B, H, dv, max_steps, n_out, s)
-                  : launch_tiled<128, NarrowTiling>(a, B, H, dv, max_steps, n_out, s);
-    else
-        st = wide ? launch_tiled<64, WideTiling>(a, B, H, dv, max_steps, n_out, s)
-                  : launch_tiled<64, NarrowTiling>(a, B, H, dv, max_steps, n_out, s);
+    if (wide) {
+        const size_t per_team = dk == 128 ? GdnSmem<128>(max_steps, n_out).total : GdnSmem<64>(max_steps, n_out).total;
+        int teams = static_cast<int>((slabs + sms - 1) / sms);
+        if (teams > MAX_TEAMS) teams = MAX_TEAMS;
+        while (teams > 1 && per_team * teams > static_cast<size_t>(XV_GDN_SMEM_MAX)) --teams;
+        st = dk == 128 ? launch_tiled<128, WideTiling>(a, teams, max_steps, n_out, s)
+                       : launch_tiled<64, WideTiling>(a, teams, max_steps, n_out, s);
+    } else {
+        st = dk == 128 ? launch_tiled<128, NarrowTiling>(a, 1, max_steps, n_out, s)
+                       : launch_tiled<64, NarrowTiling>(a, 1, max_steps, n_out, s);
+    }
     if (st) return st;
     // algorithmic bytes with every sequence replaying max_commit steps: the state
     // read (and written back after a replay), the step inputs, the outputs
