@@ -24,28 +24,31 @@
 // lane ends with the same bits.  Nothing a row computes depends on which
 // thread, warp or CTA holds it.
 //
-// Tiling (free, chosen per launch): a "team" of threads owns one slab of 32
-// state rows of one head; a thread holds RPT rows of it (rows lane/4,
-// lane/4 + 8, ... of its warp's 8 * RPT).  Every step reads the whole k and q
-// vectors from shared memory into each row's lanes; with one row per thread
-// that read (1 KB per row per step) is the bound, so wide launches hold 4 rows
-// per thread (a team is one warp) and read each slice once for the four.  A
-// wide CTA holds several such warps, each with its own slab, barrier and
-// staging, and there is at most one CTA per SM, so the whole call is one wave;
-// a narrow CTA (few slabs: a latency-bound call) is one team of 4 warps with
-// one row per thread.
+// Tiling (free, chosen per launch): a thread holds RPT rows (rows lane/4,
+// lane/4 + 8, ... of its warp's 8 * RPT) of a slab of 32 state rows.  Every
+// step reads the whole k and q vectors from shared memory into each row's
+// lanes; with one row per thread that read (1 KB per row per step) is the
+// bound, so wide calls hold 4 rows per thread (a warp per slab) and read each
+// slice once for the four.
+//  - Narrow calls (fewer heads than SMs: latency-bound) give each slab a CTA
+//    of 4 warps with one row per thread.
+//  - Wide calls give each (sequence, head) a CTA with a warp per slab; the
+//    head's staged steps (q, k normalised once, v, beta, gate) are shared by
+//    its warps, which keeps the shared memory of a head small enough for two
+//    heads per SM, so a whole batch of 8 is one wave.
 //
-// Data movement: everything a team reads arrives by bulk asynchronous copies
-// on one mbarrier, issued right after the dependency wait: its 16 KB slab of
-// the state (contiguous rows) and, per staged step, the raw q and k of its
-// head and its slice of v.  (Plain per-thread loads of the state, one 16-byte
-// piece at a time, queued behind each other in the load/store unit and held
-// the shared-memory traffic of the steps behind them.)  The state then lives
-// in registers across all replay and speculative steps; after a replay it
-// goes back through shared memory and one bulk store, and the outputs of
-// every step are gathered in shared memory and written in 16-byte pieces at
-// the end.  q and k are L2-normalised in place (the raw bf16 vector lands in
-// the upper half of its fp32 array) by 4 threads per vector.
+// Data movement: everything a CTA reads arrives by asynchronous bulk copies
+// on mbarriers, issued right after the dependency wait: the state (16 KB per
+// slab, contiguous rows) and the steps' raw q, k and v.  (Plain per-thread
+// loads of the state, one 16-byte piece at a time, queued behind each other in
+// the load/store unit and held the shared-memory traffic of the steps behind
+// them.)  In wide calls the steps come by tensor copies (one per source and
+// vector) and the slabs are requested one after another, each on its own
+// barrier, so the first warps start on their slab while the later slabs are
+// still arriving.  The state then lives in registers across all replay and
+// speculative steps; after a replay it goes back through shared memory and a
+// bulk store, and the outputs of every step are gathered in shared memory and
+// written in 16-byte pieces at the end.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
@@ -55,7 +58,6 @@ namespace {
 constexpr int LPR = 4;                          // lanes per state row
 constexpr int NORM_LANES = 4;                   // threads per q or k vector in the normalisation
 constexpr int SLAB = 32;                        // state rows per team
-constexpr int MAX_TEAMS = 8;                    // slabs (warps) per wide CTA
 
 // A launch shape: RPT state rows per thread, TEAM threads per slab.
 template <int RPT_>
@@ -64,9 +66,16 @@ struct Tiling {
     static constexpr int TEAM = SLAB * LPR / RPT;        // threads sharing one slab
     static constexpr int ROWS_PER_WARP = 32 / LPR * RPT;
 };
-using NarrowTiling = Tiling<1>;   // 128 threads per slab, one CTA each: few slabs (latency-bound calls)
-using WideTiling = Tiling<4>;     // one warp per slab, up to MAX_TEAMS per CTA: shared-memory reads amortised
-static_assert(WideTiling::TEAM == 32, "a wide team is one warp");
+using NarrowTiling = Tiling<1>;   // 128 threads per slab, one CTA each: few heads (latency-bound calls)
+using WideTiling = Tiling<4>;     // one warp per slab, a CTA per head: shared-memory reads amortised
+static_assert(WideTiling::TEAM == 32 && WideTiling::ROWS_PER_WARP == SLAB, "a wide team is one warp holding a slab");
+constexpr int MAX_SLABS_PER_HEAD = 8;   // dv <= 256
+
+// Tensor maps of the wide kernel's step inputs: pending q, k, v, then draft q, k, v (2-D views
+// [rows, columns] of the step sources; a box is one head's vector over the staged rows).
+struct GdnMaps {
+    CUtensorMap m[6];
+};
 
 struct GdnArgs {
     float* state;
@@ -83,7 +92,6 @@ struct GdnArgs {
     unsigned* err;
     int o_vec;     // o and o_stride allow 16-byte stores
     int n_slabs;   // B * H * dv / SLAB
-    int teams;     // slabs per CTA (blockDim.x / TEAM)
 };
 
 // Per-step inputs staged in shared memory: q and k (fp32, normalised; their raw bf16 copies land in
@@ -132,22 +140,25 @@ __device__ __forceinline__ void team_sync() {
     else __syncthreads();
 }
 
-// Vector w of the staged steps (step w / 2; q for even w, k for odd) from its raw bf16 copy (upper
-// half of the fp32 array) to fp32 in place, L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)):
-// thread j of the vector's group of NORM_LANES takes the 16-byte raw pieces j, j + 4, j + 8, ...
-// (8 elements each, so the group's reads and writes fall in distinct banks), sums their squares
-// in four interleaved chains (element index mod 4) added as (c0 + c1) + (c2 + c3), the group adds
-// its partials by an xor tree (1, 2), and every thread scales its own elements.
-template <int DK, int TEAM>
-__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bool l2, int tid) {
+// Vector w of the staged steps (step w / 2; q for even w, k for odd) from its raw bf16 copy to fp32,
+// L2-normalised when l2 (x / sqrt(sum x^2 + 1e-6)).  The raw copy is row t of rq / rk, or, when rq
+// is null, the upper half of the fp32 array itself (converted in place).  Thread j of the vector's
+// group of NORM_LANES takes the 16-byte raw pieces j, j + 4, j + 8, ... (8 elements each, so the
+// group's reads and writes fall in distinct banks), sums their squares in four interleaved chains
+// (element index mod 4) added as (c0 + c1) + (c2 + c3), the group adds its partials by an xor
+// tree (1, 2), and every thread scales its own elements.  nthreads threads (whole warps) take part.
+template <int DK>
+__device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, const uint16_t* rq, const uint16_t* rk, int total,
+                                              bool l2, int tid, int nthreads) {
     constexpr int PIECES = DK / 8 / NORM_LANES;   // raw 16-byte pieces per thread
     const int jl = tid % NORM_LANES;
-    for (int w0 = 0; w0 < 2 * total; w0 += TEAM / NORM_LANES) {   // same trip count for every thread
+    for (int w0 = 0; w0 < 2 * total; w0 += nthreads / NORM_LANES) {   // same trip count for every thread
         const int w = w0 + tid / NORM_LANES;
         const bool act = w < 2 * total;
         const int t = act ? w >> 1 : 0;
         float* y = (w & 1) ? steps[t].k : steps[t].q;
-        const uint16_t* x = reinterpret_cast<const uint16_t*>(y + DK / 2);
+        const uint16_t* x = rq ? ((w & 1) ? rk : rq) + static_cast<size_t>(t) * DK
+                               : reinterpret_cast<const uint16_t*>(y + DK / 2);
         float f[8 * PIECES];
 #pragma unroll
         for (int i = 0; i < PIECES; ++i) {
@@ -174,7 +185,7 @@ __device__ __forceinline__ void normalise_all(StepSmem<DK>* steps, int total, bo
             ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
             inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ss, 1e-6f)));
         }
-        __syncwarp();   // the group's raw halves are read before any fp32 element overwrites them
+        __syncwarp();   // an in-place group's raw halves are read before any fp32 element overwrites them
         if (!act) continue;
 #pragma unroll
         for (int i = 0; i < PIECES; ++i) {
@@ -271,7 +282,7 @@ __device__ __forceinline__ void gdn_step(float2 (&s)[RPT][DK / (2 * LPR)], const
 }
 
 template <int DK, class T>
-__global__ void __launch_bounds__(T::TEAM == 32 ? 32 * MAX_TEAMS : T::TEAM, T::TEAM == 32 ? 1 : 2) gdn_kernel(GdnArgs A) {
+__global__ void __launch_bounds__(T::TEAM, 2) gdn_kernel(GdnArgs A) {
     griddep_launch();
     constexpr int NP = DK / (2 * LPR);
     constexpr int RPT = T::RPT, TEAM = T::TEAM;
@@ -279,10 +290,9 @@ __global__ void __launch_bounds__(T::TEAM == 32 ? 32 * MAX_TEAMS : T::TEAM, T::T
     const int total = A.max_commit + A.k;
     const int n_out = A.k + (A.emit_replay ? A.max_commit : 0);
     const GdnSmem<DK> L(total, n_out);
-    const int team = static_cast<int>(threadIdx.x) / TEAM, tid = static_cast<int>(threadIdx.x) % TEAM;
-    const int slab_id = blockIdx.x * A.teams + team;
-    if (slab_id >= A.n_slabs) return;   // a whole team (a warp, or the CTA) leaves together
-    uint8_t* smem_raw = smem_all + L.total * team;
+    const int tid = static_cast<int>(threadIdx.x);
+    const int slab_id = blockIdx.x;
+    uint8_t* smem_raw = smem_all;
     float* sstate = reinterpret_cast<float*>(smem_raw);
     StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem_raw + L.steps);
     uint16_t* rawv = reinterpret_cast<uint16_t*>(smem_raw + L.rawv);
@@ -345,7 +355,7 @@ __global__ void __launch_bounds__(T::TEAM == 32 ? 32 * MAX_TEAMS : T::TEAM, T::T
     }
     mbar_wait(bar, 0, A.err);
 
-    normalise_all<DK, TEAM>(steps, total, A.l2 != 0, tid);
+    normalise_all<DK>(steps, nullptr, nullptr, total, A.l2 != 0, tid, TEAM);
     for (int idx = tid; idx < 2 * total; idx += TEAM) {
         long long row;
         const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
@@ -423,15 +433,213 @@ __global__ void __launch_bounds__(T::TEAM == 32 ? 32 * MAX_TEAMS : T::TEAM, T::T
     if (nc > 0 && tid == 0) bulk_wait_read();   // the state slab stays in shared memory until read
 }
 
-template <int DK, class T>
-xv_status launch_tiled(GdnArgs a, int teams, int total, int n_out, cudaStream_t s) {
-    const size_t per_team = GdnSmem<DK>(total, n_out).total;
+// Shared-memory plan of a wide (per-head) CTA: the staged steps (fp32 q, k, beta, gate), the raw
+// q, k and v rows the tensor copies land in, each warp's state slab and outputs, the barriers (the
+// step inputs', then one per slab).
+template <int DK>
+struct HeadSmem {
+    size_t rawq, rawk, rawv, state, obuf, bars, total;
+    __host__ __device__ HeadSmem(int n_steps, int n_out, int dv) {
+        const size_t nsl = dv / SLAB;
+        auto r128 = [](size_t x) { return (x + 127) & ~static_cast<size_t>(127); };
+        rawq = r128(sizeof(StepSmem<DK>) * n_steps);
+        rawk = r128(rawq + static_cast<size_t>(n_steps) * DK * 2);
+        rawv = r128(rawk + static_cast<size_t>(n_steps) * DK * 2);
+        state = r128(rawv + static_cast<size_t>(n_steps) * dv * 2);
+        obuf = state + nsl * SLAB * DK * 4;
+        bars = r128(obuf + nsl * n_out * SLAB * 2);
+        total = bars + 8 * (1 + nsl);
+    }
+};
+
+// One (sequence, head) per CTA, a warp per 32-row slab with 4 rows per thread.  Thread 0 requests
+// the step inputs (six tensor copies: pending and draft q, k, v over the staged rows), then the
+// slabs one after another, each on its own barrier; all threads normalise the head's q and k once;
+// each warp then waits only for its own slab.
+template <int DK>
+__global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
+    gdn_head_kernel(const __grid_constant__ GdnMaps M, GdnArgs A) {
+    griddep_launch();
+    constexpr int NP = DK / (2 * LPR), RPT = WideTiling::RPT;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int total = A.max_commit + A.k;
+    const int n_out = A.k + (A.emit_replay ? A.max_commit : 0);
+    const int nsl = A.dv / SLAB, nthreads = 32 * nsl;
+    const HeadSmem<DK> L(total, n_out, A.dv);
+    StepSmem<DK>* steps = reinterpret_cast<StepSmem<DK>*>(smem);
+    uint16_t* rawq = reinterpret_cast<uint16_t*>(smem + L.rawq);
+    uint16_t* rawk = reinterpret_cast<uint16_t*>(smem + L.rawk);
+    uint16_t* rawv = reinterpret_cast<uint16_t*>(smem + L.rawv);
+    const int h = blockIdx.x % A.H, b = blockIdx.x / A.H, hk = h / A.qk_group;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane % LPR;
+    float* sstate = reinterpret_cast<float*>(smem + L.state) + warp * SLAB * DK;
+    uint16_t* obuf = reinterpret_cast<uint16_t*>(smem + L.obuf) + warp * n_out * SLAB;
+    const uint32_t bar_in = smem_u32(smem + L.bars), bar_slab = bar_in + 8 * (1 + warp);
+    const int row0 = warp * SLAB;
+    float* ghead = A.state + (static_cast<size_t>(b) * A.H + h) * A.dv * DK;
+    int r[RPT];                                           // rows within the slab
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) r[x] = x * (32 / LPR) + lane / LPR;
+    if (tid == 0) {
+        for (int i = 0; i <= nsl; ++i) mbar_init(bar_in + 8 * i, 1);
+        fence_mbar_init();
+        for (int i = 0; i < 6; ++i) tma_prefetch_desc(&M.m[i]);
+        l2_prefetch(ghead, static_cast<uint32_t>(A.dv) * DK * 4);   // a hint only: the copies come after the wait
+    }
+    __syncthreads();
+    griddep_wait();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_in, static_cast<uint32_t>(total) * (4 * DK + 2 * A.dv));
+        if (A.max_commit > 0) {
+            const int y = b * A.pend.rows_per_seq;
+            tma_load_2d(smem_u32(rawq), &M.m[0], hk * DK, y, bar_in);
+            tma_load_2d(smem_u32(rawk), &M.m[1], hk * DK, y, bar_in);
+            tma_load_2d(smem_u32(rawv), &M.m[2], h * A.dv, y, bar_in);
+        }
+        if (A.k > 0) {
+            const int y = b * A.draft.rows_per_seq;
+            tma_load_2d(smem_u32(rawq + A.max_commit * DK), &M.m[3], hk * DK, y, bar_in);
+            tma_load_2d(smem_u32(rawk + A.max_commit * DK), &M.m[4], hk * DK, y, bar_in);
+            tma_load_2d(smem_u32(rawv + A.max_commit * A.dv), &M.m[5], h * A.dv, y, bar_in);
+        }
+        for (int w = 0; w < nsl; ++w) {
+            const uint32_t bw = bar_in + 8 * (1 + w);
+            mbar_arrive_expect_tx(bw, SLAB * DK * 4);
+            bulk_load(smem_u32(reinterpret_cast<float*>(smem + L.state) + w * SLAB * DK),
+                      ghead + static_cast<size_t>(w) * SLAB * DK, SLAB * DK * 4, bw);
+        }
+    }
+    uint16_t bg[2] = {0, 0};   // entries tid and tid + nthreads of (beta, gate) x step
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int idx = tid + q * nthreads;
+        if (idx < 2 * total) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
+            bg[q] = (idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
+        }
+    }
+    int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
+    if (nc < 0 || nc > A.max_commit) {
+        if (tid == 0) atomicOr(A.err, ERR_BAD_COUNT);
+        nc = nc < 0 ? 0 : A.max_commit;
+    }
+    mbar_wait(bar_in, 0, A.err);
+    normalise_all<DK>(steps, rawq, rawk, total, A.l2 != 0, tid, nthreads);
+    for (int idx = tid; idx < 2 * total; idx += nthreads) {
+        long long row;
+        const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
+        const uint16_t raw = idx < 2 * nthreads ? (idx >= nthreads ? bg[1] : bg[0])
+                                                : ((idx & 1) ? src.gate[row * src.gate_stride + h]
+                                                             : src.beta[row * src.gate_stride + h]);
+        const float x = gate_value(raw, idx & 1, src.raw_gates != 0);
+        if (idx & 1) steps[idx >> 1].gate = x;
+        else steps[idx >> 1].beta = x;
+    }
+    __syncthreads();
+    mbar_wait(bar_slab, 0, A.err);
+    float2 s[RPT][NP];
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], sstate + r[x] * DK, g);
+    __syncwarp();
+
+    float o[RPT];
+    const int orow_spec = A.emit_replay ? nc : 0;
+    for (int t = 0; t < nc; ++t) {
+        gdn_step<DK, RPT>(s, steps[t], rawv + t * A.dv + row0, g, r, A.emit_replay != 0, o);
+        if (A.emit_replay && g == 0) {
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) obuf[t * SLAB + r[x]] = f32_to_bf16(o[x]);
+        }
+    }
+    if (nc > 0) {
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+#pragma unroll
+            for (int u = 0; u < NP / 2; ++u)
+                *reinterpret_cast<float4*>(sstate + r[x] * DK + 4 * (g + LPR * u)) =
+                    make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_store(ghead + static_cast<size_t>(row0) * DK, smem_u32(sstate), SLAB * DK * 4);
+            bulk_commit();
+        }
+    }
+    for (int t = 0; t < A.k; ++t) {
+        gdn_step<DK, RPT>(s, steps[A.max_commit + t], rawv + (A.max_commit + t) * A.dv + row0, g, r, true, o);
+        if (g == 0) {
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) obuf[(orow_spec + t) * SLAB + r[x]] = f32_to_bf16(o[x]);
+        }
+    }
+    __syncwarp();
+    const int rows_out = orow_spec + A.k;
+    constexpr int CH = SLAB / 8;
+    for (int idx = lane; idx < rows_out * CH; idx += 32) {
+        const int t = idx / CH, c = idx % CH;
+        const long long orow = t < orow_spec ? static_cast<long long>(b) * nc + t
+                                             : static_cast<long long>(b) * A.k + (t - orow_spec);
+        uint16_t* dst = A.o + orow * A.o_stride + static_cast<long long>(h) * A.dv + row0 + 8 * c;
+        const uint4 v = *reinterpret_cast<const uint4*>(obuf + t * SLAB + 8 * c);
+        if (A.o_vec) {
+            *reinterpret_cast<uint4*>(dst) = v;
+        } else {
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dst[2 * i] = static_cast<uint16_t>(w4[i] & 0xFFFFu);
+                dst[2 * i + 1] = static_cast<uint16_t>(w4[i] >> 16);
+            }
+        }
+    }
+    if (nc > 0 && lane == 0) bulk_wait_read();   // the slab stays in shared memory until read
+}
+
+template <int DK>
+xv_status launch_narrow(const GdnArgs& a, int total, int n_out, cudaStream_t s) {
+    using T = NarrowTiling;
     if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_kernel<DK, T>), XV_GDN_SMEM_MAX, true,
                                         "gdn: set shared memory size"))
         return st;
-    a.teams = teams;
-    const int grid = (a.n_slabs + teams - 1) / teams;
-    launch_k(gdn_kernel<DK, T>, dim3(grid), dim3(T::TEAM * teams), per_team * teams, s, a);
+    launch_k(gdn_kernel<DK, T>, dim3(a.n_slabs), dim3(T::TEAM), GdnSmem<DK>(total, n_out).total, s, a);
+    return XV_OK;
+}
+
+// 2-D view [rows, cols] of a step source's columns starting at `base`, boxes of `box_cols` x
+// `box_rows` (bf16, no swizzle).
+inline xv_status step_map(CUtensorMap* m, const uint16_t* base, long long cols, long long rows, long long stride,
+                          int box_cols, int box_rows) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(stride) * 2};
+    const uint32_t box[2] = {static_cast<uint32_t>(box_cols), static_cast<uint32_t>(box_rows)};
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <int DK>
+xv_status launch_head(const GdnArgs& a, int B, int Hk, int total, int n_out, size_t smem, cudaStream_t s) {
+    GdnMaps M{};
+    const GdnStepsDev* src[2] = {&a.pend, &a.draft};
+    const int rows[2] = {a.max_commit, a.k};
+    for (int i = 0; i < 2; ++i) {
+        if (rows[i] == 0) continue;
+        const GdnStepsDev& d = *src[i];
+        const long long nrows = static_cast<long long>(B) * d.rows_per_seq;
+        xv_status st;
+        if ((st = step_map(&M.m[3 * i], d.q, static_cast<long long>(Hk) * DK, nrows, d.qkv_stride, DK, rows[i])))
+            return st;
+        if ((st = step_map(&M.m[3 * i + 1], d.k, static_cast<long long>(Hk) * DK, nrows, d.qkv_stride, DK, rows[i])))
+            return st;
+        if ((st = step_map(&M.m[3 * i + 2], d.v, static_cast<long long>(a.H) * a.dv, nrows, d.qkv_stride, a.dv, rows[i])))
+            return st;
+    }
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_head_kernel<DK>), XV_GDN_SMEM_MAX, true,
+                                        "gdn: set shared memory size"))
+        return st;
+    (void)total;
+    (void)n_out;
+    launch_k(gdn_head_kernel<DK>, dim3(B * a.H), dim3(32 * (a.dv / SLAB)), smem, s, M, a);
     return XV_OK;
 }
 
@@ -447,31 +655,29 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     const long long slabs = static_cast<long long>(B) * H * (dv / SLAB);   // dv is a multiple of SLAB (checked)
     if (slabs > (1ll << 30)) return fail(XV_ERR_UNSUPPORTED, "gdn: %lld slabs", slabs);
     GdnArgs a{state, pending, n_commit, n_fixed, max_commit, emit_replay ? 1 : 0, draft, k, o, o_stride, H, dv,
-              qk_l2norm ? 1 : 0, H / Hk, err, (aligned16(o) && o_stride % 8 == 0) ? 1 : 0, static_cast<int>(slabs), 1};
+              qk_l2norm ? 1 : 0, H / Hk, err, (aligned16(o) && o_stride % 8 == 0) ? 1 : 0, static_cast<int>(slabs)};
     const int max_steps = max_commit + k;
     if (max_steps > XV_GDN_MAX_STAGED)
         return fail(XV_ERR_UNSUPPORTED, "gdn: %d steps in one call exceed %d", max_steps, XV_GDN_MAX_STAGED);
     const int n_out = k + (emit_replay ? max_commit : 0);
-    // With at least two slabs per SM the wide tiling (4 rows per thread, a warp per slab, the
-    // slabs of an SM in one CTA: one wave) reads each k and q slice once for four rows; below that
-    // the narrow one (a row per thread, four warps per slab) keeps more warps on each slab's
-    // latency-bound chain.  Every row's arithmetic is the same in both.
+    // With at least one head per SM the wide kernel (a CTA per head, a warp per slab, 4 rows per
+    // thread) reads each k and q slice once for four rows and shares the head's staged steps among
+    // its slabs, as long as two such CTAs fit an SM (else the batch would take two waves); below
+    // that, or with more staged steps (prefill chunks), the narrow one (a CTA per slab, a row per
+    // thread) keeps more warps on each slab's latency-bound chain.  Every row's arithmetic is the
+    // same in both.
     int sms = 0;
     if (xv_status st = device_sm_count(&sms)) return st;
-    const bool wide = slabs >= 2ll * sms;
+    const size_t head_smem = dk == 128 ? HeadSmem<128>(max_steps, n_out, dv).total : HeadSmem<64>(max_steps, n_out, dv).total;
+    const bool wide = static_cast<long long>(B) * H >= sms && dv / SLAB <= MAX_SLABS_PER_HEAD &&
+                      2 * (head_smem + 1024) <= static_cast<size_t>(XV_GDN_SMEM_SM) && B * H < (1 << 30);
     trace_pre(s);
     xv_status st;
-    if (wide) {
-        const size_t per_team = dk == 128 ? GdnSmem<128>(max_steps, n_out).total : GdnSmem<64>(max_steps, n_out).total;
-        int teams = static_cast<int>((slabs + sms - 1) / sms);
-        if (teams > MAX_TEAMS) teams = MAX_TEAMS;
-        while (teams > 1 && per_team * teams > static_cast<size_t>(XV_GDN_SMEM_MAX)) --teams;
-        st = dk == 128 ? launch_tiled<128, WideTiling>(a, teams, max_steps, n_out, s)
-                       : launch_tiled<64, WideTiling>(a, teams, max_steps, n_out, s);
-    } else {
-        st = dk == 128 ? launch_tiled<128, NarrowTiling>(a, 1, max_steps, n_out, s)
-                       : launch_tiled<64, NarrowTiling>(a, 1, max_steps, n_out, s);
-    }
+    if (wide)
+        st = dk == 128 ? launch_head<128>(a, B, Hk, max_steps, n_out, head_smem, s)
+                       : launch_head<64>(a, B, Hk, max_steps, n_out, head_smem, s);
+    else
+        st = dk == 128 ? launch_narrow<128>(a, max_steps, n_out, s) : launch_narrow<64>(a, max_steps, n_out, s);
     if (st) return st;
     // algorithmic bytes with every sequence replaying max_commit steps: the state
     // read (and written back after a replay), the step inputs, the outputs

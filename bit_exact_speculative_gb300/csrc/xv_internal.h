@@ -95,8 +95,9 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, in
 // ---- GDN (gdn.cu)
 // Steps one GDN call stages: up to XV_KMAX replayed ones and XV_KMAX speculative ones.
 constexpr int XV_GDN_MAX_STAGED = 2 * XV_KMAX;
-// Dynamic shared memory a GDN launch may take per CTA.
+// Dynamic shared memory a GDN launch may take per CTA, and the shared memory of an SM.
 constexpr int XV_GDN_SMEM_MAX = 227 * 1024;
+constexpr int XV_GDN_SMEM_SM = 228 * 1024;
 struct GdnStepsDev {
     const uint16_t* q;
     const uint16_t* k;
