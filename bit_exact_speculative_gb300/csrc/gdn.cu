@@ -71,11 +71,21 @@ using WideTiling = Tiling<4>;     // one warp per slab, a CTA per head: shared-m
 static_assert(WideTiling::TEAM == 32 && WideTiling::ROWS_PER_WARP == SLAB, "a wide team is one warp holding a slab");
 constexpr int MAX_SLABS_PER_HEAD = 8;   // dv <= 256
 
-// Tensor maps of the wide kernel's step inputs: pending q, k, v, then draft q, k, v (2-D views
-// [rows, columns] of the step sources; a box is one head's vector over the staged rows).
+// Tensor maps of the wide kernel: its step inputs (pending q, k, v, then draft q, k, v: 2-D views
+// [rows, columns] of the step sources, a box one head's vector over the staged rows), then the
+// state viewed as [B H dv rows, dk columns] fp32 in boxes of 32 rows x 32 columns (128 bytes, with
+// the 128-byte swizzle: in shared memory the 16-byte chunk j of row r sits at chunk j ^ (r % 8),
+// so the lanes of two rows never meet in a bank).
 struct GdnMaps {
-    CUtensorMap m[6];
+    CUtensorMap m[7];
 };
+constexpr int SW_COLS = 32;                     // fp32 columns of one swizzled state box (128 bytes)
+
+// Address of fp32 element 4 c of row r in a swizzled slab: column block c / 8, chunk c % 8 of the
+// row's 128 bytes there, moved to c % 8 ^ (r % 8).
+__device__ __forceinline__ float* swz(float* slab, int r, int c) {
+    return slab + (c >> 3) * (SLAB * SW_COLS) + r * SW_COLS + 4 * ((c & 7) ^ (r & 7));
+}
 
 struct GdnArgs {
     float* state;
@@ -445,7 +455,7 @@ struct HeadSmem {
         rawq = r128(sizeof(StepSmem<DK>) * n_steps);
         rawk = r128(rawq + static_cast<size_t>(n_steps) * DK * 2);
         rawv = r128(rawk + static_cast<size_t>(n_steps) * DK * 2);
-        state = r128(rawv + static_cast<size_t>(n_steps) * dv * 2);
+        state = (rawv + static_cast<size_t>(n_steps) * dv * 2 + 1023) & ~static_cast<size_t>(1023);
         obuf = state + nsl * SLAB * DK * 4;
         bars = r128(obuf + nsl * n_out * SLAB * 2);
         total = bars + 8 * (1 + nsl);
@@ -476,15 +486,13 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
     uint16_t* obuf = reinterpret_cast<uint16_t*>(smem + L.obuf) + warp * n_out * SLAB;
     const uint32_t bar_in = smem_u32(smem + L.bars), bar_slab = bar_in + 8 * (1 + warp);
     const int row0 = warp * SLAB;
-    float* ghead = A.state + (static_cast<size_t>(b) * A.H + h) * A.dv * DK;
     int r[RPT];                                           // rows within the slab
 #pragma unroll
     for (int x = 0; x < RPT; ++x) r[x] = x * (32 / LPR) + lane / LPR;
     if (tid == 0) {
         for (int i = 0; i <= nsl; ++i) mbar_init(bar_in + 8 * i, 1);
         fence_mbar_init();
-        for (int i = 0; i < 6; ++i) tma_prefetch_desc(&M.m[i]);
-        l2_prefetch(ghead, static_cast<uint32_t>(A.dv) * DK * 4);   // a hint only: the copies come after the wait
+        for (int i = 0; i < 7; ++i) tma_prefetch_desc(&M.m[i]);
     }
     __syncthreads();
     griddep_wait();
@@ -502,11 +510,14 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
             tma_load_2d(smem_u32(rawk + A.max_commit * DK), &M.m[4], hk * DK, y, bar_in);
             tma_load_2d(smem_u32(rawv + A.max_commit * A.dv), &M.m[5], h * A.dv, y, bar_in);
         }
+        const int grow = (b * A.H + h) * A.dv;   // first state row of the head
         for (int w = 0; w < nsl; ++w) {
             const uint32_t bw = bar_in + 8 * (1 + w);
+            float* slab = reinterpret_cast<float*>(smem + L.state) + w * SLAB * DK;
             mbar_arrive_expect_tx(bw, SLAB * DK * 4);
-            bulk_load(smem_u32(reinterpret_cast<float*>(smem + L.state) + w * SLAB * DK),
-                      ghead + static_cast<size_t>(w) * SLAB * DK, SLAB * DK * 4, bw);
+#pragma unroll
+            for (int cb = 0; cb < DK / SW_COLS; ++cb)
+                tma_load_2d(smem_u32(slab + cb * SLAB * SW_COLS), &M.m[6], cb * SW_COLS, grow + w * SLAB, bw);
         }
     }
     uint16_t bg[2] = {0, 0};   // entries tid and tid + nthreads of (beta, gate) x step
@@ -540,7 +551,14 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
     mbar_wait(bar_slab, 0, A.err);
     float2 s[RPT][NP];
 #pragma unroll
-    for (int x = 0; x < RPT; ++x) load_slice<DK>(s[x], sstate + r[x] * DK, g);
+    for (int x = 0; x < RPT; ++x) {
+#pragma unroll
+        for (int u = 0; u < NP / 2; ++u) {
+            const float4 t = *reinterpret_cast<const float4*>(swz(sstate, r[x], g + LPR * u));
+            s[x][2 * u] = make_float2(t.x, t.y);
+            s[x][2 * u + 1] = make_float2(t.z, t.w);
+        }
+    }
     __syncwarp();
 
     float o[RPT];
@@ -557,13 +575,16 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
         for (int x = 0; x < RPT; ++x) {
 #pragma unroll
             for (int u = 0; u < NP / 2; ++u)
-                *reinterpret_cast<float4*>(sstate + r[x] * DK + 4 * (g + LPR * u)) =
+                *reinterpret_cast<float4*>(swz(sstate, r[x], g + LPR * u)) =
                     make_float4(s[x][2 * u].x, s[x][2 * u].y, s[x][2 * u + 1].x, s[x][2 * u + 1].y);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            bulk_store(ghead + static_cast<size_t>(row0) * DK, smem_u32(sstate), SLAB * DK * 4);
+            const int grow = (b * A.H + h) * A.dv + row0;
+#pragma unroll
+            for (int cb = 0; cb < DK / SW_COLS; ++cb)
+                tma_store_2d(&M.m[6], cb * SW_COLS, grow, smem_u32(sstate + cb * SLAB * SW_COLS));
             bulk_commit();
         }
     }
@@ -632,6 +653,14 @@ xv_status launch_head(const GdnArgs& a, int B, int Hk, int total, int n_out, siz
         if ((st = step_map(&M.m[3 * i + 1], d.k, static_cast<long long>(Hk) * DK, nrows, d.qkv_stride, DK, rows[i])))
             return st;
         if ((st = step_map(&M.m[3 * i + 2], d.v, static_cast<long long>(a.H) * a.dv, nrows, d.qkv_stride, a.dv, rows[i])))
+            return st;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(DK), static_cast<uint64_t>(B) * a.H * a.dv};
+        const uint64_t strides[1] = {static_cast<uint64_t>(DK) * 4};
+        const uint32_t box[2] = {SW_COLS, SLAB};
+        if (xv_status st = encode_tiled(&M.m[6], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.state, dims, strides, box,
+                                        CU_TENSOR_MAP_SWIZZLE_128B))
             return st;
     }
     if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(gdn_head_kernel<DK>), XV_GDN_SMEM_MAX, true,

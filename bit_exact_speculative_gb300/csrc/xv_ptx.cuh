@@ -168,6 +168,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// Tiled tensor store of a 2-D box from shared memory at global coordinates (c0, c1), in the issuing
+// thread's current bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
 // Bulk copy of `bytes` (a multiple of 16) from shared to global memory, both 16-byte aligned, in
 // the issuing thread's current bulk group.
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
