@@ -142,17 +142,22 @@ def dist_env():
 
 # ----------------------------------------------------------------- setup
 
-def make_stack(args, device, rank=0, extra_rounds=0):
+def make_stack(args, device, rank=0, extra_rounds=0, w=None, wd=None, device_kv=False):
     """The 4-layer stack with its weights (the same on every rank: replicas of one model) and
-    rank's own sequences (caches, GDN states and draft tokens from the rank's seed)."""
+    rank's own sequences (caches, GDN states and draft tokens from the rank's seed).  ``w`` / ``wd``
+    reuse weights already drawn (host bits / device tensors); with ``device_kv`` the KV caches are
+    drawn on the device (seeded N(0, 1), the recipe's distribution) instead of on the host, for the
+    long-context timing lines."""
     import torch
     from synth import workloads
     from bit_exact_speculative_gb300.model import HybridStack
     from bit_exact_speculative_gb300.replicas import rank_seed
 
     cfg = workloads.STACK_FULL if args.full_gdn else workloads.STACK
-    w = workloads.weights(cfg, seed=0)
-    wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
+    if w is None:
+        w = workloads.weights(cfg, seed=0)
+    if wd is None:
+        wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
     B, k, L = args.batch, args.k, args.context
     seq = rank_seed(0, rank)
     rounds = 3 * (args.steps + args.warmup) + 8 + extra_rounds
@@ -176,12 +181,22 @@ def make_stack(args, device, rank=0, extra_rounds=0):
                 stk.state[f"{l}.state"].copy_(torch.from_numpy(workloads.gdn_state(cfg, seq, l, B)))
                 if cfg.get("gdn_conv"):
                     stk.state[f"{l}.conv"].copy_(torch.from_numpy(workloads.conv_state(cfg, seq, l, B).view(np.int16)))
+            elif device_kv:
+                g = torch.Generator(device=device)
+                g.manual_seed(seq * 1000 + l)
+                for name in ("kc", "vc"):
+                    c = stk.state[f"{l}.{name}"]
+                    c.zero_()
+                    for b in range(B):
+                        c[b, :, :L].copy_(torch.randn(c[b, :, :L].shape, generator=g, device=device)
+                                          .to(torch.bfloat16).view(torch.int16))
             else:
                 kc, vc = workloads.kv_cache(cfg, seq, l, B, [L] * B, Lmax)
                 stk.load_kv(l, torch.from_numpy(kc.view(np.int16)), torch.from_numpy(vc.view(np.int16)))
 
     reset()
     stk.reset = reset
+    stk.wd = wd
     toks = np.stack([workloads.draft_tokens(cfg, seq, r, B, k) for r in range(rounds)])
     return cfg, w, stk, toks
 
@@ -221,20 +236,24 @@ def traffic_ratio_from_profile(kernel_src: str):
 
 # ------------------------------------------------------ per-kernel rooflines
 
-def _traced_median_ms(xv, launch, n):
-    """Median device time of n launches (each bracketed by events on its stream)."""
+def _back_to_back_ms(launch, n):
+    """Device time per launch of n launches issued back to back (programmatic dependent launch
+    as in the step), between two events on the launching stream."""
     import torch
-    xv.xv_trace_enable(4 * n)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
     for i in range(n):
         launch(i)
+    e1.record(stream)
     torch.cuda.synchronize()
-    recs = xv.xv_trace_read()
-    xv.xv_trace_disable()
-    return recs
+    return e0.elapsed_time(e1) / n
 
 
 def kernel_rooflines(xv, device, peak):
-    """The three hot kernels alone, L2-cold (inputs rotated through more than 3x L2), timed per launch."""
+    """The three hot kernels alone, each timed over back-to-back launches with its inputs rotated
+    through more than 3x L2 (every launch reads cold data), per launch."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(0)
@@ -246,38 +265,43 @@ def kernel_rooflines(xv, device, peak):
     def copies_for(nbytes):
         return max(2, int(np.ceil(400e6 / max(nbytes, 1))))
 
-    # small-M GEMM, every projection shape of the stack
-    gem = {}
-    for M in (8, 64):
-        for N, K, name, f32 in [(12352, 5120, "gdn_in", False), (5120, 4096, "gdn_out", False),
-                                (14336, 5120, "attn_in", False), (5120, 6144, "attn_out", False),
-                                (34816, 5120, "gate_up", False), (5120, 17408, "down", False),
-                                (151936, 5120, "lm_head", True)]:
-            nc = copies_for(2 * N * K)
-            Ws = [rnd((N, K), 0.02) for _ in range(nc)]
-            X = rnd((M, K))
-            Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
-            ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K), device=device)
-            for i in range(nc):
-                xv.xv_gemm_small_m(X, Ws[i], Y, ws)
-            recs = _traced_median_ms(xv, lambda i: xv.xv_gemm_small_m(X, Ws[i % nc], Y, ws), 3 * nc)
-            # a launch's time includes its split-K combine kernel where it has one (M > 8, > 4 segments)
-            per_launch = []
-            for k_, t_, _ in recs:
-                if k_ == "gemm_small_m":
-                    per_launch.append(t_)
-                elif k_ == "gemm_combine" and per_launch:
-                    per_launch[-1] += t_
-            ms = float(np.median(per_launch))
-            nbytes = 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)
-            gem[f"{name}_M{M}"] = {"N": N, "K": K, "splits": xv.xv_gemm_splits(N, K), "us": round(ms * 1e3, 2),
-                                   "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
-                                   "frac": round(nbytes / ms / 1e6 / peak, 4)}
-            del Ws
-            torch.cuda.empty_cache()
-    out["gemm_small_m"] = gem
+    def line(ms, nbytes):
+        return {"us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                "frac": round(nbytes / ms / 1e6 / peak, 4)}
 
-    # GDN verify: 32 heads of 128 x 128 fp32, k = 8 speculative steps after 1 replayed step
+    # small-M GEMM: every projection shape of the stack at 8 and 64 token rows, and the
+    # gate/up (17408 x 5120) and down (5120 x 17408) sweep over M in {1, 2, 4, 8, 9, 16}
+    gem, sweep = {}, {}
+    cases = [(M, N, K, name, f32, gem) for M in (8, 64)
+             for N, K, name, f32 in [(12352, 5120, "gdn_in", False), (5120, 4096, "gdn_out", False),
+                                     (14336, 5120, "attn_in", False), (5120, 6144, "attn_out", False),
+                                     (34816, 5120, "gate_up", False), (5120, 17408, "down", False),
+                                     (151936, 5120, "lm_head", True)]]
+    cases += [(M, N, K, name, False, sweep) for M in (1, 2, 4, 8, 9, 16)
+              for N, K, name in [(17408, 5120, "up17408"), (5120, 17408, "down17408")]]
+    W_cache = {}
+    for M, N, K, name, f32, dst in cases:
+        nc = copies_for(2 * N * K)
+        if (N, K) not in W_cache:
+            W_cache.clear()
+            torch.cuda.empty_cache()
+            W_cache[(N, K)] = [rnd((N, K), 0.02) for _ in range(nc)]
+        Ws = W_cache[(N, K)]
+        X = rnd((M, K))
+        Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
+        ws = xv.workspace(max(xv.xv_gemm_workspace_size(M, N, K), 256), device=device)
+        launch = lambda i: xv.xv_gemm_small_m(X, Ws[i % nc], Y, ws)
+        for i in range(nc):
+            launch(i)
+        ms = _back_to_back_ms(launch, 3 * nc)
+        nbytes = 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)
+        dst[f"{name}_M{M}"] = dict(N=N, K=K, splits=xv.xv_gemm_splits(N, K), **line(ms, nbytes))
+    W_cache.clear()
+    torch.cuda.empty_cache()
+    out["gemm_small_m"] = gem
+    out["gemm_sweep"] = sweep
+
+    # GDN verify: 32 heads of 128 x 128 fp32, k = 8 speculative steps after 1 replayed step (8 staged)
     H, D, k = 32, 128, 8
     gd = {}
     for B in (1, 8):
@@ -293,16 +317,14 @@ def kernel_rooflines(xv, device, peak):
         launch = lambda i: xv.xv_gdn_verify(states[i % nc], st, n, k, st, k, o, H * D, B, H, D, D, True)
         for i in range(nc):
             launch(i)
-        recs = _traced_median_ms(xv, launch, 3 * nc)
-        ms = float(np.median([t for kk, t, _ in recs if kk == "gdn"]))
+        ms = _back_to_back_ms(launch, 3 * nc)
         nbytes = 2 * state_bytes + 2 * (1 + k) * B * H * (3 * D + 2) + 2 * k * B * H * D
-        gd[f"B{B}"] = {"us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
-                       "frac": round(nbytes / ms / 1e6 / peak, 4)}
+        gd[f"B{B}"] = line(ms, nbytes)
         del states
         torch.cuda.empty_cache()
     out["gdn_verify"] = gd
 
-    # decode-row attention: 24 q / 4 kv heads of 256, 8 rows per sequence
+    # decode-row attention (split + combine): 24 q / 4 kv heads of 256, 8 rows per sequence
     Hq, Hkv, hd, R = 24, 4, 256, 8
     at = {}
     for L in (640, 2183, 131072):
@@ -320,19 +342,75 @@ def kernel_rooflines(xv, device, peak):
                                                       Lmax, L + R - 1, hd ** -0.5, outb, outb.stride(0), ws)
             for i in range(nc):
                 launch(i)
-            reps = max(3 * nc, 5)
-            recs = _traced_median_ms(xv, launch, reps)
-            split = [t for kk, t, _ in recs if kk == "attn_split"]
-            comb = [t for kk, t, _ in recs if kk == "attn_combine"]
-            ms = float(np.median(split)) + float(np.median(comb))
+            ms = _back_to_back_ms(launch, max(3 * nc, 5))
             nbytes = B * (4 * Hkv * (L + R - 1) * hd + 2 * 2 * R * Hq * hd)   # K+V of every visible position, q, out
-            at[f"L{L}_B{B}"] = {"us": round(ms * 1e3, 2), "split_us": round(float(np.median(split)) * 1e3, 2),
-                                "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
-                                "frac": round(nbytes / ms / 1e6 / peak, 4)}
+            at[f"L{L}_B{B}"] = line(ms, nbytes)
             del kcs, vcs
             torch.cuda.empty_cache()
     out["attn_decode_rows"] = at
+    out["timing"] = ("per launch over back-to-back launches between two CUDA events, inputs rotated through "
+                     "more than 3x L2 (cold every launch)")
     return out
+
+
+def gemm_chain_ms(xv, stk, cfg, M, reps, device):
+    """The step's 17 projection GEMMs alone, in step order, on the stack's own weights, issued back
+    to back with programmatic dependent launch as in the step (each still waits for the previous
+    one before reading its activations): device time per GEMM launch.  The weights (4.4 GB) stream
+    from HBM every round."""
+    import torch
+    from bit_exact_speculative_gb300.model import gdn_in_dim
+    H, F, V = cfg["hidden"], cfg["mlp"], cfg["vocab"]
+    w = stk.wd
+    plan = []
+    for l, kd in enumerate(cfg["kinds"]):
+        inner = cfg["gdn_heads"] * cfg["gdn_dv"] if kd == 0 else cfg["attn_hq"] * cfg["attn_hd"]
+        plan += [(w[f"{l}.w_in"], H, False), (w[f"{l}.w_out"], inner, False), (w[f"{l}.w_gu"], H, False),
+                 (w[f"{l}.w_down"], F, False)]
+    plan.append((w["lm_head"], H, True))
+    g = torch.Generator(device=device)
+    g.manual_seed(1)
+    Xs = {K: torch.randn((M, K), generator=g, device=device).to(torch.bfloat16) for _, K, _ in plan}
+    calls = []
+    for W, K, f32 in plan:
+        N = W.shape[0]
+        Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
+        ws = xv.workspace(max(xv.xv_gemm_workspace_size(M, N, K), 256), device=device)
+        calls.append((Xs[K], W.view(torch.bfloat16), Y, ws, 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)))
+    launch = lambda i: xv.xv_gemm_small_m(*calls[i % len(calls)][:4])
+    for i in range(len(calls)):
+        launch(i)
+    ms = _back_to_back_ms(launch, reps * len(calls))
+    return ms, sum(c[4] for c in calls) / len(calls), len(calls)
+
+
+def step_line(args, device, w, wd, batch, context, steps=10, warmup=3):
+    """ms per verify step and verified tok/s of one more (batch, context) configuration of the same
+    stack (KV caches drawn on the device)."""
+    import copy
+    import torch
+    a = copy.copy(args)
+    a.batch, a.context, a.steps, a.warmup, a.page_size, a.lmax = batch, context, steps, warmup, None, None
+    cfg, _, stk, toks = make_stack(a, device, 0, w=w, wd=wd, device_kv=True)
+    tok_dev = torch.from_numpy(toks).to(device)
+    k = a.k
+    for i in range(warmup):
+        stk.verify(tok_dev[i], k, logits=False)
+        stk.commit()
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        stk.verify(tok_dev[warmup + i], k, logits=False)
+        stk.commit()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del stk
+    torch.cuda.empty_cache()
+    return {"batch": batch, "context": context, "k": k, "steps": steps, "ms_per_step": round(ms, 4),
+            "value": round(batch * k / (ms / 1e3), 1), "unit": UNIT}
 
 
 # ------------------------------------------------------ one kernel alone
@@ -548,7 +626,8 @@ def run_gpu(args):
     ms_max = s_max * 1e3
     code = xv.xv_device_check()
 
-    # ---- per-kernel durations: the same steps with every launch bracketed by events
+    # ---- per-kernel durations (serialised: every launch bracketed by events, which breaks the
+    # programmatic overlap; used for shares only)
     xv.xv_trace_enable(64 * args.steps)
     for _ in range(args.steps):
         step(rnd)
@@ -562,10 +641,8 @@ def run_gpu(args):
         d[0] += 1
         d[1] += tms
         d[2] += nb
-    g = per_kind.get("gemm_small_m", [0, 0.0, 0])
-    gc = per_kind.get("gemm_combine", [0, 0.0, 0])    # split-K combines of the M > 8 narrow shapes
-    gemm_ms_per_launch = (g[1] + gc[1]) / max(g[0], 1)
-    gemm_bytes_per_launch = g[2] / max(g[0], 1)
+    # ---- the dominant kernel as it runs in the step: the step's GEMMs back to back
+    gemm_ms_per_launch, gemm_bytes_per_launch, _ = gemm_chain_ms(xv, stk, cfg, B * k, max(2, args.steps // 5), device)
     achieved = gemm_bytes_per_launch / (gemm_ms_per_launch / 1e3) / 1e9
     peak, peak_kind = peaks()
     gemm_bytes_step = sum(2 * N * K + 2 * B * k * K + B * k * N * o for N, K, o in gemm_shapes(cfg, B * k))
@@ -591,9 +668,16 @@ def run_gpu(args):
     e2e_value, _, _ = job_throughput(e2e_s, B * k * args.steps, device)
     barrier()
 
-    rooflines = None
+    rooflines, more = None, None
     if rank == 0 and world == 1 and not args.no_kernel_rooflines:
+        wd = stk.wd
         del stk
+        torch.cuda.empty_cache()
+        more = {}
+        for bb, ctx in ((1, 131072), (8, 2183), (8, 131072)):
+            if (bb, ctx) != (B, args.context):
+                more[f"batch{bb}_ctx{ctx}"] = step_line(args, device, w_host, wd, bb, ctx)
+        del wd
         torch.cuda.empty_cache()
         rooflines = kernel_rooflines(xv, device, peak)
 
@@ -616,13 +700,17 @@ def run_gpu(args):
                          "traffic_source": ("ncu dram bytes per algorithmic byte of the down projection (M=8) "
                                             "x this launch average" if traffic_ratio else None),
                          "algorithmic_bytes_per_launch": round(gemm_bytes_per_launch),
-                         "launches_per_step": n_gemm, "ms_per_launch": round(gemm_ms_per_launch, 5)},
+                         "launches_per_step": n_gemm, "ms_per_launch": round(gemm_ms_per_launch, 5),
+                         "timing": "the step's GEMMs alone, back to back with programmatic launch as in the step, "
+                                   "CUDA events around the chain"},
             "step_roofline": {"algorithmic_bytes": gemm_bytes_step,
                               "achieved_gbs": round(gemm_bytes_step / (ms_max / args.steps / 1e3) / 1e9, 1),
                               "frac": round(gemm_bytes_step / (ms_max / args.steps / 1e3) / 1e9 / peak, 4)},
             "kernels": {n: {"launches": v[0], "ms_total": round(v[1], 4),
                             "share": round(v[1] / max(sum(x[1] for x in per_kind.values()), 1e-9), 4)}
                         for n, v in sorted(per_kind.items(), key=lambda kv: -kv[1][1])},
+            "kernels_timing": "every launch bracketed by events (serialised, no programmatic overlap): shares only",
+            "more_configs": more,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(B * k * 4),
                     "d2h_bytes_per_step": int(B * k * 4 + B * 4)},
             "clocks": clk.summary(),
@@ -664,13 +752,15 @@ def oracle_sample(args, cfg, w, budget_s=12.0):
     """The oracle decoding verify positions of the same workload until ~budget_s of CPU time."""
     st, toks = oracle_session(args, cfg, w)
     n, t0 = 0, time.perf_counter()
-    while n < args.k and (n == 0 or time.perf_counter() - t0 < budget_s):
+    limit = min(len(toks), st.Lmax - st.len)
+    while n < limit and (n == 0 or time.perf_counter() - t0 < budget_s):
         st.decode(int(toks[n]))
         n += 1
     dt = time.perf_counter() - t0
     return {"value": round(n / dt, 4), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
-            "sample": f"{n} of the {args.k} verify positions of one sequence (the oracle verifies by decoding "
-                      f"them one at a time), context {args.context}, full-size weights; {dt:.1f} s"}
+            "sample": f"{n} verify positions of one sequence ({n / args.k:.1f} verify steps of k = {args.k}; the "
+                      f"oracle verifies by decoding them one at a time), context {args.context}, full-size "
+                      f"weights; {dt:.1f} s"}
 
 
 def run_reference(args):
