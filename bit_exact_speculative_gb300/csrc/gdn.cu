@@ -496,6 +496,20 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
     }
     __syncthreads();
     griddep_wait();
+    // The beta and gate scalars first (plain loads by warps 1.., so they are queued ahead of the
+    // copies and warp 0 is free to issue those), then thread 0 requests the step inputs and the
+    // slabs in order.
+    const int gtid = tid - 32, gthreads = nthreads - 32;   // the gate threads (all warps but 0)
+    uint16_t bg[2] = {0, 0};   // entries gtid and gtid + gthreads of (beta, gate) x step
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int idx = gtid + q * gthreads;
+        if (gtid >= 0 && idx < 2 * total) {
+            long long row;
+            const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
+            bg[q] = (idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
+        }
+    }
     if (tid == 0) {
         mbar_arrive_expect_tx(bar_in, static_cast<uint32_t>(total) * (4 * DK + 2 * A.dv));
         if (A.max_commit > 0) {
@@ -520,16 +534,6 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
                 tma_load_2d(smem_u32(slab + cb * SLAB * SW_COLS), &M.m[6], cb * SW_COLS, grow + w * SLAB, bw);
         }
     }
-    uint16_t bg[2] = {0, 0};   // entries tid and tid + nthreads of (beta, gate) x step
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * nthreads;
-        if (idx < 2 * total) {
-            long long row;
-            const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
-            bg[q] = (idx & 1) ? src.gate[row * src.gate_stride + h] : src.beta[row * src.gate_stride + h];
-        }
-    }
     int nc = A.n_commit ? A.n_commit[b] : A.n_fixed;
     if (nc < 0 || nc > A.max_commit) {
         if (tid == 0) atomicOr(A.err, ERR_BAD_COUNT);
@@ -537,10 +541,10 @@ __global__ void __launch_bounds__(32 * MAX_SLABS_PER_HEAD, 1)
     }
     mbar_wait(bar_in, 0, A.err);
     normalise_all<DK>(steps, rawq, rawk, total, A.l2 != 0, tid, nthreads);
-    for (int idx = tid; idx < 2 * total; idx += nthreads) {
+    for (int idx = gtid; gtid >= 0 && idx < 2 * total; idx += gthreads) {
         long long row;
         const GdnStepsDev& src = step_src(A, b, idx >> 1, &row);
-        const uint16_t raw = idx < 2 * nthreads ? (idx >= nthreads ? bg[1] : bg[0])
+        const uint16_t raw = idx < 2 * gthreads ? (idx >= gthreads ? bg[1] : bg[0])
                                                 : ((idx & 1) ? src.gate[row * src.gate_stride + h]
                                                              : src.beta[row * src.gate_stride + h]);
         const float x = gate_value(raw, idx & 1, src.raw_gates != 0);
@@ -698,7 +702,7 @@ xv_status gdn_launch(float* state, const GdnStepsDev& pending, const int32_t* n_
     int sms = 0;
     if (xv_status st = device_sm_count(&sms)) return st;
     const size_t head_smem = dk == 128 ? HeadSmem<128>(max_steps, n_out, dv).total : HeadSmem<64>(max_steps, n_out, dv).total;
-    const bool wide = static_cast<long long>(B) * H >= sms && dv / SLAB <= MAX_SLABS_PER_HEAD &&
+    const bool wide = static_cast<long long>(B) * H >= sms && dv / SLAB >= 2 && dv / SLAB <= MAX_SLABS_PER_HEAD &&
                       2 * (head_smem + 1024) <= static_cast<size_t>(XV_GDN_SMEM_SM) && B * H < (1 << 30);
     trace_pre(s);
     xv_status st;

@@ -217,3 +217,72 @@ def test_hundred_runs_identical(xv):
         else:
             assert same_bits(S, ref_S) and same_bits(o, ref_o)
     assert xv.xv_device_check() == 0
+
+
+def grouped_inputs(seed, B, T, Hv, Hk, d):
+    """Step rows [B*T, 2*Hk*d + Hv*d] = q | k (Hk heads, raw) | v (Hv heads) and gates [B*T, 2*Hv]."""
+    rows = B * T
+    q = synth.normal_bf16(seed, synth.tid("gw.q"), (rows, Hk * d))
+    k = synth.normal_bf16(seed, synth.tid("gw.k"), (rows, Hk * d))
+    v = synth.normal_bf16(seed, synth.tid("gw.v"), (rows, Hv * d))
+    bl = synth.normal_bf16(seed, synth.tid("gw.b"), (rows, Hv))
+    al = synth.normal_bf16(seed, synth.tid("gw.a"), (rows, Hv))
+    beta, gate = oracle.gdn_gates(bl, al)
+    return np.ascontiguousarray(np.concatenate([q, k, v], axis=1)), np.ascontiguousarray(np.concatenate([beta, gate], 1))
+
+
+@pytest.mark.parametrize("Hv,Hk,d", [(32, 32, 64), (32, 16, 128), (48, 48, 128)])
+def test_wide_batch_equals_each_sequence_alone_and_oracle(xv, Hv, Hk, d):
+    """A batch wide enough for the per-head kernel (B * heads >= SMs: a CTA per head, 4 rows per
+    thread) against each sequence alone (the per-slab kernel, a row per thread): outputs and
+    committed states bit for bit, with a different replay count per sequence, grouped q/k heads
+    and dk = 64 or 128; sequence 0 of the batch against the oracle's steps."""
+    B, K = 8, 8
+    qkv_h, gates_h = grouped_inputs(8, B, K, Hv, Hk, d)
+    qkv, gates = dev(qkv_h), dev(gates_h)
+    S0h = synth.normal_f32(8, synth.tid("gw.S0"), (B, Hv, d, d), sigma=0.1)
+    S0 = dev(S0h)
+    n_h = np.array([1, 8, 3, 0, 5, 2, 7, 4], dtype=np.int32)
+
+    def view(buf, g, row0=0):
+        base, gg = buf[row0:], g[row0:]
+        return xv.gdn_steps(base, base[:, Hk * d:], base[:, 2 * Hk * d:], gg, gg[:, Hv:], buf.shape[1], 2 * Hv, K)
+
+    Sb = S0.clone()
+    o = torch.full((B * K, Hv * d), -1, dtype=torch.int16, device="cuda")
+    xv.xv_gdn_verify_grouped(Sb, view(qkv, gates), dev(n_h), K, view(qkv, gates), K, o, Hv * d, B, Hv, Hk, d, d, True)
+    for b in range(B):
+        Sa = S0[b:b + 1].clone()
+        oa = torch.full((K, Hv * d), -1, dtype=torch.int16, device="cuda")
+        pa = view(qkv, gates, b * K)
+        xv.xv_gdn_verify_grouped(Sa, pa, dev(n_h[b:b + 1]), K, pa, K, oa, Hv * d, 1, Hv, Hk, d, d, True)
+        assert same_bits(Sa[0], Sb[b]) and same_bits(oa, o[b * K:(b + 1) * K]), f"sequence {b} differs in the batch"
+    assert xv.xv_device_check() == 0
+    # the oracle: sequence 0 replays n_h[0] pending rows into the state, then speculates K rows
+    S = S0h[0].astype(np.float64)
+    q = qkv_h[:, :Hk * d].reshape(B * K, Hk, d)
+    k = qkv_h[:, Hk * d:2 * Hk * d].reshape(B * K, Hk, d)
+    v = qkv_h[:, 2 * Hk * d:].reshape(B * K, Hv, d)
+    for t in range(n_h[0]):
+        oracle.gdn_step_heads_grouped(S, q[t], k[t], v[t], gates_h[t, :Hv], gates_h[t, Hv:], True)
+    assert_state_close(host(Sb)[0], S)
+    og = host_u16(o)
+    Ss = S.copy()
+    for t in range(K):
+        ob = oracle.gdn_step_heads_grouped(Ss, q[t], k[t], v[t], gates_h[t, :Hv], gates_h[t, Hv:], True)
+        assert_bf16_close(og[t].reshape(Hv, d), ob, what=f"speculative step {t}")
+
+
+def test_wide_batch_decode_equals_alone(xv):
+    """Decode steps (a replayed step that emits its output) at B = 8 with dk = dv = 64 (the per-head
+    kernel) equal the same steps of each sequence alone."""
+    B, T, h, d = 8, 3, 32, 64
+    qkv_h, gates_h = make_inputs(9, B, T, H=h, dk=d, dv=d, prenorm=False)
+    qkv, gates = dev(qkv_h), dev(gates_h)
+    S0 = dev(init_state(9, B, H=h, dk=d, dv=d))
+    Sb = S0.clone()
+    ob = decode_seq(xv, Sb, qkv, gates, B, T, H=h, dk=d, dv=d, l2=True)
+    for b in range(B):
+        Sa = S0[b:b + 1].clone()
+        oa = decode_seq(xv, Sa, qkv[b * T:(b + 1) * T], gates[b * T:(b + 1) * T], 1, T, H=h, dk=d, dv=d, l2=True)
+        assert same_bits(Sa[0], Sb[b]) and same_bits(oa[0], ob[b]), f"sequence {b}"
