@@ -181,17 +181,12 @@ __device__ __forceinline__ void load_q_tile(uint8_t* sq, const AttnArgs& A, cons
 // and the absolute tile positions only, so a verify row gets the bits of the decode row at its
 // position, whichever CTA and whichever neighbours it has.  MULTI = false is the launch with one
 // item per CTA (CTA i takes item i), with the cross-item hand-offs compiled out.
-template <int HD, bool MULTI, int HS>
+template <int HD, bool MULTI>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs A) {
     griddep_launch();
     using S = AttnShape<HD>;
     constexpr int CB = S::CB, SK = S::SK, SV = S::SV, TILE_BYTES = S::TILE_BYTES, BLK = S::BLK;
-    // HS column slices: this CTA's P V covers columns [hslice * ON, (hslice + 1) * ON) of the head
-    // (CBS of its CB column blocks); S, m, l and P are those of the whole item in every slice
-    static_assert(!MULTI || HS == 1, "the persistent launch takes whole items");
-    static_assert(CB % HS == 0, "a slice is whole column blocks");
-    constexpr int CBS = CB / HS, ON = HD / HS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_abort;
@@ -224,9 +219,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = A.R * A.G, nrt = (rows + 63) / 64;
     const int n_items = A.nsplit * nrt * A.Hkv * A.B;
-    const int hslice = MULTI ? 0 : static_cast<int>(blockIdx.x) % HS;
-    const int it0 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x) * n_items / gridDim.x)
-                          : static_cast<int>(blockIdx.x) / HS;
+    const int it0 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x) * n_items / gridDim.x) : blockIdx.x;
     const int it1 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_items / gridDim.x) : it0 + 1;
     griddep_wait();
     int first = it0;
@@ -315,12 +308,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                     }
                     const uint32_t fb = isK ? fullK(st) : fullV(st);
                     const uint32_t dst = isK ? sK(st) : sV(st);
-                    mbar_arrive_expect_tx(fb, isK ? TILE_BYTES : CBS * BLK);
+                    mbar_arrive_expect_tx(fb, TILE_BYTES);
                     int row;
                     const int z = kv_page(A.kv, I.b, I.p_begin + i * T, &row, A.err) * A.Hkv + I.g;
 #pragma unroll
-                    for (int cb = 0; cb < (isK ? CB : CBS); ++cb)
-                        tma_load_3d(dst + cb * BLK, map, (isK ? cb : hslice * CBS + cb) * 64, row, z, fb);
+                    for (int cb = 0; cb < CB; ++cb) tma_load_3d(dst + cb * BLK, map, cb * 64, row, z, fb);
                     ++t;
                 }
             }
@@ -332,7 +324,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                 if (WW(fullV(st), (tl / SV) & 1u)) {
                     for (int idx = first_row * 8 + lane; idx < T * 8; idx += 32)
 #pragma unroll
-                        for (int cb = 0; cb < CBS; ++cb)
+                        for (int cb = 0; cb < CB; ++cb)
                             *reinterpret_cast<uint4*>(smem + (sV(st) - base) + cb * BLK + idx * 16) = make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -348,11 +340,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     } else if (warp == 6) {
         // ---- MMA issuer: Q K^T of tile t+1 goes out before P V of tile t (within an item)
         if (lane == 0) {
-            constexpr uint32_t IDS = idesc_bf16_f32(128, T), IDO = idesc_bf16_f32(128, ON, true);
+            constexpr uint32_t IDS = idesc_bf16_f32(128, T), IDO = idesc_bf16_f32(128, HD, true);
             // the next 64 dims of V sit one block further; with a single block the field is never
             // used and holds the group stride, which keeps every address of the operand inside
             // its stage under either reading of the two fields
-            constexpr uint32_t VBLK = CBS > 1 ? BLK : 1024;
+            constexpr uint32_t VBLK = CB > 1 ? BLK : 1024;
             auto qk = [&](int tt) -> bool {
                 const int st = tt % SK;
                 if (!W(fullK(st), (tt / SK) & 1u)) return false;
@@ -434,10 +426,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             const bool live = grow < rows && len > I.p_begin;
             const int r = grow / A.G, h = I.g * A.G + grow % A.G;
             const long long idx = ((static_cast<long long>(I.b) * A.R + r) * A.Hq + h) * A.nsplit + I.split;
-            float* op = A.opart + idx * HD + hslice * ON;
+            float* op = A.opart + idx * HD;
             const float2 ml = ml_sm[rho];
 #pragma unroll 1
-            for (int c = 0; c < CBS; ++c) {
+            for (int c = 0; c < HD / 64; ++c) {
                 float o[64];
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
@@ -448,7 +440,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                         *reinterpret_cast<float4*>(op + c * 64 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
                 }
             }
-            if (live && hslice == 0) A.ml[idx] = ml;   // every slice holds the same m and l
+            if (live) A.ml[idx] = ml;
             tc_fence_before();
             mbar_arrive(ofree);   // O (and ml_sm) may be overwritten by the next item
             t += I.ntiles;
@@ -514,7 +506,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                     if (!WW(pfree((tt - 1) & 1), ((tt - 1) >> 1) & 1u)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < CBS; ++c) {
+                    for (int c = 0; c < HD / 64; ++c) {
                         float o[64];
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tO + lane_off + c * 64 + q4 * 16, o + q4 * 16);
@@ -709,36 +701,23 @@ template <int HD>
 xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int B, cudaStream_t s) {
     using S = AttnShape<HD>;
     int sms = 0;
-    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(attn_split_kernel<HD, true, 1>), S::SMEM, false,
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(attn_split_kernel<HD, true>), S::SMEM, false,
                                         "attn: set shared memory size"))
         return st;
-    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(attn_split_kernel<HD, false, 1>), S::SMEM, false,
+    if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(attn_split_kernel<HD, false>), S::SMEM, false,
                                         "attn: set shared memory size"))
         return st;
     if (xv_status st = device_sm_count(&sms)) return st;
     // past two waves of items, one persistent CTA per SM (the shared-memory plan admits one);
     // otherwise one CTA per item (measured in the verify step: with 160 items the persistent
-    // launch was 4 us slower, with 1028 and 8224 items 15 and 218 us faster), and when the items
-    // leave most SMs idle, each item's P V is split over HS CTAs by columns (each recomputes the
-    // item's identical S, m, l and P and loads only its columns of V), up to one CTA per SM
+    // launch was 4 us slower, with 1028 and 8224 items 15 and 218 us faster)
     const long long n_items = static_cast<long long>(a.nsplit) * ((a.R * a.G + 63) / 64) * a.Hkv * B;
     if (n_items > (1ll << 30)) return fail(XV_ERR_UNSUPPORTED, "attn: %lld work items", n_items);
     const bool multi = n_items > 2ll * sms;
-    int hs = 1;
-    if (!multi && HD == 256) hs = 4 * n_items <= sms ? 4 : 2 * n_items <= sms ? 2 : 1;
+    dim3 grid(static_cast<unsigned>(multi ? sms : n_items));
     trace_pre(s);
-    if (multi) {
-        launch_k(attn_split_kernel<HD, true, 1>, dim3(sms), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
-    } else if (hs == 1) {
-        launch_k(attn_split_kernel<HD, false, 1>, dim3(static_cast<unsigned>(n_items)), dim3(ATTN_THREADS), S::SMEM, s,
-                 tmK, tmV, a);
-    } else if constexpr (HD == 256) {
-        auto kern = hs == 4 ? attn_split_kernel<HD, false, 4> : attn_split_kernel<HD, false, 2>;
-        if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(kern), S::SMEM, false,
-                                            "attn: set shared memory size"))
-            return st;
-        launch_k(kern, dim3(static_cast<unsigned>(n_items * hs)), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
-    }
+    if (multi) launch_k(attn_split_kernel<HD, true>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
+    else launch_k(attn_split_kernel<HD, false>, dim3(grid), dim3(ATTN_THREADS), S::SMEM, s, tmK, tmV, a);
     // bound: every sequence at the longest length the launch is sized for
     const long long bytes = 4ll * B * a.Hkv * a.max_len * HD + 2ll * B * a.R * a.Hq * HD +
                             4ll * B * a.R * a.Hq * a.nsplit * (HD + 2);
