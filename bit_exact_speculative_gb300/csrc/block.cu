@@ -92,6 +92,7 @@ Carve carve(const Dims& d, int B, int kmax, int Lmax, uint8_t* base) {
     const int M = B * kmax;
     size_t off = 0;
     auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += r256(bytes); return p; };
+    // the residual stream comes first: the header promises the final hidden state at offset 0
     c.x = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.H * 2));
     c.xn = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.H * 2));
     c.proj = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * (d.ain > 0 ? d.ain : 8) * 2));

@@ -231,6 +231,13 @@ class HybridStack:
         self._last_k = k
         return lg, self.argmax[: self.B * k], self.n_accept
 
+    def hidden(self) -> torch.Tensor:
+        """The residual stream after the last layer of the last verify (the hidden state before
+        the final RMSNorm), bf16 bits [B*k, H]: a view of the workspace, valid until the next call
+        that uses it."""
+        n = self.B * self._last_k * self.cfg["hidden"]
+        return self.ws[: 2 * n].view(torch.int16).view(self.B * self._last_k, self.cfg["hidden"])
+
     def commit(self, n_keep: torch.Tensor | None = None, stream=None):
         """Keeps n_keep[b] positions of the last verify (default: the accepted drafts + 1)."""
         if n_keep is None:

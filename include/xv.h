@@ -421,7 +421,11 @@ size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int 
  * position before them (0..k-1).  Requires 1 <= k <= st->kmax, B == st->B,
  * B*k <= XV_GEMM_M_MAX, st->max_ctx + k <= Lmax.  Appends the k rows to the KV
  * caches (uncommitted), replays the pending GDN steps into the states and
- * records this call's GDN inputs as the next pending steps.
+ * records this call's GDN inputs as the next pending steps.  Once the call's
+ * work has run on the stream, the workspace begins (offset 0) with the
+ * residual stream after the last layer, i.e. the hidden state before the final
+ * RMSNorm: bf16 [B*k][H], row b*k + j for position j of sequence b; it stays
+ * there until the workspace is used again.
  * Errors: XV_ERR_ARG (invalid configuration, incomplete weights or state, null
  * tokens/argmax/n_accept, k outside [1, kmax], the previous verify not yet
  * committed, st->max_ctx + k > Lmax, pending_rows out of range),

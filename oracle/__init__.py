@@ -86,6 +86,7 @@ def lib(f32: bool = False):
         L.orc_gdn_in_dim.argtypes, L.orc_gdn_in_dim.restype = [vp], i32
         L.orc_attn_in_dim.argtypes, L.orc_attn_in_dim.restype = [vp], i32
         L.orc_decode_token.argtypes = [vp, vp, vp, ctypes.c_int32, vp]
+        L.orc_layer_token.argtypes = [vp, vp, vp, i32, vp, vp]
         if f32:
             _lib32 = L
         else:
@@ -316,8 +317,7 @@ class Stack:
             self.vc[l][...] = vc[l]
         self.len = n
 
-    def decode(self, token: int) -> np.ndarray:
-        """One token through the stack; returns fp64 logits [V]."""
+    def _seq(self):
         L = len(self.cfg["kinds"])
         Sp = (vp * L)(*[_p(self.S[l]) if l in self.S else None for l in range(L)])
         Kp = (vp * L)(*[_p(self.kc[l]) if l in self.kc else None for l in range(L)])
@@ -325,11 +325,33 @@ class Stack:
         Cp = (vp * L)(*[_p(self.conv[l]) if l in self.conv else None for l in range(L)])
         seq = _Seq(ctypes.cast(Sp, vp).value, ctypes.cast(Kp, vp).value, ctypes.cast(Vp, vp).value,
                    self.Lmax, self.len, ctypes.cast(Cp, vp).value)
+        return seq, (Sp, Kp, Vp, Cp)
+
+    def decode(self, token: int) -> np.ndarray:
+        """One token through the stack; returns fp64 logits [V]."""
+        seq, keep = self._seq()
         logits = np.empty(self.cfg["V"], dtype=np.float64)
         lib(self._f32).orc_decode_token(ctypes.byref(self._c), ctypes.byref(self._W), ctypes.byref(seq),
                                         int(token), _p(logits))
         self.len = seq.len
         return logits
+
+    def layer_rows(self, layer: int, x, mid: bool = False):
+        """Layer ``layer`` alone over n consecutive positions len .. len + n - 1, each row of x
+        (bf16 [n, H]) being that position's residual input; returns the layer's outputs [n, H]
+        (with ``mid``, also the residual between the mixer and the MLP).  The layer's state
+        advances n steps; ``len`` is left as it is, so that the next layer takes the same
+        positions."""
+        out = _c(x, np.uint16).copy()
+        mids = np.empty_like(out)
+        len0 = self.len
+        for j in range(out.shape[0]):
+            self.len = len0 + j
+            seq, keep = self._seq()
+            lib(self._f32).orc_layer_token(ctypes.byref(self._c), ctypes.byref(self._W), ctypes.byref(seq),
+                                           int(layer), _p(out[j]), _p(mids[j]))
+        self.len = len0
+        return (out, mids) if mid else out
 
     def verify(self, tokens):
         """k tokens -> logits [k,V]; by definition k sequential decodes."""

@@ -466,32 +466,43 @@ static void attn_mixer(const orc_cfg* c, orc_seq* s, int layer, const uint16_t* 
     free(p); free(o);
 }
 
-/* One decode step of one sequence: token in, logits [V] (double) out; the
- * GDN states advance one step, the token's K/V land at position len, and
- * len grows by one. */
-void orc_decode_token(const orc_cfg* c, const orc_weights* w, orc_seq* s, int32_t token, double* logits) {
+/* Layer l of the stack for one position (s->len): the residual row x (bf16 [H]) in place through
+ * x <- x + mixer(rmsnorm(x)), then x <- x + down(silu(gate) * up) of rmsnorm(x), each sum
+ * rounded to bf16; mid (bf16 [H], or NULL) receives x between the two.  The layer's GDN state and
+ * convolution state advance one step, or the position's K/V land at s->len; s->len is left as
+ * it is. */
+void orc_layer_token(const orc_cfg* c, const orc_weights* w, orc_seq* s, int l, uint16_t* x, uint16_t* mid) {
     int H = c->H, F = c->F;
-    uint16_t* x = (uint16_t*)malloc(sizeof(uint16_t) * H);
     uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * H);
     uint16_t* y = (uint16_t*)malloc(sizeof(uint16_t) * H);
     uint16_t* gu = (uint16_t*)malloc(sizeof(uint16_t) * 2 * F);
     uint16_t* act = (uint16_t*)malloc(sizeof(uint16_t) * F);
+    orc_rmsnorm(x, w->norm1[l], H, c->eps, xn);
+    if (c->kind[l] == 0)
+        gdn_mixer(c, s->S[l], c->gdn_conv > 0 ? s->conv[l] : NULL, c->gdn_conv > 0 ? w->conv_w[l] : NULL,
+                  c->gdn_onorm ? w->onorm[l] : NULL, xn, w->w_in[l], w->w_out[l], y);
+    else attn_mixer(c, s, l, xn, w->w_in[l], w->w_out[l], y);
+    residual(x, y, H);
+    if (mid) memcpy(mid, x, sizeof(uint16_t) * H);
+    orc_rmsnorm(x, w->norm2[l], H, c->eps, xn);
+    proj(xn, w->w_gu[l], 2 * F, H, gu);
+    orc_swiglu(gu, gu + F, F, act);
+    proj(act, w->w_down[l], H, F, y);
+    residual(x, y, H);
+    free(xn); free(y); free(gu); free(act);
+}
+
+/* One decode step of one sequence: token in, logits [V] (double) out; the
+ * GDN states advance one step, the token's K/V land at position len, and
+ * len grows by one. */
+void orc_decode_token(const orc_cfg* c, const orc_weights* w, orc_seq* s, int32_t token, double* logits) {
+    int H = c->H;
+    uint16_t* x = (uint16_t*)malloc(sizeof(uint16_t) * H);
+    uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * H);
     memcpy(x, w->embed + (int64_t)token * H, sizeof(uint16_t) * H);
-    for (int l = 0; l < c->n_layers; ++l) {
-        orc_rmsnorm(x, w->norm1[l], H, c->eps, xn);
-        if (c->kind[l] == 0)
-            gdn_mixer(c, s->S[l], c->gdn_conv > 0 ? s->conv[l] : NULL, c->gdn_conv > 0 ? w->conv_w[l] : NULL,
-                      c->gdn_onorm ? w->onorm[l] : NULL, xn, w->w_in[l], w->w_out[l], y);
-        else attn_mixer(c, s, l, xn, w->w_in[l], w->w_out[l], y);
-        residual(x, y, H);
-        orc_rmsnorm(x, w->norm2[l], H, c->eps, xn);
-        proj(xn, w->w_gu[l], 2 * F, H, gu);
-        orc_swiglu(gu, gu + F, F, act);
-        proj(act, w->w_down[l], H, F, y);
-        residual(x, y, H);
-    }
+    for (int l = 0; l < c->n_layers; ++l) orc_layer_token(c, w, s, l, x, NULL);
     orc_rmsnorm(x, w->final_norm, H, c->eps, xn);
     orc_gemm(xn, H, w->lm_head, 1, c->V, H, logits);
     s->len += 1;
-    free(x); free(xn); free(y); free(gu); free(act);
+    free(x); free(xn);
 }

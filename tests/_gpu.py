@@ -20,6 +20,23 @@ Tolerances (stated once, used everywhere):
     oracle's top-1/top-2 margin exceeds twice the max bound (no pair of
     logits within the bound can swap there); each such check must find a
     decisive row;
+  - one layer of the stack, teacher forced (the oracle's layer fed the GPU's
+    own bf16 residual input x and the same layer state): the layer is
+    x -> mid = bf16(x + y1) -> out = bf16(mid + y2) with y1 the mixer's and y2
+    the MLP's bf16 output.  If each of y1, y2 carries at most the per-output
+    error 2e-2 * RMS and each residual sum rounds the other way at most once
+    (a flip costs the bf16 spacing at that element), element i satisfies
+    |err_i| <= 2e-2 * (RMS(y1) + RMS(y2)) + spacing(mid_i) + spacing(out_i)
+    (y1, y2, mid, out from the double oracle).  The MLP is three storage
+    points deep, and on the 5120-wide stack its 17408 bf16 SwiGLU values, each
+    of which may round the other way, move a faithful single-precision
+    evaluation of y2 by up to 2.3% of RMS(y2) at the worst of 10240 elements,
+    past that bound; so element i may also deviate by up to 3 * max|spread|,
+    the spread being the single-precision oracle's layer output minus the
+    double one on the same inputs (as for the logits).  RMS(err) <=
+    max(2e-2 * RMS(out - x), 3 * RMS(spread)).  (The bare 2e-2 * RMS(out) per
+    element rejects the single-precision evaluation there too: one flip at an
+    element of magnitude 16..32 costs 0.125.)
   - GPU vs GPU comparisons: 0 differing bits.
 """
 import numpy as np
@@ -109,6 +126,40 @@ def assert_argmax(ids, got, ref, max_bound, min_decisive=1):
             decisive += 1
     assert decisive >= min_decisive, f"{decisive} decisive rows (margin > {2 * max_bound:.3e}), {min_decisive} needed"
     return decisive
+
+
+def bf16_spacing(v) -> np.ndarray:
+    """The gap from |v| to the next bf16 value above it, 2^(floor(log2 |v|) - 7); 0 at 0."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, e = np.frexp(a)
+    return np.where(a > 0, np.ldexp(1.0, e - 8), 0.0)
+
+
+def layer_bound(x_in, mid, out, rel=BF16_REL):
+    """The per-element bound and the RMS bound of a teacher-forced layer output from the
+    per-output error and the residual roundings alone (bf16 bits of the residual input, the
+    oracle's mid residual and its output; see the module docstring)."""
+    x, m, o = f64(x_in), f64(mid), f64(out)
+    per = rel * (rms(m - x) + rms(o - m)) + bf16_spacing(m) + bf16_spacing(o)
+    return per, rel * rms(o - x)
+
+
+def assert_layer_close(got_u16, x_in, mid, out, out32, rel=BF16_REL, what=""):
+    """got: the GPU's layer output (bf16 bits [n, H]); x_in its residual input; mid, out: the
+    double oracle's layer run on x_in, out32 the single-precision oracle's.  Returns the largest
+    err / per-element bound."""
+    g = f64(got_u16)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    per, rms_bound = layer_bound(x_in, mid, out, rel)
+    spread = f64(out32) - f64(out)
+    per = np.maximum(per, SPREAD_FACTOR * float(np.max(np.abs(spread))))
+    rms_bound = max(rms_bound, SPREAD_FACTOR * rms(spread))
+    e = np.abs(g - f64(out))
+    worst = float(np.max(e / per))
+    i = np.unravel_index(int(np.argmax(e / per)), e.shape)
+    assert worst <= 1.0, f"{what}: err {e[i]:.3e} at {i} > bound {per[i]:.3e}"
+    assert rms(e) <= rms_bound, f"{what}: RMS err {rms(e):.3e} > {rel} * RMS(out - x) = {rms_bound:.3e}"
+    return worst
 
 
 def assert_state_close(got, ref, rel=STATE_REL, what="state"):

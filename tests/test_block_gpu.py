@@ -9,7 +9,7 @@ import torch
 import oracle
 from synth import workloads
 from _block import gpu_stack, kv_host, oracle_logits, oracle_stack, restore, snapshot
-from _gpu import assert_argmax, assert_block_close, dev, host, rms, same_bits
+from _gpu import assert_argmax, assert_block_close, assert_layer_close, dev, host, host_u16, rms, same_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -437,3 +437,37 @@ def test_stack_prefill_chunks_equal(stack):
     for lg, lgv in res:
         assert same_bits(lg, lgS[:, -1])
         assert same_bits(lgv, lgvS)
+
+
+# ------------------------------------------------------------ layer by layer, teacher forced
+
+@pytest.mark.parametrize("name,lens,k", [("TINY", [128, 37], 4), ("TINY_FULL", [128, 5, 77, 250], 4),
+                                         ("STACK", [2183], 8)])
+def test_layers_teacher_forced_vs_oracle(stack, name, lens, k):
+    """Each layer on its own: stacks of the first d layers (d = 1 .. L, the same weights and
+    states) give the residual stream after layer d (the hidden state the verify leaves at the
+    start of its workspace); the oracle's layer d, fed the GPU's residual input to it, must land
+    within the per-layer bound.  TINY_FULL at 4 x 4 rows takes the M > 8 paths."""
+    if name == "STACK":
+        cfg, w, wd = stack
+    else:
+        cfg = getattr(workloads, name)
+        w = workloads.weights(cfg, seed=0)
+        wd = {n: dev(v) for n, v in w.items()}
+    B, Lmax, nl = len(lens), max(lens) + 64, len(cfg["kinds"])
+    toks = workloads.draft_tokens(cfg, 0, 0, B, k)
+    kv = kv_host(cfg, lens, Lmax)
+    xs = [w["embed"][toks.reshape(-1)]]
+    for d in range(1, nl + 1):
+        A = gpu_stack(dict(cfg, kinds=cfg["kinds"][:d]), w, B, k, Lmax, lens, weights_dev=wd, kv=kv)
+        A.verify(dev(toks), k, logits=False)
+        xs.append(host_u16(A.hidden()).copy())
+        del A
+    for b in range(B):
+        rows = slice(b * k, (b + 1) * k)
+        o64 = oracle_stack(cfg, w, b, B, lens, Lmax)
+        o32 = oracle_stack(cfg, w, b, B, lens, Lmax, f32=True)
+        for l in range(nl):
+            out, mid = o64.layer_rows(l, xs[l][rows], mid=True)
+            out32 = o32.layer_rows(l, xs[l][rows])
+            assert_layer_close(xs[l + 1][rows], xs[l][rows], mid, out, out32, what=f"{name} sequence {b} layer {l}")

@@ -792,6 +792,59 @@ def test_full_attention_layer_composition():
         np.testing.assert_allclose(logits, _np_logits(w, x2), rtol=1e-12, atol=1e-13)
 
 
+def test_layer_rows_compose_to_sequential_decode():
+    """The one-layer entry point that per-layer comparisons feed (each layer given a residual
+    input from outside): running the layers one after another over the same k positions, from
+    the embedding rows, and finishing with the final norm and the LM head gives the logits of k
+    sequential decodes bit for bit, leaves the same GDN state and KV cache, and does not move the
+    position."""
+    cfg = _tiny_cfg()
+    w = _tiny_weights(cfg)
+    toks = [4, 9, 1, 7]
+    a, b = oracle.Stack(cfg, w, Lmax=16), oracle.Stack(cfg, w, Lmax=16)
+    a.verify([3, 3])
+    b.verify([3, 3])
+    la = a.verify(toks)
+    x = w["embed"][toks]
+    for l in range(len(cfg["kinds"])):
+        x = b.layer_rows(l, x)
+    assert b.len == 2
+    lb = oracle.gemm(oracle.rmsnorm(x, w["final_norm"], cfg["eps"]), w["lm_head"])
+    assert np.array_equal(la, lb)
+    assert np.array_equal(a.S[0], b.S[0]) and np.array_equal(a.kc[1], b.kc[1]) and np.array_equal(a.vc[1], b.vc[1])
+
+
+@pytest.mark.parametrize("name,L,k", [("TINY_FULL", 128, 4), ("STACK", 64, 2)])
+def test_single_precision_layers_and_the_teacher_forced_bound(name, L, k):
+    """How a second faithful evaluation (the single-precision oracle, fed the same residual input
+    at every layer) sits against the teacher-forced layer bound: its RMS deviation is within
+    2e-2 * RMS(out - x) everywhere; on the tiny complete block every element is within the bound
+    built from the per-output error and the two residual roundings, while on the 5120-wide stack
+    some element exceeds that bound and the bare 2e-2 * RMS(out) alike (the MLP's bf16 SwiGLU
+    values, which is why the GPU comparison also admits 3 * the spread)."""
+    from _block import oracle_stack
+    from _gpu import f64, layer_bound, rms
+    cfg = getattr(synth.workloads, name)
+    w = synth.workloads.weights(cfg, seed=0)
+    toks = synth.workloads.draft_tokens(cfg, 0, 0, 1, k)[0]
+    a = oracle_stack(cfg, w, 0, 1, [L], L + 16)
+    b = oracle_stack(cfg, w, 0, 1, [L], L + 16, f32=True)
+    x = w["embed"][toks]
+    within, bare = [], []
+    for l in range(len(cfg["kinds"])):
+        out, mid = a.layer_rows(l, x, mid=True)
+        e = np.abs(f64(b.layer_rows(l, x)) - f64(out))
+        per, rms_bound = layer_bound(x, mid, out)
+        assert rms(e) <= rms_bound, f"layer {l}"
+        within.append(bool(np.all(e <= per)))
+        bare.append(bool(e.max() > 2e-2 * rms(f64(out))))
+        x = out
+    if name == "STACK":
+        assert not all(within) and any(bare)
+    else:
+        assert all(within)
+
+
 def test_single_precision_evaluation_is_close_but_distinct():
     """The single-precision build (the same source with ORC_F32) that sizes block tolerances:
     on the tiny stack its logits stay within 1% RMS of the double build's yet differ (it is a
