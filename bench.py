@@ -150,14 +150,15 @@ def make_stack(args, device, rank=0, extra_rounds=0, w=None, wd=None, device_kv=
     long-context timing lines."""
     import torch
     from synth import workloads
-    from bit_exact_speculative_gb300.model import HybridStack
+    from bit_exact_speculative_gb300.model import HybridStack, tile_weights
     from bit_exact_speculative_gb300.replicas import rank_seed
 
     cfg = workloads.STACK_FULL if args.full_gdn else workloads.STACK
     if w is None:
         w = workloads.weights(cfg, seed=0)
     if wd is None:
-        wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
+        # the GEMM weights in the tiled layout (the same bits as row-major, faster streaming)
+        wd = tile_weights(cfg, {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()})
     B, k, L = args.batch, args.k, args.context
     seq = rank_seed(0, rank)
     rounds = 3 * (args.steps + args.warmup) + 8 + extra_rounds
@@ -285,7 +286,7 @@ def kernel_rooflines(xv, device, peak):
         if (N, K) not in W_cache:
             W_cache.clear()
             torch.cuda.empty_cache()
-            W_cache[(N, K)] = [rnd((N, K), 0.02) for _ in range(nc)]
+            W_cache[(N, K)] = [xv.tile_weight(rnd((N, K), 0.02)) for _ in range(nc)]
         Ws = W_cache[(N, K)]
         X = rnd((M, K))
         Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
@@ -376,7 +377,7 @@ def gemm_chain_ms(xv, stk, cfg, M, reps, device):
         N = W.shape[0]
         Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
         ws = xv.workspace(max(xv.xv_gemm_workspace_size(M, N, K), 256), device=device)
-        calls.append((Xs[K], W.view(torch.bfloat16), Y, ws, 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)))
+        calls.append((Xs[K], W, Y, ws, 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)))
     launch = lambda i: xv.xv_gemm_small_m(*calls[i % len(calls)][:4])
     for i in range(len(calls)):
         launch(i)
@@ -437,7 +438,7 @@ def run_one_kernel(args):
     if args.kernel == "gemm":
         N, K = GEMM_SHAPES[args.shape]
         M = B * k
-        Ws = [rnd((N, K), 0.02) for _ in range(3)]
+        Ws = [xv.tile_weight(rnd((N, K), 0.02)) for _ in range(3)]
         X = rnd((M, K))
         Y = torch.empty((M, N), dtype=torch.float32 if args.shape == "lm_head" else torch.bfloat16, device=device)
         ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K), device=device)
@@ -489,12 +490,12 @@ def run_prefill(args):
     import torch
     from synth import workloads
     from bit_exact_speculative_gb300 import build
-    from bit_exact_speculative_gb300.model import HybridStack
+    from bit_exact_speculative_gb300.model import HybridStack, tile_weights
     build.build()
     device = torch.device("cuda", 0)
     cfg = workloads.STACK_FULL if args.full_gdn else workloads.STACK
     w = workloads.weights(cfg, seed=0)
-    wd = {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()}
+    wd = tile_weights(cfg, {n: torch.from_numpy(a.view(np.int16)).to(device) for n, a in w.items()})
     B, T = args.batch, args.prefill
     k = args.chunk if args.chunk else max(1, 64 // B)
     stk = HybridStack(cfg, wd, B, k, T + 64, device=device)
@@ -692,6 +693,7 @@ def run_gpu(args):
                        "kv_cache": f"paged, {args.page_size}-position pages" if args.page_size else "contiguous",
                        "gdn_layer": "complete (conv 4, gated norm, 16 q/k heads)" if args.full_gdn else
                                     "recurrence only (32 q/k/v heads)",
+                       "weights": "GEMM weights in the tiled layout (128 x 64 tiles contiguous)",
                        "l2": "inputs larger than L2 (4.4 GB of weights per step)"},
             "gpu_launches": int(launches),
             "roofline": {"bound": "hbm", "kernel": "gemm_small_m", "achieved": round(achieved, 1),

@@ -65,7 +65,7 @@ struct Trace {
 } g_trace;
 const char* const KIND_NAMES[K_COUNT] = {"gemm_small_m", "gdn", "attn_split", "attn_combine", "kv_append", "embed",
                                          "rmsnorm", "swiglu", "gdn_gates", "argmax", "accept", "commit", "zero",
-                                         "conv", "gated_norm", "gemm_combine"};
+                                         "conv", "gated_norm", "gemm_combine", "tile_weights"};
 }  // namespace
 
 void trace_pre(cudaStream_t s) {
@@ -256,13 +256,35 @@ static xv_status gemm_checks(const uint16_t* X, int ldx, const uint16_t* W, cons
 xv_status xv_gemm_small_m(const uint16_t* X, int ldx, const uint16_t* W, uint16_t* Y, int ldy, int M, int N, int K,
                           void* ws, size_t ws_bytes, xv_stream s) {
     if (xv_status st = gemm_checks(X, ldx, W, Y, ldy, M, N, K, ws, ws_bytes)) return st;
-    return gemm_launch(X, ldx, W, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return gemm_launch(X, ldx, W, false, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, float* Y, int ldy, int M, int N, int K,
                                  void* ws, size_t ws_bytes, xv_stream s) {
     if (xv_status st = gemm_checks(X, ldx, W, Y, ldy, M, N, K, ws, ws_bytes)) return st;
-    return gemm_launch(X, ldx, W, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return gemm_launch(X, ldx, W, false, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+size_t xv_gemm_tiled_bytes(int N, int K) { return (N < 1 || K < 1) ? 0 : gemm_tiled_bytes(N, K); }
+
+xv_status xv_gemm_tile_weights(const uint16_t* W, int N, int K, uint16_t* Wt, xv_stream s) {
+    if (!W || !Wt) return fail(XV_ERR_ARG, "tile weights: null W or Wt");
+    if (N < 1 || K < 8) return fail(XV_ERR_ARG, "tile weights: need N >= 1, K >= 8 (got %d, %d)", N, K);
+    if (K % 8) return fail(XV_ERR_UNSUPPORTED, "tile weights: K must be a multiple of 8");
+    if (!aligned16(W) || !aligned16(Wt)) return fail(XV_ERR_UNSUPPORTED, "tile weights: W and Wt must be 16-byte aligned");
+    return gemm_tile_weights_launch(W, N, K, Wt, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gemm_small_m_tiled(const uint16_t* X, int ldx, const uint16_t* Wt, uint16_t* Y, int ldy, int M, int N,
+                                int K, void* ws, size_t ws_bytes, xv_stream s) {
+    if (xv_status st = gemm_checks(X, ldx, Wt, Y, ldy, M, N, K, ws, ws_bytes)) return st;
+    return gemm_launch(X, ldx, Wt, true, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gemm_small_m_tiled_f32out(const uint16_t* X, int ldx, const uint16_t* Wt, float* Y, int ldy, int M,
+                                       int N, int K, void* ws, size_t ws_bytes, xv_stream s) {
+    if (xv_status st = gemm_checks(X, ldx, Wt, Y, ldy, M, N, K, ws, ws_bytes)) return st;
+    return gemm_launch(X, ldx, Wt, true, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 // ------------------------------------------------------------------- GDN

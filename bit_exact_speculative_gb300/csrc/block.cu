@@ -228,6 +228,7 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
     const int par = st->parity & 1;
     const int attn_len = st->max_ctx + k;   // bound on ctx_len + 1 + (k - 1)
     const KvPages kv = state_pages(st);
+    const bool wt = w->tiled != 0;
 
 #define XV_TRY(expr) do { if (xv_status e_ = (expr)) return e_; } while (0)
     XV_TRY(embed_rmsnorm_launch(tokens, M, w->embed, d.V, d.H, w->layers[0].norm1, eps, c.x, c.xn, s));
@@ -237,7 +238,7 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
     auto residual_gemm = [&](const uint16_t* A, int K, const uint16_t* Wt, const uint16_t* gain) -> xv_status {
         float* part = nullptr;
         int S = 0;
-        XV_TRY(gemm_launch(A, K, Wt, c.y, d.H, false, M, d.H, K, c.gemm_ws, c.gemm_ws_bytes, s, &part, &S));
+        XV_TRY(gemm_launch(A, K, Wt, wt, c.y, d.H, false, M, d.H, K, c.gemm_ws, c.gemm_ws_bytes, s, &part, &S));
         if (part) return residual_rmsnorm_part_launch(c.x, part, S, gain, M, d.H, eps, c.xn, s);
         return residual_rmsnorm_launch(c.x, c.y, gain, M, d.H, eps, c.xn, s);
     };
@@ -246,7 +247,7 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
         xv_layer_state& ls = st->layers[l];
         if (cfg->layer_kind[l] == 0) {
             uint16_t* hist = ls.gdn_hist[par];
-            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, hist, d.gstride, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, wt, hist, d.gstride, false, M, d.gin, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
             // the recurrence kernel reads q, k, v (the convolution's outputs, or the history rows
             // themselves) and the raw b, a columns of the history rows
             const uint16_t* ph = ls.gdn_hist[par ^ 1];
@@ -272,7 +273,7 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
                                          c.obuf, d.ginner, s));
             XV_TRY(residual_gemm(c.obuf, d.ginner, lw.w_out, lw.norm2));
         } else {
-            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, c.proj, d.ain, false, M, d.ain, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_in, wt, c.proj, d.ain, false, M, d.ain, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
             XV_TRY(kv_append_launch(c.proj + 2 * d.ainner, d.ain, st->ctx_len, 0, k, B, d.hkv, d.hd, kv, ls.k_cache,
                                     ls.v_cache, s));
             XV_TRY(attn_launch(c.proj, d.ain, ls.k_cache, ls.v_cache, kv, st->ctx_len, 1, k, B, d.hq, d.hkv, d.hd,
@@ -280,13 +281,13 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
                                d.ainner, c.attn_ws, c.attn_ws_bytes, s));
             XV_TRY(residual_gemm(c.obuf, d.ainner, lw.w_out, lw.norm2));
         }
-        XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, c.gu, 2 * d.F, false, M, 2 * d.F, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+        XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, wt, c.gu, 2 * d.F, false, M, 2 * d.F, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
         XV_TRY(swiglu_launch(c.gu, M, d.F, c.act, s));
         const uint16_t* next_norm = (l + 1 < d.L) ? w->layers[l + 1].norm1 : w->final_norm;
         XV_TRY(residual_gemm(c.act, d.F, lw.w_down, next_norm));
     }
     if (head) {
-        XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+        XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, wt, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
         XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
     }
 #undef XV_TRY

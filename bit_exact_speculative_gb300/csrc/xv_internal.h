@@ -15,7 +15,7 @@ xv_status fail(xv_status code, const char* fmt, ...);
 xv_status cuda_check(cudaError_t e, const char* what);
 // Kernel kinds of the launch trace.
 enum Kind : int { K_GEMM = 0, K_GDN, K_ATTN_SPLIT, K_ATTN_COMBINE, K_KV_APPEND, K_EMBED, K_RMSNORM, K_SWIGLU,
-                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_CONV, K_GNORM, K_GEMM_COMBINE, K_COUNT };
+                  K_GATES, K_ARGMAX, K_ACCEPT, K_COMMIT, K_ZERO, K_CONV, K_GNORM, K_GEMM_COMBINE, K_TILE, K_COUNT };
 // Call right before a launch on stream s (records the opening trace event when tracing).
 void trace_pre(cudaStream_t s);
 // Checks the launch just made on the calling thread, counts it and closes its trace record.
@@ -89,8 +89,13 @@ bool gemm_uses_counters(int M, int N, int K);
 // defer_part: when the GEMM would combine its partials in a separate kernel (M > 8, more segments
 // than a cluster), it skips that kernel and returns the partials [S][M][N] and S instead (else
 // *defer_part = nullptr).
-xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, void* Y, int ldy, bool f32out, int M, int N,
-                      int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part = nullptr, int* defer_S = nullptr);
+// wtiled: W in the tiled layout of gemm_tile_weights_launch instead of row-major [N, K].
+xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, bool wtiled, void* Y, int ldy, bool f32out, int M,
+                      int N, int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part = nullptr,
+                      int* defer_S = nullptr);
+// The tiled weight layout: [ceil(N/128)][ceil(K/64)][128][64] bf16, zero past N and K.
+size_t gemm_tiled_bytes(int N, int K);
+xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, uint16_t* Wt, cudaStream_t s);
 
 // ---- GDN (gdn.cu)
 // Steps one GDN call stages: up to XV_KMAX replayed ones and XV_KMAX speculative ones.

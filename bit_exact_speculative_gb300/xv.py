@@ -48,7 +48,7 @@ class LayerWeights(ctypes.Structure):
 
 
 class BlockWeights(ctypes.Structure):
-    _fields_ = [("embed", vp), ("layers", vp), ("final_norm", vp), ("lm_head", vp)]
+    _fields_ = [("embed", vp), ("layers", vp), ("final_norm", vp), ("lm_head", vp), ("tiled", c_int)]
 
 
 class LayerState(ctypes.Structure):
@@ -84,6 +84,10 @@ _SIGS = {
     "xv_gemm_small_m_f32out": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
     "xv_gemm_splits": ([c_int, c_int], c_int),
     "xv_gemm_small_m_noalloc": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp], c_int),
+    "xv_gemm_tiled_bytes": ([c_int, c_int], c_sz),
+    "xv_gemm_tile_weights": ([vp, c_int, c_int, vp, vp], c_int),
+    "xv_gemm_small_m_tiled": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
+    "xv_gemm_small_m_tiled_f32out": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
     "xv_gdn_decode_step": ([vp, ctypes.POINTER(GdnSteps), vp, c_ll, c_int, c_int, c_int, c_int, c_int, vp], c_int),
     "xv_gdn_verify": ([vp, ctypes.POINTER(GdnSteps), vp, c_int, ctypes.POINTER(GdnSteps), c_int, vp, c_ll,
                        c_int, c_int, c_int, c_int, c_int, vp], c_int),
@@ -211,10 +215,42 @@ def xv_gemm_splits(N: int, K: int) -> int:
     return int(lib().xv_gemm_splits(N, K))
 
 
+class TiledWeight:
+    """A weight [N, K] in the GEMM's tiled layout (see :func:`tile_weight`): ``data`` holds the
+    tiled copy, ``shape`` is the logical (N, K)."""
+
+    def __init__(self, data: torch.Tensor, N: int, K: int):
+        self.data, self.shape = data, torch.Size((N, K))
+
+    def data_ptr(self) -> int:
+        return self.data.data_ptr()
+
+    @property
+    def device(self):
+        return self.data.device
+
+
+def xv_gemm_tiled_bytes(N: int, K: int) -> int:
+    return int(lib().xv_gemm_tiled_bytes(N, K))
+
+
+def tile_weight(W: torch.Tensor, stream=None) -> TiledWeight:
+    """The tiled copy of a row-major weight W [N, K] (2-byte dtype), made on the device."""
+    N, K = W.shape
+    data = torch.empty(xv_gemm_tiled_bytes(N, K) // 2, dtype=W.dtype, device=W.device)
+    _check(lib().xv_gemm_tile_weights(_ptr(W), N, K, _ptr(data), _stream(stream)))
+    return TiledWeight(data, N, K)
+
+
 def xv_gemm_small_m(X, W, Y, ws, stream=None):
+    """Y = X W^T; W a row-major tensor [N, K] or a :class:`TiledWeight`."""
     M, K = X.shape[0], X.shape[1]
     N = W.shape[0]
-    fn = lib().xv_gemm_small_m_f32out if Y.dtype == torch.float32 else lib().xv_gemm_small_m
+    f32 = Y.dtype == torch.float32
+    if isinstance(W, TiledWeight):
+        fn = lib().xv_gemm_small_m_tiled_f32out if f32 else lib().xv_gemm_small_m_tiled
+    else:
+        fn = lib().xv_gemm_small_m_f32out if f32 else lib().xv_gemm_small_m
     _check(fn(_ptr(X), _row_stride(X), _ptr(W), _ptr(Y), _row_stride(Y), M, N, K, _ptr(ws),
               0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
     return Y
@@ -320,7 +356,8 @@ class Block:
     ``cfg`` is a dict (hidden, vocab, mlp, kinds, gdn_heads, gdn_dk, gdn_dv, attn_hq, attn_hkv,
     attn_hd, rms_eps); ``weights`` a dict of device tensors (embed, final_norm, lm_head and per
     layer ``f"{l}.norm1"``, ``.w_in``, ``.w_out``, ``.norm2``, ``.w_gu``, ``.w_down`` and, for complete GDN
-    layers, ``.conv_w``, ``.onorm``);
+    layers, ``.conv_w``, ``.onorm``), where lm_head and the four projections are either all
+    row-major tensors or all :class:`TiledWeight`;
     ``state`` a dict (ctx_len, n_commit and per layer ``f"{l}.state"``, ``.hist0``, ``.hist1`` (and
     ``.conv``, ``.cout0``, ``.cout1`` with a convolution) or ``.kc``, ``.vc``).  With ``pages`` (a :class:`KvPages` over ``state["page_table"]``) the
     attention caches are page pools.  Tensors are kept referenced here.
@@ -340,8 +377,13 @@ class Block:
         lw = [LayerWeights(*[weights[f"{l}.{n}"].data_ptr() if f"{l}.{n}" in weights else None for n in names])
               for l in range(len(kinds))]
         self._lw = (LayerWeights * len(kinds))(*lw)
+        gemm = [weights["lm_head"]] + [weights[f"{l}.{n}"] for l in range(len(kinds))
+                                       for n in ("w_in", "w_out", "w_gu", "w_down")]
+        tiled = {isinstance(t, TiledWeight) for t in gemm}
+        if len(tiled) != 1:
+            raise ValueError("the projection weights and the LM head must be all tiled or all row-major")
         self.weights = BlockWeights(weights["embed"].data_ptr(), ctypes.cast(self._lw, vp).value,
-                                    weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr())
+                                    weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr(), int(tiled.pop()))
         ls = []
         for l, kd in enumerate(kinds):
             if kd == 0:

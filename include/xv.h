@@ -55,7 +55,7 @@ typedef int xv_status;
 #define XV_ERR_CUDA        -4   /* a CUDA runtime call or launch failed */
 #define XV_ERR_DEVICE_CHECK -5  /* a kernel recorded a device-side error (see xv_device_check) */
 
-#define XV_ABI_VERSION 3
+#define XV_ABI_VERSION 4
 #define XV_GEMM_M_MAX 64        /* rows per small-M GEMM call */
 #define XV_KMAX 64              /* tokens per sequence per verify (or prefill chunk) call */
 #define XV_CONV_MAX 8           /* widest causal convolution of a complete GDN layer */
@@ -127,6 +127,34 @@ xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, 
                                  int M, int N, int K, void* ws, size_t ws_bytes, xv_stream s);
 /* Number of K-segments the GEMM uses for (N, K) (a pure function of N and K). */
 int xv_gemm_splits(int N, int K);
+
+/* Tiled weight layout (a layout of this library; the pages have none).  The
+ * GEMM streams each 128-row x 64-column weight tile (one ring stage) as one
+ * copy; row-major, such a tile is 128 pieces of 128 bytes, K * 2 bytes apart.
+ * The tiled layout stores it as one contiguous 16 KiB block, and the K-blocks
+ * of a tile row one after another:
+ *     Wt[t][kb][r][c] = W[128 t + r][64 kb + c],
+ * t < ceil(N/128), kb < ceil(K/64), zero past N or K.  The GEMM places the
+ * same values in the same shared-memory slots from either layout, so Y is
+ * bit-identical to the row-major call's.  Measured on GB300 the tiled weights
+ * stream faster (the 151936 x 5120 LM head at M = 8: 254 -> 242 us alone).
+ *
+ * xv_gemm_tiled_bytes: bytes of the tiled copy of an N x K weight (0 for
+ *   N < 1 or K < 1).
+ * xv_gemm_tile_weights: writes Wt (device, xv_gemm_tiled_bytes(N, K) bytes,
+ *   caller-owned) from W [N, K] row-major on stream s (one kernel).  W and
+ *   Wt 16-byte aligned and not overlapping, K % 8 == 0.  Errors: XV_ERR_ARG
+ *   (null pointer, N < 1, K < 8), XV_ERR_UNSUPPORTED (K % 8 != 0,
+ *   alignment), XV_ERR_CUDA.
+ * xv_gemm_small_m_tiled(_f32out): xv_gemm_small_m(_f32out) reading the
+ *   weights from a tiled copy Wt (16-byte aligned); arguments, errors and
+ *   the bits of Y as there. */
+size_t xv_gemm_tiled_bytes(int N, int K);
+xv_status xv_gemm_tile_weights(const uint16_t* W, int N, int K, uint16_t* Wt, xv_stream s);
+xv_status xv_gemm_small_m_tiled(const uint16_t* X, int ldx, const uint16_t* Wt, uint16_t* Y, int ldy,
+                                int M, int N, int K, void* ws, size_t ws_bytes, xv_stream s);
+xv_status xv_gemm_small_m_tiled_f32out(const uint16_t* X, int ldx, const uint16_t* Wt, float* Y, int ldy,
+                                       int M, int N, int K, void* ws, size_t ws_bytes, xv_stream s);
 
 /* The same GEMM (bf16 out) for callers that cannot allocate device memory or
  * pass a workspace: code running under another framework's memory pool,
@@ -372,6 +400,9 @@ typedef struct {
     const xv_layer_weights* layers;   /* HOST array [n_layers] of device pointers */
     const uint16_t* final_norm;       /* [H] */
     const uint16_t* lm_head;          /* [V, H] */
+    int tiled;                        /* 1: w_in, w_out, w_gate_up, w_down and lm_head are tiled
+                                         copies (xv_gemm_tile_weights); embed stays [V, H].
+                                         0: every weight row-major.  The bits do not depend on it. */
 } xv_block_weights;
 
 typedef struct {

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(xv):
 
 
 def test_abi_version(xv):
-    assert xv.xv_abi_version() == 3
+    assert xv.xv_abi_version() == 4
 
 
 def _code(fn, *args):
@@ -62,6 +62,33 @@ def test_gemm_validation_without_gpu(xv):
     # every shape's workspace fits the allocation-free entry point's 10 MiB scratch
     for N in (1024, 4096, 5120, 9728):
         assert xv.xv_gemm_workspace_size(64, N, 17408) <= 10 << 20
+
+
+def test_tiled_weights_size_and_validation_without_gpu(xv):
+    """The tiled copy holds whole 128 x 64 tiles (zero padded past N and K); the tiling call and
+    the tiled GEMM reject bad arguments on the host."""
+    L = xv.lib()
+    assert xv.xv_gemm_tiled_bytes(128, 64) == 128 * 64 * 2
+    assert xv.xv_gemm_tiled_bytes(129, 64) == 2 * 128 * 64 * 2
+    assert xv.xv_gemm_tiled_bytes(300, 1000) == 3 * 16 * 128 * 64 * 2
+    assert xv.xv_gemm_tiled_bytes(151936, 5120) == 151936 * 5120 * 2
+    assert xv.xv_gemm_tiled_bytes(0, 64) == 0
+    p = ctypes.c_void_p(0x10000)
+    assert L.xv_gemm_tile_weights(None, 64, 64, p, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_tile_weights(p, 64, 64, None, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_tile_weights(p, 0, 64, p, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_tile_weights(p, 64, 4, p, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_tile_weights(p, 64, 68, p, None) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_gemm_tile_weights(ctypes.c_void_p(0x10002), 64, 64, p, None) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_gemm_small_m_tiled(None, 64, p, p, 64, 1, 64, 64, None, 0, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_small_m_tiled(p, 64, p, p, 64, 65, 64, 64, None, 0, None) == xv.XV_ERR_UNSUPPORTED
+    assert L.xv_gemm_small_m_tiled_f32out(p, 8192, p, p, 1024, 8, 1024, 8192, None, 0, None) == xv.XV_ERR_WORKSPACE
+
+
+def test_block_weights_layout(xv):
+    """The binding's weights struct ends with the tiled flag (after the four pointers)."""
+    assert [f[0] for f in xv.BlockWeights._fields_] == ["embed", "layers", "final_norm", "lm_head", "tiled"]
+    assert xv.BlockWeights.tiled.offset == 32
 
 
 def test_gemm_noalloc_scratch_holds_every_shape(xv):

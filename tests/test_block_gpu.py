@@ -139,9 +139,12 @@ def test_tiny_speculative_rounds_emit_greedy_decode(tiny):
 
 @pytest.fixture(scope="module")
 def stack(built):
+    """The 5120-wide stack with its GEMM weights in the tiled layout (as the bench runs it); the
+    tiny blocks keep row-major weights."""
+    from bit_exact_speculative_gb300.model import tile_weights
     cfg = workloads.STACK
     w = workloads.weights(cfg, seed=0)
-    wd = {k: dev(v) for k, v in w.items()}
+    wd = tile_weights(cfg, {k: dev(v) for k, v in w.items()})
     return cfg, w, wd
 
 
@@ -471,3 +474,29 @@ def test_layers_teacher_forced_vs_oracle(stack, name, lens, k):
             out, mid = o64.layer_rows(l, xs[l][rows], mid=True)
             out32 = o32.layer_rows(l, xs[l][rows])
             assert_layer_close(xs[l + 1][rows], xs[l][rows], mid, out, out32, what=f"{name} sequence {b} layer {l}")
+
+
+def test_stack_tiled_weights_equal_row_major(stack):
+    """The same stack on row-major weights: 8 sequences of mixed lengths, two verify + commit
+    rounds and a prefill chunk give the same logits, argmax and accept counts bit for bit."""
+    cfg, w, wd = stack
+    rm = {n: dev(v) for n, v in w.items()}
+    B, k = 8, 8
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500]
+    Lmax = max(lens) + 3 * k + 64
+    kv = kv_host(cfg, lens, Lmax)
+    out = []
+    for weights in (wd, rm):
+        A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=weights, kv=kv)
+        got = []
+        for r in range(2):
+            lg, am, na = A.verify(dev(workloads.draft_tokens(cfg, 0, r, B, k)), k)
+            got += [lg.clone(), am.clone(), na.clone()]
+            A.commit()
+        plg, pam = A.prefill(dev(workloads.draft_tokens(cfg, 0, 9, B, 5)))
+        got += [plg.clone(), pam.clone()]
+        out.append(got)
+        del A
+    for a, b in zip(*out):
+        assert same_bits(a, b)
+    del rm

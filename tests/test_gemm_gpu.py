@@ -1,6 +1,7 @@
 """Small-M GEMM: parity with the oracle, row bits independent of M and of row
 position, run-to-run repeatability — at small ragged shapes and at the
-5120 x 17408 gate/up and down projection shapes."""
+5120 x 17408 gate/up and down projection shapes; weights row-major and in the
+tiled layout (the same bits from both)."""
 import numpy as np
 import pytest
 import torch
@@ -52,8 +53,12 @@ def big(xv):
     # a narrow, deep shape whose K split (16 segments) is combined through the workspace
     Wn = synth.normal_bf16(0, synth.tid("sweep.w_narrow"), (1024, 8192), sigma=0.02)
     Xn = synth.normal_bf16(0, synth.tid("sweep.x_narrow"), (64, 8192))
-    return {"gu": (Xgu, Wgu, dev(Xgu), dev(Wgu)), "down": (Xd, Wd, dev(Xd), dev(Wd)),
-            "narrow": (Xn, Wn, dev(Xn), dev(Wn))}
+    out = {"gu": (Xgu, Wgu, dev(Xgu), dev(Wgu)), "down": (Xd, Wd, dev(Xd), dev(Wd)),
+           "narrow": (Xn, Wn, dev(Xn), dev(Wn))}
+    for which in list(out):
+        Xh, Wh, X, W = out[which]
+        out[which + "_tiled"] = (Xh, Wh, X, xv.tile_weight(W))
+    return out
 
 
 def test_split_paths(xv):
@@ -66,7 +71,7 @@ def test_split_paths(xv):
     assert xv.xv_gemm_splits(1024, 8192) > 4 and xv.xv_gemm_workspace_size(8, 1024, 8192) > 0
 
 
-@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
+@pytest.mark.parametrize("which", ["gu", "down", "narrow", "gu_tiled", "down_tiled", "narrow_tiled"])
 def test_row_bits_independent_of_M(xv, big, which):
     _, _, X, W = big[which]
     ref = run(xv, X, W, M=16)
@@ -76,7 +81,7 @@ def test_row_bits_independent_of_M(xv, big, which):
         assert same_bits(Y[:m], ref[:m]), f"M={M}: rows differ from the M=16 call"
 
 
-@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
+@pytest.mark.parametrize("which", ["gu", "down", "narrow", "gu_tiled", "down_tiled", "narrow_tiled"])
 def test_row_bits_independent_of_position(xv, big, which):
     _, _, X, W = big[which]
     perm = torch.tensor([5, 0, 7, 3, 1, 6, 2, 4], device="cuda")
@@ -96,7 +101,7 @@ def test_full_size_parity_sampled(xv, big, which):
     assert_bf16_close(Y[:, cols], ref, what=f"{which} sampled")
 
 
-@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
+@pytest.mark.parametrize("which", ["gu", "down", "narrow", "gu_tiled", "down_tiled", "narrow_tiled"])
 def test_hundred_runs_identical(xv, big, which):
     _, _, X, W = big[which]
     ref = run(xv, X, W, M=16)
@@ -117,3 +122,51 @@ def test_lm_head_shape_f32(xv):
     Y = host(run(xv, dev(Xh), dev(Wh), f32=True))
     cols = np.random.default_rng(1).choice(N, 64, replace=False)
     assert_f32_close(Y[:, cols], oracle.gemm(Xh, Wh[cols]), rel=1e-3, what="lm head")
+
+
+def _tiles_by_definition(W):
+    """The tiled layout written out on the host: Wt[t][kb][r][c] = W[128 t + r][64 kb + c], zero
+    past N and K."""
+    N, K = W.shape
+    Np, Kp = -(-N // 128) * 128, -(-K // 64) * 64
+    P = np.zeros((Np, Kp), dtype=W.dtype)
+    P[:N, :K] = W
+    return P.reshape(Np // 128, 128, Kp // 64, 64).transpose(0, 2, 1, 3).reshape(-1)
+
+
+@pytest.mark.parametrize("N,K", [(300, 1000), (131, 72), (128, 64), (1024, 640)])
+def test_tiled_layout_matches_its_definition(xv, N, K):
+    W = synth.normal_bf16(0, synth.tid(f"tw{N}.{K}"), (N, K), sigma=0.02)
+    Wt = xv.tile_weight(dev(W))
+    assert Wt.shape == (N, K) and Wt.data.numel() * 2 == xv.xv_gemm_tiled_bytes(N, K)
+    assert np.array_equal(host_u16(Wt.data), _tiles_by_definition(W))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1000), (9, 300, 1000), (64, 300, 1000), (17, 131, 72), (8, 1024, 640),
+                                   (3, 256, 4096)])
+def test_tiled_equals_row_major_small(xv, M, N, K):
+    X = dev(synth.normal_bf16(0, synth.tid(f"gx{M}.{N}.{K}"), (M, K)))
+    W = dev(synth.normal_bf16(0, synth.tid(f"gw{M}.{N}.{K}"), (N, K), sigma=0.02))
+    Wt = xv.tile_weight(W)
+    for f32 in (False, True):
+        assert same_bits(run(xv, X, Wt, f32=f32), run(xv, X, W, f32=f32)), f"f32={f32}"
+    assert xv.xv_device_check() == 0
+
+
+@pytest.mark.parametrize("which", ["gu", "down", "narrow"])
+def test_tiled_equals_row_major_full_size(xv, big, which):
+    """Every path the split rule takes (cluster combine, workspace combine with tile counters at
+    M <= 8, the separate combine past 8 rows) gives the same bits from either layout."""
+    _, _, X, W = big[which]
+    Wt = big[which + "_tiled"][3]
+    for M in (1, 8, 9, 64):
+        assert same_bits(run(xv, X, Wt, M=M), run(xv, X, W, M=M)), f"M={M}"
+    assert xv.xv_device_check() == 0
+
+
+def test_tiled_lm_head_equals_row_major(xv):
+    N, K = 151936, 5120
+    W = dev(synth.normal_bf16(0, synth.tid("lm_head_test"), (N, K), sigma=0.02))
+    X = dev(synth.normal_bf16(0, synth.tid("lm_x"), (8, K)))
+    Wt = xv.tile_weight(W)
+    assert same_bits(run(xv, X, Wt, f32=True), run(xv, X, W, f32=True))
