@@ -65,6 +65,7 @@ constexpr int SM_COUNT_TARGET = 152;   // GB300
 // too few tiles to fill the GPU otherwise, go through the workspace.
 constexpr int CLUSTER_MAX = 4;
 constexpr int RESIDENT_PER_SM = 2;
+constexpr int MIN_SEGMENT_KB = 16;   // K-blocks a split-K segment streams at least
 
 template <bool F32OUT>
 __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
@@ -352,27 +353,28 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 }  // namespace
 
-// Narrow shapes (at most half an SM's worth of tiles per SM) split K to fill the GPU; every wider
-// shape splits K in two.  Measured on the 17 GEMMs of a verify step (same GPU, back to back):
-// the two-way split of the gate/up projection (544 CTAs instead of 272, about 1.8 waves of 2 CTAs
-// per SM, so the hardware evens out SMs that stream at different rates) took the step from 895
-// to 862 us; two-way splits of the input projections (instead of 3 and 2) and of the LM head a
-// further 5 us; 3 segments for the GDN input projection were slower.  The narrow shapes take as
-// many segments as fit in one wave of 2 CTAs per SM (the three N = 5120 projections: 7 segments,
-// 280 CTAs, combined through the workspace): 909.5 -> 889.4 us per step against 4 segments in
-// clusters (160 CTAs); 3 segments (120 CTAs) 967 us, 8 (320 CTAs, a second wave) 984 us; the
-// workspace combine instead of clusters for the splits of 2..4 cost 30 us.
+// Shapes with more tiles than SMs stay whole; shapes of one to two SMs' worth split K in two;
+// narrow shapes split K to fill one wave of 2 CTAs per SM, with at least 16 K-blocks per segment.
+// Measured on GB300 with tiled weights, the verify step (B = 1 / B = 8, context 2183): the
+// 34816-wide gate/up and the LM head whole instead of in two halves 865 -> 819 / 1006 -> 918 us
+// (a CTA streams one contiguous run of its whole tile row, and no combine); the GDN output
+// projection (N = 5120, K = 4096) in 4 segments instead of 7: -5 us at B = 1; the input
+// projections (97 and 112 tiles) whole +18 us, in 3 segments +9..+24 us; the down projection in
+// 6 or 7 segments the same, in 8 (a second wave) +67 us.  (With row-major weights the two-way
+// splits of the wide shapes had been the faster choice.)
 int gemm_splits(int N, int K) {
     const int tiles = num_tiles(N);
     const int nkb = ceil_div(K, GEMM_BK);
     int s;
-    if (2 * tiles > SM_COUNT_TARGET) {
+    if (tiles > SM_COUNT_TARGET) {
+        s = 1;
+    } else if (2 * tiles > SM_COUNT_TARGET) {
         s = 2;
     } else {
         s = (SM_COUNT_TARGET * RESIDENT_PER_SM) / tiles;
         if (s > 16) s = 16;
     }
-    while (s > 1 && nkb / s < 4) --s;
+    while (s > 1 && nkb / s < MIN_SEGMENT_KB) --s;
     return s;
 }
 
