@@ -286,16 +286,21 @@ def kernel_rooflines(xv, device, peak):
         if (N, K) not in W_cache:
             W_cache.clear()
             torch.cuda.empty_cache()
-            W_cache[(N, K)] = [xv.tile_weight(rnd((N, K), 0.02)) for _ in range(nc)]
+            tile = xv.tile_gate_up if name == "gate_up" else xv.tile_weight
+            W_cache[(N, K)] = [tile(rnd((N, K), 0.02)) for _ in range(nc)]
         Ws = W_cache[(N, K)]
         X = rnd((M, K))
-        Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
+        gated = name == "gate_up"   # as in the step: the SwiGLU fused, F = N / 2 outputs
+        Y = torch.empty((M, N // 2 if gated else N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
         ws = xv.workspace(max(xv.xv_gemm_workspace_size(M, N, K), 256), device=device)
-        launch = lambda i: xv.xv_gemm_small_m(X, Ws[i % nc], Y, ws)
+        if gated:
+            launch = lambda i: xv.xv_gemm_swiglu(X, Ws[i % nc], Y)
+        else:
+            launch = lambda i: xv.xv_gemm_small_m(X, Ws[i % nc], Y, ws)
         for i in range(nc):
             launch(i)
         ms = _back_to_back_ms(launch, 3 * nc)
-        nbytes = 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)
+        nbytes = 2 * N * K + 2 * M * K + Y.numel() * Y.element_size()
         dst[f"{name}_M{M}"] = dict(N=N, K=K, splits=xv.xv_gemm_splits(N, K), **line(ms, nbytes))
     W_cache.clear()
     torch.cuda.empty_cache()
@@ -375,10 +380,17 @@ def gemm_chain_ms(xv, stk, cfg, M, reps, device):
     calls = []
     for W, K, f32 in plan:
         N = W.shape[0]
-        Y = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
+        gated = getattr(W, "gated", False)   # gate/up with the SwiGLU fused: F = N / 2 outputs
+        Y = torch.empty((M, N // 2 if gated else N), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
         ws = xv.workspace(max(xv.xv_gemm_workspace_size(M, N, K), 256), device=device)
-        calls.append((Xs[K], W, Y, ws, 2 * N * K + 2 * M * K + M * N * (4 if f32 else 2)))
-    launch = lambda i: xv.xv_gemm_small_m(*calls[i % len(calls)][:4])
+        calls.append((Xs[K], W, Y, ws, 2 * N * K + 2 * M * K + Y.numel() * Y.element_size()))
+
+    def launch(i):
+        X, W, Y, ws, _ = calls[i % len(calls)]
+        if getattr(W, "gated", False):
+            xv.xv_gemm_swiglu(X, W, Y)
+        else:
+            xv.xv_gemm_small_m(X, W, Y, ws)
     for i in range(len(calls)):
         launch(i)
     ms = _back_to_back_ms(launch, reps * len(calls))

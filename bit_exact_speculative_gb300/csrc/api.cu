@@ -240,14 +240,14 @@ size_t xv_gemm_workspace_size(int M, int N, int K) {
 }
 
 static xv_status gemm_checks(const uint16_t* X, int ldx, const uint16_t* W, const void* Y, int ldy, int M, int N, int K,
-                             const void* ws, size_t ws_bytes) {
+                             const void* ws, size_t ws_bytes, bool split = true) {
     if (!X || !W || !Y) return fail(XV_ERR_ARG, "gemm: null X, W or Y");
     if (M < 1 || N < 1 || K < 8) return fail(XV_ERR_ARG, "gemm: need M >= 1, N >= 1, K >= 8 (got %d, %d, %d)", M, N, K);
     if (M > XV_GEMM_M_MAX) return fail(XV_ERR_UNSUPPORTED, "gemm: M = %d exceeds %d", M, XV_GEMM_M_MAX);
     if (ldx < K || ldy < N) return fail(XV_ERR_ARG, "gemm: ldx < K or ldy < N");
     if (K % 8 || ldx % 8) return fail(XV_ERR_UNSUPPORTED, "gemm: K and ldx must be multiples of 8");
     if (!aligned16(X) || !aligned16(W)) return fail(XV_ERR_UNSUPPORTED, "gemm: X and W must be 16-byte aligned");
-    size_t need = gemm_workspace_size(M, N, K);
+    size_t need = split ? gemm_workspace_size(M, N, K) : 0;
     if (need && (!ws || ws_bytes < need))
         return fail(XV_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed, %zu given", need, ws ? ws_bytes : 0);
     return XV_OK;
@@ -256,13 +256,13 @@ static xv_status gemm_checks(const uint16_t* X, int ldx, const uint16_t* W, cons
 xv_status xv_gemm_small_m(const uint16_t* X, int ldx, const uint16_t* W, uint16_t* Y, int ldy, int M, int N, int K,
                           void* ws, size_t ws_bytes, xv_stream s) {
     if (xv_status st = gemm_checks(X, ldx, W, Y, ldy, M, N, K, ws, ws_bytes)) return st;
-    return gemm_launch(X, ldx, W, false, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return gemm_launch(X, ldx, W, W_ROWS, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 xv_status xv_gemm_small_m_f32out(const uint16_t* X, int ldx, const uint16_t* W, float* Y, int ldy, int M, int N, int K,
                                  void* ws, size_t ws_bytes, xv_stream s) {
     if (xv_status st = gemm_checks(X, ldx, W, Y, ldy, M, N, K, ws, ws_bytes)) return st;
-    return gemm_launch(X, ldx, W, false, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return gemm_launch(X, ldx, W, W_ROWS, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 size_t xv_gemm_tiled_bytes(int N, int K) { return (N < 1 || K < 1) ? 0 : gemm_tiled_bytes(N, K); }
@@ -272,19 +272,36 @@ xv_status xv_gemm_tile_weights(const uint16_t* W, int N, int K, uint16_t* Wt, xv
     if (N < 1 || K < 8) return fail(XV_ERR_ARG, "tile weights: need N >= 1, K >= 8 (got %d, %d)", N, K);
     if (K % 8) return fail(XV_ERR_UNSUPPORTED, "tile weights: K must be a multiple of 8");
     if (!aligned16(W) || !aligned16(Wt)) return fail(XV_ERR_UNSUPPORTED, "tile weights: W and Wt must be 16-byte aligned");
-    return gemm_tile_weights_launch(W, N, K, Wt, reinterpret_cast<cudaStream_t>(s));
+    return gemm_tile_weights_launch(W, N, K, false, Wt, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gemm_tile_gate_up(const uint16_t* W, int F, int K, uint16_t* Wt, xv_stream s) {
+    if (!W || !Wt) return fail(XV_ERR_ARG, "tile gate/up: null W or Wt");
+    if (F < 1 || K < 8) return fail(XV_ERR_ARG, "tile gate/up: need F >= 1, K >= 8 (got %d, %d)", F, K);
+    if (F % 64 || K % 8) return fail(XV_ERR_UNSUPPORTED, "tile gate/up: F must be a multiple of 64 and K of 8");
+    if (!aligned16(W) || !aligned16(Wt)) return fail(XV_ERR_UNSUPPORTED, "tile gate/up: W and Wt must be 16-byte aligned");
+    return gemm_tile_weights_launch(W, 2 * F, K, true, Wt, reinterpret_cast<cudaStream_t>(s));
+}
+
+xv_status xv_gemm_swiglu_tiled(const uint16_t* X, int ldx, const uint16_t* Wt, uint16_t* act, int ldact, int M, int F,
+                               int K, xv_stream s) {
+    if (!act) return fail(XV_ERR_ARG, "gemm swiglu: null act");
+    if (F < 1 || F % 64) return fail(XV_ERR_UNSUPPORTED, "gemm swiglu: F must be a positive multiple of 64");
+    if (ldact < F) return fail(XV_ERR_ARG, "gemm swiglu: ldact < F");
+    if (xv_status st = gemm_checks(X, ldx, Wt, act, 2 * F, M, 2 * F, K, nullptr, 0, false)) return st;
+    return gemm_launch(X, ldx, Wt, W_GATED, act, ldact, false, M, 2 * F, K, nullptr, 0, reinterpret_cast<cudaStream_t>(s));
 }
 
 xv_status xv_gemm_small_m_tiled(const uint16_t* X, int ldx, const uint16_t* Wt, uint16_t* Y, int ldy, int M, int N,
                                 int K, void* ws, size_t ws_bytes, xv_stream s) {
     if (xv_status st = gemm_checks(X, ldx, Wt, Y, ldy, M, N, K, ws, ws_bytes)) return st;
-    return gemm_launch(X, ldx, Wt, true, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return gemm_launch(X, ldx, Wt, W_TILED, Y, ldy, false, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 xv_status xv_gemm_small_m_tiled_f32out(const uint16_t* X, int ldx, const uint16_t* Wt, float* Y, int ldy, int M,
                                        int N, int K, void* ws, size_t ws_bytes, xv_stream s) {
     if (xv_status st = gemm_checks(X, ldx, Wt, Y, ldy, M, N, K, ws, ws_bytes)) return st;
-    return gemm_launch(X, ldx, Wt, true, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+    return gemm_launch(X, ldx, Wt, W_TILED, Y, ldy, true, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s));
 }
 
 // ------------------------------------------------------------------- GDN

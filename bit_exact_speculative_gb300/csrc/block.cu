@@ -211,6 +211,7 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
             return fail(XV_ERR_ARG, "block: GDN layer %d convolution taps or output norm weights missing", l);
     }
     if (!tokens || (head && (!argmax || !n_accept))) return fail(XV_ERR_ARG, "block: null tokens, argmax or n_accept");
+    if (w->tiled && d.F % 64) return fail(XV_ERR_UNSUPPORTED, "block: tiled weights need mlp a multiple of 64");
     if (st->last_k != 0) return fail(XV_ERR_ARG, "block: the previous verify has not been committed");
     const int B = st->B;
     if (k < 1 || k > st->kmax) return fail(XV_ERR_ARG, "block: k = %d outside [1, kmax = %d]", k, st->kmax);
@@ -228,7 +229,7 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
     const int par = st->parity & 1;
     const int attn_len = st->max_ctx + k;   // bound on ctx_len + 1 + (k - 1)
     const KvPages kv = state_pages(st);
-    const bool wt = w->tiled != 0;
+    const WLayout wt = w->tiled ? W_TILED : W_ROWS;
 
 #define XV_TRY(expr) do { if (xv_status e_ = (expr)) return e_; } while (0)
     XV_TRY(embed_rmsnorm_launch(tokens, M, w->embed, d.V, d.H, w->layers[0].norm1, eps, c.x, c.xn, s));
@@ -281,8 +282,14 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
                                d.ainner, c.attn_ws, c.attn_ws_bytes, s));
             XV_TRY(residual_gemm(c.obuf, d.ainner, lw.w_out, lw.norm2));
         }
-        XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, wt, c.gu, 2 * d.F, false, M, 2 * d.F, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-        XV_TRY(swiglu_launch(c.gu, M, d.F, c.act, s));
+        if (wt == W_TILED) {
+            // gate/up in the gated tiled layout: the GEMM writes the SwiGLU activations itself
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, W_GATED, c.act, d.F, false, M, 2 * d.F, d.H, nullptr, 0, s));
+        } else {
+            XV_TRY(gemm_launch(c.xn, d.H, lw.w_gate_up, wt, c.gu, 2 * d.F, false, M, 2 * d.F, d.H, c.gemm_ws,
+                               c.gemm_ws_bytes, s));
+            XV_TRY(swiglu_launch(c.gu, M, d.F, c.act, s));
+        }
         const uint16_t* next_norm = (l + 1 < d.L) ? w->layers[l + 1].norm1 : w->final_norm;
         XV_TRY(residual_gemm(c.act, d.F, lw.w_down, next_norm));
     }

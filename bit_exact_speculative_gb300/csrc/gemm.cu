@@ -27,6 +27,13 @@
 //     whichever CTA is last — rounds once and resets the counter.
 //   - Every mbarrier wait is bounded; a timeout records an error bit and
 //     the CTA drains its copies in flight, frees TMEM and returns.
+//   - Gate/up with the SwiGLU fused: in the gated tiled layout a tile holds
+//     64 gate rows and the 64 up rows of the same features, so one CTA has
+//     both halves of each of its 64 features; the epilogue rounds g and u to
+//     bf16 as a stored gate/up row would be, forms bf16(silu(g) u) with the
+//     SwiGLU kernel's own arithmetic and writes only the activations.  Such a
+//     GEMM is never split (each output is one whole-K sum, as for the
+//     34816-wide gate/up anyway), so its bits are those of GEMM + SwiGLU.
 //   - Weights come in one of two layouts: row-major [N, K], or tiled, each
 //     128 x 64 tile (one ring stage) a contiguous 16 KiB and a tile row's
 //     K-blocks one after another.  A row-major stage is 128 pieces of 128
@@ -67,7 +74,7 @@ constexpr int CLUSTER_MAX = 4;
 constexpr int RESIDENT_PER_SM = 2;
 constexpr int MIN_SEGMENT_KB = 16;   // K-blocks a split-K segment streams at least
 
-template <bool F32OUT>
+template <bool F32OUT, bool GATED>
 __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         void* __restrict__ Y, int ldy, int M, int N, int nkb, int S, float* __restrict__ part,
@@ -252,6 +259,29 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
         }
         __syncwarp();
         cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+    } else if (GATED) {
+        // rows 0..63 of the tile are the gate rows of features 64 tile + 0..63, rows 64..127 the
+        // up rows of the same features: every warp parks its rows rounded to bf16 (as a stored
+        // gate/up row would be) in shared memory (the drained stage ring), then the CTA forms the
+        // M x 64 activations, consecutive threads on consecutive features.  The loop is kept
+        // short (unrolled by 4): fully unrolled over the 64 token rows, each with an exp, it was
+        // measured 3-6 us slower per launch, its code streaming through the instruction cache.
+        uint16_t* gbuf = reinterpret_cast<uint16_t*>(smem);   // [m][128]: gate rows, then up rows
+        const int r_local = warp * 32 + lane;
+#pragma unroll
+        for (int m = 0; m < GEMM_TOK; ++m)
+            if (m < M) gbuf[m * GEMM_BN + r_local] = f32_to_bf16(acc[m]);
+        __syncthreads();
+        const int F = N >> 1;
+#pragma unroll 4
+        for (int e = threadIdx.x; e < M * 64; e += blockDim.x) {
+            const int m = e >> 6, fl = e & 63, f = tile * 64 + fl;
+            if (f < F) {
+                const float g = bf16_to_f32(gbuf[m * GEMM_BN + fl]);
+                const float u = bf16_to_f32(gbuf[m * GEMM_BN + 64 + fl]);
+                static_cast<uint16_t*>(Y)[static_cast<size_t>(m) * ldy + f] = f32_to_bf16(swiglu_f(g, u));
+            }
+        }
     } else if (S == 1) {
         if (live) {
 #pragma unroll
@@ -400,9 +430,12 @@ size_t gemm_workspace_size(int M, int N, int K) {
     return COUNTER_BYTES + round256(static_cast<size_t>(S) * M * N * sizeof(float));
 }
 
-xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, bool wtiled, void* Y, int ldy, bool f32out, int M,
+xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, WLayout wl, void* Y, int ldy, bool f32out, int M,
                       int N, int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part, int* defer_S) {
     (void)ws_bytes;
+    const bool wtiled = wl != W_ROWS, gated = wl == W_GATED;
+    if (gated && (f32out || N % 128))
+        return fail(XV_ERR_UNSUPPORTED, "gemm: the fused SwiGLU needs bf16 out and a multiple of 64 features");
     if (defer_part) *defer_part = nullptr;
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "gemm: device error word unavailable");
@@ -426,7 +459,7 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, bool wtiled
                                         CU_TENSOR_MAP_SWIZZLE_128B))
             return st;
     }
-    const int tiles = num_tiles(N), S = gemm_splits(N, K), nkb = ceil_div(K, GEMM_BK);
+    const int tiles = num_tiles(N), S = gated ? 1 : gemm_splits(N, K), nkb = ceil_div(K, GEMM_BK);
     float* part = nullptr;
     unsigned* cnt = nullptr;
     // Past 8 token rows the last-arriving CTA's combine is a long serial tail (one round trip per
@@ -436,7 +469,8 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, bool wtiled
         cnt = sep_combine ? nullptr : static_cast<unsigned*>(ws);
         part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + COUNTER_BYTES);
     }
-    auto kern = f32out ? gemm_small_m_kernel<true> : gemm_small_m_kernel<false>;
+    auto kern = gated ? gemm_small_m_kernel<false, true>
+                      : (f32out ? gemm_small_m_kernel<true, false> : gemm_small_m_kernel<false, false>);
     if (xv_status st = kernel_smem_once(reinterpret_cast<const void*>(kern), SMEM_MAX, false, "gemm: set shared memory size"))
         return st;
     const int xb = M <= X_SMALL_M ? 1024 : B_BYTES, xr = M <= X_SMALL_M ? X_RING : STAGES;
@@ -450,7 +484,7 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, bool wtiled
     else
         launch_k(kern, grid, dim3(128), smem, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster, xb, xr,
                  wtiled ? 1 : 0);
-    const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * N * (f32out ? 4 : 2);
+    const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * (gated ? N / 2 : N) * (f32out ? 4 : 2);
     if (xv_status st = launched("gemm_small_m_kernel", s, K_GEMM, bytes)) return st;
     if (sep_combine && defer_part) {
         *defer_part = part;
@@ -472,7 +506,7 @@ namespace {
 // tile (t, kb) is W[128 t + r][64 kb + c], zero past N or K (K % 8 == 0, so a 16-byte piece lies
 // wholly inside or wholly outside W).  Consecutive threads write consecutive pieces; 8 of them
 // read one 128-byte piece of a weight row.
-__global__ void tile_weights_kernel(const uint4* __restrict__ W, int N, int K, int nkb, long long pieces,
+__global__ void tile_weights_kernel(const uint4* __restrict__ W, int N, int K, int nkb, long long pieces, int gate_f,
                                     uint4* __restrict__ Wt) {
     griddep_launch();
     griddep_wait();
@@ -483,7 +517,9 @@ __global__ void tile_weights_kernel(const uint4* __restrict__ W, int N, int K, i
     const long long blk = i >> 10;   // (t, kb) block: 128 rows x 8 pieces
     const int kb = static_cast<int>(blk % nkb);
     const long long t = blk / nkb;
-    const long long row = t * GEMM_BN + r;
+    // gated (gate_f = F features): rows 0..63 of tile t are gate rows 64 t + r, rows 64..127 the
+    // up rows F + 64 t + r - 64
+    const long long row = gate_f ? (r < 64 ? t * 64 + r : gate_f + t * 64 + r - 64) : t * GEMM_BN + r;
     const int col = kb * GEMM_BK + c8 * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (row < N && col < K) v = W[(row * K + col) / 8];
@@ -495,11 +531,12 @@ size_t gemm_tiled_bytes(int N, int K) {
     return static_cast<size_t>(num_tiles(N)) * ceil_div(K, GEMM_BK) * GEMM_BN * GEMM_BK * 2;
 }
 
-xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, uint16_t* Wt, cudaStream_t s) {
+xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, bool gated, uint16_t* Wt, cudaStream_t s) {
     const long long pieces = static_cast<long long>(gemm_tiled_bytes(N, K) / 16);
     constexpr int T = 256;
     launch_k(tile_weights_kernel, dim3(static_cast<unsigned>((pieces + T - 1) / T)), dim3(T), 0, s,
-             reinterpret_cast<const uint4*>(W), N, K, ceil_div(K, GEMM_BK), pieces, reinterpret_cast<uint4*>(Wt));
+             reinterpret_cast<const uint4*>(W), N, K, ceil_div(K, GEMM_BK), pieces, gated ? N / 2 : 0,
+             reinterpret_cast<uint4*>(Wt));
     return launched("tile_weights_kernel", s, K_TILE, 2 * static_cast<long long>(gemm_tiled_bytes(N, K)));
 }
 

@@ -75,5 +75,5 @@ extern "C" xv_status xv_gemm_small_m_noalloc(const uint16_t* X, int ldx, const u
     if (gemm_uses_counters(M, N, K))
         if (xv_status st = cuda_check(cudaMemsetAsync(scratch, 0, GEMM_COUNTER_BYTES, s), "gemm_noalloc: clear counters"))
             return st;
-    return gemm_launch(X, ldx, W, false, Y, ldy, false, M, N, K, scratch, XV_GEMM_NOALLOC_SCRATCH_BYTES, s);
+    return gemm_launch(X, ldx, W, W_ROWS, Y, ldy, false, M, N, K, scratch, XV_GEMM_NOALLOC_SCRATCH_BYTES, s);
 }

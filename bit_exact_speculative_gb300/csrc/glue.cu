@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x,
     }
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return __frcp_rn(__fadd_rn(1.f, expf(-x))); }
 
 // act = bf16(silu(g) * u), 8 elements per thread
 __global__ void swiglu_kernel(const uint16_t* __restrict__ gu, int F, uint16_t* __restrict__ act) {
@@ -171,7 +170,7 @@ __global__ void swiglu_kernel(const uint16_t* __restrict__ gu, int F, uint16_t* 
     unpack8(reinterpret_cast<const uint4*>(gu + row * 2 * F)[c], g);
     unpack8(reinterpret_cast<const uint4*>(gu + row * 2 * F + F)[c], u);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(g[e], sigmoid_f(g[e])), u[e]);
+    for (int e = 0; e < 8; ++e) o[e] = swiglu_f(g[e], u[e]);
     reinterpret_cast<uint4*>(act + row * F)[c] = pack8(o);
 }
 

@@ -89,13 +89,17 @@ bool gemm_uses_counters(int M, int N, int K);
 // defer_part: when the GEMM would combine its partials in a separate kernel (M > 8, more segments
 // than a cluster), it skips that kernel and returns the partials [S][M][N] and S instead (else
 // *defer_part = nullptr).
-// wtiled: W in the tiled layout of gemm_tile_weights_launch instead of row-major [N, K].
-xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, bool wtiled, void* Y, int ldy, bool f32out, int M,
+// Weight layouts: row-major [N, K]; tiled (gemm_tile_weights_launch); gated tiled, a gate/up
+// weight [2F, K] whose tiles pair 64 gate rows with the 64 up rows of the same features, read by
+// the GEMM with the SwiGLU fused (N = 2F weight rows in, F bf16 activations per row out, never
+// split).
+enum WLayout : int { W_ROWS = 0, W_TILED = 1, W_GATED = 2 };
+xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, WLayout wl, void* Y, int ldy, bool f32out, int M,
                       int N, int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part = nullptr,
                       int* defer_S = nullptr);
 // The tiled weight layout: [ceil(N/128)][ceil(K/64)][128][64] bf16, zero past N and K.
 size_t gemm_tiled_bytes(int N, int K);
-xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, uint16_t* Wt, cudaStream_t s);
+xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, bool gated, uint16_t* Wt, cudaStream_t s);
 
 // ---- GDN (gdn.cu)
 // Steps one GDN call stages: up to XV_KMAX replayed ones and XV_KMAX speculative ones.

@@ -289,6 +289,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+// The MLP's SwiGLU of one element, silu(g) u = (g sigmoid(g)) u with sigmoid(g) = 1 / (1 + exp(-g)),
+// each operation rounded once; shared by the SwiGLU kernel and the gate/up GEMM's fused epilogue,
+// so both give the same bits.
+__device__ __forceinline__ float swiglu_f(float g, float u) {
+    return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.f, expf(-g)))), u);
+}
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);

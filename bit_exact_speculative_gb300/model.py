@@ -69,13 +69,15 @@ GEMM_WEIGHTS = ("w_in", "w_out", "w_gu", "w_down")
 
 def tile_weights(cfg: dict, weights: dict, stream=None) -> dict:
     """A copy of ``weights`` with the LM head and every layer's projections in the GEMM's tiled
-    layout (:func:`xv.tile_weight`; the other tensors are shared): the same bits, faster
-    streaming.  The row-major projection tensors may be dropped afterwards."""
+    layout (:func:`xv.tile_weight`; gate/up by :func:`xv.tile_gate_up`, which lets the GEMM form
+    the SwiGLU itself; the other tensors are shared): the same bits, faster streaming, one launch
+    fewer per layer.  The row-major projection tensors may be dropped afterwards."""
     out = dict(weights)
     names = ["lm_head"] + [f"{l}.{n}" for l in range(len(cfg["kinds"])) for n in GEMM_WEIGHTS]
     for n in names:
         if not isinstance(out[n], xv.TiledWeight):
-            out[n] = xv.tile_weight(out[n], stream=stream)
+            gated = n.endswith(".w_gu")
+            out[n] = (xv.tile_gate_up if gated else xv.tile_weight)(out[n], stream=stream)
     return out
 
 

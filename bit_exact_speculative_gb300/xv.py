@@ -88,6 +88,8 @@ _SIGS = {
     "xv_gemm_tile_weights": ([vp, c_int, c_int, vp, vp], c_int),
     "xv_gemm_small_m_tiled": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
     "xv_gemm_small_m_tiled_f32out": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp, c_sz, vp], c_int),
+    "xv_gemm_tile_gate_up": ([vp, c_int, c_int, vp, vp], c_int),
+    "xv_gemm_swiglu_tiled": ([vp, c_int, vp, vp, c_int, c_int, c_int, c_int, vp], c_int),
     "xv_gdn_decode_step": ([vp, ctypes.POINTER(GdnSteps), vp, c_ll, c_int, c_int, c_int, c_int, c_int, vp], c_int),
     "xv_gdn_verify": ([vp, ctypes.POINTER(GdnSteps), vp, c_int, ctypes.POINTER(GdnSteps), c_int, vp, c_ll,
                        c_int, c_int, c_int, c_int, c_int, vp], c_int),
@@ -217,10 +219,11 @@ def xv_gemm_splits(N: int, K: int) -> int:
 
 class TiledWeight:
     """A weight [N, K] in the GEMM's tiled layout (see :func:`tile_weight`): ``data`` holds the
-    tiled copy, ``shape`` is the logical (N, K)."""
+    tiled copy, ``shape`` is the logical (N, K); ``gated`` marks a gate/up weight tiled by
+    :func:`tile_gate_up`."""
 
-    def __init__(self, data: torch.Tensor, N: int, K: int):
-        self.data, self.shape = data, torch.Size((N, K))
+    def __init__(self, data: torch.Tensor, N: int, K: int, gated: bool = False):
+        self.data, self.shape, self.gated = data, torch.Size((N, K)), gated
 
     def data_ptr(self) -> int:
         return self.data.data_ptr()
@@ -242,11 +245,31 @@ def tile_weight(W: torch.Tensor, stream=None) -> TiledWeight:
     return TiledWeight(data, N, K)
 
 
+def tile_gate_up(W: torch.Tensor, stream=None) -> TiledWeight:
+    """The gated tiled copy of a gate/up weight W [2F, K] (F gate rows, then F up rows)."""
+    N, K = W.shape
+    data = torch.empty(xv_gemm_tiled_bytes(N, K) // 2, dtype=W.dtype, device=W.device)
+    _check(lib().xv_gemm_tile_gate_up(_ptr(W), N // 2, K, _ptr(data), _stream(stream)))
+    return TiledWeight(data, N, K, gated=True)
+
+
+def xv_gemm_swiglu(X, Wgu: TiledWeight, act, stream=None):
+    """act [M, F] = bf16(silu(g) u) of the gate/up projection X Wgu^T, in one kernel."""
+    assert Wgu.gated, "the weight must come from tile_gate_up"
+    M, K = X.shape[0], X.shape[1]
+    F = Wgu.shape[0] // 2
+    _check(lib().xv_gemm_swiglu_tiled(_ptr(X), _row_stride(X), _ptr(Wgu), _ptr(act), _row_stride(act), M, F, K,
+                                      _stream(stream)))
+    return act
+
+
 def xv_gemm_small_m(X, W, Y, ws, stream=None):
     """Y = X W^T; W a row-major tensor [N, K] or a :class:`TiledWeight`."""
     M, K = X.shape[0], X.shape[1]
     N = W.shape[0]
     f32 = Y.dtype == torch.float32
+    if isinstance(W, TiledWeight) and W.gated:
+        raise ValueError("a gated gate/up weight goes through xv_gemm_swiglu")
     if isinstance(W, TiledWeight):
         fn = lib().xv_gemm_small_m_tiled_f32out if f32 else lib().xv_gemm_small_m_tiled
     else:
@@ -382,6 +405,8 @@ class Block:
         tiled = {isinstance(t, TiledWeight) for t in gemm}
         if len(tiled) != 1:
             raise ValueError("the projection weights and the LM head must be all tiled or all row-major")
+        if True in tiled and not all(weights[f"{l}.w_gu"].gated for l in range(len(kinds))):
+            raise ValueError("with tiled weights every w_gu must come from tile_gate_up")
         self.weights = BlockWeights(weights["embed"].data_ptr(), ctypes.cast(self._lw, vp).value,
                                     weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr(), int(tiled.pop()))
         ls = []

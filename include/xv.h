@@ -151,6 +151,24 @@ int xv_gemm_splits(int N, int K);
  *   the bits of Y as there. */
 size_t xv_gemm_tiled_bytes(int N, int K);
 xv_status xv_gemm_tile_weights(const uint16_t* W, int N, int K, uint16_t* Wt, xv_stream s);
+
+/* Gate/up projection with the SwiGLU fused.  xv_gemm_tile_gate_up tiles a
+ * gate/up weight W [2F, K] (F gate rows, then F up rows) so that tile t holds
+ * gate rows 64t..64t+63 followed by up rows F+64t..F+64t+63 (Wt of
+ * xv_gemm_tiled_bytes(2F, K) bytes; F % 64 == 0, K % 8 == 0, 16-byte
+ * aligned).  xv_gemm_swiglu_tiled then computes, for each row m of X and
+ * feature f < F,
+ *     act[m, f] = bf16(silu(g) u),  g = bf16((X W^T)[m, f]),
+ *                                   u = bf16((X W^T)[m, F + f]),
+ * silu(g) u = (g / (1 + exp(-g))) u in fp32: the bits of xv_gemm_small_m into
+ * a [M, 2F] buffer followed by the SwiGLU of the verify block, in one kernel
+ * and without the [M, 2F] buffer.  The GEMM is never split over K (no
+ * workspace).  act [M, ldact] bf16, ldact >= F.  Errors: XV_ERR_ARG (null
+ * pointer, sizes out of range, ldact < F), XV_ERR_UNSUPPORTED (F % 64,
+ * K % 8, alignment, M > XV_GEMM_M_MAX), XV_ERR_CUDA. */
+xv_status xv_gemm_tile_gate_up(const uint16_t* W, int F, int K, uint16_t* Wt, xv_stream s);
+xv_status xv_gemm_swiglu_tiled(const uint16_t* X, int ldx, const uint16_t* Wt, uint16_t* act, int ldact,
+                               int M, int F, int K, xv_stream s);
 xv_status xv_gemm_small_m_tiled(const uint16_t* X, int ldx, const uint16_t* Wt, uint16_t* Y, int ldy,
                                 int M, int N, int K, void* ws, size_t ws_bytes, xv_stream s);
 xv_status xv_gemm_small_m_tiled_f32out(const uint16_t* X, int ldx, const uint16_t* Wt, float* Y, int ldy,
@@ -400,9 +418,11 @@ typedef struct {
     const xv_layer_weights* layers;   /* HOST array [n_layers] of device pointers */
     const uint16_t* final_norm;       /* [H] */
     const uint16_t* lm_head;          /* [V, H] */
-    int tiled;                        /* 1: w_in, w_out, w_gate_up, w_down and lm_head are tiled
-                                         copies (xv_gemm_tile_weights); embed stays [V, H].
-                                         0: every weight row-major.  The bits do not depend on it. */
+    int tiled;                        /* 1: w_in, w_out, w_down and lm_head are tiled copies
+                                         (xv_gemm_tile_weights), w_gate_up a gated tiled copy
+                                         (xv_gemm_tile_gate_up; the SwiGLU is then fused into its
+                                         GEMM; mlp % 64 == 0); embed stays [V, H].  0: every weight
+                                         row-major.  The bits do not depend on it. */
 } xv_block_weights;
 
 typedef struct {

@@ -89,6 +89,19 @@ def test_tiled_weights_size_and_validation_without_gpu(xv):
     assert L.xv_gemm_small_m_tiled_f32out(p, 8192, p, p, 1024, 8, 1024, 8192, None, 0, None) == xv.XV_ERR_WORKSPACE
 
 
+def test_gate_up_tiling_and_fused_swiglu_validation_without_gpu(xv):
+    L = xv.lib()
+    p = ctypes.c_void_p(0x10000)
+    assert L.xv_gemm_tile_gate_up(None, 64, 64, p, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_tile_gate_up(p, 0, 64, p, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_tile_gate_up(p, 100, 64, p, None) == xv.XV_ERR_UNSUPPORTED      # F % 64
+    assert L.xv_gemm_swiglu_tiled(p, 64, p, None, 64, 1, 64, 64, None) == xv.XV_ERR_ARG
+    assert L.xv_gemm_swiglu_tiled(p, 64, p, p, 64, 1, 96, 64, None) == xv.XV_ERR_UNSUPPORTED   # F % 64
+    assert L.xv_gemm_swiglu_tiled(p, 64, p, p, 32, 1, 64, 64, None) == xv.XV_ERR_ARG           # ldact < F
+    assert L.xv_gemm_swiglu_tiled(p, 64, p, p, 64, 65, 64, 64, None) == xv.XV_ERR_UNSUPPORTED  # M > 64
+    assert L.xv_gemm_swiglu_tiled(p, 72, p, p, 64, 1, 64, 68, None) == xv.XV_ERR_UNSUPPORTED   # K % 8
+
+
 def test_block_weights_layout(xv):
     """The binding's weights struct ends with the tiled flag (after the four pointers)."""
     assert [f[0] for f in xv.BlockWeights._fields_] == ["embed", "layers", "final_norm", "lm_head", "tiled"]

@@ -171,3 +171,33 @@ def test_tiled_lm_head_equals_row_major(xv):
     X = dev(synth.normal_bf16(0, synth.tid("lm_x"), (8, K)))
     Wt = xv.tile_weight(W)
     assert same_bits(run(xv, X, Wt, f32=True), run(xv, X, W, f32=True))
+
+
+@pytest.mark.parametrize("F,K", [(64, 64), (128, 1000), (512, 256)])
+def test_gate_up_tiling_matches_its_definition(xv, F, K):
+    """Tile t of the gated layout holds gate rows 64t..64t+63, then up rows F+64t..F+64t+63."""
+    W = synth.normal_bf16(0, synth.tid(f"tgu{F}.{K}"), (2 * F, K), sigma=0.02)
+    order = np.concatenate([np.r_[64 * t:64 * t + 64, F + 64 * t:F + 64 * t + 64] for t in range(F // 64)])
+    Wt = xv.tile_gate_up(dev(W))
+    assert Wt.gated and Wt.shape == (2 * F, K)
+    assert np.array_equal(host_u16(Wt.data), _tiles_by_definition(W[order]))
+
+
+@pytest.mark.parametrize("M,F,K", [(1, 512, 256), (8, 512, 256), (9, 1024, 1000), (64, 512, 256), (8, 17408, 5120)])
+def test_fused_swiglu_vs_oracle(xv, M, F, K):
+    """act = bf16(silu(g) u) with g, u the bf16 gate/up outputs: against the oracle's GEMM and
+    SwiGLU (bf16 tolerance), every row independent of M."""
+    X = synth.normal_bf16(0, synth.tid(f"sx{M}.{F}.{K}"), (64, K))
+    W = synth.normal_bf16(0, synth.tid(f"sw{F}.{K}"), (2 * F, K), sigma=0.05)
+    Wt = xv.tile_gate_up(dev(W))
+    Xd = dev(X)
+    act = torch.empty((M, F), dtype=torch.int16, device="cuda")
+    xv.xv_gemm_swiglu(Xd[:M], Wt, act)
+    cols = np.arange(F) if F <= 1024 else np.sort(np.random.default_rng(2).choice(F, 128, replace=False))
+    gu = oracle.round_bf16(oracle.gemm(X[:M], np.concatenate([W[cols], W[F + cols]])))
+    ref = oracle.swiglu(gu[:, :len(cols)], gu[:, len(cols):])
+    assert_bf16_close(host_u16(act)[:, cols], ref, what=f"fused swiglu {M}x{F}x{K}")
+    full = torch.empty((64, F), dtype=torch.int16, device="cuda")
+    xv.xv_gemm_swiglu(Xd, Wt, full)
+    assert same_bits(act, full[:M])
+    assert xv.xv_device_check() == 0
