@@ -13,6 +13,7 @@
 // committed state, then speculates over this call's k tokens without
 // writing the state; its own inputs become the next pending steps.  State
 // traffic is one read and one write per call instead of k writes.
+#include <algorithm>
 #include <vector>
 
 #include "xv_internal.h"
@@ -102,7 +103,9 @@ Carve carve(const Dims& d, int B, int kmax, int Lmax, uint8_t* base) {
     c.gu = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * 2 * d.F * 2));
     c.act = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(M) * d.F * 2));
     c.logits = reinterpret_cast<float*>(take(static_cast<size_t>(M) * d.V * 4));
-    c.argmax_ws = take(argmax_workspace_size(M, d.V));
+    // argmax partials: per 8192-logit chunk, or per LM-head tile when the LM head forms them
+    const size_t amax_tiles = static_cast<size_t>(M) * ceil_div(d.V, GEMM_BN) * sizeof(float2);
+    c.argmax_ws = take(std::max(argmax_workspace_size(M, d.V), amax_tiles));
     size_t g = 0;
     auto gm = [&](int N, int K) { size_t s = gemm_workspace_size(M, N, K); if (s > g) g = s; };
     if (d.gin) { gm(d.gin, d.H); gm(d.H, d.ginner); }
@@ -294,8 +297,17 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
         XV_TRY(residual_gemm(c.act, d.F, lw.w_down, next_norm));
     }
     if (head) {
-        XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, wt, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-        XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
+        if (gemm_splits(d.V, d.H) == 1) {
+            // the LM head leaves each tile's (max, lowest index) per row and writes logits only
+            // when the caller wants them; the acceptance kernel finishes the argmax
+            float2* amax = static_cast<float2*>(c.argmax_ws);
+            XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, wt, logits, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s,
+                               nullptr, nullptr, amax));
+            XV_TRY(accept_from_parts_launch(amax, ceil_div(d.V, GEMM_BN), B, k, argmax, tokens, k_seq, n_accept, s));
+        } else {
+            XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, wt, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
+            XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
+        }
     }
 #undef XV_TRY
     st->last_k = k;
@@ -387,8 +399,10 @@ xv_status xv_block_prefill(const xv_block_config* cfg, const xv_block_weights* w
                                                        cudaMemcpyDeviceToDevice, s),
                                      "prefill: gather the chunk"))
             return e;
-        // only the last chunk's logits are read: the others stop before the LM head
-        if (xv_status e = verify_impl(cfg, w, st, tok, k, nullptr, nullptr, am, na, ws, vbytes, stream, last)) return e;
+        // only the last chunk's logits are read: the others stop before the LM head, and the
+        // last one writes its logits (into the workspace) only when the caller asks for them
+        float* lg = (last && last_logits) ? c.logits : nullptr;
+        if (xv_status e = verify_impl(cfg, w, st, tok, k, nullptr, lg, am, na, ws, vbytes, stream, last)) return e;
         if (last) {
             // the last position of each sequence: row b*k + k - 1
             if (last_logits &&

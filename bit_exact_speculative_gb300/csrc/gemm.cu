@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         void* __restrict__ Y, int ldy, int M, int N, int nkb, int S, float* __restrict__ part,
                         unsigned* __restrict__ cnt, unsigned* __restrict__ err, int cluster_combine, int xb,
-                        int xr, int wtiled) {
+                        int xr, int wtiled, float2* __restrict__ amax) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_last;
     const uint32_t raw = smem_u32(smem_raw);
@@ -283,13 +283,42 @@ __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
             }
         }
     } else if (S == 1) {
-        if (live) {
+        if (live && Y) {
 #pragma unroll
             for (int m = 0; m < GEMM_TOK; ++m) {
                 if (m < M) {
                     if (F32OUT) static_cast<float*>(Y)[static_cast<size_t>(m) * ldy + n] = acc[m];
                     else static_cast<uint16_t*>(Y)[static_cast<size_t>(m) * ldy + n] = f32_to_bf16(acc[m]);
                 }
+            }
+        }
+        if (F32OUT && amax) {
+            // the tile's (max, lowest index) of every token row, for the argmax: rows parked in
+            // shared memory (the drained stage ring), then warp w reduces token rows w, w + 4, ...
+            // (value, -index) is a total order (a NaN never wins), so the final argmax over the
+            // tiles equals that of the whole row whatever the grouping
+            float* vbuf = reinterpret_cast<float*>(smem);   // [m][128]
+#pragma unroll
+            for (int m = 0; m < GEMM_TOK; ++m)
+                if (m < M) vbuf[m * GEMM_BN + warp * 32 + lane] = acc[m];
+            __syncthreads();
+#pragma unroll 1
+            for (int m = warp; m < M; m += 4) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = q * 32 + lane, row = tile * GEMM_BN + r;
+                    const float v = vbuf[m * GEMM_BN + r];
+                    if (row < N && (v > bv || (v == bv && row < bi))) { bv = v; bi = row; }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+                }
+                if (lane == 0) amax[static_cast<size_t>(m) * gridDim.x + tile] = make_float2(bv, __int_as_float(bi));
             }
         }
     } else if (!cnt) {
@@ -431,11 +460,15 @@ size_t gemm_workspace_size(int M, int N, int K) {
 }
 
 xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, WLayout wl, void* Y, int ldy, bool f32out, int M,
-                      int N, int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part, int* defer_S) {
+                      int N, int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part, int* defer_S,
+                      float2* amax) {
     (void)ws_bytes;
     const bool wtiled = wl != W_ROWS, gated = wl == W_GATED;
     if (gated && (f32out || N % 128))
         return fail(XV_ERR_UNSUPPORTED, "gemm: the fused SwiGLU needs bf16 out and a multiple of 64 features");
+    if (amax && (!f32out || gemm_splits(N, K) != 1))
+        return fail(XV_ERR_UNSUPPORTED, "gemm: argmax partials need fp32 out and an unsplit shape");
+    if (!Y && !amax) return fail(XV_ERR_ARG, "gemm: null Y");
     if (defer_part) *defer_part = nullptr;
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "gemm: device error word unavailable");
@@ -480,11 +513,13 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, WLayout wl,
     trace_pre(s);
     if (cluster)
         launch_k_cluster(kern, grid, dim3(128), smem, s, dim3(1, S, 1), tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt,
-                         err, cluster, xb, xr, wtiled ? 1 : 0);
+                         err, cluster, xb, xr, wtiled ? 1 : 0, amax);
     else
         launch_k(kern, grid, dim3(128), smem, s, tmW, tmX, Y, ldy, M, N, nkb, S, part, cnt, err, cluster, xb, xr,
-                 wtiled ? 1 : 0);
-    const long long bytes = 2ll * N * K + 2ll * M * K + static_cast<long long>(M) * (gated ? N / 2 : N) * (f32out ? 4 : 2);
+                 wtiled ? 1 : 0, amax);
+    const long long bytes = 2ll * N * K + 2ll * M * K +
+                            (Y ? static_cast<long long>(M) * (gated ? N / 2 : N) * (f32out ? 4 : 2) : 0) +
+                            (amax ? 8ll * M * tiles : 0);
     if (xv_status st = launched("gemm_small_m_kernel", s, K_GEMM, bytes)) return st;
     if (sep_combine && defer_part) {
         *defer_part = part;

@@ -378,6 +378,18 @@ xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t
     return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
 }
 
+xv_status accept_from_parts_launch(const float2* part, int nchunk, int B, int k, int32_t* idx, const int32_t* tokens,
+                                   const int32_t* k_seq, int32_t* n_accept, cudaStream_t s) {
+    unsigned* err = device_error_word();
+    if (!err) return fail(XV_ERR_CUDA, "argmax: device error word unavailable");
+    if (k < 1 || k > XV_KMAX) return fail(XV_ERR_ARG, "argmax: k = %d outside [1, %d]", k, XV_KMAX);
+    const int M = B * k;
+    trace_pre(s);
+    launch_k(argmax_accept_kernel, dim3(B), dim3(32 * (k < 32 ? k : 32)), 0, s, part, nchunk, k, idx, tokens, k_seq,
+             n_accept, err);
+    return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
+}
+
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, const int32_t* k_seq, int32_t* ctx_len,
                         int32_t* n_commit,
                         cudaStream_t s) {

@@ -94,9 +94,12 @@ bool gemm_uses_counters(int M, int N, int K);
 // the GEMM with the SwiGLU fused (N = 2F weight rows in, F bf16 activations per row out, never
 // split).
 enum WLayout : int { W_ROWS = 0, W_TILED = 1, W_GATED = 2 };
+// amax (fp32 out, unsplit shapes only): also writes, for every row m and weight tile t, the tile's
+// maximum and its lowest index as amax[m * ceil(N/128) + t] = (value, index bits); Y may then be
+// null (no outputs written).
 xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, WLayout wl, void* Y, int ldy, bool f32out, int M,
                       int N, int K, void* ws, size_t ws_bytes, cudaStream_t s, float** defer_part = nullptr,
-                      int* defer_S = nullptr);
+                      int* defer_S = nullptr, float2* amax = nullptr);
 // The tiled weight layout: [ceil(N/128)][ceil(K/64)][128][64] bf16, zero past N and K.
 size_t gemm_tiled_bytes(int N, int K);
 xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, bool gated, uint16_t* Wt, cudaStream_t s);
@@ -181,6 +184,10 @@ size_t argmax_workspace_size(int M, int V);
 // k_b = k_seq[b] (k when k_seq is null) (two kernels)
 xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
                                const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s);
+// The same from per-chunk (max, index) partials part[row * nchunk + c] already formed (the LM
+// head GEMM's amax output): the second kernel only.
+xv_status accept_from_parts_launch(const float2* part, int nchunk, int B, int k, int32_t* idx, const int32_t* tokens,
+                                   const int32_t* k_seq, int32_t* n_accept, cudaStream_t s);
 // ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (checked to lie in [1, k_b],
 // k_b = k_seq[b] or k)
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, const int32_t* k_seq, int32_t* ctx_len,

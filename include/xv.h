@@ -467,7 +467,8 @@ int xv_gdn_conv_stride(const xv_block_config* cfg);
  * configuration or sizes below 1). */
 size_t xv_block_workspace_size(const xv_block_config* cfg, int B, int kmax, int Lmax);
 
-/* tokens [B, k] int32 device; logits [B*k, V] fp32 device or NULL; argmax
+/* tokens [B, k] int32 device; logits [B*k, V] fp32 device or NULL (then no
+ * logits are written: the LM head leaves only per-tile argmax partials); argmax
  * [B*k] int32; n_accept [B] int32 = leading drafts equal to the argmax of the
  * position before them (0..k-1).  Requires 1 <= k <= st->kmax, B == st->B,
  * B*k <= XV_GEMM_M_MAX, st->max_ctx + k <= Lmax.  Appends the k rows to the KV

@@ -500,3 +500,21 @@ def test_stack_tiled_weights_equal_row_major(stack):
     for a, b in zip(*out):
         assert same_bits(a, b)
     del rm
+
+
+def test_stack_argmax_without_logits(stack):
+    """Without a logits buffer the LM head writes no logits and the argmax comes from its per-tile
+    partials alone: the same argmax ids and accept counts as with logits, at 8 sequences."""
+    cfg, w, wd = stack
+    B, k = 8, 8
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500]
+    Lmax = max(lens) + 64
+    A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd)
+    snap = snapshot(A)
+    toks = dev(workloads.draft_tokens(cfg, 0, 3, B, k))
+    lg, am, na = A.verify(toks, k)
+    am1, na1 = am.clone(), na.clone()
+    assert torch.equal(am1.cpu(), torch.argmax(lg, dim=1).to(torch.int32).cpu())
+    restore(A, snap)
+    _, am2, na2 = A.verify(toks, k, logits=False)
+    assert torch.equal(am1, am2) and torch.equal(na1, na2)
