@@ -496,8 +496,13 @@ xv_status gemm_launch(const uint16_t* X, int ldx, const uint16_t* W, WLayout wl,
     float* part = nullptr;
     unsigned* cnt = nullptr;
     // Past 8 token rows the last-arriving CTA's combine is a long serial tail (one round trip per
-    // 8 rows); a separate kernel with a thread per output combines them in one round trip.
-    const bool sep_combine = S > CLUSTER_MAX && M > X_SMALL_M;
+    // 8 rows); a separate kernel with a thread per output combines them in one round trip.  A
+    // caller that can take the partials itself (the residual RMSNorm after the output and down
+    // projections) always does: measured in the verify step at 8 rows, the last-arriving CTA's
+    // combine (fence, counter, then its partial loads queued behind the next GEMM's early weight
+    // loads) took 5-7 us after the last MMAs, and handing the partials on took the step from
+    // 805 to 795 us.
+    const bool sep_combine = S > CLUSTER_MAX && (M > X_SMALL_M || defer_part != nullptr);
     if (S > CLUSTER_MAX) {
         cnt = sep_combine ? nullptr : static_cast<unsigned*>(ws);
         part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + COUNTER_BYTES);

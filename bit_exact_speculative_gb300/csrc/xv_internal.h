@@ -86,9 +86,9 @@ size_t gemm_workspace_size(int M, int N, int K);
 constexpr size_t GEMM_COUNTER_BYTES = 1024;
 // Whether a GEMM of this shape combines its split-K partials through the workspace's tile counters.
 bool gemm_uses_counters(int M, int N, int K);
-// defer_part: when the GEMM would combine its partials in a separate kernel (M > 8, more segments
-// than a cluster), it skips that kernel and returns the partials [S][M][N] and S instead (else
-// *defer_part = nullptr).
+// defer_part: when the GEMM splits K into more segments than a cluster combines, it writes its
+// partials [S][M][N] and returns them and S instead of combining them (for any M; else
+// *defer_part = nullptr): the caller adds them in segment order.
 // Weight layouts: row-major [N, K]; tiled (gemm_tile_weights_launch); gated tiled, a gate/up
 // weight [2F, K] whose tiles pair 64 gate rows with the 64 up rows of the same features, read by
 // the GEMM with the SwiGLU fused (N = 2F weight rows in, F bf16 activations per row out, never
