@@ -72,7 +72,7 @@ constexpr int SM_COUNT_TARGET = 152;   // GB300
 // too few tiles to fill the GPU otherwise, go through the workspace.
 constexpr int CLUSTER_MAX = 4;
 constexpr int RESIDENT_PER_SM = 2;
-constexpr int MIN_SEGMENT_KB = 16;   // K-blocks a split-K segment streams at least
+constexpr int MIN_SEGMENT_KB = 8;    // K-blocks a split-K segment streams at least
 
 template <bool F32OUT, bool GATED>
 __global__ void __launch_bounds__(128, RESIDENT_PER_SM)
@@ -413,11 +413,14 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 }  // namespace
 
 // Shapes with more tiles than SMs stay whole; shapes of one to two SMs' worth split K in two;
-// narrow shapes split K to fill one wave of 2 CTAs per SM, with at least 16 K-blocks per segment.
+// narrow shapes split K to fill one wave of 2 CTAs per SM, with at least 8 K-blocks per segment.
 // Measured on GB300 with tiled weights, the verify step (B = 1 / B = 8, context 2183): the
 // 34816-wide gate/up and the LM head whole instead of in two halves 865 -> 819 / 1006 -> 918 us
 // (a CTA streams one contiguous run of its whole tile row, and no combine); the GDN output
-// projection (N = 5120, K = 4096) in 4 segments instead of 7: -5 us at B = 1; the input
+// projection (N = 5120, K = 4096) in 7 segments (9 K-blocks each) instead of 4 and the attention
+// output projection (K = 6144) in 7 instead of 6, now that their partials go to the residual
+// RMSNorm: -3.5 / -2 us (in 4 segments, while the last CTA of a tile still combined them, the
+// GDN output projection had been 5 us faster than in 7); the input
 // projections (97 and 112 tiles) whole +18 us, in 3 segments +9..+24 us; the down projection in
 // 6 or 7 segments the same, in 8 (a second wave) +67 us.  (With row-major weights the two-way
 // splits of the wide shapes had been the faster choice.)

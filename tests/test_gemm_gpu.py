@@ -64,10 +64,10 @@ def big(xv):
 def test_split_paths(xv):
     """The 17408-wide half of gate/up (136 tiles): 2 segments combined in a cluster; the fused
     34816-wide gate/up stays whole; down: 7 (one wave of 2 CTAs per SM) through the workspace;
-    narrow: 8 through the workspace; a shape too short in K for two segments stays whole."""
+    narrow: 16 through the workspace; a shape too short in K for two segments stays whole."""
     assert xv.xv_gemm_splits(17408, 5120) == 2
     assert xv.xv_gemm_splits(34816, 5120) == 1
-    assert xv.xv_gemm_splits(17408, 1024) == 1
+    assert xv.xv_gemm_splits(17408, 512) == 1
     assert xv.xv_gemm_splits(5120, 17408) == 7 and xv.xv_gemm_workspace_size(8, 5120, 17408) > 0
     assert xv.xv_gemm_splits(1024, 8192) > 4 and xv.xv_gemm_workspace_size(8, 1024, 8192) > 0
 

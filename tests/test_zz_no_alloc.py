@@ -48,10 +48,10 @@ def _noalloc(xv, X, W, M, N, K):
     return Y
 
 
-# (1, 1024, 8192) and (8, 5120, 17408) split K in 8 and 7 segments with at most 8 token rows:
+# (1, 1024, 8192) and (8, 5120, 17408) split K in 16 and 7 segments with at most 8 token rows:
 # their last-arriving CTAs combine the partials through the scratch's tile counters.  (16, ...)
-# and (64, ...) split as much but combine in a separate kernel; (5, 10000, 2048) takes a cluster
-# of two, (5, 300, 1000) stays whole.
+# and (64, ...) split as much but combine in a separate kernel; (5, 10000, 2048) and
+# (5, 300, 1000) take clusters of two.
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 8192), (8, 5120, 17408), (16, 1024, 8192), (64, 1024, 8192),
                                    (16, 5120, 17408), (5, 10000, 2048), (5, 300, 1000)])
 def test_noalloc_matches_workspace_entry_point_twice(xv, M, N, K):
