@@ -548,6 +548,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 struct CombineArgs {
     const int32_t* ctx_len;
     int len_bias, R, Hq, nsplit, max_len, hd;
+    int ch, nb;   // splits per staged chunk and chunk buffers (combine_shape)
     const float* opart;
     const float2* ml;
     const uint16_t* gate;
@@ -561,11 +562,22 @@ struct CombineArgs {
 // order s = 0..ns-1:  w_s = exp2(m_s - M), L += w_s l_s, acc += w_s o_s;  out = acc / L, where M
 // is the largest m_s (a maximum is exact in any order, so the CTA takes it as a tree).  The
 // split partials o_s of a (row, head) are contiguous: they stream through shared memory in
-// chunks of COMB_CH splits by bulk copies, COMB_NB chunks in flight.
+// chunks of up to COMB_CH splits by bulk copies, up to COMB_NB chunks in flight.  The staging is
+// sized by the number of splits (a short context needs a few KB, not 96): measured at batch 8 /
+// context 2183 (2048 CTAs), the full 96 KB let 2 CTAs share an SM and the combine ran in ~7
+// waves, 13 us of the step.
 constexpr int COMB_CH = 32, COMB_NB = 3;
 
+inline void combine_shape(int nsplit, int* ch, int* nb) {
+    *ch = nsplit < COMB_CH ? nsplit : COMB_CH;
+    const int chunks = (nsplit + *ch - 1) / *ch;
+    *nb = chunks < COMB_NB ? chunks : COMB_NB;
+}
+
 inline size_t combine_smem(int hd, int nsplit) {
-    return static_cast<size_t>(COMB_NB) * COMB_CH * hd * 4 + static_cast<size_t>(nsplit) * 8;
+    int ch, nb;
+    combine_shape(nsplit, &ch, &nb);
+    return static_cast<size_t>(nb) * ch * hd * 4 + static_cast<size_t>(nsplit) * 8;
 }
 
 __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
@@ -573,6 +585,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
     griddep_wait();
     extern __shared__ __align__(128) uint8_t csm[];
     __shared__ __align__(8) uint64_t cbar[COMB_NB];
+    const int CH = C.ch, NB = C.nb;
     __shared__ float wmax[4];
     __shared__ volatile int s_abort;
     const int hq = blockIdx.x % C.Hq;
@@ -583,25 +596,25 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
     const int ns = (len + ATTN_SPLIT - 1) / ATTN_SPLIT;
     const long long idx0 = (br * C.Hq + hq) * C.nsplit;
     const int tid = threadIdx.x, nt = blockDim.x;
-    float* obuf = reinterpret_cast<float*>(csm);               // COMB_NB chunks of [COMB_CH][hd]
-    float* wv = obuf + COMB_NB * COMB_CH * C.hd;               // w_s
+    float* obuf = reinterpret_cast<float*>(csm);               // NB chunks of [CH][hd]
+    float* wv = obuf + NB * CH * C.hd;                         // w_s
     float* lv = wv + C.nsplit;                                 // l_s
-    const int nchunk = (ns + COMB_CH - 1) / COMB_CH;
+    const int nchunk = (ns + CH - 1) / CH;
     const float* src = C.opart + idx0 * C.hd;
     auto bar = [&](int i) { return smem_u32(&cbar[i]); };
     auto issue = [&](int c) {
-        const int n = min(COMB_CH, ns - c * COMB_CH);
+        const int n = min(CH, ns - c * CH);
         const uint32_t bytes = static_cast<uint32_t>(n) * C.hd * 4;
-        mbar_arrive_expect_tx(bar(c % COMB_NB), bytes);
-        bulk_load(smem_u32(obuf + (c % COMB_NB) * COMB_CH * C.hd), src + static_cast<long long>(c) * COMB_CH * C.hd,
-                  bytes, bar(c % COMB_NB));
+        mbar_arrive_expect_tx(bar(c % NB), bytes);
+        bulk_load(smem_u32(obuf + (c % NB) * CH * C.hd), src + static_cast<long long>(c) * CH * C.hd, bytes,
+                  bar(c % NB));
     };
     int issued = 0;   // thread 0: chunks whose copies have been issued
     if (tid == 0) {
-        for (int i = 0; i < COMB_NB; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < NB; ++i) mbar_init(bar(i), 1);
         fence_mbar_init();
         s_abort = 0;
-        for (; issued < nchunk && issued < COMB_NB; ++issued) issue(issued);
+        for (; issued < nchunk && issued < NB; ++issued) issue(issued);
     }
     float mx = NEG_INF;
     for (int s = tid; s < ns; s += nt) {
@@ -621,11 +634,11 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
     const int d = 2 * tid;
     float L = 0.f, acc0 = 0.f, acc1 = 0.f;
     for (int c = 0; c < nchunk; ++c) {
-        const int st = c % COMB_NB;
-        if (!s_abort && !mbar_wait(bar(st), (c / COMB_NB) & 1u, C.err)) s_abort = 1;
+        const int st = c % NB;
+        if (!s_abort && !mbar_wait(bar(st), (c / NB) & 1u, C.err)) s_abort = 1;
         if (!s_abort) {
-            const float* ob = obuf + st * COMB_CH * C.hd + d;
-            const int s0 = c * COMB_CH, n = min(COMB_CH, ns - s0);
+            const float* ob = obuf + st * CH * C.hd + d;
+            const int s0 = c * CH, n = min(CH, ns - s0);
             for (int j = 0; j < n; ++j) {
                 const float w = wv[s0 + j];
                 const float2 o = *reinterpret_cast<const float2*>(ob + j * C.hd);
@@ -635,16 +648,16 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
             }
         }
         __syncthreads();   // every thread is done with chunk c's buffer
-        if (tid == 0 && c + COMB_NB < nchunk && !s_abort) {
+        if (tid == 0 && c + NB < nchunk && !s_abort) {
             fence_proxy_async_smem();
-            issue(c + COMB_NB);
+            issue(c + NB);
             ++issued;
         }
     }
     if (s_abort) {
         // copies still in flight land before the CTA leaves: wait for the last one of each buffer
         if (tid == 0)
-            for (int c = issued - 1; c >= 0 && c >= issued - COMB_NB; --c) mbar_wait(bar(c % COMB_NB), (c / COMB_NB) & 1u, C.err);
+            for (int c = issued - 1; c >= 0 && c >= issued - NB; --c) mbar_wait(bar(c % NB), (c / NB) & 1u, C.err);
         return;
     }
     float y0 = __fdiv_rn(acc0, L), y1 = __fdiv_rn(acc1, L);
@@ -755,7 +768,10 @@ xv_status attn_launch(const uint16_t* q, long long q_stride, const uint16_t* kc,
                scale * 1.4426950408889634f, opart, ml, err};
     xv_status st = hd == 256 ? launch_split<256>(tmK, tmV, a, B, s) : launch_split<64>(tmK, tmV, a, B, s);
     if (st) return st;
-    CombineArgs c{ctx_len, len_bias, R, Hq, nsplit, max_len, hd, opart, ml, gate, gate_stride, out, out_stride, err};
+    int cch, cnb;
+    combine_shape(nsplit, &cch, &cnb);
+    CombineArgs c{ctx_len, len_bias, R, Hq, nsplit, max_len, hd, cch, cnb, opart, ml, gate, gate_stride, out, out_stride,
+                  err};
     const size_t csm = combine_smem(hd, nsplit);
     if (xv_status e = kernel_smem_once(reinterpret_cast<const void*>(attn_combine_kernel), static_cast<int>(csm), false,
                                        "attn: set combine shared memory size"))
