@@ -37,14 +37,19 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 
 // y = bf16( x / sqrt(mean(x^2) + eps) * (1 + w) ); with y_res != null first x <- bf16(x + y_res);
 // with tokens != null the row is first gathered from the embedding, x <- E[tokens[row]].
-// One CTA per row; thread t < nt owns the 8-element chunks t, t + nt, ... (at most NORM_MAXC),
-// so the per-thread sum order and the tree below are fixed by H alone.
+// A thread-block cluster of NORM_CL CTAs per row: CTA q owns the 8-element chunks
+// [q cpc, (q + 1) cpc) of the row (cpc = ceil(H / 8 / NORM_CL)) and its thread t the chunks
+// q cpc + t, + nt, ... (at most NORM_MAXC).  The sum of squares runs per thread in chunk and
+// element order, through a fixed shuffle tree per warp, over the warps in order per CTA, and
+// over the CTAs in rank order (every CTA reads all the CTA sums over distributed shared memory
+// and adds them the same way), so its order is fixed by H alone.
 //
 // With part != null, y_res is instead bf16(part_0 + ... + part_{S-1}), a GEMM's split-K partials
-// [S][M][H] added in segment order (the bits of the GEMM's own combine).  All blockDim threads
-// first form that row of y in shared memory; threads past nt then take no chunk, and their
-// warps add zeros after the others in the fixed tree, which leaves the sum's bits unchanged.
+// [S][M][H] added in segment order (the bits of the GEMM's own combine), formed by the chunk's
+// owner.  Spreading a row over a cluster (rather than one CTA per row) spreads those partial
+// loads over NORM_CL SMs: measured at 8 rows, a row of 7 partials is 140 KB.
 constexpr int NORM_MAXC = 4;
+constexpr int NORM_CL = 8;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -88,48 +93,46 @@ __device__ __forceinline__ uint4 partial_sum8(const float* __restrict__ part, in
     return pack8(r);
 }
 
+constexpr int NORM_THREADS_MAX = 256;   // a row of up to NORM_CL * NORM_THREADS_MAX * NORM_MAXC chunks
+
 template <bool PART>
-__global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x, const uint16_t* __restrict__ y_res,
+__global__ void __launch_bounds__(NORM_THREADS_MAX) rmsnorm_kernel(uint16_t* __restrict__ x, const uint16_t* __restrict__ y_res,
                                                        const uint16_t* __restrict__ w, int H, float eps,
                                                        uint16_t* __restrict__ out, const int32_t* __restrict__ tokens,
                                                        const uint16_t* __restrict__ E, int V, unsigned* err,
-                                                       const float* __restrict__ part, int S, int M, int nt) {
+                                                       const float* __restrict__ part, int S, int M, int cpc) {
     griddep_launch();
     griddep_wait();
     __shared__ float red[33];
-    extern __shared__ uint4 ysm[];
-    const long long row = blockIdx.x;
-    const int nch = H / 8;
+    __shared__ float cta_ss;
+    const int q = static_cast<int>(cluster_ctarank());
+    const long long row = blockIdx.y;
+    const int nch = H / 8, nt = blockDim.x;
+    const int c0 = q * cpc, c1 = min(c0 + cpc, nch);
     uint4* xr = reinterpret_cast<uint4*>(x + row * H);
     const uint4* src = xr;
     if (tokens) {
         int t = tokens[row];
         if (t < 0 || t >= V) {
-            if (threadIdx.x == 0) atomicOr(err, ERR_BAD_TOKEN);
+            if (q == 0 && threadIdx.x == 0) atomicOr(err, ERR_BAD_TOKEN);
             t = 0;
         }
         src = reinterpret_cast<const uint4*>(E + static_cast<long long>(t) * H);
     }
     const uint4* yr = y_res ? reinterpret_cast<const uint4*>(y_res + row * H) : nullptr;
-    if constexpr (PART) {
-        for (int c = threadIdx.x; c < nch; c += blockDim.x) ysm[c] = partial_sum8(part, S, M, H, row, c);
-        __syncthreads();
-        yr = ysm;
-    }
-    const bool owner = !PART || threadIdx.x < nt;
     float v[NORM_MAXC][8];
     float ss = 0.f;
     bool first = true;
 #pragma unroll
     for (int j = 0; j < NORM_MAXC; ++j) {
-        const int c = threadIdx.x + j * nt;
-        if (owner && c < nch) {
+        const int c = c0 + threadIdx.x + j * nt;
+        if (c < c1) {
             const uint4 raw = src[c];
             if (tokens) xr[c] = raw;
             unpack8(raw, v[j]);
-            if (yr) {
+            if (PART || yr) {
                 float t[8];
-                unpack8(yr[c], t);
+                unpack8(PART ? partial_sum8(part, S, M, H, row, c) : yr[c], t);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[j][e] = bf16_to_f32(f32_to_bf16(__fadd_rn(v[j][e], t[e])));
                 xr[c] = pack8(v[j]);
@@ -142,13 +145,19 @@ __global__ void __launch_bounds__(1024) rmsnorm_kernel(uint16_t* __restrict__ x,
         }
     }
     ss = block_sum_fixed(ss, red);
+    if (threadIdx.x == 0) cta_ss = ss;
+    cluster_sync();
+    const uint32_t a = smem_u32(&cta_ss);
+    ss = ld_dsmem(mapa_shared(a, 0));
+    for (int r = 1; r < NORM_CL; ++r) ss = __fadd_rn(ss, ld_dsmem(mapa_shared(a, r)));
+    cluster_sync();   // no CTA leaves while a peer may still read its sum
     const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), eps)));
     const uint4* wr = reinterpret_cast<const uint4*>(w);
     uint4* orow = reinterpret_cast<uint4*>(out + row * H);
 #pragma unroll
     for (int j = 0; j < NORM_MAXC; ++j) {
-        const int c = threadIdx.x + j * nt;
-        if (owner && c < nch) {
+        const int c = c0 + threadIdx.x + j * nt;
+        if (c < c1) {
             float wf[8], o[8];
             unpack8(wr[c], wf);
 #pragma unroll
@@ -306,17 +315,33 @@ __global__ void zero_i32_kernel(int32_t* p, int n) {
 }  // namespace
 
 
+// Chunks per CTA of a row's cluster, and threads per CTA (one chunk each when that fits).
+static int norm_cpc(int H) { return (H / 8 + NORM_CL - 1) / NORM_CL; }
 static int norm_threads(int H) {
-    int t = ((H / 8 + NORM_MAXC - 1) / NORM_MAXC + 31) / 32 * 32;
-    const int want = (H / 8 + 31) / 32 * 32;       // one chunk per thread when it fits
-    if (want <= 1024) t = want;
+    const int cpc = norm_cpc(H);
+    int t = ((cpc + NORM_MAXC - 1) / NORM_MAXC + 31) / 32 * 32;
+    const int want = (cpc + 31) / 32 * 32;       // one chunk per thread when it fits
+    if (want <= NORM_THREADS_MAX) t = want;
     return t < 32 ? 32 : t;
+}
+static xv_status norm_width(int H) {
+    if (H < 8 || H % 8 || norm_threads(H) > NORM_THREADS_MAX)
+        return fail(XV_ERR_UNSUPPORTED, "rmsnorm: width %d (a multiple of 8 up to %d)", H,
+                    NORM_CL * NORM_THREADS_MAX * NORM_MAXC * 8);
+    return XV_OK;
+}
+
+template <bool PART, typename... Args>
+static void launch_norm(int M, int H, cudaStream_t s, Args&&... args) {
+    launch_k_cluster(rmsnorm_kernel<PART>, dim3(NORM_CL, M), dim3(norm_threads(H)), 0, s, dim3(NORM_CL, 1, 1),
+                     static_cast<Args&&>(args)..., norm_cpc(H));
 }
 
 xv_status rmsnorm_launch(const uint16_t* x, const uint16_t* w, int M, int H, float eps, uint16_t* y, cudaStream_t s) {
+    if (xv_status st = norm_width(H)) return st;
     trace_pre(s);
-    launch_k(rmsnorm_kernel<false>, dim3(M), dim3(norm_threads(H)), 0, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y,
-             nullptr, nullptr, 0, nullptr, nullptr, 0, 0, norm_threads(H));
+    launch_norm<false>(M, H, s, const_cast<uint16_t*>(x), nullptr, w, H, eps, y, nullptr, nullptr, 0, nullptr, nullptr,
+                       0, 0);
     return launched("rmsnorm_kernel", s, K_RMSNORM, 4ll * M * H + 2ll * H);
 }
 
@@ -324,31 +349,26 @@ xv_status embed_rmsnorm_launch(const int32_t* tokens, int M, const uint16_t* E, 
                                float eps, uint16_t* x, uint16_t* xn, cudaStream_t s) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "embed: device error word unavailable");
+    if (xv_status st = norm_width(H)) return st;
     trace_pre(s);
-    launch_k(rmsnorm_kernel<false>, dim3(M), dim3(norm_threads(H)), 0, s, x, nullptr, w, H, eps, xn, tokens, E, V, err,
-             nullptr, 0, 0, norm_threads(H));
+    launch_norm<false>(M, H, s, x, nullptr, w, H, eps, xn, tokens, E, V, err, nullptr, 0, 0);
     return launched("rmsnorm_kernel(embed)", s, K_EMBED, 6ll * M * H + 2ll * H + 4ll * M);
 }
 
 xv_status residual_rmsnorm_launch(uint16_t* x, const uint16_t* y, const uint16_t* w, int M, int H, float eps, uint16_t* xn,
                                   cudaStream_t s) {
+    if (xv_status st = norm_width(H)) return st;
     trace_pre(s);
-    launch_k(rmsnorm_kernel<false>, dim3(M), dim3(norm_threads(H)), 0, s, x, y, w, H, eps, xn, nullptr, nullptr, 0, nullptr,
-             nullptr, 0, 0, norm_threads(H));
+    launch_norm<false>(M, H, s, x, y, w, H, eps, xn, nullptr, nullptr, 0, nullptr, nullptr, 0, 0);
     return launched("rmsnorm_kernel(residual)", s, K_RMSNORM, 8ll * M * H + 2ll * H);
 }
 
 xv_status residual_rmsnorm_part_launch(uint16_t* x, const float* part, int S, const uint16_t* w, int M, int H, float eps,
                                        uint16_t* xn, cudaStream_t s) {
     if (S < 1 || S > 16) return fail(XV_ERR_ARG, "rmsnorm: %d partials outside [1, 16]", S);
-    if (H % 8 || H > 16384) return fail(XV_ERR_UNSUPPORTED, "rmsnorm: width %d with partials", H);
+    if (xv_status st = norm_width(H)) return st;
     trace_pre(s);
-    const int nt = norm_threads(H);
-    int threads = (H / 8 + 31) / 32 * 32;
-    if (threads > 1024) threads = 1024;
-    if (threads < nt) threads = nt;
-    launch_k(rmsnorm_kernel<true>, dim3(M), dim3(threads), static_cast<size_t>(H) * 2, s, x, nullptr, w, H, eps, xn, nullptr,
-             nullptr, 0, nullptr, part, S, M, nt);
+    launch_norm<true>(M, H, s, x, nullptr, w, H, eps, xn, nullptr, nullptr, 0, nullptr, part, S, M);
     return launched("rmsnorm_kernel(residual, partials)", s, K_RMSNORM, 4ll * S * M * H + 6ll * M * H + 2ll * H);
 }
 
