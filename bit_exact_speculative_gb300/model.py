@@ -192,8 +192,10 @@ class HybridStack:
         self.ws = xv.workspace(self.blk.ws_bytes, device=d)
         self._pf_ws = None           # the prefill workspace, made on first use
         self.logits = torch.empty((B * kmax, cfg["vocab"]), dtype=torch.float32, device=d)
-        self.argmax = torch.empty(B * kmax, dtype=torch.int32, device=d)
-        self.n_accept = torch.empty(B, dtype=torch.int32, device=d)
+        # argmax ids and accept counts side by side, so that one copy reads a step's results
+        self.results = torch.empty(B * kmax + B, dtype=torch.int32, device=d)
+        self.argmax = self.results[: B * kmax]
+        self.n_accept = self.results[B * kmax:]
 
     def set_context(self, ctx_len):
         """Sets every sequence's committed length (host list); the caller has filled the caches/states."""
