@@ -406,7 +406,7 @@ xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z
 
 // ------------------------------------------------------------- attention
 
-int xv_attn_split_size(void) { return ATTN_SPLIT; }
+int xv_attn_split_begin(int s) { return s < 0 ? -1 : attn_split_begin(s); }
 
 size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx) {
     if (B < 1 || R < 1 || Hq < 1 || hd < 1 || max_ctx < 1) return 0;

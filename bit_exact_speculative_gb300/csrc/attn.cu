@@ -5,13 +5,14 @@
 // Here every row — a decode token or draft position r of a verify block — is
 // computed by exactly the same sequence of operations, determined by its own
 // length alone:
-//   - positions are cut into splits of ATTN_SPLIT tokens at fixed absolute
-//     boundaries, and each split into tiles of 64 positions;
+//   - positions are cut into splits at fixed absolute boundaries (512
+//     positions each below 4096, 2048 beyond: attn_split_begin), and each
+//     split into tiles of 64 positions;
 //   - inside a split, an fp32 online softmax (log2 domain) runs over the
 //     split's tiles in order; a tile or position past the row's length is
 //     masked to -inf, contributes p = 0, and leaves the reference max, sum and
 //     output bit-for-bit unchanged;
-//   - the splits 0..ceil(len/ATTN_SPLIT)-1 are combined in split order by a
+//   - the splits 0..attn_split_count(len)-1 are combined in split order by a
 //     second kernel.
 // The rows of a verify block share the K/V tiles (loaded once per CTA, for
 // up to 64 rows (r, q head) of a kv head; more rows take more CTAs, which
@@ -127,9 +128,9 @@ __device__ __forceinline__ AttnItem attn_item(const AttnArgs& A, int it, int nrt
     // the longest visible length among the item's rows; positions past a row's own length are
     // masked (p = 0), so how far the item runs does not change any row's bits
     I.maxlen = I.L0 + (min(rows, I.row_base + 64) - 1) / A.G;
-    I.p_begin = I.split * ATTN_SPLIT;
+    I.p_begin = attn_split_begin(I.split);
     I.live = !I.bad && I.p_begin < I.maxlen;
-    I.ntiles = I.live ? (min(I.p_begin + ATTN_SPLIT, I.maxlen) - I.p_begin + T - 1) / T : 0;
+    I.ntiles = I.live ? (min(attn_split_begin(I.split + 1), I.maxlen) - I.p_begin + T - 1) / T : 0;
     return I;
 }
 
@@ -593,7 +594,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs C) {
     const int b = static_cast<int>(br / C.R), r = static_cast<int>(br % C.R);
     const int len = C.ctx_len[b] + C.len_bias + r;
     if (len < 1 || len - r + C.R - 1 > C.max_len) return;   // reported by the split kernel
-    const int ns = (len + ATTN_SPLIT - 1) / ATTN_SPLIT;
+    const int ns = attn_split_count(len);
     const long long idx0 = (br * C.Hq + hq) * C.nsplit;
     const int tid = threadIdx.x, nt = blockDim.x;
     float* obuf = reinterpret_cast<float*>(csm);               // NB chunks of [CH][hd]
@@ -708,7 +709,7 @@ __global__ void kv_append_kernel(const uint16_t* __restrict__ src, long long src
 }
 
 inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-inline int nsplit_for(int max_len) { return (max_len + ATTN_SPLIT - 1) / ATTN_SPLIT; }
+inline int nsplit_for(int max_len) { return attn_split_count(max_len); }
 
 template <int HD>
 xv_status launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int B, cudaStream_t s) {

@@ -143,7 +143,24 @@ xv_status gated_norm_launch(const uint16_t* o, long long o_stride, const uint16_
                             cudaStream_t s);
 
 // ---- attention (attn.cu)
-constexpr int ATTN_SPLIT = 512;   // positions per split, fixed absolute boundaries
+// Splits at fixed absolute boundaries: ATTN_SPLIT positions each below ATTN_SPLIT_SWITCH,
+// ATTN_SPLIT_LONG beyond.  Measured on GB300 (verify step, context 131072): splits of 2048 past
+// 4096 instead of 512 throughout cut the persistent CTAs' item boundaries (about 3 us each) from
+// ~7 to ~2 per CTA at batch 1 and from ~54 to ~15 at batch 8: 900 -> 872 us and 1738 -> 1636 us
+// per step; 1024 past 4096 or 2048: -9 / -95 us; 4096 past 16384: +370 us at batch 8 (too few,
+// too coarse items to balance); shorter contexts are unchanged.
+constexpr int ATTN_SPLIT = 512, ATTN_SPLIT_SWITCH = 4096, ATTN_SPLIT_LONG = 2048;
+// First position of split s; split s covers [attn_split_begin(s), attn_split_begin(s + 1)).
+__host__ __device__ inline int attn_split_begin(int s) {
+    constexpr int NS = ATTN_SPLIT_SWITCH / ATTN_SPLIT;
+    return s < NS ? s * ATTN_SPLIT : ATTN_SPLIT_SWITCH + (s - NS) * ATTN_SPLIT_LONG;
+}
+// Splits a row of `len` visible positions spans.
+__host__ __device__ inline int attn_split_count(int len) {
+    constexpr int NS = ATTN_SPLIT_SWITCH / ATTN_SPLIT;
+    return len <= ATTN_SPLIT_SWITCH ? (len + ATTN_SPLIT - 1) / ATTN_SPLIT
+                                    : NS + (len - ATTN_SPLIT_SWITCH + ATTN_SPLIT_LONG - 1) / ATTN_SPLIT_LONG;
+}
 constexpr int ATTN_TILE = 64;     // positions per tile inside a split
 size_t attn_workspace_size(int B, int R, int Hq, int hd, int max_len);
 // Where position p of sequence b lives in a K or V cache of Hkv heads: page

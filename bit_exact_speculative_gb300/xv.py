@@ -98,7 +98,7 @@ _SIGS = {
     "xv_gdn_conv": ([vp, vp, c_ll, c_int, vp, c_int, vp, c_ll, c_int, c_int, vp, c_int, c_int, c_int, vp, c_ll, vp],
                     c_int),
     "xv_gated_norm": ([vp, c_ll, vp, c_ll, vp, c_int, c_int, c_int, c_float, vp, c_ll, vp], c_int),
-    "xv_attn_split_size": ([], c_int),
+    "xv_attn_split_begin": ([c_int], c_int),
     "xv_attn_workspace_size": ([c_int, c_int, c_int, c_int, c_int], c_sz),
     "xv_attn_decode_rows": ([vp, c_ll, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                              vp, c_ll, vp, c_ll, vp, c_sz, vp], c_int),
@@ -330,8 +330,9 @@ def xv_gated_norm(o, o_stride: int, z, z_stride: int, w, M: int, H: int, dv: int
 
 # ------------------------------------------------------------- attention
 
-def xv_attn_split_size() -> int:
-    return int(lib().xv_attn_split_size())
+def xv_attn_split_begin(s: int) -> int:
+    """First position of attention split s (fixed absolute boundaries)."""
+    return int(lib().xv_attn_split_begin(s))
 
 
 def xv_attn_workspace_size(B, R, Hq, hd, max_ctx) -> int:

@@ -55,7 +55,7 @@ typedef int xv_status;
 #define XV_ERR_CUDA        -4   /* a CUDA runtime call or launch failed */
 #define XV_ERR_DEVICE_CHECK -5  /* a kernel recorded a device-side error (see xv_device_check) */
 
-#define XV_ABI_VERSION 4
+#define XV_ABI_VERSION 5
 #define XV_GEMM_M_MAX 64        /* rows per small-M GEMM call */
 #define XV_KMAX 64              /* tokens per sequence per verify (or prefill chunk) call */
 #define XV_CONV_MAX 8           /* widest causal convolution of a complete GDN layer */
@@ -299,10 +299,12 @@ xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z
  * as decode rows, one per draft position.  Row r of sequence b is the query
  * at position ctx_len[b] - 1 + r and attends to positions [0, ctx_len[b] + r):
  *   out = softmax(q . K^T * scale) V      per query head h, kv head h / (Hq/Hkv).
- * The positions are cut into splits of xv_attn_split_size() tokens at fixed
- * absolute boundaries, each split is reduced with an fp32 online softmax over
- * fixed 64-position tiles, and the splits are combined in split order; a row
- * therefore gets the same bits as an R = 1 call with ctx_len[b] + r.
+ * The positions are cut into splits at fixed absolute boundaries (split s
+ * covers [xv_attn_split_begin(s), xv_attn_split_begin(s + 1)): 512 positions
+ * each below 4096, 2048 beyond), each split is reduced with an fp32 online
+ * softmax over fixed 64-position tiles, and the splits are combined in split
+ * order; a row therefore gets the same bits as an R = 1 call with
+ * ctx_len[b] + r.
  *
  *   q     [B*R rows, Hq*hd] bf16, row stride q_stride elements (16-byte aligned rows)
  *   kc,vc [B, Hkv, Lmax, hd] bf16 (16-byte aligned)
@@ -324,7 +326,7 @@ xv_status xv_gated_norm(const uint16_t* o, long long o_stride, const uint16_t* z
  * caches or workspace), XV_ERR_WORKSPACE (missing or small workspace),
  * XV_ERR_CUDA (launch).  A sequence whose ctx_len[b] + R - 1 falls outside
  * [1, max_ctx] is skipped on the device and reported by xv_device_check. */
-int xv_attn_split_size(void);
+int xv_attn_split_begin(int s);   /* -1 for s < 0 */
 size_t xv_attn_workspace_size(int B, int R, int Hq, int hd, int max_ctx);
 xv_status xv_attn_decode_rows(const uint16_t* q, long long q_stride, const uint16_t* kc, const uint16_t* vc,
                               const int32_t* ctx_len, int R, int B, int Hq, int Hkv, int hd, int Lmax,

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(xv):
 
 
 def test_abi_version(xv):
-    assert xv.xv_abi_version() == 4
+    assert xv.xv_abi_version() == 5
 
 
 def _code(fn, *args):
@@ -156,7 +156,9 @@ def test_attn_validation_without_gpu(xv):
     assert L.xv_attn_decode_rows(*args(max_ctx=5000)) == xv.XV_ERR_ARG              # beyond Lmax
     assert L.xv_attn_decode_rows(*args(ws=None)) == xv.XV_ERR_WORKSPACE
     assert L.xv_attn_decode_rows(*args(ws=ctypes.c_void_p(0x10008))) == xv.XV_ERR_UNSUPPORTED   # misaligned
-    assert xv.xv_attn_split_size() == 512
+    # splits of 512 positions below 4096, 2048 beyond
+    assert [xv.xv_attn_split_begin(s) for s in (0, 1, 7, 8, 9, 10)] == [0, 512, 3584, 4096, 6144, 8192]
+    assert xv.xv_attn_split_begin(-1) == -1
     assert xv.xv_attn_workspace_size(1, 8, 24, 256, 2183) >= 8 * 24 * 5 * 256 * 4
 
 

@@ -47,7 +47,8 @@ def attn(xv, q, kc, vc, ctx, R, B, Hq, Hkv, hd, Lmax, max_ctx, gate=None):
 
 
 @pytest.mark.parametrize("hd,Hq,Hkv,R,lens", [(256, 4, 2, 3, [700, 1100]), (64, 2, 1, 4, [128, 1]),
-                                               (256, 24, 4, 8, [2183]), (64, 6, 2, 1, [63, 64, 65, 513])])
+                                               (256, 24, 4, 8, [2183]), (64, 6, 2, 1, [63, 64, 65, 513]),
+                                               (64, 4, 2, 8, [4093, 6141])])
 def test_parity_with_oracle(xv, hd, Hq, Hkv, R, lens):
     B = len(lens)
     Lmax = max(lens) + R + 64
@@ -74,9 +75,10 @@ def test_gated_output_parity(xv):
     assert_bf16_close(out, gated, rel=2 * 2e-2, what="gated")
 
 
-@pytest.mark.parametrize("L", [640, 2183, 131072])
+@pytest.mark.parametrize("L", [640, 2183, 4090, 6140, 131072])
 def test_verify_rows_equal_decode_rows(xv, L):
-    """Row r of an R=8 call equals an R=1 call with ctx_len + r (GQA 24/4, hd 256)."""
+    """Row r of an R=8 call equals an R=1 call with ctx_len + r (GQA 24/4, hd 256); at 4090 and
+    6140 the rows cross the switch to 2048-position splits at 4096 and a long split's end."""
     B, R, Hq, Hkv, hd = 1, 8, 24, 4, 256
     Lmax = L + R
     q, kc, vc = make(3, B, R, Hq, Hkv, hd, Lmax, name=f"rows{L}")

@@ -374,16 +374,17 @@ def test_attn_rows_gqa_mapping_and_causal_rows():
 def test_attn_split_combine_identity():
     """Softmax attention over any partition of the positions: per part the local max m_p, sum l_p
     and unnormalised output o_p, merged with weights exp(m_p - M), equals the explicit softmax of
-    the oracle to 1e-12 (the identity the split kernels rest on), for the fixed 512-position
-    splits and for random cuts."""
+    the oracle to 1e-12 (the identity the split kernels rest on), for the kernels' fixed splits
+    (512 positions below 4096, 2048 beyond) and for random cuts."""
     rng = np.random.default_rng(17)
-    hd, n = 16, 1300
+    hd, n = 16, 9000
     q, K, V = bf(rng.normal(size=hd)), bf(rng.normal(size=(n, hd))), bf(rng.normal(size=(n, hd)))
     scale = 0.3
     ref = oracle.attn_row(q, K, V, n, scale)
     s = oracle.bf16_to_f64(K) @ oracle.bf16_to_f64(q) * scale
     Vf = oracle.bf16_to_f64(V)
-    cuts_list = [list(range(0, n, 512)) + [n], [0] + sorted(rng.choice(np.arange(1, n), 9, replace=False).tolist()) + [n]]
+    fixed = list(range(0, 4096, 512)) + list(range(4096, n, 2048)) + [n]
+    cuts_list = [fixed, [0] + sorted(rng.choice(np.arange(1, n), 9, replace=False).tolist()) + [n]]
     for cuts in cuts_list:
         parts = []
         for a, b in zip(cuts[:-1], cuts[1:]):
