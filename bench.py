@@ -18,6 +18,7 @@ over the max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import atexit
 import json
 import os
 import subprocess
@@ -80,7 +81,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running, each sample tagged
+    with the host time it arrived."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -91,17 +93,18 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "50", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                          "-lms", "20", "-i", str(self.index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            atexit.register(self.__exit__)   # the sampler never outlives the bench, even on an error
         except FileNotFoundError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def wait_first(self, timeout=5.0):
         """Blocks until the sampler has produced a line (so the timed region is covered)."""
@@ -110,27 +113,37 @@ class ClockSampler:
             time.sleep(0.02)
 
     def __exit__(self, *a):
-        if self.proc:
+        if self.proc and self.proc.poll() is None:
             self.proc.terminate()
             self.proc.wait(timeout=5)
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    def summary(self, t0, t1, t_load):
+        """Samples of the timed region [t0, t1] (host times), and of the loaded window [t0, t_load]
+        that continues it with more steps of the same workload: the median SM clock over the
+        timed region's samples (over the loaded window's when a short region caught fewer than
+        three), throttle reasons seen anywhere in the loaded window."""
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        timed, loaded, mx, reasons = [], [], None, set()
+        for t, ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 7 or not (t0 <= t <= t_load):
                 continue
             try:
-                sm.append(float(parts[0]))
+                f = float(parts[0])
                 mx = float(parts[1])
             except ValueError:
                 continue
+            loaded.append(f)
+            if t <= t1:
+                timed.append(f)
             for n, v in zip(names, parts[3:7]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        use = timed if len(timed) >= 3 else loaded
+        return {"sm_mhz": float(np.median(use)) if use else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(timed), "samples_loaded": len(loaded),
+                "window": "timed region" if use is timed else
+                          "timed region and the traced and end-to-end steps that follow it"}
 
 
 def dist_env():
@@ -620,19 +633,20 @@ def run_gpu(args):
 
     # ---- timed region: K steps on device-resident inputs
     launches0 = xv.xv_launch_count()
-    with ClockSampler(local) as clk:
-        clk.wait_first()
-        barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step(rnd)
-            rnd += 1
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        time.sleep(0.25)   # one more sample after the region
+    clk = ClockSampler(local).__enter__()
+    clk.wait_first()
+    barrier()
+    torch.cuda.synchronize()
+    t_region0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(rnd)
+        rnd += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_region1 = time.time()
+    barrier()
     launches = xv.xv_launch_count() - launches0
     ms = e0.elapsed_time(e1)
     value, s_max, _ = job_throughput(ms / 1e3, B * k * args.steps, device)   # all ranks' tokens / slowest
@@ -679,6 +693,9 @@ def run_gpu(args):
         stk.commit()
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
+    t_loaded = time.time()
+    clk.__exit__(None, None, None)
+    clocks = clk.summary(t_region0, t_region1, t_loaded)
     e2e_value, _, _ = job_throughput(e2e_s, B * k * args.steps, device)
     barrier()
 
@@ -728,7 +745,7 @@ def run_gpu(args):
             "more_configs": more,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(B * k * 4),
                     "d2h_bytes_per_step": int(stk_results_bytes)},
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "kernel_rooflines": rooflines,
             "device_error_bits": code,
         }
