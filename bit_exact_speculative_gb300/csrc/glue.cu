@@ -68,7 +68,7 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 
 // Sum of the S partials of the 8 elements of chunk c of `row`, in segment order, as bf16.
 __device__ __forceinline__ uint4 partial_sum8(const float* __restrict__ part, int S, int M, int H, long long row, int c) {
-    constexpr int G = 4;   // segments whose loads are in flight together
+    constexpr int G = 8;   // segments whose loads are in flight together (7 per projection: one round trip)
     float r[8];
     for (int q0 = 0; q0 < S; q0 += G) {
         float4 p[G][2];
