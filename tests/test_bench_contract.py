@@ -5,6 +5,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -34,3 +35,21 @@ def test_reference_line_keys(reference_line):
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_clock_record_uses_the_timed_region():
+    """The clock record of the GPU line: the median over the samples taken inside the timed region
+    when there are at least three, else over the loaded window that continues it (and it says
+    which); throttle reasons seen anywhere in the loaded window are reported."""
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+    line = lambda mhz, pc="Not Active": f"{mhz}, 2070, 900.0, Not Active, Not Active, Not Active, {pc}"
+    c.lines = [(0.5, line(900)), (1.1, line(2070)), (1.2, line(2060)), (1.3, line(2070)), (1.9, line(2000, "Active")),
+               (3.0, line(1000))]
+    s = c.summary(1.0, 1.5, 2.0)
+    assert s["samples"] == 3 and s["samples_loaded"] == 4 and s["sm_mhz"] == 2070.0
+    assert s["window"] == "timed region" and s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
+    short = c.summary(1.0, 1.15, 2.0)
+    assert short["samples"] == 1 and short["window"].startswith("timed region and")
+    assert short["sm_mhz"] == float(np.median([2070, 2060, 2070, 2000]))
