@@ -78,7 +78,7 @@ def test_tiny_forced_reject_then_next_round(tiny, keep):
     sequential(S, t1[:, :keep], B)
     lgS, _ = sequential(S, t2, B)
     assert same_bits(lgA.view(B, k, -1), lgS)
-    # commit all of round 2 and flush both: GDN states and lengths agree bit for bit
+    # commit all of the second verify and flush both: GDN states and lengths agree bit for bit
     A.commit(torch.full((B,), k, dtype=torch.int32, device="cuda"))
     A.flush()
     S.flush()
@@ -341,14 +341,14 @@ def test_stack_ragged_k_per_sequence(stack):
     for b in range(B):
         S = gpu_stack(cfg, w, B, kmax, Lmax, lens, weights_dev=wd, only=b)
         lgS, amS = sequential(S, t1[b:b + 1, :ks1[b]], 1)
-        assert same_bits(lg1[b, :ks1[b]], lgS[0]), f"sequence {b}, round 1"
+        assert same_bits(lg1[b, :ks1[b]], lgS[0]), f"sequence {b}, first verify"
         assert np.array_equal(am1[b, :ks1[b]], host(amS[0]))
         assert int(na1[b]) == oracle.accept(t1[b, :ks1[b]], am1[b, :ks1[b]])
         del S
         S = gpu_stack(cfg, w, B, kmax, Lmax, lens, weights_dev=wd, only=b)
         sequential(S, t1[b:b + 1, :keep[b]], 1)
         lgS, _ = sequential(S, t2[b:b + 1, :ks2[b]], 1)
-        assert same_bits(lg2[b, :ks2[b]], lgS[0]), f"sequence {b}, round 2"
+        assert same_bits(lg2[b, :ks2[b]], lgS[0]), f"sequence {b}, second verify"
         del S
         torch.cuda.empty_cache()
 

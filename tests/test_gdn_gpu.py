@@ -154,10 +154,10 @@ def test_replay_then_speculate_matches_decode(xv, K, keep):
     """Round 2 of a speculative loop: replay `keep` kept steps, speculate K new ones (up to 128
     staged steps in one call)."""
     B = 2
-    qkv_h, gates_h = make_inputs(5, B, 2 * K)          # rows b*2K + t: first K = round 1, last K = round 2
+    qkv_h, gates_h = make_inputs(5, B, 2 * K)          # rows b*2K + t: first K = first verify, last K = second verify
     qkv, gates = dev(qkv_h), dev(gates_h)
     S0 = dev(init_state(5, B))
-    # decode reference: `keep` steps of round 1, then the K of round 2
+    # decode reference: `keep` steps of the first verify, then the K of the second
     Sd = S0.clone()
     outs = []
     for t in list(range(keep)) + list(range(K, 2 * K)):
@@ -168,7 +168,7 @@ def test_replay_then_speculate_matches_decode(xv, K, keep):
         xv.xv_gdn_decode_step(Sd, st, ob, H * DV, B, H, DK, DV, False)
         outs.append(ob)
     ref = torch.stack(outs[keep:], dim=1)
-    # verify: pending = round 1 rows (rows_per_seq 2K from row 0), draft = round 2 rows (from row K)
+    # verify: pending = the first verify's rows (rows_per_seq 2K from row 0), draft = the second's (from row K)
     Sv = S0.clone()
     pend = steps(xv, qkv, gates, 2 * K)
     draft = steps(xv, qkv, gates, 2 * K, row0=K)
