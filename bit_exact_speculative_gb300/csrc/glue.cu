@@ -254,9 +254,19 @@ __global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk
         const long long row = static_cast<long long>(b) * k + j;
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        for (int c = lane; c < nchunk; c += 32) {
-            const float2 p = part[row * nchunk + c];
-            better(bv, bi, p.x, __float_as_int(p.y));
+        // 16 partials per lane in flight before their compares (a row has one per LM-head tile,
+        // 1187 at a vocabulary of 151936); (value, -index) is a total order, so the batching
+        // leaves the result as it is
+        constexpr int U = 16;
+        for (int c0 = lane; c0 < nchunk; c0 += 32 * U) {
+            float2 p[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * 32;
+                p[u] = c < nchunk ? part[row * nchunk + c] : make_float2(-INFINITY, __int_as_float(0x7fffffff));
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) better(bv, bi, p[u].x, __float_as_int(p[u].y));
         }
         warp_best(bv, bi);
         if (lane == 0) {
