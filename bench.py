@@ -421,15 +421,13 @@ def step_line(args, device, w, wd, batch, context, steps=10, warmup=3):
     tok_dev = torch.from_numpy(toks).to(device)
     k = a.k
     for i in range(warmup):
-        stk.verify(tok_dev[i], k, logits=False)
-        stk.commit()
+        stk.verify_commit(tok_dev[i], k)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(steps):
-        stk.verify(tok_dev[warmup + i], k, logits=False)
-        stk.commit()
+        stk.verify_commit(tok_dev[warmup + i], k)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
@@ -619,8 +617,7 @@ def run_gpu(args):
     rnd = 0
 
     def step(i):
-        stk.verify(tok_dev[i], k, logits=False)
-        stk.commit()
+        stk.verify_commit(tok_dev[i], k)
 
     for _ in range(args.warmup):
         step(rnd)
@@ -688,9 +685,8 @@ def run_gpu(args):
     t0 = time.perf_counter()
     for i in range(args.steps):
         d_tok.copy_(h_tok[i], non_blocking=True)
-        stk.verify(d_tok, k, logits=False)
+        stk.verify_commit(d_tok, k)
         h_res.copy_(stk.results, non_blocking=True)
-        stk.commit()
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
     t_loaded = time.time()

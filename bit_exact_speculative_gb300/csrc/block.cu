@@ -199,9 +199,12 @@ static KvPages state_pages(const xv_block_state* st) {
 
 // The verify pass; with head = false it stops after the final RMSNorm (no LM head, argmax or
 // acceptance: a prefill chunk whose logits nobody reads).
+// With commit, the acceptance kernel also commits the accepted drafts + 1 of every sequence and
+// the host-side state advances as xv_block_commit_accepted would advance it.
 static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
                              const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
-                             int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream, bool head) {
+                             int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream, bool head,
+                             bool commit = false) {
     Dims d{};
     if (xv_status e = check_cfg(cfg, &d)) return e;
     if (xv_status e = check_state(d, cfg, st)) return e;
@@ -303,16 +306,32 @@ static xv_status verify_impl(const xv_block_config* cfg, const xv_block_weights*
             float2* amax = static_cast<float2*>(c.argmax_ws);
             XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, wt, logits, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s,
                                nullptr, nullptr, amax));
-            XV_TRY(accept_from_parts_launch(amax, ceil_div(d.V, GEMM_BN), B, k, argmax, tokens, k_seq, n_accept, s));
+            XV_TRY(accept_from_parts_launch(amax, ceil_div(d.V, GEMM_BN), B, k, argmax, tokens, k_seq, n_accept, s,
+                                            commit ? st->ctx_len : nullptr, commit ? st->n_commit : nullptr));
         } else {
             XV_TRY(gemm_launch(c.xn, d.H, w->lm_head, wt, lg, d.V, true, M, d.V, d.H, c.gemm_ws, c.gemm_ws_bytes, s));
-            XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s));
+            XV_TRY(argmax_accept_launch(lg, B, k, d.V, argmax, c.argmax_ws, tokens, k_seq, n_accept, s,
+                                        commit ? st->ctx_len : nullptr, commit ? st->n_commit : nullptr));
         }
     }
 #undef XV_TRY
+    if (commit && head) {
+        st->parity ^= 1;
+        st->pending_rows = k;
+        st->max_ctx += k;
+        st->last_k = 0;
+        st->last_k_seq = nullptr;
+        return XV_OK;
+    }
     st->last_k = k;
     st->last_k_seq = k_seq;
     return XV_OK;
+}
+
+xv_status xv_verify_block_commit_accepted(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                                          const int32_t* tokens, int k, float* logits, int32_t* argmax,
+                                          int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream) {
+    return verify_impl(cfg, w, st, tokens, k, nullptr, logits, argmax, n_accept, ws, ws_bytes, stream, true, true);
 }
 
 xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,

@@ -242,10 +242,13 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_chunk_kernel(const floa
 
 // Pass 2 and the greedy acceptance of one sequence per CTA: warp j reduces the chunk results of
 // row b*k + j into idx[b*k + j]; then n_accept[b] = the number of leading drafts tokens[b][j+1]
-// equal to idx[b*k + j], over the sequence's own k_b <= k rows.
+// equal to idx[b*k + j], over the sequence's own k_b <= k rows.  With ctx_len != null the CTA
+// then commits those positions itself, as the commit kernel would with n_accept[b] + 1:
+// ctx_len[b] += n_accept[b] + 1, n_commit[b] = n_accept[b] + 1 (always within [1, k_b]).
 __global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk, int k, int32_t* __restrict__ idx,
                                      const int32_t* __restrict__ tokens, const int32_t* __restrict__ k_seq,
-                                     int32_t* __restrict__ n_accept, unsigned* err) {
+                                     int32_t* __restrict__ n_accept, unsigned* err, int32_t* __restrict__ ctx_len,
+                                     int32_t* __restrict__ n_commit) {
     griddep_launch();
     griddep_wait();
     __shared__ int pred[XV_KMAX];
@@ -288,6 +291,10 @@ __global__ void argmax_accept_kernel(const float2* __restrict__ part, int nchunk
         int n = 0;
         while (n < kb - 1 && pred[n] == tokens[static_cast<long long>(b) * k + n + 1]) ++n;
         n_accept[b] = n;
+        if (ctx_len) {
+            ctx_len[b] += n + 1;
+            n_commit[b] = n + 1;
+        }
     }
 }
 
@@ -392,7 +399,8 @@ xv_status swiglu_launch(const uint16_t* gu, int M, int F, uint16_t* act, cudaStr
 size_t argmax_workspace_size(int M, int V) { return static_cast<size_t>(M) * ceil_div(V, ARGMAX_CHUNK) * sizeof(float2); }
 
 xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
-                               const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s) {
+                               const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s,
+                               int32_t* ctx_len, int32_t* n_commit) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "argmax: device error word unavailable");
     if (k < 1 || k > XV_KMAX) return fail(XV_ERR_ARG, "argmax: k = %d outside [1, %d]", k, XV_KMAX);
@@ -404,19 +412,20 @@ xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t
     if (xv_status st = launched("argmax_chunk_kernel", s, K_ARGMAX, 4ll * M * V)) return st;
     trace_pre(s);
     launch_k(argmax_accept_kernel, dim3(B), dim3(32 * (k < 32 ? k : 32)), 0, s, part, nchunk, k, idx, tokens, k_seq,
-             n_accept, err);
+             n_accept, err, ctx_len, n_commit);
     return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
 }
 
 xv_status accept_from_parts_launch(const float2* part, int nchunk, int B, int k, int32_t* idx, const int32_t* tokens,
-                                   const int32_t* k_seq, int32_t* n_accept, cudaStream_t s) {
+                                   const int32_t* k_seq, int32_t* n_accept, cudaStream_t s, int32_t* ctx_len,
+                                   int32_t* n_commit) {
     unsigned* err = device_error_word();
     if (!err) return fail(XV_ERR_CUDA, "argmax: device error word unavailable");
     if (k < 1 || k > XV_KMAX) return fail(XV_ERR_ARG, "argmax: k = %d outside [1, %d]", k, XV_KMAX);
     const int M = B * k;
     trace_pre(s);
     launch_k(argmax_accept_kernel, dim3(B), dim3(32 * (k < 32 ? k : 32)), 0, s, part, nchunk, k, idx, tokens, k_seq,
-             n_accept, err);
+             n_accept, err, ctx_len, n_commit);
     return launched("argmax_accept_kernel", s, K_ACCEPT, 8ll * M * nchunk + 8ll * M + 4ll * B);
 }
 

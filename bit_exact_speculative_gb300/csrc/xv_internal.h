@@ -199,12 +199,16 @@ size_t argmax_workspace_size(int M, int V);
 // idx[b*k + j] = argmax of logits row b*k + j (lowest index among equal maxima);
 // n_accept[b] = leading drafts tokens[b][j+1] (j + 1 < k_b) equal to idx[b*k + j], where
 // k_b = k_seq[b] (k when k_seq is null) (two kernels)
+// With ctx_len != null the acceptance kernel also commits n_accept[b] + 1 positions of every
+// sequence (ctx_len[b] += n, n_commit[b] = n), as the commit kernel would.
 xv_status argmax_accept_launch(const float* logits, int B, int k, int V, int32_t* idx, void* ws,
-                               const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s);
+                               const int32_t* tokens, const int32_t* k_seq, int32_t* n_accept, cudaStream_t s,
+                               int32_t* ctx_len = nullptr, int32_t* n_commit = nullptr);
 // The same from per-chunk (max, index) partials part[row * nchunk + c] already formed (the LM
 // head GEMM's amax output): the second kernel only.
 xv_status accept_from_parts_launch(const float2* part, int nchunk, int B, int k, int32_t* idx, const int32_t* tokens,
-                                   const int32_t* k_seq, int32_t* n_accept, cudaStream_t s);
+                                   const int32_t* k_seq, int32_t* n_accept, cudaStream_t s, int32_t* ctx_len = nullptr,
+                                   int32_t* n_commit = nullptr);
 // ctx_len[b] += keep[b] + keep_bias; n_commit[b] = keep[b] + keep_bias (checked to lie in [1, k_b],
 // k_b = k_seq[b] or k)
 xv_status commit_launch(const int32_t* keep, int keep_bias, int B, int k, const int32_t* k_seq, int32_t* ctx_len,

@@ -250,6 +250,17 @@ class HybridStack:
         self._last_k = k
         return lg, self.argmax[: self.B * k], self.n_accept
 
+    def verify_commit(self, tokens: torch.Tensor, k: int, logits: bool = False, stream=None):
+        """verify(tokens, k) then commit() of the accepted drafts + 1, in one call with one launch
+        fewer (the same bits).  Returns (logits [B*k, V] or None, argmax [B*k], n_accept [B])."""
+        self._prepare(k, stream)
+        lg = self.logits[: self.B * k] if logits else None
+        xv.xv_verify_block_commit_accepted(self.blk, tokens, k, lg, self.argmax, self.n_accept, self.ws, stream=stream)
+        self._bound = [n + k for n in self._bound]
+        self._k_seq = None
+        self._last_k = k
+        return lg, self.argmax[: self.B * k], self.n_accept
+
     def hidden(self) -> torch.Tensor:
         """The residual stream after the last layer of the last verify (the hidden state before
         the final RMSNorm), bf16 bits [B*k, H]: a view of the workspace, valid until the next call

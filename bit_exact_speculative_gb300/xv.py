@@ -114,6 +114,8 @@ _SIGS = {
     "xv_block_workspace_size": ([ctypes.POINTER(BlockConfig), c_int, c_int, c_int], c_sz),
     "xv_verify_block": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState),
                          vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
+    "xv_verify_block_commit_accepted": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
+                                         ctypes.POINTER(BlockState), vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
     "xv_verify_block_ragged": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
                                 ctypes.POINTER(BlockState), vp, c_int, vp, vp, vp, vp, vp, c_sz, vp], c_int),
     "xv_block_commit": ([ctypes.POINTER(BlockState), vp, vp], c_int),
@@ -444,6 +446,13 @@ def xv_verify_block(blk: Block, tokens, k: int, logits, argmax, n_accept, ws, st
     _check(lib().xv_verify_block(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
                                  _ptr(tokens), k, _ptr(logits), _ptr(argmax), _ptr(n_accept), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def xv_verify_block_commit_accepted(blk: Block, tokens, k: int, logits, argmax, n_accept, ws, stream=None):
+    _check(lib().xv_verify_block_commit_accepted(ctypes.byref(blk.cfg), ctypes.byref(blk.weights),
+                                                 ctypes.byref(blk.state), _ptr(tokens), k, _ptr(logits), _ptr(argmax),
+                                                 _ptr(n_accept), _ptr(ws), ws.numel() * ws.element_size(),
+                                                 _stream(stream)))
 
 
 def xv_verify_block_ragged(blk: Block, tokens, k: int, k_seq, logits, argmax, n_accept, ws, stream=None):

@@ -491,6 +491,16 @@ xv_status xv_verify_block(const xv_block_config* cfg, const xv_block_weights* w,
                           const int32_t* tokens, int k, float* logits, int32_t* argmax, int32_t* n_accept,
                           void* ws, size_t ws_bytes, xv_stream s);
 
+/* xv_verify_block followed by xv_block_commit_accepted, the step of a greedy
+ * speculative loop, with one launch fewer: the acceptance kernel commits each
+ * sequence's accepted drafts + 1 itself (ctx_len += n_accept[b] + 1,
+ * n_commit = n_accept[b] + 1) and the host-side state advances as the commit
+ * would advance it.  Arguments, errors and every bit of the outputs and of
+ * the state as with the two calls. */
+xv_status xv_verify_block_commit_accepted(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                                          const int32_t* tokens, int k, float* logits, int32_t* argmax,
+                                          int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream s);
+
 /* Verify with a number of tokens per sequence: sequence b verifies k_b =
  * k_seq[b] tokens (device [B] int32, 1 <= k_b <= k), laid out as the first
  * k_b of its k rows in tokens [B, k]; rows k_b..k-1 are padding (any valid

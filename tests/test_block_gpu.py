@@ -518,3 +518,40 @@ def test_stack_argmax_without_logits(stack):
     restore(A, snap)
     _, am2, na2 = A.verify(toks, k, logits=False)
     assert torch.equal(am1, am2) and torch.equal(na1, na2)
+
+
+@pytest.mark.parametrize("name", ["TINY", "STACK"])
+def test_verify_commit_equals_verify_then_commit(stack, name):
+    """The fused verify + commit-accepted call against the two calls: three rounds on 8 sequences
+    of mixed lengths give the same logits, argmax and accept counts, and leave every state tensor
+    (lengths, commit counts, GDN states and histories, caches) the same bit for bit."""
+    if name == "STACK":
+        cfg, w, wd = stack
+    else:
+        cfg = workloads.TINY
+        w = workloads.weights(cfg, seed=0)
+        wd = {n: dev(v) for n, v in w.items()}
+    B, k = 8, 8 if name == "STACK" else 4
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500] if name == "STACK" else [128, 5, 77, 250, 1, 64, 99, 31]
+    Lmax = max(lens) + 4 * k + 64
+    kv = kv_host(cfg, lens, Lmax)
+    A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd, kv=kv)
+    S = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd, kv=kv)
+    for r in range(3):
+        toks = dev(workloads.draft_tokens(cfg, 0, 20 + r, B, k))
+        la, aa, na = A.verify_commit(toks, k, logits=True)
+        ls, as_, ns = S.verify(toks, k)
+        res_s = (ls.clone(), as_.clone(), ns.clone())
+        S.commit()
+        assert same_bits(la, res_s[0]) and torch.equal(aa, res_s[1]) and torch.equal(na, res_s[2]), f"round {r}"
+    torch.cuda.synchronize()
+    for n, t in A.state.items():
+        assert torch.equal(t, S.state[n]), n
+    sa, ss = A.blk.state, S.blk.state
+    assert (sa.parity, sa.pending_rows, sa.max_ctx, sa.last_k) == (ss.parity, ss.pending_rows, ss.max_ctx, ss.last_k)
+    assert xv_device_check_ok()
+
+
+def xv_device_check_ok():
+    from bit_exact_speculative_gb300 import xv
+    return xv.xv_device_check() == 0
