@@ -675,7 +675,6 @@ def run_gpu(args):
 
     # ---- end to end through the public API: pinned host tokens in, results out, every step
     h_tok = torch.from_numpy(toks[rnd: rnd + args.steps].copy()).pin_memory()
-    d_tok = torch.empty((B, k), dtype=torch.int32, device=device)
     # the step's argmax ids and accept counts, read back in one copy (HybridStack keeps them side
     # by side: argmax [B * kmax] then n_accept [B])
     h_res = torch.empty(stk.results.shape, dtype=torch.int32).pin_memory()
@@ -684,9 +683,8 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        d_tok.copy_(h_tok[i], non_blocking=True)
-        stk.verify_commit(d_tok, k)
-        h_res.copy_(stk.results, non_blocking=True)
+        # one call: the drafts copied in, verify + commit, the results copied out
+        stk.step_host(h_tok[i], h_res)
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
     t_loaded = time.time()

@@ -334,6 +334,26 @@ xv_status xv_verify_block_commit_accepted(const xv_block_config* cfg, const xv_b
     return verify_impl(cfg, w, st, tokens, k, nullptr, logits, argmax, n_accept, ws, ws_bytes, stream, true, true);
 }
 
+xv_status xv_block_step_host(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                             const int32_t* host_tokens, int32_t* dev_tokens, int k, int32_t* dev_results,
+                             int32_t* host_results, void* ws, size_t ws_bytes, xv_stream stream) {
+    if (!st || !host_tokens || !dev_tokens || !dev_results || !host_results)
+        return fail(XV_ERR_ARG, "step: null buffer");
+    if (k < 1 || k > st->kmax) return fail(XV_ERR_ARG, "step: k = %d outside [1, kmax = %d]", k, st->kmax);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t B = static_cast<size_t>(st->B);
+    if (xv_status e = cuda_check(cudaMemcpyAsync(dev_tokens, host_tokens, 4 * B * k, cudaMemcpyHostToDevice, s),
+                                 "step: copy the drafts in"))
+        return e;
+    int32_t* argmax = dev_results;
+    int32_t* n_accept = dev_results + B * st->kmax;
+    if (xv_status e = verify_impl(cfg, w, st, dev_tokens, k, nullptr, nullptr, argmax, n_accept, ws, ws_bytes, stream,
+                                  true, true))
+        return e;
+    return cuda_check(cudaMemcpyAsync(host_results, dev_results, 4 * (B * st->kmax + B), cudaMemcpyDeviceToHost, s),
+                      "step: copy the results out");
+}
+
 xv_status xv_verify_block_ragged(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
                                  const int32_t* tokens, int k, const int32_t* k_seq, float* logits, int32_t* argmax,
                                  int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream stream) {

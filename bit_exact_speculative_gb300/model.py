@@ -194,6 +194,7 @@ class HybridStack:
         self.logits = torch.empty((B * kmax, cfg["vocab"]), dtype=torch.float32, device=d)
         # argmax ids and accept counts side by side, so that one copy reads a step's results
         self.results = torch.empty(B * kmax + B, dtype=torch.int32, device=d)
+        self._step_tokens = None       # the device copy of step_host's drafts
         self.argmax = self.results[: B * kmax]
         self.n_accept = self.results[B * kmax:]
 
@@ -260,6 +261,22 @@ class HybridStack:
         self._k_seq = None
         self._last_k = k
         return lg, self.argmax[: self.B * k], self.n_accept
+
+    def step_host(self, host_tokens: torch.Tensor, host_results: torch.Tensor, stream=None):
+        """One host-driven speculative step in one call: host_tokens [B, k] int32 (pinned) in,
+        verify + commit of the accepted drafts, and host_results [B*kmax + B] int32 (pinned;
+        argmax ids then accept counts) out, all enqueued on the stream (synchronise before
+        reading host_results)."""
+        k = host_tokens.shape[-1]
+        if self.pool is not None:
+            self._prepare(k, stream)
+        if self._step_tokens is None or self._step_tokens.shape[1] != k:
+            self._step_tokens = torch.empty((self.B, k), dtype=torch.int32, device=self.results.device)
+        xv.xv_block_step_host(self.blk, host_tokens, self._step_tokens, k, self.results, host_results, self.ws,
+                              stream=stream)
+        self._bound = [n + k for n in self._bound]
+        self._k_seq = None
+        self._last_k = k
 
     def hidden(self) -> torch.Tensor:
         """The residual stream after the last layer of the last verify (the hidden state before

@@ -116,6 +116,8 @@ _SIGS = {
                          vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
     "xv_verify_block_commit_accepted": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
                                          ctypes.POINTER(BlockState), vp, c_int, vp, vp, vp, vp, c_sz, vp], c_int),
+    "xv_block_step_host": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(BlockState),
+                            vp, vp, c_int, vp, vp, vp, c_sz, vp], c_int),
     "xv_verify_block_ragged": ([ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
                                 ctypes.POINTER(BlockState), vp, c_int, vp, vp, vp, vp, vp, c_sz, vp], c_int),
     "xv_block_commit": ([ctypes.POINTER(BlockState), vp, vp], c_int),
@@ -453,6 +455,12 @@ def xv_verify_block_commit_accepted(blk: Block, tokens, k: int, logits, argmax, 
                                                  ctypes.byref(blk.state), _ptr(tokens), k, _ptr(logits), _ptr(argmax),
                                                  _ptr(n_accept), _ptr(ws), ws.numel() * ws.element_size(),
                                                  _stream(stream)))
+
+
+def xv_block_step_host(blk: Block, host_tokens, dev_tokens, k: int, dev_results, host_results, ws, stream=None):
+    _check(lib().xv_block_step_host(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
+                                    _ptr(host_tokens), _ptr(dev_tokens), k, _ptr(dev_results), _ptr(host_results),
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def xv_verify_block_ragged(blk: Block, tokens, k: int, k_seq, logits, argmax, n_accept, ws, stream=None):

@@ -501,6 +501,16 @@ xv_status xv_verify_block_commit_accepted(const xv_block_config* cfg, const xv_b
                                           const int32_t* tokens, int k, float* logits, int32_t* argmax,
                                           int32_t* n_accept, void* ws, size_t ws_bytes, xv_stream s);
 
+/* One step of a host-driven greedy speculative loop, all enqueued on the stream by one call:
+ * the drafts host_tokens [B, k] int32 (pinned host memory) are copied into dev_tokens (device,
+ * [B, k]), xv_verify_block_commit_accepted runs (no logits), and the results are copied back:
+ * dev_results (device, [B*kmax + B] int32: argmax [B*kmax] then n_accept [B]) into
+ * host_results (pinned host memory, the same layout).  The caller synchronises the stream before
+ * reading host_results.  Errors as for xv_verify_block, and XV_ERR_ARG for a null buffer. */
+xv_status xv_block_step_host(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
+                             const int32_t* host_tokens, int32_t* dev_tokens, int k, int32_t* dev_results,
+                             int32_t* host_results, void* ws, size_t ws_bytes, xv_stream s);
+
 /* Verify with a number of tokens per sequence: sequence b verifies k_b =
  * k_seq[b] tokens (device [B] int32, 1 <= k_b <= k), laid out as the first
  * k_b of its k rows in tokens [B, k]; rows k_b..k-1 are padding (any valid

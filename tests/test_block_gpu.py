@@ -555,3 +555,26 @@ def test_verify_commit_equals_verify_then_commit(stack, name):
 def xv_device_check_ok():
     from bit_exact_speculative_gb300 import xv
     return xv.xv_device_check() == 0
+
+
+def test_step_host_equals_verify_commit(stack):
+    """The one-call host-driven step (drafts in from pinned host memory, results out to it) against
+    verify_commit on device tensors: three rounds on 8 sequences give the same argmax ids and
+    accept counts in the host buffer and the same state."""
+    cfg, w, wd = stack
+    B, k = 8, 8
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500]
+    Lmax = max(lens) + 4 * k + 64
+    kv = kv_host(cfg, lens, Lmax)
+    A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd, kv=kv)
+    S = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd, kv=kv)
+    h_res = torch.empty(A.results.shape, dtype=torch.int32).pin_memory()
+    for r in range(3):
+        toks = workloads.draft_tokens(cfg, 0, 30 + r, B, k)
+        A.step_host(torch.from_numpy(toks).pin_memory(), h_res)
+        _, am, na = S.verify_commit(dev(toks), k)
+        torch.cuda.synchronize()
+        assert torch.equal(h_res[: B * k], am.cpu()) and torch.equal(h_res[B * k:], na.cpu()), f"round {r}"
+    for n, t in A.state.items():
+        assert torch.equal(t, S.state[n]), n
+    assert xv_device_check_ok()
