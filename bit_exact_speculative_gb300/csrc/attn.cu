@@ -220,7 +220,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = A.R * A.G, nrt = (rows + 63) / 64;
     const int n_items = A.nsplit * nrt * A.Hkv * A.B;
-    const int it0 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x) * n_items / gridDim.x) : blockIdx.x;
+    // One CTA per item: blocks take the items split-slowest, so the rows' last splits (often a
+    // few tiles only) come last and fill a second wave that a full split would drag out; a
+    // persistent CTA walks a contiguous range numbered split-fastest (consecutive items share Q).
+    const int per_split = n_items / A.nsplit;
+    const int it0 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x) * n_items / gridDim.x)
+                          : (static_cast<int>(blockIdx.x) % per_split) * A.nsplit + static_cast<int>(blockIdx.x) / per_split;
     const int it1 = MULTI ? static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_items / gridDim.x) : it0 + 1;
     griddep_wait();
     int first = it0;
