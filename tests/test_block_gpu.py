@@ -445,12 +445,13 @@ def test_stack_prefill_chunks_equal(stack):
 # ------------------------------------------------------------ layer by layer, teacher forced
 
 @pytest.mark.parametrize("name,lens,k", [("TINY", [128, 37], 4), ("TINY_FULL", [128, 5, 77, 250], 4),
-                                         ("STACK", [2183], 8)])
+                                         ("STACK", [2183], 8), ("STACK", [2183, 700], 8)])
 def test_layers_teacher_forced_vs_oracle(stack, name, lens, k):
     """Each layer on its own: stacks of the first d layers (d = 1 .. L, the same weights and
     states) give the residual stream after layer d (the hidden state the verify leaves at the
     start of its workspace); the oracle's layer d, fed the GPU's residual input to it, must land
-    within the per-layer bound.  TINY_FULL at 4 x 4 rows takes the M > 8 paths."""
+    within the per-layer bound.  TINY_FULL at 4 x 4 rows and the stack at 2 x 8 rows take the
+    M > 8 paths."""
     if name == "STACK":
         cfg, w, wd = stack
     else:
