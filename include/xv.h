@@ -177,7 +177,7 @@ xv_status xv_gemm_small_m_tiled_f32out(const uint16_t* X, int ldx, const uint16_
 /* The same GEMM (bf16 out) for callers that cannot allocate device memory or
  * pass a workspace: code running under another framework's memory pool,
  * plugins inside a host process that owns every device allocation, loops
- * where an allocation is not allowed.  The paper has no counterpart; this is
+ * where an allocation is not allowed.  The method itself needs no such entry point; this is
  * a convenience of this library.  Its scratch (split-K partial sums and tile
  * counters) is a fixed array of XV_GEMM_NOALLOC_SCRATCH_BYTES that every GPU
  * loading the library holds until the process exits.  The first call on a

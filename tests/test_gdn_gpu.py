@@ -151,7 +151,7 @@ def test_verify_equals_sequential_decode_and_rollback(xv, B, K):
 
 @pytest.mark.parametrize("K,keep", [(8, 3), (64, 37), (64, 64)])
 def test_replay_then_speculate_matches_decode(xv, K, keep):
-    """Round 2 of a speculative loop: replay `keep` kept steps, speculate K new ones (up to 128
+    """The second pass of a speculative loop: replay `keep` kept steps, speculate K new ones (up to 128
     staged steps in one call)."""
     B = 2
     qkv_h, gates_h = make_inputs(5, B, 2 * K)          # rows b*2K + t: first K = first verify, last K = second verify
