@@ -265,8 +265,8 @@ class HybridStack:
     def step_host(self, host_tokens: torch.Tensor, host_results: torch.Tensor, stream=None):
         """One host-driven speculative step in one call: host_tokens [B, k] int32 (pinned) in,
         verify + commit of the accepted drafts, and host_results [B*kmax + B] int32 (pinned;
-        argmax ids then accept counts) out, all enqueued on the stream (synchronise before
-        reading host_results)."""
+        argmax ids in its first B*k entries, row b*k + j, then from B*kmax on the accept counts)
+        out, all enqueued on the stream (synchronise before reading host_results)."""
         k = host_tokens.shape[-1]
         if self.pool is not None:
             self._prepare(k, stream)

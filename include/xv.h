@@ -504,8 +504,9 @@ xv_status xv_verify_block_commit_accepted(const xv_block_config* cfg, const xv_b
 /* One step of a host-driven greedy speculative loop, all enqueued on the stream by one call:
  * the drafts host_tokens [B, k] int32 (pinned host memory) are copied into dev_tokens (device,
  * [B, k]), xv_verify_block_commit_accepted runs (no logits), and the results are copied back:
- * dev_results (device, [B*kmax + B] int32: argmax [B*kmax] then n_accept [B]) into
- * host_results (pinned host memory, the same layout).  The caller synchronises the stream before
+ * dev_results (device, [B*kmax + B] int32: an argmax region of B*kmax entries, of which row
+ * b*k + j holds position j of sequence b and entries from B*k on are left as they were, then
+ * n_accept [B]) into host_results (pinned host memory, the same layout).  The caller synchronises the stream before
  * reading host_results.  Errors as for xv_verify_block, and XV_ERR_ARG for a null buffer. */
 xv_status xv_block_step_host(const xv_block_config* cfg, const xv_block_weights* w, xv_block_state* st,
                              const int32_t* host_tokens, int32_t* dev_tokens, int k, int32_t* dev_results,
