@@ -568,6 +568,13 @@ __global__ void tile_weights_kernel(const uint4* __restrict__ W, int N, int K, i
     if (row < N && col < K) v = W[(row * K + col) / 8];
     Wt[i] = v;
 }
+
+// Enqueued right after a tiling with a plain launch (no programmatic serialisation): it starts
+// only once the tiled weights are complete in memory, and it lets its successor start only when
+// it has exited.  Every GEMM requests its first weight tiles before its dependency wait (weights
+// are not written by the kernel before it), so this is what keeps a GEMM launched straight after
+// a tiling from reading tiles still being written.
+__global__ void tile_fence_kernel() {}
 }  // namespace
 
 size_t gemm_tiled_bytes(int N, int K) {
@@ -577,10 +584,15 @@ size_t gemm_tiled_bytes(int N, int K) {
 xv_status gemm_tile_weights_launch(const uint16_t* W, int N, int K, bool gated, uint16_t* Wt, cudaStream_t s) {
     const long long pieces = static_cast<long long>(gemm_tiled_bytes(N, K) / 16);
     constexpr int T = 256;
+    trace_pre(s);
     launch_k(tile_weights_kernel, dim3(static_cast<unsigned>((pieces + T - 1) / T)), dim3(T), 0, s,
              reinterpret_cast<const uint4*>(W), N, K, ceil_div(K, GEMM_BK), pieces, gated ? N / 2 : 0,
              reinterpret_cast<uint4*>(Wt));
-    return launched("tile_weights_kernel", s, K_TILE, 2 * static_cast<long long>(gemm_tiled_bytes(N, K)));
+    if (xv_status e = launched("tile_weights_kernel", s, K_TILE, 2 * static_cast<long long>(gemm_tiled_bytes(N, K))))
+        return e;
+    trace_pre(s);
+    tile_fence_kernel<<<1, 32, 0, s>>>();
+    return launched("tile_fence_kernel", s, K_TILE, 0);
 }
 
 }  // namespace xv
