@@ -83,6 +83,10 @@ unsigned long long xv_launch_count(void);
  * (default on): a kernel may start its independent prologue (barrier set-up,
  * TMEM allocation, prefetch of weights) while its predecessor in the stream
  * finishes, and waits for the predecessor before touching activations.
+ * Weights are requested before that wait, so they must be complete when the
+ * GEMM is enqueued: written by a kernel that has finished, a copy, or
+ * xv_gemm_tile_weights / xv_gemm_tile_gate_up (which end with a kernel that
+ * lets its successor start only after the tiling is complete in memory).
  * Results are identical either way; 0 turns it off (for timing comparisons). */
 xv_status xv_set_overlap(int enable);
 
