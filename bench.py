@@ -789,6 +789,68 @@ def oracle_sample(args, cfg, w, budget_s=12.0):
                       f"weights; {dt:.1f} s"}
 
 
+def oracle_configs(args, cfg, w):
+    """The oracle on the other configurations, one bounded sample each, in the units of the GPU
+    figures beside it (µs per call; positions per second for the step): the 17408-wide GEMMs at
+    M = 1 and 16, GDN verify of one sequence (1 replayed and 8 speculative steps of 32 heads of
+    128 x 128), the decode-row attention of one sequence (8 rows, 24 q / 4 kv heads of 256) at 640,
+    2183 and 131072 positions, and the verify step at context 131072.  The oracle takes sequences
+    one after another, so its batch-8 figures are 8 x the per-sequence time (its rate per position
+    stays the same)."""
+    import types
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+
+    def bf16(shape, scale=1.0):
+        x = (rng.standard_normal(int(np.prod(shape)), dtype=np.float32) * scale).reshape(shape)
+        return (x.view(np.uint32) >> 16).astype(np.uint16)   # truncated: the values do not matter here
+
+    def timed(fn, reps=1):
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        return (time.perf_counter() - t0) / reps * 1e6
+
+    out = {"cores": cores_used(), "kind": "oracle"}
+    gemm = {}
+    for name, (N, K) in (("up17408", (17408, 5120)), ("down17408", (5120, 17408))):
+        W = bf16((N, K), 0.02)
+        for M in (1, 16):
+            X = bf16((M, K))
+            gemm[f"{name}_M{M}"] = round(timed(lambda: oracle.gemm(X, W)), 1)
+        del W
+    out["gemm_sweep_us"] = gemm
+    H, D, k = 32, 128, 8
+    S = rng.standard_normal((H, D, D)) * 0.1
+    q, kk, v = bf16((k + 1, H, D)), bf16((k + 1, H, D)), bf16((k + 1, H, D))
+    beta, gate = bf16((k + 1, H)), bf16((k + 1, H))
+
+    def gdn():
+        St = S.copy()
+        for t in range(k + 1):
+            oracle.gdn_step_heads(St, q[t], kk[t], v[t], beta[t], gate[t], True)
+    out["gdn_verify_us_per_sequence"] = round(timed(gdn), 1)
+    attn = {}
+    for L in (640, 2183, 131072):
+        R = 8 if L < 100000 else 1   # one of the 8 rows at 131072, scaled by 8
+        kc, vc = bf16((4, L + 8, 256)), bf16((4, L + 8, 256))
+        qq = bf16((R, 24, 256))
+        attn[f"L{L}"] = round(timed(lambda: oracle.attn_rows(qq, kc, vc, L, 256 ** -0.5)) * (8 // R), 1)
+        del kc, vc
+    out["attn_decode_rows_us_per_sequence"] = attn
+    st, toks = oracle_session(types.SimpleNamespace(context=131072, steps=1, warmup=1), cfg, w)
+    n, t0 = 0, time.perf_counter()
+    while n == 0 or (n < 4 and time.perf_counter() - t0 < 5.0):
+        st.decode(int(toks[n]))
+        n += 1
+    out["step_ctx131072"] = {"value": round(n / (time.perf_counter() - t0), 4), "unit": UNIT,
+                             "sample": f"{n} verify positions of one sequence decoded one at a time"}
+    out["sample"] = ("one call per GEMM shape and per attention length (at 131072 one of the 8 rows, "
+                     "scaled by 8), one GDN verify, 1-4 positions of the 131072-position step")
+    return out
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step verifies one position of the workload on the host
     cores (verify = sequential decode by definition); value = positions per second."""
@@ -841,6 +903,7 @@ def main():
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = oracle_sample(args, cfg, w)
+            out["cpu_configs"] = oracle_configs(args, cfg, w)
         print(json.dumps(out), flush=True)
 
 
