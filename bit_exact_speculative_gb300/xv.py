@@ -458,6 +458,14 @@ def xv_verify_block_commit_accepted(blk: Block, tokens, k: int, logits, argmax, 
 
 
 def xv_block_step_host(blk: Block, host_tokens, dev_tokens, k: int, dev_results, host_results, ws, stream=None):
+    # the library copies these sizes from and into raw pointers: host buffers too short would be
+    # overrun on the host, so their sizes are checked here
+    B, kmax = blk.state.B, blk.state.kmax
+    for name, t, n, host in (("host_tokens", host_tokens, B * k, True), ("dev_tokens", dev_tokens, B * k, False),
+                             ("dev_results", dev_results, B * kmax + B, False),
+                             ("host_results", host_results, B * kmax + B, True)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n or t.is_cuda == host:
+            raise ValueError(f"{name}: {n} contiguous int32 in {'host' if host else 'device'} memory needed")
     _check(lib().xv_block_step_host(ctypes.byref(blk.cfg), ctypes.byref(blk.weights), ctypes.byref(blk.state),
                                     _ptr(host_tokens), _ptr(dev_tokens), k, _ptr(dev_results), _ptr(host_results),
                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))

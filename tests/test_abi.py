@@ -270,3 +270,19 @@ def test_binding_constants_match_the_header(xv):
         assert m, name
         value = xv.xv_abi_version() if name == "XV_ABI_VERSION" else getattr(xv, name)
         assert value == int(m.group(1)), name
+
+
+def test_step_host_checks_its_buffers_before_any_copy(xv):
+    """The host step copies B*k draft ids in and B*kmax + B results out through raw pointers: the
+    binding refuses buffers too short, of another type or in the wrong memory before calling."""
+    import types
+
+    import torch
+    blk = types.SimpleNamespace(state=types.SimpleNamespace(B=2, kmax=8))
+    host = lambda n, dt=torch.int32: torch.zeros(n, dtype=dt)   # noqa: E731
+    with pytest.raises(ValueError, match="host_tokens"):
+        xv.xv_block_step_host(blk, host(2 * 8 - 1), None, 8, None, host(18), None)
+    with pytest.raises(ValueError, match="host_tokens"):
+        xv.xv_block_step_host(blk, host(16, torch.int64), None, 8, None, host(18), None)
+    with pytest.raises(ValueError, match="dev_tokens"):      # a host tensor where device memory is needed
+        xv.xv_block_step_host(blk, host(16), host(16), 8, None, host(18), None)
