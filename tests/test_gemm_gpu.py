@@ -201,3 +201,25 @@ def test_fused_swiglu_vs_oracle(xv, M, F, K):
     xv.xv_gemm_swiglu(Xd, Wt, full)
     assert same_bits(act, full[:M])
     assert xv.xv_device_check() == 0
+
+
+def test_gemm_straight_after_tiling(xv):
+    """A GEMM enqueued right after the tiling of its weight, nothing else between them on the
+    stream, reads finished tiles (every GEMM requests its first weight tiles before its dependency
+    wait).  The tiled buffer is reused from one call to the next and holds the other weight's
+    tiles before each tiling, so a read of unfinished tiles would show up as the other result."""
+    M, N, K = 8, 5120, 17408
+    X = dev(synth.normal_bf16(0, synth.tid("after_tiling_x"), (M, K)))
+    Ws = [dev(synth.normal_bf16(0, synth.tid(f"after_tiling_w{i}"), (N, K), sigma=0.02)) for i in range(2)]
+    refs = [run(xv, X, W) for W in Ws]
+    Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    ws = xv.workspace(xv.xv_gemm_workspace_size(M, N, K))
+    outs = []
+    for i in range(20):
+        Wt = xv.tile_weight(Ws[i % 2])
+        xv.xv_gemm_small_m(X, Wt, Y, ws)
+        outs.append(Y.clone())
+        del Wt
+    for i, o in enumerate(outs):
+        assert same_bits(o, refs[i % 2]), f"call {i}"
+    assert xv.xv_device_check() == 0
