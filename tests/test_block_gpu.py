@@ -579,3 +579,33 @@ def test_step_host_equals_verify_commit(stack):
     for n, t in A.state.items():
         assert torch.equal(t, S.state[n]), n
     assert xv_device_check_ok()
+
+
+def test_stack_same_bits_without_programmatic_launch(stack, built):
+    """Programmatic dependent launch lets each kernel start its prologue (and request its weights)
+    while its predecessor finishes; turning it off serialises the launches.  Three verify + commit
+    rounds of 8 sequences give the same logits, argmax, accept counts and states either way."""
+    xv = built
+    cfg, w, wd = stack
+    B, k = 8, 8
+    lens = [2183, 640, 1000, 1, 513, 2047, 300, 1500]
+    Lmax = max(lens) + 4 * k + 64
+    A = gpu_stack(cfg, w, B, k, Lmax, lens, weights_dev=wd)
+    snap = snapshot(A)
+    runs = []
+    try:
+        for overlap in (1, 0):
+            xv.xv_set_overlap(overlap)
+            restore(A, snap)
+            out = []
+            for rnd in range(3):
+                lg, am, na = A.verify_commit(dev(workloads.draft_tokens(cfg, 0, 40 + rnd, B, k)), k, logits=True)
+                out += [lg.clone(), am.clone(), na.clone()]
+            torch.cuda.synchronize()
+            out += [t.clone() for t in A.state.values()]
+            runs.append(out)
+    finally:
+        xv.xv_set_overlap(True)
+    assert xv.xv_device_check() == 0
+    for a, b in zip(*runs):
+        assert same_bits(a, b)
