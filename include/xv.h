@@ -146,7 +146,9 @@ int xv_gemm_splits(int N, int K);
  * xv_gemm_tiled_bytes: bytes of the tiled copy of an N x K weight (0 for
  *   N < 1 or K < 1).
  * xv_gemm_tile_weights: writes Wt (device, xv_gemm_tiled_bytes(N, K) bytes,
- *   caller-owned) from W [N, K] row-major on stream s (one kernel).  W and
+ *   caller-owned) from W [N, K] row-major on stream s (the tiling kernel,
+ *   then an empty kernel that lets the next one start only once the tiles
+ *   are complete, so a GEMM may follow on the same stream at once).  W and
  *   Wt 16-byte aligned and not overlapping, K % 8 == 0.  Errors: XV_ERR_ARG
  *   (null pointer, N < 1, K < 8), XV_ERR_UNSUPPORTED (K % 8 != 0,
  *   alignment), XV_ERR_CUDA.
