@@ -162,7 +162,8 @@ xv_status xv_gemm_tile_weights(const uint16_t* W, int N, int K, uint16_t* Wt, xv
  * gate/up weight W [2F, K] (F gate rows, then F up rows) so that tile t holds
  * gate rows 64t..64t+63 followed by up rows F+64t..F+64t+63 (Wt of
  * xv_gemm_tiled_bytes(2F, K) bytes; F % 64 == 0, K % 8 == 0, 16-byte
- * aligned).  xv_gemm_swiglu_tiled then computes, for each row m of X and
+ * aligned; enqueued as xv_gemm_tile_weights is, fence kernel included).
+ * xv_gemm_swiglu_tiled then computes, for each row m of X and
  * feature f < F,
  *     act[m, f] = bf16(silu(g) u),  g = bf16((X W^T)[m, f]),
  *                                   u = bf16((X W^T)[m, F + f]),
