@@ -232,18 +232,29 @@ def gemm_shapes(cfg, M):
     return out
 
 
+def code_digest(path: str) -> str:
+    """sha256 (16 hex digits) of a C++/CUDA source with its comments and white space removed: a
+    comment edit leaves it as it is, any change to the code does not."""
+    import hashlib
+    import re
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()[:16]
+
+
 def traffic_ratio_from_profile(kernel_src: str):
     """ncu DRAM bytes (read + write) per algorithmic byte of the GEMM kernel, from the committed
-    capture of one projection shape (profiles/traffic.json), if that capture matches this source;
-    else None.  The GEMM streams each weight once, so its traffic scales with the bytes it moves."""
-    import hashlib
+    capture of one projection shape (profiles/traffic.json), if that capture matches this source's
+    code (`code_digest`); else None.  The GEMM streams each weight once, so its traffic scales with
+    the bytes it moves."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    h = code_digest(kernel_src)
     e = d.get("gemm_small_m")
-    if not e or e.get("source_sha") != h:
+    if not e or e.get("code_digest") != h:
         return None
     return float(e["ratio"])
 

@@ -42,6 +42,13 @@
 //     to the same shared-memory places from either layout, so the bits
 //     agree; measured on GB300 the tiled layout streams faster (the 151936 x
 //     5120 LM head 254 -> 242 us, the verify step 894 -> 865 us).
+//   - The unsplit fp32 GEMM (the LM head) can also leave, for every token row
+//     and weight tile, the tile's maximum and its lowest index, from which the
+//     argmax follows without a pass over the logits (which it then need not
+//     write).
+//   - A split GEMM can hand its segment partials [S][M][N] to the caller
+//     instead of combining them; the residual RMSNorm adds them in the same
+//     segment order, so the bits are those of the combine.
 #include "xv_internal.h"
 #include "xv_ptx.cuh"
 
