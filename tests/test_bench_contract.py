@@ -53,3 +53,20 @@ def test_clock_record_uses_the_timed_region():
     short = c.summary(1.0, 1.15, 2.0)
     assert short["samples"] == 1 and short["window"].startswith("timed region and")
     assert short["sm_mhz"] == float(np.median([2070, 2060, 2070, 2000]))
+
+
+def test_traffic_record_follows_the_gemm_code(tmp_path):
+    """The committed DRAM-traffic ratio is used only while gemm.cu's code is the one it was captured
+    with: its digest ignores comments and white space and changes with any code token."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(ROOT, "bit_exact_speculative_gb300", "csrc", "gemm.cu")
+    assert bench.traffic_ratio_from_profile(src) is not None     # the record matches the code as committed
+    code = open(src).read()
+    a = tmp_path / "a.cu"
+    a.write_text("// a new comment\n/* and a block\n comment */\n" + code.replace("\n", "\n  "))
+    assert bench.code_digest(str(a)) == bench.code_digest(src)
+    b = tmp_path / "b.cu"
+    b.write_text(code.replace("constexpr int STAGES = 4;", "constexpr int STAGES = 5;"))
+    assert bench.code_digest(str(b)) != bench.code_digest(src)
+    assert bench.traffic_ratio_from_profile(str(b)) is None
